@@ -1,0 +1,149 @@
+/*
+ * gdn_oracle.h -- plain CPU oracle for the gated-delta-rule (GDN) layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This library exists to check the CUDA library
+ * against a slow, obviously correct restatement of the method.  Only the test
+ * suite, the smoke check and the CPU-baseline leg of the benchmark may load it.
+ * It shares no code, header, table or constant with the CUDA path.
+ *
+ * Sources (page title, then the function on it):
+ *   [cpu.rs]       ferrum-kernels 0.8.0, src/ferrum_kernels/backend/cpu.rs
+ *   [cpu_ops.cpp]  vllm.cpp, src/vt/cpu/cpu_ops.cpp
+ *   [qwen3_5.cpp]  vllm.cpp, src/vllm/model_executor/models/qwen3_5.cpp
+ *
+ * Conventions
+ *   - Every exported routine comes in an f32 and an f64 instantiation (suffix).
+ *     All arithmetic happens in that type; callers widen bf16 inputs exactly.
+ *   - Layouts: q,k [T,Hk,Dk]; v,out [T,Hv,Dv]; g,beta [T,Hv];
+ *     state pool [slots,Hv,Dv,Dk]; conv-tail pool [slots,C_conv,K-1] oldest
+ *     first; mixed_qkv [T, >=C_conv] with row stride x_stride (elements).
+ *   - Return value: ORC_OK or an ORC_ERR_* code; msg (if non-NULL) receives the
+ *     diagnostic text.
+ *
+ * Parity pins: every function here is pinned by tests that do not re-type its
+ * formula (closed forms, invariants, library routines, brute force); see the
+ * module docstrings of tests/test_oracle_*.py.
+ */
+#ifndef GDN_ORACLE_H_
+#define GDN_ORACLE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  ORC_OK = 0,
+  ORC_ERR_SHAPE = 1,    /* non-positive dims, Hv % Hk != 0, short buffer */
+  ORC_ERR_INVALID = 2,  /* bad cu_seqlens, bad state index */
+};
+
+/* ---- scalar gate functions, [cpu.rs] sigmoid / silu / softplus ---------- */
+float orc_sigmoid_f32(float x);
+float orc_silu_f32(float x);
+float orc_softplus_f32(float x);
+double orc_sigmoid_f64(double x);
+double orc_silu_f64(double x);
+double orc_softplus_f64(double x);
+
+/* ---- validators ---------------------------------------------------------- */
+/* [cpu.rs] validate_gated_delta_rule_shape; lengths are element counts. */
+int orc_validate_gated_delta_rule_shape(int64_t query_len, int64_t key_len, int64_t value_len,
+                                        int64_t g_len, int64_t beta_len,
+                                        int64_t initial_state_len, int64_t out_len,
+                                        int64_t final_state_len, int64_t tokens,
+                                        int64_t key_heads, int64_t value_heads,
+                                        int64_t key_dim, int64_t value_dim, char* msg,
+                                        size_t msg_cap);
+/* [cpu.rs] validate_linear_attention_prepare_shape. */
+int orc_validate_linear_attention_prepare_shape(
+    int64_t mixed_qkv_raw_len, int64_t conv_weight_len, int64_t a_raw_len, int64_t b_raw_len,
+    int64_t a_log_len, int64_t dt_bias_len, int64_t query_len, int64_t key_len,
+    int64_t value_len, int64_t g_len, int64_t beta_len, int64_t tokens, int64_t key_heads,
+    int64_t value_heads, int64_t key_dim, int64_t value_dim, int64_t conv_kernel, char* msg,
+    size_t msg_cap);
+/* [cpu.rs] validate_linear_attention_decode_prepare_shape. */
+int orc_validate_linear_attention_decode_prepare_shape(
+    int64_t mixed_qkv_raw_len, int64_t conv_weight_len, int64_t conv_state_len,
+    int64_t a_raw_len, int64_t b_raw_len, int64_t a_log_len, int64_t dt_bias_len,
+    int64_t query_len, int64_t key_len, int64_t value_len, int64_t g_len, int64_t beta_len,
+    int64_t next_conv_state_len, int64_t key_heads, int64_t value_heads, int64_t key_dim,
+    int64_t value_dim, int64_t conv_kernel, char* msg, size_t msg_cap);
+/* [cpu.rs] recurrent_gated_delta_rule_varlen_f32: cu_seqlens starts at 0, ends
+ * at total_tokens, every range non-empty and increasing. */
+int orc_validate_cu_seqlens(const int32_t* cu_seqlens, int64_t batch, int64_t total_tokens,
+                            char* msg, size_t msg_cap);
+/* [qwen3_5.cpp] ValidateGdnStateIndices: -1 is the only negative value, a live
+ * slot is < state_slots, no duplicate live slot.  Both the O(n) seen-set pass
+ * and (when force_full != 0) the O(n^2) pairwise re-check run. */
+int orc_validate_state_indices(const int32_t* indices, int64_t n, int64_t state_slots,
+                               int force_full, char* msg, size_t msg_cap);
+
+/* ---- O1: prepare (conv1d + SiLU + split + gates + q/k L2 norm) ------------
+ * [cpu.rs] linear_attention_prepare_varlen_f32 and
+ * linear_attention_decode_prepare_batch_f32, with the conv tails read from and
+ * written back to a slot pool chosen by state_indices (the [cpu_ops.cpp]
+ * CausalConv1dUpdateKernel / GdnStateGatherKernel indexing):
+ *   state_indices == NULL     -> slot = sequence number
+ *   state_indices[s] == -1    -> padded sequence: outputs computed from a zero
+ *                                tail, the pool row is neither read nor written
+ *   has_initial_state == NULL -> every live sequence starts from its pool tail
+ *   has_initial_state[s] == 0 -> zero tail; the new tail is still written
+ * nthreads: 0 = hardware concurrency; results do not depend on it. */
+#define ORC_PREPARE_PARAMS(R)                                                              \
+  const R *mixed_qkv, int64_t x_stride, const R *conv_weight, R *conv_pool,                \
+      int64_t conv_slots, const int32_t *state_indices, const uint8_t *has_initial_state, \
+      const R *a_raw, int64_t a_stride, const R *b_raw, int64_t b_stride, const R *a_log,  \
+      const R *dt_bias, const int32_t *cu_seqlens, int64_t n_seqs, int64_t tokens,         \
+      int64_t key_heads, int64_t value_heads, int64_t key_dim, int64_t value_dim,          \
+      int64_t conv_kernel, int apply_qk_l2norm, R *query, R *key, R *value, R *g, R *beta, \
+      int nthreads
+int orc_prepare_varlen_f32(ORC_PREPARE_PARAMS(float));
+int orc_prepare_varlen_f64(ORC_PREPARE_PARAMS(double));
+
+/* ---- O2: sequential recurrence over varlen sequences ----------------------
+ * [cpu.rs] recurrent_gated_delta_rule_varlen_f32 (loop order, q/k norm form,
+ * k scaled by k_inv, q by q_inv*scale) on a state pool:
+ *   state_indices[s] == -1    -> out rows of sequence s are zero, pool untouched
+ *   has_initial_state[s] == 0 -> the recurrence starts from S = 0
+ *   the final state of each live sequence is written to its pool slot.
+ * items/n_items: optional list of work items (seq*Hv + head) to compute; the
+ * out rows of other items are left untouched (NULL = every item). */
+#define ORC_RECUR_PARAMS(R)                                                                 \
+  const R *query, const R *key, const R *value, const R *g, const R *beta, R *state_pool,   \
+      int64_t state_slots, const int32_t *state_indices, const uint8_t *has_initial_state,  \
+      const int32_t *cu_seqlens, int64_t n_seqs, int64_t tokens, int64_t key_heads,         \
+      int64_t value_heads, int64_t key_dim, int64_t value_dim, R scale, int use_qk_l2norm,  \
+      const int32_t *items, int64_t n_items, R *out, int nthreads
+int orc_gdn_varlen_f32(ORC_RECUR_PARAMS(float));
+int orc_gdn_varlen_f64(ORC_RECUR_PARAMS(double));
+
+/* ---- O3: decode, one token per row ----------------------------------------
+ * [cpu_ops.cpp] GdnDecodeKernel semantics: row b uses pool slot
+ * state_indices[b] (NULL -> b) in place; a negative index zeroes out row b and
+ * leaves the pool untouched. */
+#define ORC_DECODE_PARAMS(R)                                                              \
+  const R *query, const R *key, const R *value, const R *g, const R *beta, R *state_pool, \
+      int64_t state_slots, const int32_t *state_indices, int64_t batch, int64_t key_heads, \
+      int64_t value_heads, int64_t key_dim, int64_t value_dim, R scale, int use_qk_l2norm, \
+      R *out, int nthreads
+int orc_gdn_decode_f32(ORC_DECODE_PARAMS(float));
+int orc_gdn_decode_f64(ORC_DECODE_PARAMS(double));
+
+/* ---- O4: chunked WY/UT form, f64 only (self-check of the algebra) ---------
+ * Same contract as orc_gdn_varlen_f64; chunk = tokens per chunk (>= 1). */
+int orc_gdn_chunked_f64(const double* query, const double* key, const double* value,
+                        const double* g, const double* beta, double* state_pool,
+                        int64_t state_slots, const int32_t* state_indices,
+                        const uint8_t* has_initial_state, const int32_t* cu_seqlens,
+                        int64_t n_seqs, int64_t tokens, int64_t key_heads, int64_t value_heads,
+                        int64_t key_dim, int64_t value_dim, double scale, int use_qk_l2norm,
+                        int64_t chunk, double* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_ORACLE_H_ */
