@@ -1,0 +1,446 @@
+#!/usr/bin/env python3
+"""Benchmark of the GDN layer step on GB300.
+
+A step is one pass of the whole hot path over one batch: gdn_prepare over every
+token (conv1d + SiLU + split + q/k L2 norm + gates, conv tails in the pool),
+gdn_decode on the leading single-token rows and gdn_prefill_varlen (chunked
+tensor-core form) on the prefill sequences.  The default workload is the mixed
+serving step (512 decodes + 4 new 2048-token prefills, Hk=16 Hv=64 Dk=Dv=128,
+bf16 activations, f32 state pool of 1024 slots): the one configuration that
+runs every step of the path.  Inputs are seeded synthetic data already resident
+in HBM; the working set (state rows streamed by the decodes, 214 MB of
+mixed_qkv) is far larger than the 129 MB L2, so no flush is inserted.
+
+Prints ONE JSON line (rank 0).  Multi-GPU: one process per GPU under torchrun;
+each rank runs its own replica of the workload (the layer shards by sequence
+and head with no exchange), so scaling is weak and the value counts the tokens
+of all ranks over the slowest rank's time.
+
+--impl reference times the CPU oracle (the plain C++ restatement of the
+pages' CPU code) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GDN tokens/sec (decode, prefill) and % of HBM / bf16 tensor roofline"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mixed_hv64")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the single-kernel decode / prefill workloads")
+    ap.add_argument("--algo", type=int, default=0, help="prefill algorithm (0 auto)")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# ---- clocks ------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    QUERY = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.bus_id = (bus_id or "").lower()
+        self.proc = None
+        self.fh = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.flush()
+        self.fh.seek(0)
+        rows = [r.split(",") for r in self.fh.read().strip().splitlines() if r.strip()]
+        os.unlink(self.fh.name)
+        rows = [[c.strip() for c in r] for r in rows if len(r) >= 10]
+        if self.bus_id:
+            mine = [r for r in rows if r[1].lower().endswith(self.bus_id[-12:])]
+            rows = mine or rows
+        if not rows:
+            return None
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v == "Active"})
+        loaded = [s for s in sm if mx and s >= 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---- our arm ---------------------------------------------------------------------
+
+def dev_inputs(w, dev):
+    return dict(mixed_qkv=w.mixed_qkv.to(dev), conv_weight=w.conv_weight.to(dev),
+                a_raw=w.a_raw.to(dev), b_raw=w.b_raw.to(dev), A_log=w.A_log.to(dev),
+                dt_bias=w.dt_bias.to(dev), cu_seqlens=w.cu_seqlens.to(dev),
+                state_indices=w.state_indices.to(dev),
+                has_initial_state=w.has_initial_state.to(dev),
+                state_pool=w.state_pool.to(dev), conv_pool=w.conv_pool.to(dev),
+                cu_seqlens_prefill=w.cu_seqlens_prefill.to(dev))
+
+
+def run_step_events(step, d, stream, evs):
+    """One step with an event between every library call (on the launch stream)."""
+    import gated_delta_rule_44_gb300.binding as B
+    nd, ndt = step.n_decode, step.nd_tok
+    evs[0].record(stream)
+    B.gdn_prepare(d["mixed_qkv"], d["conv_weight"], d["a_raw"], d["b_raw"], d["A_log"],
+                  d["dt_bias"], d["cu_seqlens"], d["conv_pool"], step.q, step.k, step.v, step.g,
+                  step.beta, Hk=step.Hk, Hv=step.Hv, Dk=step.Dk, Dv=step.Dv, K=step.K,
+                  state_indices=d["state_indices"], has_initial_state=d["has_initial_state"],
+                  stream=stream)
+    evs[1].record(stream)
+    if nd > 0:
+        B.gdn_decode(step.q[:ndt], step.k[:ndt], step.v[:ndt], step.g[:ndt], step.beta[:ndt],
+                     d["state_pool"], step.out[:ndt], state_indices=d["state_indices"][:nd],
+                     stream=stream)
+    evs[2].record(stream)
+    if step.N > nd:
+        B.gdn_prefill_varlen(step.q[ndt:], step.k[ndt:], step.v[ndt:], step.g[ndt:],
+                             step.beta[ndt:], d["state_pool"], d["cu_seqlens_prefill"],
+                             step.out[ndt:], state_indices=d["state_indices"][nd:],
+                             has_initial_state=d["has_initial_state"][nd:], algo=step.algo,
+                             workspace=step.workspace, stream=stream)
+    evs[3].record(stream)
+
+
+def time_workload(w, dev, steps, warmup, algo, dist=None, clocks=None):
+    """Device-timed K steps; returns timing dict incl. per-kernel averages."""
+    import torch
+    import gated_delta_rule_44_gb300.binding as B
+    from gated_delta_rule_44_gb300.layer import GdnStep
+    d = dev_inputs(w, dev)
+    step = GdnStep(w.T, w.N, w.n_decode, w.Hk, w.Hv, w.Dk, w.Dv, w.K, w.act_dtype, dev,
+                   algo=algo)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                  for _ in range(steps + warmup)]
+        for i in range(warmup):
+            run_step_events(step, d, stream, evsets[i])
+        stream.synchronize()
+        B.gdn_read_device_status(stream)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        if clocks is not None:
+            clocks.start()
+            time.sleep(0.3)
+        launches0 = B.gdn_launch_count()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(warmup, warmup + steps):
+            run_step_events(step, d, stream, evsets[i])
+        t1.record(stream)
+        launches = B.gdn_launch_count() - launches0
+        stream.synchronize()
+        torch.cuda.synchronize(dev)
+        clk = clocks.stop() if clocks is not None else None
+        if dist is not None:
+            dist.barrier()
+        B.gdn_read_device_status(stream)
+    total_ms = t0.elapsed_time(t1)
+    per = {"prepare": [], "decode": [], "prefill": []}
+    for i in range(warmup, warmup + steps):
+        e = evsets[i]
+        per["prepare"].append(e[0].elapsed_time(e[1]))
+        per["decode"].append(e[1].elapsed_time(e[2]))
+        per["prefill"].append(e[2].elapsed_time(e[3]))
+    avg = {k: sum(v) / len(v) for k, v in per.items()}
+    del d, step
+    torch.cuda.empty_cache()
+    return dict(total_ms=total_ms, ms_per_step=total_ms / steps, kernel_ms=avg,
+                launches=launches, clocks=clk)
+
+
+def kernel_report(w, kernel_ms, peaks):
+    from gated_delta_rule_44_gb300 import roofline as R
+    work = R.step_work(w)
+    rep = {}
+    for name, wk in work.items():
+        ms = kernel_ms.get(name, 0.0)
+        if ms <= 0:
+            continue
+        entry = {"avg_us": round(ms * 1e3, 2)}
+        gbs = wk["bytes"] / (ms * 1e-3) / 1e9
+        entry["algorithmic_bytes"] = wk["bytes"]
+        entry["achieved_gbs"] = round(gbs, 1)
+        entry["hbm_frac_of_measured"] = round(gbs / peaks["hbm"], 4)
+        entry["hbm_frac_of_8tbs"] = round(gbs / 8000.0, 4)
+        if "flops" in wk:
+            tf = wk["flops"] / (ms * 1e-3) / 1e12
+            entry["algorithmic_flops"] = wk["flops"]
+            entry["achieved_tflops"] = round(tf, 2)
+            entry["tensor_frac_of_measured"] = round(tf / peaks["bf16"], 4)
+        rep[name] = entry
+    return rep, work
+
+
+def roofline_entry(w, kernel_ms, peaks, traffic=None):
+    rep, work = kernel_report(w, kernel_ms, peaks)
+    dom = max(rep, key=lambda k: rep[k]["avg_us"])
+    r = rep[dom]
+    if "flops" in work[dom]:
+        ach = r["achieved_tflops"]
+        return dom, {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peaks["bf16"],
+                     "unit": "TFLOP/s", "frac": round(ach / peaks["bf16"], 4),
+                     "traffic": traffic, "peak_source": peaks["source"] + " (burst)"}, rep
+    ach = r["achieved_gbs"]
+    return dom, {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peaks["hbm"],
+                 "unit": "GB/s", "frac": round(ach / peaks["hbm"], 4), "traffic": traffic,
+                 "peak_source": peaks["source"]}, rep
+
+
+def time_e2e(w, dev, steps, warmup, algo):
+    """Same step through the public API with the step's inputs in pinned host
+    memory: H2D of the inputs and D2H of the output inside the timed region."""
+    import torch
+    from gated_delta_rule_44_gb300.layer import GdnStep
+    d = dev_inputs(w, dev)
+    host_in = {k: getattr(w, k).pin_memory() for k in ("mixed_qkv", "a_raw", "b_raw",
+                                                      "cu_seqlens", "state_indices",
+                                                      "has_initial_state")}
+    host_in["cu_seqlens_prefill"] = w.cu_seqlens_prefill.pin_memory()
+    step = GdnStep(w.T, w.N, w.n_decode, w.Hk, w.Hv, w.Dk, w.Dv, w.K, w.act_dtype, dev,
+                   algo=algo)
+    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = out_host.numel() * out_host.element_size()
+    stream = torch.cuda.Stream(device=dev)
+
+    def one():
+        for k, t in host_in.items():
+            d[k].copy_(t, non_blocking=True)
+        step.run(d["mixed_qkv"], d["a_raw"], d["b_raw"], d["conv_weight"], d["A_log"],
+                 d["dt_bias"], d["cu_seqlens"], d["state_indices"], d["has_initial_state"],
+                 d["state_pool"], d["conv_pool"], d["cu_seqlens_prefill"], stream=stream)
+        out_host.copy_(step.out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            one()
+        stream.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(steps):
+            one()
+        t1.record(stream)
+        stream.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    del d, step
+    torch.cuda.empty_cache()
+    return {"value": round(w.T / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ---- CPU oracle baseline -----------------------------------------------------------
+
+def oracle_sample(w, heads_sampled, nthreads):
+    """Time the oracle (prepare over every token + recurrence over every
+    sequence for `heads_sampled` of the Hv value heads) and extrapolate the
+    recurrence linearly in heads.  Returns (tokens/s, seconds spent, sample)."""
+    import numpy as np
+    import oracle
+    T = w.T
+    f32 = lambda t: t.float().numpy()
+    pool = w.conv_pool.numpy().copy()
+    t0 = time.perf_counter()
+    prep = oracle.prepare_varlen(f32(w.mixed_qkv), w.conv_weight.numpy(), pool, f32(w.a_raw),
+                                 f32(w.b_raw), w.A_log.numpy(), w.dt_bias.numpy(),
+                                 w.cu_seqlens.numpy(), w.Hk, w.Hv, w.Dk, w.Dv, w.K,
+                                 state_indices=w.state_indices.numpy(),
+                                 has_initial_state=w.has_initial_state.numpy(),
+                                 dtype=np.float32, nthreads=nthreads)
+    t_prep = time.perf_counter() - t0
+    heads = list(range(heads_sampled))
+    seqs = list(range(w.N))
+    slots = [int(s) for s in w.state_indices.tolist()]
+    live = [i for i, s in enumerate(slots) if s >= 0]
+    cpool = np.stack([w.state_pool[slots[i]][: heads_sampled].numpy() for i in live]) \
+        if live else np.zeros((1, heads_sampled, w.Dv, w.Dk), np.float32)
+    # A pool holding only the sampled heads: present those heads as Hv' = heads_sampled.
+    remap = np.full(w.N, -1, np.int32)
+    for j, i in enumerate(live):
+        remap[i] = j
+    Hk_s = max(1, heads_sampled // (w.Hv // w.Hk))
+    t1 = time.perf_counter()
+    oracle.gdn_varlen(prep["q"][:, :Hk_s], prep["k"][:, :Hk_s], prep["v"][:, :heads_sampled],
+                      prep["g"][:, :heads_sampled], prep["beta"][:, :heads_sampled],
+                      np.ascontiguousarray(cpool), w.cu_seqlens.numpy(), 1.0 / np.sqrt(w.Dk),
+                      state_indices=remap, has_initial_state=w.has_initial_state.numpy(),
+                      dtype=np.float32, nthreads=nthreads)
+    t_rec = time.perf_counter() - t1
+    est = t_prep + t_rec * (w.Hv / heads_sampled)
+    sample = (f"oracle f32 prepare over all {T} tokens + recurrence over all {w.N} sequences "
+              f"for {heads_sampled} of {w.Hv} value heads (key heads {Hk_s}); step time "
+              f"extrapolated linearly in heads: {t_prep:.2f}s + {t_rec:.2f}s x "
+              f"{w.Hv / heads_sampled:g}")
+    return T / est, t_prep + t_rec, sample
+
+
+def cpu_baseline(w, nthreads, budget_s=20.0):
+    heads = 1
+    tps, spent, sample = oracle_sample(w, heads, nthreads)
+    # grow the sample toward the budget (bounded: at most all heads)
+    while spent < budget_s / 3 and heads * 2 <= w.Hv:
+        heads *= 2
+        tps, spent, sample = oracle_sample(w, heads, nthreads)
+    return {"value": round(tps, 2), "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+            "sample": sample, "seconds": round(spent, 2)}
+
+
+def rank_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def main_reference(args):
+    ws, rank, _ = rank_info()
+    if rank != 0:
+        return 0
+    from gated_delta_rule_44_gb300 import workloads as W
+    import oracle
+    oracle.build()
+    w = W.named(args.workload)
+    nthreads = os.cpu_count() or 1
+    vals = []
+    samp = ""
+    for i in range(args.warmup + args.steps):
+        tps, spent, samp = oracle_sample(w, 1, nthreads)
+        if i >= args.warmup:
+            vals.append(tps)
+    v = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 2), "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(w.T / v * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": args.workload, "tokens_per_step": w.T},
+            "cpu_baseline": {"value": round(v, 2), "unit": "tokens/s", "cores": nthreads,
+                             "kind": "oracle", "sample": samp},
+            "e2e": {"value": round(v, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return main_reference(args)
+    import torch
+    ws, rank, local = rank_info()
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    import gated_delta_rule_44_gb300.binding as B
+    from gated_delta_rule_44_gb300 import workloads as W
+    B.lib()
+    peaks = load_peaks()
+    w = W.named(args.workload)
+    props = torch.cuda.get_device_properties(dev)
+    bus = getattr(props, "pci_bus_id", None)
+    clocks = ClockSampler(bus) if rank == 0 else None
+    res = time_workload(w, dev, args.steps, max(args.warmup, 3), args.algo, dist, clocks)
+    ms = res["ms_per_step"]
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = w.T * ws / (ms * 1e-3)
+    dom, roof, kernels = roofline_entry(w, res["kernel_ms"], peaks)
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "tokens_per_step": w.T, "decodes": w.n_decode,
+                       "prefill_seqlens": w.seqlens[w.n_decode:], "Hk": w.Hk, "Hv": w.Hv,
+                       "Dk": w.Dk, "Dv": w.Dv, "conv_kernel": w.K, "state_slots": w.slots,
+                       "state_dtype": "f32", "parallelism": f"replicas{ws}",
+                       "l2": "inputs larger than L2 (no flush)",
+                       "prefill_algo": B.gdn_prefill_resolve_algo(w.Dk, w.Dv, 1, args.algo)},
+            "roofline": roof, "kernels": kernels, "gpu_launches": res["launches"],
+            "clocks": res["clocks"]}
+    if rank == 0 and not args.no_extra:
+        extra = {}
+        for name in ("decode_b256", "prefill_4k"):
+            wx = W.named(name)
+            rx = time_workload(wx, dev, max(args.steps, 10), max(args.warmup, 3), args.algo)
+            _, rf, kx = roofline_entry(wx, rx["kernel_ms"], peaks)
+            extra[name] = {"tokens_per_s": round(wx.T / (rx["ms_per_step"] * 1e-3), 1),
+                           "ms_per_step": round(rx["ms_per_step"], 4), "roofline": rf,
+                           "kernels": kx}
+            del wx
+        line["extra_workloads"] = extra
+    if rank == 0 and not args.no_e2e:
+        line["e2e"] = time_e2e(w, dev, max(3, args.steps // 2), 3, args.algo)
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        line["cpu_baseline"] = cpu_baseline(w, os.cpu_count() or 1)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

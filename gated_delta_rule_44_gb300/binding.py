@@ -1,0 +1,247 @@
+"""Thin ctypes binding of libgdn (include/gdn.h).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  Functions take torch tensors (device memory and streams come from
+PyTorch) and raise ``GdnError`` on a non-zero status.  There is no fallback:
+if the library cannot be built or loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+GDN_OK = 0
+GDN_ERR_SHAPE = 1
+GDN_ERR_INVALID_ARGUMENT = 2
+GDN_ERR_DTYPE = 3
+GDN_ERR_UNSUPPORTED = 4
+GDN_ERR_CUDA = 5
+GDN_ERR_TIMEOUT = 6
+GDN_ERR_DEVICE_CHECK = 7
+
+GDN_DTYPE_F32 = 0
+GDN_DTYPE_BF16 = 1
+
+GDN_PREFILL_AUTO = 0
+GDN_PREFILL_CHUNKED = 1
+GDN_PREFILL_RECURRENT = 2
+
+_i64 = ctypes.c_int64
+_i32 = ctypes.c_int32
+_vp = ctypes.c_void_p
+_f32 = ctypes.c_float
+
+
+class gdn_prepare_args(ctypes.Structure):
+    _fields_ = [("T", _i64), ("N", _i64), ("Hk", _i64), ("Hv", _i64), ("Dk", _i64), ("Dv", _i64),
+                ("K", _i64), ("act_dtype", _i32), ("apply_qk_l2norm", _i32),
+                ("mixed_qkv", _vp), ("mixed_qkv_stride", _i64), ("mixed_qkv_len", _i64),
+                ("conv_weight", _vp), ("conv_weight_len", _i64),
+                ("a_raw", _vp), ("a_raw_stride", _i64), ("a_raw_len", _i64),
+                ("b_raw", _vp), ("b_raw_stride", _i64), ("b_raw_len", _i64),
+                ("A_log", _vp), ("A_log_len", _i64), ("dt_bias", _vp), ("dt_bias_len", _i64),
+                ("cu_seqlens", _vp), ("state_indices", _vp), ("has_initial_state", _vp),
+                ("cu_seqlens_host", _vp), ("state_indices_host", _vp),
+                ("conv_state", _vp), ("conv_state_slots", _i64), ("conv_state_len", _i64),
+                ("q", _vp), ("q_len", _i64), ("k", _vp), ("k_len", _i64), ("v", _vp),
+                ("v_len", _i64), ("g", _vp), ("g_len", _i64), ("beta", _vp),
+                ("beta_len", _i64)]
+
+
+class gdn_decode_args(ctypes.Structure):
+    _fields_ = [("B", _i64), ("Hk", _i64), ("Hv", _i64), ("Dk", _i64), ("Dv", _i64),
+                ("act_dtype", _i32), ("use_qk_l2norm", _i32), ("scale", _f32),
+                ("q", _vp), ("q_len", _i64), ("k", _vp), ("k_len", _i64), ("v", _vp),
+                ("v_len", _i64), ("g", _vp), ("g_len", _i64), ("beta", _vp), ("beta_len", _i64),
+                ("state", _vp), ("state_slots", _i64), ("state_len", _i64),
+                ("state_indices", _vp), ("state_indices_host", _vp),
+                ("out", _vp), ("out_len", _i64)]
+
+
+class gdn_prefill_args(ctypes.Structure):
+    _fields_ = [("T", _i64), ("N", _i64), ("Hk", _i64), ("Hv", _i64), ("Dk", _i64), ("Dv", _i64),
+                ("act_dtype", _i32), ("use_qk_l2norm", _i32), ("scale", _f32), ("algo", _i32),
+                ("q", _vp), ("q_len", _i64), ("k", _vp), ("k_len", _i64), ("v", _vp),
+                ("v_len", _i64), ("g", _vp), ("g_len", _i64), ("beta", _vp), ("beta_len", _i64),
+                ("state", _vp), ("state_slots", _i64), ("state_len", _i64),
+                ("cu_seqlens", _vp), ("state_indices", _vp), ("has_initial_state", _vp),
+                ("cu_seqlens_host", _vp), ("state_indices_host", _vp),
+                ("out", _vp), ("out_len", _i64), ("workspace", _vp),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+EXPORTED = ("gdn_prepare", "gdn_decode", "gdn_prefill_varlen", "gdn_prefill_workspace_bytes",
+            "gdn_prefill_resolve_algo", "gdn_status_string", "gdn_last_error_message",
+            "gdn_read_device_status", "gdn_version", "gdn_launch_count")
+
+
+class GdnError(RuntimeError):
+    def __init__(self, code: int, name: str, msg: str):
+        super().__init__(f"{name}: {msg}")
+        self.code = code
+        self.status = name
+        self.msg = msg
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Build (if stale) and load libgdn.so; raises if that is impossible."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ctypes.CDLL(_build.build_library())
+            for name in ("gdn_prepare", "gdn_decode", "gdn_prefill_varlen",
+                         "gdn_read_device_status", "gdn_version"):
+                getattr(L, name).restype = ctypes.c_int
+            L.gdn_prepare.argtypes = [ctypes.POINTER(gdn_prepare_args), _vp]
+            L.gdn_decode.argtypes = [ctypes.POINTER(gdn_decode_args), _vp]
+            L.gdn_prefill_varlen.argtypes = [ctypes.POINTER(gdn_prefill_args), _vp]
+            L.gdn_read_device_status.argtypes = [_vp]
+            L.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
+            L.gdn_prefill_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64, _i64, _i32, _i32]
+            L.gdn_prefill_resolve_algo.restype = _i32
+            L.gdn_prefill_resolve_algo.argtypes = [_i64, _i64, _i32, _i32]
+            L.gdn_status_string.restype = ctypes.c_char_p
+            L.gdn_status_string.argtypes = [ctypes.c_int]
+            L.gdn_last_error_message.restype = ctypes.c_char_p
+            L.gdn_last_error_message.argtypes = []
+            L.gdn_launch_count.restype = ctypes.c_uint64
+            L.gdn_launch_count.argtypes = []
+            _lib = L
+        return _lib
+
+
+def _check(rc: int) -> None:
+    if rc != GDN_OK:
+        L = lib()
+        raise GdnError(rc, L.gdn_status_string(rc).decode(), L.gdn_last_error_message().decode())
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return GDN_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return GDN_DTYPE_F32
+    raise GdnError(GDN_ERR_DTYPE, "GDN_ERR_DTYPE", f"unsupported activation dtype {t.dtype}")
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _n(t: Optional[torch.Tensor]) -> int:
+    """Elements reachable from the tensor's first element (its allocation length)."""
+    if t is None:
+        return 0
+    if t.numel() == 0:
+        return 0
+    return int(sum((s - 1) * st for s, st in zip(t.shape, t.stride())) + 1)
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _host_i32(t: Optional[torch.Tensor]):
+    if t is None:
+        return None, None
+    h = t.detach().to("cpu", torch.int32).contiguous()
+    return h, h.data_ptr()
+
+
+def gdn_prepare(mixed_qkv, conv_weight, a_raw, b_raw, A_log, dt_bias, cu_seqlens, conv_state,
+                q, k, v, g, beta, *, Hk, Hv, Dk, Dv, K, state_indices=None,
+                has_initial_state=None, cu_seqlens_host=None, state_indices_host=None,
+                apply_qk_l2norm=True, stream=None) -> None:
+    """include/gdn.h gdn_prepare; outputs q, k, v, g, beta are written, the
+    conv_state pool is updated in place."""
+    T = mixed_qkv.shape[0]
+    N = cu_seqlens.numel() - 1
+    cuh, cuh_p = _host_i32(cu_seqlens_host)
+    sih, sih_p = _host_i32(state_indices_host)
+    a = gdn_prepare_args(
+        T=T, N=N, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, K=K, act_dtype=_dt(mixed_qkv),
+        apply_qk_l2norm=int(apply_qk_l2norm),
+        mixed_qkv=_p(mixed_qkv), mixed_qkv_stride=mixed_qkv.stride(0), mixed_qkv_len=_n(mixed_qkv),
+        conv_weight=_p(conv_weight), conv_weight_len=_n(conv_weight),
+        a_raw=_p(a_raw), a_raw_stride=a_raw.stride(0), a_raw_len=_n(a_raw),
+        b_raw=_p(b_raw), b_raw_stride=b_raw.stride(0), b_raw_len=_n(b_raw),
+        A_log=_p(A_log), A_log_len=_n(A_log), dt_bias=_p(dt_bias), dt_bias_len=_n(dt_bias),
+        cu_seqlens=_p(cu_seqlens), state_indices=_p(state_indices),
+        has_initial_state=_p(has_initial_state), cu_seqlens_host=cuh_p,
+        state_indices_host=sih_p, conv_state=_p(conv_state),
+        conv_state_slots=conv_state.shape[0] if conv_state is not None else 0,
+        conv_state_len=_n(conv_state), q=_p(q), q_len=_n(q), k=_p(k), k_len=_n(k), v=_p(v),
+        v_len=_n(v), g=_p(g), g_len=_n(g), beta=_p(beta), beta_len=_n(beta))
+    _check(lib().gdn_prepare(ctypes.byref(a), _stream(stream)))
+
+
+def gdn_decode(q, k, v, g, beta, state, out, *, scale=-1.0, state_indices=None,
+               state_indices_host=None, use_qk_l2norm=False, stream=None) -> None:
+    """include/gdn.h gdn_decode; `state` [slots,Hv,Dv,Dk] f32 updated in place."""
+    B, Hk, Dk = q.shape
+    _, Hv, Dv = v.shape
+    sih, sih_p = _host_i32(state_indices_host)
+    a = gdn_decode_args(
+        B=B, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, act_dtype=_dt(q), use_qk_l2norm=int(use_qk_l2norm),
+        scale=float(scale), q=_p(q), q_len=_n(q), k=_p(k), k_len=_n(k), v=_p(v), v_len=_n(v),
+        g=_p(g), g_len=_n(g), beta=_p(beta), beta_len=_n(beta), state=_p(state),
+        state_slots=state.shape[0], state_len=_n(state), state_indices=_p(state_indices),
+        state_indices_host=sih_p, out=_p(out), out_len=_n(out))
+    _check(lib().gdn_decode(ctypes.byref(a), _stream(stream)))
+
+
+def gdn_prefill_workspace_bytes(T, N, Hv, Dk, Dv, act_dtype=GDN_DTYPE_BF16,
+                                algo=GDN_PREFILL_AUTO) -> int:
+    return int(lib().gdn_prefill_workspace_bytes(T, N, Hv, Dk, Dv, act_dtype, algo))
+
+
+def gdn_prefill_resolve_algo(Dk, Dv, act_dtype=GDN_DTYPE_BF16, algo=GDN_PREFILL_AUTO) -> int:
+    return int(lib().gdn_prefill_resolve_algo(Dk, Dv, act_dtype, algo))
+
+
+def gdn_prefill_varlen(q, k, v, g, beta, state, cu_seqlens, out, *, scale=-1.0,
+                       state_indices=None, has_initial_state=None, cu_seqlens_host=None,
+                       state_indices_host=None, use_qk_l2norm=False, algo=GDN_PREFILL_AUTO,
+                       workspace=None, stream=None) -> None:
+    """include/gdn.h gdn_prefill_varlen; `state` updated in place.  `workspace`
+    is a uint8 device tensor of at least gdn_prefill_workspace_bytes() bytes."""
+    T, Hk, Dk = q.shape
+    _, Hv, Dv = v.shape
+    N = cu_seqlens.numel() - 1
+    cuh, cuh_p = _host_i32(cu_seqlens_host)
+    sih, sih_p = _host_i32(state_indices_host)
+    a = gdn_prefill_args(
+        T=T, N=N, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, act_dtype=_dt(q), use_qk_l2norm=int(use_qk_l2norm),
+        scale=float(scale), algo=int(algo), q=_p(q), q_len=_n(q), k=_p(k), k_len=_n(k),
+        v=_p(v), v_len=_n(v), g=_p(g), g_len=_n(g), beta=_p(beta), beta_len=_n(beta),
+        state=_p(state), state_slots=state.shape[0], state_len=_n(state),
+        cu_seqlens=_p(cu_seqlens), state_indices=_p(state_indices),
+        has_initial_state=_p(has_initial_state), cu_seqlens_host=cuh_p,
+        state_indices_host=sih_p, out=_p(out), out_len=_n(out), workspace=_p(workspace),
+        workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size())
+    _check(lib().gdn_prefill_varlen(ctypes.byref(a), _stream(stream)))
+
+
+def gdn_read_device_status(stream=None) -> None:
+    """Synchronises the stream and raises GdnError if a kernel flagged an error."""
+    _check(lib().gdn_read_device_status(_stream(stream)))
+
+
+def gdn_version() -> int:
+    return int(lib().gdn_version())
+
+
+def gdn_launch_count() -> int:
+    """Kernel launches issued through the library by this process so far."""
+    return int(lib().gdn_launch_count())

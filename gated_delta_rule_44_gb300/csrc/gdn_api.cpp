@@ -1,0 +1,426 @@
+// gdn_api.cpp -- the C ABI of libgdn: argument validation and dispatch.
+//
+// Shape and length rules follow [cpu.rs] (ferrum-kernels 0.8.0,
+// src/ferrum_kernels/backend/cpu.rs) validate_gated_delta_rule_shape,
+// validate_linear_attention_prepare_shape and the cu_seqlens rules of
+// recurrent_gated_delta_rule_varlen_f32, with the same message text.  Index
+// rules follow [qwen3_5.cpp] (vllm.cpp, src/vllm/model_executor/models/
+// qwen3_5.cpp) ValidateGdnStateIndices.  On any error nothing is launched.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/gdn.h"
+#include "gdn_internal.h"
+
+namespace {
+
+thread_local std::string t_msg;
+
+int fail(int code, std::string m) {
+  t_msg = std::move(m);
+  return code;
+}
+int succeed() {
+  t_msg.clear();
+  return GDN_OK;
+}
+
+std::string S(int64_t v) { return std::to_string(v); }
+
+struct LenRule {
+  const char* label;
+  int64_t actual, expected;
+};
+
+template <size_t N>
+int check_lengths(const char* prefix, const LenRule (&rules)[N]) {
+  for (const auto& r : rules)
+    if (r.actual < r.expected)
+      return fail(GDN_ERR_SHAPE, std::string(prefix) + " " + r.label + " length " + S(r.actual) +
+                                     " < expected " + S(r.expected));
+  return GDN_OK;
+}
+
+int check_act_dtype(int32_t dt) {
+  if (dt != GDN_DTYPE_F32 && dt != GDN_DTYPE_BF16)
+    return fail(GDN_ERR_DTYPE, "act_dtype must be GDN_DTYPE_F32 or GDN_DTYPE_BF16, got " + S(dt));
+  return GDN_OK;
+}
+
+int64_t elem_size(int32_t dt) { return dt == GDN_DTYPE_BF16 ? 2 : 4; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int require_ptr(const void* p, const char* label) {
+  if (p == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, std::string(label) + " is NULL");
+  return GDN_OK;
+}
+
+int require_aligned(const void* p, const char* label) {
+  if (!aligned16(p))
+    return fail(GDN_ERR_INVALID_ARGUMENT, std::string(label) + " must be 16-byte aligned");
+  return GDN_OK;
+}
+
+// [cpu.rs] validate_gated_delta_rule_shape: dims positive, Hv % Hk == 0.
+int check_recurrence_dims(int64_t tokens, int64_t hk, int64_t hv, int64_t dk, int64_t dv) {
+  if (tokens <= 0 || hk <= 0 || hv <= 0 || dk <= 0 || dv <= 0)
+    return fail(GDN_ERR_SHAPE, "gated_delta_rule shape must be positive, got tokens=" + S(tokens) +
+                                   " key_heads=" + S(hk) + " value_heads=" + S(hv) +
+                                   " key_dim=" + S(dk) + " value_dim=" + S(dv));
+  if (hv % hk != 0)
+    return fail(GDN_ERR_SHAPE, "gated_delta_rule value_heads " + S(hv) +
+                                   " must be divisible by key_heads " + S(hk));
+  return GDN_OK;
+}
+
+// [cpu.rs] recurrent_gated_delta_rule_varlen_f32 cu_seqlens rules.
+int check_cu_host(const int32_t* cu, int64_t n, int64_t total, const char* who) {
+  if (cu[0] != 0 || cu[n] != total)
+    return fail(GDN_ERR_INVALID_ARGUMENT,
+                std::string(who) + " cu_seqlens must start at 0 and end at total_tokens " +
+                    S(total) + ", got first=" + S(cu[0]) + " last=" + S(cu[n]));
+  for (int64_t s = 0; s < n; ++s)
+    if (cu[s + 1] <= cu[s])
+      return fail(GDN_ERR_INVALID_ARGUMENT, std::string(who) + " sequence " + S(s) +
+                                                " has empty or non-monotonic range " +
+                                                S(cu[s]) + ".." + S(cu[s + 1]));
+  return GDN_OK;
+}
+
+// [qwen3_5.cpp] ValidateGdnStateIndices: -1 is the only allowed negative, live
+// slots in range and distinct (O(n) seen-set).
+int check_indices_host(const int32_t* idx, int64_t n, int64_t slots) {
+  std::vector<unsigned char> seen(static_cast<size_t>(slots), 0);
+  for (int64_t i = 0; i < n; ++i) {
+    const int32_t slot = idx[i];
+    if (slot < 0) {
+      if (slot != -1) return fail(GDN_ERR_INVALID_ARGUMENT, "invalid negative GDN state index");
+      continue;
+    }
+    if (slot >= slots) return fail(GDN_ERR_INVALID_ARGUMENT, "GDN state index out of range");
+    if (seen[slot]) return fail(GDN_ERR_INVALID_ARGUMENT, "duplicate live GDN state index");
+    seen[slot] = 1;
+  }
+  return GDN_OK;
+}
+
+bool fits_i32(int64_t v) { return v >= 0 && v <= INT32_MAX; }
+
+int launch_result(cudaError_t e, const char* what) {
+  if (e != cudaSuccess)
+    return fail(GDN_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+  return succeed();
+}
+
+float resolve_scale(float scale, int64_t dk) {
+  return scale < 0.0f ? 1.0f / std::sqrt(static_cast<float>(dk)) : scale;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_version(void) { return 100; }
+
+const char* gdn_status_string(int status) {
+  switch (status) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_SHAPE: return "GDN_ERR_SHAPE";
+    case GDN_ERR_INVALID_ARGUMENT: return "GDN_ERR_INVALID_ARGUMENT";
+    case GDN_ERR_DTYPE: return "GDN_ERR_DTYPE";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+    case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT";
+    case GDN_ERR_DEVICE_CHECK: return "GDN_ERR_DEVICE_CHECK";
+    default: return "GDN_ERR_UNKNOWN";
+  }
+}
+
+const char* gdn_last_error_message(void) { return t_msg.c_str(); }
+
+int gdn_read_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(GDN_ERR_CUDA, std::string("sync: ") + cudaGetErrorString(e));
+  unsigned* w = gdn::status_word();
+  if (w == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
+  unsigned v = 0;
+  e = cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(w, 0, sizeof(unsigned));
+  if (e != cudaSuccess)
+    return fail(GDN_ERR_CUDA, std::string("status read: ") + cudaGetErrorString(e));
+  if (v & gdn::kStatusTimeout) return fail(GDN_ERR_TIMEOUT, "a device-side wait timed out");
+  if (v & gdn::kStatusBadIndex)
+    return fail(GDN_ERR_DEVICE_CHECK, "a kernel saw a state index outside [-1, slots)");
+  if (v & gdn::kStatusBadSeqlens)
+    return fail(GDN_ERR_DEVICE_CHECK, "a kernel saw malformed cu_seqlens");
+  return succeed();
+}
+
+int gdn_prepare(const gdn_prepare_args* a, void* stream) {
+  if (a == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "args is NULL");
+  if (int rc = check_act_dtype(a->act_dtype)) return rc;
+  // [cpu.rs] validate_linear_attention_prepare_shape
+  if (a->T <= 0 || a->Hk <= 0 || a->Hv <= 0 || a->Dk <= 0 || a->Dv <= 0 || a->K <= 0)
+    return fail(GDN_ERR_SHAPE, "linear_attention_prepare shape must be positive, got tokens=" +
+                                   S(a->T) + " key_heads=" + S(a->Hk) + " value_heads=" +
+                                   S(a->Hv) + " key_dim=" + S(a->Dk) + " value_dim=" + S(a->Dv) +
+                                   " conv_kernel=" + S(a->K));
+  if (a->N <= 0) return fail(GDN_ERR_SHAPE, "linear_attention_prepare_varlen batch must be positive");
+  const int64_t qk_total = a->Hk * a->Dk, v_total = a->Hv * a->Dv;
+  const int64_t C = 2 * qk_total + v_total;
+  const int64_t x_stride = a->mixed_qkv_stride > 0 ? a->mixed_qkv_stride : C;
+  const int64_t a_stride = a->a_raw_stride > 0 ? a->a_raw_stride : a->Hv;
+  const int64_t b_stride = a->b_raw_stride > 0 ? a->b_raw_stride : a->Hv;
+  if (x_stride < C || a_stride < a->Hv || b_stride < a->Hv)
+    return fail(GDN_ERR_SHAPE, "linear_attention_prepare row stride shorter than the row");
+  const LenRule rules[] = {
+      {"mixed_qkv_raw", a->mixed_qkv_len, (a->T - 1) * x_stride + C},
+      {"conv_weight", a->conv_weight_len, C * a->K},
+      {"a_raw", a->a_raw_len, (a->T - 1) * a_stride + a->Hv},
+      {"b_raw", a->b_raw_len, (a->T - 1) * b_stride + a->Hv},
+      {"a_log", a->A_log_len, a->Hv},
+      {"dt_bias", a->dt_bias_len, a->Hv},
+      {"query", a->q_len, a->T * qk_total},
+      {"key", a->k_len, a->T * qk_total},
+      {"value", a->v_len, a->T * v_total},
+      {"g", a->g_len, a->T * a->Hv},
+      {"beta", a->beta_len, a->T * a->Hv},
+  };
+  if (int rc = check_lengths("linear_attention_prepare", rules)) return rc;
+  if (a->conv_state_slots <= 0)
+    return fail(GDN_ERR_SHAPE, "linear_attention_prepare conv_state must have at least one slot");
+  const LenRule pool_rule[] = {
+      {"conv_state", a->conv_state_len, a->conv_state_slots * C * (a->K - 1)}};
+  if (int rc = check_lengths("linear_attention_prepare", pool_rule)) return rc;
+  for (auto pr : {std::make_pair((const void*)a->mixed_qkv, "mixed_qkv"),
+                  std::make_pair((const void*)a->conv_weight, "conv_weight"),
+                  std::make_pair((const void*)a->a_raw, "a_raw"),
+                  std::make_pair((const void*)a->b_raw, "b_raw"),
+                  std::make_pair((const void*)a->A_log, "A_log"),
+                  std::make_pair((const void*)a->dt_bias, "dt_bias"),
+                  std::make_pair((const void*)a->cu_seqlens, "cu_seqlens"),
+                  std::make_pair((const void*)a->q, "q"), std::make_pair((const void*)a->k, "k"),
+                  std::make_pair((const void*)a->v, "v"), std::make_pair((const void*)a->g, "g"),
+                  std::make_pair((const void*)a->beta, "beta")})
+    if (int rc = require_ptr(pr.first, pr.second)) return rc;
+  if (a->K > 1)
+    if (int rc = require_ptr(a->conv_state, "conv_state")) return rc;
+  // Kernel coverage.
+  const int64_t cpt = a->act_dtype == GDN_DTYPE_BF16 ? 8 : 4;  // channels per 16-byte vector
+  const bool dk_pow2 = (a->Dk & (a->Dk - 1)) == 0;
+  if (a->K > 8 || !dk_pow2 || a->Dk < cpt || a->Dk > 32 * cpt || a->Dv % cpt != 0)
+    return fail(GDN_ERR_UNSUPPORTED,
+                "gdn_prepare supports K <= 8, Dk a power of two in [" + S(cpt) + ", " +
+                    S(32 * cpt) + "] and Dv a multiple of " + S(cpt));
+  if (!fits_i32(a->T) || !fits_i32(a->N) || !fits_i32(a->T * C))
+    return fail(GDN_ERR_UNSUPPORTED, "gdn_prepare sizes exceed 32-bit token indexing");
+  const int64_t es = elem_size(a->act_dtype);
+  for (auto pr : {std::make_pair((const void*)a->mixed_qkv, "mixed_qkv"),
+                  std::make_pair((const void*)a->q, "q"), std::make_pair((const void*)a->k, "k"),
+                  std::make_pair((const void*)a->v, "v")})
+    if (int rc = require_aligned(pr.first, pr.second)) return rc;
+  if ((x_stride * es) % 16 != 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "mixed_qkv row stride must be a multiple of 16 bytes");
+  if (a->cu_seqlens_host != nullptr)
+    if (int rc = check_cu_host(a->cu_seqlens_host, a->N, a->T, "linear_attention_prepare_varlen"))
+      return rc;
+  if (a->state_indices_host != nullptr)
+    if (int rc = check_indices_host(a->state_indices_host, a->N, a->conv_state_slots)) return rc;
+  if (a->state_indices == nullptr && a->N > a->conv_state_slots)
+    return fail(GDN_ERR_SHAPE, "linear_attention_prepare conv_state has fewer slots than sequences");
+
+  gdn::PrepareLaunch p{};
+  p.T = (int)a->T;
+  p.N = (int)a->N;
+  p.Hk = (int)a->Hk;
+  p.Hv = (int)a->Hv;
+  p.Dk = (int)a->Dk;
+  p.Dv = (int)a->Dv;
+  p.K = (int)a->K;
+  p.bf16 = a->act_dtype == GDN_DTYPE_BF16;
+  p.norm = a->apply_qk_l2norm != 0;
+  p.x = a->mixed_qkv;
+  p.x_stride = x_stride;
+  p.w = a->conv_weight;
+  p.a = a->a_raw;
+  p.a_stride = a_stride;
+  p.b = a->b_raw;
+  p.b_stride = b_stride;
+  p.A_log = a->A_log;
+  p.dt_bias = a->dt_bias;
+  p.cu = a->cu_seqlens;
+  p.sidx = a->state_indices;
+  p.has_init = a->has_initial_state;
+  p.conv_pool = a->conv_state;
+  p.slots = a->conv_state_slots;
+  p.q = a->q;
+  p.k = a->k;
+  p.v = a->v;
+  p.g = a->g;
+  p.beta = a->beta;
+  p.status = gdn::status_word();
+  if (p.status == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
+  return launch_result(gdn::launch_prepare(p, static_cast<cudaStream_t>(stream)), "gdn_prepare");
+}
+
+namespace {
+
+// Shared checks of decode and prefill: [cpu.rs] validate_gated_delta_rule_shape
+// with the state pool in place of initial/final state.
+int check_recurrence(int64_t tokens, int64_t Hk, int64_t Hv, int64_t Dk, int64_t Dv,
+                     int32_t act_dtype, const void* q, int64_t q_len, const void* k,
+                     int64_t k_len, const void* v, int64_t v_len, const float* g, int64_t g_len,
+                     const float* beta, int64_t beta_len, const float* state,
+                     int64_t state_slots, int64_t state_len, const void* out, int64_t out_len) {
+  if (int rc = check_act_dtype(act_dtype)) return rc;
+  if (int rc = check_recurrence_dims(tokens, Hk, Hv, Dk, Dv)) return rc;
+  if (state_slots <= 0) return fail(GDN_ERR_SHAPE, "gated_delta_rule state must have at least one slot");
+  const LenRule rules[] = {
+      {"query", q_len, tokens * Hk * Dk},
+      {"key", k_len, tokens * Hk * Dk},
+      {"value", v_len, tokens * Hv * Dv},
+      {"g", g_len, tokens * Hv},
+      {"beta", beta_len, tokens * Hv},
+      {"state", state_len, state_slots * Hv * Dv * Dk},
+      {"out", out_len, tokens * Hv * Dv},
+  };
+  if (int rc = check_lengths("gated_delta_rule", rules)) return rc;
+  for (auto pr : {std::make_pair(q, "q"), std::make_pair(k, "k"), std::make_pair(v, "v"),
+                  std::make_pair((const void*)g, "g"), std::make_pair((const void*)beta, "beta"),
+                  std::make_pair((const void*)state, "state"), std::make_pair(out, "out")})
+    if (int rc = require_ptr(pr.first, pr.second)) return rc;
+  for (auto pr : {std::make_pair(q, "q"), std::make_pair(k, "k"), std::make_pair(v, "v"),
+                  std::make_pair((const void*)state, "state"), std::make_pair(out, "out")})
+    if (int rc = require_aligned(pr.first, pr.second)) return rc;
+  if (!fits_i32(tokens) || !fits_i32(tokens * Hv * Dv) || !fits_i32(tokens * Hk * Dk))
+    return fail(GDN_ERR_UNSUPPORTED, "gated_delta_rule sizes exceed 32-bit token indexing");
+  return GDN_OK;
+}
+
+}  // namespace
+
+int gdn_decode(const gdn_decode_args* a, void* stream) {
+  if (a == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "args is NULL");
+  if (int rc = check_recurrence(a->B, a->Hk, a->Hv, a->Dk, a->Dv, a->act_dtype, a->q, a->q_len,
+                                a->k, a->k_len, a->v, a->v_len, a->g, a->g_len, a->beta,
+                                a->beta_len, a->state, a->state_slots, a->state_len, a->out,
+                                a->out_len))
+    return rc;
+  if (!gdn::recurrent_supported((int)a->Dk))
+    return fail(GDN_ERR_UNSUPPORTED, "gdn_decode supports Dk in {16, 32, 64, 128, 256}");
+  if (a->state_indices_host != nullptr)
+    if (int rc = check_indices_host(a->state_indices_host, a->B, a->state_slots)) return rc;
+  if (a->state_indices == nullptr && a->B > a->state_slots)
+    return fail(GDN_ERR_SHAPE, "gated_delta_rule state has fewer slots than rows");
+  gdn::RecurLaunch p{};
+  p.T = (int)a->B;
+  p.N = (int)a->B;
+  p.Hk = (int)a->Hk;
+  p.Hv = (int)a->Hv;
+  p.Dk = (int)a->Dk;
+  p.Dv = (int)a->Dv;
+  p.bf16 = a->act_dtype == GDN_DTYPE_BF16;
+  p.norm = a->use_qk_l2norm != 0;
+  p.scale = resolve_scale(a->scale, a->Dk);
+  p.q = a->q;
+  p.k = a->k;
+  p.v = a->v;
+  p.g = a->g;
+  p.beta = a->beta;
+  p.pool = a->state;
+  p.slots = a->state_slots;
+  p.cu = nullptr;
+  p.sidx = a->state_indices;
+  p.has_init = nullptr;
+  p.out = a->out;
+  p.status = gdn::status_word();
+  if (p.status == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
+  return launch_result(gdn::launch_decode(p, static_cast<cudaStream_t>(stream)), "gdn_decode");
+}
+
+int32_t gdn_prefill_resolve_algo(int64_t Dk, int64_t Dv, int32_t act_dtype, int32_t algo) {
+  if (algo != GDN_PREFILL_AUTO) return algo;
+  return gdn::chunked_supported((int)Dk, (int)Dv, act_dtype == GDN_DTYPE_BF16)
+             ? GDN_PREFILL_CHUNKED
+             : GDN_PREFILL_RECURRENT;
+}
+
+size_t gdn_prefill_workspace_bytes(int64_t T, int64_t N, int64_t Hv, int64_t Dk, int64_t Dv,
+                                   int32_t act_dtype, int32_t algo) {
+  if (gdn_prefill_resolve_algo(Dk, Dv, act_dtype, algo) != GDN_PREFILL_CHUNKED) return 0;
+  if (T <= 0 || N <= 0 || Hv <= 0) return 0;
+  return gdn::chunked_workspace_bytes(T, N, Hv, Dk, Dv);
+}
+
+int gdn_prefill_varlen(const gdn_prefill_args* a, void* stream) {
+  if (a == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "args is NULL");
+  if (int rc = check_recurrence(a->T, a->Hk, a->Hv, a->Dk, a->Dv, a->act_dtype, a->q, a->q_len,
+                                a->k, a->k_len, a->v, a->v_len, a->g, a->g_len, a->beta,
+                                a->beta_len, a->state, a->state_slots, a->state_len, a->out,
+                                a->out_len))
+    return rc;
+  if (a->N <= 0)
+    return fail(GDN_ERR_SHAPE, "gated_delta_rule_varlen shape must be positive, got batch=" +
+                                   S(a->N) + " total_tokens=" + S(a->T));
+  if (require_ptr(a->cu_seqlens, "cu_seqlens")) return GDN_ERR_INVALID_ARGUMENT;
+  if (a->algo < GDN_PREFILL_AUTO || a->algo > GDN_PREFILL_RECURRENT)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "unknown prefill algo " + S(a->algo));
+  if (a->cu_seqlens_host != nullptr)
+    if (int rc = check_cu_host(a->cu_seqlens_host, a->N, a->T, "gated_delta_rule_varlen"))
+      return rc;
+  if (a->state_indices_host != nullptr)
+    if (int rc = check_indices_host(a->state_indices_host, a->N, a->state_slots)) return rc;
+  if (a->state_indices == nullptr && a->N > a->state_slots)
+    return fail(GDN_ERR_SHAPE, "gated_delta_rule state has fewer slots than sequences");
+  const int32_t algo = gdn_prefill_resolve_algo(a->Dk, a->Dv, a->act_dtype, a->algo);
+  gdn::RecurLaunch p{};
+  p.T = (int)a->T;
+  p.N = (int)a->N;
+  p.Hk = (int)a->Hk;
+  p.Hv = (int)a->Hv;
+  p.Dk = (int)a->Dk;
+  p.Dv = (int)a->Dv;
+  p.bf16 = a->act_dtype == GDN_DTYPE_BF16;
+  p.norm = a->use_qk_l2norm != 0;
+  p.scale = resolve_scale(a->scale, a->Dk);
+  p.q = a->q;
+  p.k = a->k;
+  p.v = a->v;
+  p.g = a->g;
+  p.beta = a->beta;
+  p.pool = a->state;
+  p.slots = a->state_slots;
+  p.cu = a->cu_seqlens;
+  p.sidx = a->state_indices;
+  p.has_init = a->has_initial_state;
+  p.out = a->out;
+  p.status = gdn::status_word();
+  if (p.status == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (algo == GDN_PREFILL_CHUNKED) {
+    if (!gdn::chunked_supported((int)a->Dk, (int)a->Dv, p.bf16))
+      return fail(GDN_ERR_UNSUPPORTED,
+                  "the chunked prefill supports bf16 activations with Dk = Dv = 128");
+    const size_t need = gdn::chunked_workspace_bytes(a->T, a->N, a->Hv, a->Dk, a->Dv);
+    if (need > 0) {
+      if (a->workspace == nullptr || a->workspace_bytes < need)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_prefill_varlen workspace needs " +
+                                                  S((int64_t)need) + " bytes, got " +
+                                                  S((int64_t)a->workspace_bytes));
+      if ((reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
+    }
+    gdn::ChunkedLaunch c{p, a->workspace, a->workspace_bytes};
+    return launch_result(gdn::launch_chunked(c, st), "gdn_prefill_varlen(chunked)");
+  }
+  if (!gdn::recurrent_supported((int)a->Dk))
+    return fail(GDN_ERR_UNSUPPORTED, "the recurrent prefill supports Dk in {16, 32, 64, 128, 256}");
+  return launch_result(gdn::launch_recurrent(p, st), "gdn_prefill_varlen(recurrent)");
+}
+
+}  // extern "C"

@@ -1,0 +1,84 @@
+// gdn_internal.h -- launch descriptors shared by the host API (gdn_api.cpp)
+// and the kernel translation units.  Everything here is already validated:
+// the launchers only choose a configuration and launch.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+// Bits of the per-device status word (see gdn_status.cu).
+enum : unsigned {
+  kStatusBadIndex = 1u,     // state index outside [-1, slots)
+  kStatusBadSeqlens = 2u,   // cu_seqlens not 0..T, empty or decreasing range
+  kStatusTimeout = 4u,      // a bounded device wait gave up
+};
+
+// Counts one kernel launch (gdn_launch_count()).
+void note_launch();
+
+// Device address of the current device's status word (cached per device);
+// nullptr if the symbol could not be resolved.
+unsigned* status_word();
+
+struct PrepareLaunch {
+  int T, N, Hk, Hv, Dk, Dv, K;
+  bool bf16, norm;
+  const void* x;
+  int64_t x_stride;  // elements
+  const float* w;
+  const void* a;
+  int64_t a_stride;
+  const void* b;
+  int64_t b_stride;
+  const float* A_log;
+  const float* dt_bias;
+  const int32_t* cu;
+  const int32_t* sidx;      // may be null
+  const uint8_t* has_init;  // may be null
+  float* conv_pool;
+  int64_t slots;
+  void* q;
+  void* k;
+  void* v;
+  float* g;
+  float* beta;
+  unsigned* status;
+};
+cudaError_t launch_prepare(const PrepareLaunch& p, cudaStream_t s);
+
+// One token per row (decode) or token-sequential over sequences (recurrent
+// prefill) -- the same register-resident row update.
+struct RecurLaunch {
+  int T, N, Hk, Hv, Dk, Dv;
+  bool bf16, norm;
+  float scale;
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const float* beta;
+  float* pool;
+  int64_t slots;
+  const int32_t* cu;        // null for decode (row b = sequence b)
+  const int32_t* sidx;      // may be null
+  const uint8_t* has_init;  // may be null (prefill only)
+  void* out;
+  unsigned* status;
+};
+cudaError_t launch_decode(const RecurLaunch& p, cudaStream_t s);
+cudaError_t launch_recurrent(const RecurLaunch& p, cudaStream_t s);
+bool recurrent_supported(int Dk);
+
+// Chunked (C = 64) tensor-core prefill.
+struct ChunkedLaunch {
+  RecurLaunch r;
+  void* workspace;
+  size_t workspace_bytes;
+};
+bool chunked_supported(int Dk, int Dv, bool bf16);
+size_t chunked_workspace_bytes(int64_t T, int64_t N, int64_t Hv, int64_t Dk, int64_t Dv);
+cudaError_t launch_chunked(const ChunkedLaunch& p, cudaStream_t s);
+
+}  // namespace gdn

@@ -1,0 +1,309 @@
+// gdn_prepare.cu -- fused prepare kernel: causal depthwise conv1d + SiLU +
+// q/k/v split + q/k L2 norm + gates, with the conv tail carried in a slot pool.
+//
+// Defines: [cpu.rs] (ferrum-kernels 0.8.0, src/ferrum_kernels/backend/cpu.rs)
+// linear_attention_prepare_varlen_f32 and linear_attention_decode_prepare_
+// batch_f32; [cpu_ops.cpp] (vllm.cpp, src/vt/cpu/cpu_ops.cpp)
+// CausalConv1dFwdKernel, CausalConv1dUpdateKernel and GdnPostConvKernel.
+//
+// Work decomposition.  A thread owns one 16-byte vector of channels (8 bf16 or
+// 4 f32) and walks the tokens of a tile in order, keeping the last K-1 raw
+// inputs of its channels in registers (the conv window).  A warp therefore
+// reads 512 contiguous bytes of a token row per step; a CTA of 4 warps covers
+// 2 KB of the row.  grid.x = token tiles of `tile` tokens, grid.y = channel
+// blocks (+1 block row for the gates).  The L2 norm of a key head (Dk channels =
+// Dk/8 lanes) is a shuffle reduction inside the warp.
+//
+// Conv-tail ownership.  The old tail of a sequence is read by the outputs of
+// its first K-1 tokens, and the new tail replaces it in place.  Both are done
+// by the tile that holds the sequence's first token: it also computes the
+// first K-1 tokens of the sequence when they spill past its end, and the next
+// tile skips them.  So no tail is written while another CTA may still read it,
+// and no grid-wide synchronisation is needed (tile >= K-1).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+
+__device__ __forceinline__ float sigmoid_f(float x) {
+  if (x >= 0.0f) {
+    const float z = expf(-x);
+    return 1.0f / (1.0f + z);
+  }
+  const float z = expf(x);
+  return z / (1.0f + z);
+}
+
+__device__ __forceinline__ float softplus_f(float x) {
+  if (x > 20.0f) return x;
+  if (x < -20.0f) return expf(x);
+  return log1pf(expf(x));
+}
+
+template <typename TA>
+struct Act;
+
+template <>
+struct Act<float> {
+  static constexpr int kVec = 4;  // channels per 16-byte vector
+  __device__ static void load(const float* p, float (&o)[4]) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(p));
+    o[0] = v.x;
+    o[1] = v.y;
+    o[2] = v.z;
+    o[3] = v.w;
+  }
+  __device__ static void store(float* p, const float (&o)[4]) {
+    *reinterpret_cast<float4*>(p) = make_float4(o[0], o[1], o[2], o[3]);
+  }
+  __device__ static float scalar(const float* p) { return __ldg(p); }
+};
+
+template <>
+struct Act<__nv_bfloat16> {
+  static constexpr int kVec = 8;
+  __device__ static void load(const __nv_bfloat16* p, float (&o)[8]) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = __uint_as_float(w[i] << 16);
+      o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+  __device__ static void store(__nv_bfloat16* p, const float (&o)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  __device__ static float scalar(const __nv_bfloat16* p) { return __bfloat162float(p[0]); }
+};
+
+// Largest s in [0, n) with cu[s] <= t (cu assumed non-decreasing; callers
+// re-check the bracket, so a malformed cu only yields a bounded wrong guess).
+__device__ __forceinline__ int find_seq(const int32_t* __restrict__ cu, int n, int t) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(cu + mid) <= t)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+template <typename TA, int KW>
+__global__ void __launch_bounds__(kThreads) prepare_kernel(const PrepareLaunch p, int tile,
+                                                           int chan_blocks) {
+  constexpr int V = Act<TA>::kVec;
+  constexpr int W = KW - 1;  // conv tail length
+  const int qk_total = p.Hk * p.Dk;
+  const int C = 2 * qk_total + p.Hv * p.Dv;
+  const int t_begin = blockIdx.x * tile;
+  const int t_end = min(p.T, t_begin + tile);
+  const TA* __restrict__ x = static_cast<const TA*>(p.x);
+
+  if (blockIdx.y == chan_blocks) {  // gates: g, beta per (token, value head)
+    const TA* __restrict__ a = static_cast<const TA*>(p.a);
+    const TA* __restrict__ b = static_cast<const TA*>(p.b);
+    const int n = (t_end - t_begin) * p.Hv;
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      const int t = t_begin + i / p.Hv, h = i % p.Hv;
+      const float av = Act<TA>::scalar(a + (int64_t)t * p.a_stride + h);
+      const float bv = Act<TA>::scalar(b + (int64_t)t * p.b_stride + h);
+      p.g[(int64_t)t * p.Hv + h] = -expf(__ldg(p.A_log + h)) * softplus_f(av + __ldg(p.dt_bias + h));
+      p.beta[(int64_t)t * p.Hv + h] = sigmoid_f(bv);
+    }
+    return;
+  }
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c0 = ((blockIdx.y * kWarps + warp) * 32 + lane) * V;
+  const bool active = c0 < C;
+  const bool is_qk = c0 < 2 * qk_total;
+  const int group = p.Dk / V;  // lanes per key head (power of two <= 32)
+
+  float wt[V][KW];
+#pragma unroll
+  for (int i = 0; i < V; ++i)
+#pragma unroll
+    for (int j = 0; j < KW; ++j) wt[i][j] = active ? __ldg(p.w + (int64_t)(c0 + i) * KW + j) : 0.0f;
+
+  TA* __restrict__ out_ptr;  // row base of this thread's output vector
+  int64_t out_stride;
+  if (c0 < qk_total) {
+    out_ptr = static_cast<TA*>(p.q) + c0;
+    out_stride = qk_total;
+  } else if (c0 < 2 * qk_total) {
+    out_ptr = static_cast<TA*>(p.k) + (c0 - qk_total);
+    out_stride = qk_total;
+  } else {
+    out_ptr = static_cast<TA*>(p.v) + (c0 - 2 * qk_total);
+    out_stride = (int64_t)p.Hv * p.Dv;
+  }
+
+  float win[W > 0 ? W : 1][V];  // win[j] = input at token t - W + j
+#pragma unroll
+  for (int j = 0; j < W; ++j)
+#pragma unroll
+    for (int i = 0; i < V; ++i) win[j][i] = 0.0f;
+
+  // Sequence bracket of the tile's first token.
+  int s = find_seq(p.cu, p.N, t_begin);
+  int seq_lo = __ldg(p.cu + s), seq_hi = __ldg(p.cu + s + 1);
+  if (__ldg(p.cu) != 0 || __ldg(p.cu + p.N) != p.T || !(seq_lo <= t_begin && t_begin < seq_hi) ||
+      seq_lo < 0 || seq_hi > p.T) {
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusBadSeqlens);
+    return;
+  }
+
+  // Starts sequence s at its first token: loads the old tail into the window
+  // and writes the new tail (last W raw inputs of tail || x) to the slot.
+  auto begin_sequence = [&]() {
+    int slot = p.sidx != nullptr ? __ldg(p.sidx + s) : s;
+    if (slot < -1 || slot >= p.slots) {
+      if (threadIdx.x == 0) atomicOr(p.status, kStatusBadIndex);
+      slot = -1;
+    }
+    const bool live = slot >= 0;
+    const bool init = live && (p.has_init == nullptr || __ldg(p.has_init + s) != 0);
+    float* tail = live ? p.conv_pool + ((int64_t)slot * C + c0) * W : nullptr;
+#pragma unroll
+    for (int j = 0; j < W; ++j)
+#pragma unroll
+      for (int i = 0; i < V; ++i) win[j][i] = (init && active) ? tail[i * W + j] : 0.0f;
+    if (live && active) {
+      const int len = seq_hi - seq_lo;
+#pragma unroll
+      for (int pos = 0; pos < W; ++pos) {
+        const int src = len + pos - W;  // token index inside the sequence
+        float nv[V];
+        if (src >= 0) {
+          Act<TA>::load(x + (int64_t)(seq_lo + src) * p.x_stride + c0, nv);
+        } else {
+#pragma unroll
+          for (int i = 0; i < V; ++i) {
+            float o = 0.0f;
+#pragma unroll
+            for (int j = 0; j < W; ++j) o = (j == W + src) ? win[j][i] : o;
+            nv[i] = o;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < V; ++i) tail[i * W + pos] = nv[i];
+      }
+    }
+  };
+
+  int t = t_begin;
+  if (t > seq_lo && t < seq_lo + W) t = min(seq_lo + W, seq_hi);  // owned by the previous tile
+  if (t == seq_lo) {
+    begin_sequence();
+  } else if (t < seq_hi) {  // mid-sequence: the window comes from earlier raw inputs
+#pragma unroll
+    for (int j = 0; j < W; ++j)
+      if (active) Act<TA>::load(x + (int64_t)(t - W + j) * p.x_stride + c0, win[j]);
+  }
+
+  for (;;) {
+    if (t == seq_hi) {  // sequence s is finished
+      if (t >= t_end || s + 1 >= p.N) break;
+      ++s;
+      seq_lo = seq_hi;
+      seq_hi = __ldg(p.cu + s + 1);
+      if (seq_hi <= seq_lo || seq_hi > p.T) {
+        if (threadIdx.x == 0) atomicOr(p.status, kStatusBadSeqlens);
+        break;
+      }
+      begin_sequence();
+    }
+    if (t >= t_end && t >= seq_lo + W) break;
+
+    float xt[V];
+    if (active) {
+      Act<TA>::load(x + (int64_t)t * p.x_stride + c0, xt);
+    } else {
+#pragma unroll
+      for (int i = 0; i < V; ++i) xt[i] = 0.0f;
+    }
+    float y[V];
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      float acc = 0.0f;
+#pragma unroll
+      for (int j = 0; j < W; ++j) acc = fmaf(win[j][i], wt[i][j], acc);
+      acc = fmaf(xt[i], wt[i][W], acc);
+      y[i] = acc * sigmoid_f(acc);  // silu
+      ss = fmaf(y[i], y[i], ss);
+    }
+    if (p.norm) {  // uniform across the warp: every lane joins the shuffles
+      for (int m = 1; m < group; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+      if (is_qk) {
+        const float inv = 1.0f / sqrtf(ss + 1e-6f);
+#pragma unroll
+        for (int i = 0; i < V; ++i) y[i] *= inv;
+      }
+    }
+    if (active) Act<TA>::store(out_ptr + (int64_t)t * out_stride, y);
+#pragma unroll
+    for (int j = 0; j + 1 < W; ++j)
+#pragma unroll
+      for (int i = 0; i < V; ++i) win[j][i] = win[j + 1][i];
+    if (W > 0)
+#pragma unroll
+      for (int i = 0; i < V; ++i) win[W - 1][i] = xt[i];
+    ++t;
+  }
+}
+
+template <typename TA, int KW>
+cudaError_t launch_k(const PrepareLaunch& p, cudaStream_t s) {
+  constexpr int V = Act<TA>::kVec;
+  const int C = 2 * p.Hk * p.Dk + p.Hv * p.Dv;
+  const int chan_blocks = (C + kThreads * V - 1) / (kThreads * V);
+  // Tiles of at least K-1 tokens (tail ownership); shrink them while the grid
+  // is short of ~8 CTAs per SM.
+  int tile = 16;
+  while (tile > 4 && (int64_t)((p.T + tile - 1) / tile) * chan_blocks < 8 * 152) tile >>= 1;
+  if (tile < KW - 1) tile = KW - 1;
+  dim3 grid((p.T + tile - 1) / tile, chan_blocks + 1);
+  if (grid.y > 65535) return cudaErrorInvalidConfiguration;
+  prepare_kernel<TA, KW><<<grid, kThreads, 0, s>>>(p, tile, chan_blocks);
+  note_launch();
+  return cudaGetLastError();
+}
+
+template <typename TA>
+cudaError_t launch_dtype(const PrepareLaunch& p, cudaStream_t s) {
+  switch (p.K) {
+    case 1: return launch_k<TA, 1>(p, s);
+    case 2: return launch_k<TA, 2>(p, s);
+    case 3: return launch_k<TA, 3>(p, s);
+    case 4: return launch_k<TA, 4>(p, s);
+    case 5: return launch_k<TA, 5>(p, s);
+    case 6: return launch_k<TA, 6>(p, s);
+    case 7: return launch_k<TA, 7>(p, s);
+    case 8: return launch_k<TA, 8>(p, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prepare(const PrepareLaunch& p, cudaStream_t s) {
+  return p.bf16 ? launch_dtype<__nv_bfloat16>(p, s) : launch_dtype<float>(p, s);
+}
+
+}  // namespace gdn

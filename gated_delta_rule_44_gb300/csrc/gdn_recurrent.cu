@@ -1,0 +1,352 @@
+// gdn_recurrent.cu -- the gated delta rule one token at a time, on CUDA cores.
+//
+// Defines: [cpu_ops.cpp] (vllm.cpp, src/vt/cpu/cpu_ops.cpp) GdnHeadTokenStep,
+// GdnDecodeKernel and GdnPrefillKernel; [cpu.rs] (ferrum-kernels 0.8.0,
+// src/ferrum_kernels/backend/cpu.rs) recurrent_gated_delta_rule_batch_f32 and
+// recurrent_gated_delta_rule_varlen_f32.
+//
+// Per value head h and token, with S = [Dv, Dk] f32:
+//   S *= exp(g);  u = beta (v - S k);  S += u k^T;  o = S (scale q)
+// Row i of S evolves on its own given k, q, v_i: with a = S_i.k and b = S_i.q
+// taken on the OLD row,
+//   u_i = beta (v_i - e^g a),  S_i <- e^g S_i + u_i k,  o_i = scale (e^g b + u_i (k.q))
+// which is the same update, so each row is read once and written once.
+//
+// Thread layout.  A row of Dk floats is split over LPR = Dk/16 lanes, each
+// holding 16 floats as 4 float4 at columns 4*lr + 4*LPR*m (m = 0..3): one
+// load instruction of a warp covers 32/LPR rows x 128 contiguous bytes.  The
+// two dots are xor-shuffle reductions over the LPR lanes of a row.  A CTA of
+// 128 threads holds PASSES x (128/LPR) rows of one (sequence, head).
+//
+// gdn_decode: one CTA per (row b, head, row slice); the state slice streams
+// HBM -> registers -> HBM once (evict-first loads and stores).
+// recurrent prefill: one CTA per (sequence, head, row slice) keeps its slice in
+// registers across the sequence's tokens, prefetching the next token's q/k/v.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 128;
+
+template <typename TA>
+__device__ __forceinline__ float ld_act(const TA* p);
+template <>
+__device__ __forceinline__ float ld_act<float>(const float* p) {
+  return __ldg(p);
+}
+template <>
+__device__ __forceinline__ float ld_act<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat162float(__ldg(p));
+}
+template <typename TA>
+__device__ __forceinline__ void st_act(TA* p, float v);
+template <>
+__device__ __forceinline__ void st_act<float>(float* p, float v) {
+  *p = v;
+}
+template <>
+__device__ __forceinline__ void st_act<__nv_bfloat16>(__nv_bfloat16* p, float v) {
+  *p = __float2bfloat16_rn(v);
+}
+
+// 4 consecutive activations starting at p (16-byte aligned for f32, 8 for bf16).
+template <typename TA>
+__device__ __forceinline__ float4 ld_act4(const TA* p);
+template <>
+__device__ __forceinline__ float4 ld_act4<float>(const float* p) {
+  return __ldg(reinterpret_cast<const float4*>(p));
+}
+template <>
+__device__ __forceinline__ float4 ld_act4<__nv_bfloat16>(const __nv_bfloat16* p) {
+  const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+  return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                     __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+}
+
+template <int LPR>
+__device__ __forceinline__ float row_sum(float v) {
+#pragma unroll
+  for (int m = 1; m < LPR; m <<= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+  return v;
+}
+
+__device__ __forceinline__ float dot4(const float4& a, const float4& b) {
+  return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+}
+
+// q and k columns of one lane (16 each), optionally L2-normalised, plus k.q.
+template <typename TA, int DK>
+struct QK {
+  static constexpr int LPR = DK / 16;
+  float4 k[4], q[4];
+  float kq;
+  __device__ __forceinline__ void load(const TA* kp, const TA* qp, int lr) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      k[m] = ld_act4<TA>(kp + 4 * lr + 4 * LPR * m);
+      q[m] = ld_act4<TA>(qp + 4 * lr + 4 * LPR * m);
+    }
+  }
+  __device__ __forceinline__ void finish(bool norm) {
+    if (norm) {
+      float kk = 0.f, qq = 0.f;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        kk += dot4(k[m], k[m]);
+        qq += dot4(q[m], q[m]);
+      }
+      kk = row_sum<LPR>(kk);
+      qq = row_sum<LPR>(qq);
+      const float ki = 1.0f / sqrtf(kk + 1e-6f), qi = 1.0f / sqrtf(qq + 1e-6f);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        k[m].x *= ki; k[m].y *= ki; k[m].z *= ki; k[m].w *= ki;
+        q[m].x *= qi; q[m].y *= qi; q[m].z *= qi; q[m].w *= qi;
+      }
+    }
+    float d = 0.f;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) d += dot4(k[m], q[m]);
+    kq = row_sum<LPR>(d);
+  }
+};
+
+// The row update for one token.  Returns o_i (before scale) for this row.
+template <int LPR>
+__device__ __forceinline__ float row_step(float4 (&s)[4], const float4 (&k)[4],
+                                          const float4 (&q)[4], float kq, float decay,
+                                          float beta, float v) {
+  float a = 0.f, b = 0.f;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    a += dot4(s[m], k[m]);
+    b += dot4(s[m], q[m]);
+  }
+  a = row_sum<LPR>(a);
+  b = row_sum<LPR>(b);
+  const float u = beta * (v - decay * a);
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    s[m].x = fmaf(decay, s[m].x, u * k[m].x);
+    s[m].y = fmaf(decay, s[m].y, u * k[m].y);
+    s[m].z = fmaf(decay, s[m].z, u * k[m].z);
+    s[m].w = fmaf(decay, s[m].w, u * k[m].w);
+  }
+  return fmaf(decay, b, u * kq);
+}
+
+// ---------------------------------------------------------------------------
+// Decode: grid.x = B * Hv * slices.
+template <typename TA, int DK, int PASSES>
+__global__ void __launch_bounds__(kThreads) decode_kernel(const RecurLaunch p, int slices) {
+  constexpr int LPR = DK / 16;
+  constexpr int RPP = kThreads / LPR;  // rows per pass
+  const int tid = threadIdx.x;
+  const int lr = tid % LPR, rg = tid / LPR;
+  const int slice = blockIdx.x % slices;
+  const int bh = blockIdx.x / slices;
+  const int h = bh % p.Hv, b = bh / p.Hv;
+  const int row0 = slice * (RPP * PASSES) + rg;
+  TA* out = static_cast<TA*>(p.out) + ((int64_t)b * p.Hv + h) * p.Dv;
+
+  int slot = p.sidx != nullptr ? __ldg(p.sidx + b) : b;
+  if (slot < -1 || slot >= p.slots) {
+    if (tid == 0) atomicOr(p.status, kStatusBadIndex);
+    slot = -1;
+  }
+  if (slot < 0) {  // padding row: zero output, state untouched
+#pragma unroll
+    for (int ps = 0; ps < PASSES; ++ps) {
+      const int r = row0 + ps * RPP;
+      if (lr == 0 && r < p.Dv) st_act<TA>(out + r, 0.0f);
+    }
+    return;
+  }
+  const int hk = h / (p.Hv / p.Hk);
+  float* S = p.pool + ((int64_t)slot * p.Hv + h) * p.Dv * DK;
+
+  // Issue every state load of the slice first (memory-level parallelism).
+  float4 st[PASSES][4];
+#pragma unroll
+  for (int ps = 0; ps < PASSES; ++ps) {
+    const int r = row0 + ps * RPP;
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+      st[ps][m] = r < p.Dv ? __ldcs(reinterpret_cast<const float4*>(S + (int64_t)r * DK + 4 * lr +
+                                                                      4 * LPR * m))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  QK<TA, DK> qk;
+  const TA* kp = static_cast<const TA*>(p.k) + ((int64_t)b * p.Hk + hk) * DK;
+  const TA* qp = static_cast<const TA*>(p.q) + ((int64_t)b * p.Hk + hk) * DK;
+  qk.load(kp, qp, lr);
+  qk.finish(p.norm);
+  const float decay = expf(__ldg(p.g + (int64_t)b * p.Hv + h));
+  const float beta = __ldg(p.beta + (int64_t)b * p.Hv + h);
+  const TA* vp = static_cast<const TA*>(p.v) + ((int64_t)b * p.Hv + h) * p.Dv;
+
+#pragma unroll
+  for (int ps = 0; ps < PASSES; ++ps) {
+    const int r = row0 + ps * RPP;
+    const float vv = r < p.Dv ? ld_act<TA>(vp + r) : 0.0f;
+    const float o = row_step<LPR>(st[ps], qk.k, qk.q, qk.kq, decay, beta, vv);
+    if (r < p.Dv) {
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        __stcs(reinterpret_cast<float4*>(S + (int64_t)r * DK + 4 * lr + 4 * LPR * m), st[ps][m]);
+      if (lr == 0) st_act<TA>(out + r, o * p.scale);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Recurrent prefill: grid.x = N * Hv * slices; tokens of the sequence in order.
+template <typename TA, int DK, int PASSES>
+__global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurLaunch p, int slices) {
+  constexpr int LPR = DK / 16;
+  constexpr int RPP = kThreads / LPR;
+  const int tid = threadIdx.x;
+  const int lr = tid % LPR, rg = tid / LPR;
+  const int slice = blockIdx.x % slices;
+  const int sh = blockIdx.x / slices;
+  const int h = sh % p.Hv, s = sh / p.Hv;
+  const int row0 = slice * (RPP * PASSES) + rg;
+
+  const int t0 = __ldg(p.cu + s), t1 = __ldg(p.cu + s + 1);
+  if (__ldg(p.cu) != 0 || __ldg(p.cu + p.N) != p.T || t0 < 0 || t1 <= t0 || t1 > p.T) {
+    if (tid == 0) atomicOr(p.status, kStatusBadSeqlens);
+    return;
+  }
+  int slot = p.sidx != nullptr ? __ldg(p.sidx + s) : s;
+  if (slot < -1 || slot >= p.slots) {
+    if (tid == 0) atomicOr(p.status, kStatusBadIndex);
+    slot = -1;
+  }
+  if (slot < 0) {  // padded sequence: zero outputs, pool untouched
+    for (int t = t0; t < t1; ++t) {
+      TA* out = static_cast<TA*>(p.out) + ((int64_t)t * p.Hv + h) * p.Dv;
+#pragma unroll
+      for (int ps = 0; ps < PASSES; ++ps) {
+        const int r = row0 + ps * RPP;
+        if (lr == 0 && r < p.Dv) st_act<TA>(out + r, 0.0f);
+      }
+    }
+    return;
+  }
+  const int hk = h / (p.Hv / p.Hk);
+  float* S = p.pool + ((int64_t)slot * p.Hv + h) * p.Dv * DK;
+  const bool init = p.has_init == nullptr || __ldg(p.has_init + s) != 0;
+
+  float4 st[PASSES][4];
+#pragma unroll
+  for (int ps = 0; ps < PASSES; ++ps) {
+    const int r = row0 + ps * RPP;
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+      st[ps][m] = (init && r < p.Dv)
+                      ? *reinterpret_cast<const float4*>(S + (int64_t)r * DK + 4 * lr + 4 * LPR * m)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+
+  const TA* kbase = static_cast<const TA*>(p.k) + (int64_t)hk * DK;
+  const TA* qbase = static_cast<const TA*>(p.q) + (int64_t)hk * DK;
+  const TA* vbase = static_cast<const TA*>(p.v) + (int64_t)h * p.Dv;
+  const int64_t qk_row = (int64_t)p.Hk * DK, v_row = (int64_t)p.Hv * p.Dv;
+
+  // Software pipeline: operands of token t+1 load while token t computes.
+  QK<TA, DK> cur, nxt;
+  float v_cur[PASSES], v_nxt[PASSES];
+  float g_cur, b_cur, g_nxt = 0.f, b_nxt = 0.f;
+  cur.load(kbase + (int64_t)t0 * qk_row, qbase + (int64_t)t0 * qk_row, lr);
+#pragma unroll
+  for (int ps = 0; ps < PASSES; ++ps) {
+    const int r = row0 + ps * RPP;
+    v_cur[ps] = r < p.Dv ? ld_act<TA>(vbase + (int64_t)t0 * v_row + r) : 0.f;
+  }
+  g_cur = __ldg(p.g + (int64_t)t0 * p.Hv + h);
+  b_cur = __ldg(p.beta + (int64_t)t0 * p.Hv + h);
+
+  for (int t = t0; t < t1; ++t) {
+    if (t + 1 < t1) {
+      nxt.load(kbase + (int64_t)(t + 1) * qk_row, qbase + (int64_t)(t + 1) * qk_row, lr);
+#pragma unroll
+      for (int ps = 0; ps < PASSES; ++ps) {
+        const int r = row0 + ps * RPP;
+        v_nxt[ps] = r < p.Dv ? ld_act<TA>(vbase + (int64_t)(t + 1) * v_row + r) : 0.f;
+      }
+      g_nxt = __ldg(p.g + (int64_t)(t + 1) * p.Hv + h);
+      b_nxt = __ldg(p.beta + (int64_t)(t + 1) * p.Hv + h);
+    }
+    cur.finish(p.norm);
+    const float decay = expf(g_cur);
+    TA* out = static_cast<TA*>(p.out) + ((int64_t)t * p.Hv + h) * p.Dv;
+#pragma unroll
+    for (int ps = 0; ps < PASSES; ++ps) {
+      const int r = row0 + ps * RPP;
+      const float o = row_step<LPR>(st[ps], cur.k, cur.q, cur.kq, decay, b_cur, v_cur[ps]);
+      if (lr == 0 && r < p.Dv) st_act<TA>(out + r, o * p.scale);
+    }
+    cur = nxt;
+#pragma unroll
+    for (int ps = 0; ps < PASSES; ++ps) v_cur[ps] = v_nxt[ps];
+    g_cur = g_nxt;
+    b_cur = b_nxt;
+  }
+
+#pragma unroll
+  for (int ps = 0; ps < PASSES; ++ps) {
+    const int r = row0 + ps * RPP;
+    if (r < p.Dv)
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        *reinterpret_cast<float4*>(S + (int64_t)r * DK + 4 * lr + 4 * LPR * m) = st[ps][m];
+  }
+}
+
+template <typename TA, int DK, int PASSES>
+cudaError_t launch_dk(const RecurLaunch& p, cudaStream_t s, bool decode) {
+  constexpr int rows_per_cta = (kThreads / (DK / 16)) * PASSES;
+  const int slices = (p.Dv + rows_per_cta - 1) / rows_per_cta;
+  const int64_t blocks = (int64_t)(decode ? p.T : p.N) * p.Hv * slices;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  if (decode)
+    decode_kernel<TA, DK, PASSES><<<(unsigned)blocks, kThreads, 0, s>>>(p, slices);
+  else
+    recurrent_kernel<TA, DK, PASSES><<<(unsigned)blocks, kThreads, 0, s>>>(p, slices);
+  note_launch();
+  return cudaGetLastError();
+}
+
+// PASSES chosen so a CTA holds 64 rows (32 floats of state per thread at
+// Dk = 128); decode issues all of them before the first use.
+template <typename TA>
+cudaError_t launch_any(const RecurLaunch& p, cudaStream_t s, bool decode) {
+  switch (p.Dk) {
+    case 16: return launch_dk<TA, 16, 1>(p, s, decode);
+    case 32: return launch_dk<TA, 32, 1>(p, s, decode);
+    case 64: return launch_dk<TA, 64, 2>(p, s, decode);
+    case 128: return launch_dk<TA, 128, 4>(p, s, decode);
+    case 256: return launch_dk<TA, 256, 4>(p, s, decode);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+bool recurrent_supported(int Dk) {
+  return Dk == 16 || Dk == 32 || Dk == 64 || Dk == 128 || Dk == 256;
+}
+
+cudaError_t launch_decode(const RecurLaunch& p, cudaStream_t s) {
+  return p.bf16 ? launch_any<__nv_bfloat16>(p, s, true) : launch_any<float>(p, s, true);
+}
+
+cudaError_t launch_recurrent(const RecurLaunch& p, cudaStream_t s) {
+  return p.bf16 ? launch_any<__nv_bfloat16>(p, s, false) : launch_any<float>(p, s, false);
+}
+
+}  // namespace gdn

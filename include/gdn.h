@@ -1,0 +1,262 @@
+/*
+ * gdn.h -- C ABI of libgdn, the gated-delta-rule (GDN) linear-attention layer
+ * on GB300 (sm_103a).
+ *
+ * The layer has two parts, each on a caller-owned CUDA stream:
+ *   gdn_prepare         causal depthwise conv1d + SiLU + q/k/v split + q/k L2
+ *                       norm + gates g, beta, with the conv tail carried in a
+ *                       slot pool
+ *   gdn_decode          the state recurrence for one token per sequence
+ *   gdn_prefill_varlen  the state recurrence over packed variable-length
+ *                       sequences (chunked, tensor-core form)
+ *
+ * Sources (page title, then the function that defines the operation):
+ *   [cpu.rs]       ferrum-kernels 0.8.0, src/ferrum_kernels/backend/cpu.rs
+ *   [cpu_ops.cpp]  vllm.cpp, src/vt/cpu/cpu_ops.cpp
+ *   [qwen3_5.cpp]  vllm.cpp, src/vllm/model_executor/models/qwen3_5.cpp
+ *
+ * General rules for every call
+ *   - Every pointer is a DEVICE pointer unless its name ends in _host.  The
+ *     caller owns every buffer; the library allocates nothing on any call.
+ *   - Lengths (*_len) are element counts of the buffers as allocated; a call
+ *     fails with GDN_ERR_SHAPE when a buffer is shorter than the shape needs,
+ *     with the same message text as [cpu.rs] validate_* ("... {label} length
+ *     {actual} < expected {expected}").
+ *   - Host-side validation is synchronous; on any error nothing is launched
+ *     and no buffer is touched.  Work is asynchronous on `stream` (a
+ *     cudaStream_t passed as void*; NULL = the legacy default stream).
+ *   - No C++ exception crosses this boundary.  gdn_last_error_message()
+ *     returns the calling thread's last diagnostic.
+ *   - Errors that only the device can see (a state index outside the pool or a
+ *     malformed cu_seqlens when no host mirror was passed) are recorded in a
+ *     per-device status word and the offending sequence is skipped;
+ *     gdn_read_device_status() returns and clears it.
+ *   - Layouts (row-major, innermost last):
+ *       mixed_qkv [T, >=C_conv], C_conv = 2*Hk*Dk + Hv*Dv, row stride in elements
+ *       q, k      [T, Hk, Dk]          v, out [T, Hv, Dv]
+ *       g, beta   [T, Hv] f32          a_raw, b_raw [T, >=Hv] (row stride)
+ *       state     [slots, Hv, Dv, Dk] f32, the SSM state of one sequence per slot
+ *       conv_state[slots, C_conv, K-1] f32, the last K-1 raw inputs, oldest first
+ *     Value head h reads key head h / (Hv/Hk)  ([cpu_ops.cpp] GdnTokenStep).
+ *   - Alignment: every activation pointer and row stride must give 16-byte
+ *     aligned rows (GDN_ERR_INVALID_ARGUMENT otherwise).
+ *   - Index rules ([cpu_ops.cpp] GdnDecodeKernel, CausalConv1dUpdateKernel;
+ *     [qwen3_5.cpp] ValidateGdnStateIndices):
+ *       state_indices == NULL      sequence i uses slot i
+ *       state_indices[i] == -1     padding: its outputs are zero (recurrence)
+ *                                  and its pool rows are neither read nor written
+ *       any other negative, a slot >= slots, or a duplicate live slot is an
+ *       error; duplicates are only detected when the _host mirror is passed.
+ *       has_initial_state[i] == 0  start from a zero state / zero conv tail; the
+ *                                  final state is still written to the slot.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdn_status {
+  GDN_OK = 0,
+  GDN_ERR_SHAPE = 1,            /* non-positive dims, Hv % Hk != 0, short buffer */
+  GDN_ERR_INVALID_ARGUMENT = 2, /* bad cu_seqlens, bad index, NULL or misaligned pointer */
+  GDN_ERR_DTYPE = 3,            /* act_dtype not a gdn_dtype */
+  GDN_ERR_UNSUPPORTED = 4,      /* valid, but outside the dims the kernels are built for */
+  GDN_ERR_CUDA = 5,             /* a CUDA runtime call failed */
+  GDN_ERR_TIMEOUT = 6,          /* a bounded device-side wait ran out */
+  GDN_ERR_DEVICE_CHECK = 7      /* a kernel saw a bad index or cu_seqlens */
+} gdn_status;
+
+typedef enum gdn_dtype {
+  GDN_DTYPE_F32 = 0,
+  GDN_DTYPE_BF16 = 1
+} gdn_dtype;
+
+/* Which recurrence kernel gdn_prefill_varlen runs. */
+typedef enum gdn_prefill_algo {
+  GDN_PREFILL_AUTO = 0,      /* chunked when supported (bf16, Dk = Dv = 128), else recurrent */
+  GDN_PREFILL_CHUNKED = 1,   /* chunk-64 WY/UT form on tcgen05 tensor cores */
+  GDN_PREFILL_RECURRENT = 2  /* token-sequential recurrence on CUDA cores */
+} gdn_prefill_algo;
+
+/* ---------------------------------------------------------------------------
+ * gdn_prepare -- [cpu.rs] linear_attention_prepare_varlen_f32 and
+ * linear_attention_decode_prepare_batch_f32; [cpu_ops.cpp]
+ * CausalConv1dFwdKernel, CausalConv1dUpdateKernel, GdnPostConvKernel.
+ *
+ * For each sequence s (tokens cu_seqlens[s] .. cu_seqlens[s+1]-1) and channel c:
+ *   y[t,c] = silu( sum_{j<K} conv_weight[c,j] * x~[t - (K-1) + j] )
+ * where x~ is the sequence's raw input preceded by its conv tail (zero when
+ * has_initial_state[s] == 0).  q = y[:, 0:HkDk], k = y[:, HkDk:2HkDk],
+ * v = y[:, 2HkDk:]; when apply_qk_l2norm, q and k are scaled per (token, key
+ * head) by 1/sqrt(sum of squares + 1e-6).  Gates per (token, value head):
+ *   g = -exp(A_log[h]) * softplus(a_raw + dt_bias[h]),  beta = sigmoid(b_raw)
+ * with softplus(x) = x for x > 20.  The conv tail row of the sequence's slot is
+ * replaced by the last K-1 raw inputs of tail || x.  A decode batch is N == T
+ * with cu_seqlens = 0,1,...,T.  q,k,v are stored in act_dtype (bf16 rounds to
+ * nearest even); g, beta in f32.
+ * Supported: K in [2, 8]; Dk a power of two in [8, 256] (bf16) or [4, 128]
+ * (f32); Dv a multiple of 8 (bf16) or 4 (f32).
+ * ------------------------------------------------------------------------- */
+typedef struct gdn_prepare_args {
+  int64_t T, N;             /* tokens, sequences */
+  int64_t Hk, Hv, Dk, Dv;   /* key heads, value heads, key dim, value dim */
+  int64_t K;                /* conv width (conv_kernel) */
+  int32_t act_dtype;        /* gdn_dtype of mixed_qkv, a_raw, b_raw, q, k, v */
+  int32_t apply_qk_l2norm;  /* 1: L2-normalise q and k rows */
+  const void* mixed_qkv;    /* [T, mixed_qkv_stride] */
+  int64_t mixed_qkv_stride; /* elements per row, >= C_conv; 0 = C_conv */
+  int64_t mixed_qkv_len;
+  const float* conv_weight; /* [C_conv, K] */
+  int64_t conv_weight_len;
+  const void* a_raw;        /* [T, a_raw_stride] */
+  int64_t a_raw_stride;     /* 0 = Hv */
+  int64_t a_raw_len;
+  const void* b_raw;        /* [T, b_raw_stride] */
+  int64_t b_raw_stride;     /* 0 = Hv */
+  int64_t b_raw_len;
+  const float* A_log;       /* [Hv] */
+  int64_t A_log_len;
+  const float* dt_bias;     /* [Hv] */
+  int64_t dt_bias_len;
+  const int32_t* cu_seqlens;        /* [N+1] */
+  const int32_t* state_indices;     /* [N] conv pool slot per sequence, or NULL */
+  const uint8_t* has_initial_state; /* [N] or NULL (= all 1) */
+  const int32_t* cu_seqlens_host;   /* optional host copy: full validation */
+  const int32_t* state_indices_host;/* optional host copy: full validation */
+  float* conv_state;        /* [conv_state_slots, C_conv, K-1], updated in place */
+  int64_t conv_state_slots;
+  int64_t conv_state_len;
+  void* q;                  /* [T, Hk, Dk] */
+  int64_t q_len;
+  void* k;                  /* [T, Hk, Dk] */
+  int64_t k_len;
+  void* v;                  /* [T, Hv, Dv] */
+  int64_t v_len;
+  float* g;                 /* [T, Hv] */
+  int64_t g_len;
+  float* beta;              /* [T, Hv] */
+  int64_t beta_len;
+} gdn_prepare_args;
+
+int gdn_prepare(const gdn_prepare_args* args, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * gdn_decode -- [cpu_ops.cpp] GdnDecodeKernel / GdnHeadTokenStep;
+ * [cpu.rs] recurrent_gated_delta_rule_batch_f32.
+ *
+ * Row b is one token of one sequence whose state S = state[state_indices[b],
+ * h] ([Dv, Dk]) is updated in place, per value head h:
+ *   S *= exp(g);  u = beta * (v - S k);  S += u k^T;  out = S (scale * q)
+ * k is not scaled.  scale < 0 selects 1/sqrt(Dk).  When use_qk_l2norm, q and
+ * k are first L2-normalised in f32 (eps 1e-6 inside the sqrt).
+ * Supported: Dk in {16, 32, 64, 128, 256}; any Dv >= 1.
+ * ------------------------------------------------------------------------- */
+typedef struct gdn_decode_args {
+  int64_t B;                /* rows (sequences), one token each */
+  int64_t Hk, Hv, Dk, Dv;
+  int32_t act_dtype;        /* gdn_dtype of q, k, v, out */
+  int32_t use_qk_l2norm;
+  float scale;              /* < 0: 1/sqrt(Dk) */
+  const void* q;            /* [B, Hk, Dk] */
+  int64_t q_len;
+  const void* k;            /* [B, Hk, Dk] */
+  int64_t k_len;
+  const void* v;            /* [B, Hv, Dv] */
+  int64_t v_len;
+  const float* g;           /* [B, Hv] */
+  int64_t g_len;
+  const float* beta;        /* [B, Hv] */
+  int64_t beta_len;
+  float* state;             /* [state_slots, Hv, Dv, Dk], updated in place */
+  int64_t state_slots;
+  int64_t state_len;
+  const int32_t* state_indices;      /* [B] or NULL (slot = b) */
+  const int32_t* state_indices_host; /* optional host copy: full validation */
+  void* out;                /* [B, Hv, Dv] */
+  int64_t out_len;
+} gdn_decode_args;
+
+int gdn_decode(const gdn_decode_args* args, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * gdn_prefill_varlen -- [cpu.rs] recurrent_gated_delta_rule_varlen_f32;
+ * [cpu_ops.cpp] GdnPrefillKernel.
+ *
+ * The recurrence of gdn_decode over every token of every sequence in order,
+ * starting from the sequence's slot (or zero when has_initial_state[s] == 0),
+ * writing out[t] for every token and the final state back to the slot.
+ * cu_seqlens must start at 0, end at T, and every range must be non-empty
+ * ([cpu.rs] recurrent_gated_delta_rule_varlen_f32).
+ * The chunked algorithm splits each sequence into chunks of 64 tokens (the
+ * last may be partial; chunks never cross sequences) and needs
+ * gdn_prefill_workspace_bytes() bytes of 256-byte aligned device scratch in
+ * `workspace`; the recurrent algorithm needs none.
+ * ------------------------------------------------------------------------- */
+typedef struct gdn_prefill_args {
+  int64_t T, N;
+  int64_t Hk, Hv, Dk, Dv;
+  int32_t act_dtype;        /* gdn_dtype of q, k, v, out */
+  int32_t use_qk_l2norm;
+  float scale;              /* < 0: 1/sqrt(Dk) */
+  int32_t algo;             /* gdn_prefill_algo */
+  const void* q;            /* [T, Hk, Dk] */
+  int64_t q_len;
+  const void* k;
+  int64_t k_len;
+  const void* v;            /* [T, Hv, Dv] */
+  int64_t v_len;
+  const float* g;           /* [T, Hv] */
+  int64_t g_len;
+  const float* beta;
+  int64_t beta_len;
+  float* state;             /* [state_slots, Hv, Dv, Dk], updated in place */
+  int64_t state_slots;
+  int64_t state_len;
+  const int32_t* cu_seqlens;        /* [N+1] */
+  const int32_t* state_indices;     /* [N] or NULL */
+  const uint8_t* has_initial_state; /* [N] or NULL (= all 1) */
+  const int32_t* cu_seqlens_host;   /* optional host copies: full validation */
+  const int32_t* state_indices_host;
+  void* out;                /* [T, Hv, Dv] */
+  int64_t out_len;
+  void* workspace;          /* device scratch, see gdn_prefill_workspace_bytes */
+  size_t workspace_bytes;
+} gdn_prefill_args;
+
+int gdn_prefill_varlen(const gdn_prefill_args* args, void* stream);
+
+/* Scratch bytes gdn_prefill_varlen needs for these sizes and algorithm (0 for
+ * the recurrent algorithm).  Depends only on the arguments. */
+size_t gdn_prefill_workspace_bytes(int64_t T, int64_t N, int64_t Hv, int64_t Dk, int64_t Dv,
+                                   int32_t act_dtype, int32_t algo);
+
+/* The algorithm GDN_PREFILL_AUTO resolves to for these sizes. */
+int32_t gdn_prefill_resolve_algo(int64_t Dk, int64_t Dv, int32_t act_dtype, int32_t algo);
+
+/* Static text for a status code. */
+const char* gdn_status_string(int status);
+
+/* The calling thread's last diagnostic ("" after a successful call). */
+const char* gdn_last_error_message(void);
+
+/* Synchronises `stream`, then returns (and clears) the current device's
+ * status word: GDN_OK, GDN_ERR_DEVICE_CHECK or GDN_ERR_TIMEOUT. */
+int gdn_read_device_status(void* stream);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int gdn_version(void);
+
+/* Number of kernel launches this process has issued through the library
+ * (all devices, all threads).  Lets a caller count the kernels a step runs. */
+uint64_t gdn_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

@@ -1,0 +1,187 @@
+"""The C-ABI library builds, loads and exports every symbol include/gdn.h
+declares; host-side validation answers through the ABI with the documented
+codes and the [cpu.rs] (ferrum-kernels 0.8.0, src/ferrum_kernels/backend/
+cpu.rs) message texts.  No test here launches a kernel: every call fails
+validation (or, on a machine without a GPU, at the device lookup) before any
+launch, and the fake device addresses are never dereferenced on the host.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from gated_delta_rule_44_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 0x100000  # a 16-byte aligned address never dereferenced by host code
+
+
+def header_functions():
+    with open(os.path.join(ROOT, "include", "gdn.h")) as fh:
+        text = fh.read()
+    return sorted(set(re.findall(r"^(?:const\s+)?[A-Za-z_0-9]+\s*\*?\s*(gdn_[a-z_0-9]+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    fns = header_functions()
+    for name in ("gdn_prepare", "gdn_decode", "gdn_prefill_varlen", "gdn_prefill_workspace_bytes",
+                 "gdn_status_string", "gdn_last_error_message", "gdn_read_device_status"):
+        assert name in fns
+
+
+def test_library_exports_every_declared_symbol():
+    L = B.lib()
+    for name in header_functions():
+        assert hasattr(L, name), name
+    assert set(B.EXPORTED) <= set(header_functions())
+
+
+def test_status_strings():
+    L = B.lib()
+    for code, name in ((0, "GDN_OK"), (1, "GDN_ERR_SHAPE"), (2, "GDN_ERR_INVALID_ARGUMENT"),
+                       (3, "GDN_ERR_DTYPE"), (4, "GDN_ERR_UNSUPPORTED"), (5, "GDN_ERR_CUDA"),
+                       (6, "GDN_ERR_TIMEOUT"), (7, "GDN_ERR_DEVICE_CHECK")):
+        assert L.gdn_status_string(code).decode() == name
+    assert B.gdn_version() >= 100
+
+
+def decode_args(B_=2, Hk=1, Hv=2, Dk=128, Dv=64, **over):
+    a = dict(B=B_, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, act_dtype=B.GDN_DTYPE_BF16, use_qk_l2norm=0,
+             scale=-1.0, q=FAKE, q_len=B_ * Hk * Dk, k=FAKE, k_len=B_ * Hk * Dk, v=FAKE,
+             v_len=B_ * Hv * Dv, g=FAKE, g_len=B_ * Hv, beta=FAKE, beta_len=B_ * Hv, state=FAKE,
+             state_slots=4, state_len=4 * Hv * Dv * Dk, state_indices=None,
+             state_indices_host=None, out=FAKE, out_len=B_ * Hv * Dv)
+    a.update(over)
+    return B.gdn_decode_args(**a)
+
+
+def call_decode(args):
+    L = B.lib()
+    rc = L.gdn_decode(ctypes.byref(args), None)
+    return rc, L.gdn_last_error_message().decode()
+
+
+def test_decode_shape_messages():
+    rc, msg = call_decode(decode_args(q_len=2 * 128 - 1))
+    assert rc == B.GDN_ERR_SHAPE and msg == "gated_delta_rule query length 255 < expected 256"
+    rc, msg = call_decode(decode_args(Hk=2, Hv=3, q_len=10**9, k_len=10**9))
+    assert rc == B.GDN_ERR_SHAPE
+    assert msg == "gated_delta_rule value_heads 3 must be divisible by key_heads 2"
+    rc, msg = call_decode(decode_args(B_=0))
+    assert rc == B.GDN_ERR_SHAPE and msg.startswith("gated_delta_rule shape must be positive")
+    rc, msg = call_decode(decode_args(state_len=4 * 2 * 64 * 128 - 1))
+    assert rc == B.GDN_ERR_SHAPE and "state length" in msg
+
+
+def test_decode_other_rejections():
+    assert call_decode(decode_args(act_dtype=7))[0] == B.GDN_ERR_DTYPE
+    assert call_decode(decode_args(q=None))[0] == B.GDN_ERR_INVALID_ARGUMENT
+    assert call_decode(decode_args(q=FAKE + 2))[0] == B.GDN_ERR_INVALID_ARGUMENT
+    rc, msg = call_decode(decode_args(Dk=48, q_len=96, k_len=96, state_len=4 * 2 * 64 * 48))
+    assert rc == B.GDN_ERR_UNSUPPORTED
+    idx = (ctypes.c_int32 * 2)(1, 1)
+    rc, msg = call_decode(decode_args(state_indices=FAKE, state_indices_host=ctypes.addressof(idx)))
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT and msg == "duplicate live GDN state index"
+    idx = (ctypes.c_int32 * 2)(-2, 1)
+    rc, msg = call_decode(decode_args(state_indices=FAKE, state_indices_host=ctypes.addressof(idx)))
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT and msg == "invalid negative GDN state index"
+    idx = (ctypes.c_int32 * 2)(0, 4)
+    rc, msg = call_decode(decode_args(state_indices=FAKE, state_indices_host=ctypes.addressof(idx)))
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT and msg == "GDN state index out of range"
+
+
+def prefill_args(T=10, N=2, Hk=1, Hv=2, Dk=128, Dv=128, **over):
+    a = dict(T=T, N=N, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, act_dtype=B.GDN_DTYPE_BF16, use_qk_l2norm=0,
+             scale=-1.0, algo=B.GDN_PREFILL_RECURRENT, q=FAKE, q_len=T * Hk * Dk, k=FAKE,
+             k_len=T * Hk * Dk, v=FAKE, v_len=T * Hv * Dv, g=FAKE, g_len=T * Hv, beta=FAKE,
+             beta_len=T * Hv, state=FAKE, state_slots=N, state_len=N * Hv * Dv * Dk,
+             cu_seqlens=FAKE, state_indices=None, has_initial_state=None, cu_seqlens_host=None,
+             state_indices_host=None, out=FAKE, out_len=T * Hv * Dv, workspace=None,
+             workspace_bytes=0)
+    a.update(over)
+    return B.gdn_prefill_args(**a)
+
+
+def call_prefill(args):
+    L = B.lib()
+    rc = L.gdn_prefill_varlen(ctypes.byref(args), None)
+    return rc, L.gdn_last_error_message().decode()
+
+
+def test_prefill_cu_seqlens_messages():
+    cu = (ctypes.c_int32 * 3)(0, 4, 9)
+    rc, msg = call_prefill(prefill_args(cu_seqlens_host=ctypes.addressof(cu)))
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT
+    assert msg == ("gated_delta_rule_varlen cu_seqlens must start at 0 and end at total_tokens 10,"
+                   " got first=0 last=9")
+    cu = (ctypes.c_int32 * 3)(0, 0, 10)
+    rc, msg = call_prefill(prefill_args(cu_seqlens_host=ctypes.addressof(cu)))
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT
+    assert msg == "gated_delta_rule_varlen sequence 0 has empty or non-monotonic range 0..0"
+    assert call_prefill(prefill_args(algo=9))[0] == B.GDN_ERR_INVALID_ARGUMENT
+    assert call_prefill(prefill_args(cu_seqlens=None))[0] == B.GDN_ERR_INVALID_ARGUMENT
+    assert call_prefill(prefill_args(N=0))[0] == B.GDN_ERR_SHAPE
+
+
+def test_prefill_workspace_rules():
+    algo = B.gdn_prefill_resolve_algo(128, 128, B.GDN_DTYPE_BF16, B.GDN_PREFILL_AUTO)
+    assert algo in (B.GDN_PREFILL_CHUNKED, B.GDN_PREFILL_RECURRENT)
+    assert B.gdn_prefill_resolve_algo(32, 32, B.GDN_DTYPE_F32, B.GDN_PREFILL_AUTO) == \
+        B.GDN_PREFILL_RECURRENT
+    assert B.gdn_prefill_workspace_bytes(100, 2, 4, 32, 32, B.GDN_DTYPE_F32) == 0
+    need = B.gdn_prefill_workspace_bytes(4096, 1, 32, 128, 128, B.GDN_DTYPE_BF16,
+                                         B.GDN_PREFILL_CHUNKED)
+    if need > 0:
+        rc, msg = call_prefill(prefill_args(algo=B.GDN_PREFILL_CHUNKED, workspace=None))
+        assert rc == B.GDN_ERR_INVALID_ARGUMENT and "workspace needs" in msg
+
+
+def prepare_args(T=3, N=1, Hk=1, Hv=1, Dk=8, Dv=8, K=4, **over):
+    C = 2 * Hk * Dk + Hv * Dv
+    a = dict(T=T, N=N, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, K=K, act_dtype=B.GDN_DTYPE_BF16,
+             apply_qk_l2norm=1, mixed_qkv=FAKE, mixed_qkv_stride=0, mixed_qkv_len=T * C,
+             conv_weight=FAKE, conv_weight_len=C * K, a_raw=FAKE, a_raw_stride=0,
+             a_raw_len=T * Hv, b_raw=FAKE, b_raw_stride=0, b_raw_len=T * Hv, A_log=FAKE,
+             A_log_len=Hv, dt_bias=FAKE, dt_bias_len=Hv, cu_seqlens=FAKE, state_indices=None,
+             has_initial_state=None, cu_seqlens_host=None, state_indices_host=None,
+             conv_state=FAKE, conv_state_slots=N, conv_state_len=N * C * (K - 1), q=FAKE,
+             q_len=T * Hk * Dk, k=FAKE, k_len=T * Hk * Dk, v=FAKE, v_len=T * Hv * Dv, g=FAKE,
+             g_len=T * Hv, beta=FAKE, beta_len=T * Hv)
+    a.update(over)
+    return B.gdn_prepare_args(**a)
+
+
+def call_prepare(args):
+    L = B.lib()
+    rc = L.gdn_prepare(ctypes.byref(args), None)
+    return rc, L.gdn_last_error_message().decode()
+
+
+def test_prepare_messages():
+    rc, msg = call_prepare(prepare_args(conv_weight_len=95))
+    assert rc == B.GDN_ERR_SHAPE
+    assert msg == "linear_attention_prepare conv_weight length 95 < expected 96"
+    rc, msg = call_prepare(prepare_args(K=0))
+    assert rc == B.GDN_ERR_SHAPE and msg.endswith("conv_kernel=0")
+    rc, msg = call_prepare(prepare_args(mixed_qkv_stride=20, mixed_qkv_len=10**6))
+    assert rc == B.GDN_ERR_SHAPE  # stride shorter than a row of 24 channels
+    rc, msg = call_prepare(prepare_args(K=9, conv_weight_len=10**6, conv_state_len=10**6))
+    assert rc == B.GDN_ERR_UNSUPPORTED
+    rc, msg = call_prepare(prepare_args(Dk=12, q_len=10**6, k_len=10**6, mixed_qkv_len=10**6,
+                                        conv_weight_len=10**6, conv_state_len=10**6))
+    assert rc == B.GDN_ERR_UNSUPPORTED
+    rc, msg = call_prepare(prepare_args(mixed_qkv_stride=28, mixed_qkv_len=10**6))
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT  # 28 bf16 = 56 bytes: rows not 16-byte aligned
+    rc, msg = call_prepare(prepare_args(act_dtype=5))
+    assert rc == B.GDN_ERR_DTYPE
+
+
+def test_valid_call_without_gpu_stops_before_launch():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("this machine has a GPU")
+    rc, msg = call_decode(decode_args())
+    assert rc == B.GDN_ERR_CUDA

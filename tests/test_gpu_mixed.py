@@ -1,0 +1,61 @@
+"""End-to-end GPU parity of one mixed serving step (prepare, then decode on the
+leading single-token rows and the prefill on the rest) against the oracle's
+prepare + sequential recurrence from the same raw inputs.
+
+The GPU stores q, k, v and out in bf16; the oracle keeps f32 throughout, so the
+bf16 tolerance covers both rounding points.  The full-size mixed workload
+(512 decodes + 4 x 2048-token prefills, Hv = 64, 1024-slot pool) is compared on
+sampled decode rows and sampled prefill heads, plus the whole conv pool.
+"""
+import numpy as np
+import pytest
+import torch
+
+import helpers as H
+import oracle
+from gated_delta_rule_44_gb300 import layer
+from gated_delta_rule_44_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def run_mixed(w, dev, seqs, heads):
+    d = H.to_dev(w, dev)
+    out = layer.mixed_step(d["mixed_qkv"], d["a_raw"], d["b_raw"], d["conv_weight"], d["A_log"],
+                           d["dt_bias"], d["cu_seqlens"], d["state_indices"],
+                           d["has_initial_state"], d["state_pool"], d["conv_pool"],
+                           n_decode=w.n_decode, Hk=w.Hk, Hv=w.Hv, Dk=w.Dk, Dv=w.Dv, K=w.K,
+                           cu_seqlens_prefill=d["cu_seqlens_prefill"])
+    torch.cuda.synchronize()
+    ref_prep, ref_conv = H.oracle_prepare(w)
+    cpool, remap = H.compact_pool(w, seqs)
+    items = H.seq_head_items(w, seqs, heads)
+    ref_out = oracle.gdn_varlen(ref_prep["q"], ref_prep["k"], ref_prep["v"], ref_prep["g"],
+                                ref_prep["beta"], cpool, w.cu_seqlens.numpy(),
+                                1.0 / np.sqrt(w.Dk), state_indices=remap,
+                                has_initial_state=w.has_initial_state.numpy(), items=items,
+                                dtype=np.float32)
+    cu = w.cu_seqlens.tolist()
+    rows = np.concatenate([np.arange(cu[s], cu[s + 1]) for s in seqs])
+    tol = H.tol_for(w)
+    e_out = H.assert_close(H.f32(out)[rows][:, heads], ref_out[rows][:, heads], tol, "out")
+    gp = H.f32(d["state_pool"])
+    live = [s for s in seqs if remap[s] >= 0]
+    e_state = H.assert_close(np.stack([gp[int(w.state_indices[s])][heads] for s in live]),
+                             np.stack([cpool[remap[s]][heads] for s in live]), tol, "state")
+    np.testing.assert_array_equal(H.f32(d["conv_pool"]), ref_conv)
+    return e_out, e_state
+
+
+@pytest.mark.parametrize("weak", [False, True])
+def test_mixed_small(weak, cuda_device):
+    w = W.make_workload("m", 400, [1] * 9 + [70, 129, 3], 2, 4, 128, 128, slots=20, n_decode=9,
+                        prefill_new=True, padded=[4], weak_decay=weak, state_std=0.3)
+    run_mixed(w, cuda_device, list(range(w.N)), list(range(w.Hv)))
+
+
+def test_mixed_hv64_full_size_sampled(cuda_device):
+    w = W.named("mixed_hv64")
+    seqs = list(range(0, 512, 37)) + [512, 513, 514, 515]
+    e = run_mixed(w, cuda_device, seqs, [0, 1, 30, 63])
+    print(f"mixed_hv64: out err {e[0]:.2e}, state err {e[1]:.2e}")

@@ -1,0 +1,131 @@
+"""GPU parity of gdn_prefill_varlen against the oracle's sequential recurrence (O2).
+
+Both algorithms (chunked tensor-core form where supported, token-sequential
+recurrent form everywhere) are checked on: ragged varlen batches whose lengths
+straddle the chunk size (1, 63, 64, 65, 127, 128, 129, ...), padding slots,
+has_initial_state mixes, GQA ratios, f32 and bf16, in-kernel q/k norm, the
+weak-decay twins (slow decay, so a wrong carried state is not hidden), and the
+prefill workloads at full size (outputs of every head for the single 4096-token
+sequence; sampled (sequence, head) pairs for the 8-sequence varlen batch).
+Inputs are the oracle's prepare outputs rounded to the activation dtype by
+torch; the oracle gets the same rounded values.
+"""
+import numpy as np
+import pytest
+import torch
+
+import helpers as H
+import oracle
+from gated_delta_rule_44_gb300 import binding as B
+from gated_delta_rule_44_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+ALGOS = (B.GDN_PREFILL_RECURRENT, B.GDN_PREFILL_CHUNKED)
+
+
+def algo_ok(algo, w):
+    if algo == B.GDN_PREFILL_RECURRENT:
+        return True
+    dt = B.GDN_DTYPE_BF16 if w.act_dtype == torch.bfloat16 else B.GDN_DTYPE_F32
+    return B.gdn_prefill_resolve_algo(w.Dk, w.Dv, dt, B.GDN_PREFILL_AUTO) == B.GDN_PREFILL_CHUNKED
+
+
+def run_prefill(w, dev, algo, seqs=None, heads=None, norm=False, scale=-1.0, host=True):
+    ref_prep, _ = H.oracle_prepare(w, norm=not norm)
+    acts = {k: torch.from_numpy(ref_prep[k]).to(w.act_dtype) for k in ("q", "k", "v")}
+    g = torch.from_numpy(ref_prep["g"])
+    beta = torch.from_numpy(ref_prep["beta"])
+    out = torch.full((w.T, w.Hv, w.Dv), float("nan"), dtype=w.act_dtype, device=dev)
+    pool = w.state_pool.to(dev)
+    dt = B.GDN_DTYPE_BF16 if w.act_dtype == torch.bfloat16 else B.GDN_DTYPE_F32
+    ws_bytes = B.gdn_prefill_workspace_bytes(w.T, w.N, w.Hv, w.Dk, w.Dv, dt, algo)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev) if ws_bytes else None
+    B.gdn_prefill_varlen(acts["q"].to(dev), acts["k"].to(dev), acts["v"].to(dev), g.to(dev),
+                         beta.to(dev), pool, w.cu_seqlens.to(dev), out, scale=scale,
+                         state_indices=w.state_indices.to(dev),
+                         has_initial_state=w.has_initial_state.to(dev),
+                         cu_seqlens_host=w.cu_seqlens if host else None,
+                         state_indices_host=w.state_indices if host else None,
+                         use_qk_l2norm=norm, algo=algo, workspace=ws)
+    B.gdn_read_device_status()
+    seqs = list(range(w.N)) if seqs is None else seqs
+    heads = list(range(w.Hv)) if heads is None else heads
+    cpool, remap = H.compact_pool(w, seqs)
+    items = H.seq_head_items(w, seqs, heads)
+    sc = scale if scale >= 0 else 1.0 / np.sqrt(w.Dk)
+    ref_out = oracle.gdn_varlen(H.f32(acts["q"]), H.f32(acts["k"]), H.f32(acts["v"]), g.numpy(),
+                                beta.numpy(), cpool, w.cu_seqlens.numpy(), sc,
+                                state_indices=remap, has_initial_state=w.has_initial_state.numpy(),
+                                use_qk_l2norm=norm, items=items, dtype=np.float32)
+    tol = H.tol_for(w)
+    cu = w.cu_seqlens.tolist()
+    got = H.f32(out)
+    rows = np.concatenate([np.arange(cu[s], cu[s + 1]) for s in seqs])
+    e_out = H.assert_close(got[rows][:, heads], ref_out[rows][:, heads], tol, "out")
+    got_pool = H.f32(pool)
+    live = [s for s in seqs if remap[s] >= 0]
+    e_state = 0.0
+    if live:
+        gp = np.stack([got_pool[int(w.state_indices[s])][heads] for s in live])
+        rp = np.stack([cpool[remap[s]][heads] for s in live])
+        e_state = H.assert_close(gp, rp, tol, "state")
+    if len(seqs) == w.N and len(heads) == w.Hv:
+        used = {int(s) for s in w.state_indices.tolist() if s >= 0}
+        for slot in range(w.slots):
+            if slot not in used:
+                np.testing.assert_array_equal(got_pool[slot], w.state_pool[slot].numpy())
+    return e_out, e_state
+
+
+SMALL = [
+    # seqlens, Hk, Hv, Dk, Dv, dtype, padded, prefill_new, weak
+    ([64], 2, 4, 32, 32, torch.float32, None, True, False),
+    ([1, 63, 64, 65, 2, 127], 2, 4, 32, 32, torch.float32, [3], False, True),
+    ([1, 63, 64, 65, 2, 127], 2, 4, 128, 128, torch.bfloat16, [3], False, True),
+    ([129, 128, 3, 200], 1, 4, 128, 128, torch.bfloat16, None, True, True),
+    ([129, 128, 3, 200], 2, 2, 128, 128, torch.bfloat16, None, False, False),
+    ([300, 5], 2, 4, 64, 64, torch.bfloat16, None, False, True),
+    ([40, 9, 17], 2, 6, 16, 24, torch.float32, [1], False, True),
+]
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("case", range(len(SMALL)))
+def test_prefill_small(case, algo, cuda_device):
+    seqlens, Hk, Hv, Dk, Dv, dt, padded, new, weak = SMALL[case]
+    w = W.make_workload("p", 300 + case, seqlens, Hk, Hv, Dk, Dv, act_dtype=dt,
+                        slots=len(seqlens) + 2, padded=padded, prefill_new=new, n_decode=0,
+                        weak_decay=weak, state_std=0.3)
+    if not algo_ok(algo, w):
+        pytest.skip("algorithm not built for these dims")
+    run_prefill(w, cuda_device, algo)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_prefill_norm_scale_no_mirrors(algo, cuda_device):
+    w = W.make_workload("p", 320, [70, 1, 64], 2, 4, 128, 128, act_dtype=torch.bfloat16,
+                        weak_decay=True, state_std=0.3)
+    if not algo_ok(algo, w):
+        pytest.skip("algorithm not built for these dims")
+    run_prefill(w, cuda_device, algo, norm=True, scale=0.2, host=False)
+
+
+@pytest.mark.parametrize("weak", [False, True])
+@pytest.mark.parametrize("algo", ALGOS)
+def test_prefill_4k_full_size(algo, weak, cuda_device):
+    w = W.named("prefill_4k", weak_decay=weak)
+    if not algo_ok(algo, w):
+        pytest.skip("algorithm not built for these dims")
+    e = run_prefill(w, cuda_device, algo)
+    print(f"prefill_4k algo={algo} weak={weak}: out err {e[0]:.2e}, state err {e[1]:.2e}")
+
+
+@pytest.mark.parametrize("weak", [False, True])
+@pytest.mark.parametrize("algo", ALGOS)
+def test_varlen_8_full_size_sampled(algo, weak, cuda_device):
+    w = W.named("varlen_8", weak_decay=weak)
+    if not algo_ok(algo, w):
+        pytest.skip("algorithm not built for these dims")
+    e = run_prefill(w, cuda_device, algo, seqs=list(range(w.N)), heads=[0, 13, 31])
+    print(f"varlen_8 algo={algo} weak={weak}: out err {e[0]:.2e}, state err {e[1]:.2e}")
