@@ -65,6 +65,53 @@ def _load():
         return _lib
 
 
+class using_library:
+    """Context manager that routes every oracle call to another build of the
+    oracle source (used by the mutation tests, which compile a copy with one
+    planted mistake)."""
+
+    def __init__(self, path: str):
+        self.path = path
+        self.prev = None
+
+    def __enter__(self):
+        global _lib
+        L = ctypes.CDLL(self.path)
+        _declare(L)
+        with _lock:
+            self.prev = _lib
+            _lib = L
+        return L
+
+    def __exit__(self, *exc):
+        global _lib
+        with _lock:
+            _lib = self.prev
+        return False
+
+
+def build_variant(src_text: str, out_dir: str) -> str:
+    """Compiles `src_text` (a modified copy of gdn_oracle.cpp) with the same
+    flags into out_dir; returns the library path."""
+    os.makedirs(out_dir, exist_ok=True)
+    src = os.path.join(out_dir, "gdn_oracle.cpp")
+    with open(src, "w") as fh:
+        fh.write(src_text)
+    with open(_HDR) as fh:
+        hdr = fh.read()
+    with open(os.path.join(out_dir, "gdn_oracle.h"), "w") as fh:
+        fh.write(hdr)
+    lib_path = os.path.join(out_dir, "libgdn_oracle_variant.so")
+    subprocess.run(["g++", "-std=c++17", "-O2", "-ffp-contract=off", "-fPIC", "-shared",
+                    "-pthread", "-o", lib_path, src], check=True)
+    return lib_path
+
+
+def source_text() -> str:
+    with open(_SRC) as fh:
+        return fh.read()
+
+
 _i64 = ctypes.c_int64
 _vp = ctypes.c_void_p
 
