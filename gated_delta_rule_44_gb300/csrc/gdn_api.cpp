@@ -399,8 +399,6 @@ int gdn_prefill_varlen(const gdn_prefill_args* a, void* stream) {
   p.sidx = a->state_indices;
   p.has_init = a->has_initial_state;
   p.out = a->out;
-  p.status = gdn::status_word();
-  if (p.status == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (algo == GDN_PREFILL_CHUNKED) {
     if (!gdn::chunked_supported((int)a->Dk, (int)a->Dv, p.bf16))
@@ -415,11 +413,15 @@ int gdn_prefill_varlen(const gdn_prefill_args* a, void* stream) {
       if ((reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0)
         return fail(GDN_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
     }
+    p.status = gdn::status_word();
+    if (p.status == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
     gdn::ChunkedLaunch c{p, a->workspace, a->workspace_bytes};
     return launch_result(gdn::launch_chunked(c, st), "gdn_prefill_varlen(chunked)");
   }
   if (!gdn::recurrent_supported((int)a->Dk))
     return fail(GDN_ERR_UNSUPPORTED, "the recurrent prefill supports Dk in {16, 32, 64, 128, 256}");
+  p.status = gdn::status_word();
+  if (p.status == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
   return launch_result(gdn::launch_recurrent(p, st), "gdn_prefill_varlen(recurrent)");
 }
 

@@ -63,6 +63,13 @@ struct Act<float> {
     *reinterpret_cast<float4*>(p) = make_float4(o[0], o[1], o[2], o[3]);
   }
   __device__ static float scalar(const float* p) { return __ldg(p); }
+  __device__ static uint4 load_raw(const float* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+  __device__ static void unpack(const uint4& v, float (&o)[4]) {
+    o[0] = __uint_as_float(v.x);
+    o[1] = __uint_as_float(v.y);
+    o[2] = __uint_as_float(v.z);
+    o[3] = __uint_as_float(v.w);
+  }
 };
 
 template <>
@@ -87,6 +94,17 @@ struct Act<__nv_bfloat16> {
     *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
   }
   __device__ static float scalar(const __nv_bfloat16* p) { return __bfloat162float(p[0]); }
+  __device__ static uint4 load_raw(const __nv_bfloat16* p) {
+    return __ldg(reinterpret_cast<const uint4*>(p));
+  }
+  __device__ static void unpack(const uint4& v, float (&o)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = __uint_as_float(w[i] << 16);
+      o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
 };
 
 // Largest s in [0, n) with cu[s] <= t (cu assumed non-decreasing; callers
@@ -108,6 +126,7 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(const PrepareLaunch p
                                                            int chan_blocks) {
   constexpr int V = Act<TA>::kVec;
   constexpr int W = KW - 1;  // conv tail length
+  constexpr int WV = W > 0 ? W : 1;
   const int qk_total = p.Hk * p.Dk;
   const int C = 2 * qk_total + p.Hv * p.Dv;
   const int t_begin = blockIdx.x * tile;
@@ -153,11 +172,30 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(const PrepareLaunch p
     out_stride = (int64_t)p.Hv * p.Dv;
   }
 
-  float win[W > 0 ? W : 1][V];  // win[j] = input at token t - W + j
+  // conv + SiLU + (norm) + store of token t, given its window (oldest first)
+  // and its own input.  Uniform across the warp: every lane joins the shuffles.
+  auto emit = [&](int t, const float (&win)[WV][V], const float (&xt)[V]) {
+    float y[V];
+    float ss = 0.0f;
 #pragma unroll
-  for (int j = 0; j < W; ++j)
+    for (int i = 0; i < V; ++i) {
+      float acc = 0.0f;
 #pragma unroll
-    for (int i = 0; i < V; ++i) win[j][i] = 0.0f;
+      for (int j = 0; j < W; ++j) acc = fmaf(win[j][i], wt[i][j], acc);
+      acc = fmaf(xt[i], wt[i][W], acc);
+      y[i] = acc * sigmoid_f(acc);  // silu
+      ss = fmaf(y[i], y[i], ss);
+    }
+    if (p.norm) {
+      for (int m = 1; m < group; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+      if (is_qk) {
+        const float inv = 1.0f / sqrtf(ss + 1e-6f);
+#pragma unroll
+        for (int i = 0; i < V; ++i) y[i] *= inv;
+      }
+    }
+    if (active) Act<TA>::store(out_ptr + (int64_t)t * out_stride, y);
+  };
 
   // Sequence bracket of the tile's first token.
   int s = find_seq(p.cu, p.N, t_begin);
@@ -168,14 +206,122 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(const PrepareLaunch p
     return;
   }
 
-  // Starts sequence s at its first token: loads the old tail into the window
-  // and writes the new tail (last W raw inputs of tail || x) to the slot.
-  auto begin_sequence = [&]() {
-    int slot = p.sidx != nullptr ? __ldg(p.sidx + s) : s;
+  // ---- interior tile: every token's window lies inside one sequence --------------
+  // All K-1+tile input rows are loaded before any is used.
+  if (seq_lo + W <= t_begin && t_end <= seq_hi) {
+    constexpr int kMaxTile = 16;
+    const int n = t_end - t_begin;
+    uint4 raw[kMaxTile + WV];
+#pragma unroll
+    for (int r = 0; r < kMaxTile + W; ++r)
+      raw[r] = (active && r < n + W) ? Act<TA>::load_raw(x + (int64_t)(t_begin - W + r) * p.x_stride + c0)
+                                     : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int r = 0; r < kMaxTile; ++r) {
+      if (r < n) {
+        float win[WV][V], xt[V];
+#pragma unroll
+        for (int j = 0; j < W; ++j) Act<TA>::unpack(raw[r + j], win[j]);
+        Act<TA>::unpack(raw[r + W], xt);
+        emit(t_begin + r, win, xt);
+      }
+    }
+    return;
+  }
+
+  // Resolves the pool slot of sequence sq (bad index -> reported, treated as padding).
+  auto slot_of = [&](int sq) {
+    int slot = p.sidx != nullptr ? __ldg(p.sidx + sq) : sq;
     if (slot < -1 || slot >= p.slots) {
       if (threadIdx.x == 0) atomicOr(p.status, kStatusBadIndex);
       slot = -1;
     }
+    return slot;
+  };
+
+  // ---- decode tile: every token is a sequence of length one ----------------------
+  {
+    const int n = t_end - t_begin;
+    bool one = true;
+    if (seq_lo != t_begin) {
+      one = false;
+    } else if (lane < n) {
+      one = s + lane < p.N && __ldg(p.cu + s + lane + 1) == t_begin + lane + 1;
+    }
+    if (__all_sync(0xffffffffu, one) && W > 0) {
+      constexpr int kBatch = 2;
+      for (int b0 = 0; b0 < n; b0 += kBatch) {
+        float tails[kBatch][WV][V];
+        uint4 xr[kBatch];
+        float* tp[kBatch];
+#pragma unroll
+        for (int bi = 0; bi < kBatch; ++bi) {
+          const int i = b0 + bi;
+          tp[bi] = nullptr;
+          xr[bi] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int j = 0; j < W; ++j)
+#pragma unroll
+            for (int e = 0; e < V; ++e) tails[bi][j][e] = 0.0f;
+          if (i < n) {
+            const int slot = slot_of(s + i);
+            const bool init = slot >= 0 && (p.has_init == nullptr || __ldg(p.has_init + s + i) != 0);
+            if (slot >= 0 && active) tp[bi] = p.conv_pool + ((int64_t)slot * C + c0) * W;
+            if (active) xr[bi] = Act<TA>::load_raw(x + (int64_t)(t_begin + i) * p.x_stride + c0);
+            if (init && active) {
+              // V*W consecutive floats, channel-major: element (e, j) at e*W + j.
+              const float4* src = reinterpret_cast<const float4*>(tp[bi]);
+#pragma unroll
+              for (int q4 = 0; q4 < V * W / 4; ++q4) {
+                const float4 f = src[q4];
+                const float fv[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const int idx = q4 * 4 + u;
+                  tails[bi][idx % WV][idx / WV] = fv[u];
+                }
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int bi = 0; bi < kBatch; ++bi) {
+          const int i = b0 + bi;
+          if (i < n) {
+            float xt[V];
+            Act<TA>::unpack(xr[bi], xt);
+            emit(t_begin + i, tails[bi], xt);
+            if (tp[bi] != nullptr) {  // new tail: old[1..W-1], x
+              float nt[V * WV];
+#pragma unroll
+              for (int e = 0; e < V; ++e) {
+#pragma unroll
+                for (int j = 0; j + 1 < W; ++j) nt[e * W + j] = tails[bi][j + 1][e];
+                nt[e * W + W - 1] = xt[e];
+              }
+              float4* dst = reinterpret_cast<float4*>(tp[bi]);
+#pragma unroll
+              for (int q4 = 0; q4 < V * W / 4; ++q4)
+                dst[q4] = make_float4(nt[4 * q4], nt[4 * q4 + 1], nt[4 * q4 + 2], nt[4 * q4 + 3]);
+            }
+          }
+        }
+      }
+      return;
+    }
+  }
+
+  // ---- general tile: sequence starts, tails, short sequences --------------------
+  float win[WV][V];  // win[j] = input at token t - W + j
+#pragma unroll
+  for (int j = 0; j < WV; ++j)
+#pragma unroll
+    for (int i = 0; i < V; ++i) win[j][i] = 0.0f;
+
+  // Starts sequence s at its first token: loads the old tail into the window
+  // and writes the new tail (last W raw inputs of tail || x) to the slot.
+  auto begin_sequence = [&]() {
+    const int slot = slot_of(s);
     const bool live = slot >= 0;
     const bool init = live && (p.has_init == nullptr || __ldg(p.has_init + s) != 0);
     float* tail = live ? p.conv_pool + ((int64_t)slot * C + c0) * W : nullptr;
@@ -237,26 +383,7 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(const PrepareLaunch p
 #pragma unroll
       for (int i = 0; i < V; ++i) xt[i] = 0.0f;
     }
-    float y[V];
-    float ss = 0.0f;
-#pragma unroll
-    for (int i = 0; i < V; ++i) {
-      float acc = 0.0f;
-#pragma unroll
-      for (int j = 0; j < W; ++j) acc = fmaf(win[j][i], wt[i][j], acc);
-      acc = fmaf(xt[i], wt[i][W], acc);
-      y[i] = acc * sigmoid_f(acc);  // silu
-      ss = fmaf(y[i], y[i], ss);
-    }
-    if (p.norm) {  // uniform across the warp: every lane joins the shuffles
-      for (int m = 1; m < group; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-      if (is_qk) {
-        const float inv = 1.0f / sqrtf(ss + 1e-6f);
-#pragma unroll
-        for (int i = 0; i < V; ++i) y[i] *= inv;
-      }
-    }
-    if (active) Act<TA>::store(out_ptr + (int64_t)t * out_stride, y);
+    emit(t, win, xt);
 #pragma unroll
     for (int j = 0; j + 1 < W; ++j)
 #pragma unroll
@@ -276,8 +403,8 @@ cudaError_t launch_k(const PrepareLaunch& p, cudaStream_t s) {
   // Tiles of at least K-1 tokens (tail ownership); shrink them while the grid
   // is short of ~8 CTAs per SM.
   int tile = 16;
-  while (tile > 4 && (int64_t)((p.T + tile - 1) / tile) * chan_blocks < 8 * 152) tile >>= 1;
-  if (tile < KW - 1) tile = KW - 1;
+  while (tile > 2 && (int64_t)((p.T + tile - 1) / tile) * chan_blocks < 8 * 152) tile >>= 1;
+  if (tile < KW - 1) tile = KW - 1;  // >= K-1 for the tail ownership rule (K <= 8: <= 16)
   dim3 grid((p.T + tile - 1) / tile, chan_blocks + 1);
   if (grid.y > 65535) return cudaErrorInvalidConfiguration;
   prepare_kernel<TA, KW><<<grid, kThreads, 0, s>>>(p, tile, chan_blocks);

@@ -62,7 +62,8 @@ def run_prefill(w, dev, algo, seqs=None, heads=None, norm=False, scale=-1.0, hos
     cu = w.cu_seqlens.tolist()
     got = H.f32(out)
     rows = np.concatenate([np.arange(cu[s], cu[s + 1]) for s in seqs])
-    e_out = H.assert_close(got[rows][:, heads], ref_out[rows][:, heads], tol, "out")
+    e_out = H.assert_close(got[rows][:, heads], ref_out[rows][:, heads], tol, "out",
+                           stored_bf16=w.act_dtype == torch.bfloat16)
     got_pool = H.f32(pool)
     live = [s for s in seqs if remap[s] >= 0]
     e_state = 0.0

@@ -3,8 +3,9 @@
 Small cases span several token tiles and channel blocks, ragged sequence
 lengths (1, 2, 3, K-1, K, 63, 64, 65, ...), padding slots (-1), a mix of
 has_initial_state, conv widths 2..6, f32 and bf16; the five named workloads run
-at full size.  q, k, v, g, beta must match within the parity tolerance; the
-conv-tail pool holds raw inputs and must match bit for bit.
+at full size.  q, k, v, g, beta must match within the parity tolerance (q, k, v with the
+bf16-storage metric of tests/helpers.py when stored in bf16); the conv-tail
+pool holds raw inputs and must match bit for bit.
 """
 import numpy as np
 import pytest
@@ -23,7 +24,7 @@ def check(w, dev, norm=True, host_mirrors=True):
     tol = H.tol_for(w)
     errs = {}
     for key in ("q", "k", "v", "g", "beta"):
-        errs[key] = H.assert_close(H.f32(got[key]), ref[key], tol, key)
+        errs[key] = H.check(got[key], ref[key], tol, key)
     np.testing.assert_array_equal(H.f32(d["conv_pool"]), ref_pool)
     return errs
 
@@ -69,7 +70,7 @@ def test_prepare_strided_rows(cuda_device):
     got = H.gpu_prepare(w, d)
     ref, ref_pool = H.oracle_prepare(w)
     for key in ("q", "k", "v", "g", "beta"):
-        H.assert_close(H.f32(got[key]), ref[key], H.tol_for(w), key)
+        H.check(got[key], ref[key], H.tol_for(w), key)
     np.testing.assert_array_equal(H.f32(d["conv_pool"]), ref_pool)
 
 
