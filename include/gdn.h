@@ -230,6 +230,27 @@ typedef struct gdn_prefill_args {
 
 int gdn_prefill_varlen(const gdn_prefill_args* args, void* stream);
 
+/* gdn_prefill_varlen for callers that cannot allocate device memory (the
+ * pages have no counterpart: this is a deployment convenience).  Some callers
+ * cannot supply the chunked prefill's scratch buffer: a plug-in inside a host
+ * runtime that owns all device memory and gives plug-ins no allocator, or a
+ * serving loop that must never call cudaMalloc (it can synchronise the device
+ * and can fail under memory pressure).  This call takes the same arguments
+ * except that workspace / workspace_bytes are ignored: it uses a fixed 64 MiB
+ * scratch array that is part of the library's device image, and calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *   - Limit: sizes whose gdn_prefill_workspace_bytes() exceeds 64 MiB
+ *     (67108864 bytes) are rejected with GDN_ERR_INVALID_ARGUMENT before
+ *     anything is launched; sizes that need no scratch run as usual.
+ *   - Every GPU that loads the library holds the 64 MiB until process exit.
+ *   - The first call on each device (with that device current) looks up the
+ *     array's device address once; make that first call before any stream
+ *     capture.  A failed look-up returns GDN_ERR_CUDA.
+ *   - All calls share the one array, and it keeps the last call's contents
+ *     (nothing in it needs to start at zero): calls whose GPU work overlaps
+ *     (on different streams or from different host threads) race on it. */
+int gdn_prefill_varlen_noalloc(const gdn_prefill_args* args, void* stream);
+
 /* Scratch bytes gdn_prefill_varlen needs for these sizes and algorithm (0 for
  * the recurrent algorithm).  Depends only on the arguments. */
 size_t gdn_prefill_workspace_bytes(int64_t T, int64_t N, int64_t Hv, int64_t Dk, int64_t Dv,
