@@ -70,10 +70,17 @@ constexpr long long kWaitBudget = 2000000000LL;  // ~1 s of SM clock per wait
 
 // Workspace blob of one (chunk, value head).
 constexpr uint32_t kBlobW = 0;       // W image: K-major SW128, 2 boxes of [64 x 64] bf16
-constexpr uint32_t kBlobU = 16384;   // Ut: [2 slices][64 tokens][64] f32, row-major
+constexpr uint32_t kBlobU = 16384;   // Ut: [2 slices][64 tokens][64] f32, see ut_offset
 constexpr uint32_t kBlobG = 49152;   // gam: 64 f32
 constexpr uint32_t kBlobKn = 49408;  // 1/|k_i| (or 1): 64 f32
 constexpr uint32_t kBlobBytes = 49664;
+
+// Byte offset of Ut element (row i, column c < 64) inside one 16 KB slice: 256-byte
+// rows whose 16-byte chunks are XOR-swizzled by (i % 16), so that threads reading
+// the same chunk of consecutive rows hit different shared-memory banks.
+__device__ __forceinline__ uint32_t ut_offset(int i, int c) {
+  return i * 256 + ((((c >> 2) ^ (i & 15))) << 4) + (c & 3) * 4;
+}
 
 // TMEM row of an M = 64 accumulator held by (warp, lane): rows 16w .. 16w+15
 // sit in lanes 0..15 of warp w's 32-lane quarter.
@@ -190,8 +197,10 @@ struct PrepSmem {
   static constexpr uint32_t TUL = 57344;     // Tu lo
   static constexpr uint32_t A = 65536;       // A, f32 [64][68]
   static constexpr uint32_t kAStride = 68;
-  static constexpr uint32_t GB = A + 64 * kAStride * 4;  // g, beta, gam, kn: 4 x 64 f32
-  static constexpr uint32_t BYTES = GB + 4 * 64 * 4;
+  static constexpr uint32_t TT = A + 64 * kAStride * 4;   // T = (I + A)^-1, f32 [64][68]
+  static constexpr uint32_t X = TT + 64 * kAStride * 4;   // block scratch, f32 [3][16][17]
+  static constexpr uint32_t GB = X + 3 * 16 * 17 * 4;     // g, beta, gam, kn, wj, uj: 6 x 64 f32
+  static constexpr uint32_t BYTES = GB + 6 * 64 * 4;
 };
 
 __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(
@@ -289,7 +298,7 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(
 #pragma unroll
         for (int q16 = 0; q16 < 8; ++q16) {
           float v[8];
-          ld_bf16x8(sm + PrepSmem::K + box * 8192 + tid * 128 + q16 * 16, v);
+          ld_bf16x8(sm + PrepSmem::K + box * 8192 + tid * 128 + ((q16 ^ (tid & 7)) << 4), v);
 #pragma unroll
           for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
         }
@@ -337,36 +346,76 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(
   }
   fence_before_sync();
   __syncthreads();
+  float* sT = reinterpret_cast<float*>(sm + PrepSmem::TT);
+  float* sX = reinterpret_cast<float*>(sm + PrepSmem::X);
+  float* swj = skn + 64;
+  float* suj = swj + 64;
+  constexpr int S_ = PrepSmem::kAStride;
+  for (int e = tid; e < 64 * S_; e += kThreads) sT[e] = 0.0f;  // blocks above the diagonal
   if (tid < 64) {
-    // Column j of T = (I + A)^-1 by forward substitution:
-    //   T[i][j] = [i == j] - sum_{m < i} A[i][m] T[m][j]
-    const int j = tid;
-    float t[kC];
+    swj[tid] = sb[tid] * skn[tid] * __expf(sgam[tid]);
+    suj[tid] = sb[tid];
+  }
+  fence_before_sync();
+  __syncthreads();
+  // T = (I + A)^-1 in 16 x 16 blocks, A strictly lower triangular.
+  // (1) diagonal blocks D_b = (I + A_bb)^-1, column c of block b per thread:
+  //     x_i = [i == c] - sum_{m < i} A[16b+i][16b+m] x_m.
+  if (tid < 64) {
+    const int b = tid >> 4, c = tid & 15, r0 = 16 * b;
+    float x[16];
 #pragma unroll
-    for (int i = 0; i < kC; ++i) {
-      float acc0 = 0.f, acc1 = 0.f;
-      const float* Ai = sA + i * PrepSmem::kAStride;
+    for (int i = 0; i < 16; ++i) {
+      float acc = 0.0f;
 #pragma unroll
-      for (int m = 0; m + 1 < i; m += 2) {
-        acc0 = fmaf(Ai[m], t[m], acc0);
-        acc1 = fmaf(Ai[m + 1], t[m + 1], acc1);
+      for (int m = 0; m < i; ++m) acc = fmaf(sA[(r0 + i) * S_ + r0 + m], x[m], acc);
+      x[i] = (i == c ? 1.0f : 0.0f) - acc;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sT[(r0 + i) * S_ + r0 + c] = x[i];
+  }
+  __syncthreads();
+  // (2) below-diagonal blocks by distance L = I - J:
+  //     Y = sum_{K=J}^{I-1} A_IK T_KJ,   T_IJ = -D_I Y.
+#pragma unroll
+  for (int L = 1; L < 4; ++L) {
+    const int nblk = 4 - L;
+    for (int e = tid; e < nblk * 256; e += kThreads) {
+      const int J = e >> 8, i = (e >> 4) & 15, j = e & 15, I = J + L;
+      float y = 0.0f;
+      for (int K = J; K < I; ++K) {
+        const float* arow = sA + (16 * I + i) * S_ + 16 * K;
+        const float* tcol = sT + (16 * K) * S_ + 16 * J + j;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) y = fmaf(arow[m], tcol[m * S_], y);
       }
-      if (i & 1) acc0 = fmaf(Ai[i - 1], t[i - 1], acc0);
-      t[i] = (i == j ? 1.0f : 0.0f) - (acc0 + acc1);
+      sX[(J * 16 + i) * 17 + j] = y;
     }
-    const float wj = sb[j] * skn[j] * __expf(sgam[j]), uj = sb[j];
+    __syncthreads();
+    for (int e = tid; e < nblk * 256; e += kThreads) {
+      const int J = e >> 8, i = (e >> 4) & 15, j = e & 15, I = J + L;
+      const float* drow = sT + (16 * I + i) * S_ + 16 * I;
+      float t = 0.0f;
 #pragma unroll
-    for (int i = 0; i < kC; ++i) {
-      const uint32_t off = swz128_offset(i, j, 8192);
-      const float tw = t[i] * wj, tu = t[i] * uj;
-      const __nv_bfloat16 twh = __float2bfloat16_rn(tw), tuh = __float2bfloat16_rn(tu);
-      *reinterpret_cast<__nv_bfloat16*>(sm + PrepSmem::TWH + off) = twh;
-      *reinterpret_cast<__nv_bfloat16*>(sm + PrepSmem::TWL + off) =
-          __float2bfloat16_rn(tw - __bfloat162float(twh));
-      *reinterpret_cast<__nv_bfloat16*>(sm + PrepSmem::TUH + off) = tuh;
-      *reinterpret_cast<__nv_bfloat16*>(sm + PrepSmem::TUL + off) =
-          __float2bfloat16_rn(tu - __bfloat162float(tuh));
+      for (int m = 0; m < 16; ++m) t = fmaf(drow[m], sX[(J * 16 + m) * 17 + j], t);
+      sT[(16 * I + i) * S_ + 16 * J + j] = -t;
     }
+    __syncthreads();
+  }
+  // Tw = T diag(beta e^gam kn), Tu = T diag(beta) as hi + lo bf16 images:
+  // one (row, 8-column chunk) per thread and step, 16-byte stores.
+  for (int item = tid; item < 64 * 8; item += kThreads) {
+    const int i = item >> 3, q = item & 7;
+    float tw[8], tu[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float t = sT[i * S_ + 8 * q + e];
+      tw[e] = t * swj[8 * q + e];
+      tu[e] = t * suj[8 * q + e];
+    }
+    const uint32_t off = swz128_offset(i, 8 * q, 8192);
+    st_split8(sm + PrepSmem::TWH + off, sm + PrepSmem::TWL + off, tw);
+    st_split8(sm + PrepSmem::TUH + off, sm + PrepSmem::TUL + off, tu);
   }
   fence_proxy_async();
   fence_before_sync();
@@ -418,11 +467,11 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(
       tmem_ld16(tmem + lane_addr + 128 + c, v);
       tmem_ld_wait();
       if (i >= 0) {
-        float4* dst = reinterpret_cast<float4*>(blob + kBlobU + (c / 64) * 16384 + i * 256 +
-                                                (c % 64) * 4);
+        uint8_t* slice_base = blob + kBlobU + (c / 64) * 16384;
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+          *reinterpret_cast<float4*>(slice_base + ut_offset(i, (c % 64) + 4 * e)) =
+              make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
       }
     }
   }
@@ -438,6 +487,20 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(
 
 // ---------------------------------------------------------------------------
 // Kernel 2: per (sequence, value head, 64-row slice of Dv), chunks in order.
+//
+// 8 warps.  TMEM lane quadrant q = warp % 4 is shared by warps q and q + 4,
+// which split every 64-column tile into halves hf = warp / 4.
+//   U warps (q = 0, 1):  token rows 0..63 of W S^T -> U, U'
+//   P warps (q = 2, 3):  token rows 0..63 of Q S^T, Q K^T -> P, outputs
+//   all warps:           dk rows 0..127 of the state increment
+// MMAs (thread 0), hi and lo operands side by side along N = 128:
+//   D1 = [W; Q] [S_hi | S_lo]^T      rows 0..63 W S^T, 64..127 Q S^T
+//   Dp = [W; Q] K^T                  rows 64..127 Q K^T
+//   D2 = K^T [U'_hi | U'_lo]         rows = dk
+//   D3 = [0; P_hi] [U_hi | U_lo] + [0; P_lo] [U_hi | U_lo]   rows 64..127 P U
+// Each result's two column halves are added in the epilogue.  D3 of chunk c is
+// issued with D1 of chunk c + 1, so building P (and the output) stays off the
+// serial path D1 -> U -> D2 -> S; Q S^T is kept in registers until then.
 struct ScanSmem {
   // pipeline stage (x2): A1 = [W; Q] as a 128-row K-major tile, K tile, gam, kn
   static constexpr uint32_t A1 = 0;           // [W box0 | Q box0 | W box1 | Q box1], 32 KB
@@ -447,20 +510,21 @@ struct ScanSmem {
   static constexpr uint32_t STAGE = 50176;    // 49 KB (1 KB aligned)
   static constexpr uint32_t TX = 32768 + 16384 + 512;
   // single buffers
-  static constexpr uint32_t UT = 2 * STAGE;   // Ut slice f32 [64 tokens][64], 16 KB
-  static constexpr uint32_t SH = UT + 16384;  // S^T hi image [128 dk x 64 dv], 16 KB
-  static constexpr uint32_t SL = SH + 16384;  // S^T lo
-  static constexpr uint32_t UH = SL + 16384;  // U hi image [64 tok x 64 dv], 8 KB
+  static constexpr uint32_t UT = 2 * STAGE;   // Ut slice f32 [64 tokens][64] (ut_offset), 16 KB
+  static constexpr uint32_t SH = UT + 16384;  // S^T hi image [128 dk x 64 dv], 16 KB, then
+  static constexpr uint32_t SL = SH + 16384;  //   S^T lo: one MN-major B operand of N = 128
+  static constexpr uint32_t UH = SL + 16384;  // U hi image [64 tok x 64 dv], 8 KB, then U lo
   static constexpr uint32_t UL = UH + 8192;
-  static constexpr uint32_t U2H = UL + 8192;  // U' hi
+  static constexpr uint32_t U2H = UL + 8192;  // U' hi, then U' lo
   static constexpr uint32_t U2L = U2H + 8192;
   static constexpr uint32_t PH = U2L + 8192;  // [0; P hi] as a 128-row K-major tile, 16 KB
   static constexpr uint32_t PL = PH + 16384;  // [0; P lo]
-  static constexpr uint32_t QN = PL + 16384;  // 1/|q| of the last two chunks: 2 x 64 f32
-  static constexpr uint32_t BYTES = QN + 512;
+  static constexpr uint32_t BYTES = PL + 16384;
 };
 
-__global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
+constexpr int kScanThreads = 256;
+
+__global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const RecurLaunch p, const uint8_t* __restrict__ ws, int n_chunks_max) {
   extern __shared__ uint8_t smem_raw[];
@@ -470,6 +534,7 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
   __shared__ uint32_t tslot;
   __shared__ int s_base, s_bad;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, hf = warp >> 2;  // TMEM lane quadrant, column half
   const int slice = blockIdx.x & 1;
   const int sh = blockIdx.x >> 1;
   const int h = sh % p.Hv, s = sh / p.Hv;
@@ -487,7 +552,7 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
   }
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
   if (slot < 0) {  // padded sequence: zero outputs, pool untouched
-    for (int idx = tid; idx < (hi - lo) * 8; idx += kThreads) {
+    for (int idx = tid; idx < (hi - lo) * 8; idx += kScanThreads) {
       const int t = lo + idx / 8, q16 = idx % 8;
       *reinterpret_cast<uint4*>(out + ((int64_t)t * p.Hv + h) * kD + slice * 64 + q16 * 8) =
           make_uint4(0, 0, 0, 0);
@@ -520,7 +585,7 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
     mbar_init(smem_u32(&mb_e), 1);
     fence_mbar_init();
   }
-  for (int i = tid; i < 2 * 512; i += kThreads) {  // the zero halves of [0; P]
+  for (int i = tid; i < 2 * 512; i += kScanThreads) {  // the zero halves of [0; P]
     const uint32_t off = (i < 512 ? ScanSmem::PH : ScanSmem::PL);
     *reinterpret_cast<uint4*>(sm + off + (i % 512) * 16) = make_uint4(0, 0, 0, 0);
   }
@@ -553,6 +618,19 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
     mbar_expect_tx(mb, 16384);
     bulk_g2s(base + ScanSmem::UT, blob_of(c) + kBlobU + slice * 16384, 16384, mb);
   };
+  // D3 = [0; P_hi][U_hi | U_lo] + [0; P_lo][U_hi | U_lo]  (M = 128, N = 128, K = 64)
+  auto issue_d3 = [&]() {  // thread 0 only
+    const uint32_t id3 = idesc_bf16_f32(128, 128, false, true);
+#pragma unroll
+    for (int part = 0; part < 2; ++part)
+#pragma unroll
+      for (int kk = 0; kk < kC; kk += 16)
+        mma_bf16(tmem + 320,
+                 desc_sw128(base + (part ? ScanSmem::PL : ScanSmem::PH) + (kk % 64) * 2, 16, 1024),
+                 desc_sw128(base + ScanSmem::UH + (kk / 8) * 1024, 8192, 1024), id3,
+                 part > 0 || kk > 0);
+    mma_commit(smem_u32(&mb_d));
+  };
   // Loads issued so far (thread 0), for the error path.
   int issued_ld = 0, issued_ut = 0;
   if (tid == 0) {
@@ -566,18 +644,20 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
     issued_ut = 1;
   }
 
-  // State slice: thread tid owns dk = tid and the 64 dv of this slice, f32.
-  const int dk = tid;
-  float S[64];
+  // State: thread (quad, hf, lane) owns dk = 32 quad + lane and dv columns
+  // 32 hf .. 32 hf + 31 of this slice, in f32.
+  const int dk = quad * 32 + lane;
+  float S[32];
   float* pool = p.pool + ((int64_t)slot * p.Hv + h) * kD * kD;
   const bool init = p.has_init == nullptr || __ldg(p.has_init + s) != 0;
 #pragma unroll
-  for (int e = 0; e < 64; ++e) S[e] = init ? pool[(int64_t)(slice * 64 + e) * kD + dk] : 0.0f;
-  auto write_s = [&]() {  // S^T hi / lo images: row dk, 64 dv (MN-major B operand)
+  for (int e = 0; e < 32; ++e)
+    S[e] = init ? pool[(int64_t)(slice * 64 + hf * 32 + e) * kD + dk] : 0.0f;
+  auto write_s = [&]() {  // S^T hi / lo images: row dk, 32 dv columns (MN-major B operand)
 #pragma unroll
-    for (int c = 0; c < 64; c += 8) {
-      const uint32_t off = swz128_offset(dk, c, 16384);
-      st_split8(sm + ScanSmem::SH + off, sm + ScanSmem::SL + off, S + c);
+    for (int e = 0; e < 32; e += 8) {
+      const uint32_t off = swz128_offset(dk, hf * 32 + e, 16384);
+      st_split8(sm + ScanSmem::SH + off, sm + ScanSmem::SL + off, S + e);
     }
   };
   write_s();
@@ -586,36 +666,29 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
   __syncthreads();
   fence_after_sync();
 
-  const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
-  const uint32_t tm_d1 = tmem, tm_dp = tmem + 128, tm_d2 = tmem + 192, tm_d3 = tmem + 256;
-  float* qn_s = reinterpret_cast<float*>(sm + ScanSmem::QN);
+  const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+  const uint32_t tm_d1 = tmem, tm_dp = tmem + 128, tm_d2 = tmem + 192, tm_d3 = tmem + 320;
+  const bool u_warp = quad < 2;
+  const int row = (quad & 1) * 32 + lane;  // token row of U and P warps
+  // P warps carry the previous chunk's Q S^T and output factor to its output.
+  float qs_prev[32];
+  float fo_prev = 0.0f;
 
-  // Output of chunk cc by warps 2-3 (token row tid - 64):
-  //   O = e^{gam} scale qn Q S^T + P U
-  auto emit_output = [&](int cc) -> bool {
-    const bool w_ok = mbar_wait(smem_u32(&mb_d), cc & 1, kWaitBudget);
-    fence_after_sync();
-    const int st = cc & 1;
-    const float* gam = reinterpret_cast<const float*>(sm + st * ScanSmem::STAGE + ScanSmem::GAM);
-    const int row = tid - 64;
+  // Output of chunk cc by the P warps: O = e^{gam} scale qn Q S^T + P U.
+  auto emit_output = [&](int cc) {
     const int t0 = lo + cc * kC;
     const int L = min(kC, hi - t0);
-    const float fo = p.scale * __expf(gam[row]) * qn_s[st * 64 + row];
+    float a[32], b[32];
+    tmem_ld32(tm_d3 + lane_addr + hf * 32, a);
+    tmem_ld32(tm_d3 + lane_addr + 64 + hf * 32, b);
+    tmem_ld_wait();
+    if (row < L) {
 #pragma unroll
-    for (int c4 = 0; c4 < 64; c4 += 16) {
-      float a[16], b[16];
-      tmem_ld16(tm_d1 + st * 64 + lane_addr + c4, a);
-      tmem_ld16(tm_d3 + st * 64 + lane_addr + c4, b);
-      tmem_ld_wait();
-      if (row < L) {
+      for (int e = 0; e < 32; ++e) a[e] = fmaf(fo_prev, qs_prev[e], a[e] + b[e]);
+      __nv_bfloat16* dst = out + ((int64_t)(t0 + row) * p.Hv + h) * kD + slice * 64 + hf * 32;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) a[e] = fmaf(fo, a[e], b[e]);
-        __nv_bfloat16* dst = out + ((int64_t)(t0 + row) * p.Hv + h) * kD + slice * 64 + c4;
-        st_bf16x8(dst, a);
-        st_bf16x8(dst + 8, a + 8);
-      }
+      for (int e = 0; e < 32; e += 8) st_bf16x8(dst + e, a + e);
     }
-    return w_ok;
   };
 
   bool ok = true;
@@ -630,7 +703,7 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
     ok = mbar_wait(smem_u32(&mb_ld[st]), (c >> 1) & 1, kWaitBudget);
     if (!__syncthreads_and(ok)) break;
     if (L < kC) {  // zero K rows past the chunk end (they meet U rows that are 0)
-      for (int i = tid; i < (kC - L) * 8; i += kThreads) {
+      for (int i = tid; i < (kC - L) * 8; i += kScanThreads) {
         const int r = L + i / 8, q16 = i % 8;
         *reinterpret_cast<uint4*>(sst + ScanSmem::K + r * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4*>(sst + ScanSmem::K + 8192 + r * 128 + q16 * 16) =
@@ -641,77 +714,73 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
     }
     if (tid == 0) {
       fence_after_sync();
-      // D1[st] = [W; Q] (S_hi + S_lo)^T  (M = 128, N = 64, K = 128)
-      const uint32_t id1 = idesc_bf16_f32(128, 64, false, true);
+      // D1 = [W; Q] [S_hi | S_lo]^T  (M = 128, N = 128, K = 128)
+      const uint32_t id1 = idesc_bf16_f32(128, 128, false, true);
 #pragma unroll
-      for (int part = 0; part < 2; ++part)
-#pragma unroll
-        for (int kk = 0; kk < kD; kk += 16) {
-          const uint32_t a_off = (kk / 64) * 16384 + (kk % 64) * 2;
-          const uint32_t b_img = part ? ScanSmem::SL : ScanSmem::SH;
-          mma_bf16(tm_d1 + st * 64, desc_sw128(sb + ScanSmem::A1 + a_off, 16, 1024),
-                   desc_sw128(base + b_img + (kk / 8) * 1024, 16384, 1024), id1,
-                   part > 0 || kk > 0);
-        }
+      for (int kk = 0; kk < kD; kk += 16)
+        mma_bf16(tm_d1, desc_sw128(sb + ScanSmem::A1 + (kk / 64) * 16384 + (kk % 64) * 2, 16, 1024),
+                 desc_sw128(base + ScanSmem::SH + (kk / 8) * 1024, 16384, 1024), id1, kk > 0);
       mma_commit(smem_u32(&mb_a));
+      if (c > 0) issue_d3();  // previous chunk's P U (its P and U images are intact)
       // Dp = [W; Q] K^T  (M = 128, N = 64 tokens, K = 128; B = K tile, K-major)
       const uint32_t idp = idesc_bf16_f32(128, 64, false, false);
 #pragma unroll
-      for (int kk = 0; kk < kD; kk += 16) {
-        const uint32_t a_off = (kk / 64) * 16384 + (kk % 64) * 2;
-        const uint32_t b_off = (kk / 64) * 8192 + (kk % 64) * 2;
-        mma_bf16(tm_dp, desc_sw128(sb + ScanSmem::A1 + a_off, 16, 1024),
-                 desc_sw128(sb + ScanSmem::K + b_off, 16, 1024), idp, kk > 0);
-      }
+      for (int kk = 0; kk < kD; kk += 16)
+        mma_bf16(tm_dp, desc_sw128(sb + ScanSmem::A1 + (kk / 64) * 16384 + (kk % 64) * 2, 16, 1024),
+                 desc_sw128(sb + ScanSmem::K + (kk / 64) * 8192 + (kk % 64) * 2, 16, 1024), idp,
+                 kk > 0);
       mma_commit(smem_u32(&mb_p));
       last_mma = c;
     }
     __syncwarp();
     const float* gam = reinterpret_cast<const float*>(sst + ScanSmem::GAM);
     const float* kn = reinterpret_cast<const float*>(sst + ScanSmem::KN);
-    if (warp < 2) {
-      // U = Ut - W S^T, U' = diag(e^{gam_L - gam} kn) U for token row tid (hi + lo).
+    if (u_warp) {
+      // U = Ut - W S^T and U' = diag(e^{gam_L - gam} kn) U, this thread's row and
+      // column half, written as hi + lo images once D3 of the previous chunk is done.
       ok = mbar_wait(smem_u32(&mb_ut), c & 1, kWaitBudget);
       ok = mbar_wait(smem_u32(&mb_a), c & 1, kWaitBudget) && ok;
       fence_after_sync();
-      const int row = tid;
+      float wa[32], wb[32];
+      tmem_ld32(tm_d1 + lane_addr + hf * 32, wa);
+      tmem_ld32(tm_d1 + lane_addr + 64 + hf * 32, wb);
+      tmem_ld_wait();
       const float fu = __expf(gam[kC - 1] - gam[row]) * kn[row];
-      const float* ut = reinterpret_cast<const float*>(sm + ScanSmem::UT) + row * 64;
+      const uint8_t* ut = sm + ScanSmem::UT;
+      float u[32];
 #pragma unroll
-      for (int cc = 0; cc < 64; cc += 16) {
-        float v[16];
-        tmem_ld16(tm_d1 + st * 64 + lane_addr + cc, v);
-        tmem_ld_wait();
-        float u2[16];
+      for (int e = 0; e < 32; e += 4) {
+        const float4 f = *reinterpret_cast<const float4*>(ut + ut_offset(row, hf * 32 + e));
+        u[e] = f.x - (wa[e] + wb[e]);
+        u[e + 1] = f.y - (wa[e + 1] + wb[e + 1]);
+        u[e + 2] = f.z - (wa[e + 2] + wb[e + 2]);
+        u[e + 3] = f.w - (wa[e + 3] + wb[e + 3]);
+      }
+      if (c > 0) ok = mbar_wait(smem_u32(&mb_d), (c - 1) & 1, kWaitBudget) && ok;
 #pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-          const float4 f = *reinterpret_cast<const float4*>(ut + cc + e);
-          v[e] = f.x - v[e];
-          v[e + 1] = f.y - v[e + 1];
-          v[e + 2] = f.z - v[e + 2];
-          v[e + 3] = f.w - v[e + 3];
-        }
+      for (int e = 0; e < 32; e += 8) {
+        float u2[8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) u2[e] = fu * v[e];
-#pragma unroll
-        for (int half = 0; half < 16; half += 8) {
-          const uint32_t off = swz128_offset(row, cc + half, 8192);
-          st_split8(sm + ScanSmem::UH + off, sm + ScanSmem::UL + off, v + half);
-          st_split8(sm + ScanSmem::U2H + off, sm + ScanSmem::U2L + off, u2 + half);
-        }
+        for (int x = 0; x < 8; ++x) u2[x] = fu * u[e + x];
+        const uint32_t off = swz128_offset(row, hf * 32 + e, 8192);
+        st_split8(sm + ScanSmem::UH + off, sm + ScanSmem::UL + off, u + e);
+        st_split8(sm + ScanSmem::U2H + off, sm + ScanSmem::U2L + off, u2);
       }
       fence_proxy_async();
-      named_bar(1, 64);  // Ut consumed: fetch the next chunk's
+      named_bar(1, 128);  // Ut consumed: fetch the next chunk's
       if (tid == 0 && c + 1 < nchunks) {
-        fence_proxy_async();  // generic reads of Ut before the async overwrite
+        fence_proxy_async();
         issue_ut(c + 1);
         issued_ut = c + 2;
       }
     } else {
-      // Previous chunk's output; then 1/|q| and P = scale e^{gam_i - gam_j} qn_i kn_j Q K^T
-      // (j <= i) for token row tid - 64 of this chunk (hi + lo into [0; P]).
-      if (c > 0) ok = emit_output(c - 1);
-      const int row = tid - 64;
+      // The previous chunk's output (needs its D3), then Q S^T of this chunk into
+      // registers, then P = scale e^{gam_i - gam_j} qn_i kn_j Q K^T (j <= i) as hi + lo.
+      if (c > 0) {
+        ok = mbar_wait(smem_u32(&mb_d), (c - 1) & 1, kWaitBudget) && ok;
+        fence_after_sync();
+        emit_output(c - 1);
+      }
       float ss = 0.0f;
       if (p.norm) {
 #pragma unroll
@@ -719,31 +788,40 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
 #pragma unroll
           for (int q16 = 0; q16 < 8; ++q16) {
             float v[8];
-            ld_bf16x8(sst + ScanSmem::A1 + box * 16384 + 8192 + row * 128 + q16 * 16, v);
+            ld_bf16x8(sst + ScanSmem::A1 + box * 16384 + 8192 + row * 128 +
+                          ((q16 ^ (row & 7)) << 4), v);
 #pragma unroll
             for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
           }
       }
       const float qn = p.norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
-      qn_s[st * 64 + row] = qn;
-      ok = mbar_wait(smem_u32(&mb_p), c & 1, kWaitBudget) && ok;
+      ok = mbar_wait(smem_u32(&mb_a), c & 1, kWaitBudget) && ok;
       fence_after_sync();
-      const float gi = gam[row], fi = p.scale * qn;
-#pragma unroll
-      for (int cc = 0; cc < 64; cc += 16) {
-        float v[16];
-        tmem_ld16(tm_dp + lane_addr + cc, v);
+      {
+        float qa[32], qb[32];
+        tmem_ld32(tm_d1 + lane_addr + hf * 32, qa);
+        tmem_ld32(tm_d1 + lane_addr + 64 + hf * 32, qb);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int jj = cc + e;
-          v[e] = jj <= row ? fi * kn[jj] * __expf(gi - gam[jj]) * v[e] : 0.0f;
-        }
+        for (int e = 0; e < 32; ++e) qs_prev[e] = qa[e] + qb[e];
+      }
+      fo_prev = p.scale * __expf(gam[row]) * qn;  // consumed by emit_output(c) next time
+      ok = mbar_wait(smem_u32(&mb_p), c & 1, kWaitBudget) && ok;
+      fence_after_sync();
+      float qk[32];
+      tmem_ld32(tm_dp + lane_addr + hf * 32, qk);
+      tmem_ld_wait();
+      const float gi = gam[row], fi = p.scale * qn;
 #pragma unroll
-        for (int half = 0; half < 16; half += 8) {
-          const uint32_t off = swz128_offset(64 + row, cc + half, 16384);
-          st_split8(sm + ScanSmem::PH + off, sm + ScanSmem::PL + off, v + half);
+      for (int e = 0; e < 32; e += 8) {
+        float v[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+          const int jj = hf * 32 + e + x;
+          v[x] = jj <= row ? fi * kn[jj] * __expf(gi - gam[jj]) * qk[e + x] : 0.0f;
         }
+        const uint32_t off = swz128_offset(64 + row, hf * 32 + e, 16384);
+        st_split8(sm + ScanSmem::PH + off, sm + ScanSmem::PL + off, v);
       }
       fence_proxy_async();
     }
@@ -751,59 +829,48 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
     if (!__syncthreads_and(ok)) break;
     fence_after_sync();
     if (tid == 0) {
-      if (c >= 1 && c + 1 < nchunks) {
-        // Stage (c+1)&1 held chunk c-1, whose MMAs (mb_d) and readers are done.
-        fence_proxy_async();
-        issue_load(c + 1);
-        issued_ld = c + 2;
-      }
-      // D2 = K^T (U'_hi + U'_lo)  (M = 128 dk, N = 64, K = 64 tokens; A = K tile MN-major)
-      const uint32_t id2 = idesc_bf16_f32(128, 64, true, true);
+      // D2 = K^T [U'_hi | U'_lo]  (M = 128 dk, N = 128, K = 64 tokens; A = K tile MN-major)
+      const uint32_t id2 = idesc_bf16_f32(128, 128, true, true);
 #pragma unroll
-      for (int part = 0; part < 2; ++part)
-#pragma unroll
-        for (int kk = 0; kk < kC; kk += 16)
-          mma_bf16(tm_d2, desc_sw128(sb + ScanSmem::K + (kk / 8) * 1024, 8192, 1024),
-                   desc_sw128(base + (part ? ScanSmem::U2L : ScanSmem::U2H) + (kk / 8) * 1024,
-                              8192, 1024),
-                   id2, part > 0 || kk > 0);
+      for (int kk = 0; kk < kC; kk += 16)
+        mma_bf16(tm_d2, desc_sw128(sb + ScanSmem::K + (kk / 8) * 1024, 8192, 1024),
+                 desc_sw128(base + ScanSmem::U2H + (kk / 8) * 1024, 8192, 1024), id2, kk > 0);
       mma_commit(smem_u32(&mb_c));
-      // D3[st] = [0; P] U = P_hi U_hi + P_hi U_lo + P_lo U_hi  (M = 128, N = 64, K = 64)
-      const uint32_t id3 = idesc_bf16_f32(128, 64, false, true);
-#pragma unroll
-      for (int part = 0; part < 3; ++part)
-#pragma unroll
-        for (int kk = 0; kk < kC; kk += 16) {
-          const uint32_t a_img = part == 2 ? ScanSmem::PL : ScanSmem::PH;
-          const uint32_t b_img = part == 1 ? ScanSmem::UL : ScanSmem::UH;
-          mma_bf16(tm_d3 + st * 64, desc_sw128(base + a_img + (kk % 64) * 2, 16, 1024),
-                   desc_sw128(base + b_img + (kk / 8) * 1024, 8192, 1024), id3,
-                   part > 0 || kk > 0);
-        }
-      mma_commit(smem_u32(&mb_d));
     }
     __syncwarp();
-    ok = mbar_wait(smem_u32(&mb_c), c & 1, kWaitBudget);
+    ok = mbar_wait(smem_u32(&mb_c), c & 1, kWaitBudget) && ok;
     fence_after_sync();
     {
       // S = e^{gam_L} S + D2  (f32, registers), new S^T hi / lo images.
       const float dL = __expf(gam[kC - 1]);
+      float da[32], db[32];
+      tmem_ld32(tm_d2 + lane_addr + hf * 32, da);
+      tmem_ld32(tm_d2 + lane_addr + 64 + hf * 32, db);
+      tmem_ld_wait();
 #pragma unroll
-      for (int cc = 0; cc < 64; cc += 16) {
-        float v[16];
-        tmem_ld16(tm_d2 + lane_addr + cc, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) S[cc + e] = fmaf(dL, S[cc + e], v[e]);
-      }
+      for (int e = 0; e < 32; ++e) S[e] = fmaf(dL, S[e], da[e] + db[e]);
     }
     write_s();
     fence_proxy_async();
     fence_before_sync();
     if (!__syncthreads_and(ok)) break;
     fence_after_sync();
+    // Every reader of this stage (D1, Dp, D2 and the generic reads) is done:
+    // refill it with chunk c + 2.
+    if (tid == 0 && c + 2 < nchunks) {
+      fence_proxy_async();
+      issue_load(c + 2);
+      issued_ld = c + 3;
+    }
   }
-  if (c == nchunks && warp >= 2) ok = emit_output(nchunks - 1);
+  if (c == nchunks) {
+    if (tid == 0) issue_d3();  // the last chunk's P U
+    if (!u_warp) {
+      ok = mbar_wait(smem_u32(&mb_d), (nchunks - 1) & 1, kWaitBudget) && ok;
+      fence_after_sync();
+      emit_output(nchunks - 1);
+    }
+  }
   ok = __syncthreads_and(ok);
   if (c < nchunks || !ok) {
     // A wait ran out: report; let in-flight MMAs and loads finish (bounded); free TMEM.
@@ -823,7 +890,7 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
     return;
   }
 #pragma unroll
-  for (int e = 0; e < 64; ++e) pool[(int64_t)(slice * 64 + e) * kD + dk] = S[e];
+  for (int e = 0; e < 32; ++e) pool[(int64_t)(slice * 64 + hf * 32 + e) * kD + dk] = S[e];
   fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 512);
@@ -898,7 +965,7 @@ cudaError_t launch_chunked(const ChunkedLaunch& c, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int64_t blocks = static_cast<int64_t>(p.N) * p.Hv * 2;
   if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  chunk_scan_kernel<<<static_cast<unsigned>(blocks), kThreads, ScanSmem::BYTES + 1024, s>>>(
+  chunk_scan_kernel<<<static_cast<unsigned>(blocks), kScanThreads, ScanSmem::BYTES + 1024, s>>>(
       tq, tk, p, ws, static_cast<int>(nch));
   note_launch();
   return cudaGetLastError();

@@ -122,8 +122,8 @@ __device__ __forceinline__ int find_seq(const int32_t* __restrict__ cu, int n, i
 }
 
 template <typename TA, int KW>
-__global__ void __launch_bounds__(kThreads) prepare_kernel(const PrepareLaunch p, int tile,
-                                                           int chan_blocks) {
+__global__ void __launch_bounds__(kThreads, 4) prepare_kernel(const PrepareLaunch p, int tile,
+                                                              int chan_blocks) {
   constexpr int V = Act<TA>::kVec;
   constexpr int W = KW - 1;  // conv tail length
   constexpr int WV = W > 0 ? W : 1;
@@ -183,13 +183,15 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(const PrepareLaunch p
 #pragma unroll
       for (int j = 0; j < W; ++j) acc = fmaf(win[j][i], wt[i][j], acc);
       acc = fmaf(xt[i], wt[i][W], acc);
-      y[i] = acc * sigmoid_f(acc);  // silu
+      // silu(acc) = acc * sigmoid(acc); e^{-acc} may overflow to inf, whose
+      // reciprocal is 0, so no branch is needed.
+      y[i] = acc * __frcp_rn(1.0f + __expf(-acc));
       ss = fmaf(y[i], y[i], ss);
     }
     if (p.norm) {
       for (int m = 1; m < group; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
       if (is_qk) {
-        const float inv = 1.0f / sqrtf(ss + 1e-6f);
+        const float inv = rsqrtf(ss + 1e-6f);
 #pragma unroll
         for (int i = 0; i < V; ++i) y[i] *= inv;
       }
@@ -207,23 +209,46 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(const PrepareLaunch p
   }
 
   // ---- interior tile: every token's window lies inside one sequence --------------
-  // All K-1+tile input rows are loaded before any is used.
+  // Groups of 4 rows, the next group's loads in flight while one is computed.
   if (seq_lo + W <= t_begin && t_end <= seq_hi) {
-    constexpr int kMaxTile = 16;
+    constexpr int kG = 4;
     const int n = t_end - t_begin;
-    uint4 raw[kMaxTile + WV];
+    const TA* xrow = x + (int64_t)t_begin * p.x_stride + c0;
+    float win[WV][V];
 #pragma unroll
-    for (int r = 0; r < kMaxTile + W; ++r)
-      raw[r] = (active && r < n + W) ? Act<TA>::load_raw(x + (int64_t)(t_begin - W + r) * p.x_stride + c0)
-                                     : make_uint4(0, 0, 0, 0);
+    for (int j = 0; j < W; ++j) {
+      uint4 r = active ? Act<TA>::load_raw(xrow - (int64_t)(W - j) * p.x_stride) : make_uint4(0, 0, 0, 0);
+      Act<TA>::unpack(r, win[j]);
+    }
+    uint4 nxt[kG];
 #pragma unroll
-    for (int r = 0; r < kMaxTile; ++r) {
-      if (r < n) {
-        float win[WV][V], xt[V];
+    for (int u = 0; u < kG; ++u)
+      nxt[u] = (active && u < n) ? Act<TA>::load_raw(xrow + (int64_t)u * p.x_stride)
+                                 : make_uint4(0, 0, 0, 0);
+#pragma unroll 1
+    for (int r0 = 0; r0 < n; r0 += kG) {
+      uint4 cur[kG];
 #pragma unroll
-        for (int j = 0; j < W; ++j) Act<TA>::unpack(raw[r + j], win[j]);
-        Act<TA>::unpack(raw[r + W], xt);
-        emit(t_begin + r, win, xt);
+      for (int u = 0; u < kG; ++u) {
+        cur[u] = nxt[u];
+        const int r = r0 + kG + u;
+        nxt[u] = (active && r < n) ? Act<TA>::load_raw(xrow + (int64_t)r * p.x_stride)
+                                   : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kG; ++u) {
+        if (r0 + u < n) {
+          float xt[V];
+          Act<TA>::unpack(cur[u], xt);
+          emit(t_begin + r0 + u, win, xt);
+#pragma unroll
+          for (int j = 0; j + 1 < W; ++j)
+#pragma unroll
+            for (int i = 0; i < V; ++i) win[j][i] = win[j + 1][i];
+          if (W > 0)
+#pragma unroll
+            for (int i = 0; i < V; ++i) win[WV - 1][i] = xt[i];
+        }
       }
     }
     return;
