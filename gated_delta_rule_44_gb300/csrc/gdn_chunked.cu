@@ -30,24 +30,24 @@
 //
 // Two launches on the caller's stream:
 //  1. chunk_prep (one CTA per (chunk, value head), all chunks in parallel):
-//     G = K K^T (tcgen05, M = 64), A from G, T by column-parallel forward
-//     substitution (f32), W = Tw K and Ut = Tu V (tcgen05, hi + lo).  Writes W
-//     (as the swizzled shared-memory image the second kernel copies), Ut
-//     (f32), gam and 1/|k| to the workspace.
-//  2. chunk_scan (one CTA per (sequence, value head, 64-row slice of Dv), its
-//     chunks in order; TMA double-buffers W, Q, K, gam):
-//        D1 = [W; Q] S^T     (M = 128: rows 0..63 W S^T, rows 64..127 Q S^T)
-//        Dp = [W; Q] K^T     (rows 64..127: Q K^T, for P)
-//        warps 0-1: U = Ut - W S^T, U' = diag(e^{gam_L - gam} kn) U   (hi + lo)
-//        warps 2-3: P from Q K^T (hi + lo); the previous chunk's output
-//        D2 = K^T U'         (M = 128 dk rows: the state increment)
-//        D3 = [0; P] U       (rows 64..127: P U)
-//        S = e^{gam_L} S + D2 in f32 registers; S^T hi + lo images
-//     The output of chunk c (e^{gam} scale qn Q S^T + P U) is emitted by warps
-//     2-3 while chunk c+1's D1 runs; D1 and D3 are double-buffered in TMEM.
+//     [K; Q] K^T (tcgen05, M = 128) gives A and P; T by 32 x 32 blocks (f32);
+//     W = Tw K and Ut = Tu V (tcgen05, hi + lo).  Writes everything of the
+//     chunk that does not depend on the state: W and P as the swizzled
+//     shared-memory images the second kernel copies, Ut (f32) and the row
+//     factors fo = scale qn e^gam, fu = kn e^{gam_L - gam}, e^{gam_L}.
+//  2. chunk_scan (one CTA per (sequence, value head, 64-column slice of Dv), its
+//     chunks in order; TMA double-buffers W, Q, P, K and the factors).  Per
+//     chunk, the serial path is D1 -> U -> D2 -> S:
+//        D1 = [W; Q] [S_hi | S_lo]^T  (M = 128: rows 0..63 W S^T, 64..127 Q S^T)
+//        U warps: U = Ut - W S^T, U' = diag(fu) U            (hi + lo images)
+//        D2 = K^T [U'_hi | U'_lo]    (M = 128 dk rows: the state increment)
+//        D3 = [*; P_hi] U + [*; P_lo] U   (rows 64..127: P U; rows 0..63 unused)
+//        all warps: S = e^{gam_L} S + D2 in f32 registers; S^T hi + lo images
+//     Output warps emit chunk c (fo Q S^T + P U) while chunk c + 1 runs; D3 is
+//     double-buffered in TMEM.  One extra warp issues every MMA and copy.
 //
-// Partial chunks: K and V rows past the chunk end are zeroed in shared memory
-// and their g, beta taken as 0, so every derived row is exactly zero.
+// Partial chunks: K, Q and V rows past the chunk end are zeroed in shared
+// memory and their g, beta taken as 0, so every derived row is exactly zero.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -65,15 +65,16 @@ using namespace umma;
 
 constexpr int kC = 64;      // chunk length
 constexpr int kD = 128;     // Dk = Dv
-constexpr int kThreads = 128;
 constexpr long long kWaitBudget = 2000000000LL;  // ~1 s of SM clock per wait
 
-// Workspace blob of one (chunk, value head).
-constexpr uint32_t kBlobW = 0;       // W image: K-major SW128, 2 boxes of [64 x 64] bf16
-constexpr uint32_t kBlobU = 16384;   // Ut: [2 slices][64 tokens][64] f32, see ut_offset
-constexpr uint32_t kBlobG = 49152;   // gam: 64 f32
-constexpr uint32_t kBlobKn = 49408;  // 1/|k_i| (or 1): 64 f32
-constexpr uint32_t kBlobBytes = 49664;
+// Workspace blob of one (chunk, value head): everything of the chunk that does
+// not depend on the state.
+constexpr uint32_t kBlobW = 0;        // W image: K-major SW128, 2 boxes of [64 x 64] bf16
+constexpr uint32_t kBlobP = 16384;    // P hi image, then P lo: K-major SW128 [64 x 64] bf16
+constexpr uint32_t kBlobF = 32768;    // fo[64], fu[64], e^{gam_L}, 3 x 0 (f32)
+constexpr uint32_t kBlobFBytes = 528;
+constexpr uint32_t kBlobU = 33792;    // Ut: [2 slices][64 tokens][64] f32, see ut_offset
+constexpr uint32_t kBlobBytes = 66560;
 
 // Byte offset of Ut element (row i, column c < 64) inside one 16 KB slice: 256-byte
 // rows whose 16-byte chunks are XOR-swizzled by (i % 16), so that threads reading
@@ -186,33 +187,42 @@ __device__ int chunk_base(const int32_t* __restrict__ cu, int s, bool& bad) {
   return b;
 }
 
-// ---------------------------------------------------------------------------
-// Kernel 1: per (chunk, value head).
-struct PrepSmem {
-  static constexpr uint32_t K = 0;           // [K box0 | K box1], 16 KB
-  static constexpr uint32_t V = 16384;       // [V box0 | V box1], 16 KB
-  static constexpr uint32_t TWH = 32768;     // Tw hi image [64 x 64] bf16, 8 KB
-  static constexpr uint32_t TWL = 40960;     // Tw lo
-  static constexpr uint32_t TUH = 49152;     // Tu hi
-  static constexpr uint32_t TUL = 57344;     // Tu lo
-  static constexpr uint32_t A = 65536;       // A, f32 [64][68]
-  static constexpr uint32_t kAStride = 68;
-  static constexpr uint32_t TT = A + 64 * kAStride * 4;   // T = (I + A)^-1, f32 [64][68]
-  static constexpr uint32_t X = TT + 64 * kAStride * 4;   // block scratch, f32 [3][16][17]
-  static constexpr uint32_t GB = X + 3 * 16 * 17 * 4;     // g, beta, gam, kn, wj, uj: 6 x 64 f32
-  static constexpr uint32_t BYTES = GB + 6 * 64 * 4;
-};
 
-__global__ void __launch_bounds__(kThreads) chunk_prep_kernel(
-    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-    const RecurLaunch p, uint8_t* __restrict__ ws) {
+// ---------------------------------------------------------------------------
+// Kernel 1: per (chunk, value head).  8 warps; TMEM lane quadrant q = warp % 4
+// is shared by warps q and q + 4, which split columns into halves hf = warp / 4.
+struct PrepSmem {
+  static constexpr uint32_t KQ = 0;          // [K box0 | Q box0 | K box1 | Q box1], 32 KB
+  static constexpr uint32_t V = 32768;       // [V box0 | V box1], 16 KB
+  static constexpr uint32_t TWH = 49152;     // Tw hi image [64 x 64] bf16, 8 KB
+  static constexpr uint32_t TWL = 57344;     // Tw lo
+  static constexpr uint32_t TUH = 65536;     // Tu hi
+  static constexpr uint32_t TUL = 73728;     // Tu lo
+  static constexpr uint32_t AT = 81920;      // A, then T = (I + A)^-1 in place, f32 [64][68]
+  static constexpr uint32_t kAStride = 68;
+  static constexpr uint32_t Y = AT + 64 * kAStride * 4;   // A21 T11, f32 [32][36]
+  static constexpr uint32_t kYStride = 36;
+  static constexpr uint32_t GB = Y + 32 * kYStride * 4;   // g, beta, gam, kn, qn, wj, uj
+  static constexpr uint32_t BYTES = GB + 7 * 64 * 4;
+};
+constexpr int kPrepThreads = 256;
+
+// Shared memory rounded up to the 1024-byte alignment of swizzled tiles; the
+// pointer keeps the shared address space, so accesses compile to shared ones.
+__device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
+  return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+}
+
+__global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_v, const RecurLaunch p, uint8_t* __restrict__ ws) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
+  uint8_t* sm = aligned_smem(smem_raw);
   __shared__ uint64_t mbar_tma, mbar_mma;
   __shared__ uint32_t tslot;
   __shared__ int s_seq, s_chunk, s_ok;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, hf = warp >> 2;
   const int gc = blockIdx.x, h = blockIdx.y;
 
   if (warp == 0) {
@@ -236,7 +246,13 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(
   float* sb = sg + 64;
   float* sgam = sb + 64;
   float* skn = sgam + 64;
-  float* sA = reinterpret_cast<float*>(sm + PrepSmem::A);
+  float* sqn = skn + 64;
+  float* swj = sqn + 64;
+  float* suj = swj + 64;
+  float* sA = reinterpret_cast<float*>(sm + PrepSmem::AT);
+  float* sY = reinterpret_cast<float*>(sm + PrepSmem::Y);
+  constexpr int S_ = PrepSmem::kAStride;
+  constexpr int SY = PrepSmem::kYStride;
   const uint32_t base = smem_u32(sm);
   const uint32_t mb_tma = smem_u32(&mbar_tma), mb_mma = smem_u32(&mbar_mma);
 
@@ -247,9 +263,11 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(
   }
   __syncthreads();
   if (tid == 0) {
-    mbar_expect_tx(mb_tma, 4 * 8192);
-    tma_load_3d(base + PrepSmem::K + 0, &tm_k, mb_tma, 0, hk, t0);
-    tma_load_3d(base + PrepSmem::K + 8192, &tm_k, mb_tma, 64, hk, t0);
+    mbar_expect_tx(mb_tma, 6 * 8192);
+    tma_load_3d(base + PrepSmem::KQ + 0, &tm_k, mb_tma, 0, hk, t0);
+    tma_load_3d(base + PrepSmem::KQ + 8192, &tm_q, mb_tma, 0, hk, t0);
+    tma_load_3d(base + PrepSmem::KQ + 16384, &tm_k, mb_tma, 64, hk, t0);
+    tma_load_3d(base + PrepSmem::KQ + 24576, &tm_q, mb_tma, 64, hk, t0);
     tma_load_3d(base + PrepSmem::V + 0, &tm_v, mb_tma, 0, h, t0);
     tma_load_3d(base + PrepSmem::V + 8192, &tm_v, mb_tma, 64, h, t0);
   }
@@ -275,141 +293,169 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(
     sgam[2 * lane] = x - b;
   }
   bool ok = mbar_wait(mb_tma, 0, kWaitBudget);
-  if (L < kC) {  // zero K and V rows past the chunk end
-    for (int i = tid; i < (kC - L) * 8; i += kThreads) {
+  if (L < kC) {  // zero K, Q and V rows past the chunk end
+    for (int i = tid; i < (kC - L) * 8; i += kPrepThreads) {
       const int r = L + i / 8, q16 = i % 8;
 #pragma unroll
-      for (int box = 0; box < 4; ++box)
+      for (int box = 0; box < 6; ++box)
         *reinterpret_cast<uint4*>(sm + box * 8192 + r * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
     }
     fence_proxy_async();
   }
-  __syncthreads();
   if (!__syncthreads_and(ok)) {
     if (tid == 0) atomicOr(p.status, kStatusTimeout);
     if (warp == 0) tmem_dealloc(tmem, 256);
     return;
   }
-  if (tid < 64) {  // inverse k row norms
+  fence_after_sync();
+  // [K; Q] K^T  (M = 128, N = 64, K = 128): A is the 128-row K-major tile
+  // [K; Q] (boxes 16 KB apart), B the K tile (its first 64 rows).
+  if (tid == 0) {
+    const uint32_t idesc = idesc_bf16_f32(128, 64, false, false);
+#pragma unroll
+    for (int kk = 0; kk < kD; kk += 16) {
+      const uint32_t off = (kk / 64) * 16384 + (kk % 64) * 2;
+      mma_bf16(tmem, desc_sw128(base + PrepSmem::KQ + off, 16, 1024),
+               desc_sw128(base + PrepSmem::KQ + off, 16, 1024), idesc, kk > 0);
+    }
+    mma_commit(mb_mma);
+  }
+  if (tid < 128) {  // inverse row norms: threads 0..63 rows of K, 64..127 rows of Q
+    const int r = tid & 63;
     float ss = 0.0f;
     if (p.norm) {
+      const uint8_t* row = sm + PrepSmem::KQ + (tid < 64 ? 0 : 8192) + r * 128;
 #pragma unroll
       for (int box = 0; box < 2; ++box)
 #pragma unroll
         for (int q16 = 0; q16 < 8; ++q16) {
           float v[8];
-          ld_bf16x8(sm + PrepSmem::K + box * 8192 + tid * 128 + ((q16 ^ (tid & 7)) << 4), v);
+          ld_bf16x8(row + box * 16384 + ((q16 ^ (r & 7)) << 4), v);
 #pragma unroll
           for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
         }
     }
-    skn[tid] = p.norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+    (tid < 64 ? skn : sqn)[r] = p.norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
   }
-  fence_after_sync();
-  // G = K K^T  (M = 64, N = 64, K = 128; both operands the K tile, K-major).
-  if (tid == 0) {
-    const uint32_t idesc = idesc_bf16_f32(64, 64, false, false);
-#pragma unroll
-    for (int kk = 0; kk < kD; kk += 16) {
-      const uint32_t off = (kk / 64) * 8192 + (kk % 64) * 2;
-      mma_bf16(tmem, desc_sw128(base + PrepSmem::K + off, 16, 1024),
-               desc_sw128(base + PrepSmem::K + off, 16, 1024), idesc, kk > 0);
-    }
-    mma_commit(mb_mma);
-  }
-  __syncthreads();  // also publishes skn
-  ok = mbar_wait(mb_mma, 0, kWaitBudget);
-  fence_after_sync();
+  __syncthreads();  // publishes skn, sqn
   uint8_t* blob = ws + ((int64_t)gc * p.Hv + h) * kBlobBytes;
-  {
-    const int i = m64_row(warp, lane);
-    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
-    const float gi = i >= 0 ? sgam[i] : 0.0f;
-    const float fi = i >= 0 ? sb[i] * skn[i] : 0.0f;
-#pragma unroll
-    for (int c = 0; c < kC; c += 16) {
-      float v[16];
-      tmem_ld16(tmem + lane_addr + c, v);
-      tmem_ld_wait();
-      if (i >= 0) {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int jj = c + e;
-          v[e] = jj < i ? fi * skn[jj] * __expf(gi - sgam[jj]) * v[e] : 0.0f;
-        }
-#pragma unroll
-        for (int e = 0; e < 16; e += 4)
-          *reinterpret_cast<float4*>(sA + i * PrepSmem::kAStride + c + e) =
-              make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
-      }
-    }
-  }
-  fence_before_sync();
-  __syncthreads();
-  float* sT = reinterpret_cast<float*>(sm + PrepSmem::TT);
-  float* sX = reinterpret_cast<float*>(sm + PrepSmem::X);
-  float* swj = skn + 64;
-  float* suj = swj + 64;
-  constexpr int S_ = PrepSmem::kAStride;
-  for (int e = tid; e < 64 * S_; e += kThreads) sT[e] = 0.0f;  // blocks above the diagonal
   if (tid < 64) {
     swj[tid] = sb[tid] * skn[tid] * __expf(sgam[tid]);
     suj[tid] = sb[tid];
+    float* F = reinterpret_cast<float*>(blob + kBlobF);
+    F[tid] = p.scale * sqn[tid] * __expf(sgam[tid]);           // fo
+    F[64 + tid] = __expf(sgam[kC - 1] - sgam[tid]) * skn[tid];  // fu
+    if (tid < 4) F[128 + tid] = tid == 0 ? __expf(sgam[kC - 1]) : 0.0f;
   }
-  fence_before_sync();
-  __syncthreads();
-  // T = (I + A)^-1 in 16 x 16 blocks, A strictly lower triangular.
-  // (1) diagonal blocks D_b = (I + A_bb)^-1, column c of block b per thread:
-  //     x_i = [i == c] - sum_{m < i} A[16b+i][16b+m] x_m.
-  if (tid < 64) {
-    const int b = tid >> 4, c = tid & 15, r0 = 16 * b;
-    float x[16];
+  ok = mbar_wait(mb_mma, 0, kWaitBudget);
+  fence_after_sync();
+  {
+    // Lanes 0..63 hold K K^T -> A (f32, shared); lanes 64..127 hold Q K^T -> P
+    // (hi + lo images, straight to the workspace).  Row i, columns 32 hf ...
+    const int i = (quad & 1) * 32 + lane;
+    float v[32];
+    tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + hf * 32, v);
+    tmem_ld_wait();
+    const float gi = sgam[i];
+    if (quad < 2) {
+      const float fi = sb[i] * skn[i];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float acc = 0.0f;
-#pragma unroll
-      for (int m = 0; m < i; ++m) acc = fmaf(sA[(r0 + i) * S_ + r0 + m], x[m], acc);
-      x[i] = (i == c ? 1.0f : 0.0f) - acc;
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) sT[(r0 + i) * S_ + r0 + c] = x[i];
-  }
-  __syncthreads();
-  // (2) below-diagonal blocks by distance L = I - J:
-  //     Y = sum_{K=J}^{I-1} A_IK T_KJ,   T_IJ = -D_I Y.
-#pragma unroll
-  for (int L = 1; L < 4; ++L) {
-    const int nblk = 4 - L;
-    for (int e = tid; e < nblk * 256; e += kThreads) {
-      const int J = e >> 8, i = (e >> 4) & 15, j = e & 15, I = J + L;
-      float y = 0.0f;
-      for (int K = J; K < I; ++K) {
-        const float* arow = sA + (16 * I + i) * S_ + 16 * K;
-        const float* tcol = sT + (16 * K) * S_ + 16 * J + j;
-#pragma unroll
-        for (int m = 0; m < 16; ++m) y = fmaf(arow[m], tcol[m * S_], y);
+      for (int e = 0; e < 32; ++e) {
+        const int j = hf * 32 + e;
+        v[e] = j < i ? fi * skn[j] * __expf(gi - sgam[j]) * v[e] : 0.0f;
       }
-      sX[(J * 16 + i) * 17 + j] = y;
-    }
-    __syncthreads();
-    for (int e = tid; e < nblk * 256; e += kThreads) {
-      const int J = e >> 8, i = (e >> 4) & 15, j = e & 15, I = J + L;
-      const float* drow = sT + (16 * I + i) * S_ + 16 * I;
-      float t = 0.0f;
 #pragma unroll
-      for (int m = 0; m < 16; ++m) t = fmaf(drow[m], sX[(J * 16 + m) * 17 + j], t);
-      sT[(16 * I + i) * S_ + 16 * J + j] = -t;
+      for (int e = 0; e < 32; e += 4)
+        *reinterpret_cast<float4*>(sA + i * S_ + hf * 32 + e) =
+            make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+    } else {
+      const float fi = p.scale * sqn[i];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int j = hf * 32 + e;
+        v[e] = j <= i ? fi * skn[j] * __expf(gi - sgam[j]) * v[e] : 0.0f;
+      }
+#pragma unroll
+      for (int e = 0; e < 32; e += 8) {
+        const uint32_t off = swz128_offset(i, hf * 32 + e, 8192);
+        st_split8(blob + kBlobP + off, blob + kBlobP + 8192 + off, v + e);
+      }
     }
-    __syncthreads();
   }
+  __syncthreads();
+  // T = (I + A)^-1, A strictly lower triangular, by 32 x 32 blocks:
+  // (1) T11, T22 by forward substitution, warp b for block b, lane = column c:
+  //     x_i = [i == c] - sum_{m < i} A[32b+i][32b+m] x_m.
+  if (warp < 2) {
+    const int b0 = 32 * warp, c = lane;
+    float x[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float* arow = sA + (b0 + i) * S_ + b0;
+      float a0 = i == c ? 1.0f : 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+#pragma unroll
+      for (int m = 0; m < i; m += 4) {
+        const float4 av = *reinterpret_cast<const float4*>(arow + m);
+        a0 = fmaf(-av.x, x[m], a0);
+        if (m + 1 < i) a1 = fmaf(-av.y, x[m + 1], a1);
+        if (m + 2 < i) a2 = fmaf(-av.z, x[m + 2], a2);
+        if (m + 3 < i) a3 = fmaf(-av.w, x[m + 3], a3);
+      }
+      x[i] = (a0 + a1) + (a2 + a3);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) sA[(b0 + i) * S_ + b0 + c] = x[i];
+  }
+  __syncthreads();
+  // (2) Y = A21 T11, (3) T21 = -T22 Y: thread -> row i, columns j0 .. j0 + 3.
+  const int bi = tid >> 3, bj = (tid & 7) * 4;
+  {
+    const float* arow = sA + (32 + bi) * S_;
+    float y[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int k = 0; k < 32; k += 4) {
+      const float4 a = *reinterpret_cast<const float4*>(arow + k);
+      const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 t = *reinterpret_cast<const float4*>(sA + (k + q) * S_ + bj);
+        y[0] = fmaf(av[q], t.x, y[0]);
+        y[1] = fmaf(av[q], t.y, y[1]);
+        y[2] = fmaf(av[q], t.z, y[2]);
+        y[3] = fmaf(av[q], t.w, y[3]);
+      }
+    }
+    *reinterpret_cast<float4*>(sY + bi * SY + bj) = make_float4(y[0], y[1], y[2], y[3]);
+  }
+  __syncthreads();
+  {
+    const float* trow = sA + (32 + bi) * S_ + 32;
+    float y[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int k = 0; k < 32; k += 4) {
+      const float4 a = *reinterpret_cast<const float4*>(trow + k);
+      const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 t = *reinterpret_cast<const float4*>(sY + (k + q) * SY + bj);
+        y[0] = fmaf(av[q], t.x, y[0]);
+        y[1] = fmaf(av[q], t.y, y[1]);
+        y[2] = fmaf(av[q], t.z, y[2]);
+        y[3] = fmaf(av[q], t.w, y[3]);
+      }
+    }
+    *reinterpret_cast<float4*>(sA + (32 + bi) * S_ + bj) = make_float4(-y[0], -y[1], -y[2], -y[3]);
+  }
+  __syncthreads();
   // Tw = T diag(beta e^gam kn), Tu = T diag(beta) as hi + lo bf16 images:
   // one (row, 8-column chunk) per thread and step, 16-byte stores.
-  for (int item = tid; item < 64 * 8; item += kThreads) {
+  for (int item = tid; item < 64 * 8; item += kPrepThreads) {
     const int i = item >> 3, q = item & 7;
     float tw[8], tu[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const float t = sT[i * S_ + 8 * q + e];
+      const float t = sA[i * S_ + 8 * q + e];
       tw[e] = t * swj[8 * q + e];
       tu[e] = t * suj[8 * q + e];
     }
@@ -422,23 +468,23 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(
   __syncthreads();
   fence_after_sync();
   // W = (Tw_hi + Tw_lo) K, Ut = (Tu_hi + Tu_lo) V  (M = 64, N = 128, K = 64): B is
-  // the K (V) tile, MN-major: token rows, dk (dv) contiguous, boxes 8 KB apart.
+  // the K (V) tile, MN-major: token rows, dk (dv) contiguous.
   if (tid == 0) {
     const uint32_t idesc = idesc_bf16_f32(64, 128, false, true);
 #pragma unroll
     for (int part = 0; part < 2; ++part)
 #pragma unroll
       for (int kk = 0; kk < kC; kk += 16) {
-        const uint32_t a_off = (part ? PrepSmem::TWL : PrepSmem::TWH) + (kk % 64) * 2;
+        const uint32_t a_off = (part ? PrepSmem::TWL : PrepSmem::TWH) + kk * 2;
         mma_bf16(tmem, desc_sw128(base + a_off, 16, 1024),
-                 desc_sw128(base + PrepSmem::K + (kk / 8) * 1024, 8192, 1024), idesc,
+                 desc_sw128(base + PrepSmem::KQ + (kk / 8) * 1024, 16384, 1024), idesc,
                  part > 0 || kk > 0);
       }
 #pragma unroll
     for (int part = 0; part < 2; ++part)
 #pragma unroll
       for (int kk = 0; kk < kC; kk += 16) {
-        const uint32_t a_off = (part ? PrepSmem::TUL : PrepSmem::TUH) + (kk % 64) * 2;
+        const uint32_t a_off = (part ? PrepSmem::TUL : PrepSmem::TUH) + kk * 2;
         mma_bf16(tmem + 128, desc_sw128(base + a_off, 16, 1024),
                  desc_sw128(base + PrepSmem::V + (kk / 8) * 1024, 8192, 1024), idesc,
                  part > 0 || kk > 0);
@@ -446,38 +492,36 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(
     mma_commit(mb_mma);
   }
   __syncwarp();
-  ok = ok && mbar_wait(mb_mma, 1, kWaitBudget);
+  ok = mbar_wait(mb_mma, 1, kWaitBudget) && ok;
   fence_after_sync();
   {
-    const int i = m64_row(warp, lane);
-    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    // M = 64 accumulators: row 16 q + l in lane l < 16 of quadrant q.  Warp
+    // halves hf take W columns 64 hf .. and the Ut slice hf.
+    const int i = m64_row(quad, lane);
+    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
 #pragma unroll
-    for (int c = 0; c < kD; c += 16) {
+    for (int c = 0; c < 64; c += 16) {
       float v[16];
-      tmem_ld16(tmem + lane_addr + c, v);
+      tmem_ld16(tmem + lane_addr + hf * 64 + c, v);
       tmem_ld_wait();
       if (i >= 0) {
-        st_bf16x8(blob + kBlobW + swz128_offset(i, c, 8192), v);
-        st_bf16x8(blob + kBlobW + swz128_offset(i, c + 8, 8192), v + 8);
+        st_bf16x8(blob + kBlobW + swz128_offset(i, hf * 64 + c, 8192), v);
+        st_bf16x8(blob + kBlobW + swz128_offset(i, hf * 64 + c + 8, 8192), v + 8);
       }
     }
+    uint8_t* slice_base = blob + kBlobU + hf * 16384;
 #pragma unroll
-    for (int c = 0; c < kD; c += 16) {
+    for (int c = 0; c < 64; c += 16) {
       float v[16];
-      tmem_ld16(tmem + lane_addr + 128 + c, v);
+      tmem_ld16(tmem + lane_addr + 128 + hf * 64 + c, v);
       tmem_ld_wait();
       if (i >= 0) {
-        uint8_t* slice_base = blob + kBlobU + (c / 64) * 16384;
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          *reinterpret_cast<float4*>(slice_base + ut_offset(i, (c % 64) + 4 * e)) =
+          *reinterpret_cast<float4*>(slice_base + ut_offset(i, c + 4 * e)) =
               make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
       }
     }
-  }
-  if (tid < 64) {
-    reinterpret_cast<float*>(blob + kBlobG)[tid] = sgam[tid];
-    reinterpret_cast<float*>(blob + kBlobKn)[tid] = skn[tid];
   }
   if (!ok && tid == 0) atomicOr(p.status, kStatusTimeout);
   fence_before_sync();
@@ -486,29 +530,31 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// Kernel 2: per (sequence, value head, 64-row slice of Dv), chunks in order.
+// Kernel 2: per (sequence, value head, 64-column slice of Dv), chunks in order.
 //
-// 8 warps.  TMEM lane quadrant q = warp % 4 is shared by warps q and q + 4,
-// which split every 64-column tile into halves hf = warp / 4.
-//   U warps (q = 0, 1):  token rows 0..63 of W S^T -> U, U'
-//   P warps (q = 2, 3):  token rows 0..63 of Q S^T, Q K^T -> P, outputs
-//   all warps:           dk rows 0..127 of the state increment
-// MMAs (thread 0), hi and lo operands side by side along N = 128:
+// 17 warps.  TMEM lane quadrant q = warp % 4 is shared by warps q, q+4, q+8,
+// q+12, which split every 64-column tile into 16-column groups cg = warp / 4:
+//   U warps (q = 0, 1):       token rows 0..63 of W S^T -> U, U'
+//   output warps (q = 2, 3):  token rows 0..63 of Q S^T and P U -> outputs
+//   warps 0..15:             dk rows 0..127 of the state, 16 columns each
+//   warp 16 (lane 0):        every MMA, TMA and bulk copy
+// MMAs, hi and lo operands side by side along N = 128:
 //   D1 = [W; Q] [S_hi | S_lo]^T      rows 0..63 W S^T, 64..127 Q S^T
-//   Dp = [W; Q] K^T                  rows 64..127 Q K^T
 //   D2 = K^T [U'_hi | U'_lo]         rows = dk
-//   D3 = [0; P_hi] [U_hi | U_lo] + [0; P_lo] [U_hi | U_lo]   rows 64..127 P U
-// Each result's two column halves are added in the epilogue.  D3 of chunk c is
-// issued with D1 of chunk c + 1, so building P (and the output) stays off the
-// serial path D1 -> U -> D2 -> S; Q S^T is kept in registers until then.
+//   D3 = [*; P_hi] [U_hi | U_lo] + [*; P_lo] [U_hi | U_lo]   rows 64..127 P U
+// Each result's two column halves are added in the epilogue.  The A tiles of
+// D3 are 128-row windows that end with P_hi (P_lo): their first 64 rows are
+// whatever precedes it in the stage and only fill TMEM lanes 0..63, which
+// nobody reads.
 struct ScanSmem {
-  // pipeline stage (x2): A1 = [W; Q] as a 128-row K-major tile, K tile, gam, kn
-  static constexpr uint32_t A1 = 0;           // [W box0 | Q box0 | W box1 | Q box1], 32 KB
-  static constexpr uint32_t K = 32768;        // [K box0 | K box1], 16 KB
-  static constexpr uint32_t GAM = 49152;      // gam (64 f32), kn (64 f32)
-  static constexpr uint32_t KN = GAM + 256;
-  static constexpr uint32_t STAGE = 50176;    // 49 KB (1 KB aligned)
-  static constexpr uint32_t TX = 32768 + 16384 + 512;
+  // pipeline stage (x2)
+  static constexpr uint32_t A1 = 0;         // [W box0 | Q box0 | W box1 | Q box1], 32 KB
+  static constexpr uint32_t PH = 32768;     // P hi image, 8 KB
+  static constexpr uint32_t PL = 40960;     // P lo image, 8 KB
+  static constexpr uint32_t K = 49152;      // [K box0 | K box1], 16 KB
+  static constexpr uint32_t F = 65536;      // fo[64], fu[64], e^{gam_L}
+  static constexpr uint32_t STAGE = 66560;  // 65 KB (1 KB aligned)
+  static constexpr uint32_t TX = 32768 + 16384 + 16384 + kBlobFBytes;
   // single buffers
   static constexpr uint32_t UT = 2 * STAGE;   // Ut slice f32 [64 tokens][64] (ut_offset), 16 KB
   static constexpr uint32_t SH = UT + 16384;  // S^T hi image [128 dk x 64 dv], 16 KB, then
@@ -517,24 +563,30 @@ struct ScanSmem {
   static constexpr uint32_t UL = UH + 8192;
   static constexpr uint32_t U2H = UL + 8192;  // U' hi, then U' lo
   static constexpr uint32_t U2L = U2H + 8192;
-  static constexpr uint32_t PH = U2L + 8192;  // [0; P hi] as a 128-row K-major tile, 16 KB
-  static constexpr uint32_t PL = PH + 16384;  // [0; P lo]
-  static constexpr uint32_t BYTES = PL + 16384;
+  static constexpr uint32_t BYTES = U2L + 8192;
 };
 
-constexpr int kScanThreads = 256;
+static_assert(ScanSmem::PL == ScanSmem::PH + 8192 && ScanSmem::PH == ScanSmem::A1 + 32768,
+              "the D3 A windows [Q box1; P_hi] and [P_hi; P_lo] must be contiguous");
+static_assert(ScanSmem::BYTES + 1024 <= 232448, "shared memory per CTA");
+static_assert(PrepSmem::BYTES + 1024 <= 116736 - 2048, "two chunk_prep CTAs per SM");
+
+constexpr int kScanWorkers = 512;               // warps 0..15
+constexpr int kScanThreads = kScanWorkers + 32;  // + the issuing warp
+constexpr int kBarU = 1;                         // named barrier: U warps + issuer
 
 __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const RecurLaunch p, const uint8_t* __restrict__ ws, int n_chunks_max) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
-  __shared__ uint64_t mb_ld[2], mb_ut, mb_a, mb_p, mb_c, mb_d, mb_e;
+  uint8_t* sm = aligned_smem(smem_raw);
+  __shared__ uint64_t mb_ld[2], mb_ut, mb_a, mb_c, mb_d[2], mb_e;
   __shared__ uint32_t tslot;
   __shared__ int s_base, s_bad;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quad = warp & 3, hf = warp >> 2;  // TMEM lane quadrant, column half
+  const int quad = warp & 3, cg = warp >> 2;  // TMEM lane quadrant, 16-column group
+  const bool issuer_warp = warp == 16;
+  const bool issuer = tid == kScanWorkers;
   const int slice = blockIdx.x & 1;
   const int sh = blockIdx.x >> 1;
   const int h = sh % p.Hv, s = sh / p.Hv;
@@ -579,15 +631,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
     mbar_init(smem_u32(&mb_ld[1]), 1);
     mbar_init(smem_u32(&mb_ut), 1);
     mbar_init(smem_u32(&mb_a), 1);
-    mbar_init(smem_u32(&mb_p), 1);
     mbar_init(smem_u32(&mb_c), 1);
-    mbar_init(smem_u32(&mb_d), 1);
+    mbar_init(smem_u32(&mb_d[0]), 1);
+    mbar_init(smem_u32(&mb_d[1]), 1);
     mbar_init(smem_u32(&mb_e), 1);
     fence_mbar_init();
-  }
-  for (int i = tid; i < 2 * 512; i += kScanThreads) {  // the zero halves of [0; P]
-    const uint32_t off = (i < 512 ? ScanSmem::PH : ScanSmem::PL);
-    *reinterpret_cast<uint4*>(sm + off + (i % 512) * 16) = make_uint4(0, 0, 0, 0);
   }
   if (warp == 0) tmem_alloc(smem_u32(&tslot), 512);
   fence_before_sync();
@@ -598,7 +646,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
   auto blob_of = [&](int c) {
     return ws + ((int64_t)(gc0 + c) * p.Hv + h) * kBlobBytes;
   };
-  // Loads W, Q, K, gam, kn of chunk c into stage c & 1 (thread 0 only).
+  // Loads W, Q, P, K and the factors of chunk c into stage c & 1 (issuer only).
   auto issue_load = [&](int c) {
     const uint32_t sb = base + (c & 1) * ScanSmem::STAGE;
     const uint32_t mb = smem_u32(&mb_ld[c & 1]);
@@ -607,33 +655,21 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
     mbar_expect_tx(mb, ScanSmem::TX);
     bulk_g2s(sb + ScanSmem::A1, blob + kBlobW, 8192, mb);
     bulk_g2s(sb + ScanSmem::A1 + 16384, blob + kBlobW + 8192, 8192, mb);
-    bulk_g2s(sb + ScanSmem::GAM, blob + kBlobG, 512, mb);  // gam, kn
+    bulk_g2s(sb + ScanSmem::PH, blob + kBlobP, 16384, mb);
+    bulk_g2s(sb + ScanSmem::F, blob + kBlobF, kBlobFBytes, mb);
     tma_load_3d(sb + ScanSmem::A1 + 8192, &tm_q, mb, 0, hk, t0);
     tma_load_3d(sb + ScanSmem::A1 + 24576, &tm_q, mb, 64, hk, t0);
     tma_load_3d(sb + ScanSmem::K, &tm_k, mb, 0, hk, t0);
     tma_load_3d(sb + ScanSmem::K + 8192, &tm_k, mb, 64, hk, t0);
   };
-  auto issue_ut = [&](int c) {  // thread 0 only
+  auto issue_ut = [&](int c) {  // issuer only
     const uint32_t mb = smem_u32(&mb_ut);
     mbar_expect_tx(mb, 16384);
     bulk_g2s(base + ScanSmem::UT, blob_of(c) + kBlobU + slice * 16384, 16384, mb);
   };
-  // D3 = [0; P_hi][U_hi | U_lo] + [0; P_lo][U_hi | U_lo]  (M = 128, N = 128, K = 64)
-  auto issue_d3 = [&]() {  // thread 0 only
-    const uint32_t id3 = idesc_bf16_f32(128, 128, false, true);
-#pragma unroll
-    for (int part = 0; part < 2; ++part)
-#pragma unroll
-      for (int kk = 0; kk < kC; kk += 16)
-        mma_bf16(tmem + 320,
-                 desc_sw128(base + (part ? ScanSmem::PL : ScanSmem::PH) + (kk % 64) * 2, 16, 1024),
-                 desc_sw128(base + ScanSmem::UH + (kk / 8) * 1024, 8192, 1024), id3,
-                 part > 0 || kk > 0);
-    mma_commit(smem_u32(&mb_d));
-  };
-  // Loads issued so far (thread 0), for the error path.
+  // Loads issued so far (issuer), for the error path.
   int issued_ld = 0, issued_ut = 0;
-  if (tid == 0) {
+  if (issuer) {
     issue_load(0);
     issued_ld = 1;
     if (nchunks > 1) {
@@ -644,237 +680,210 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
     issued_ut = 1;
   }
 
-  // State: thread (quad, hf, lane) owns dk = 32 quad + lane and dv columns
-  // 32 hf .. 32 hf + 31 of this slice, in f32.
+  // State: worker (quad, cg, lane) owns dk = 32 quad + lane and dv columns
+  // 16 cg .. 16 cg + 15 of this slice, in f32.
   const int dk = quad * 32 + lane;
-  float S[32];
+  float S[16];
   float* pool = p.pool + ((int64_t)slot * p.Hv + h) * kD * kD;
   const bool init = p.has_init == nullptr || __ldg(p.has_init + s) != 0;
+  if (!issuer_warp) {
 #pragma unroll
-  for (int e = 0; e < 32; ++e)
-    S[e] = init ? pool[(int64_t)(slice * 64 + hf * 32 + e) * kD + dk] : 0.0f;
-  auto write_s = [&]() {  // S^T hi / lo images: row dk, 32 dv columns (MN-major B operand)
+    for (int e = 0; e < 16; ++e)
+      S[e] = init ? pool[(int64_t)(slice * 64 + cg * 16 + e) * kD + dk] : 0.0f;
+  }
+  auto write_s = [&]() {  // S^T hi / lo images: row dk, 16 dv columns (MN-major B operand)
 #pragma unroll
-    for (int e = 0; e < 32; e += 8) {
-      const uint32_t off = swz128_offset(dk, hf * 32 + e, 16384);
+    for (int e = 0; e < 16; e += 8) {
+      const uint32_t off = swz128_offset(dk, cg * 16 + e, 16384);
       st_split8(sm + ScanSmem::SH + off, sm + ScanSmem::SL + off, S + e);
     }
   };
-  write_s();
+  if (!issuer_warp) write_s();
   fence_proxy_async();
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
 
   const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-  const uint32_t tm_d1 = tmem, tm_dp = tmem + 128, tm_d2 = tmem + 192, tm_d3 = tmem + 320;
-  const bool u_warp = quad < 2;
-  const int row = (quad & 1) * 32 + lane;  // token row of U and P warps
-  // P warps carry the previous chunk's Q S^T and output factor to its output.
-  float qs_prev[32];
+  const uint32_t tm_d1 = tmem, tm_d2 = tmem + 128, tm_d3 = tmem + 256;  // D3: 2 x 128
+  const bool u_warp = !issuer_warp && quad < 2;
+  const int row = (quad & 1) * 32 + lane;  // token row of U and output warps
+  // Output warps carry the previous chunk's Q S^T and output factor.
+  float qs_prev[16];
   float fo_prev = 0.0f;
 
-  // Output of chunk cc by the P warps: O = e^{gam} scale qn Q S^T + P U.
+  // Output of chunk cc by the output warps: O = fo Q S^T + P U.
   auto emit_output = [&](int cc) {
     const int t0 = lo + cc * kC;
     const int L = min(kC, hi - t0);
-    float a[32], b[32];
-    tmem_ld32(tm_d3 + lane_addr + hf * 32, a);
-    tmem_ld32(tm_d3 + lane_addr + 64 + hf * 32, b);
+    const uint32_t d3 = tm_d3 + (cc & 1) * 128 + lane_addr + cg * 16;
+    float a[16], b[16];
+    tmem_ld16(d3, a);
+    tmem_ld16(d3 + 64, b);
     tmem_ld_wait();
     if (row < L) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) a[e] = fmaf(fo_prev, qs_prev[e], a[e] + b[e]);
-      __nv_bfloat16* dst = out + ((int64_t)(t0 + row) * p.Hv + h) * kD + slice * 64 + hf * 32;
-#pragma unroll
-      for (int e = 0; e < 32; e += 8) st_bf16x8(dst + e, a + e);
+      for (int e = 0; e < 16; ++e) a[e] = fmaf(fo_prev, qs_prev[e], a[e] + b[e]);
+      __nv_bfloat16* dst = out + ((int64_t)(t0 + row) * p.Hv + h) * kD + slice * 64 + cg * 16;
+      st_bf16x8(dst, a);
+      st_bf16x8(dst + 8, a + 8);
     }
   };
 
   bool ok = true;
   int c = 0;
-  int last_mma = -1;  // thread 0: last chunk whose MMAs were issued
+  int last_mma = -1;  // issuer: last chunk whose MMAs were issued
   for (; c < nchunks; ++c) {
     const int st = c & 1;
     uint8_t* sst = sm + st * ScanSmem::STAGE;
     const uint32_t sb = base + st * ScanSmem::STAGE;
     const int t0 = lo + c * kC;
     const int L = min(kC, hi - t0);
-    ok = mbar_wait(smem_u32(&mb_ld[st]), (c >> 1) & 1, kWaitBudget);
-    if (!__syncthreads_and(ok)) break;
-    if (L < kC) {  // zero K rows past the chunk end (they meet U rows that are 0)
-      for (int i = tid; i < (kC - L) * 8; i += kScanThreads) {
-        const int r = L + i / 8, q16 = i % 8;
-        *reinterpret_cast<uint4*>(sst + ScanSmem::K + r * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(sst + ScanSmem::K + 8192 + r * 128 + q16 * 16) =
-            make_uint4(0, 0, 0, 0);
+    const float* F = reinterpret_cast<const float*>(sst + ScanSmem::F);
+    ok = mbar_wait(smem_u32(&mb_ld[st]), (c >> 1) & 1, kWaitBudget) && ok;
+    if (issuer_warp) {
+      if (issuer && ok) {
+        fence_after_sync();
+        // D1 = [W; Q] [S_hi | S_lo]^T  (M = 128, N = 128, K = 128)
+        const uint32_t id1 = idesc_bf16_f32(128, 128, false, true);
+#pragma unroll
+        for (int kk = 0; kk < kD; kk += 16)
+          mma_bf16(tm_d1,
+                   desc_sw128(sb + ScanSmem::A1 + (kk / 64) * 16384 + (kk % 64) * 2, 16, 1024),
+                   desc_sw128(base + ScanSmem::SH + (kk / 8) * 1024, 16384, 1024), id1, kk > 0);
+        mma_commit(smem_u32(&mb_a));
+        last_mma = c;
       }
-      fence_proxy_async();
-      __syncthreads();
-    }
-    if (tid == 0) {
-      fence_after_sync();
-      // D1 = [W; Q] [S_hi | S_lo]^T  (M = 128, N = 128, K = 128)
-      const uint32_t id1 = idesc_bf16_f32(128, 128, false, true);
+      __syncwarp();
+      named_bar(kBarU, 256 + 32);  // U, U' images written, K tail zeroed, Ut consumed
+      if (issuer) {
+        if (ok) {
+          fence_after_sync();
+          // D2 = K^T [U'_hi | U'_lo]  (M = 128 dk, N = 128, K = 64 tokens; A = K tile MN-major)
+          const uint32_t id2 = idesc_bf16_f32(128, 128, true, true);
 #pragma unroll
-      for (int kk = 0; kk < kD; kk += 16)
-        mma_bf16(tm_d1, desc_sw128(sb + ScanSmem::A1 + (kk / 64) * 16384 + (kk % 64) * 2, 16, 1024),
-                 desc_sw128(base + ScanSmem::SH + (kk / 8) * 1024, 16384, 1024), id1, kk > 0);
-      mma_commit(smem_u32(&mb_a));
-      if (c > 0) issue_d3();  // previous chunk's P U (its P and U images are intact)
-      // Dp = [W; Q] K^T  (M = 128, N = 64 tokens, K = 128; B = K tile, K-major)
-      const uint32_t idp = idesc_bf16_f32(128, 64, false, false);
+          for (int kk = 0; kk < kC; kk += 16)
+            mma_bf16(tm_d2, desc_sw128(sb + ScanSmem::K + (kk / 8) * 1024, 8192, 1024),
+                     desc_sw128(base + ScanSmem::U2H + (kk / 8) * 1024, 8192, 1024), id2,
+                     kk > 0);
+          mma_commit(smem_u32(&mb_c));
+          // D3 = [*; P_hi] [U_hi | U_lo] + [*; P_lo] [U_hi | U_lo]  (M = 128, N = 128, K = 64)
+          const uint32_t id3 = idesc_bf16_f32(128, 128, false, true);
 #pragma unroll
-      for (int kk = 0; kk < kD; kk += 16)
-        mma_bf16(tm_dp, desc_sw128(sb + ScanSmem::A1 + (kk / 64) * 16384 + (kk % 64) * 2, 16, 1024),
-                 desc_sw128(sb + ScanSmem::K + (kk / 64) * 8192 + (kk % 64) * 2, 16, 1024), idp,
-                 kk > 0);
-      mma_commit(smem_u32(&mb_p));
-      last_mma = c;
-    }
-    __syncwarp();
-    const float* gam = reinterpret_cast<const float*>(sst + ScanSmem::GAM);
-    const float* kn = reinterpret_cast<const float*>(sst + ScanSmem::KN);
-    if (u_warp) {
-      // U = Ut - W S^T and U' = diag(e^{gam_L - gam} kn) U, this thread's row and
-      // column half, written as hi + lo images once D3 of the previous chunk is done.
-      ok = mbar_wait(smem_u32(&mb_ut), c & 1, kWaitBudget);
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int kk = 0; kk < kC; kk += 16)
+              mma_bf16(tm_d3 + st * 128,
+                       desc_sw128(sb + (part ? ScanSmem::PH : ScanSmem::A1 + 24576) + kk * 2, 16,
+                                  1024),
+                       desc_sw128(base + ScanSmem::UH + (kk / 8) * 1024, 8192, 1024), id3,
+                       part > 0 || kk > 0);
+          mma_commit(smem_u32(&mb_d[st]));
+        }
+        if (c + 1 < nchunks) {
+          fence_proxy_async();
+          issue_ut(c + 1);
+          issued_ut = c + 2;
+        }
+      }
+    } else if (u_warp) {
+      // U = Ut - W S^T and U' = diag(fu) U, this thread's row and 16 columns,
+      // written as hi + lo images once D3 of the previous chunk is done.
+      if (L < kC) {  // zero K rows past the chunk end (D2 meets them with U' rows of 0)
+        const int ui = (cg * 2 + quad) * 32 + lane;  // 0 .. 255 over the U warps
+        for (int i = ui; i < (kC - L) * 16; i += 256) {
+          const int r = L + i / 16, q16 = i % 16;
+          *reinterpret_cast<uint4*>(sst + ScanSmem::K + (q16 >> 3) * 8192 + r * 128 +
+                                    (q16 & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      ok = mbar_wait(smem_u32(&mb_ut), c & 1, kWaitBudget) && ok;
       ok = mbar_wait(smem_u32(&mb_a), c & 1, kWaitBudget) && ok;
       fence_after_sync();
-      float wa[32], wb[32];
-      tmem_ld32(tm_d1 + lane_addr + hf * 32, wa);
-      tmem_ld32(tm_d1 + lane_addr + 64 + hf * 32, wb);
+      float wa[16], wb[16];
+      tmem_ld16(tm_d1 + lane_addr + cg * 16, wa);
+      tmem_ld16(tm_d1 + lane_addr + 64 + cg * 16, wb);
       tmem_ld_wait();
-      const float fu = __expf(gam[kC - 1] - gam[row]) * kn[row];
+      const float fu = F[64 + row];
       const uint8_t* ut = sm + ScanSmem::UT;
-      float u[32];
+      float u[16];
 #pragma unroll
-      for (int e = 0; e < 32; e += 4) {
-        const float4 f = *reinterpret_cast<const float4*>(ut + ut_offset(row, hf * 32 + e));
+      for (int e = 0; e < 16; e += 4) {
+        const float4 f = *reinterpret_cast<const float4*>(ut + ut_offset(row, cg * 16 + e));
         u[e] = f.x - (wa[e] + wb[e]);
         u[e + 1] = f.y - (wa[e + 1] + wb[e + 1]);
         u[e + 2] = f.z - (wa[e + 2] + wb[e + 2]);
         u[e + 3] = f.w - (wa[e + 3] + wb[e + 3]);
       }
-      if (c > 0) ok = mbar_wait(smem_u32(&mb_d), (c - 1) & 1, kWaitBudget) && ok;
+      if (c > 0) ok = mbar_wait(smem_u32(&mb_d[st ^ 1]), ((c - 1) >> 1) & 1, kWaitBudget) && ok;
 #pragma unroll
-      for (int e = 0; e < 32; e += 8) {
+      for (int e = 0; e < 16; e += 8) {
         float u2[8];
 #pragma unroll
         for (int x = 0; x < 8; ++x) u2[x] = fu * u[e + x];
-        const uint32_t off = swz128_offset(row, hf * 32 + e, 8192);
+        const uint32_t off = swz128_offset(row, cg * 16 + e, 8192);
         st_split8(sm + ScanSmem::UH + off, sm + ScanSmem::UL + off, u + e);
         st_split8(sm + ScanSmem::U2H + off, sm + ScanSmem::U2L + off, u2);
       }
       fence_proxy_async();
-      named_bar(1, 128);  // Ut consumed: fetch the next chunk's
-      if (tid == 0 && c + 1 < nchunks) {
-        fence_proxy_async();
-        issue_ut(c + 1);
-        issued_ut = c + 2;
-      }
+      fence_before_sync();
+      named_bar(kBarU, 256 + 32);
     } else {
-      // The previous chunk's output (needs its D3), then Q S^T of this chunk into
-      // registers, then P = scale e^{gam_i - gam_j} qn_i kn_j Q K^T (j <= i) as hi + lo.
+      // The previous chunk's output (needs its D3), then Q S^T of this chunk.
       if (c > 0) {
-        ok = mbar_wait(smem_u32(&mb_d), (c - 1) & 1, kWaitBudget) && ok;
+        ok = mbar_wait(smem_u32(&mb_d[st ^ 1]), ((c - 1) >> 1) & 1, kWaitBudget) && ok;
         fence_after_sync();
         emit_output(c - 1);
       }
-      float ss = 0.0f;
-      if (p.norm) {
-#pragma unroll
-        for (int box = 0; box < 2; ++box)
-#pragma unroll
-          for (int q16 = 0; q16 < 8; ++q16) {
-            float v[8];
-            ld_bf16x8(sst + ScanSmem::A1 + box * 16384 + 8192 + row * 128 +
-                          ((q16 ^ (row & 7)) << 4), v);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
-          }
-      }
-      const float qn = p.norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
       ok = mbar_wait(smem_u32(&mb_a), c & 1, kWaitBudget) && ok;
       fence_after_sync();
-      {
-        float qa[32], qb[32];
-        tmem_ld32(tm_d1 + lane_addr + hf * 32, qa);
-        tmem_ld32(tm_d1 + lane_addr + 64 + hf * 32, qb);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) qs_prev[e] = qa[e] + qb[e];
-      }
-      fo_prev = p.scale * __expf(gam[row]) * qn;  // consumed by emit_output(c) next time
-      ok = mbar_wait(smem_u32(&mb_p), c & 1, kWaitBudget) && ok;
-      fence_after_sync();
-      float qk[32];
-      tmem_ld32(tm_dp + lane_addr + hf * 32, qk);
+      float qa[16], qb[16];
+      tmem_ld16(tm_d1 + lane_addr + cg * 16, qa);
+      tmem_ld16(tm_d1 + lane_addr + 64 + cg * 16, qb);
       tmem_ld_wait();
-      const float gi = gam[row], fi = p.scale * qn;
 #pragma unroll
-      for (int e = 0; e < 32; e += 8) {
-        float v[8];
-#pragma unroll
-        for (int x = 0; x < 8; ++x) {
-          const int jj = hf * 32 + e + x;
-          v[x] = jj <= row ? fi * kn[jj] * __expf(gi - gam[jj]) * qk[e + x] : 0.0f;
-        }
-        const uint32_t off = swz128_offset(64 + row, hf * 32 + e, 16384);
-        st_split8(sm + ScanSmem::PH + off, sm + ScanSmem::PL + off, v);
-      }
-      fence_proxy_async();
+      for (int e = 0; e < 16; ++e) qs_prev[e] = qa[e] + qb[e];
+      fo_prev = F[row];  // consumed by emit_output(c) next time
     }
-    fence_before_sync();
-    if (!__syncthreads_and(ok)) break;
-    fence_after_sync();
-    if (tid == 0) {
-      // D2 = K^T [U'_hi | U'_lo]  (M = 128 dk, N = 128, K = 64 tokens; A = K tile MN-major)
-      const uint32_t id2 = idesc_bf16_f32(128, 128, true, true);
-#pragma unroll
-      for (int kk = 0; kk < kC; kk += 16)
-        mma_bf16(tm_d2, desc_sw128(sb + ScanSmem::K + (kk / 8) * 1024, 8192, 1024),
-                 desc_sw128(base + ScanSmem::U2H + (kk / 8) * 1024, 8192, 1024), id2, kk > 0);
-      mma_commit(smem_u32(&mb_c));
-    }
-    __syncwarp();
-    ok = mbar_wait(smem_u32(&mb_c), c & 1, kWaitBudget) && ok;
-    fence_after_sync();
-    {
+    if (!issuer_warp) {
       // S = e^{gam_L} S + D2  (f32, registers), new S^T hi / lo images.
-      const float dL = __expf(gam[kC - 1]);
-      float da[32], db[32];
-      tmem_ld32(tm_d2 + lane_addr + hf * 32, da);
-      tmem_ld32(tm_d2 + lane_addr + 64 + hf * 32, db);
+      ok = mbar_wait(smem_u32(&mb_c), c & 1, kWaitBudget) && ok;
+      fence_after_sync();
+      const float dL = F[128];
+      float da[16], db[16];
+      tmem_ld16(tm_d2 + lane_addr + cg * 16, da);
+      tmem_ld16(tm_d2 + lane_addr + 64 + cg * 16, db);
       tmem_ld_wait();
 #pragma unroll
-      for (int e = 0; e < 32; ++e) S[e] = fmaf(dL, S[e], da[e] + db[e]);
+      for (int e = 0; e < 16; ++e) S[e] = fmaf(dL, S[e], da[e] + db[e]);
+      write_s();
+      fence_proxy_async();
     }
-    write_s();
-    fence_proxy_async();
     fence_before_sync();
     if (!__syncthreads_and(ok)) break;
     fence_after_sync();
-    // Every reader of this stage (D1, Dp, D2 and the generic reads) is done:
-    // refill it with chunk c + 2.
-    if (tid == 0 && c + 2 < nchunks) {
-      fence_proxy_async();
-      issue_load(c + 2);
-      issued_ld = c + 3;
+    // Every reader of this stage but D3 (P) is done: once D3 is, refill the
+    // stage with chunk c + 2.
+    if (issuer && c + 2 < nchunks) {
+      if (mbar_wait(smem_u32(&mb_d[st]), (c >> 1) & 1, kWaitBudget)) {
+        fence_proxy_async();
+        issue_load(c + 2);
+        issued_ld = c + 3;
+      } else {
+        ok = false;
+      }
     }
   }
-  if (c == nchunks) {
-    if (tid == 0) issue_d3();  // the last chunk's P U
-    if (!u_warp) {
-      ok = mbar_wait(smem_u32(&mb_d), (nchunks - 1) & 1, kWaitBudget) && ok;
-      fence_after_sync();
-      emit_output(nchunks - 1);
-    }
+  if (c == nchunks && !u_warp && !issuer_warp) {  // the last chunk's output
+    ok = mbar_wait(smem_u32(&mb_d[(nchunks - 1) & 1]), ((nchunks - 1) >> 1) & 1, kWaitBudget) &&
+         ok;
+    fence_after_sync();
+    emit_output(nchunks - 1);
   }
   ok = __syncthreads_and(ok);
   if (c < nchunks || !ok) {
     // A wait ran out: report; let in-flight MMAs and loads finish (bounded); free TMEM.
-    if (tid == 0) {
+    if (issuer) {
       atomicOr(p.status, kStatusTimeout);
       if (last_mma >= 0) {
         mma_commit(smem_u32(&mb_e));
@@ -889,8 +898,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
     if (warp == 0) tmem_dealloc(tmem, 512);
     return;
   }
+  if (!issuer_warp) {
 #pragma unroll
-  for (int e = 0; e < 32; ++e) pool[(int64_t)(slice * 64 + hf * 32 + e) * kD + dk] = S[e];
+    for (int e = 0; e < 16; ++e) pool[(int64_t)(slice * 64 + cg * 16 + e) * kD + dk] = S[e];
+  }
   fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 512);
@@ -958,8 +969,8 @@ cudaError_t launch_chunked(const ChunkedLaunch& c, cudaStream_t s) {
   uint8_t* ws = static_cast<uint8_t*>(c.workspace);
   const int64_t nch = max_chunks(p.T, p.N);
   if (nch > 0x7fffffff || p.Hv > 65535) return cudaErrorInvalidConfiguration;
-  chunk_prep_kernel<<<dim3(static_cast<unsigned>(nch), p.Hv), kThreads, PrepSmem::BYTES + 1024,
-                      s>>>(tk, tv, p, ws);
+  chunk_prep_kernel<<<dim3(static_cast<unsigned>(nch), p.Hv), kPrepThreads,
+                      PrepSmem::BYTES + 1024, s>>>(tq, tk, tv, p, ws);
   note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
