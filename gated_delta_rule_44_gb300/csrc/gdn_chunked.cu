@@ -18,7 +18,8 @@
 //
 // Precision.  q, k, v are exact bf16 inputs.  Every operand the kernels compute
 // (T, S, U, U', P) enters the tensor core as a pair of bf16 values hi + lo
-// with hi = bf16(x), lo = bf16(x - hi), and products use hi*y + lo*y (or
+// with hi = x rounded to 8 significant bits (a bf16 value), lo = bf16(x - hi),
+// and products use hi*y + lo*y (or
 // hi*hi + hi*lo + lo*hi): about 16 significant bits, so the result tracks the
 // f32 recurrence instead of picking up one bf16 rounding per step.  Ut is kept
 // in f32, W as one bf16 value (its error reaches the output only through the
@@ -36,10 +37,10 @@
 //     shared-memory images the second kernel copies, Ut (f32) and the row
 //     factors fo = scale qn e^gam, fu = kn e^{gam_L - gam}, e^{gam_L}.
 //  2. chunk_scan (one CTA per (sequence, value head, 64-column slice of Dv), its
-//     chunks in order; TMA double-buffers W, Q, P, K and the factors).  Per
-//     chunk, the serial path is D1 -> U -> D2 -> S:
+//     chunks in order; TMA double-buffers W, Q, K and the factors, and P).
+//     Per chunk, the serial path is D1 -> U' -> D2 -> S:
 //        D1 = [W; Q] [S_hi | S_lo]^T  (M = 128: rows 0..63 W S^T, 64..127 Q S^T)
-//        U warps: U = Ut - W S^T, U' = diag(fu) U            (hi + lo images)
+//        U warps: U = Ut - W S^T; U' = diag(fu) U images, then U images (hi + lo)
 //        D2 = K^T [U'_hi | U'_lo]    (M = 128 dk rows: the state increment)
 //        D3 = [*; P_hi] U + [*; P_lo] U   (rows 64..127: P U; rows 0..63 unused)
 //        all warps: S = e^{gam_L} S + D2 in f32 registers; S^T hi + lo images
@@ -100,16 +101,27 @@ __device__ __forceinline__ void st_bf16x8(void* p, const float* v) {
                                             pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
 }
 
-// hi = bf16(v), lo = bf16(v - hi) for 8 values, each into one 16-byte chunk.
+// x rounded to nearest with 8 significant bits (Veltkamp's splitting with the
+// factor 2^16 + 1), so exactly a bf16 value; x - hi is exact in f32.  Plain
+// f32 arithmetic: it runs on the FMA pipe instead of the (quarter-rate)
+// conversion unit.  Valid for |x| < FLT_MAX / 65537.
+__device__ __forceinline__ float split_hi(float x) {
+  const float c = __fmul_rn(x, 65537.0f);
+  return __fsub_rn(c, __fsub_rn(c, x));
+}
+
+// hi = x rounded to 8 significant bits, lo = bf16(x - hi) for 8 values, each
+// into one 16-byte chunk: hi + lo carries about 16 significant bits of x.
 __device__ __forceinline__ void st_split8(void* hi, void* lo, const float* v) {
-  float h[8], l[8];
+  uint32_t hw[4], lw[4];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    h[e] = __bfloat162float(__float2bfloat16_rn(v[e]));
-    l[e] = v[e] - h[e];
+  for (int e = 0; e < 8; e += 2) {
+    const float h0 = split_hi(v[e]), h1 = split_hi(v[e + 1]);
+    hw[e / 2] = __byte_perm(__float_as_uint(h0), __float_as_uint(h1), 0x7632);  // upper halves
+    lw[e / 2] = pack_bf16x2(__fsub_rn(v[e], h0), __fsub_rn(v[e + 1], h1));
   }
-  st_bf16x8(hi, h);
-  st_bf16x8(lo, l);
+  *reinterpret_cast<uint4*>(hi) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  *reinterpret_cast<uint4*>(lo) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
 }
 
 __device__ __forceinline__ void ld_bf16x8(const void* p, float* v) {
@@ -544,43 +556,44 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
 //   D3 = [*; P_hi] [U_hi | U_lo] + [*; P_lo] [U_hi | U_lo]   rows 64..127 P U
 // Each result's two column halves are added in the epilogue.  The A tiles of
 // D3 are 128-row windows that end with P_hi (P_lo): their first 64 rows are
-// whatever precedes it in the stage and only fill TMEM lanes 0..63, which
+// whatever precedes it in shared memory and only fill TMEM lanes 0..63, which
 // nobody reads.
 struct ScanSmem {
   // pipeline stage (x2)
   static constexpr uint32_t A1 = 0;         // [W box0 | Q box0 | W box1 | Q box1], 32 KB
-  static constexpr uint32_t PH = 32768;     // P hi image, 8 KB
-  static constexpr uint32_t PL = 40960;     // P lo image, 8 KB
-  static constexpr uint32_t K = 49152;      // [K box0 | K box1], 16 KB
-  static constexpr uint32_t F = 65536;      // fo[64], fu[64], e^{gam_L}
-  static constexpr uint32_t STAGE = 66560;  // 65 KB (1 KB aligned)
-  static constexpr uint32_t TX = 32768 + 16384 + 16384 + kBlobFBytes;
+  static constexpr uint32_t K = 32768;      // [K box0 | K box1], 16 KB
+  static constexpr uint32_t F = 49152;      // fo[64], fu[64], e^{gam_L}
+  static constexpr uint32_t STAGE = 50176;  // 49 KB (1 KB aligned)
+  static constexpr uint32_t TX = 32768 + 16384 + kBlobFBytes;
   // single buffers
-  static constexpr uint32_t UT = 2 * STAGE;   // Ut slice f32 [64 tokens][64] (ut_offset), 16 KB
-  static constexpr uint32_t SH = UT + 16384;  // S^T hi image [128 dk x 64 dv], 16 KB, then
-  static constexpr uint32_t SL = SH + 16384;  //   S^T lo: one MN-major B operand of N = 128
-  static constexpr uint32_t UH = SL + 16384;  // U hi image [64 tok x 64 dv], 8 KB, then U lo
+  static constexpr uint32_t UT = 2 * STAGE;    // Ut slice f32 [64 tokens][64] (ut_offset), 16 KB
+  static constexpr uint32_t SH = UT + 16384;   // S^T hi image [128 dk x 64 dv], 16 KB, then
+  static constexpr uint32_t SL = SH + 16384;   //   S^T lo: one MN-major B operand of N = 128
+  static constexpr uint32_t UH = SL + 16384;   // U hi image [64 tok x 64 dv], 8 KB, then U lo
   static constexpr uint32_t UL = UH + 8192;
-  static constexpr uint32_t U2H = UL + 8192;  // U' hi, then U' lo
+  static constexpr uint32_t P0 = UL + 8192;    // P of even chunks: hi image, lo image (8 KB each)
+  static constexpr uint32_t U2H = P0 + 16384;  // U' hi, then U' lo
   static constexpr uint32_t U2L = U2H + 8192;
-  static constexpr uint32_t BYTES = U2L + 8192;
+  static constexpr uint32_t P1 = U2L + 8192;   // P of odd chunks
+  static constexpr uint32_t BYTES = P1 + 16384;
 };
-
-static_assert(ScanSmem::PL == ScanSmem::PH + 8192 && ScanSmem::PH == ScanSmem::A1 + 32768,
-              "the D3 A windows [Q box1; P_hi] and [P_hi; P_lo] must be contiguous");
+// D3's first A window for a P buffer starts 8 KB before it.
+static_assert(ScanSmem::P0 == ScanSmem::UL + 8192 && ScanSmem::P1 == ScanSmem::U2L + 8192,
+              "each P buffer must follow 8 KB of other tiles (the unused rows of D3's A)");
 static_assert(ScanSmem::BYTES + 1024 <= 232448, "shared memory per CTA");
 static_assert(PrepSmem::BYTES + 1024 <= 116736 - 2048, "two chunk_prep CTAs per SM");
 
 constexpr int kScanWorkers = 512;               // warps 0..15
 constexpr int kScanThreads = kScanWorkers + 32;  // + the issuing warp
-constexpr int kBarU = 1;                         // named barrier: U warps + issuer
+constexpr int kBarU1 = 1;  // named barriers of the U warps and the issuer: U' images ready,
+constexpr int kBarU2 = 2;  //   U images ready
 
 __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const RecurLaunch p, const uint8_t* __restrict__ ws, int n_chunks_max) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = aligned_smem(smem_raw);
-  __shared__ uint64_t mb_ld[2], mb_ut, mb_a, mb_c, mb_d[2], mb_e;
+  __shared__ uint64_t mb_ld[2], mb_p[2], mb_ut, mb_a, mb_c, mb_d[2], mb_e;
   __shared__ uint32_t tslot;
   __shared__ int s_base, s_bad;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -629,6 +642,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
   if (tid == 0) {
     mbar_init(smem_u32(&mb_ld[0]), 1);
     mbar_init(smem_u32(&mb_ld[1]), 1);
+    mbar_init(smem_u32(&mb_p[0]), 1);
+    mbar_init(smem_u32(&mb_p[1]), 1);
     mbar_init(smem_u32(&mb_ut), 1);
     mbar_init(smem_u32(&mb_a), 1);
     mbar_init(smem_u32(&mb_c), 1);
@@ -646,7 +661,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
   auto blob_of = [&](int c) {
     return ws + ((int64_t)(gc0 + c) * p.Hv + h) * kBlobBytes;
   };
-  // Loads W, Q, P, K and the factors of chunk c into stage c & 1 (issuer only).
+  // Loads W, Q, K and the factors of chunk c into stage c & 1 (issuer only).
   auto issue_load = [&](int c) {
     const uint32_t sb = base + (c & 1) * ScanSmem::STAGE;
     const uint32_t mb = smem_u32(&mb_ld[c & 1]);
@@ -655,12 +670,16 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
     mbar_expect_tx(mb, ScanSmem::TX);
     bulk_g2s(sb + ScanSmem::A1, blob + kBlobW, 8192, mb);
     bulk_g2s(sb + ScanSmem::A1 + 16384, blob + kBlobW + 8192, 8192, mb);
-    bulk_g2s(sb + ScanSmem::PH, blob + kBlobP, 16384, mb);
     bulk_g2s(sb + ScanSmem::F, blob + kBlobF, kBlobFBytes, mb);
     tma_load_3d(sb + ScanSmem::A1 + 8192, &tm_q, mb, 0, hk, t0);
     tma_load_3d(sb + ScanSmem::A1 + 24576, &tm_q, mb, 64, hk, t0);
     tma_load_3d(sb + ScanSmem::K, &tm_k, mb, 0, hk, t0);
     tma_load_3d(sb + ScanSmem::K + 8192, &tm_k, mb, 64, hk, t0);
+  };
+  auto issue_p = [&](int c) {  // P of chunk c into P buffer c & 1 (issuer only)
+    const uint32_t mb = smem_u32(&mb_p[c & 1]);
+    mbar_expect_tx(mb, 16384);
+    bulk_g2s(base + ((c & 1) ? ScanSmem::P1 : ScanSmem::P0), blob_of(c) + kBlobP, 16384, mb);
   };
   auto issue_ut = [&](int c) {  // issuer only
     const uint32_t mb = smem_u32(&mb_ut);
@@ -668,13 +687,15 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
     bulk_g2s(base + ScanSmem::UT, blob_of(c) + kBlobU + slice * 16384, 16384, mb);
   };
   // Loads issued so far (issuer), for the error path.
-  int issued_ld = 0, issued_ut = 0;
+  int issued_ld = 0, issued_ut = 0, issued_p = 0;
   if (issuer) {
     issue_load(0);
-    issued_ld = 1;
+    issue_p(0);
+    issued_ld = issued_p = 1;
     if (nchunks > 1) {
       issue_load(1);
-      issued_ld = 2;
+      issue_p(1);
+      issued_ld = issued_p = 2;
     }
     issue_ut(0);
     issued_ut = 1;
@@ -753,9 +774,19 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
                    desc_sw128(base + ScanSmem::SH + (kk / 8) * 1024, 16384, 1024), id1, kk > 0);
         mma_commit(smem_u32(&mb_a));
         last_mma = c;
+        // P buffer (c + 1) & 1 is free once D3 of chunk c - 1 is done.
+        if (c >= 1 && c + 1 < nchunks) {
+          if (mbar_wait(smem_u32(&mb_d[st ^ 1]), ((c - 1) >> 1) & 1, kWaitBudget)) {
+            fence_proxy_async();
+            issue_p(c + 1);
+            issued_p = c + 2;
+          } else {
+            ok = false;
+          }
+        }
       }
       __syncwarp();
-      named_bar(kBarU, 256 + 32);  // U, U' images written, K tail zeroed, Ut consumed
+      named_bar(kBarU1, 256 + 32);  // U' images written, K tail zeroed, Ut consumed
       if (issuer) {
         if (ok) {
           fence_after_sync();
@@ -767,23 +798,31 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
                      desc_sw128(base + ScanSmem::U2H + (kk / 8) * 1024, 8192, 1024), id2,
                      kk > 0);
           mma_commit(smem_u32(&mb_c));
-          // D3 = [*; P_hi] [U_hi | U_lo] + [*; P_lo] [U_hi | U_lo]  (M = 128, N = 128, K = 64)
-          const uint32_t id3 = idesc_bf16_f32(128, 128, false, true);
-#pragma unroll
-          for (int part = 0; part < 2; ++part)
-#pragma unroll
-            for (int kk = 0; kk < kC; kk += 16)
-              mma_bf16(tm_d3 + st * 128,
-                       desc_sw128(sb + (part ? ScanSmem::PH : ScanSmem::A1 + 24576) + kk * 2, 16,
-                                  1024),
-                       desc_sw128(base + ScanSmem::UH + (kk / 8) * 1024, 8192, 1024), id3,
-                       part > 0 || kk > 0);
-          mma_commit(smem_u32(&mb_d[st]));
         }
         if (c + 1 < nchunks) {
           fence_proxy_async();
           issue_ut(c + 1);
           issued_ut = c + 2;
+        }
+      }
+      __syncwarp();
+      named_bar(kBarU2, 256 + 32);  // U images written
+      if (issuer) {
+        ok = mbar_wait(smem_u32(&mb_p[st]), (c >> 1) & 1, kWaitBudget) && ok;
+        if (ok) {
+          fence_after_sync();
+          // D3 = [*; P_hi] [U_hi | U_lo] + [*; P_lo] [U_hi | U_lo]  (M = 128, N = 128, K = 64):
+          // 128-row A windows that end with P_hi, then with P_lo.
+          const uint32_t id3 = idesc_bf16_f32(128, 128, false, true);
+          const uint32_t pb = base + (st ? ScanSmem::P1 : ScanSmem::P0);
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int kk = 0; kk < kC; kk += 16)
+              mma_bf16(tm_d3 + st * 128, desc_sw128(pb + part * 8192 - 8192 + kk * 2, 16, 1024),
+                       desc_sw128(base + ScanSmem::UH + (kk / 8) * 1024, 8192, 1024), id3,
+                       part > 0 || kk > 0);
+          mma_commit(smem_u32(&mb_d[st]));
         }
       }
     } else if (u_warp) {
@@ -815,19 +854,26 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
         u[e + 2] = f.z - (wa[e + 2] + wb[e + 2]);
         u[e + 3] = f.w - (wa[e + 3] + wb[e + 3]);
       }
-      if (c > 0) ok = mbar_wait(smem_u32(&mb_d[st ^ 1]), ((c - 1) >> 1) & 1, kWaitBudget) && ok;
 #pragma unroll
-      for (int e = 0; e < 16; e += 8) {
+      for (int e = 0; e < 16; e += 8) {  // U' first: D2 waits for it
         float u2[8];
 #pragma unroll
         for (int x = 0; x < 8; ++x) u2[x] = fu * u[e + x];
         const uint32_t off = swz128_offset(row, cg * 16 + e, 8192);
-        st_split8(sm + ScanSmem::UH + off, sm + ScanSmem::UL + off, u + e);
         st_split8(sm + ScanSmem::U2H + off, sm + ScanSmem::U2L + off, u2);
       }
       fence_proxy_async();
       fence_before_sync();
-      named_bar(kBarU, 256 + 32);
+      named_bar(kBarU1, 256 + 32);
+      // The U images were read by D3 of the previous chunk.
+      if (c > 0) ok = mbar_wait(smem_u32(&mb_d[st ^ 1]), ((c - 1) >> 1) & 1, kWaitBudget) && ok;
+#pragma unroll
+      for (int e = 0; e < 16; e += 8) {
+        const uint32_t off = swz128_offset(row, cg * 16 + e, 8192);
+        st_split8(sm + ScanSmem::UH + off, sm + ScanSmem::UL + off, u + e);
+      }
+      fence_proxy_async();
+      named_bar(kBarU2, 256 + 32);
     } else {
       // The previous chunk's output (needs its D3), then Q S^T of this chunk.
       if (c > 0) {
@@ -862,16 +908,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
     fence_before_sync();
     if (!__syncthreads_and(ok)) break;
     fence_after_sync();
-    // Every reader of this stage but D3 (P) is done: once D3 is, refill the
-    // stage with chunk c + 2.
+    // Every reader of this stage (D1, D2 and the factor reads) is done:
+    // refill it with chunk c + 2.
     if (issuer && c + 2 < nchunks) {
-      if (mbar_wait(smem_u32(&mb_d[st]), (c >> 1) & 1, kWaitBudget)) {
-        fence_proxy_async();
-        issue_load(c + 2);
-        issued_ld = c + 3;
-      } else {
-        ok = false;
-      }
+      fence_proxy_async();
+      issue_load(c + 2);
+      issued_ld = c + 3;
     }
   }
   if (c == nchunks && !u_warp && !issuer_warp) {  // the last chunk's output
@@ -892,6 +934,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
       for (int k = c; k < issued_ld; ++k)
         mbar_wait(smem_u32(&mb_ld[k & 1]), (k >> 1) & 1, kWaitBudget);
       for (int k = c; k < issued_ut; ++k) mbar_wait(smem_u32(&mb_ut), k & 1, kWaitBudget);
+      for (int k = c; k < issued_p; ++k)
+        mbar_wait(smem_u32(&mb_p[k & 1]), (k >> 1) & 1, kWaitBudget);
     }
     fence_before_sync();
     __syncthreads();
