@@ -549,7 +549,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
 //   U warps (q = 0, 1):       token rows 0..63 of W S^T -> U, U'
 //   output warps (q = 2, 3):  token rows 0..63 of Q S^T and P U -> outputs
 //   warps 0..15:             dk rows 0..127 of the state, 16 columns each
-//   warp 16 (lane 0):        every MMA, TMA and bulk copy
+//   warp 16 (lane 0):        every MMA and the P, Ut copies
+//   thread 64 (output warp): the stage copies (W, Q, K, factors)
 // MMAs, hi and lo operands side by side along N = 128:
 //   D1 = [W; Q] [S_hi | S_lo]^T      rows 0..63 W S^T, 64..127 Q S^T
 //   D2 = K^T [U'_hi | U'_lo]         rows = dk
@@ -600,6 +601,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
   const int quad = warp & 3, cg = warp >> 2;  // TMEM lane quadrant, 16-column group
   const bool issuer_warp = warp == 16;
   const bool issuer = tid == kScanWorkers;
+  const bool loader = tid == 64;
   const int slice = blockIdx.x & 1;
   const int sh = blockIdx.x >> 1;
   const int h = sh % p.Hv, s = sh / p.Hv;
@@ -661,7 +663,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
   auto blob_of = [&](int c) {
     return ws + ((int64_t)(gc0 + c) * p.Hv + h) * kBlobBytes;
   };
-  // Loads W, Q, K and the factors of chunk c into stage c & 1 (issuer only).
+  // Loads W, Q, K and the factors of chunk c into stage c & 1 (loader only).
   auto issue_load = [&](int c) {
     const uint32_t sb = base + (c & 1) * ScanSmem::STAGE;
     const uint32_t mb = smem_u32(&mb_ld[c & 1]);
@@ -686,16 +688,22 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
     mbar_expect_tx(mb, 16384);
     bulk_g2s(base + ScanSmem::UT, blob_of(c) + kBlobU + slice * 16384, 16384, mb);
   };
-  // Loads issued so far (issuer), for the error path.
+  // Copies issued so far (loader: stages; issuer: P, Ut), for the error path.
   int issued_ld = 0, issued_ut = 0, issued_p = 0;
-  if (issuer) {
+  if (loader) {
     issue_load(0);
-    issue_p(0);
-    issued_ld = issued_p = 1;
+    issued_ld = 1;
     if (nchunks > 1) {
       issue_load(1);
+      issued_ld = 2;
+    }
+  }
+  if (issuer) {
+    issue_p(0);
+    issued_p = 1;
+    if (nchunks > 1) {
       issue_p(1);
-      issued_ld = issued_p = 2;
+      issued_p = 2;
     }
     issue_ut(0);
     issued_ut = 1;
@@ -910,7 +918,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
     fence_after_sync();
     // Every reader of this stage (D1, D2 and the factor reads) is done:
     // refill it with chunk c + 2.
-    if (issuer && c + 2 < nchunks) {
+    if (loader && c + 2 < nchunks) {
       fence_proxy_async();
       issue_load(c + 2);
       issued_ld = c + 3;
@@ -931,11 +939,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
         mma_commit(smem_u32(&mb_e));
         mbar_wait(smem_u32(&mb_e), 0, kWaitBudget);
       }
-      for (int k = c; k < issued_ld; ++k)
-        mbar_wait(smem_u32(&mb_ld[k & 1]), (k >> 1) & 1, kWaitBudget);
       for (int k = c; k < issued_ut; ++k) mbar_wait(smem_u32(&mb_ut), k & 1, kWaitBudget);
       for (int k = c; k < issued_p; ++k)
         mbar_wait(smem_u32(&mb_p[k & 1]), (k >> 1) & 1, kWaitBudget);
+    }
+    if (loader) {
+      for (int k = c; k < issued_ld; ++k)
+        mbar_wait(smem_u32(&mb_ld[k & 1]), (k >> 1) & 1, kWaitBudget);
     }
     fence_before_sync();
     __syncthreads();

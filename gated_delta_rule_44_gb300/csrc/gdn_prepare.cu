@@ -46,6 +46,17 @@ __device__ __forceinline__ float softplus_f(float x) {
   return log1pf(expf(x));
 }
 
+// 1 / y: the hardware's approximate reciprocal refined by one Newton-Raphson
+// step, r <- r + r (1 - y r), which roughly doubles its correct bits (to
+// within about one ulp of the correctly rounded value).  A lone approximate
+// reciprocal is biased enough to shift bf16 roundings of whole tensors the
+// same way.  For finite y >= 1.
+__device__ __forceinline__ float recip_nr(float y) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
+  return fmaf(r, fmaf(-y, r, 1.0f), r);
+}
+
 template <typename TA>
 struct Act;
 
@@ -183,9 +194,10 @@ __global__ void __launch_bounds__(kThreads, 4) prepare_kernel(const PrepareLaunc
 #pragma unroll
       for (int j = 0; j < W; ++j) acc = fmaf(win[j][i], wt[i][j], acc);
       acc = fmaf(xt[i], wt[i][W], acc);
-      // silu(acc) = acc * sigmoid(acc); e^{-acc} may overflow to inf, whose
-      // reciprocal is 0, so no branch is needed.
-      y[i] = acc * __frcp_rn(1.0f + __expf(-acc));
+      // silu(acc) = acc / (1 + e^{-acc}).  e^{-acc} is capped at e^80 (the
+      // result is then below 1e-32 in magnitude either way) so that the
+      // reciprocal's operand stays finite.
+      y[i] = acc * recip_nr(1.0f + __expf(fminf(-acc, 80.0f)));
       ss = fmaf(y[i], y[i], ss);
     }
     if (p.norm) {
@@ -427,7 +439,7 @@ cudaError_t launch_k(const PrepareLaunch& p, cudaStream_t s) {
   const int chan_blocks = (C + kThreads * V - 1) / (kThreads * V);
   // Tiles of at least K-1 tokens (tail ownership); shrink them while the grid
   // is short of ~8 CTAs per SM.
-  int tile = 16;
+  int tile = 32;
   while (tile > 2 && (int64_t)((p.T + tile - 1) / tile) * chan_blocks < 8 * 152) tile >>= 1;
   if (tile < KW - 1) tile = KW - 1;  // >= K-1 for the tail ownership rule (K <= 8: <= 16)
   dim3 grid((p.T + tile - 1) / tile, chan_blocks + 1);
