@@ -44,8 +44,9 @@
 //        D2 = K^T [U'_hi | U'_lo]    (M = 128 dk rows: the state increment)
 //        D3 = [*; P_hi] U + [*; P_lo] U   (rows 64..127: P U; rows 0..63 unused)
 //        all warps: S = e^{gam_L} S + D2 in f32 registers; S^T hi + lo images
-//     Output warps emit chunk c (fo Q S^T + P U) while chunk c + 1 runs; D3 is
-//     double-buffered in TMEM.  One extra warp issues every MMA and copy.
+//     D3 of chunk c runs behind D2 of chunk c + 1, and the output warps emit
+//     chunk c (fo Q S^T + P U) while chunk c + 2 runs; the U images and D3
+//     are double-buffered.  One extra warp issues every MMA.
 //
 // Partial chunks: K, Q and V rows past the chunk end are zeroed in shared
 // memory and their g, beta taken as 0, so every derived row is exactly zero.
@@ -549,52 +550,58 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
 //   U warps (q = 0, 1):       token rows 0..63 of W S^T -> U, U'
 //   output warps (q = 2, 3):  token rows 0..63 of Q S^T and P U -> outputs
 //   warps 0..15:             dk rows 0..127 of the state, 16 columns each
-//   warp 16 (lane 0):        every MMA and the P, Ut copies
-//   thread 64 (output warp): the stage copies (W, Q, K, factors)
+//   warp 16 (lane 0):        every MMA
+//   thread 64 (output warp): every copy (W, Q, K, factors; P; Ut)
 // MMAs, hi and lo operands side by side along N = 128:
 //   D1 = [W; Q] [S_hi | S_lo]^T      rows 0..63 W S^T, 64..127 Q S^T
 //   D2 = K^T [U'_hi | U'_lo]         rows = dk
-//   D3 = [*; P_hi] [U_hi | U_lo] + [*; P_lo] [U_hi | U_lo]   rows 64..127 P U
+//   D3 = [*; P_hi] [U_hi | U_lo] + [*; P_lo] [U_hi | U_lo]   rows 64..127 P U,
+//        accumulated onto [fo Q S^T | 0], which the output warps store there
 // Each result's two column halves are added in the epilogue.  The A tiles of
 // D3 are 128-row windows that end with P_hi (P_lo): their first 64 rows are
 // whatever precedes it in shared memory and only fill TMEM lanes 0..63, which
 // nobody reads.
+//
+// Per chunk c the tensor pipe runs D1(c), D2(c), D3(c - 1): D3 never delays
+// the serial path D1 -> U' -> D2 -> S.  The U and P images and the D3
+// accumulator are double-buffered by chunk parity; P of chunk c is fetched
+// while chunk c runs, chunk c's output is emitted while chunk c + 2 runs.
 struct ScanSmem {
-  // pipeline stage (x2)
+  // pipeline stage (x2): W, Q, K tiles; the stage's factors are at F0 / F1
   static constexpr uint32_t A1 = 0;         // [W box0 | Q box0 | W box1 | Q box1], 32 KB
   static constexpr uint32_t K = 32768;      // [K box0 | K box1], 16 KB
-  static constexpr uint32_t F = 49152;      // fo[64], fu[64], e^{gam_L}
-  static constexpr uint32_t STAGE = 50176;  // 49 KB (1 KB aligned)
+  static constexpr uint32_t STAGE = 49152;
   static constexpr uint32_t TX = 32768 + 16384 + kBlobFBytes;
-  // single buffers
+  // single and parity buffers (1 KB aligned operand tiles)
   static constexpr uint32_t UT = 2 * STAGE;    // Ut slice f32 [64 tokens][64] (ut_offset), 16 KB
   static constexpr uint32_t SH = UT + 16384;   // S^T hi image [128 dk x 64 dv], 16 KB, then
   static constexpr uint32_t SL = SH + 16384;   //   S^T lo: one MN-major B operand of N = 128
-  static constexpr uint32_t UH = SL + 16384;   // U hi image [64 tok x 64 dv], 8 KB, then U lo
-  static constexpr uint32_t UL = UH + 8192;
-  static constexpr uint32_t P0 = UL + 8192;    // P of even chunks: hi image, lo image (8 KB each)
-  static constexpr uint32_t U2H = P0 + 16384;  // U' hi, then U' lo
+  static constexpr uint32_t U2H = SL + 16384;  // U' hi image [64 tok x 64 dv], 8 KB, then U' lo
   static constexpr uint32_t U2L = U2H + 8192;
-  static constexpr uint32_t P1 = U2L + 8192;   // P of odd chunks
-  static constexpr uint32_t BYTES = P1 + 16384;
+  static constexpr uint32_t U0 = U2L + 8192;   // U images of even chunks: hi, then lo
+  static constexpr uint32_t P0 = U0 + 16384;   // P images of even chunks: hi, then lo
+  static constexpr uint32_t U1 = P0 + 16384;   // U images of odd chunks
+  static constexpr uint32_t P1 = U1 + 16384;   // P images of odd chunks
+  static constexpr uint32_t F0 = P1 + 16384;   // fo[64], fu[64], e^{gam_L} of stage 0, then stage 1
+  static constexpr uint32_t BYTES = F0 + 2 * kBlobFBytes;
 };
-// D3's first A window for a P buffer starts 8 KB before it.
-static_assert(ScanSmem::P0 == ScanSmem::UL + 8192 && ScanSmem::P1 == ScanSmem::U2L + 8192,
-              "each P buffer must follow 8 KB of other tiles (the unused rows of D3's A)");
+// D3's first A window starts 8 KB before P_hi (the lo half of the U images
+// before it), its second at P_hi.
+static_assert(ScanSmem::P0 == ScanSmem::U0 + 16384 && ScanSmem::P1 == ScanSmem::U1 + 16384,
+              "each P buffer must follow 8 KB of other tiles");
 static_assert(ScanSmem::BYTES + 1024 <= 232448, "shared memory per CTA");
 static_assert(PrepSmem::BYTES + 1024 <= 116736 - 2048, "two chunk_prep CTAs per SM");
 
 constexpr int kScanWorkers = 512;               // warps 0..15
 constexpr int kScanThreads = kScanWorkers + 32;  // + the issuing warp
-constexpr int kBarU1 = 1;  // named barriers of the U warps and the issuer: U' images ready,
-constexpr int kBarU2 = 2;  //   U images ready
+constexpr int kBarU = 1;  // named barrier of the U warps and the issuer: U' images ready
 
 __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const RecurLaunch p, const uint8_t* __restrict__ ws, int n_chunks_max) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = aligned_smem(smem_raw);
-  __shared__ uint64_t mb_ld[2], mb_p[2], mb_ut, mb_a, mb_c, mb_d[2], mb_e;
+  __shared__ uint64_t mb_ld[2], mb_p[2], mb_ut, mb_utfree, mb_a, mb_c, mb_d[2], mb_e;
   __shared__ uint32_t tslot;
   __shared__ int s_base, s_bad;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -647,6 +654,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
     mbar_init(smem_u32(&mb_p[0]), 1);
     mbar_init(smem_u32(&mb_p[1]), 1);
     mbar_init(smem_u32(&mb_ut), 1);
+    mbar_init(smem_u32(&mb_utfree), 8);  // one arrival per U warp
     mbar_init(smem_u32(&mb_a), 1);
     mbar_init(smem_u32(&mb_c), 1);
     mbar_init(smem_u32(&mb_d[0]), 1);
@@ -672,41 +680,55 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
     mbar_expect_tx(mb, ScanSmem::TX);
     bulk_g2s(sb + ScanSmem::A1, blob + kBlobW, 8192, mb);
     bulk_g2s(sb + ScanSmem::A1 + 16384, blob + kBlobW + 8192, 8192, mb);
-    bulk_g2s(sb + ScanSmem::F, blob + kBlobF, kBlobFBytes, mb);
+    bulk_g2s(base + ScanSmem::F0 + (c & 1) * kBlobFBytes, blob + kBlobF, kBlobFBytes, mb);
     tma_load_3d(sb + ScanSmem::A1 + 8192, &tm_q, mb, 0, hk, t0);
     tma_load_3d(sb + ScanSmem::A1 + 24576, &tm_q, mb, 64, hk, t0);
     tma_load_3d(sb + ScanSmem::K, &tm_k, mb, 0, hk, t0);
     tma_load_3d(sb + ScanSmem::K + 8192, &tm_k, mb, 64, hk, t0);
   };
-  auto issue_p = [&](int c) {  // P of chunk c into P buffer c & 1 (issuer only)
+  auto issue_p = [&](int c) {  // P of chunk c into P buffer c & 1 (loader only)
     const uint32_t mb = smem_u32(&mb_p[c & 1]);
     mbar_expect_tx(mb, 16384);
     bulk_g2s(base + ((c & 1) ? ScanSmem::P1 : ScanSmem::P0), blob_of(c) + kBlobP, 16384, mb);
   };
-  auto issue_ut = [&](int c) {  // issuer only
+  auto issue_ut = [&](int c) {  // loader only
     const uint32_t mb = smem_u32(&mb_ut);
     mbar_expect_tx(mb, 16384);
     bulk_g2s(base + ScanSmem::UT, blob_of(c) + kBlobU + slice * 16384, 16384, mb);
   };
-  // Copies issued so far (loader: stages; issuer: P, Ut), for the error path.
+  // D3 of chunk cc += [*; P_hi] [U_hi | U_lo] + [*; P_lo] [U_hi | U_lo]  (M = 128,
+  // N = 128, K = 64) from U buffer cc & 1 onto TMEM buffer cc & 1, which holds
+  // [fo Q S^T | 0] of that chunk (issuer only).
+  auto issue_d3 = [&](int cc) {
+    if (!mbar_wait(smem_u32(&mb_p[cc & 1]), (cc >> 1) & 1, kWaitBudget)) return false;
+    fence_after_sync();
+    const uint32_t id3 = idesc_bf16_f32(128, 128, false, true);
+    const uint32_t ub = base + ((cc & 1) ? ScanSmem::U1 : ScanSmem::U0);
+    const uint32_t pb = base + ((cc & 1) ? ScanSmem::P1 : ScanSmem::P0);
+#pragma unroll
+    for (int part = 0; part < 2; ++part)
+#pragma unroll
+      for (int kk = 0; kk < kC; kk += 16)
+        mma_bf16(tmem + 256 + (cc & 1) * 128, desc_sw128(pb + part * 8192 - 8192 + kk * 2, 16, 1024),
+                 desc_sw128(ub + (kk / 8) * 1024, 8192, 1024), id3, true);
+    mma_commit(smem_u32(&mb_d[cc & 1]));
+    return true;
+  };
+  // Copies issued so far (loader), for the error path.  Write-after-read
+  // hazards on the destinations are ordered by the mbarrier and barrier waits
+  // before each copy; writers of generic data that a copy overwrites (the
+  // K-tail zeros) fence their own stores.
   int issued_ld = 0, issued_ut = 0, issued_p = 0;
   if (loader) {
+    issue_ut(0);
     issue_load(0);
-    issued_ld = 1;
+    issue_p(0);
+    issued_ut = issued_ld = issued_p = 1;
     if (nchunks > 1) {
       issue_load(1);
-      issued_ld = 2;
-    }
-  }
-  if (issuer) {
-    issue_p(0);
-    issued_p = 1;
-    if (nchunks > 1) {
       issue_p(1);
-      issued_p = 2;
+      issued_ld = issued_p = 2;
     }
-    issue_ut(0);
-    issued_ut = 1;
   }
 
   // State: worker (quad, cg, lane) owns dk = 32 quad + lane and dv columns
@@ -737,11 +759,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
   const uint32_t tm_d1 = tmem, tm_d2 = tmem + 128, tm_d3 = tmem + 256;  // D3: 2 x 128
   const bool u_warp = !issuer_warp && quad < 2;
   const int row = (quad & 1) * 32 + lane;  // token row of U and output warps
-  // Output warps carry the previous chunk's Q S^T and output factor.
-  float qs_prev[16];
-  float fo_prev = 0.0f;
-
-  // Output of chunk cc by the output warps: O = fo Q S^T + P U.
+  // Output of chunk cc by the output warps: O = fo Q S^T + P U, the sum of
+  // D3's two column halves.
   auto emit_output = [&](int cc) {
     const int t0 = lo + cc * kC;
     const int L = min(kC, hi - t0);
@@ -752,7 +771,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
     tmem_ld_wait();
     if (row < L) {
 #pragma unroll
-      for (int e = 0; e < 16; ++e) a[e] = fmaf(fo_prev, qs_prev[e], a[e] + b[e]);
+      for (int e = 0; e < 16; ++e) a[e] += b[e];
       __nv_bfloat16* dst = out + ((int64_t)(t0 + row) * p.Hv + h) * kD + slice * 64 + cg * 16;
       st_bf16x8(dst, a);
       st_bf16x8(dst + 8, a + 8);
@@ -768,7 +787,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
     const uint32_t sb = base + st * ScanSmem::STAGE;
     const int t0 = lo + c * kC;
     const int L = min(kC, hi - t0);
-    const float* F = reinterpret_cast<const float*>(sst + ScanSmem::F);
+    const float* F = reinterpret_cast<const float*>(sm + ScanSmem::F0 + st * kBlobFBytes);
     ok = mbar_wait(smem_u32(&mb_ld[st]), (c >> 1) & 1, kWaitBudget) && ok;
     if (issuer_warp) {
       if (issuer && ok) {
@@ -782,19 +801,9 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
                    desc_sw128(base + ScanSmem::SH + (kk / 8) * 1024, 16384, 1024), id1, kk > 0);
         mma_commit(smem_u32(&mb_a));
         last_mma = c;
-        // P buffer (c + 1) & 1 is free once D3 of chunk c - 1 is done.
-        if (c >= 1 && c + 1 < nchunks) {
-          if (mbar_wait(smem_u32(&mb_d[st ^ 1]), ((c - 1) >> 1) & 1, kWaitBudget)) {
-            fence_proxy_async();
-            issue_p(c + 1);
-            issued_p = c + 2;
-          } else {
-            ok = false;
-          }
-        }
       }
       __syncwarp();
-      named_bar(kBarU1, 256 + 32);  // U' images written, K tail zeroed, Ut consumed
+      named_bar(kBarU, 256 + 32);  // U' images written, K tail zeroed, Ut consumed
       if (issuer) {
         if (ok) {
           fence_after_sync();
@@ -807,35 +816,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
                      kk > 0);
           mma_commit(smem_u32(&mb_c));
         }
-        if (c + 1 < nchunks) {
-          fence_proxy_async();
-          issue_ut(c + 1);
-          issued_ut = c + 2;
-        }
-      }
-      __syncwarp();
-      named_bar(kBarU2, 256 + 32);  // U images written
-      if (issuer) {
-        ok = mbar_wait(smem_u32(&mb_p[st]), (c >> 1) & 1, kWaitBudget) && ok;
-        if (ok) {
-          fence_after_sync();
-          // D3 = [*; P_hi] [U_hi | U_lo] + [*; P_lo] [U_hi | U_lo]  (M = 128, N = 128, K = 64):
-          // 128-row A windows that end with P_hi, then with P_lo.
-          const uint32_t id3 = idesc_bf16_f32(128, 128, false, true);
-          const uint32_t pb = base + (st ? ScanSmem::P1 : ScanSmem::P0);
-#pragma unroll
-          for (int part = 0; part < 2; ++part)
-#pragma unroll
-            for (int kk = 0; kk < kC; kk += 16)
-              mma_bf16(tm_d3 + st * 128, desc_sw128(pb + part * 8192 - 8192 + kk * 2, 16, 1024),
-                       desc_sw128(base + ScanSmem::UH + (kk / 8) * 1024, 8192, 1024), id3,
-                       part > 0 || kk > 0);
-          mma_commit(smem_u32(&mb_d[st]));
-        }
+        // The previous chunk's P U, behind D2.
+        if (c >= 1 && ok) ok = issue_d3(c - 1);
       }
     } else if (u_warp) {
       // U = Ut - W S^T and U' = diag(fu) U, this thread's row and 16 columns,
-      // written as hi + lo images once D3 of the previous chunk is done.
+      // written as hi + lo images (U' first: D2 waits for it).
       if (L < kC) {  // zero K rows past the chunk end (D2 meets them with U' rows of 0)
         const int ui = (cg * 2 + quad) * 32 + lane;  // 0 .. 255 over the U warps
         for (int i = ui; i < (kC - L) * 16; i += 256) {
@@ -845,25 +831,33 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
         }
       }
       ok = mbar_wait(smem_u32(&mb_ut), c & 1, kWaitBudget) && ok;
+      float u[16];
+      {
+        const uint8_t* ut = sm + ScanSmem::UT;
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+          const float4 f = *reinterpret_cast<const float4*>(ut + ut_offset(row, cg * 16 + e));
+          u[e] = f.x;
+          u[e + 1] = f.y;
+          u[e + 2] = f.z;
+          u[e + 3] = f.w;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&mb_utfree));  // this warp is done with Ut
+      const float fu = F[64 + row];
       ok = mbar_wait(smem_u32(&mb_a), c & 1, kWaitBudget) && ok;
       fence_after_sync();
-      float wa[16], wb[16];
-      tmem_ld16(tm_d1 + lane_addr + cg * 16, wa);
-      tmem_ld16(tm_d1 + lane_addr + 64 + cg * 16, wb);
-      tmem_ld_wait();
-      const float fu = F[64 + row];
-      const uint8_t* ut = sm + ScanSmem::UT;
-      float u[16];
+      {
+        float wa[16], wb[16];
+        tmem_ld16(tm_d1 + lane_addr + cg * 16, wa);
+        tmem_ld16(tm_d1 + lane_addr + 64 + cg * 16, wb);
+        tmem_ld_wait();
 #pragma unroll
-      for (int e = 0; e < 16; e += 4) {
-        const float4 f = *reinterpret_cast<const float4*>(ut + ut_offset(row, cg * 16 + e));
-        u[e] = f.x - (wa[e] + wb[e]);
-        u[e + 1] = f.y - (wa[e + 1] + wb[e + 1]);
-        u[e + 2] = f.z - (wa[e + 2] + wb[e + 2]);
-        u[e + 3] = f.w - (wa[e + 3] + wb[e + 3]);
+        for (int e = 0; e < 16; ++e) u[e] -= wa[e] + wb[e];
       }
 #pragma unroll
-      for (int e = 0; e < 16; e += 8) {  // U' first: D2 waits for it
+      for (int e = 0; e < 16; e += 8) {
         float u2[8];
 #pragma unroll
         for (int x = 0; x < 8; ++x) u2[x] = fu * u[e + x];
@@ -872,23 +866,30 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
       }
       fence_proxy_async();
       fence_before_sync();
-      named_bar(kBarU1, 256 + 32);
-      // The U images were read by D3 of the previous chunk.
-      if (c > 0) ok = mbar_wait(smem_u32(&mb_d[st ^ 1]), ((c - 1) >> 1) & 1, kWaitBudget) && ok;
+      named_bar(kBarU, 256 + 32);
+      // U buffer c & 1 was last read by D3 of chunk c - 2.
+      if (c >= 2) ok = mbar_wait(smem_u32(&mb_d[st]), ((c - 2) >> 1) & 1, kWaitBudget) && ok;
+      uint8_t* ub = sm + (st ? ScanSmem::U1 : ScanSmem::U0);
 #pragma unroll
       for (int e = 0; e < 16; e += 8) {
         const uint32_t off = swz128_offset(row, cg * 16 + e, 8192);
-        st_split8(sm + ScanSmem::UH + off, sm + ScanSmem::UL + off, u + e);
+        st_split8(ub + off, ub + 8192 + off, u + e);
       }
       fence_proxy_async();
-      named_bar(kBarU2, 256 + 32);
     } else {
-      // The previous chunk's output (needs its D3), then Q S^T of this chunk.
-      if (c > 0) {
-        ok = mbar_wait(smem_u32(&mb_d[st ^ 1]), ((c - 1) >> 1) & 1, kWaitBudget) && ok;
+      // The output of chunk c - 2 (its D3 ran during chunk c - 1), which frees
+      // D3 buffer c & 1; then [fo Q S^T | 0] of this chunk into that buffer,
+      // for D3 of this chunk to accumulate onto.
+      if (c >= 2) {
+        ok = mbar_wait(smem_u32(&mb_d[st]), ((c - 2) >> 1) & 1, kWaitBudget) && ok;
+        if (loader && c < nchunks) {  // P buffer c & 1 is free: fetch P of this chunk
+          issue_p(c);
+          issued_p = c + 1;
+        }
         fence_after_sync();
-        emit_output(c - 1);
+        emit_output(c - 2);
       }
+      const float fo = F[row];
       ok = mbar_wait(smem_u32(&mb_a), c & 1, kWaitBudget) && ok;
       fence_after_sync();
       float qa[16], qb[16];
@@ -896,8 +897,20 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
       tmem_ld16(tm_d1 + lane_addr + 64 + cg * 16, qb);
       tmem_ld_wait();
 #pragma unroll
-      for (int e = 0; e < 16; ++e) qs_prev[e] = qa[e] + qb[e];
-      fo_prev = F[row];  // consumed by emit_output(c) next time
+      for (int e = 0; e < 16; ++e) {
+        qa[e] = fo * (qa[e] + qb[e]);
+        qb[e] = 0.0f;
+      }
+      const uint32_t d3 = tm_d3 + st * 128 + lane_addr + cg * 16;
+      tmem_st16(d3, qa);
+      tmem_st16(d3 + 64, qb);
+      tmem_st_wait();
+      // Once the U warps have read Ut, fetch the next chunk's.
+      if (loader && c + 1 < nchunks) {
+        ok = mbar_wait(smem_u32(&mb_utfree), c & 1, kWaitBudget) && ok;
+        issue_ut(c + 1);
+        issued_ut = c + 2;
+      }
     }
     if (!issuer_warp) {
       // S = e^{gam_L} S + D2  (f32, registers), new S^T hi / lo images.
@@ -919,16 +932,24 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
     // Every reader of this stage (D1, D2 and the factor reads) is done:
     // refill it with chunk c + 2.
     if (loader && c + 2 < nchunks) {
-      fence_proxy_async();
       issue_load(c + 2);
       issued_ld = c + 3;
     }
   }
-  if (c == nchunks && !u_warp && !issuer_warp) {  // the last chunk's output
-    ok = mbar_wait(smem_u32(&mb_d[(nchunks - 1) & 1]), ((nchunks - 1) >> 1) & 1, kWaitBudget) &&
-         ok;
-    fence_after_sync();
-    emit_output(nchunks - 1);
+  if (c == nchunks) {
+    if (issuer) ok = issue_d3(nchunks - 1) && ok;  // the last chunk's P U
+    if (!u_warp && !issuer_warp) {                  // the last two chunks' outputs
+      if (nchunks >= 2) {
+        const int cc = nchunks - 2;
+        ok = mbar_wait(smem_u32(&mb_d[cc & 1]), (cc >> 1) & 1, kWaitBudget) && ok;
+        fence_after_sync();
+        emit_output(cc);
+      }
+      const int cc = nchunks - 1;
+      ok = mbar_wait(smem_u32(&mb_d[cc & 1]), (cc >> 1) & 1, kWaitBudget) && ok;
+      fence_after_sync();
+      emit_output(cc);
+    }
   }
   ok = __syncthreads_and(ok);
   if (c < nchunks || !ok) {
@@ -939,13 +960,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
         mma_commit(smem_u32(&mb_e));
         mbar_wait(smem_u32(&mb_e), 0, kWaitBudget);
       }
-      for (int k = c; k < issued_ut; ++k) mbar_wait(smem_u32(&mb_ut), k & 1, kWaitBudget);
-      for (int k = c; k < issued_p; ++k)
-        mbar_wait(smem_u32(&mb_p[k & 1]), (k >> 1) & 1, kWaitBudget);
     }
     if (loader) {
       for (int k = c; k < issued_ld; ++k)
         mbar_wait(smem_u32(&mb_ld[k & 1]), (k >> 1) & 1, kWaitBudget);
+      for (int k = c; k < issued_ut; ++k) mbar_wait(smem_u32(&mb_ut), k & 1, kWaitBudget);
+      for (int k = max(0, issued_p - 2); k < issued_p; ++k)
+        mbar_wait(smem_u32(&mb_p[k & 1]), (k >> 1) & 1, kWaitBudget);
     }
     fence_before_sync();
     __syncthreads();
