@@ -148,6 +148,26 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// Bulk copy shared -> global (one thread), tracked by its bulk async-group.
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile(
+      "cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(
+          reinterpret_cast<uint64_t>(dst)),
+      "r"(src), "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+}
+// Waits until this thread's bulk copies have read their shared-memory sources.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+}
+// Waits until this thread's bulk copies are complete.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
+}
+
 // Sequence and chunk-in-sequence of global chunk `gc`, from cu_seqlens (warp 0).
 // Returns false when gc is past the last chunk or cu_seqlens is malformed.
 __device__ bool locate_chunk(const int32_t* __restrict__ cu, int N, int T, int gc, int& s_out,
@@ -389,13 +409,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
         v[e] = j <= i ? fi * skn[j] * __expf(gi - sgam[j]) * v[e] : 0.0f;
       }
 #pragma unroll
-      for (int e = 0; e < 32; e += 8) {
+      for (int e = 0; e < 32; e += 8) {  // staged in the (still unused) Tw image space
         const uint32_t off = swz128_offset(i, hf * 32 + e, 8192);
-        st_split8(blob + kBlobP + off, blob + kBlobP + 8192 + off, v + e);
+        st_split8(sm + PrepSmem::TWH + off, sm + PrepSmem::TWL + off, v + e);
       }
+      fence_proxy_async();
     }
   }
   __syncthreads();
+  if (tid == 0) {  // P hi, P lo images: one 16 KB store
+    bulk_s2g(blob + kBlobP, base + PrepSmem::TWH, 16384);
+    bulk_commit();
+  }
   // T = (I + A)^-1, A strictly lower triangular, by 32 x 32 blocks:
   // (1) T11, T22 by forward substitution, warp b for block b, lane = column c:
   //     x_i = [i == c] - sum_{m < i} A[32b+i][32b+m] x_m.
@@ -461,6 +486,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
     *reinterpret_cast<float4*>(sA + (32 + bi) * S_ + bj) = make_float4(-y[0], -y[1], -y[2], -y[3]);
   }
   __syncthreads();
+  if (tid == 0) bulk_wait_read();  // the P store has read the Tw image space
+  __syncthreads();
   // Tw = T diag(beta e^gam kn), Tu = T diag(beta) as hi + lo bf16 images:
   // one (row, 8-column chunk) per thread and step, 16-byte stores.
   for (int item = tid; item < 64 * 8; item += kPrepThreads) {
@@ -509,20 +536,24 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
   fence_after_sync();
   {
     // M = 64 accumulators: row 16 q + l in lane l < 16 of quadrant q.  Warp
-    // halves hf take W columns 64 hf .. and the Ut slice hf.
+    // halves hf take W columns 64 hf .. and the Ut slice hf.  Both are staged
+    // in the K, Q, V space (free once these MMAs are done) in their workspace
+    // layouts, then written by two bulk stores.
     const int i = m64_row(quad, lane);
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    uint8_t* w_img = sm + PrepSmem::KQ;          // 16 KB
+    uint8_t* ut_img = sm + PrepSmem::KQ + 16384;  // 2 slices x 16 KB
 #pragma unroll
     for (int c = 0; c < 64; c += 16) {
       float v[16];
       tmem_ld16(tmem + lane_addr + hf * 64 + c, v);
       tmem_ld_wait();
       if (i >= 0) {
-        st_bf16x8(blob + kBlobW + swz128_offset(i, hf * 64 + c, 8192), v);
-        st_bf16x8(blob + kBlobW + swz128_offset(i, hf * 64 + c + 8, 8192), v + 8);
+        st_bf16x8(w_img + swz128_offset(i, hf * 64 + c, 8192), v);
+        st_bf16x8(w_img + swz128_offset(i, hf * 64 + c + 8, 8192), v + 8);
       }
     }
-    uint8_t* slice_base = blob + kBlobU + hf * 16384;
+    uint8_t* slice_base = ut_img + hf * 16384;
 #pragma unroll
     for (int c = 0; c < 64; c += 16) {
       float v[16];
@@ -535,6 +566,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
               make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
       }
     }
+    fence_proxy_async();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    bulk_s2g(blob + kBlobW, base + PrepSmem::KQ, 16384);
+    bulk_s2g(blob + kBlobU, base + PrepSmem::KQ + 16384, 32768);
+    bulk_commit();
+    bulk_wait_all();
   }
   if (!ok && tid == 0) atomicOr(p.status, kStatusTimeout);
   fence_before_sync();
