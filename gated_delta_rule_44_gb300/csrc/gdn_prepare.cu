@@ -57,6 +57,13 @@ __device__ __forceinline__ float recip_nr(float y) {
   return fmaf(r, fmaf(-y, r, 1.0f), r);
 }
 
+// silu(x) = x / (1 + e^{-x}).  e^{-x} is capped at e^80 (the result is then
+// below 1e-32 in magnitude either way) so that the reciprocal's operand stays
+// finite.
+__device__ __forceinline__ float silu_f(float x) {
+  return x * recip_nr(1.0f + __expf(fminf(-x, 80.0f)));
+}
+
 template <typename TA>
 struct Act;
 
@@ -159,6 +166,18 @@ __global__ void __launch_bounds__(kThreads, 4) prepare_kernel(const PrepareLaunc
   }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Stream this CTA's rows (the tile and the W rows before it, its channel
+  // block) into L2 up front, one bulk prefetch per row: the per-thread loads
+  // below then wait on L2 rather than on HBM, without holding registers.
+  {
+    const int cb = blockIdx.y * kThreads * V;
+    const int bytes = min(kThreads * V, C - cb) * static_cast<int>(sizeof(TA));
+    const int r = t_begin - W + static_cast<int>(threadIdx.x);
+    if (r >= 0 && r < t_end && bytes > 0)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(x + (int64_t)r * p.x_stride + cb),
+                   "r"(bytes)
+                   : "memory");
+  }
   const int c0 = ((blockIdx.y * kWarps + warp) * 32 + lane) * V;
   const bool active = c0 < C;
   const bool is_qk = c0 < 2 * qk_total;
@@ -194,10 +213,7 @@ __global__ void __launch_bounds__(kThreads, 4) prepare_kernel(const PrepareLaunc
 #pragma unroll
       for (int j = 0; j < W; ++j) acc = fmaf(win[j][i], wt[i][j], acc);
       acc = fmaf(xt[i], wt[i][W], acc);
-      // silu(acc) = acc / (1 + e^{-acc}).  e^{-acc} is capped at e^80 (the
-      // result is then below 1e-32 in magnitude either way) so that the
-      // reciprocal's operand stays finite.
-      y[i] = acc * recip_nr(1.0f + __expf(fminf(-acc, 80.0f)));
+      y[i] = silu_f(acc);
       ss = fmaf(y[i], y[i], ss);
     }
     if (p.norm) {
@@ -221,10 +237,14 @@ __global__ void __launch_bounds__(kThreads, 4) prepare_kernel(const PrepareLaunc
   }
 
   // ---- interior tile: every token's window lies inside one sequence --------------
-  // Groups of 4 rows, the next group's loads in flight while one is computed.
+  // Groups of kG rows: the next group's loads are issued as this group's rows
+  // are consumed; the L2 norms of a group's kG tokens share their shuffle
+  // rounds.  A warp's 256 channels never straddle q, k and v, so the norm is
+  // skipped on v warps.
   if (seq_lo + W <= t_begin && t_end <= seq_hi) {
     constexpr int kG = 4;
     const int n = t_end - t_begin;
+    const bool do_norm = p.norm && is_qk;  // uniform across the warp
     const TA* xrow = x + (int64_t)t_begin * p.x_stride + c0;
     float win[WV][V];
 #pragma unroll
@@ -239,29 +259,47 @@ __global__ void __launch_bounds__(kThreads, 4) prepare_kernel(const PrepareLaunc
                                  : make_uint4(0, 0, 0, 0);
 #pragma unroll 1
     for (int r0 = 0; r0 < n; r0 += kG) {
-      uint4 cur[kG];
+      float y[kG][V];
+      float ss[kG];
 #pragma unroll
       for (int u = 0; u < kG; ++u) {
-        cur[u] = nxt[u];
+        float xt[V];
+        Act<TA>::unpack(nxt[u], xt);
         const int r = r0 + kG + u;
         nxt[u] = (active && r < n) ? Act<TA>::load_raw(xrow + (int64_t)r * p.x_stride)
                                    : make_uint4(0, 0, 0, 0);
+        ss[u] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+          float acc = 0.0f;
+#pragma unroll
+          for (int j = 0; j < W; ++j) acc = fmaf(win[j][i], wt[i][j], acc);
+          acc = fmaf(xt[i], wt[i][W], acc);
+          y[u][i] = silu_f(acc);
+          ss[u] = fmaf(y[u][i], y[u][i], ss[u]);
+        }
+#pragma unroll
+        for (int j = 0; j + 1 < W; ++j)
+#pragma unroll
+          for (int i = 0; i < V; ++i) win[j][i] = win[j + 1][i];
+        if (W > 0)
+#pragma unroll
+          for (int i = 0; i < V; ++i) win[WV - 1][i] = xt[i];
       }
+      if (do_norm) {
+        for (int m = 1; m < group; m <<= 1)
 #pragma unroll
-      for (int u = 0; u < kG; ++u) {
-        if (r0 + u < n) {
-          float xt[V];
-          Act<TA>::unpack(cur[u], xt);
-          emit(t_begin + r0 + u, win, xt);
+          for (int u = 0; u < kG; ++u) ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], m);
 #pragma unroll
-          for (int j = 0; j + 1 < W; ++j)
+        for (int u = 0; u < kG; ++u) {
+          const float inv = rsqrtf(ss[u] + 1e-6f);
 #pragma unroll
-            for (int i = 0; i < V; ++i) win[j][i] = win[j + 1][i];
-          if (W > 0)
-#pragma unroll
-            for (int i = 0; i < V; ++i) win[WV - 1][i] = xt[i];
+          for (int i = 0; i < V; ++i) y[u][i] *= inv;
         }
       }
+#pragma unroll
+      for (int u = 0; u < kG; ++u)
+        if (active && r0 + u < n) Act<TA>::store(out_ptr + (int64_t)(t_begin + r0 + u) * out_stride, y[u]);
     }
     return;
   }
