@@ -138,6 +138,19 @@ __device__ __forceinline__ void ld_bf16x8(const void* p, float* v) {
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Named barrier that also ANDs a predicate over the participating threads.
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                          uint32_t mbar) {
@@ -634,13 +647,14 @@ static_assert(PrepSmem::BYTES + 1024 <= 116736 - 2048, "two chunk_prep CTAs per 
 constexpr int kScanWorkers = 512;               // warps 0..15
 constexpr int kScanThreads = kScanWorkers + 32;  // + the issuing warp
 constexpr int kBarU = 1;  // named barrier of the U warps and the issuer: U' images ready
+constexpr int kBarW = 2;  // end-of-chunk barrier of the worker warps (not the issuer)
 
 __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const RecurLaunch p, const uint8_t* __restrict__ ws, int n_chunks_max) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = aligned_smem(smem_raw);
-  __shared__ uint64_t mb_ld[2], mb_p[2], mb_ut, mb_utfree, mb_a, mb_c, mb_d[2], mb_e;
+  __shared__ uint64_t mb_ld[2], mb_p[2], mb_ut, mb_utfree, mb_a, mb_c, mb_d[2], mb_s, mb_e;
   __shared__ uint32_t tslot;
   __shared__ int s_base, s_bad;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -698,6 +712,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
     mbar_init(smem_u32(&mb_c), 1);
     mbar_init(smem_u32(&mb_d[0]), 1);
     mbar_init(smem_u32(&mb_d[1]), 1);
+    mbar_init(smem_u32(&mb_s), 1);
     mbar_init(smem_u32(&mb_e), 1);
     fence_mbar_init();
   }
@@ -829,6 +844,15 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
     const float* F = reinterpret_cast<const float*>(sm + ScanSmem::F0 + st * kBlobFBytes);
     ok = mbar_wait(smem_u32(&mb_ld[st]), (c >> 1) & 1, kWaitBudget) && ok;
     if (issuer_warp) {
+      // The workers finished chunk c - 1: S images of chunk c, U images and the
+      // D3 preload of chunk c - 1 are in place.  No signal in time means they
+      // have stopped (they leave the loop only at their end-of-chunk barrier,
+      // so none of them will reach the U barrier again).
+      const bool go = c < 1 || mbar_wait(smem_u32(&mb_s), (c - 1) & 1, kWaitBudget);
+      if (!__all_sync(0xffffffffu, go)) {  // leave the loop as a whole warp
+        ok = false;
+        break;
+      }
       if (issuer && ok) {
         fence_after_sync();
         // D1 = [W; Q] [S_hi | S_lo]^T  (M = 128, N = 128, K = 128)
@@ -964,19 +988,25 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
       for (int e = 0; e < 16; ++e) S[e] = fmaf(dL, S[e], da[e] + db[e]);
       write_s();
       fence_proxy_async();
-    }
-    fence_before_sync();
-    if (!__syncthreads_and(ok)) break;
-    fence_after_sync();
-    // Every reader of this stage (D1, D2 and the factor reads) is done:
-    // refill it with chunk c + 2.
-    if (loader && c + 2 < nchunks) {
-      issue_load(c + 2);
-      issued_ld = c + 3;
+      fence_before_sync();
+      ok = named_bar_and(kBarW, kScanWorkers, ok);
+      if (!ok) break;
+      if (tid == 0) mbar_arrive(smem_u32(&mb_s));  // chunk c done: the issuer may go on
+      fence_after_sync();
+      // Every reader of this stage (D1, D2 and the factor reads) is done:
+      // refill it with chunk c + 2.
+      if (loader && c + 2 < nchunks) {
+        issue_load(c + 2);
+        issued_ld = c + 3;
+      }
     }
   }
   if (c == nchunks) {
-    if (issuer) ok = issue_d3(nchunks - 1) && ok;  // the last chunk's P U
+    if (issuer_warp) {  // the last chunk's P U, once the workers are done with it
+      const bool go = mbar_wait(smem_u32(&mb_s), (nchunks - 1) & 1, kWaitBudget);
+      if (issuer) ok = go && issue_d3(nchunks - 1) && ok;
+      else ok = go && ok;
+    }
     if (!u_warp && !issuer_warp) {                  // the last two chunks' outputs
       if (nchunks >= 2) {
         const int cc = nchunks - 2;
