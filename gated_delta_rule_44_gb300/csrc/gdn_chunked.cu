@@ -235,8 +235,10 @@ __device__ int chunk_base(const int32_t* __restrict__ cu, int s, bool& bad) {
 
 
 // ---------------------------------------------------------------------------
-// Kernel 1: per (chunk, value head).  8 warps; TMEM lane quadrant q = warp % 4
-// is shared by warps q and q + 4, which split columns into halves hf = warp / 4.
+// Kernel 1: per (chunk, key head), its value heads in turn (K, Q, their norms
+// and [K; Q] K^T are the same for all of them).  8 warps; TMEM lane quadrant
+// q = warp % 4 is shared by warps q and q + 4, which split columns into halves
+// hf = warp / 4.
 struct PrepSmem {
   static constexpr uint32_t KQ = 0;          // [K box0 | Q box0 | K box1 | Q box1], 32 KB
   static constexpr uint32_t V = 32768;       // [V box0 | V box1], 16 KB
@@ -264,12 +266,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
     const __grid_constant__ CUtensorMap tm_v, const RecurLaunch p, uint8_t* __restrict__ ws) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = aligned_smem(smem_raw);
-  __shared__ uint64_t mbar_tma, mbar_mma;
+  __shared__ uint64_t mbar_tma, mbar_v, mbar_mma;
   __shared__ uint32_t tslot;
   __shared__ int s_seq, s_chunk, s_ok;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3, hf = warp >> 2;
-  const int gc = blockIdx.x, h = blockIdx.y;
+  const int gc = blockIdx.x, hk = blockIdx.y;
+  const int G = p.Hv / p.Hk;  // value heads of this key head: hk G .. hk G + G - 1
 
   if (warp == 0) {
     int s = 0, j = 0;
@@ -279,7 +282,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
       s_seq = s;
       s_chunk = j;
       s_ok = ok ? 1 : 0;
-      if (bad && gc == 0 && h == 0) atomicOr(p.status, kStatusBadSeqlens);
+      if (bad && gc == 0 && hk == 0) atomicOr(p.status, kStatusBadSeqlens);
     }
   }
   __syncthreads();
@@ -287,7 +290,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
   const int s = s_seq;
   const int t0 = __ldg(p.cu + s) + kC * s_chunk;
   const int L = min(kC, __ldg(p.cu + s + 1) - t0);
-  const int hk = h / (p.Hv / p.Hk);
   float* sg = reinterpret_cast<float*>(sm + PrepSmem::GB);
   float* sb = sg + 64;
   float* sgam = sb + 64;
@@ -300,68 +302,66 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
   constexpr int S_ = PrepSmem::kAStride;
   constexpr int SY = PrepSmem::kYStride;
   const uint32_t base = smem_u32(sm);
-  const uint32_t mb_tma = smem_u32(&mbar_tma), mb_mma = smem_u32(&mbar_mma);
+  const uint32_t mb_tma = smem_u32(&mbar_tma), mb_v = smem_u32(&mbar_v),
+                 mb_mma = smem_u32(&mbar_mma);
 
   if (tid == 0) {
     mbar_init(mb_tma, 1);
+    mbar_init(mb_v, 1);
     mbar_init(mb_mma, 1);
     fence_mbar_init();
   }
   __syncthreads();
+  auto load_v = [&](int h) {  // thread 0
+    mbar_expect_tx(mb_v, 2 * 8192);
+    tma_load_3d(base + PrepSmem::V + 0, &tm_v, mb_v, 0, h, t0);
+    tma_load_3d(base + PrepSmem::V + 8192, &tm_v, mb_v, 64, h, t0);
+  };
   if (tid == 0) {
-    mbar_expect_tx(mb_tma, 6 * 8192);
+    mbar_expect_tx(mb_tma, 4 * 8192);
     tma_load_3d(base + PrepSmem::KQ + 0, &tm_k, mb_tma, 0, hk, t0);
     tma_load_3d(base + PrepSmem::KQ + 8192, &tm_q, mb_tma, 0, hk, t0);
     tma_load_3d(base + PrepSmem::KQ + 16384, &tm_k, mb_tma, 64, hk, t0);
     tma_load_3d(base + PrepSmem::KQ + 24576, &tm_q, mb_tma, 64, hk, t0);
-    tma_load_3d(base + PrepSmem::V + 0, &tm_v, mb_tma, 0, h, t0);
-    tma_load_3d(base + PrepSmem::V + 8192, &tm_v, mb_tma, 64, h, t0);
+    load_v(hk * G);
   }
   if (warp == 0) tmem_alloc(smem_u32(&tslot), 256);
-  if (tid < 64) {
-    const bool in = tid < L;
-    sg[tid] = in ? __ldg(p.g + (int64_t)(t0 + tid) * p.Hv + h) : 0.0f;
-    sb[tid] = in ? __ldg(p.beta + (int64_t)(t0 + tid) * p.Hv + h) : 0.0f;
-  }
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = tslot;
-  if (warp == 0) {  // inclusive scan of g over the chunk (2 tokens per lane)
-    const float a = sg[2 * lane], b = sg[2 * lane + 1];
-    float x = a + b;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    sgam[2 * lane + 1] = x;
-    sgam[2 * lane] = x - b;
-  }
+  // TMEM: columns 0..63 [K; Q] K^T (kept for every value head), 64..191 the
+  // M = 64 results W, then Ut, of the current head.
+  const uint32_t tm_g = tmem, tm_wu = tmem + 64;
   bool ok = mbar_wait(mb_tma, 0, kWaitBudget);
-  if (L < kC) {  // zero K, Q and V rows past the chunk end
+  if (L < kC) {  // zero K and Q rows past the chunk end
     for (int i = tid; i < (kC - L) * 8; i += kPrepThreads) {
       const int r = L + i / 8, q16 = i % 8;
 #pragma unroll
-      for (int box = 0; box < 6; ++box)
+      for (int box = 0; box < 4; ++box)
         *reinterpret_cast<uint4*>(sm + box * 8192 + r * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
     }
     fence_proxy_async();
   }
   if (!__syncthreads_and(ok)) {
-    if (tid == 0) atomicOr(p.status, kStatusTimeout);
+    if (tid == 0) {
+      atomicOr(p.status, kStatusTimeout);
+      mbar_wait(mb_v, 0, kWaitBudget);  // the first V load
+    }
+    __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
     return;
   }
   fence_after_sync();
   // [K; Q] K^T  (M = 128, N = 64, K = 128): A is the 128-row K-major tile
-  // [K; Q] (boxes 16 KB apart), B the K tile (its first 64 rows).
+  // [K; Q] (boxes 16 KB apart), B the K tile (its first 64 rows).  Shared by
+  // every value head of this key head.
   if (tid == 0) {
     const uint32_t idesc = idesc_bf16_f32(128, 64, false, false);
 #pragma unroll
     for (int kk = 0; kk < kD; kk += 16) {
       const uint32_t off = (kk / 64) * 16384 + (kk % 64) * 2;
-      mma_bf16(tmem, desc_sw128(base + PrepSmem::KQ + off, 16, 1024),
+      mma_bf16(tm_g, desc_sw128(base + PrepSmem::KQ + off, 16, 1024),
                desc_sw128(base + PrepSmem::KQ + off, 16, 1024), idesc, kk > 0);
     }
     mma_commit(mb_mma);
@@ -383,212 +383,270 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
     }
     (tid < 64 ? skn : sqn)[r] = p.norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
   }
-  __syncthreads();  // publishes skn, sqn
-  uint8_t* blob = ws + ((int64_t)gc * p.Hv + h) * kBlobBytes;
-  if (tid < 64) {
-    swj[tid] = sb[tid] * skn[tid] * __expf(sgam[tid]);
-    suj[tid] = sb[tid];
-    float* F = reinterpret_cast<float*>(blob + kBlobF);
-    F[tid] = p.scale * sqn[tid] * __expf(sgam[tid]);           // fo
-    F[64 + tid] = __expf(sgam[kC - 1] - sgam[tid]) * skn[tid];  // fu
-    if (tid < 4) F[128 + tid] = tid == 0 ? __expf(sgam[kC - 1]) : 0.0f;
-  }
   ok = mbar_wait(mb_mma, 0, kWaitBudget);
+  uint32_t mma_phase = 1;
   fence_after_sync();
-  {
-    // Lanes 0..63 hold K K^T -> A (f32, shared); lanes 64..127 hold Q K^T -> P
-    // (hi + lo images, straight to the workspace).  Row i, columns 32 hf ...
-    const int i = (quad & 1) * 32 + lane;
-    float v[32];
-    tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + hf * 32, v);
-    tmem_ld_wait();
-    const float gi = sgam[i];
-    if (quad < 2) {
-      const float fi = sb[i] * skn[i];
+  __syncthreads();  // publishes skn, sqn; the Q tile is free from here on
+
+  for (int jh = 0; jh < G; ++jh) {
+    const int h = hk * G + jh;
+    uint8_t* blob = ws + ((int64_t)gc * p.Hv + h) * kBlobBytes;
+    if (tid < 64) {
+      const bool in = tid < L;
+      sg[tid] = in ? __ldg(p.g + (int64_t)(t0 + tid) * p.Hv + h) : 0.0f;
+      sb[tid] = in ? __ldg(p.beta + (int64_t)(t0 + tid) * p.Hv + h) : 0.0f;
+    }
+    // The previous head's Ut store has read the image space the P images use.
+    if (tid == 0) bulk_wait_read();
+    __syncthreads();
+    if (warp == 0) {  // inclusive scan of g over the chunk (2 tokens per lane)
+      const float a = sg[2 * lane], b = sg[2 * lane + 1];
+      float x = a + b;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int j = hf * 32 + e;
-        v[e] = j < i ? fi * skn[j] * __expf(gi - sgam[j]) * v[e] : 0.0f;
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
       }
+      sgam[2 * lane + 1] = x;
+      sgam[2 * lane] = x - b;
+    }
+    __syncthreads();
+    if (tid < 64) {
+      swj[tid] = sb[tid] * skn[tid] * __expf(sgam[tid]);
+      suj[tid] = sb[tid];
+      float* F = reinterpret_cast<float*>(blob + kBlobF);
+      F[tid] = p.scale * sqn[tid] * __expf(sgam[tid]);           // fo
+      F[64 + tid] = __expf(sgam[kC - 1] - sgam[tid]) * skn[tid];  // fu
+      if (tid < 4) F[128 + tid] = tid == 0 ? __expf(sgam[kC - 1]) : 0.0f;
+    }
+    {
+      // Lanes 0..63 hold K K^T -> A (f32, shared); lanes 64..127 hold Q K^T -> P
+      // (hi + lo images, staged in the Tw image space).  Row i, columns 32 hf ...
+      const int i = (quad & 1) * 32 + lane;
+      float v[32];
+      tmem_ld32(tm_g + (static_cast<uint32_t>(quad * 32) << 16) + hf * 32, v);
+      tmem_ld_wait();
+      const float gi = sgam[i];
+      if (quad < 2) {
+        const float fi = sb[i] * skn[i];
 #pragma unroll
-      for (int e = 0; e < 32; e += 4)
-        *reinterpret_cast<float4*>(sA + i * S_ + hf * 32 + e) =
-            make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
-    } else {
-      const float fi = p.scale * sqn[i];
+        for (int e = 0; e < 32; ++e) {
+          const int j = hf * 32 + e;
+          v[e] = j < i ? fi * skn[j] * __expf(gi - sgam[j]) * v[e] : 0.0f;
+        }
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int j = hf * 32 + e;
-        v[e] = j <= i ? fi * skn[j] * __expf(gi - sgam[j]) * v[e] : 0.0f;
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(sA + i * S_ + hf * 32 + e) =
+              make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+      } else {
+        const float fi = p.scale * sqn[i];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int j = hf * 32 + e;
+          v[e] = j <= i ? fi * skn[j] * __expf(gi - sgam[j]) * v[e] : 0.0f;
+        }
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          const uint32_t off = swz128_offset(i, hf * 32 + e, 8192);
+          st_split8(sm + PrepSmem::TWH + off, sm + PrepSmem::TWL + off, v + e);
+        }
+        fence_proxy_async();
       }
+    }
+    __syncthreads();
+    if (tid == 0) {  // P hi, P lo images: one 16 KB store
+      bulk_s2g(blob + kBlobP, base + PrepSmem::TWH, 16384);
+      bulk_commit();
+    }
+    // T = (I + A)^-1, A strictly lower triangular, by 32 x 32 blocks:
+    // (1) T11, T22 by forward substitution, warp b for block b, lane = column c:
+    //     x_i = [i == c] - sum_{m < i} A[32b+i][32b+m] x_m.
+    if (warp < 2) {
+      const int b0 = 32 * warp, c = lane;
+      float x[32];
 #pragma unroll
-      for (int e = 0; e < 32; e += 8) {  // staged in the (still unused) Tw image space
-        const uint32_t off = swz128_offset(i, hf * 32 + e, 8192);
-        st_split8(sm + PrepSmem::TWH + off, sm + PrepSmem::TWL + off, v + e);
+      for (int i = 0; i < 32; ++i) {
+        const float* arow = sA + (b0 + i) * S_ + b0;
+        float a0 = i == c ? 1.0f : 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+#pragma unroll
+        for (int m = 0; m < i; m += 4) {
+          const float4 av = *reinterpret_cast<const float4*>(arow + m);
+          a0 = fmaf(-av.x, x[m], a0);
+          if (m + 1 < i) a1 = fmaf(-av.y, x[m + 1], a1);
+          if (m + 2 < i) a2 = fmaf(-av.z, x[m + 2], a2);
+          if (m + 3 < i) a3 = fmaf(-av.w, x[m + 3], a3);
+        }
+        x[i] = (a0 + a1) + (a2 + a3);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) sA[(b0 + i) * S_ + b0 + c] = x[i];
+    }
+    __syncthreads();
+    // (2) Y = A21 T11, (3) T21 = -T22 Y: thread -> row i, columns j0 .. j0 + 3.
+    const int bi = tid >> 3, bj = (tid & 7) * 4;
+    {
+      const float* arow = sA + (32 + bi) * S_;
+      float y[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int k = 0; k < 32; k += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(arow + k);
+        const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 t = *reinterpret_cast<const float4*>(sA + (k + q) * S_ + bj);
+          y[0] = fmaf(av[q], t.x, y[0]);
+          y[1] = fmaf(av[q], t.y, y[1]);
+          y[2] = fmaf(av[q], t.z, y[2]);
+          y[3] = fmaf(av[q], t.w, y[3]);
+        }
+      }
+      *reinterpret_cast<float4*>(sY + bi * SY + bj) = make_float4(y[0], y[1], y[2], y[3]);
+    }
+    __syncthreads();
+    {
+      const float* trow = sA + (32 + bi) * S_ + 32;
+      float y[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int k = 0; k < 32; k += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(trow + k);
+        const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 t = *reinterpret_cast<const float4*>(sY + (k + q) * SY + bj);
+          y[0] = fmaf(av[q], t.x, y[0]);
+          y[1] = fmaf(av[q], t.y, y[1]);
+          y[2] = fmaf(av[q], t.z, y[2]);
+          y[3] = fmaf(av[q], t.w, y[3]);
+        }
+      }
+      *reinterpret_cast<float4*>(sA + (32 + bi) * S_ + bj) =
+          make_float4(-y[0], -y[1], -y[2], -y[3]);
+    }
+    if (tid == 0) bulk_wait_read();  // the P store has read the Tw image space
+    __syncthreads();
+    // Tw = T diag(beta e^gam kn), Tu = T diag(beta) as hi + lo bf16 images:
+    // one (row, 8-column chunk) per thread and step, 16-byte stores.
+    for (int item = tid; item < 64 * 8; item += kPrepThreads) {
+      const int i = item >> 3, q = item & 7;
+      float tw[8], tu[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float t = sA[i * S_ + 8 * q + e];
+        tw[e] = t * swj[8 * q + e];
+        tu[e] = t * suj[8 * q + e];
+      }
+      const uint32_t off = swz128_offset(i, 8 * q, 8192);
+      st_split8(sm + PrepSmem::TWH + off, sm + PrepSmem::TWL + off, tw);
+      st_split8(sm + PrepSmem::TUH + off, sm + PrepSmem::TUL + off, tu);
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    ok = __syncthreads_and(ok);
+    fence_after_sync();
+    const int i64 = m64_row(quad, lane);  // M = 64 rows: row 16 q + l in lane l < 16
+    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    // W = (Tw_hi + Tw_lo) K  (M = 64, N = 128, K = 64): B is the K tile,
+    // MN-major: token rows, dk contiguous, boxes 16 KB apart.
+    if (tid == 0 && ok) {
+      const uint32_t idesc = idesc_bf16_f32(64, 128, false, true);
+#pragma unroll
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int kk = 0; kk < kC; kk += 16) {
+          const uint32_t a_off = (part ? PrepSmem::TWL : PrepSmem::TWH) + kk * 2;
+          mma_bf16(tm_wu, desc_sw128(base + a_off, 16, 1024),
+                   desc_sw128(base + PrepSmem::KQ + (kk / 8) * 1024, 16384, 1024), idesc,
+                   part > 0 || kk > 0);
+        }
+      mma_commit(mb_mma);
+    }
+    __syncwarp();
+    ok = ok && mbar_wait(mb_mma, mma_phase & 1, kWaitBudget);
+    ++mma_phase;
+    fence_after_sync();
+    {
+      // W image staged in the (free) Q boxes of the K/Q tile, in its workspace
+      // layout: box b of W at the Q box b.  Warp halves hf take columns 64 hf ..
+      uint8_t* w_box = sm + PrepSmem::KQ + 8192 + hf * 16384;
+#pragma unroll
+      for (int c = 0; c < 64; c += 16) {
+        float v[16];
+        tmem_ld16(tm_wu + lane_addr + hf * 64 + c, v);
+        tmem_ld_wait();
+        if (i64 >= 0) {
+          st_bf16x8(w_box + swz128_offset(i64, c, 8192), v);
+          st_bf16x8(w_box + swz128_offset(i64, c + 8, 8192), v + 8);
+        }
       }
       fence_proxy_async();
     }
-  }
-  __syncthreads();
-  if (tid == 0) {  // P hi, P lo images: one 16 KB store
-    bulk_s2g(blob + kBlobP, base + PrepSmem::TWH, 16384);
-    bulk_commit();
-  }
-  // T = (I + A)^-1, A strictly lower triangular, by 32 x 32 blocks:
-  // (1) T11, T22 by forward substitution, warp b for block b, lane = column c:
-  //     x_i = [i == c] - sum_{m < i} A[32b+i][32b+m] x_m.
-  if (warp < 2) {
-    const int b0 = 32 * warp, c = lane;
-    float x[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float* arow = sA + (b0 + i) * S_ + b0;
-      float a0 = i == c ? 1.0f : 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
-#pragma unroll
-      for (int m = 0; m < i; m += 4) {
-        const float4 av = *reinterpret_cast<const float4*>(arow + m);
-        a0 = fmaf(-av.x, x[m], a0);
-        if (m + 1 < i) a1 = fmaf(-av.y, x[m + 1], a1);
-        if (m + 2 < i) a2 = fmaf(-av.z, x[m + 2], a2);
-        if (m + 3 < i) a3 = fmaf(-av.w, x[m + 3], a3);
+    // V of this head (loaded during the previous head), rows past the chunk end zeroed.
+    ok = mbar_wait(mb_v, jh & 1, kWaitBudget) && ok;
+    if (L < kC) {
+      for (int i = tid; i < (kC - L) * 8; i += kPrepThreads) {
+        const int r = L + i / 8, q16 = i % 8;
+        *reinterpret_cast<uint4*>(sm + PrepSmem::V + r * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(sm + PrepSmem::V + 8192 + r * 128 + q16 * 16) =
+            make_uint4(0, 0, 0, 0);
       }
-      x[i] = (a0 + a1) + (a2 + a3);
+      fence_proxy_async();
+    }
+    fence_before_sync();
+    ok = __syncthreads_and(ok);
+    fence_after_sync();
+    if (tid == 0) {
+      bulk_s2g(blob + kBlobW, base + PrepSmem::KQ + 8192, 8192);
+      bulk_s2g(blob + kBlobW + 8192, base + PrepSmem::KQ + 24576, 8192);
+      bulk_commit();
+      // Ut = (Tu_hi + Tu_lo) V  (M = 64, N = 128, K = 64): B is the V tile, MN-major.
+      if (ok) {
+        const uint32_t idesc = idesc_bf16_f32(64, 128, false, true);
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int kk = 0; kk < kC; kk += 16) {
+            const uint32_t a_off = (part ? PrepSmem::TUL : PrepSmem::TUH) + kk * 2;
+            mma_bf16(tm_wu, desc_sw128(base + a_off, 16, 1024),
+                     desc_sw128(base + PrepSmem::V + (kk / 8) * 1024, 8192, 1024), idesc,
+                     part > 0 || kk > 0);
+          }
+        mma_commit(mb_mma);
+      }
     }
     __syncwarp();
+    ok = ok && mbar_wait(mb_mma, mma_phase & 1, kWaitBudget);
+    ++mma_phase;
+    fence_after_sync();
+    __syncthreads();  // the Ut MMA has read V and the Tu images
+    if (tid == 0 && jh + 1 < G) load_v(h + 1);  // next head's V, during this epilogue
+    {
+      // Ut staged in the (free) Tw/Tu image space, both slices, in the workspace
+      // layout; warp halves hf take the Ut slice hf.
+      uint8_t* slice_base = sm + PrepSmem::TWH + hf * 16384;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) sA[(b0 + i) * S_ + b0 + c] = x[i];
-  }
-  __syncthreads();
-  // (2) Y = A21 T11, (3) T21 = -T22 Y: thread -> row i, columns j0 .. j0 + 3.
-  const int bi = tid >> 3, bj = (tid & 7) * 4;
-  {
-    const float* arow = sA + (32 + bi) * S_;
-    float y[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      for (int c = 0; c < 64; c += 16) {
+        float v[16];
+        tmem_ld16(tm_wu + lane_addr + hf * 64 + c, v);
+        tmem_ld_wait();
+        if (i64 >= 0) {
 #pragma unroll
-    for (int k = 0; k < 32; k += 4) {
-      const float4 a = *reinterpret_cast<const float4*>(arow + k);
-      const float av[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 t = *reinterpret_cast<const float4*>(sA + (k + q) * S_ + bj);
-        y[0] = fmaf(av[q], t.x, y[0]);
-        y[1] = fmaf(av[q], t.y, y[1]);
-        y[2] = fmaf(av[q], t.z, y[2]);
-        y[3] = fmaf(av[q], t.w, y[3]);
+          for (int e = 0; e < 4; ++e)
+            *reinterpret_cast<float4*>(slice_base + ut_offset(i64, c + 4 * e)) =
+                make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        }
       }
+      fence_proxy_async();
     }
-    *reinterpret_cast<float4*>(sY + bi * SY + bj) = make_float4(y[0], y[1], y[2], y[3]);
-  }
-  __syncthreads();
-  {
-    const float* trow = sA + (32 + bi) * S_ + 32;
-    float y[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-    for (int k = 0; k < 32; k += 4) {
-      const float4 a = *reinterpret_cast<const float4*>(trow + k);
-      const float av[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 t = *reinterpret_cast<const float4*>(sY + (k + q) * SY + bj);
-        y[0] = fmaf(av[q], t.x, y[0]);
-        y[1] = fmaf(av[q], t.y, y[1]);
-        y[2] = fmaf(av[q], t.z, y[2]);
-        y[3] = fmaf(av[q], t.w, y[3]);
-      }
+    fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+      bulk_s2g(blob + kBlobU, base + PrepSmem::TWH, 32768);
+      bulk_commit();
     }
-    *reinterpret_cast<float4*>(sA + (32 + bi) * S_ + bj) = make_float4(-y[0], -y[1], -y[2], -y[3]);
-  }
-  __syncthreads();
-  if (tid == 0) bulk_wait_read();  // the P store has read the Tw image space
-  __syncthreads();
-  // Tw = T diag(beta e^gam kn), Tu = T diag(beta) as hi + lo bf16 images:
-  // one (row, 8-column chunk) per thread and step, 16-byte stores.
-  for (int item = tid; item < 64 * 8; item += kPrepThreads) {
-    const int i = item >> 3, q = item & 7;
-    float tw[8], tu[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float t = sA[i * S_ + 8 * q + e];
-      tw[e] = t * swj[8 * q + e];
-      tu[e] = t * suj[8 * q + e];
-    }
-    const uint32_t off = swz128_offset(i, 8 * q, 8192);
-    st_split8(sm + PrepSmem::TWH + off, sm + PrepSmem::TWL + off, tw);
-    st_split8(sm + PrepSmem::TUH + off, sm + PrepSmem::TUL + off, tu);
-  }
-  fence_proxy_async();
-  fence_before_sync();
-  __syncthreads();
-  fence_after_sync();
-  // W = (Tw_hi + Tw_lo) K, Ut = (Tu_hi + Tu_lo) V  (M = 64, N = 128, K = 64): B is
-  // the K (V) tile, MN-major: token rows, dk (dv) contiguous.
-  if (tid == 0) {
-    const uint32_t idesc = idesc_bf16_f32(64, 128, false, true);
-#pragma unroll
-    for (int part = 0; part < 2; ++part)
-#pragma unroll
-      for (int kk = 0; kk < kC; kk += 16) {
-        const uint32_t a_off = (part ? PrepSmem::TWL : PrepSmem::TWH) + kk * 2;
-        mma_bf16(tmem, desc_sw128(base + a_off, 16, 1024),
-                 desc_sw128(base + PrepSmem::KQ + (kk / 8) * 1024, 16384, 1024), idesc,
-                 part > 0 || kk > 0);
-      }
-#pragma unroll
-    for (int part = 0; part < 2; ++part)
-#pragma unroll
-      for (int kk = 0; kk < kC; kk += 16) {
-        const uint32_t a_off = (part ? PrepSmem::TUL : PrepSmem::TUH) + kk * 2;
-        mma_bf16(tmem + 128, desc_sw128(base + a_off, 16, 1024),
-                 desc_sw128(base + PrepSmem::V + (kk / 8) * 1024, 8192, 1024), idesc,
-                 part > 0 || kk > 0);
-      }
-    mma_commit(mb_mma);
-  }
-  __syncwarp();
-  ok = mbar_wait(mb_mma, 1, kWaitBudget) && ok;
-  fence_after_sync();
-  {
-    // M = 64 accumulators: row 16 q + l in lane l < 16 of quadrant q.  Warp
-    // halves hf take W columns 64 hf .. and the Ut slice hf.  Both are staged
-    // in the K, Q, V space (free once these MMAs are done) in their workspace
-    // layouts, then written by two bulk stores.
-    const int i = m64_row(quad, lane);
-    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-    uint8_t* w_img = sm + PrepSmem::KQ;          // 16 KB
-    uint8_t* ut_img = sm + PrepSmem::KQ + 16384;  // 2 slices x 16 KB
-#pragma unroll
-    for (int c = 0; c < 64; c += 16) {
-      float v[16];
-      tmem_ld16(tmem + lane_addr + hf * 64 + c, v);
-      tmem_ld_wait();
-      if (i >= 0) {
-        st_bf16x8(w_img + swz128_offset(i, hf * 64 + c, 8192), v);
-        st_bf16x8(w_img + swz128_offset(i, hf * 64 + c + 8, 8192), v + 8);
-      }
-    }
-    uint8_t* slice_base = ut_img + hf * 16384;
-#pragma unroll
-    for (int c = 0; c < 64; c += 16) {
-      float v[16];
-      tmem_ld16(tmem + lane_addr + 128 + hf * 64 + c, v);
-      tmem_ld_wait();
-      if (i >= 0) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          *reinterpret_cast<float4*>(slice_base + ut_offset(i, c + 4 * e)) =
-              make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-      }
-    }
-    fence_proxy_async();
-  }
-  __syncthreads();
-  if (tid == 0) {
-    bulk_s2g(blob + kBlobW, base + PrepSmem::KQ, 16384);
-    bulk_s2g(blob + kBlobU, base + PrepSmem::KQ + 16384, 32768);
-    bulk_commit();
-    bulk_wait_all();
   }
   if (!ok && tid == 0) atomicOr(p.status, kStatusTimeout);
+  if (tid == 0) bulk_wait_all();
   fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 256);
@@ -1113,7 +1171,7 @@ cudaError_t launch_chunked(const ChunkedLaunch& c, cudaStream_t s) {
   uint8_t* ws = static_cast<uint8_t*>(c.workspace);
   const int64_t nch = max_chunks(p.T, p.N);
   if (nch > 0x7fffffff || p.Hv > 65535) return cudaErrorInvalidConfiguration;
-  chunk_prep_kernel<<<dim3(static_cast<unsigned>(nch), p.Hv), kPrepThreads,
+  chunk_prep_kernel<<<dim3(static_cast<unsigned>(nch), p.Hk), kPrepThreads,
                       PrepSmem::BYTES + 1024, s>>>(tq, tk, tv, p, ws);
   note_launch();
   cudaError_t e = cudaGetLastError();
