@@ -326,6 +326,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
     load_v(hk * G);
   }
   if (warp == 0) tmem_alloc(smem_u32(&tslot), 256);
+  // Gates of the current value head, read ahead of their use (the first
+  // head's here, the next head's during the solve of the current one).
+  float g_next = 0.0f, b_next = 0.0f;
+  auto load_gates = [&](int h) {  // threads 0..63
+    if (tid < L) {
+      g_next = __ldg(p.g + (int64_t)(t0 + tid) * p.Hv + h);
+      b_next = __ldg(p.beta + (int64_t)(t0 + tid) * p.Hv + h);
+    } else {
+      g_next = b_next = 0.0f;
+    }
+  };
+  if (tid < 64) load_gates(hk * G);
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
@@ -392,9 +404,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
     const int h = hk * G + jh;
     uint8_t* blob = ws + ((int64_t)gc * p.Hv + h) * kBlobBytes;
     if (tid < 64) {
-      const bool in = tid < L;
-      sg[tid] = in ? __ldg(p.g + (int64_t)(t0 + tid) * p.Hv + h) : 0.0f;
-      sb[tid] = in ? __ldg(p.beta + (int64_t)(t0 + tid) * p.Hv + h) : 0.0f;
+      sg[tid] = g_next;
+      sb[tid] = b_next;
     }
     // The previous head's Ut store has read the image space the P images use.
     if (tid == 0) bulk_wait_read();
@@ -422,17 +433,26 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
     {
       // Lanes 0..63 hold K K^T -> A (f32, shared); lanes 64..127 hold Q K^T -> P
       // (hi + lo images, staged in the Tw image space).  Row i, columns 32 hf ...
+      // Rows 0..31 x columns 32..63 lie above the diagonal: all zero.
       const int i = (quad & 1) * 32 + lane;
+      const bool upper = (quad & 1) == 0 && hf == 1;  // uniform across the warp
       float v[32];
-      tmem_ld32(tm_g + (static_cast<uint32_t>(quad * 32) << 16) + hf * 32, v);
-      tmem_ld_wait();
+      if (!upper) {
+        tmem_ld32(tm_g + (static_cast<uint32_t>(quad * 32) << 16) + hf * 32, v);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = 0.0f;
+      }
       const float gi = sgam[i];
       if (quad < 2) {
         const float fi = sb[i] * skn[i];
+        if (!upper) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int j = hf * 32 + e;
-          v[e] = j < i ? fi * skn[j] * __expf(gi - sgam[j]) * v[e] : 0.0f;
+          for (int e = 0; e < 32; ++e) {
+            const int j = hf * 32 + e;
+            v[e] = j < i ? fi * skn[j] * __expf(gi - sgam[j]) * v[e] : 0.0f;
+          }
         }
 #pragma unroll
         for (int e = 0; e < 32; e += 4)
@@ -440,10 +460,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
               make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
       } else {
         const float fi = p.scale * sqn[i];
+        if (!upper) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int j = hf * 32 + e;
-          v[e] = j <= i ? fi * skn[j] * __expf(gi - sgam[j]) * v[e] : 0.0f;
+          for (int e = 0; e < 32; ++e) {
+            const int j = hf * 32 + e;
+            v[e] = j <= i ? fi * skn[j] * __expf(gi - sgam[j]) * v[e] : 0.0f;
+          }
         }
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
@@ -458,6 +480,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
       bulk_s2g(blob + kBlobP, base + PrepSmem::TWH, 16384);
       bulk_commit();
     }
+    if (tid < 64 && jh + 1 < G) load_gates(h + 1);  // consumed at the next head's start
     // T = (I + A)^-1, A strictly lower triangular, by 32 x 32 blocks:
     // (1) T11, T22 by forward substitution, warp b for block b, lane = column c:
     //     x_i = [i == c] - sum_{m < i} A[32b+i][32b+m] x_m.
