@@ -8,6 +8,12 @@ over every token; ``gdn_decode`` then takes rows [0, n_decode) and
 (the caller's ``cu_seqlens_prefill``, like the pages' prefill_query_start_loc).
 All buffers are torch tensors on one device; everything is asynchronous on the
 given stream.
+
+``GdnHostPipeline`` serves callers whose per-step inputs and outputs live in
+pinned host memory: it copies a step's inputs in and its output out on their
+own streams, so that they overlap the neighbouring steps' compute; the steps'
+compute stays in order on one stream (each step updates the state and conv
+pools the next one reads).
 """
 from __future__ import annotations
 
@@ -43,8 +49,12 @@ class GdnStep:
 
     def run(self, mixed_qkv, a_raw, b_raw, conv_weight, A_log, dt_bias, cu_seqlens, state_indices,
             has_initial_state, state_pool, conv_pool, cu_seqlens_prefill=None,
-            stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+            stream: Optional[torch.cuda.Stream] = None,
+            out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """One step; writes the output to ``out`` (default: this object's own
+        buffer) and returns it."""
         nd, ndt = self.n_decode, self.nd_tok
+        out = self.out if out is None else out
         B.gdn_prepare(mixed_qkv, conv_weight, a_raw, b_raw, A_log, dt_bias, cu_seqlens, conv_pool,
                       self.q, self.k, self.v, self.g, self.beta, Hk=self.Hk, Hv=self.Hv,
                       Dk=self.Dk, Dv=self.Dv, K=self.K, state_indices=state_indices,
@@ -52,17 +62,78 @@ class GdnStep:
                       stream=stream)
         if nd > 0:
             B.gdn_decode(self.q[:ndt], self.k[:ndt], self.v[:ndt], self.g[:ndt],
-                         self.beta[:ndt], state_pool, self.out[:ndt], scale=self.scale,
+                         self.beta[:ndt], state_pool, out[:ndt], scale=self.scale,
                          state_indices=state_indices[:nd], stream=stream)
         if self.N > nd:
             B.gdn_prefill_varlen(self.q[ndt:], self.k[ndt:], self.v[ndt:], self.g[ndt:],
                                  self.beta[ndt:], state_pool, cu_seqlens_prefill,
-                                 self.out[ndt:], scale=self.scale,
+                                 out[ndt:], scale=self.scale,
                                  state_indices=state_indices[nd:],
                                  has_initial_state=(None if has_initial_state is None
                                                     else has_initial_state[nd:]),
                                  algo=self.algo, workspace=self.workspace, stream=stream)
-        return self.out
+        return out
+
+
+class GdnHostPipeline:
+    """Steps fed from and drained to pinned host memory, pipelined over three
+    streams: step i's inputs are copied in while step i - 1 computes and step
+    i - 1's output is copied out while step i computes.  Two device buffers of
+    each per-step input and of the output alternate between steps; events keep
+    a buffer from being refilled before the compute that reads it (or the copy
+    that drains it) is done.
+
+    ``host_inputs`` passed to ``submit`` hold the per-step tensors by name:
+    mixed_qkv, a_raw, b_raw, cu_seqlens, state_indices, has_initial_state and
+    cu_seqlens_prefill (pinned, the shapes of the first call).  The weights and
+    the state and conv pools stay on the device across steps."""
+
+    INPUTS = ("mixed_qkv", "a_raw", "b_raw", "cu_seqlens", "state_indices", "has_initial_state",
+              "cu_seqlens_prefill")
+
+    def __init__(self, step: GdnStep, device):
+        self.step = step
+        self.dev = torch.device(device)
+        self.s_in = torch.cuda.Stream(device=self.dev)
+        self.s_run = torch.cuda.Stream(device=self.dev)
+        self.s_out = torch.cuda.Stream(device=self.dev)
+        self.bufs = None
+        self.outs = [torch.empty_like(step.out) for _ in range(2)]
+        self.ev_in = [torch.cuda.Event() for _ in range(2)]
+        self.ev_run = [torch.cuda.Event() for _ in range(2)]
+        self.ev_out = [torch.cuda.Event() for _ in range(2)]
+        self.n = 0
+
+    def submit(self, host_inputs, host_out, conv_weight, A_log, dt_bias, state_pool, conv_pool):
+        """Enqueues one step (asynchronous); host_out receives its output."""
+        if self.bufs is None:
+            self.bufs = [{k: torch.empty(host_inputs[k].shape, dtype=host_inputs[k].dtype,
+                                         device=self.dev) for k in self.INPUTS}
+                         for _ in range(2)]
+        b, i = self.n % 2, self.n
+        d = self.bufs[b]
+        with torch.cuda.stream(self.s_in):
+            if i >= 2:  # step i - 2 has read these buffers
+                self.s_in.wait_event(self.ev_run[b])
+            for k in self.INPUTS:
+                d[k].copy_(host_inputs[k], non_blocking=True)
+            self.ev_in[b].record(self.s_in)
+        self.s_run.wait_event(self.ev_in[b])
+        if i >= 2:  # step i - 2's output has been copied out of this buffer
+            self.s_run.wait_event(self.ev_out[b])
+        self.step.run(d["mixed_qkv"], d["a_raw"], d["b_raw"], conv_weight, A_log, dt_bias,
+                      d["cu_seqlens"], d["state_indices"], d["has_initial_state"], state_pool,
+                      conv_pool, d["cu_seqlens_prefill"], stream=self.s_run, out=self.outs[b])
+        self.ev_run[b].record(self.s_run)
+        with torch.cuda.stream(self.s_out):
+            self.s_out.wait_event(self.ev_run[b])
+            host_out.copy_(self.outs[b], non_blocking=True)
+            self.ev_out[b].record(self.s_out)
+        self.n += 1
+
+    def synchronize(self):
+        for s in (self.s_in, self.s_run, self.s_out):
+            s.synchronize()
 
 
 def mixed_step(mixed_qkv, a_raw, b_raw, conv_weight, A_log, dt_bias, cu_seqlens, state_indices,

@@ -64,3 +64,48 @@ def test_mixed_hv64_full_size_sampled(cuda_device):
     seqs = list(range(0, 512, 37)) + [512, 513, 514, 515]
     e = run_mixed(w, cuda_device, seqs, [0, 1, 30, 63])
     print(f"mixed_hv64: out err {e[0]:.2e}, state err {e[1]:.2e}")
+
+
+def test_host_pipeline_matches_sequential_steps(cuda_device):
+    """GdnHostPipeline (inputs copied in and outputs copied out on their own
+    streams, overlapping the neighbouring steps' compute) gives bit-identical
+    outputs, state and conv pools to the same steps run one after another."""
+    w = W.make_workload("pipe", 402, [1] * 5 + [70, 129], 2, 4, 128, 128, slots=12, n_decode=5,
+                        prefill_new=True, state_std=0.3)
+    steps = 3
+    # per-step inputs differ: a fresh mixed_qkv per step
+    gen = torch.Generator().manual_seed(11)
+    xs = [torch.randn(w.mixed_qkv.shape, generator=gen).to(w.mixed_qkv.dtype) for _ in range(steps)]
+
+    def make_step(d):
+        return layer.GdnStep(w.T, w.N, w.n_decode, w.Hk, w.Hv, w.Dk, w.Dv, w.K, w.act_dtype,
+                             cuda_device)
+
+    # sequential reference on the device
+    d1 = H.to_dev(w, cuda_device)
+    st1 = make_step(d1)
+    ref_out = []
+    for x in xs:
+        o = st1.run(x.to(cuda_device), d1["a_raw"], d1["b_raw"], d1["conv_weight"], d1["A_log"],
+                    d1["dt_bias"], d1["cu_seqlens"], d1["state_indices"], d1["has_initial_state"],
+                    d1["state_pool"], d1["conv_pool"], d1["cu_seqlens_prefill"])
+        ref_out.append(o.clone())
+    torch.cuda.synchronize()
+
+    # pipelined from pinned host memory
+    d2 = H.to_dev(w, cuda_device)
+    pipe = layer.GdnHostPipeline(make_step(d2), cuda_device)
+    host_outs = [torch.empty(w.T, w.Hv, w.Dv, dtype=w.act_dtype).pin_memory() for _ in range(steps)]
+    for x, ho in zip(xs, host_outs):
+        host_in = {"mixed_qkv": x.pin_memory(), "a_raw": w.a_raw.pin_memory(),
+                   "b_raw": w.b_raw.pin_memory(), "cu_seqlens": w.cu_seqlens.pin_memory(),
+                   "state_indices": w.state_indices.pin_memory(),
+                   "has_initial_state": w.has_initial_state.pin_memory(),
+                   "cu_seqlens_prefill": w.cu_seqlens_prefill.pin_memory()}
+        pipe.submit(host_in, ho, d2["conv_weight"], d2["A_log"], d2["dt_bias"], d2["state_pool"],
+                    d2["conv_pool"])
+    pipe.synchronize()
+    for r, ho in zip(ref_out, host_outs):
+        assert torch.equal(r.cpu(), ho)
+    assert torch.equal(d1["state_pool"], d2["state_pool"])
+    assert torch.equal(d1["conv_pool"], d2["conv_pool"])
