@@ -148,6 +148,12 @@ def _declare(L):
         [_i64] * 18 + [ctypes.c_char_p, ctypes.c_size_t])
     L.orc_validate_cu_seqlens.restype = ctypes.c_int
     L.orc_validate_cu_seqlens.argtypes = [_vp, _i64, _i64, ctypes.c_char_p, ctypes.c_size_t]
+    for suf, ct in (("f32", ctypes.c_float), ("f64", ctypes.c_double)):
+        fn = getattr(L, f"orc_gated_rmsnorm_{suf}")
+        fn.restype = ctypes.c_int
+        fn.argtypes = [_vp, _vp, _i64, _vp, _vp, _i64, _i64, _i64, ct, ctypes.c_int, ctypes.c_int]
+    L.orc_validate_gated_rms_norm_shape.restype = ctypes.c_int
+    L.orc_validate_gated_rms_norm_shape.argtypes = [_i64] * 7 + [ctypes.c_char_p, ctypes.c_size_t]
     L.orc_validate_state_indices.restype = ctypes.c_int
     L.orc_validate_state_indices.argtypes = [_vp, _i64, _i64, ctypes.c_int, ctypes.c_char_p,
                                              ctypes.c_size_t]
@@ -351,3 +357,35 @@ def gdn_chunked_f64(q, k, v, g, beta, state_pool, cu_seqlens, scale, chunk,
 
 def num_threads_default() -> int:
     return os.cpu_count() or 1
+
+
+# ---- O5 gated RMSNorm -------------------------------------------------------------
+
+def validate_gated_rms_norm_shape(core_len, z_len, weight_len, out_len, tokens, heads, dim):
+    b = _msgbuf()
+    rc = _load().orc_validate_gated_rms_norm_shape(int(core_len), int(z_len), int(weight_len),
+                                                    int(out_len), int(tokens), int(heads),
+                                                    int(dim), b, 512)
+    return rc, b.value.decode()
+
+
+def gated_rmsnorm(core, z, weight, eps, sigmoid_gate=False, dtype=np.float64, nthreads=0):
+    """out [T, H, D] = core / sqrt(mean_d core^2 + eps) * weight * act(z) per (token, head).
+    core [T, H, D]; z [T, H, D] or [T, >= H*D] (token rows of the gate, as a
+    merged projection's slice: the first H*D entries of each row are used)."""
+    dt = np.dtype(dtype)
+    core = _arr(core, dt, "core")
+    T, H, D = core.shape
+    z = _arr(z, dt, "z")
+    z2 = z.reshape(T, -1)
+    if z2.shape[1] < H * D:
+        raise ValueError("z rows shorter than heads * dim")
+    w = _arr(weight, dt, "weight")
+    out = np.empty_like(core)
+    rc, msg = validate_gated_rms_norm_shape(core.size, T * H * D, w.size, out.size, T, H, D)
+    if rc != ORC_OK:
+        raise OracleError(rc, msg)
+    fn = getattr(_load(), f"orc_gated_rmsnorm_{_suffix(dt)}")
+    _check(fn(_ptr(core), _ptr(z2), z2.shape[1], _ptr(w), _ptr(out), T, H, D, eps,
+              int(bool(sigmoid_gate)), int(nthreads)), "gated_rmsnorm")
+    return out

@@ -377,6 +377,28 @@ void chunk_step(const std::vector<double>& Kc, const std::vector<double>& Qc,
     }
 }
 
+// Gated RMSNorm of the recurrence output, [cpu.rs] gated_rms_norm_f32 (SiLU
+// gate) with [cpu_ops.cpp] RmsNormGatedKernel's options: a sigmoid gate and a
+// gate tensor [T, H, D] whose token rows are z_stride elements apart.  Per
+// (token, head) row of D values:
+//   inv = 1 / sqrt(sum_d core^2 / D + eps),  out = core * inv * weight[d] * act(z).
+template <typename T>
+void gated_rmsnorm_(const T* core, const T* z, int64_t z_stride, const T* weight, T* out,
+                    int64_t tokens, int64_t heads, int64_t dim, T eps, bool sigmoid_gate,
+                    int nthreads) {
+  parallel_items(tokens * heads, nthreads, [&](int64_t row) {
+    const T* x = core + row * dim;
+    const T* zr = z + (row / heads) * z_stride + (row % heads) * dim;
+    T sum_sq = 0;
+    for (int64_t d = 0; d < dim; ++d) sum_sq += x[d] * x[d];
+    const T inv = T(1) / std::sqrt(sum_sq / static_cast<T>(dim) + eps);
+    for (int64_t d = 0; d < dim; ++d) {
+      const T act = sigmoid_gate ? sigmoid_(zr[d]) : silu_(zr[d]);
+      out[row * dim + d] = x[d] * inv * weight[d] * act;
+    }
+  });
+}
+
 }  // namespace
 
 extern "C" {
@@ -665,6 +687,47 @@ int orc_gdn_chunked_f64(const double* q, const double* k, const double* v, const
           for (int64_t d = 0; d < dv; ++d) out[((c0 + i) * hv_n + h) * dv + d] = Oc[i * dv + d];
       }
     }
+  return ORC_OK;
+}
+
+int orc_validate_gated_rms_norm_shape(int64_t core_len, int64_t z_len, int64_t weight_len,
+                                      int64_t out_len, int64_t tokens, int64_t heads,
+                                      int64_t dim, char* msg, size_t cap) {
+  if (tokens <= 0 || heads <= 0 || dim <= 0) {
+    set_msg(msg, cap,
+            "gated_rms_norm shape must be positive, got tokens=" + std::to_string(tokens) +
+                " heads=" + std::to_string(heads) + " dim=" + std::to_string(dim));
+    return ORC_ERR_SHAPE;
+  }
+  const int64_t expected = tokens * heads * dim;
+  const struct {
+    const char* label;
+    int64_t actual, expected;
+  } rules[] = {{"core", core_len, expected},
+               {"z", z_len, expected},
+               {"weight", weight_len, dim},
+               {"out", out_len, expected}};
+  for (const auto& r : rules)
+    if (r.actual < r.expected) {
+      set_msg(msg, cap,
+              std::string("gated_rms_norm ") + r.label + " length " + std::to_string(r.actual) +
+                  " < expected " + std::to_string(r.expected));
+      return ORC_ERR_SHAPE;
+    }
+  return ORC_OK;
+}
+
+#define ORC_GRN_PARAMS(T)                                                                   \
+  const T *core, const T *z, int64_t z_stride, const T *weight, T *out, int64_t tokens,    \
+      int64_t heads, int64_t dim, T eps, int sigmoid_gate, int nthreads
+int orc_gated_rmsnorm_f32(ORC_GRN_PARAMS(float)) {
+  gated_rmsnorm_<float>(core, z, z_stride, weight, out, tokens, heads, dim, eps,
+                        sigmoid_gate != 0, nthreads);
+  return ORC_OK;
+}
+int orc_gated_rmsnorm_f64(ORC_GRN_PARAMS(double)) {
+  gated_rmsnorm_<double>(core, z, z_stride, weight, out, tokens, heads, dim, eps,
+                         sigmoid_gate != 0, nthreads);
   return ORC_OK;
 }
 

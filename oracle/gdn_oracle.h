@@ -142,6 +142,23 @@ int orc_gdn_chunked_f64(const double* query, const double* key, const double* va
                         int64_t key_dim, int64_t value_dim, double scale, int use_qk_l2norm,
                         int64_t chunk, double* out);
 
+/* ---- O5 gated RMSNorm of the recurrence output ----------------------------
+ * [cpu.rs] gated_rms_norm_f32 / validate_gated_rms_norm_shape, with
+ * [cpu_ops.cpp] RmsNormGatedKernel's sigmoid-gate option and strided gate.
+ * core, out [tokens, heads, dim] contiguous; z [tokens, heads, dim] with token
+ * rows z_stride elements apart (z_stride >= heads * dim); weight [dim].
+ * out = core / sqrt(mean(core^2) + eps) * weight * act(z), act = silu, or the
+ * sigmoid when sigmoid_gate != 0; one row per (token, head). */
+int orc_validate_gated_rms_norm_shape(int64_t core_len, int64_t z_len, int64_t weight_len,
+                                      int64_t out_len, int64_t tokens, int64_t heads,
+                                      int64_t dim, char* msg, size_t cap);
+int orc_gated_rmsnorm_f32(const float* core, const float* z, int64_t z_stride,
+                          const float* weight, float* out, int64_t tokens, int64_t heads,
+                          int64_t dim, float eps, int sigmoid_gate, int nthreads);
+int orc_gated_rmsnorm_f64(const double* core, const double* z, int64_t z_stride,
+                          const double* weight, double* out, int64_t tokens, int64_t heads,
+                          int64_t dim, double eps, int sigmoid_gate, int nthreads);
+
 #ifdef __cplusplus
 }
 #endif

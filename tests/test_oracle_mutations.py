@@ -6,13 +6,15 @@ build and checks that the named pin now fails.  The mistakes are the kinds a
 restatement of the pages could make: a dropped or misplaced decay, a flipped
 sign, a swapped operand, a wrong GQA index, reversed conv taps, a wrong tail
 window, eps outside the sqrt, a wrong sigmoid branch or softplus threshold, a
-dropped factor in the chunked form.
+dropped factor in the chunked form, a gated norm over the sum instead of the
+mean, swapped gates or unstrided gate rows.
 """
 import os
 
 import pytest
 
 import oracle
+import test_oracle_gated_norm as N
 import test_oracle_gates as G
 import test_oracle_prepare as P
 import test_oracle_recurrence as R
@@ -54,6 +56,22 @@ MUTATIONS = [
      "if (x > R(20)) return x;",
      "if (x > R(2)) return x;",
      [G.test_softplus_matches_logaddexp]),
+    ("gated_norm_sum_not_mean",
+     "std::sqrt(sum_sq / static_cast<T>(dim) + eps)",
+     "std::sqrt(sum_sq + eps)",
+     [lambda: N.test_unit_rms_without_eps(False)]),
+    ("gated_norm_eps_outside_sqrt",
+     "std::sqrt(sum_sq / static_cast<T>(dim) + eps)",
+     "(std::sqrt(sum_sq / static_cast<T>(dim)) + eps)",
+     [N.test_constant_row_closed_form]),
+    ("gated_norm_gates_swapped",
+     "sigmoid_gate ? sigmoid_(zr[d]) : silu_(zr[d])",
+     "sigmoid_gate ? silu_(zr[d]) : sigmoid_(zr[d])",
+     [N.test_constant_row_closed_form]),
+    ("gated_norm_gate_rows_unstrided",
+     "z + (row / heads) * z_stride + (row % heads) * dim",
+     "z + row * dim",
+     [N.test_strided_gate_rows]),
     ("chunked_drops_decay_in_W",
      "const double tw = T[i * L + j] * bc[j] * std::exp(gam[j]);",
      "const double tw = T[i * L + j] * bc[j];",
