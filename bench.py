@@ -279,6 +279,35 @@ def roofline_entry(w, kernel_ms, peaks):
                  "traffic_source": how, "peak_source": peaks["source"]}, rep
 
 
+def time_gated_rmsnorm(w, dev, peaks, iters=20):
+    """gdn_gated_rmsnorm on the step's output shape [T, Hv, Dv] (bf16; the
+    step after the recurrence, not part of the GDN step timed above).
+    Algorithmic bytes: core and z read, out written once (2 bytes each)."""
+    import torch
+    from gated_delta_rule_44_gb300 import binding as B
+    g = torch.Generator().manual_seed(17)
+    shape = (w.T, w.Hv, w.Dv)
+    core = torch.randn(shape, generator=g).to(torch.bfloat16).to(dev)
+    z = torch.randn(shape, generator=g).to(torch.bfloat16).to(dev)
+    wt = (torch.rand(w.Dv, generator=g) + 0.5).to(torch.bfloat16).to(dev)
+    out = torch.empty_like(core)
+    s = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        B.gdn_gated_rmsnorm(core, z, wt, out, stream=s)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(s)
+    for _ in range(iters):
+        B.gdn_gated_rmsnorm(core, z, wt, out, stream=s)
+    e1.record(s)
+    torch.cuda.synchronize(dev)
+    us = e0.elapsed_time(e1) / iters * 1e3
+    nbytes = core.numel() * 2 * 3 + w.Dv * 2
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"shape": list(shape), "avg_us": round(us, 2), "algorithmic_bytes": nbytes,
+            "achieved_gbs": round(gbs, 1), "hbm_frac_of_measured": round(gbs / peaks["hbm"], 4)}
+
+
 def time_e2e(w, dev, steps, warmup, algo):
     """Same step through the public API with the step's inputs in pinned host
     memory: every step copies its inputs host -> device and its output
@@ -462,6 +491,7 @@ def main():
                            "ms_per_step": round(rx["ms_per_step"], 4), "roofline": rf,
                            "kernels": kx}
             del wx
+        extra["gated_rmsnorm"] = time_gated_rmsnorm(w, dev, peaks)
         line["extra_workloads"] = extra
     if rank == 0 and not args.no_e2e:
         line["e2e"] = time_e2e(w, dev, max(3, args.steps // 2), 3, args.algo)

@@ -75,7 +75,15 @@ class gdn_prefill_args(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_size_t)]
 
 
-EXPORTED = ("gdn_prepare", "gdn_decode", "gdn_prefill_varlen", "gdn_prefill_workspace_bytes",
+class gdn_gated_rmsnorm_args(ctypes.Structure):
+    _fields_ = [("tokens", _i64), ("heads", _i64), ("dim", _i64), ("act_dtype", _i32),
+                ("sigmoid_gate", _i32), ("eps", _f32), ("core", _vp), ("core_len", _i64),
+                ("z", _vp), ("z_len", _i64), ("z_token_stride", _i64), ("weight", _vp),
+                ("weight_len", _i64), ("out", _vp), ("out_len", _i64)]
+
+
+EXPORTED = ("gdn_prepare", "gdn_decode", "gdn_prefill_varlen", "gdn_gated_rmsnorm",
+            "gdn_prefill_workspace_bytes",
             "gdn_prefill_resolve_algo", "gdn_status_string", "gdn_last_error_message",
             "gdn_read_device_status", "gdn_version", "gdn_launch_count")
 
@@ -98,12 +106,13 @@ def lib() -> ctypes.CDLL:
     with _lock:
         if _lib is None:
             L = ctypes.CDLL(_build.build_library())
-            for name in ("gdn_prepare", "gdn_decode", "gdn_prefill_varlen",
+            for name in ("gdn_prepare", "gdn_decode", "gdn_prefill_varlen", "gdn_gated_rmsnorm",
                          "gdn_read_device_status", "gdn_version"):
                 getattr(L, name).restype = ctypes.c_int
             L.gdn_prepare.argtypes = [ctypes.POINTER(gdn_prepare_args), _vp]
             L.gdn_decode.argtypes = [ctypes.POINTER(gdn_decode_args), _vp]
             L.gdn_prefill_varlen.argtypes = [ctypes.POINTER(gdn_prefill_args), _vp]
+            L.gdn_gated_rmsnorm.argtypes = [ctypes.POINTER(gdn_gated_rmsnorm_args), _vp]
             L.gdn_read_device_status.argtypes = [_vp]
             L.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
             L.gdn_prefill_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64, _i64, _i32, _i32]
@@ -199,6 +208,20 @@ def gdn_decode(q, k, v, g, beta, state, out, *, scale=-1.0, state_indices=None,
         state_slots=state.shape[0], state_len=_n(state), state_indices=_p(state_indices),
         state_indices_host=sih_p, out=_p(out), out_len=_n(out))
     _check(lib().gdn_decode(ctypes.byref(a), _stream(stream)))
+
+
+def gdn_gated_rmsnorm(core, z, weight, out, *, eps=1e-6, sigmoid_gate=False, stream=None) -> None:
+    """include/gdn.h gdn_gated_rmsnorm.  core, out [T, H, D]; weight [D]; z
+    [T, H, D] or a [T, >= H*D] tensor whose rows are the gate's token rows
+    (e.g. a slice of a merged projection), row stride taken from it."""
+    T, H, D = core.shape
+    z_stride = z.stride(0)
+    a = gdn_gated_rmsnorm_args(
+        tokens=T, heads=H, dim=D, act_dtype=_dt(core), sigmoid_gate=int(bool(sigmoid_gate)),
+        eps=float(eps), core=_p(core), core_len=_n(core), z=_p(z),
+        z_len=(T - 1) * z_stride + H * D, z_token_stride=z_stride, weight=_p(weight),
+        weight_len=_n(weight), out=_p(out), out_len=_n(out))
+    _check(lib().gdn_gated_rmsnorm(ctypes.byref(a), _stream(stream)))
 
 
 def gdn_prefill_workspace_bytes(T, N, Hv, Dk, Dv, act_dtype=GDN_DTYPE_BF16,

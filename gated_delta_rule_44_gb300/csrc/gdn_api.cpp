@@ -343,6 +343,51 @@ int gdn_decode(const gdn_decode_args* a, void* stream) {
   return launch_result(gdn::launch_decode(p, static_cast<cudaStream_t>(stream)), "gdn_decode");
 }
 
+int gdn_gated_rmsnorm(const gdn_gated_rmsnorm_args* a, void* stream) {
+  if (a == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "args is NULL");
+  if (int rc = check_act_dtype(a->act_dtype)) return rc;
+  // [cpu.rs] validate_gated_rms_norm_shape
+  if (a->tokens <= 0 || a->heads <= 0 || a->dim <= 0)
+    return fail(GDN_ERR_SHAPE, "gated_rms_norm shape must be positive, got tokens=" +
+                                   S(a->tokens) + " heads=" + S(a->heads) + " dim=" + S(a->dim));
+  const int64_t row = a->heads * a->dim, total = a->tokens * row;
+  const int64_t z_stride = a->z_token_stride > 0 ? a->z_token_stride : row;
+  if (z_stride < row)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gated_rms_norm z token stride shorter than heads * dim");
+  const LenRule rules[] = {
+      {"core", a->core_len, total},
+      {"z", a->z_len, (a->tokens - 1) * z_stride + row},
+      {"weight", a->weight_len, a->dim},
+      {"out", a->out_len, total},
+  };
+  if (int rc = check_lengths("gated_rms_norm", rules)) return rc;
+  for (auto pr : {std::make_pair(a->core, "core"), std::make_pair(a->z, "z"),
+                  std::make_pair(a->weight, "weight"), std::make_pair((const void*)a->out, "out")}) {
+    if (int rc = require_ptr(pr.first, pr.second)) return rc;
+    if (int rc = require_aligned(pr.first, pr.second)) return rc;
+  }
+  const int64_t es = elem_size(a->act_dtype), vec = 16 / es;
+  if ((z_stride * es) % 16 != 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gated_rms_norm z token stride must be a multiple of 16 bytes");
+  if (a->dim % vec != 0 || a->dim > 128 * vec)
+    return fail(GDN_ERR_UNSUPPORTED, "gdn_gated_rmsnorm supports dim a multiple of " + S(vec) +
+                                         " and at most " + S(128 * vec));
+  gdn::NormLaunch p{};
+  p.rows = total / a->dim;
+  p.heads = (int)a->heads;
+  p.dim = (int)a->dim;
+  p.bf16 = a->act_dtype == GDN_DTYPE_BF16;
+  p.sigmoid_gate = a->sigmoid_gate != 0;
+  p.eps = a->eps;
+  p.core = a->core;
+  p.z = a->z;
+  p.z_stride = z_stride;
+  p.weight = a->weight;
+  p.out = a->out;
+  return launch_result(gdn::launch_gated_rmsnorm(p, static_cast<cudaStream_t>(stream)),
+                       "gdn_gated_rmsnorm");
+}
+
 int32_t gdn_prefill_resolve_algo(int64_t Dk, int64_t Dv, int32_t act_dtype, int32_t algo) {
   if (algo != GDN_PREFILL_AUTO) return algo;
   return gdn::chunked_supported((int)Dk, (int)Dv, act_dtype == GDN_DTYPE_BF16)

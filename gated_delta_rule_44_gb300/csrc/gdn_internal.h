@@ -78,6 +78,20 @@ struct ChunkedLaunch {
   size_t workspace_bytes;
 };
 bool chunked_supported(int Dk, int Dv, bool bf16);
+
+// Gated RMSNorm of the recurrence output.
+struct NormLaunch {
+  int64_t rows;   // tokens * heads
+  int heads, dim;
+  bool bf16, sigmoid_gate;
+  float eps;
+  const void* core;
+  const void* z;
+  int64_t z_stride;  // elements between token rows of z
+  const void* weight;
+  void* out;
+};
+cudaError_t launch_gated_rmsnorm(const NormLaunch& p, cudaStream_t s);
 size_t chunked_workspace_bytes(int64_t T, int64_t N, int64_t Hv, int64_t Dk, int64_t Dv);
 cudaError_t launch_chunked(const ChunkedLaunch& p, cudaStream_t s);
 

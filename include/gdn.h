@@ -251,6 +251,47 @@ int gdn_prefill_varlen(const gdn_prefill_args* args, void* stream);
  *     (on different streams or from different host threads) race on it. */
 int gdn_prefill_varlen_noalloc(const gdn_prefill_args* args, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * gdn_gated_rmsnorm -- [cpu.rs] gated_rms_norm_f32 and
+ * validate_gated_rms_norm_shape; [cpu_ops.cpp] RmsNormGatedKernel (the
+ * sigmoid-gate option, and a gate tensor whose token rows are strided, as a
+ * slice of a merged projection).  The step after the recurrence.
+ *
+ * Per (token t, head h) row of `dim` values:
+ *   out[t,h,:] = core[t,h,:] / sqrt(mean_d(core[t,h,d]^2) + eps)
+ *                * weight[:] * act(z[t,h,:])
+ * act = silu, or the sigmoid when sigmoid_gate != 0.  f32 arithmetic; out is
+ * rounded to act_dtype once.
+ *
+ * core, out [tokens, heads, dim] contiguous; weight [dim]; z [tokens, heads,
+ * dim] with token rows z_token_stride elements apart (0 = heads * dim).  All in
+ * act_dtype.  Lengths follow cpu.rs (core, z, out >= tokens*heads*dim; z >=
+ * (tokens-1)*stride + heads*dim when strided; weight >= dim).  Pointers 16-byte
+ * aligned; z_token_stride * element size a multiple of 16 bytes.
+ * Supported: dim a multiple of 8 (bf16) or 4 (f32); dim <= 1024 (bf16), 512 (f32).
+ * Errors: GDN_ERR_SHAPE (non-positive sizes, short buffers; cpu.rs's texts),
+ * GDN_ERR_INVALID_ARGUMENT (NULL or misaligned pointers, bad stride),
+ * GDN_ERR_UNSUPPORTED (dim), GDN_ERR_DTYPE; nothing is launched on error.
+ * Asynchronous on `stream`; the caller owns every buffer.
+ * ------------------------------------------------------------------------- */
+typedef struct gdn_gated_rmsnorm_args {
+  int64_t tokens, heads, dim;
+  int32_t act_dtype;        /* gdn_dtype of core, z, weight, out */
+  int32_t sigmoid_gate;     /* 0: silu(z); else sigmoid(z) */
+  float eps;
+  const void* core;         /* [tokens, heads, dim] */
+  int64_t core_len;
+  const void* z;            /* [tokens, heads, dim], token rows z_token_stride apart */
+  int64_t z_len;
+  int64_t z_token_stride;   /* elements; 0 = heads * dim */
+  const void* weight;       /* [dim] */
+  int64_t weight_len;
+  void* out;                /* [tokens, heads, dim] */
+  int64_t out_len;
+} gdn_gated_rmsnorm_args;
+
+int gdn_gated_rmsnorm(const gdn_gated_rmsnorm_args* args, void* stream);
+
 /* Scratch bytes gdn_prefill_varlen needs for these sizes and algorithm (0 for
  * the recurrent algorithm).  Depends only on the arguments. */
 size_t gdn_prefill_workspace_bytes(int64_t T, int64_t N, int64_t Hv, int64_t Dk, int64_t Dv,

@@ -185,3 +185,44 @@ def test_valid_call_without_gpu_stops_before_launch():
         pytest.skip("this machine has a GPU")
     rc, msg = call_decode(decode_args())
     assert rc == B.GDN_ERR_CUDA
+
+
+def norm_args(T=3, H=2, D=128, **over):
+    a = dict(tokens=T, heads=H, dim=D, act_dtype=B.GDN_DTYPE_BF16, sigmoid_gate=0, eps=1e-6,
+             core=FAKE, core_len=T * H * D, z=FAKE, z_len=T * H * D, z_token_stride=0,
+             weight=FAKE, weight_len=D, out=FAKE, out_len=T * H * D)
+    a.update(over)
+    return B.gdn_gated_rmsnorm_args(**a)
+
+
+def call_norm(args):
+    L = B.lib()
+    rc = L.gdn_gated_rmsnorm(ctypes.byref(args), None)
+    return rc, L.gdn_last_error_message().decode()
+
+
+def test_gated_rmsnorm_shape_messages():
+    # [cpu.rs] validate_gated_rms_norm_shape texts
+    rc, msg = call_norm(norm_args(T=0))
+    assert rc == B.GDN_ERR_SHAPE
+    assert msg == "gated_rms_norm shape must be positive, got tokens=0 heads=2 dim=128"
+    for field, label, n, expected in (("core_len", "core", 767, 768), ("z_len", "z", 700, 768),
+                                      ("weight_len", "weight", 127, 128),
+                                      ("out_len", "out", 1, 768)):
+        rc, msg = call_norm(norm_args(**{field: n}))
+        assert rc == B.GDN_ERR_SHAPE
+        assert msg == f"gated_rms_norm {label} length {n} < expected {expected}"
+
+
+def test_gated_rmsnorm_other_rejections():
+    assert call_norm(norm_args(act_dtype=9))[0] == B.GDN_ERR_DTYPE
+    assert call_norm(norm_args(core=None))[0] == B.GDN_ERR_INVALID_ARGUMENT
+    assert call_norm(norm_args(z=FAKE + 4))[0] == B.GDN_ERR_INVALID_ARGUMENT
+    assert call_norm(norm_args(z_token_stride=100))[0] == B.GDN_ERR_INVALID_ARGUMENT  # < H*D
+    assert call_norm(norm_args(z_token_stride=260, z_len=10**6))[0] == B.GDN_ERR_INVALID_ARGUMENT
+    rc, msg = call_norm(norm_args(D=12, core_len=72, z_len=72, weight_len=12, out_len=72))
+    assert rc == B.GDN_ERR_UNSUPPORTED and "multiple of 8" in msg
+    big = 2048
+    rc, _ = call_norm(norm_args(D=big, core_len=6 * big, z_len=6 * big, weight_len=big,
+                                out_len=6 * big))
+    assert rc == B.GDN_ERR_UNSUPPORTED
