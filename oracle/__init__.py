@@ -130,6 +130,10 @@ def _declare(L):
         fn.restype = ctypes.c_int
         fn.argtypes = ([_vp] * 6 + [_i64, _vp, _vp, _vp] + [_i64] * 6 + [ct, ctypes.c_int, _vp,
                        _i64, _vp, ctypes.c_int])
+        fn = getattr(L, f"orc_kda_varlen_{suf}")
+        fn.restype = ctypes.c_int
+        fn.argtypes = ([_vp] * 6 + [_i64, _vp, _vp, _vp] + [_i64] * 6 + [ct, ctypes.c_int, _vp,
+                       _i64, _vp, ctypes.c_int])
         fn = getattr(L, f"orc_gdn_decode_{suf}")
         fn.restype = ctypes.c_int
         fn.argtypes = ([_vp] * 6 + [_i64, _vp] + [_i64] * 5 + [ct, ctypes.c_int, _vp,
@@ -319,6 +323,31 @@ def gdn_varlen(q, k, v, g, beta, state_pool, cu_seqlens, scale, state_indices=No
         _ptr(hi), _ptr(cu), cu.size - 1, T, Hk, Hv, Dk, Dv, float(scale), int(use_qk_l2norm),
         _ptr(it), 0 if it is None else it.size, _ptr(out), int(nthreads))
     _check(rc, "gdn_varlen")
+    return out
+
+
+def kda_varlen(q, k, v, g, beta, state_pool, cu_seqlens, scale, state_indices=None,
+               has_initial_state=None, items=None, out=None, dtype=np.float32, nthreads=0):
+    """O6, the KDA recurrence.  As gdn_varlen, but g [T,Hv,Dk] is a log decay per
+    key channel and q, k are used as given (no L2 norm)."""
+    sfx = _suffix(dtype)
+    q, k, v, g, beta, T, Hk, Dk, Hv, Dv = _recur_inputs(q, k, v, g, beta, dtype)
+    if g.shape != (T, Hv, Dk):
+        raise ValueError(f"KDA g must be [T, Hv, Dk] = {(T, Hv, Dk)}, got {g.shape}")
+    pool = _inplace(state_pool, dtype, "state_pool")
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    si = None if state_indices is None else np.ascontiguousarray(state_indices, dtype=np.int32)
+    hi = None if has_initial_state is None else np.ascontiguousarray(has_initial_state,
+                                                                     dtype=np.uint8)
+    it = None if items is None else np.ascontiguousarray(items, dtype=np.int32)
+    if out is None:
+        out = np.zeros((T, Hv, Dv), dtype)
+    out = _inplace(out, dtype, "out")
+    rc = getattr(_load(), f"orc_kda_varlen_{sfx}")(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(pool), pool.shape[0], _ptr(si),
+        _ptr(hi), _ptr(cu), cu.size - 1, T, Hk, Hv, Dk, Dv, float(scale), 0,
+        _ptr(it), 0 if it is None else it.size, _ptr(out), int(nthreads))
+    _check(rc, "kda_varlen")
     return out
 
 

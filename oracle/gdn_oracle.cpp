@@ -248,12 +248,51 @@ void head_chain(const R* q, const R* k, const R* v, const R* g, const R* beta, R
   }
 }
 
+// The KDA variant of one (sequence, value head) chain, [cpu_ops.cpp]
+// KdaHeadTokenStep: the decay is per key channel, g [T, Hv, Dk] (log decay of
+// column d of S), and q, k are used as given.  Per token, in the page's order:
+// first every row decays and takes its dot with k, then every row gets its
+// rank-1 update and its dot with scale * q.
+template <typename R>
+void kda_head_chain(const R* q, const R* k, const R* v, const R* g, const R* beta, R* S,
+                    int64_t t0, int64_t t1, int64_t h, int64_t hk, int64_t hk_n, int64_t hv_n,
+                    int64_t dk, int64_t dv, R scale, R* out) {
+  std::vector<R> qbuf(dk), kbuf(dk), vbuf(dv), decay(dk);
+  for (int64_t t = t0; t < t1; ++t) {
+    const R beta_t = beta[t * hv_n + h];
+    const R* g_row = g + (t * hv_n + h) * dk;
+    for (int64_t d = 0; d < dk; ++d) {
+      qbuf[d] = q[(t * hk_n + hk) * dk + d] * scale;
+      kbuf[d] = k[(t * hk_n + hk) * dk + d];
+      decay[d] = std::exp(g_row[d]);
+    }
+    for (int64_t vd = 0; vd < dv; ++vd) {
+      R* row = S + vd * dk;
+      R dot = R(0);
+      for (int64_t d = 0; d < dk; ++d) {
+        row[d] *= decay[d];
+        dot += row[d] * kbuf[d];
+      }
+      vbuf[vd] = (v[(t * hv_n + h) * dv + vd] - dot) * beta_t;
+    }
+    for (int64_t vd = 0; vd < dv; ++vd) {
+      R* row = S + vd * dk;
+      R o = R(0);
+      for (int64_t d = 0; d < dk; ++d) {
+        row[d] += vbuf[vd] * kbuf[d];
+        o += row[d] * qbuf[d];
+      }
+      out[(t * hv_n + h) * dv + vd] = o;
+    }
+  }
+}
+
 template <typename R>
 int varlen_impl(const R* q, const R* k, const R* v, const R* g, const R* beta, R* pool,
                 int64_t slots, const int32_t* sidx, const uint8_t* has_init, const int32_t* cu,
                 int64_t n_seqs, int64_t tokens, int64_t hk_n, int64_t hv_n, int64_t dk,
                 int64_t dv, R scale, int use_norm, const int32_t* items, int64_t n_items, R* out,
-                int nthreads) {
+                int nthreads, bool kda = false) {
   if (n_seqs <= 0 || tokens <= 0 || hk_n <= 0 || hv_n <= 0 || dk <= 0 || dv <= 0)
     return ORC_ERR_SHAPE;
   if (hv_n % hk_n != 0) return ORC_ERR_SHAPE;
@@ -276,8 +315,12 @@ int varlen_impl(const R* q, const R* k, const R* v, const R* g, const R* beta, R
     R* S = pool + (slot * hv_n + h) * state_len;
     if (has_init != nullptr && has_init[s] == 0)
       for (int64_t e = 0; e < state_len; ++e) S[e] = R(0);
-    head_chain(q, k, v, g, beta, S, cu[s], cu[s + 1], h, h / ratio, hk_n, hv_n, dk, dv, scale,
-               use_norm != 0, out);
+    if (kda)
+      kda_head_chain(q, k, v, g, beta, S, cu[s], cu[s + 1], h, h / ratio, hk_n, hv_n, dk, dv,
+                     scale, out);
+    else
+      head_chain(q, k, v, g, beta, S, cu[s], cu[s + 1], h, h / ratio, hk_n, hv_n, dk, dv,
+                 scale, use_norm != 0, out);
   });
   return ORC_OK;
 }
@@ -621,6 +664,21 @@ int orc_gdn_varlen_f64(ORC_RECUR_PARAMS(double)) {
                              has_initial_state, cu_seqlens, n_seqs, tokens, key_heads,
                              value_heads, key_dim, value_dim, scale, use_qk_l2norm, items,
                              n_items, out, nthreads);
+}
+
+int orc_kda_varlen_f32(ORC_RECUR_PARAMS(float)) {
+  if (use_qk_l2norm != 0) return ORC_ERR_INVALID;  // KDA uses q, k as given
+  return varlen_impl<float>(query, key, value, g, beta, state_pool, state_slots, state_indices,
+                            has_initial_state, cu_seqlens, n_seqs, tokens, key_heads,
+                            value_heads, key_dim, value_dim, scale, 0, items, n_items, out,
+                            nthreads, true);
+}
+int orc_kda_varlen_f64(ORC_RECUR_PARAMS(double)) {
+  if (use_qk_l2norm != 0) return ORC_ERR_INVALID;
+  return varlen_impl<double>(query, key, value, g, beta, state_pool, state_slots, state_indices,
+                             has_initial_state, cu_seqlens, n_seqs, tokens, key_heads,
+                             value_heads, key_dim, value_dim, scale, 0, items, n_items, out,
+                             nthreads, true);
 }
 
 int orc_gdn_decode_f32(ORC_DECODE_PARAMS(float)) {

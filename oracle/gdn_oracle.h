@@ -120,6 +120,13 @@ int orc_prepare_varlen_f64(ORC_PREPARE_PARAMS(double));
 int orc_gdn_varlen_f32(ORC_RECUR_PARAMS(float));
 int orc_gdn_varlen_f64(ORC_RECUR_PARAMS(double));
 
+/* ---- O6 KDA: per-key-channel decay, [cpu_ops.cpp] KdaHeadTokenStep /
+ * KdaGatedDeltaRuleKernel.  Same contract as orc_gdn_varlen except that g is
+ * [T, Hv, Dk] (the log decay of each key channel) and use_qk_l2norm must be 0
+ * (q and k are used as given; ORC_ERR_INVALID otherwise). */
+int orc_kda_varlen_f32(ORC_RECUR_PARAMS(float));
+int orc_kda_varlen_f64(ORC_RECUR_PARAMS(double));
+
 /* ---- O3: decode, one token per row ----------------------------------------
  * [cpu_ops.cpp] GdnDecodeKernel semantics: row b uses pool slot
  * state_indices[b] (NULL -> b) in place; a negative index zeroes out row b and

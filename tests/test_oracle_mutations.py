@@ -7,14 +7,17 @@ restatement of the pages could make: a dropped or misplaced decay, a flipped
 sign, a swapped operand, a wrong GQA index, reversed conv taps, a wrong tail
 window, eps outside the sqrt, a wrong sigmoid branch or softplus threshold, a
 dropped factor in the chunked form, a gated norm over the sum instead of the
-mean, swapped gates or unstrided gate rows.
+mean, swapped gates or unstrided gate rows, a KDA decay taken from one channel
+or applied after the dot.
 """
 import os
 
+import numpy as np
 import pytest
 
 import oracle
 import test_oracle_gated_norm as N
+import test_oracle_kda as KD
 import test_oracle_gates as G
 import test_oracle_prepare as P
 import test_oracle_recurrence as R
@@ -72,6 +75,14 @@ MUTATIONS = [
      "z + (row / heads) * z_stride + (row % heads) * dim",
      "z + row * dim",
      [N.test_strided_gate_rows]),
+    ("kda_decay_of_channel_0",
+     "decay[d] = std::exp(g_row[d]);",
+     "decay[d] = std::exp(g_row[0]);",
+     [KD.test_key_channel_permutation]),
+    ("kda_decay_after_dot",
+     "        row[d] *= decay[d];\n        dot += row[d] * kbuf[d];",
+     "        dot += row[d] * kbuf[d];\n        row[d] *= decay[d];",
+     [lambda: KD.test_uniform_channel_decay_is_gdn(np.float64)]),
     ("chunked_drops_decay_in_W",
      "const double tw = T[i * L + j] * bc[j] * std::exp(gam[j]);",
      "const double tw = T[i * L + j] * bc[j];",
