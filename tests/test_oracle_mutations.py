@@ -36,8 +36,8 @@ MUTATIONS = [
      "acc += row[d] * (kt[d] * q_inv * scale)",
      [R.test_matches_householder_form]),
     ("gqa_modulo",
-     "head_chain(q, k, v, g, beta, S, cu[s], cu[s + 1], h, h / ratio,",
-     "head_chain(q, k, v, g, beta, S, cu[s], cu[s + 1], h, h % hk_n,",
+     "      head_chain(q, k, v, g, beta, S, cu[s], cu[s + 1], h, h / ratio,",
+     "      head_chain(q, k, v, g, beta, S, cu[s], cu[s + 1], h, h % hk_n,",
      [R.test_gqa_mapping]),
     ("conv_taps_reversed",
      "acc += tap(lt + j - width) * w[c * kw + j];",
