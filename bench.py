@@ -308,6 +308,46 @@ def time_gated_rmsnorm(w, dev, peaks, iters=20):
             "achieved_gbs": round(gbs, 1), "hbm_frac_of_measured": round(gbs / peaks["hbm"], 4)}
 
 
+def time_kda_decode(dev, peaks, B_=256, Hk=16, Hv=32, D=128, slots=512, iters=10):
+    """gdn_kda_varlen on decode_b256's shape (256 one-token sequences, a
+    512-slot f32 pool, bf16 activations).  Algorithmic bytes: every live state
+    row read and written once, plus q, k, v, out (bf16), g (f32 per key
+    channel) and beta."""
+    import torch
+    from gated_delta_rule_44_gb300 import binding as B
+    gen = torch.Generator().manual_seed(23)
+    q = (torch.randn(B_, Hk, D, generator=gen) / D ** 0.5).to(torch.bfloat16).to(dev)
+    k = (torch.randn(B_, Hk, D, generator=gen) / D ** 0.5).to(torch.bfloat16).to(dev)
+    v = torch.randn(B_, Hv, D, generator=gen).to(torch.bfloat16).to(dev)
+    g = (-torch.rand(B_, Hv, D, generator=gen) * 0.3).to(dev)
+    beta = (torch.rand(B_, Hv, generator=gen) * 0.8 + 0.1).to(dev)
+    pool = (torch.randn(slots, Hv, D, D, generator=gen) * 0.02).to(dev)
+    sidx = torch.randperm(slots, generator=gen)[:B_].to(torch.int32).to(dev)
+    cu = torch.arange(B_ + 1, dtype=torch.int32).to(dev)
+    out = torch.empty(B_, Hv, D, dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.current_stream(dev)
+
+    def call():
+        B.gdn_kda_varlen(q, k, v, g, beta, pool, cu, out, state_indices=sidx, stream=s)
+
+    for _ in range(3):
+        call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(s)
+    for _ in range(iters):
+        call()
+    e1.record(s)
+    torch.cuda.synchronize(dev)
+    us = e0.elapsed_time(e1) / iters * 1e3
+    nbytes = (B_ * Hv * D * D * 4 * 2 + 2 * B_ * Hk * D * 2 + 2 * B_ * Hv * D * 2
+              + B_ * Hv * D * 4 + B_ * Hv * 4)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"tokens_per_s": round(B_ / (us * 1e-6), 1), "avg_us": round(us, 2),
+            "algorithmic_bytes": nbytes, "achieved_gbs": round(gbs, 1),
+            "hbm_frac_of_measured": round(gbs / peaks["hbm"], 4)}
+
+
 def time_e2e(w, dev, steps, warmup, algo):
     """Same step through the public API with the step's inputs in pinned host
     memory: every step copies its inputs host -> device and its output
@@ -492,6 +532,7 @@ def main():
                            "kernels": kx}
             del wx
         extra["gated_rmsnorm"] = time_gated_rmsnorm(w, dev, peaks)
+        extra["kda_decode_b256"] = time_kda_decode(dev, peaks)
         line["extra_workloads"] = extra
     if rank == 0 and not args.no_e2e:
         line["e2e"] = time_e2e(w, dev, max(3, args.steps // 2), 3, args.algo)

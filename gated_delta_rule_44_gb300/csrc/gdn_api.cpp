@@ -343,6 +343,57 @@ int gdn_decode(const gdn_decode_args* a, void* stream) {
   return launch_result(gdn::launch_decode(p, static_cast<cudaStream_t>(stream)), "gdn_decode");
 }
 
+int gdn_kda_varlen(const gdn_kda_args* a, void* stream) {
+  if (a == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "args is NULL");
+  if (int rc = check_recurrence(a->T, a->Hk, a->Hv, a->Dk, a->Dv, a->act_dtype, a->q, a->q_len,
+                                a->k, a->k_len, a->v, a->v_len, a->g, a->g_len, a->beta,
+                                a->beta_len, a->state, a->state_slots, a->state_len, a->out,
+                                a->out_len))
+    return rc;
+  if (a->g_len < a->T * a->Hv * a->Dk)
+    return fail(GDN_ERR_SHAPE, "kda_gated_delta_rule g length " + S(a->g_len) + " < expected " +
+                                   S(a->T * a->Hv * a->Dk));
+  if (int rc = require_aligned(a->g, "g")) return rc;
+  if (a->N <= 0)
+    return fail(GDN_ERR_SHAPE, "kda_gated_delta_rule shape must be positive, got batch=" +
+                                   S(a->N) + " total_tokens=" + S(a->T));
+  if (require_ptr(a->cu_seqlens, "cu_seqlens")) return GDN_ERR_INVALID_ARGUMENT;
+  if (a->cu_seqlens_host != nullptr)
+    if (int rc = check_cu_host(a->cu_seqlens_host, a->N, a->T, "kda_gated_delta_rule")) return rc;
+  if (a->state_indices_host != nullptr)
+    if (int rc = check_indices_host(a->state_indices_host, a->N, a->state_slots)) return rc;
+  if (a->state_indices == nullptr && a->N > a->state_slots)
+    return fail(GDN_ERR_SHAPE, "kda_gated_delta_rule state has fewer slots than sequences");
+  if (!gdn::recurrent_supported((int)a->Dk))
+    return fail(GDN_ERR_UNSUPPORTED, "gdn_kda_varlen supports Dk in {16, 32, 64, 128, 256}");
+  if (!fits_i32(a->T * a->Hv * a->Dk))
+    return fail(GDN_ERR_UNSUPPORTED, "kda_gated_delta_rule sizes exceed 32-bit indexing");
+  gdn::RecurLaunch p{};
+  p.T = (int)a->T;
+  p.N = (int)a->N;
+  p.Hk = (int)a->Hk;
+  p.Hv = (int)a->Hv;
+  p.Dk = (int)a->Dk;
+  p.Dv = (int)a->Dv;
+  p.bf16 = a->act_dtype == GDN_DTYPE_BF16;
+  p.norm = false;
+  p.scale = resolve_scale(a->scale, a->Dk);
+  p.q = a->q;
+  p.k = a->k;
+  p.v = a->v;
+  p.g = a->g;
+  p.beta = a->beta;
+  p.pool = a->state;
+  p.slots = a->state_slots;
+  p.cu = a->cu_seqlens;
+  p.sidx = a->state_indices;
+  p.has_init = a->has_initial_state;
+  p.out = a->out;
+  p.status = gdn::status_word();
+  if (p.status == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
+  return launch_result(gdn::launch_kda(p, static_cast<cudaStream_t>(stream)), "gdn_kda_varlen");
+}
+
 int gdn_gated_rmsnorm(const gdn_gated_rmsnorm_args* a, void* stream) {
   if (a == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "args is NULL");
   if (int rc = check_act_dtype(a->act_dtype)) return rc;

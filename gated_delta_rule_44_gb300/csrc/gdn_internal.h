@@ -69,6 +69,9 @@ struct RecurLaunch {
 };
 cudaError_t launch_decode(const RecurLaunch& p, cudaStream_t s);
 cudaError_t launch_recurrent(const RecurLaunch& p, cudaStream_t s);
+// KDA: the recurrent prefill with g [T, Hv, Dk], a log decay per key channel
+// (p.norm must be false).
+cudaError_t launch_kda(const RecurLaunch& p, cudaStream_t s);
 bool recurrent_supported(int Dk);
 
 // Chunked (C = 64) tensor-core prefill.

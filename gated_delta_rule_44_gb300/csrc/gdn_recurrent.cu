@@ -22,6 +22,11 @@
 // HBM -> registers -> HBM once (evict-first loads and stores).
 // recurrent prefill: one CTA per (sequence, head, row slice) keeps its slice in
 // registers across the sequence's tokens, prefetching the next token's q/k/v.
+//
+// KDA ([cpu_ops.cpp] KdaHeadTokenStep, KdaGatedDeltaRuleKernel): the decay is
+// per key channel, e_d = exp(g[t, h, d]).  With a = S_i.(e k) and b = S_i.(e q)
+// on the old row, u_i = beta (v_i - a), S_i <- e S_i + u_i k and
+// o_i = scale (b + u_i (k.q)): the same single pass over the row.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -139,6 +144,39 @@ __device__ __forceinline__ float row_step(float4 (&s)[4], const float4 (&k)[4],
   return fmaf(decay, b, u * kq);
 }
 
+// The KDA row update: per-column decay e (the lane's 16 columns), ek = e k and
+// eq = e q.  Returns o_i (before scale).
+template <int LPR>
+__device__ __forceinline__ float row_step_kda(float4 (&s)[4], const float4 (&e)[4],
+                                              const float4 (&ek)[4], const float4 (&eq)[4],
+                                              const float4 (&k)[4], float kq, float beta,
+                                              float v) {
+  float a = 0.f, b = 0.f;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    a += dot4(s[m], ek[m]);
+    b += dot4(s[m], eq[m]);
+  }
+  a = row_sum<LPR>(a);
+  b = row_sum<LPR>(b);
+  const float u = beta * (v - a);
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    s[m].x = fmaf(e[m].x, s[m].x, u * k[m].x);
+    s[m].y = fmaf(e[m].y, s[m].y, u * k[m].y);
+    s[m].z = fmaf(e[m].z, s[m].z, u * k[m].z);
+    s[m].w = fmaf(e[m].w, s[m].w, u * k[m].w);
+  }
+  return fmaf(u, kq, b);
+}
+
+__device__ __forceinline__ float4 exp4(const float4& g) {
+  return make_float4(expf(g.x), expf(g.y), expf(g.z), expf(g.w));
+}
+__device__ __forceinline__ float4 mul4(const float4& a, const float4& b) {
+  return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w);
+}
+
 // ---------------------------------------------------------------------------
 // Decode: grid.x = B * Hv * slices.
 template <typename TA, int DK, int PASSES>
@@ -205,7 +243,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const RecurLaunch p, i
 
 // ---------------------------------------------------------------------------
 // Recurrent prefill: grid.x = N * Hv * slices; tokens of the sequence in order.
-template <typename TA, int DK, int PASSES>
+template <typename TA, int DK, int PASSES, bool KDA>
 __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurLaunch p, int slices) {
   constexpr int LPR = DK / 16;
   constexpr int RPP = kThreads / LPR;
@@ -261,13 +299,27 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurLaunch p
   QK<TA, DK> cur, nxt;
   float v_cur[PASSES], v_nxt[PASSES];
   float g_cur, b_cur, g_nxt = 0.f, b_nxt = 0.f;
+  // KDA: this lane's 16 log decays of the token (g [T, Hv, Dk]).
+  float4 gk_cur[KDA ? 4 : 1], gk_nxt[KDA ? 4 : 1];
+  auto load_gk = [&](int t, float4 (&dst)[KDA ? 4 : 1]) {
+    if constexpr (KDA) {
+      const float* gr = p.g + ((int64_t)t * p.Hv + h) * DK;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) dst[m] = __ldg(reinterpret_cast<const float4*>(gr + 4 * lr + 4 * LPR * m));
+    }
+  };
   cur.load(kbase + (int64_t)t0 * qk_row, qbase + (int64_t)t0 * qk_row, lr);
 #pragma unroll
   for (int ps = 0; ps < PASSES; ++ps) {
     const int r = row0 + ps * RPP;
     v_cur[ps] = r < p.Dv ? ld_act<TA>(vbase + (int64_t)t0 * v_row + r) : 0.f;
   }
-  g_cur = __ldg(p.g + (int64_t)t0 * p.Hv + h);
+  if constexpr (KDA) {
+    load_gk(t0, gk_cur);
+    g_cur = 0.f;
+  } else {
+    g_cur = __ldg(p.g + (int64_t)t0 * p.Hv + h);
+  }
   b_cur = __ldg(p.beta + (int64_t)t0 * p.Hv + h);
 
   for (int t = t0; t < t1; ++t) {
@@ -278,22 +330,43 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurLaunch p
         const int r = row0 + ps * RPP;
         v_nxt[ps] = r < p.Dv ? ld_act<TA>(vbase + (int64_t)(t + 1) * v_row + r) : 0.f;
       }
-      g_nxt = __ldg(p.g + (int64_t)(t + 1) * p.Hv + h);
+      if constexpr (KDA)
+        load_gk(t + 1, gk_nxt);
+      else
+        g_nxt = __ldg(p.g + (int64_t)(t + 1) * p.Hv + h);
       b_nxt = __ldg(p.beta + (int64_t)(t + 1) * p.Hv + h);
     }
     cur.finish(p.norm);
-    const float decay = expf(g_cur);
     TA* out = static_cast<TA*>(p.out) + ((int64_t)t * p.Hv + h) * p.Dv;
+    if constexpr (KDA) {
+      float4 e[4], ek[4], eq[4];
 #pragma unroll
-    for (int ps = 0; ps < PASSES; ++ps) {
-      const int r = row0 + ps * RPP;
-      const float o = row_step<LPR>(st[ps], cur.k, cur.q, cur.kq, decay, b_cur, v_cur[ps]);
-      if (lr == 0 && r < p.Dv) st_act<TA>(out + r, o * p.scale);
+      for (int m = 0; m < 4; ++m) {
+        e[m] = exp4(gk_cur[m]);
+        ek[m] = mul4(e[m], cur.k[m]);
+        eq[m] = mul4(e[m], cur.q[m]);
+      }
+#pragma unroll
+      for (int ps = 0; ps < PASSES; ++ps) {
+        const int r = row0 + ps * RPP;
+        const float o = row_step_kda<LPR>(st[ps], e, ek, eq, cur.k, cur.kq, b_cur, v_cur[ps]);
+        if (lr == 0 && r < p.Dv) st_act<TA>(out + r, o * p.scale);
+      }
+#pragma unroll
+      for (int m = 0; m < 4; ++m) gk_cur[m] = gk_nxt[m];
+    } else {
+      const float decay = expf(g_cur);
+#pragma unroll
+      for (int ps = 0; ps < PASSES; ++ps) {
+        const int r = row0 + ps * RPP;
+        const float o = row_step<LPR>(st[ps], cur.k, cur.q, cur.kq, decay, b_cur, v_cur[ps]);
+        if (lr == 0 && r < p.Dv) st_act<TA>(out + r, o * p.scale);
+      }
+      g_cur = g_nxt;
     }
     cur = nxt;
 #pragma unroll
     for (int ps = 0; ps < PASSES; ++ps) v_cur[ps] = v_nxt[ps];
-    g_cur = g_nxt;
     b_cur = b_nxt;
   }
 
@@ -308,15 +381,17 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurLaunch p
 }
 
 template <typename TA, int DK, int PASSES>
-cudaError_t launch_dk(const RecurLaunch& p, cudaStream_t s, bool decode) {
+cudaError_t launch_dk(const RecurLaunch& p, cudaStream_t s, bool decode, bool kda) {
   constexpr int rows_per_cta = (kThreads / (DK / 16)) * PASSES;
   const int slices = (p.Dv + rows_per_cta - 1) / rows_per_cta;
   const int64_t blocks = (int64_t)(decode ? p.T : p.N) * p.Hv * slices;
   if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
   if (decode)
     decode_kernel<TA, DK, PASSES><<<(unsigned)blocks, kThreads, 0, s>>>(p, slices);
+  else if (kda)
+    recurrent_kernel<TA, DK, PASSES, true><<<(unsigned)blocks, kThreads, 0, s>>>(p, slices);
   else
-    recurrent_kernel<TA, DK, PASSES><<<(unsigned)blocks, kThreads, 0, s>>>(p, slices);
+    recurrent_kernel<TA, DK, PASSES, false><<<(unsigned)blocks, kThreads, 0, s>>>(p, slices);
   note_launch();
   return cudaGetLastError();
 }
@@ -324,13 +399,13 @@ cudaError_t launch_dk(const RecurLaunch& p, cudaStream_t s, bool decode) {
 // PASSES chosen so a CTA holds 64 rows (32 floats of state per thread at
 // Dk = 128); decode issues all of them before the first use.
 template <typename TA>
-cudaError_t launch_any(const RecurLaunch& p, cudaStream_t s, bool decode) {
+cudaError_t launch_any(const RecurLaunch& p, cudaStream_t s, bool decode, bool kda = false) {
   switch (p.Dk) {
-    case 16: return launch_dk<TA, 16, 1>(p, s, decode);
-    case 32: return launch_dk<TA, 32, 1>(p, s, decode);
-    case 64: return launch_dk<TA, 64, 2>(p, s, decode);
-    case 128: return launch_dk<TA, 128, 4>(p, s, decode);
-    case 256: return launch_dk<TA, 256, 4>(p, s, decode);
+    case 16: return launch_dk<TA, 16, 1>(p, s, decode, kda);
+    case 32: return launch_dk<TA, 32, 1>(p, s, decode, kda);
+    case 64: return launch_dk<TA, 64, 2>(p, s, decode, kda);
+    case 128: return launch_dk<TA, 128, 4>(p, s, decode, kda);
+    case 256: return launch_dk<TA, 256, 4>(p, s, decode, kda);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -347,6 +422,12 @@ cudaError_t launch_decode(const RecurLaunch& p, cudaStream_t s) {
 
 cudaError_t launch_recurrent(const RecurLaunch& p, cudaStream_t s) {
   return p.bf16 ? launch_any<__nv_bfloat16>(p, s, false) : launch_any<float>(p, s, false);
+}
+
+cudaError_t launch_kda(const RecurLaunch& p, cudaStream_t s) {
+  if (p.norm) return cudaErrorInvalidValue;
+  return p.bf16 ? launch_any<__nv_bfloat16>(p, s, false, true)
+                : launch_any<float>(p, s, false, true);
 }
 
 }  // namespace gdn

@@ -252,6 +252,49 @@ int gdn_prefill_varlen(const gdn_prefill_args* args, void* stream);
 int gdn_prefill_varlen_noalloc(const gdn_prefill_args* args, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * gdn_kda_varlen -- [cpu_ops.cpp] KdaHeadTokenStep / KdaGatedDeltaRuleKernel:
+ * the gated delta rule with one log decay per KEY CHANNEL (KDA).
+ *
+ * As gdn_prefill_varlen's recurrence, token by token per (sequence, value head),
+ * except that g is [T, Hv, Dk] and column d of S decays by exp(g[t, h, d]):
+ *   S[:, d] *= exp(g[t,h,d]);  u = beta (v - S k);  S += u k^T;  out = S (scale q)
+ * q and k are used as given (no L2 norm).  Decode is the case of N one-token
+ * sequences.  State pool, state_indices (-1 = padding), has_initial_state,
+ * cu_seqlens and their host mirrors as in gdn_prefill_varlen; g 16-byte
+ * aligned.  Runs on CUDA cores, a CTA per (sequence, head, row slice).
+ * Supported: Dk in {16, 32, 64, 128, 256}; any Dv >= 1.
+ * Errors as gdn_prefill_varlen (g: "kda_gated_delta_rule g length N <
+ * expected T*Hv*Dk").
+ * ------------------------------------------------------------------------- */
+typedef struct gdn_kda_args {
+  int64_t T, N, Hk, Hv, Dk, Dv;
+  int32_t act_dtype;        /* gdn_dtype of q, k, v, out */
+  float scale;              /* < 0: 1/sqrt(Dk) */
+  const void* q;            /* [T, Hk, Dk] */
+  int64_t q_len;
+  const void* k;            /* [T, Hk, Dk] */
+  int64_t k_len;
+  const void* v;            /* [T, Hv, Dv] */
+  int64_t v_len;
+  const float* g;           /* [T, Hv, Dk] log decay per key channel */
+  int64_t g_len;
+  const float* beta;        /* [T, Hv] */
+  int64_t beta_len;
+  float* state;             /* [state_slots, Hv, Dv, Dk], updated in place */
+  int64_t state_slots;
+  int64_t state_len;
+  const int32_t* cu_seqlens;         /* [N + 1], device */
+  const int32_t* state_indices;      /* [N] or NULL */
+  const uint8_t* has_initial_state;  /* [N] or NULL (all 1) */
+  const int32_t* cu_seqlens_host;    /* optional host mirrors: full validation */
+  const int32_t* state_indices_host;
+  void* out;                /* [T, Hv, Dv] */
+  int64_t out_len;
+} gdn_kda_args;
+
+int gdn_kda_varlen(const gdn_kda_args* args, void* stream);
+
+/* ---------------------------------------------------------------------------
  * gdn_gated_rmsnorm -- [cpu.rs] gated_rms_norm_f32 and
  * validate_gated_rms_norm_shape; [cpu_ops.cpp] RmsNormGatedKernel (the
  * sigmoid-gate option, and a gate tensor whose token rows are strided, as a

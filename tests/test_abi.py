@@ -226,3 +226,35 @@ def test_gated_rmsnorm_other_rejections():
     rc, _ = call_norm(norm_args(D=big, core_len=6 * big, z_len=6 * big, weight_len=big,
                                 out_len=6 * big))
     assert rc == B.GDN_ERR_UNSUPPORTED
+
+
+def kda_args(T=4, N=2, Hk=1, Hv=2, Dk=128, Dv=64, **over):
+    a = dict(T=T, N=N, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, act_dtype=B.GDN_DTYPE_BF16, scale=-1.0,
+             q=FAKE, q_len=T * Hk * Dk, k=FAKE, k_len=T * Hk * Dk, v=FAKE, v_len=T * Hv * Dv,
+             g=FAKE, g_len=T * Hv * Dk, beta=FAKE, beta_len=T * Hv, state=FAKE, state_slots=4,
+             state_len=4 * Hv * Dv * Dk, cu_seqlens=FAKE, state_indices=None,
+             has_initial_state=None, cu_seqlens_host=None, state_indices_host=None, out=FAKE,
+             out_len=T * Hv * Dv)
+    a.update(over)
+    return B.gdn_kda_args(**a)
+
+
+def call_kda(args):
+    L = B.lib()
+    rc = L.gdn_kda_varlen(ctypes.byref(args), None)
+    return rc, L.gdn_last_error_message().decode()
+
+
+def test_kda_rejections():
+    rc, msg = call_kda(kda_args(g_len=4 * 2 * 128 - 1))
+    assert rc == B.GDN_ERR_SHAPE and msg == "kda_gated_delta_rule g length 1023 < expected 1024"
+    rc, msg = call_kda(kda_args(q_len=10))
+    assert rc == B.GDN_ERR_SHAPE and msg == "gated_delta_rule query length 10 < expected 512"
+    assert call_kda(kda_args(g=FAKE + 4))[0] == B.GDN_ERR_INVALID_ARGUMENT
+    assert call_kda(kda_args(N=0))[0] == B.GDN_ERR_SHAPE
+    assert call_kda(kda_args(cu_seqlens=None))[0] == B.GDN_ERR_INVALID_ARGUMENT
+    rc, _ = call_kda(kda_args(Dk=48, q_len=10**6, k_len=10**6, g_len=10**6, state_len=10**8))
+    assert rc == B.GDN_ERR_UNSUPPORTED
+    cu = (ctypes.c_int32 * 3)(0, 4, 4)  # empty second sequence
+    rc, msg = call_kda(kda_args(cu_seqlens_host=ctypes.cast(cu, ctypes.c_void_p).value))
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT and "empty or non-monotonic" in msg
