@@ -130,6 +130,10 @@ def _declare(L):
         fn.restype = ctypes.c_int
         fn.argtypes = ([_vp] * 6 + [_i64, _vp, _vp, _vp] + [_i64] * 6 + [ct, ctypes.c_int, _vp,
                        _i64, _vp, ctypes.c_int])
+        fn = getattr(L, f"orc_gdn_spec_decode_{suf}")
+        fn.restype = ctypes.c_int
+        fn.argtypes = ([_vp] * 6 + [_i64, _vp, _i64, _i64, _vp, _i64, _vp] + [_i64] * 4
+                       + [ct, _vp, ctypes.c_int])
         fn = getattr(L, f"orc_kda_varlen_{suf}")
         fn.restype = ctypes.c_int
         fn.argtypes = ([_vp] * 6 + [_i64, _vp, _vp, _vp] + [_i64] * 6 + [ct, ctypes.c_int, _vp,
@@ -323,6 +327,28 @@ def gdn_varlen(q, k, v, g, beta, state_pool, cu_seqlens, scale, state_indices=No
         _ptr(hi), _ptr(cu), cu.size - 1, T, Hk, Hv, Dk, Dv, float(scale), int(use_qk_l2norm),
         _ptr(it), 0 if it is None else it.size, _ptr(out), int(nthreads))
     _check(rc, "gdn_varlen")
+    return out
+
+
+def gdn_spec_decode(q, k, v, g, beta, state_pool, cu_seqlens, state_indices, num_accepted,
+                    scale, out=None, dtype=np.float32, nthreads=0):
+    """O7.  state_indices [n_reqs, num_cols] (int32), num_accepted [n_reqs];
+    state_pool [slots, Hv, Dv, Dk] updated in place (the snapshots).  Returns
+    out [T, Hv, Dv]."""
+    sfx = _suffix(dtype)
+    q, k, v, g, beta, T, Hk, Dk, Hv, Dv = _recur_inputs(q, k, v, g, beta, dtype)
+    pool = _inplace(state_pool, dtype, "state_pool")
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    si = np.ascontiguousarray(state_indices, dtype=np.int32)
+    na = np.ascontiguousarray(num_accepted, dtype=np.int32)
+    if out is None:
+        out = np.zeros((T, Hv, Dv), dtype)
+    out = _inplace(out, dtype, "out")
+    rc = getattr(_load(), f"orc_gdn_spec_decode_{sfx}")(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(pool), pool.shape[0], _ptr(cu),
+        cu.size - 1, T, _ptr(si), si.shape[1], _ptr(na), Hk, Hv, Dk, Dv, float(scale),
+        _ptr(out), int(nthreads))
+    _check(rc, "gdn_spec_decode")
     return out
 
 

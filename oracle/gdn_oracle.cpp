@@ -18,6 +18,7 @@
 // itself; see the header for the list.
 #include "gdn_oracle.h"
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -321,6 +322,53 @@ int varlen_impl(const R* q, const R* k, const R* v, const R* g, const R* beta, R
     else
       head_chain(q, k, v, g, beta, S, cu[s], cu[s + 1], h, h / ratio, hk_n, hv_n, dk, dv,
                  scale, use_norm != 0, out);
+  });
+  return ORC_OK;
+}
+
+// ---- O7: speculative multi-token decode ([cpu_ops.cpp] GdnSpecDecodeKernel) --
+// Request i owns tokens [cu[i], cu[i+1]) and a row of num_cols pool slots.  Its
+// state starts from slot sidx[i][num_accepted[i] - 1] (the snapshot after the
+// previous step's last accepted token); after token t the state is stored into
+// slot sidx[i][t - cu[i]] (a negative column skips that store).  A negative
+// initial slot zeroes the request's outputs and leaves the pool alone.  q, k are used as
+// given ([cpu_ops.cpp] GdnHeadTokenStep).
+template <typename R>
+int spec_decode_impl(const R* q, const R* k, const R* v, const R* g, const R* beta, R* pool,
+                     int64_t slots, const int32_t* cu, int64_t n_reqs, int64_t tokens,
+                     const int32_t* sidx, int64_t num_cols, const int32_t* num_accepted,
+                     int64_t hk_n, int64_t hv_n, int64_t dk, int64_t dv, R scale, R* out,
+                     int nthreads) {
+  if (n_reqs <= 0 || tokens <= 0 || num_cols <= 0 || hk_n <= 0 || hv_n <= 0 || dk <= 0 ||
+      dv <= 0 || hv_n % hk_n != 0)
+    return ORC_ERR_SHAPE;
+  if (cu[0] != 0 || cu[n_reqs] != tokens) return ORC_ERR_INVALID;
+  for (int64_t i = 0; i < n_reqs; ++i) {
+    if (cu[i + 1] < cu[i] || cu[i + 1] - cu[i] > num_cols) return ORC_ERR_INVALID;
+    if (num_accepted[i] < 1 || num_accepted[i] > num_cols) return ORC_ERR_INVALID;
+    for (int64_t c = 0; c < num_cols; ++c)
+      if (sidx[i * num_cols + c] >= slots) return ORC_ERR_INVALID;
+  }
+  const int64_t ratio = hv_n / hk_n, state_len = dv * dk;
+  parallel_items(n_reqs * hv_n, nthreads, [&](int64_t item) {
+    const int64_t i = item / hv_n, h = item % hv_n;
+    const int64_t lo = cu[i], hi = cu[i + 1];
+    const int32_t init = sidx[i * num_cols + (num_accepted[i] - 1)];
+    if (init < 0) {
+      for (int64_t t = lo; t < hi; ++t)
+        for (int64_t d = 0; d < dv; ++d) out[(t * hv_n + h) * dv + d] = R(0);
+      return;
+    }
+    if (hi == lo) return;
+    std::vector<R> S(pool + (init * hv_n + h) * state_len,
+                     pool + (init * hv_n + h) * state_len + state_len);
+    for (int64_t t = lo; t < hi; ++t) {
+      head_chain(q, k, v, g, beta, S.data(), t, t + 1, h, h / ratio, hk_n, hv_n, dk, dv, scale,
+                 false, out);
+      const int32_t slot = sidx[i * num_cols + (t - lo)];
+      if (slot < 0) continue;
+      std::copy(S.begin(), S.end(), pool + (slot * hv_n + h) * state_len);
+    }
   });
   return ORC_OK;
 }
@@ -679,6 +727,25 @@ int orc_kda_varlen_f64(ORC_RECUR_PARAMS(double)) {
                              has_initial_state, cu_seqlens, n_seqs, tokens, key_heads,
                              value_heads, key_dim, value_dim, scale, 0, items, n_items, out,
                              nthreads, true);
+}
+
+#define ORC_SPEC_PARAMS(R)                                                                  \
+  const R *query, const R *key, const R *value, const R *g, const R *beta, R *state_pool,   \
+      int64_t state_slots, const int32_t *cu_seqlens, int64_t n_reqs, int64_t tokens,       \
+      const int32_t *state_indices, int64_t num_cols, const int32_t *num_accepted,          \
+      int64_t key_heads, int64_t value_heads, int64_t key_dim, int64_t value_dim, R scale,  \
+      R *out, int nthreads
+int orc_gdn_spec_decode_f32(ORC_SPEC_PARAMS(float)) {
+  return spec_decode_impl<float>(query, key, value, g, beta, state_pool, state_slots, cu_seqlens,
+                                 n_reqs, tokens, state_indices, num_cols, num_accepted,
+                                 key_heads, value_heads, key_dim, value_dim, scale, out,
+                                 nthreads);
+}
+int orc_gdn_spec_decode_f64(ORC_SPEC_PARAMS(double)) {
+  return spec_decode_impl<double>(query, key, value, g, beta, state_pool, state_slots,
+                                  cu_seqlens, n_reqs, tokens, state_indices, num_cols,
+                                  num_accepted, key_heads, value_heads, key_dim, value_dim,
+                                  scale, out, nthreads);
 }
 
 int orc_gdn_decode_f32(ORC_DECODE_PARAMS(float)) {

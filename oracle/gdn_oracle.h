@@ -120,6 +120,29 @@ int orc_prepare_varlen_f64(ORC_PREPARE_PARAMS(double));
 int orc_gdn_varlen_f32(ORC_RECUR_PARAMS(float));
 int orc_gdn_varlen_f64(ORC_RECUR_PARAMS(double));
 
+/* ---- O7 speculative multi-token decode, [cpu_ops.cpp] GdnSpecDecodeKernel ----
+ * Request i owns tokens [cu[i], cu[i+1]) (at most num_cols of them) and row i
+ * of state_indices [n_reqs, num_cols].  Its state starts from slot
+ * state_indices[i][num_accepted[i] - 1]; after token t the state is stored in
+ * slot state_indices[i][t - cu[i]] (a negative slot skips the store).  A
+ * negative initial slot zeroes the request's outputs.  q, k used as given;
+ * g, beta [T, Hv].  ORC_ERR_INVALID for bad cu_seqlens, num_accepted outside
+ * [1, num_cols], requests longer than num_cols, or slots >= state_slots. */
+int orc_gdn_spec_decode_f32(const float* query, const float* key, const float* value,
+                            const float* g, const float* beta, float* state_pool,
+                            int64_t state_slots, const int32_t* cu_seqlens, int64_t n_reqs,
+                            int64_t tokens, const int32_t* state_indices, int64_t num_cols,
+                            const int32_t* num_accepted, int64_t key_heads, int64_t value_heads,
+                            int64_t key_dim, int64_t value_dim, float scale, float* out,
+                            int nthreads);
+int orc_gdn_spec_decode_f64(const double* query, const double* key, const double* value,
+                            const double* g, const double* beta, double* state_pool,
+                            int64_t state_slots, const int32_t* cu_seqlens, int64_t n_reqs,
+                            int64_t tokens, const int32_t* state_indices, int64_t num_cols,
+                            const int32_t* num_accepted, int64_t key_heads, int64_t value_heads,
+                            int64_t key_dim, int64_t value_dim, double scale, double* out,
+                            int nthreads);
+
 /* ---- O6 KDA: per-key-channel decay, [cpu_ops.cpp] KdaHeadTokenStep /
  * KdaGatedDeltaRuleKernel.  Same contract as orc_gdn_varlen except that g is
  * [T, Hv, Dk] (the log decay of each key channel) and use_qk_l2norm must be 0

@@ -8,7 +8,8 @@ sign, a swapped operand, a wrong GQA index, reversed conv taps, a wrong tail
 window, eps outside the sqrt, a wrong sigmoid branch or softplus threshold, a
 dropped factor in the chunked form, a gated norm over the sum instead of the
 mean, swapped gates or unstrided gate rows, a KDA decay taken from one channel
-or applied after the dot.
+or applied after the dot, a speculative decode that starts from the wrong
+column, stores each snapshot one column late or loses the state at a -1 column.
 """
 import os
 
@@ -21,6 +22,7 @@ import test_oracle_kda as KD
 import test_oracle_gates as G
 import test_oracle_prepare as P
 import test_oracle_recurrence as R
+import test_oracle_spec_decode as SD
 
 MUTATIONS = [
     ("decay_after_dot",
@@ -83,6 +85,18 @@ MUTATIONS = [
      "        row[d] *= decay[d];\n        dot += row[d] * kbuf[d];",
      "        dot += row[d] * kbuf[d];\n        row[d] *= decay[d];",
      [lambda: KD.test_uniform_channel_decay_is_gdn(np.float64)]),
+    ("spec_initial_column_off_by_one",
+     "const int32_t init = sidx[i * num_cols + (num_accepted[i] - 1)];",
+     "const int32_t init = sidx[i * num_cols + (num_accepted[i] % num_cols)];",
+     [SD.test_initial_slot_is_column_of_last_accepted]),
+    ("spec_snapshot_one_column_late",
+     "const int32_t slot = sidx[i * num_cols + (t - lo)];",
+     "const int32_t slot = sidx[i * num_cols + (t - lo + 1) % num_cols];",
+     [SD.test_brute_force_tiny]),
+    ("spec_null_column_resets_state",
+     "      if (slot < 0) continue;\n      std::copy(",
+     "      if (slot < 0) { std::fill(S.begin(), S.end(), R(0)); continue; }\n      std::copy(",
+     [SD.test_null_initial_slot_and_null_columns]),
     ("chunked_drops_decay_in_W",
      "const double tw = T[i * L + j] * bc[j] * std::exp(gam[j]);",
      "const double tw = T[i * L + j] * bc[j];",
