@@ -348,6 +348,52 @@ def time_kda_decode(dev, peaks, B_=256, Hk=16, Hv=32, D=128, slots=512, iters=10
             "hbm_frac_of_measured": round(gbs / peaks["hbm"], 4)}
 
 
+def time_spec_decode(dev, peaks, n_reqs=128, num_cols=4, Hk=16, Hv=32, D=128, slots=1024,
+                     iters=10):
+    """gdn_spec_decode on a multi-token-prediction decode: 128 requests x 4
+    draft tokens (num_cols 4), a 1024-slot f32 pool, bf16 activations, each
+    request resuming from a random accepted column.  Algorithmic bytes: per
+    (request, head) one state read and one state write per draft token, plus
+    q, k, v, out (bf16), g, beta (f32) and the metadata."""
+    import torch
+    from gated_delta_rule_44_gb300 import binding as B
+    gen = torch.Generator().manual_seed(29)
+    T = n_reqs * num_cols
+    q = (torch.randn(T, Hk, D, generator=gen) / D ** 0.5).to(torch.bfloat16).to(dev)
+    k = (torch.randn(T, Hk, D, generator=gen) / D ** 0.5).to(torch.bfloat16).to(dev)
+    v = torch.randn(T, Hv, D, generator=gen).to(torch.bfloat16).to(dev)
+    g = (-torch.rand(T, Hv, generator=gen) * 0.3).to(dev)
+    beta = (torch.rand(T, Hv, generator=gen) * 0.8 + 0.1).to(dev)
+    pool = (torch.randn(slots, Hv, D, D, generator=gen) * 0.02).to(dev)
+    sidx = torch.randperm(slots, generator=gen)[:T].reshape(n_reqs, num_cols)
+    sidx = sidx.to(torch.int32).to(dev)
+    nat = torch.randint(1, num_cols + 1, (n_reqs,), generator=gen, dtype=torch.int32).to(dev)
+    cu = (torch.arange(n_reqs + 1, dtype=torch.int32) * num_cols).to(dev)
+    out = torch.empty(T, Hv, D, dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.current_stream(dev)
+
+    def call():
+        B.gdn_spec_decode(q, k, v, g, beta, pool, cu, sidx, nat, out, stream=s)
+
+    for _ in range(3):
+        call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(s)
+    for _ in range(iters):
+        call()
+    e1.record(s)
+    torch.cuda.synchronize(dev)
+    us = e0.elapsed_time(e1) / iters * 1e3
+    state = Hv * D * D * 4
+    nbytes = (n_reqs * state * (1 + num_cols) + 2 * T * Hk * D * 2 + 2 * T * Hv * D * 2
+              + 2 * T * Hv * 4 + 4 * (n_reqs * (num_cols + 2) + 1))
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"tokens_per_s": round(T / (us * 1e-6), 1), "avg_us": round(us, 2),
+            "requests": n_reqs, "num_cols": num_cols, "algorithmic_bytes": nbytes,
+            "achieved_gbs": round(gbs, 1), "hbm_frac_of_measured": round(gbs / peaks["hbm"], 4)}
+
+
 def time_e2e(w, dev, steps, warmup, algo):
     """Same step through the public API with the step's inputs in pinned host
     memory: every step copies its inputs host -> device and its output
@@ -533,6 +579,7 @@ def main():
             del wx
         extra["gated_rmsnorm"] = time_gated_rmsnorm(w, dev, peaks)
         extra["kda_decode_b256"] = time_kda_decode(dev, peaks)
+        extra["spec_decode_r128x4"] = time_spec_decode(dev, peaks)
         line["extra_workloads"] = extra
     if rank == 0 and not args.no_e2e:
         line["e2e"] = time_e2e(w, dev, max(3, args.steps // 2), 3, args.algo)

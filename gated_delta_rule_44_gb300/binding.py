@@ -86,6 +86,17 @@ class gdn_kda_args(ctypes.Structure):
                 ("out", _vp), ("out_len", _i64)]
 
 
+class gdn_spec_decode_args(ctypes.Structure):
+    _fields_ = [("T", _i64), ("n_reqs", _i64), ("num_cols", _i64), ("Hk", _i64), ("Hv", _i64),
+                ("Dk", _i64), ("Dv", _i64), ("act_dtype", _i32), ("scale", _f32),
+                ("q", _vp), ("q_len", _i64), ("k", _vp), ("k_len", _i64), ("v", _vp),
+                ("v_len", _i64), ("g", _vp), ("g_len", _i64), ("beta", _vp), ("beta_len", _i64),
+                ("state", _vp), ("state_slots", _i64), ("state_len", _i64),
+                ("cu_seqlens", _vp), ("state_indices", _vp), ("num_accepted", _vp),
+                ("cu_seqlens_host", _vp), ("state_indices_host", _vp), ("num_accepted_host", _vp),
+                ("out", _vp), ("out_len", _i64)]
+
+
 class gdn_gated_rmsnorm_args(ctypes.Structure):
     _fields_ = [("tokens", _i64), ("heads", _i64), ("dim", _i64), ("act_dtype", _i32),
                 ("sigmoid_gate", _i32), ("eps", _f32), ("core", _vp), ("core_len", _i64),
@@ -94,7 +105,7 @@ class gdn_gated_rmsnorm_args(ctypes.Structure):
 
 
 EXPORTED = ("gdn_prepare", "gdn_decode", "gdn_prefill_varlen", "gdn_kda_varlen",
-            "gdn_gated_rmsnorm",
+            "gdn_spec_decode", "gdn_gated_rmsnorm",
             "gdn_prefill_workspace_bytes",
             "gdn_prefill_resolve_algo", "gdn_status_string", "gdn_last_error_message",
             "gdn_read_device_status", "gdn_version", "gdn_launch_count")
@@ -119,7 +130,7 @@ def lib() -> ctypes.CDLL:
         if _lib is None:
             L = ctypes.CDLL(_build.build_library())
             for name in ("gdn_prepare", "gdn_decode", "gdn_prefill_varlen", "gdn_kda_varlen",
-                         "gdn_gated_rmsnorm",
+                         "gdn_spec_decode", "gdn_gated_rmsnorm",
                          "gdn_read_device_status", "gdn_version"):
                 getattr(L, name).restype = ctypes.c_int
             L.gdn_prepare.argtypes = [ctypes.POINTER(gdn_prepare_args), _vp]
@@ -127,6 +138,7 @@ def lib() -> ctypes.CDLL:
             L.gdn_prefill_varlen.argtypes = [ctypes.POINTER(gdn_prefill_args), _vp]
             L.gdn_gated_rmsnorm.argtypes = [ctypes.POINTER(gdn_gated_rmsnorm_args), _vp]
             L.gdn_kda_varlen.argtypes = [ctypes.POINTER(gdn_kda_args), _vp]
+            L.gdn_spec_decode.argtypes = [ctypes.POINTER(gdn_spec_decode_args), _vp]
             L.gdn_read_device_status.argtypes = [_vp]
             L.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
             L.gdn_prefill_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64, _i64, _i32, _i32]
@@ -241,6 +253,27 @@ def gdn_kda_varlen(q, k, v, g, beta, state, cu_seqlens, out, *, scale=-1.0, stat
         has_initial_state=_p(has_initial_state), cu_seqlens_host=cuh_p,
         state_indices_host=sih_p, out=_p(out), out_len=_n(out))
     _check(lib().gdn_kda_varlen(ctypes.byref(a), _stream(stream)))
+
+
+def gdn_spec_decode(q, k, v, g, beta, state, cu_seqlens, state_indices, num_accepted, out, *,
+                    scale=-1.0, cu_seqlens_host=None, state_indices_host=None,
+                    num_accepted_host=None, stream=None) -> None:
+    """include/gdn.h gdn_spec_decode; state_indices [n_reqs, num_cols] int32;
+    the snapshots are written into `state` in place."""
+    T, Hk, Dk = q.shape
+    _, Hv, Dv = v.shape
+    n_reqs, num_cols = state_indices.shape
+    cuh, cuh_p = _host_i32(cu_seqlens_host)
+    sih, sih_p = _host_i32(state_indices_host)
+    nah, nah_p = _host_i32(num_accepted_host)
+    a = gdn_spec_decode_args(
+        T=T, n_reqs=n_reqs, num_cols=num_cols, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, act_dtype=_dt(q),
+        scale=float(scale), q=_p(q), q_len=_n(q), k=_p(k), k_len=_n(k), v=_p(v), v_len=_n(v),
+        g=_p(g), g_len=_n(g), beta=_p(beta), beta_len=_n(beta), state=_p(state),
+        state_slots=state.shape[0], state_len=_n(state), cu_seqlens=_p(cu_seqlens),
+        state_indices=_p(state_indices), num_accepted=_p(num_accepted), cu_seqlens_host=cuh_p,
+        state_indices_host=sih_p, num_accepted_host=nah_p, out=_p(out), out_len=_n(out))
+    _check(lib().gdn_spec_decode(ctypes.byref(a), _stream(stream)))
 
 
 def gdn_gated_rmsnorm(core, z, weight, out, *, eps=1e-6, sigmoid_gate=False, stream=None) -> None:

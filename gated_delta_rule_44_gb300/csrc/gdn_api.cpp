@@ -394,6 +394,95 @@ int gdn_kda_varlen(const gdn_kda_args* a, void* stream) {
   return launch_result(gdn::launch_kda(p, static_cast<cudaStream_t>(stream)), "gdn_kda_varlen");
 }
 
+// [qwen3_5.cpp] spec metadata validation, on the host mirrors: offsets span
+// the tokens, a request holds at most num_cols tokens (empty requests are
+// allowed, as [cpu_ops.cpp] GdnSpecDecodeKernel skips them), num_accepted in
+// [1, num_cols], slots below state_slots; and no live slot is named by two
+// requests' rows (their CTAs would race on it).
+int check_spec_host(const int32_t* cu, const int32_t* sidx, const int32_t* nat, int64_t n,
+                    int64_t cols, int64_t total, int64_t slots) {
+  if (cu != nullptr) {
+    if (cu[0] != 0 || cu[n] != total)
+      return fail(GDN_ERR_INVALID_ARGUMENT, "spec query offsets must span the spec tokens");
+    for (int64_t i = 0; i < n; ++i)
+      if (cu[i + 1] < cu[i] || cu[i + 1] - cu[i] > cols)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "spec request " + S(i) + " has range " +
+                                                  S(cu[i]) + ".." + S(cu[i + 1]) +
+                                                  ", not 0.." + S(cols) + " tokens");
+  }
+  if (nat != nullptr)
+    for (int64_t i = 0; i < n; ++i)
+      if (nat[i] < 1 || nat[i] > cols)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "num_accepted_tokens must be in [1, num_spec + 1]");
+  if (sidx != nullptr) {
+    std::vector<int64_t> owner(static_cast<size_t>(slots), -1);
+    for (int64_t i = 0; i < n; ++i)
+      for (int64_t c = 0; c < cols; ++c) {
+        const int32_t slot = sidx[i * cols + c];
+        if (slot < 0) continue;
+        if (slot >= slots)
+          return fail(GDN_ERR_INVALID_ARGUMENT, "spec GDN state slot out of range");
+        if (owner[slot] >= 0 && owner[slot] != i)
+          return fail(GDN_ERR_INVALID_ARGUMENT, "spec GDN state slot " + S(slot) +
+                                                    " named by two requests");
+        owner[slot] = i;
+      }
+  }
+  return GDN_OK;
+}
+
+int gdn_spec_decode(const gdn_spec_decode_args* a, void* stream) {
+  if (a == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "args is NULL");
+  if (int rc = check_recurrence(a->T, a->Hk, a->Hv, a->Dk, a->Dv, a->act_dtype, a->q, a->q_len,
+                                a->k, a->k_len, a->v, a->v_len, a->g, a->g_len, a->beta,
+                                a->beta_len, a->state, a->state_slots, a->state_len, a->out,
+                                a->out_len))
+    return rc;
+  if (a->n_reqs <= 0 || a->num_cols < 1)
+    return fail(GDN_ERR_SHAPE, "spec GDN decode needs n_reqs >= 1 and num_cols >= 1, got " +
+                                   S(a->n_reqs) + " and " + S(a->num_cols));
+  if (a->T > a->n_reqs * a->num_cols)
+    return fail(GDN_ERR_SHAPE, "spec GDN decode has " + S(a->T) + " tokens, more than n_reqs * "
+                               "num_cols = " + S(a->n_reqs * a->num_cols));
+  for (auto pr : {std::make_pair((const void*)a->cu_seqlens, "cu_seqlens"),
+                  std::make_pair((const void*)a->state_indices, "state_indices"),
+                  std::make_pair((const void*)a->num_accepted, "num_accepted")})
+    if (int rc = require_ptr(pr.first, pr.second)) return rc;
+  if (int rc = check_spec_host(a->cu_seqlens_host, a->state_indices_host, a->num_accepted_host,
+                               a->n_reqs, a->num_cols, a->T, a->state_slots))
+    return rc;
+  if (!gdn::recurrent_supported((int)a->Dk))
+    return fail(GDN_ERR_UNSUPPORTED, "gdn_spec_decode supports Dk in {16, 32, 64, 128, 256}");
+  if (!fits_i32(a->n_reqs * a->num_cols) || !fits_i32(a->T * a->Hv * a->Dv))
+    return fail(GDN_ERR_UNSUPPORTED, "spec GDN decode sizes exceed 32-bit indexing");
+  gdn::RecurLaunch p{};
+  p.T = (int)a->T;
+  p.N = (int)a->n_reqs;
+  p.Hk = (int)a->Hk;
+  p.Hv = (int)a->Hv;
+  p.Dk = (int)a->Dk;
+  p.Dv = (int)a->Dv;
+  p.bf16 = a->act_dtype == GDN_DTYPE_BF16;
+  p.norm = false;
+  p.scale = resolve_scale(a->scale, a->Dk);
+  p.q = a->q;
+  p.k = a->k;
+  p.v = a->v;
+  p.g = a->g;
+  p.beta = a->beta;
+  p.pool = a->state;
+  p.slots = a->state_slots;
+  p.cu = a->cu_seqlens;
+  p.sidx = a->state_indices;
+  p.num_accepted = a->num_accepted;
+  p.num_cols = (int)a->num_cols;
+  p.out = a->out;
+  p.status = gdn::status_word();
+  if (p.status == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
+  return launch_result(gdn::launch_spec_decode(p, static_cast<cudaStream_t>(stream)),
+                       "gdn_spec_decode");
+}
+
 int gdn_gated_rmsnorm(const gdn_gated_rmsnorm_args* a, void* stream) {
   if (a == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "args is NULL");
   if (int rc = check_act_dtype(a->act_dtype)) return rc;

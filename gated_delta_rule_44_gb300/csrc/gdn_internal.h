@@ -62,8 +62,10 @@ struct RecurLaunch {
   float* pool;
   int64_t slots;
   const int32_t* cu;        // null for decode (row b = sequence b)
-  const int32_t* sidx;      // may be null
+  const int32_t* sidx;      // may be null; [N, num_cols] for the speculative decode
   const uint8_t* has_init;  // may be null (prefill only)
+  const int32_t* num_accepted;  // speculative decode only: [N]
+  int num_cols;                 // speculative decode only
   void* out;
   unsigned* status;
 };
@@ -72,6 +74,10 @@ cudaError_t launch_recurrent(const RecurLaunch& p, cudaStream_t s);
 // KDA: the recurrent prefill with g [T, Hv, Dk], a log decay per key channel
 // (p.norm must be false).
 cudaError_t launch_kda(const RecurLaunch& p, cudaStream_t s);
+// Speculative multi-token decode: sequence s's initial slot is
+// sidx[s * num_cols + num_accepted[s] - 1] and the state after its token j is
+// stored into sidx[s * num_cols + j] (negative: skipped); p.norm false.
+cudaError_t launch_spec_decode(const RecurLaunch& p, cudaStream_t s);
 bool recurrent_supported(int Dk);
 
 // Chunked (C = 64) tensor-core prefill.

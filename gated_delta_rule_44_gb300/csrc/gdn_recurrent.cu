@@ -23,6 +23,12 @@
 // recurrent prefill: one CTA per (sequence, head, row slice) keeps its slice in
 // registers across the sequence's tokens, prefetching the next token's q/k/v.
 //
+// Speculative decode ([cpu_ops.cpp] GdnSpecDecodeKernel): sequence s is a
+// request whose draft tokens run from the slot of column num_accepted[s] - 1
+// of its state_indices row; after token t the CTA stores its rows of S into
+// the slot of column t - cu[s] (negative: no store).  The initial slot is not
+// written back, so a request can later resume from any of its snapshots.
+//
 // KDA ([cpu_ops.cpp] KdaHeadTokenStep, KdaGatedDeltaRuleKernel): the decay is
 // per key channel, e_d = exp(g[t, h, d]).  With a = S_i.(e k) and b = S_i.(e q)
 // on the old row, u_i = beta (v_i - a), S_i <- e S_i + u_i k and
@@ -243,7 +249,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const RecurLaunch p, i
 
 // ---------------------------------------------------------------------------
 // Recurrent prefill: grid.x = N * Hv * slices; tokens of the sequence in order.
-template <typename TA, int DK, int PASSES, bool KDA>
+// SPEC: the speculative decode (per-token snapshots, see the file header).
+template <typename TA, int DK, int PASSES, bool KDA, bool SPEC>
 __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurLaunch p, int slices) {
   constexpr int LPR = DK / 16;
   constexpr int RPP = kThreads / LPR;
@@ -255,14 +262,29 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurLaunch p
   const int row0 = slice * (RPP * PASSES) + rg;
 
   const int t0 = __ldg(p.cu + s), t1 = __ldg(p.cu + s + 1);
-  if (__ldg(p.cu) != 0 || __ldg(p.cu + p.N) != p.T || t0 < 0 || t1 <= t0 || t1 > p.T) {
+  // a speculative request may be empty but holds at most num_cols tokens
+  const bool bad_range = SPEC ? (t1 < t0 || t1 - t0 > p.num_cols) : t1 <= t0;
+  if (__ldg(p.cu) != 0 || __ldg(p.cu + p.N) != p.T || t0 < 0 || bad_range || t1 > p.T) {
     if (tid == 0) atomicOr(p.status, kStatusBadSeqlens);
     return;
   }
-  int slot = p.sidx != nullptr ? __ldg(p.sidx + s) : s;
-  if (slot < -1 || slot >= p.slots) {
-    if (tid == 0) atomicOr(p.status, kStatusBadIndex);
-    slot = -1;
+  if (SPEC && t1 == t0) return;
+  const int32_t* spec_row = SPEC ? p.sidx + (int64_t)s * p.num_cols : nullptr;
+  int slot;
+  if constexpr (SPEC) {
+    const int accepted = __ldg(p.num_accepted + s);
+    const bool ok = accepted >= 1 && accepted <= p.num_cols;
+    slot = ok ? __ldg(spec_row + accepted - 1) : -1;
+    if (!ok || slot >= p.slots) {
+      if (tid == 0) atomicOr(p.status, kStatusBadIndex);
+      slot = -1;
+    }
+  } else {
+    slot = p.sidx != nullptr ? __ldg(p.sidx + s) : s;
+    if (slot < -1 || slot >= p.slots) {
+      if (tid == 0) atomicOr(p.status, kStatusBadIndex);
+      slot = -1;
+    }
   }
   if (slot < 0) {  // padded sequence: zero outputs, pool untouched
     for (int t = t0; t < t1; ++t) {
@@ -277,7 +299,7 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurLaunch p
   }
   const int hk = h / (p.Hv / p.Hk);
   float* S = p.pool + ((int64_t)slot * p.Hv + h) * p.Dv * DK;
-  const bool init = p.has_init == nullptr || __ldg(p.has_init + s) != 0;
+  const bool init = SPEC || p.has_init == nullptr || __ldg(p.has_init + s) != 0;
 
   float4 st[PASSES][4];
 #pragma unroll
@@ -364,34 +386,66 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurLaunch p
       }
       g_cur = g_nxt;
     }
+    if constexpr (SPEC) {  // snapshot after token t
+      int snap = __ldg(spec_row + (t - t0));
+      if (snap >= p.slots) {
+        if (tid == 0) atomicOr(p.status, kStatusBadIndex);
+        snap = -1;
+      }
+      if (snap >= 0) {
+        float* D = p.pool + ((int64_t)snap * p.Hv + h) * p.Dv * DK;
+#pragma unroll
+        for (int ps = 0; ps < PASSES; ++ps) {
+          const int r = row0 + ps * RPP;
+          if (r < p.Dv)
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+              __stcs(reinterpret_cast<float4*>(D + (int64_t)r * DK + 4 * lr + 4 * LPR * m),
+                     st[ps][m]);
+        }
+      }
+    }
     cur = nxt;
 #pragma unroll
     for (int ps = 0; ps < PASSES; ++ps) v_cur[ps] = v_nxt[ps];
     b_cur = b_nxt;
   }
 
+  if constexpr (!SPEC) {
 #pragma unroll
-  for (int ps = 0; ps < PASSES; ++ps) {
-    const int r = row0 + ps * RPP;
-    if (r < p.Dv)
+    for (int ps = 0; ps < PASSES; ++ps) {
+      const int r = row0 + ps * RPP;
+      if (r < p.Dv)
 #pragma unroll
-      for (int m = 0; m < 4; ++m)
-        *reinterpret_cast<float4*>(S + (int64_t)r * DK + 4 * lr + 4 * LPR * m) = st[ps][m];
+        for (int m = 0; m < 4; ++m)
+          *reinterpret_cast<float4*>(S + (int64_t)r * DK + 4 * lr + 4 * LPR * m) = st[ps][m];
+    }
   }
 }
 
+enum class Mode { kDecode, kRecurrent, kKda, kSpec };
+
 template <typename TA, int DK, int PASSES>
-cudaError_t launch_dk(const RecurLaunch& p, cudaStream_t s, bool decode, bool kda) {
+cudaError_t launch_dk(const RecurLaunch& p, cudaStream_t s, Mode mode) {
   constexpr int rows_per_cta = (kThreads / (DK / 16)) * PASSES;
   const int slices = (p.Dv + rows_per_cta - 1) / rows_per_cta;
-  const int64_t blocks = (int64_t)(decode ? p.T : p.N) * p.Hv * slices;
+  const int64_t blocks = (int64_t)(mode == Mode::kDecode ? p.T : p.N) * p.Hv * slices;
   if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  if (decode)
-    decode_kernel<TA, DK, PASSES><<<(unsigned)blocks, kThreads, 0, s>>>(p, slices);
-  else if (kda)
-    recurrent_kernel<TA, DK, PASSES, true><<<(unsigned)blocks, kThreads, 0, s>>>(p, slices);
-  else
-    recurrent_kernel<TA, DK, PASSES, false><<<(unsigned)blocks, kThreads, 0, s>>>(p, slices);
+  const unsigned grid = (unsigned)blocks;
+  switch (mode) {
+    case Mode::kDecode:
+      decode_kernel<TA, DK, PASSES><<<grid, kThreads, 0, s>>>(p, slices);
+      break;
+    case Mode::kRecurrent:
+      recurrent_kernel<TA, DK, PASSES, false, false><<<grid, kThreads, 0, s>>>(p, slices);
+      break;
+    case Mode::kKda:
+      recurrent_kernel<TA, DK, PASSES, true, false><<<grid, kThreads, 0, s>>>(p, slices);
+      break;
+    case Mode::kSpec:
+      recurrent_kernel<TA, DK, PASSES, false, true><<<grid, kThreads, 0, s>>>(p, slices);
+      break;
+  }
   note_launch();
   return cudaGetLastError();
 }
@@ -399,13 +453,13 @@ cudaError_t launch_dk(const RecurLaunch& p, cudaStream_t s, bool decode, bool kd
 // PASSES chosen so a CTA holds 64 rows (32 floats of state per thread at
 // Dk = 128); decode issues all of them before the first use.
 template <typename TA>
-cudaError_t launch_any(const RecurLaunch& p, cudaStream_t s, bool decode, bool kda = false) {
+cudaError_t launch_any(const RecurLaunch& p, cudaStream_t s, Mode mode) {
   switch (p.Dk) {
-    case 16: return launch_dk<TA, 16, 1>(p, s, decode, kda);
-    case 32: return launch_dk<TA, 32, 1>(p, s, decode, kda);
-    case 64: return launch_dk<TA, 64, 2>(p, s, decode, kda);
-    case 128: return launch_dk<TA, 128, 4>(p, s, decode, kda);
-    case 256: return launch_dk<TA, 256, 4>(p, s, decode, kda);
+    case 16: return launch_dk<TA, 16, 1>(p, s, mode);
+    case 32: return launch_dk<TA, 32, 1>(p, s, mode);
+    case 64: return launch_dk<TA, 64, 2>(p, s, mode);
+    case 128: return launch_dk<TA, 128, 4>(p, s, mode);
+    case 256: return launch_dk<TA, 256, 4>(p, s, mode);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -416,18 +470,27 @@ bool recurrent_supported(int Dk) {
   return Dk == 16 || Dk == 32 || Dk == 64 || Dk == 128 || Dk == 256;
 }
 
+static cudaError_t launch_mode(const RecurLaunch& p, cudaStream_t s, Mode mode) {
+  return p.bf16 ? launch_any<__nv_bfloat16>(p, s, mode) : launch_any<float>(p, s, mode);
+}
+
 cudaError_t launch_decode(const RecurLaunch& p, cudaStream_t s) {
-  return p.bf16 ? launch_any<__nv_bfloat16>(p, s, true) : launch_any<float>(p, s, true);
+  return launch_mode(p, s, Mode::kDecode);
 }
 
 cudaError_t launch_recurrent(const RecurLaunch& p, cudaStream_t s) {
-  return p.bf16 ? launch_any<__nv_bfloat16>(p, s, false) : launch_any<float>(p, s, false);
+  return launch_mode(p, s, Mode::kRecurrent);
 }
 
 cudaError_t launch_kda(const RecurLaunch& p, cudaStream_t s) {
   if (p.norm) return cudaErrorInvalidValue;
-  return p.bf16 ? launch_any<__nv_bfloat16>(p, s, false, true)
-                : launch_any<float>(p, s, false, true);
+  return launch_mode(p, s, Mode::kKda);
+}
+
+cudaError_t launch_spec_decode(const RecurLaunch& p, cudaStream_t s) {
+  if (p.norm || p.sidx == nullptr || p.num_accepted == nullptr || p.num_cols < 1)
+    return cudaErrorInvalidValue;
+  return launch_mode(p, s, Mode::kSpec);
 }
 
 }  // namespace gdn

@@ -295,6 +295,71 @@ typedef struct gdn_kda_args {
 int gdn_kda_varlen(const gdn_kda_args* args, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * gdn_spec_decode -- [cpu_ops.cpp] GdnSpecDecodeKernel with the metadata rules
+ * of [qwen3_5.cpp] (spec metadata validation): speculative multi-token decode.
+ *
+ * Request i owns the draft tokens [cu_seqlens[i], cu_seqlens[i+1]) (0 to
+ * num_cols of them) and row i of state_indices [n_reqs, num_cols].  Its state
+ * starts from slot state_indices[i][num_accepted[i] - 1] (the snapshot after
+ * the previous step's last accepted token); each token runs the gated delta
+ * rule of gdn_prefill_varlen with q, k used as given (no L2 norm):
+ *   S *= exp(g);  u = beta (v - S k);  S += u k^T;  out = S (scale q)
+ * and the state after token t is stored in slot state_indices[i][t - cu[i]].
+ * A negative slot skips that store; a negative initial slot zeroes the
+ * request's outputs and writes no slot.  The initial slot is not written
+ * back (unless a column names it), so a later step can resume from any
+ * snapshot: the snapshot in column j equals the state after running only the
+ * first j + 1 draft tokens.
+ *   - Layout: q, k [T, Hk, Dk], v [T, Hv, Dv], out [T, Hv, Dv] (act_dtype),
+ *     g, beta [T, Hv] f32, state [state_slots, Hv, Dv, Dk] f32, all row-major
+ *     and device-resident; cu_seqlens [n_reqs + 1], state_indices
+ *     [n_reqs, num_cols], num_accepted [n_reqs] int32 on the device.
+ *   - Precondition: no live slot appears in two requests' rows (the optional
+ *     host mirrors check it).  Within one row, repeats are allowed.
+ *   - Host mirrors (optional, any subset) validate fully before launch:
+ *     offsets span 0..T, request lengths in [0, num_cols], num_accepted in
+ *     [1, num_cols], slots < state_slots, no slot shared by two requests.
+ *     Without them the kernel flags GDN_DEVICE_BAD_SEQLENS (bad offsets) or
+ *     GDN_DEVICE_BAD_INDEX (bad num_accepted or slot) in the device status
+ *     word and skips the request or the store.
+ *   - Errors: GDN_ERR_SHAPE for non-positive sizes, Hv % Hk != 0, short
+ *     buffers or T > n_reqs * num_cols; GDN_ERR_INVALID_ARGUMENT for NULL or
+ *     misaligned pointers and failed mirror checks ("num_accepted_tokens must
+ *     be in [1, num_spec + 1]", "spec GDN state slot out of range", ...);
+ *     GDN_ERR_UNSUPPORTED for Dk outside {16, 32, 64, 128, 256}.
+ *   - Runs on CUDA cores, one CTA per (request, value head, row slice) holding
+ *     its rows in registers across the request's tokens.
+ * ------------------------------------------------------------------------- */
+typedef struct gdn_spec_decode_args {
+  int64_t T, n_reqs, num_cols, Hk, Hv, Dk, Dv;
+  int32_t act_dtype;        /* gdn_dtype of q, k, v, out */
+  float scale;              /* < 0: 1/sqrt(Dk) */
+  const void* q;            /* [T, Hk, Dk] */
+  int64_t q_len;
+  const void* k;            /* [T, Hk, Dk] */
+  int64_t k_len;
+  const void* v;            /* [T, Hv, Dv] */
+  int64_t v_len;
+  const float* g;           /* [T, Hv] */
+  int64_t g_len;
+  const float* beta;        /* [T, Hv] */
+  int64_t beta_len;
+  float* state;             /* [state_slots, Hv, Dv, Dk], snapshots written in place */
+  int64_t state_slots;
+  int64_t state_len;
+  const int32_t* cu_seqlens;        /* [n_reqs + 1], device */
+  const int32_t* state_indices;     /* [n_reqs, num_cols], device */
+  const int32_t* num_accepted;      /* [n_reqs], device */
+  const int32_t* cu_seqlens_host;   /* optional host mirrors */
+  const int32_t* state_indices_host;
+  const int32_t* num_accepted_host;
+  void* out;                /* [T, Hv, Dv] */
+  int64_t out_len;
+} gdn_spec_decode_args;
+
+int gdn_spec_decode(const gdn_spec_decode_args* args, void* stream);
+
+/* ---------------------------------------------------------------------------
  * gdn_gated_rmsnorm -- [cpu.rs] gated_rms_norm_f32 and
  * validate_gated_rms_norm_shape; [cpu_ops.cpp] RmsNormGatedKernel (the
  * sigmoid-gate option, and a gate tensor whose token rows are strided, as a

@@ -258,3 +258,54 @@ def test_kda_rejections():
     cu = (ctypes.c_int32 * 3)(0, 4, 4)  # empty second sequence
     rc, msg = call_kda(kda_args(cu_seqlens_host=ctypes.cast(cu, ctypes.c_void_p).value))
     assert rc == B.GDN_ERR_INVALID_ARGUMENT and "empty or non-monotonic" in msg
+
+
+def spec_args(T=5, n_reqs=2, num_cols=3, Hk=1, Hv=2, Dk=128, Dv=64, **over):
+    a = dict(T=T, n_reqs=n_reqs, num_cols=num_cols, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv,
+             act_dtype=B.GDN_DTYPE_BF16, scale=-1.0, q=FAKE, q_len=T * Hk * Dk, k=FAKE,
+             k_len=T * Hk * Dk, v=FAKE, v_len=T * Hv * Dv, g=FAKE, g_len=T * Hv, beta=FAKE,
+             beta_len=T * Hv, state=FAKE, state_slots=8, state_len=8 * Hv * Dv * Dk,
+             cu_seqlens=FAKE, state_indices=FAKE, num_accepted=FAKE, cu_seqlens_host=None,
+             state_indices_host=None, num_accepted_host=None, out=FAKE, out_len=T * Hv * Dv)
+    a.update(over)
+    return B.gdn_spec_decode_args(**a)
+
+
+def call_spec(args):
+    L = B.lib()
+    rc = L.gdn_spec_decode(ctypes.byref(args), None)
+    return rc, L.gdn_last_error_message().decode()
+
+
+def _host(*vals):
+    arr = (ctypes.c_int32 * len(vals))(*vals)
+    _host.keep.append(arr)
+    return ctypes.cast(arr, ctypes.c_void_p).value
+
+
+_host.keep = []
+
+
+def test_spec_decode_rejections():
+    assert call_spec(spec_args(n_reqs=0))[0] == B.GDN_ERR_SHAPE
+    assert call_spec(spec_args(num_cols=0))[0] == B.GDN_ERR_SHAPE
+    rc, msg = call_spec(spec_args(T=7))  # 7 tokens > 2 requests x 3 columns
+    assert rc == B.GDN_ERR_SHAPE and "more than n_reqs * num_cols" in msg
+    assert call_spec(spec_args(num_accepted=None))[0] == B.GDN_ERR_INVALID_ARGUMENT
+    assert call_spec(spec_args(state_indices=None))[0] == B.GDN_ERR_INVALID_ARGUMENT
+    assert call_spec(spec_args(g_len=9))[0] == B.GDN_ERR_SHAPE
+    rc, _ = call_spec(spec_args(Dk=48, q_len=10**6, k_len=10**6, state_len=10**8))
+    assert rc == B.GDN_ERR_UNSUPPORTED
+    # host mirrors: [qwen3_5.cpp] spec metadata rules
+    rc, msg = call_spec(spec_args(cu_seqlens_host=_host(0, 2, 4)))
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT and msg == "spec query offsets must span the spec tokens"
+    rc, msg = call_spec(spec_args(cu_seqlens_host=_host(0, 1, 5)))  # request 1: 4 > 3 tokens
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT and "not 0..3 tokens" in msg
+    rc, msg = call_spec(spec_args(num_accepted_host=_host(1, 4)))
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT
+    assert msg == "num_accepted_tokens must be in [1, num_spec + 1]"
+    assert call_spec(spec_args(num_accepted_host=_host(0, 1)))[0] == B.GDN_ERR_INVALID_ARGUMENT
+    rc, msg = call_spec(spec_args(state_indices_host=_host(0, 1, 2, 3, 4, 8)))
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT and msg == "spec GDN state slot out of range"
+    rc, msg = call_spec(spec_args(state_indices_host=_host(0, 1, 2, 3, 2, -1)))
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT and "named by two requests" in msg

@@ -33,7 +33,7 @@ def run(seqs, Hk, Hv, Dk, Dv, dtype, dev, seed, sidx=None, has_init=None, slots=
                      cu.to(dev), out, scale=-1.0, state_indices=sidx.to(dev),
                      has_initial_state=None if hi is None else hi.to(dev),
                      cu_seqlens_host=cu, state_indices_host=sidx)
-    assert B.gdn_read_device_status() is None or True
+    B.gdn_read_device_status()
     torch.cuda.synchronize()
     ref_pool = pool.numpy().astype(np.float32).copy()
     ref = oracle.kda_varlen(H.f32(q), H.f32(k), H.f32(v), g.numpy(), beta.numpy(), ref_pool,
