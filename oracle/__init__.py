@@ -130,6 +130,10 @@ def _declare(L):
         fn.restype = ctypes.c_int
         fn.argtypes = ([_vp] * 6 + [_i64, _vp, _vp, _vp] + [_i64] * 6 + [ct, ctypes.c_int, _vp,
                        _i64, _vp, ctypes.c_int])
+        fn = getattr(L, f"orc_spec_prepare_{suf}")
+        fn.restype = ctypes.c_int
+        fn.argtypes = ([_vp, _i64, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _i64, _vp, _i64, _vp, _vp,
+                        _vp] + [_i64] * 7 + [ctypes.c_int] + [_vp] * 5 + [ctypes.c_int])
         fn = getattr(L, f"orc_gdn_spec_decode_{suf}")
         fn.restype = ctypes.c_int
         fn.argtypes = ([_vp] * 6 + [_i64, _vp, _i64, _i64, _vp, _i64, _vp] + [_i64] * 4
@@ -290,6 +294,39 @@ def prepare_varlen(mixed_qkv, conv_weight, conv_pool, a_raw, b_raw, A_log, dt_bi
         _ptr(b), b.shape[1], _ptr(al), _ptr(dtb), _ptr(cu), N, T, Hk, Hv, Dk, Dv, K,
         int(apply_qk_l2norm), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), int(nthreads))
     _check(rc, "prepare_varlen")
+    return dict(q=q, k=k, v=v, g=g, beta=beta)
+
+
+def spec_prepare(mixed_qkv, conv_weight, conv_pool, a_raw, b_raw, A_log, dt_bias, cu_seqlens,
+                 conv_indices, num_accepted, Hk, Hv, Dk, Dv, K, apply_qk_l2norm=True,
+                 dtype=np.float32, nthreads=0):
+    """O8.  mixed_qkv [T, C_conv]; conv_pool [slots, C_conv, state_len] (in
+    place); conv_indices, num_accepted [n_reqs].
+
+    Returns dict(q [T,Hk,Dk], k, v [T,Hv,Dv], g [T,Hv], beta [T,Hv])."""
+    sfx = _suffix(dtype)
+    x = _arr(mixed_qkv, dtype, "mixed_qkv")
+    T = x.shape[0]
+    w = _arr(conv_weight, dtype, "conv_weight")
+    pool = _inplace(conv_pool, dtype, "conv_pool")
+    a = _arr(a_raw, dtype, "a_raw").reshape(T, -1)
+    b = _arr(b_raw, dtype, "b_raw").reshape(T, -1)
+    al = _arr(A_log, dtype, "A_log")
+    dtb = _arr(dt_bias, dtype, "dt_bias")
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    ci = np.ascontiguousarray(conv_indices, dtype=np.int32)
+    na = np.ascontiguousarray(num_accepted, dtype=np.int32)
+    q = np.empty((T, Hk, Dk), dtype)
+    k = np.empty((T, Hk, Dk), dtype)
+    v = np.empty((T, Hv, Dv), dtype)
+    g = np.empty((T, Hv), dtype)
+    beta = np.empty((T, Hv), dtype)
+    rc = getattr(_load(), f"orc_spec_prepare_{sfx}")(
+        _ptr(x), x.shape[1], _ptr(w), _ptr(pool), pool.shape[0], pool.shape[2], _ptr(ci),
+        _ptr(na), _ptr(a), a.shape[1], _ptr(b), b.shape[1], _ptr(al), _ptr(dtb), _ptr(cu),
+        cu.size - 1, T, Hk, Hv, Dk, Dv, K, int(apply_qk_l2norm), _ptr(q), _ptr(k), _ptr(v),
+        _ptr(g), _ptr(beta), int(nthreads))
+    _check(rc, "spec_prepare")
     return dict(q=q, k=k, v=v, g=g, beta=beta)
 
 

@@ -125,6 +125,12 @@ int check_slots(const int32_t* idx, int64_t n, int64_t slots, char* msg, size_t 
   return ORC_OK;
 }
 
+template <typename R>
+void prepare_gates_norm(const R* a_raw, int64_t a_stride, const R* b_raw, int64_t b_stride,
+                        const R* a_log, const R* dt_bias, int64_t tokens, int64_t hk_n,
+                        int64_t hv_n, int64_t dk, int apply_norm, R* q, R* k, R* g, R* beta,
+                        int nthreads);
+
 // ---- O1: prepare --------------------------------------------------------------
 // [cpu.rs] linear_attention_prepare_varlen_f32 per sequence:
 //   conv:   acc = sum_j x~[t + j - (K-1)] * w[c, j], x~[i] = x[i] for i >= 0 and
@@ -181,7 +187,18 @@ int prepare_impl(const R* x, int64_t x_stride, const R* w, R* conv_pool, int64_t
       for (int64_t pos = 0; pos < width; ++pos) tail_row[pos] = tap(len + pos - width);
   });
 
-  // Gates, per (token, value head).
+  prepare_gates_norm(a_raw, a_stride, b_raw, b_stride, a_log, dt_bias, tokens, hk_n, hv_n, dk,
+                     apply_norm, q, k, g, beta, nthreads);
+  return ORC_OK;
+}
+
+// The steps of O1 after the conv: gates per (token, value head) and the q/k L2
+// norm per (token, key head).
+template <typename R>
+void prepare_gates_norm(const R* a_raw, int64_t a_stride, const R* b_raw, int64_t b_stride,
+                        const R* a_log, const R* dt_bias, int64_t tokens, int64_t hk_n,
+                        int64_t hv_n, int64_t dk, int apply_norm, R* q, R* k, R* g, R* beta,
+                        int nthreads) {
   parallel_items(tokens, nthreads, [&](int64_t t) {
     for (int64_t h = 0; h < hv_n; ++h) {
       g[t * hv_n + h] = -std::exp(a_log[h]) * softplus_(a_raw[t * a_stride + h] + dt_bias[h]);
@@ -205,6 +222,74 @@ int prepare_impl(const R* x, int64_t x_stride, const R* w, R* conv_pool, int64_t
       }
     });
   }
+}
+
+// ---- O8: speculative prepare ([cpu_ops.cpp] CausalConv1dSpecUpdateKernel) ------
+// The conv of O1 for the draft tokens of a speculative step.  Each request's
+// conv row holds state_len = (K-1) + (max_q - 1) raw inputs; with
+// off = num_accepted - 1 the window before the first draft is row[off ..
+// off+K-2] (entries past the row read 0), then the drafts themselves.  The
+// row becomes row[off+1 .. off+keep] || drafts, keep = state_len - len: shifted
+// by one tap per step, so that the next step's offset picks the window that
+// ends at its last accepted token.  Split, gates and norm are O1's.
+// A negative slot: outputs from a zero window, no row written; an empty
+// request: nothing.
+template <typename R>
+int spec_prepare_impl(const R* x, int64_t x_stride, const R* w, R* conv_pool, int64_t conv_slots,
+                      int64_t state_len, const int32_t* cidx, const int32_t* num_accepted,
+                      const R* a_raw, int64_t a_stride, const R* b_raw, int64_t b_stride,
+                      const R* a_log, const R* dt_bias, const int32_t* cu, int64_t n_reqs,
+                      int64_t tokens, int64_t hk_n, int64_t hv_n, int64_t dk, int64_t dv,
+                      int64_t kw, int apply_norm, R* q, R* k, R* v, R* g, R* beta,
+                      int nthreads) {
+  if (n_reqs <= 0 || tokens <= 0 || hk_n <= 0 || hv_n <= 0 || dk <= 0 || dv <= 0 || kw <= 0)
+    return ORC_ERR_SHAPE;
+  const int64_t width = kw - 1, max_q = state_len - width + 1;
+  if (max_q < 1) return ORC_ERR_SHAPE;
+  if (cu[0] != 0 || cu[n_reqs] != tokens) return ORC_ERR_INVALID;
+  for (int64_t i = 0; i < n_reqs; ++i) {
+    if (cu[i + 1] < cu[i] || cu[i + 1] - cu[i] > max_q) return ORC_ERR_INVALID;
+    if (num_accepted[i] < 1 || num_accepted[i] > max_q) return ORC_ERR_INVALID;
+    if (cidx[i] >= conv_slots) return ORC_ERR_INVALID;
+  }
+  const int64_t qk_total = hk_n * dk, v_total = hv_n * dv;
+  const int64_t channels = 2 * qk_total + v_total;
+  if (x_stride <= 0) x_stride = channels;
+  if (a_stride <= 0) a_stride = hv_n;
+  if (b_stride <= 0) b_stride = hv_n;
+
+  parallel_items(n_reqs * channels, nthreads, [&](int64_t item) {
+    const int64_t i = item / channels, c = item % channels;
+    const int64_t lo = cu[i], len = cu[i + 1] - cu[i];
+    if (len == 0) return;
+    const bool live = cidx[i] >= 0;
+    R* row = live ? conv_pool + (cidx[i] * channels + c) * state_len : nullptr;
+    const int64_t off = num_accepted[i] - 1;
+    auto old_at = [&](int64_t j) -> R { return live && j < state_len ? row[j] : R(0); };
+    std::vector<R> stream(static_cast<size_t>(width + len));  // window || drafts
+    for (int64_t j = 0; j < width; ++j) stream[j] = old_at(off + j);
+    for (int64_t t = 0; t < len; ++t) stream[width + t] = x[(lo + t) * x_stride + c];
+    for (int64_t t = 0; t < len; ++t) {
+      R acc = R(0);
+      for (int64_t j = 0; j < kw; ++j) acc += stream[t + j] * w[c * kw + j];
+      const R y = silu_(acc);
+      const int64_t tt = lo + t;
+      if (c < qk_total)
+        q[tt * qk_total + c] = y;
+      else if (c < 2 * qk_total)
+        k[tt * qk_total + (c - qk_total)] = y;
+      else
+        v[tt * v_total + (c - 2 * qk_total)] = y;
+    }
+    if (!live) return;
+    const int64_t keep = state_len - len;
+    std::vector<R> next(static_cast<size_t>(state_len));
+    for (int64_t j = 0; j < keep; ++j) next[j] = old_at(off + 1 + j);
+    for (int64_t t = 0; t < len; ++t) next[keep + t] = stream[width + t];
+    std::copy(next.begin(), next.end(), row);
+  });
+  prepare_gates_norm(a_raw, a_stride, b_raw, b_stride, a_log, dt_bias, tokens, hk_n, hv_n, dk,
+                     apply_norm, q, k, g, beta, nthreads);
   return ORC_OK;
 }
 
@@ -684,6 +769,26 @@ int orc_validate_state_indices(const int32_t* indices, int64_t n, int64_t slots,
     }
   }
   return ORC_OK;
+}
+
+#define ORC_SPEC_PREP_PARAMS(R)                                                             \
+  const R *mixed_qkv, int64_t x_stride, const R *conv_weight, R *conv_pool,                 \
+      int64_t conv_slots, int64_t state_len, const int32_t *conv_indices,                   \
+      const int32_t *num_accepted, const R *a_raw, int64_t a_stride, const R *b_raw,        \
+      int64_t b_stride, const R *A_log, const R *dt_bias, const int32_t *cu_seqlens,        \
+      int64_t n_reqs, int64_t tokens, int64_t key_heads, int64_t value_heads,               \
+      int64_t key_dim, int64_t value_dim, int64_t conv_kernel, int apply_qk_l2norm,         \
+      R *query, R *key, R *value, R *g, R *beta, int nthreads
+#define ORC_SPEC_PREP_ARGS                                                                  \
+  mixed_qkv, x_stride, conv_weight, conv_pool, conv_slots, state_len, conv_indices,         \
+      num_accepted, a_raw, a_stride, b_raw, b_stride, A_log, dt_bias, cu_seqlens, n_reqs,   \
+      tokens, key_heads, value_heads, key_dim, value_dim, conv_kernel, apply_qk_l2norm,     \
+      query, key, value, g, beta, nthreads
+int orc_spec_prepare_f32(ORC_SPEC_PREP_PARAMS(float)) {
+  return spec_prepare_impl<float>(ORC_SPEC_PREP_ARGS);
+}
+int orc_spec_prepare_f64(ORC_SPEC_PREP_PARAMS(double)) {
+  return spec_prepare_impl<double>(ORC_SPEC_PREP_ARGS);
 }
 
 int orc_prepare_varlen_f32(ORC_PREPARE_PARAMS(float)) {

@@ -103,6 +103,36 @@ int orc_validate_state_indices(const int32_t* indices, int64_t n, int64_t state_
 int orc_prepare_varlen_f32(ORC_PREPARE_PARAMS(float));
 int orc_prepare_varlen_f64(ORC_PREPARE_PARAMS(double));
 
+/* ---- O8: speculative prepare, [cpu_ops.cpp] CausalConv1dSpecUpdateKernel ----
+ * O1 for the draft tokens of a speculative step.  conv_pool is
+ * [conv_slots, C_conv, state_len], state_len = (K-1) + (max_q - 1); request i
+ * uses row conv_indices[i] (negative: outputs from a zero window, no row
+ * written).  With off = num_accepted[i] - 1 the conv window before the first
+ * draft is row[off .. off+K-2]; the row becomes row[off+1 .. off+keep] ||
+ * drafts, keep = state_len - len.  Split, gates and norm as O1.
+ * ORC_ERR_INVALID for bad cu_seqlens, a request longer than max_q,
+ * num_accepted outside [1, max_q] or a slot >= conv_slots. */
+int orc_spec_prepare_f32(const float* mixed_qkv, int64_t x_stride, const float* conv_weight,
+                         float* conv_pool, int64_t conv_slots, int64_t state_len,
+                         const int32_t* conv_indices, const int32_t* num_accepted,
+                         const float* a_raw, int64_t a_stride, const float* b_raw,
+                         int64_t b_stride, const float* A_log, const float* dt_bias,
+                         const int32_t* cu_seqlens, int64_t n_reqs, int64_t tokens,
+                         int64_t key_heads, int64_t value_heads, int64_t key_dim,
+                         int64_t value_dim, int64_t conv_kernel, int apply_qk_l2norm,
+                         float* query, float* key, float* value, float* g, float* beta,
+                         int nthreads);
+int orc_spec_prepare_f64(const double* mixed_qkv, int64_t x_stride, const double* conv_weight,
+                         double* conv_pool, int64_t conv_slots, int64_t state_len,
+                         const int32_t* conv_indices, const int32_t* num_accepted,
+                         const double* a_raw, int64_t a_stride, const double* b_raw,
+                         int64_t b_stride, const double* A_log, const double* dt_bias,
+                         const int32_t* cu_seqlens, int64_t n_reqs, int64_t tokens,
+                         int64_t key_heads, int64_t value_heads, int64_t key_dim,
+                         int64_t value_dim, int64_t conv_kernel, int apply_qk_l2norm,
+                         double* query, double* key, double* value, double* g, double* beta,
+                         int nthreads);
+
 /* ---- O2: sequential recurrence over varlen sequences ----------------------
  * [cpu.rs] recurrent_gated_delta_rule_varlen_f32 (loop order, q/k norm form,
  * k scaled by k_inv, q by q_inv*scale) on a state pool:

@@ -9,7 +9,9 @@ window, eps outside the sqrt, a wrong sigmoid branch or softplus threshold, a
 dropped factor in the chunked form, a gated norm over the sum instead of the
 mean, swapped gates or unstrided gate rows, a KDA decay taken from one channel
 or applied after the dot, a speculative decode that starts from the wrong
-column, stores each snapshot one column late or loses the state at a -1 column.
+column, stores each snapshot one column late or loses the state at a -1 column, a
+speculative conv window read one tap late or a conv row shifted by the
+request length instead of one tap.
 """
 import os
 
@@ -23,6 +25,7 @@ import test_oracle_gates as G
 import test_oracle_prepare as P
 import test_oracle_recurrence as R
 import test_oracle_spec_decode as SD
+import test_oracle_spec_prepare as SP
 
 MUTATIONS = [
     ("decay_after_dot",
@@ -97,6 +100,14 @@ MUTATIONS = [
      "      if (slot < 0) continue;\n      std::copy(",
      "      if (slot < 0) { std::fill(S.begin(), S.end(), R(0)); continue; }\n      std::copy(",
      [SD.test_null_initial_slot_and_null_columns]),
+    ("spec_conv_window_one_tap_late",
+     "for (int64_t j = 0; j < width; ++j) stream[j] = old_at(off + j);",
+     "for (int64_t j = 0; j < width; ++j) stream[j] = old_at(off + 1 + j);",
+     [lambda: SP.test_outputs_are_the_convolution_of_the_accepted_history(4)]),
+    ("spec_conv_row_shift_by_len",
+     "for (int64_t j = 0; j < keep; ++j) next[j] = old_at(off + 1 + j);",
+     "for (int64_t j = 0; j < keep; ++j) next[j] = old_at(off + len + j);",
+     [lambda: SP.test_outputs_are_the_convolution_of_the_accepted_history(4)]),
     ("chunked_drops_decay_in_W",
      "const double tw = T[i * L + j] * bc[j] * std::exp(gam[j]);",
      "const double tw = T[i * L + j] * bc[j];",
