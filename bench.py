@@ -394,6 +394,72 @@ def time_spec_decode(dev, peaks, n_reqs=128, num_cols=4, Hk=16, Hv=32, D=128, sl
             "achieved_gbs": round(gbs, 1), "hbm_frac_of_measured": round(gbs / peaks["hbm"], 4)}
 
 
+def time_spec_prepare(dev, peaks, n_reqs=128, max_q=4, Hk=16, Hv=32, D=128, K=4, slots=1024,
+                      iters=10):
+    """gdn_spec_prepare on the same multi-token-prediction step (128 requests
+    x 4 drafts, conv rows of (K-1) + (max_q-1) = 6 raw inputs per channel).
+    Algorithmic bytes: mixed_qkv read and q, k, v written once (bf16), each
+    request's conv row read and written once (f32), the gate inputs (bf16)
+    and outputs (f32), the conv weights."""
+    import torch
+    from gated_delta_rule_44_gb300 import binding as B
+    gen = torch.Generator().manual_seed(31)
+    T, C, width = n_reqs * max_q, 2 * Hk * D + Hv * D, (K - 1) + (max_q - 1)
+    x = torch.randn(T, C, generator=gen).to(torch.bfloat16).to(dev)
+    wconv = (torch.randn(C, K, generator=gen) * 0.4).to(dev)
+    a = torch.randn(T, Hv, generator=gen).to(torch.bfloat16).to(dev)
+    b = torch.randn(T, Hv, generator=gen).to(torch.bfloat16).to(dev)
+    A_log, dt_bias = torch.zeros(Hv, device=dev), torch.zeros(Hv, device=dev)
+    pool = torch.randn(slots, C, width, generator=gen).to(dev)
+    idx = torch.randperm(slots, generator=gen)[:n_reqs].to(torch.int32).to(dev)
+    nat = torch.randint(1, max_q + 1, (n_reqs,), generator=gen, dtype=torch.int32).to(dev)
+    cu = (torch.arange(n_reqs + 1, dtype=torch.int32) * max_q).to(dev)
+    q = torch.empty(T, Hk, D, dtype=torch.bfloat16, device=dev)
+    k = torch.empty_like(q)
+    v = torch.empty(T, Hv, D, dtype=torch.bfloat16, device=dev)
+    g = torch.empty(T, Hv, device=dev)
+    beta = torch.empty_like(g)
+    s = torch.cuda.current_stream(dev)
+
+    def call():
+        B.gdn_spec_prepare(x, wconv, a, b, A_log, dt_bias, cu, pool, idx, nat, q, k, v, g, beta,
+                           Hk=Hk, Hv=Hv, Dk=D, Dv=D, K=K, stream=s)
+
+    for _ in range(3):
+        call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(s)
+    for _ in range(iters):
+        call()
+    e1.record(s)
+    torch.cuda.synchronize(dev)
+    host_us = e0.elapsed_time(e1) / iters * 1e3
+    # The kernel is shorter than one call's host-side marshalling, so the loop
+    # above measures the host.  Device time: the same calls captured in a
+    # CUDA graph and replayed.
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        cs = torch.cuda.current_stream(dev)
+        for _ in range(iters):
+            B.gdn_spec_prepare(x, wconv, a, b, A_log, dt_bias, cu, pool, idx, nat, q, k, v, g,
+                               beta, Hk=Hk, Hv=Hv, Dk=D, Dv=D, K=K, stream=cs)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    e0.record(s)
+    graph.replay()
+    e1.record(s)
+    torch.cuda.synchronize(dev)
+    us = e0.elapsed_time(e1) / iters * 1e3
+    nbytes = (2 * T * C * 2 + 2 * n_reqs * C * width * 4 + 2 * T * Hv * 2 + 2 * T * Hv * 4
+              + C * K * 4 + 4 * (2 * n_reqs + 1))
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"tokens_per_s": round(T / (us * 1e-6), 1), "avg_us": round(us, 2),
+            "timing": "CUDA graph of the calls", "host_loop_us": round(host_us, 2),
+            "requests": n_reqs, "max_q": max_q, "algorithmic_bytes": nbytes,
+            "achieved_gbs": round(gbs, 1), "hbm_frac_of_measured": round(gbs / peaks["hbm"], 4)}
+
+
 def time_e2e(w, dev, steps, warmup, algo):
     """Same step through the public API with the step's inputs in pinned host
     memory: every step copies its inputs host -> device and its output
@@ -580,6 +646,7 @@ def main():
         extra["gated_rmsnorm"] = time_gated_rmsnorm(w, dev, peaks)
         extra["kda_decode_b256"] = time_kda_decode(dev, peaks)
         extra["spec_decode_r128x4"] = time_spec_decode(dev, peaks)
+        extra["spec_prepare_r128x4"] = time_spec_prepare(dev, peaks)
         line["extra_workloads"] = extra
     if rank == 0 and not args.no_e2e:
         line["e2e"] = time_e2e(w, dev, max(3, args.steps // 2), 3, args.algo)

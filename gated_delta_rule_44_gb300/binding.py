@@ -53,6 +53,11 @@ class gdn_prepare_args(ctypes.Structure):
                 ("beta_len", _i64)]
 
 
+class gdn_spec_prepare_args(ctypes.Structure):
+    _fields_ = [("base", gdn_prepare_args), ("conv_state_width", _i64), ("num_accepted", _vp),
+                ("num_accepted_host", _vp)]
+
+
 class gdn_decode_args(ctypes.Structure):
     _fields_ = [("B", _i64), ("Hk", _i64), ("Hv", _i64), ("Dk", _i64), ("Dv", _i64),
                 ("act_dtype", _i32), ("use_qk_l2norm", _i32), ("scale", _f32),
@@ -105,7 +110,7 @@ class gdn_gated_rmsnorm_args(ctypes.Structure):
 
 
 EXPORTED = ("gdn_prepare", "gdn_decode", "gdn_prefill_varlen", "gdn_kda_varlen",
-            "gdn_spec_decode", "gdn_gated_rmsnorm",
+            "gdn_spec_prepare", "gdn_spec_decode", "gdn_gated_rmsnorm",
             "gdn_prefill_workspace_bytes",
             "gdn_prefill_resolve_algo", "gdn_status_string", "gdn_last_error_message",
             "gdn_read_device_status", "gdn_version", "gdn_launch_count")
@@ -130,7 +135,7 @@ def lib() -> ctypes.CDLL:
         if _lib is None:
             L = ctypes.CDLL(_build.build_library())
             for name in ("gdn_prepare", "gdn_decode", "gdn_prefill_varlen", "gdn_kda_varlen",
-                         "gdn_spec_decode", "gdn_gated_rmsnorm",
+                         "gdn_spec_prepare", "gdn_spec_decode", "gdn_gated_rmsnorm",
                          "gdn_read_device_status", "gdn_version"):
                 getattr(L, name).restype = ctypes.c_int
             L.gdn_prepare.argtypes = [ctypes.POINTER(gdn_prepare_args), _vp]
@@ -139,6 +144,7 @@ def lib() -> ctypes.CDLL:
             L.gdn_gated_rmsnorm.argtypes = [ctypes.POINTER(gdn_gated_rmsnorm_args), _vp]
             L.gdn_kda_varlen.argtypes = [ctypes.POINTER(gdn_kda_args), _vp]
             L.gdn_spec_decode.argtypes = [ctypes.POINTER(gdn_spec_decode_args), _vp]
+            L.gdn_spec_prepare.argtypes = [ctypes.POINTER(gdn_spec_prepare_args), _vp]
             L.gdn_read_device_status.argtypes = [_vp]
             L.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
             L.gdn_prefill_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64, _i64, _i32, _i32]
@@ -194,12 +200,11 @@ def _host_i32(t: Optional[torch.Tensor]):
     return h, h.data_ptr()
 
 
-def gdn_prepare(mixed_qkv, conv_weight, a_raw, b_raw, A_log, dt_bias, cu_seqlens, conv_state,
-                q, k, v, g, beta, *, Hk, Hv, Dk, Dv, K, state_indices=None,
-                has_initial_state=None, cu_seqlens_host=None, state_indices_host=None,
-                apply_qk_l2norm=True, stream=None) -> None:
-    """include/gdn.h gdn_prepare; outputs q, k, v, g, beta are written, the
-    conv_state pool is updated in place."""
+def _prepare_args(mixed_qkv, conv_weight, a_raw, b_raw, A_log, dt_bias, cu_seqlens, conv_state,
+                  q, k, v, g, beta, Hk, Hv, Dk, Dv, K, state_indices, has_initial_state,
+                  cu_seqlens_host, state_indices_host, apply_qk_l2norm):
+    """gdn_prepare_args of the call, and the host mirrors it points to (kept
+    alive by the caller)."""
     T = mixed_qkv.shape[0]
     N = cu_seqlens.numel() - 1
     cuh, cuh_p = _host_i32(cu_seqlens_host)
@@ -218,7 +223,36 @@ def gdn_prepare(mixed_qkv, conv_weight, a_raw, b_raw, A_log, dt_bias, cu_seqlens
         conv_state_slots=conv_state.shape[0] if conv_state is not None else 0,
         conv_state_len=_n(conv_state), q=_p(q), q_len=_n(q), k=_p(k), k_len=_n(k), v=_p(v),
         v_len=_n(v), g=_p(g), g_len=_n(g), beta=_p(beta), beta_len=_n(beta))
+    return a, (cuh, sih)
+
+
+def gdn_prepare(mixed_qkv, conv_weight, a_raw, b_raw, A_log, dt_bias, cu_seqlens, conv_state,
+                q, k, v, g, beta, *, Hk, Hv, Dk, Dv, K, state_indices=None,
+                has_initial_state=None, cu_seqlens_host=None, state_indices_host=None,
+                apply_qk_l2norm=True, stream=None) -> None:
+    """include/gdn.h gdn_prepare; outputs q, k, v, g, beta are written, the
+    conv_state pool is updated in place."""
+    a, keep = _prepare_args(mixed_qkv, conv_weight, a_raw, b_raw, A_log, dt_bias, cu_seqlens,
+                            conv_state, q, k, v, g, beta, Hk, Hv, Dk, Dv, K, state_indices,
+                            has_initial_state, cu_seqlens_host, state_indices_host,
+                            apply_qk_l2norm)
     _check(lib().gdn_prepare(ctypes.byref(a), _stream(stream)))
+
+
+def gdn_spec_prepare(mixed_qkv, conv_weight, a_raw, b_raw, A_log, dt_bias, cu_seqlens,
+                     conv_state, conv_indices, num_accepted, q, k, v, g, beta, *, Hk, Hv, Dk, Dv,
+                     K, cu_seqlens_host=None, conv_indices_host=None, num_accepted_host=None,
+                     apply_qk_l2norm=True, stream=None) -> None:
+    """include/gdn.h gdn_spec_prepare; conv_state [slots, C_conv, width] with
+    width = (K-1) + (max_q-1), updated in place; conv_indices, num_accepted
+    [requests] int32."""
+    base, keep = _prepare_args(mixed_qkv, conv_weight, a_raw, b_raw, A_log, dt_bias, cu_seqlens,
+                               conv_state, q, k, v, g, beta, Hk, Hv, Dk, Dv, K, conv_indices,
+                               None, cu_seqlens_host, conv_indices_host, apply_qk_l2norm)
+    nah, nah_p = _host_i32(num_accepted_host)
+    a = gdn_spec_prepare_args(base=base, conv_state_width=conv_state.shape[2],
+                              num_accepted=_p(num_accepted), num_accepted_host=nah_p)
+    _check(lib().gdn_spec_prepare(ctypes.byref(a), _stream(stream)))
 
 
 def gdn_decode(q, k, v, g, beta, state, out, *, scale=-1.0, state_indices=None,

@@ -109,6 +109,43 @@ int check_indices_host(const int32_t* idx, int64_t n, int64_t slots) {
   return GDN_OK;
 }
 
+// [qwen3_5.cpp] spec metadata validation, on the host mirrors: offsets span
+// the tokens, a request holds at most num_cols tokens (empty requests are
+// allowed, as [cpu_ops.cpp] GdnSpecDecodeKernel skips them), num_accepted in
+// [1, num_cols], slots below state_slots; and no live slot is named by two
+// requests' rows (their CTAs would race on it).
+int check_spec_host(const int32_t* cu, const int32_t* sidx, const int32_t* nat, int64_t n,
+                    int64_t cols, int64_t total, int64_t slots) {
+  if (cu != nullptr) {
+    if (cu[0] != 0 || cu[n] != total)
+      return fail(GDN_ERR_INVALID_ARGUMENT, "spec query offsets must span the spec tokens");
+    for (int64_t i = 0; i < n; ++i)
+      if (cu[i + 1] < cu[i] || cu[i + 1] - cu[i] > cols)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "spec request " + S(i) + " has range " +
+                                                  S(cu[i]) + ".." + S(cu[i + 1]) +
+                                                  ", not 0.." + S(cols) + " tokens");
+  }
+  if (nat != nullptr)
+    for (int64_t i = 0; i < n; ++i)
+      if (nat[i] < 1 || nat[i] > cols)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "num_accepted_tokens must be in [1, num_spec + 1]");
+  if (sidx != nullptr) {
+    std::vector<int64_t> owner(static_cast<size_t>(slots), -1);
+    for (int64_t i = 0; i < n; ++i)
+      for (int64_t c = 0; c < cols; ++c) {
+        const int32_t slot = sidx[i * cols + c];
+        if (slot < 0) continue;
+        if (slot >= slots)
+          return fail(GDN_ERR_INVALID_ARGUMENT, "spec GDN state slot out of range");
+        if (owner[slot] >= 0 && owner[slot] != i)
+          return fail(GDN_ERR_INVALID_ARGUMENT, "spec GDN state slot " + S(slot) +
+                                                    " named by two requests");
+        owner[slot] = i;
+      }
+  }
+  return GDN_OK;
+}
+
 bool fits_i32(int64_t v) { return v >= 0 && v <= INT32_MAX; }
 
 int launch_result(cudaError_t e, const char* what) {
@@ -161,8 +198,12 @@ int gdn_read_device_status(void* stream) {
   return succeed();
 }
 
-int gdn_prepare(const gdn_prepare_args* a, void* stream) {
-  if (a == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "args is NULL");
+namespace {
+
+// The checks gdn_prepare and gdn_spec_prepare share, up to the per-sequence
+// metadata; fills *p.  row_len is the conv row length per channel: K-1, or
+// the widened row of a speculative step.
+int prepare_common(const gdn_prepare_args* a, int64_t row_len, gdn::PrepareLaunch* out) {
   if (int rc = check_act_dtype(a->act_dtype)) return rc;
   // [cpu.rs] validate_linear_attention_prepare_shape
   if (a->T <= 0 || a->Hk <= 0 || a->Hv <= 0 || a->Dk <= 0 || a->Dv <= 0 || a->K <= 0)
@@ -194,8 +235,7 @@ int gdn_prepare(const gdn_prepare_args* a, void* stream) {
   if (int rc = check_lengths("linear_attention_prepare", rules)) return rc;
   if (a->conv_state_slots <= 0)
     return fail(GDN_ERR_SHAPE, "linear_attention_prepare conv_state must have at least one slot");
-  const LenRule pool_rule[] = {
-      {"conv_state", a->conv_state_len, a->conv_state_slots * C * (a->K - 1)}};
+  const LenRule pool_rule[] = {{"conv_state", a->conv_state_len, a->conv_state_slots * C * row_len}};
   if (int rc = check_lengths("linear_attention_prepare", pool_rule)) return rc;
   for (auto pr : {std::make_pair((const void*)a->mixed_qkv, "mixed_qkv"),
                   std::make_pair((const void*)a->conv_weight, "conv_weight"),
@@ -208,7 +248,7 @@ int gdn_prepare(const gdn_prepare_args* a, void* stream) {
                   std::make_pair((const void*)a->v, "v"), std::make_pair((const void*)a->g, "g"),
                   std::make_pair((const void*)a->beta, "beta")})
     if (int rc = require_ptr(pr.first, pr.second)) return rc;
-  if (a->K > 1)
+  if (row_len > 0)
     if (int rc = require_ptr(a->conv_state, "conv_state")) return rc;
   // Kernel coverage.
   const int64_t cpt = a->act_dtype == GDN_DTYPE_BF16 ? 8 : 4;  // channels per 16-byte vector
@@ -226,15 +266,9 @@ int gdn_prepare(const gdn_prepare_args* a, void* stream) {
     if (int rc = require_aligned(pr.first, pr.second)) return rc;
   if ((x_stride * es) % 16 != 0)
     return fail(GDN_ERR_INVALID_ARGUMENT, "mixed_qkv row stride must be a multiple of 16 bytes");
-  if (a->cu_seqlens_host != nullptr)
-    if (int rc = check_cu_host(a->cu_seqlens_host, a->N, a->T, "linear_attention_prepare_varlen"))
-      return rc;
-  if (a->state_indices_host != nullptr)
-    if (int rc = check_indices_host(a->state_indices_host, a->N, a->conv_state_slots)) return rc;
-  if (a->state_indices == nullptr && a->N > a->conv_state_slots)
-    return fail(GDN_ERR_SHAPE, "linear_attention_prepare conv_state has fewer slots than sequences");
 
-  gdn::PrepareLaunch p{};
+  gdn::PrepareLaunch& p = *out;
+  p = gdn::PrepareLaunch{};
   p.T = (int)a->T;
   p.N = (int)a->N;
   p.Hk = (int)a->Hk;
@@ -263,9 +297,64 @@ int gdn_prepare(const gdn_prepare_args* a, void* stream) {
   p.v = a->v;
   p.g = a->g;
   p.beta = a->beta;
+  return GDN_OK;
+}
+
+}  // namespace
+
+int gdn_prepare(const gdn_prepare_args* a, void* stream) {
+  if (a == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "args is NULL");
+  gdn::PrepareLaunch p;
+  if (int rc = prepare_common(a, a->K - 1, &p)) return rc;
+  if (a->cu_seqlens_host != nullptr)
+    if (int rc = check_cu_host(a->cu_seqlens_host, a->N, a->T, "linear_attention_prepare_varlen"))
+      return rc;
+  if (a->state_indices_host != nullptr)
+    if (int rc = check_indices_host(a->state_indices_host, a->N, a->conv_state_slots)) return rc;
+  if (a->state_indices == nullptr && a->N > a->conv_state_slots)
+    return fail(GDN_ERR_SHAPE, "linear_attention_prepare conv_state has fewer slots than sequences");
   p.status = gdn::status_word();
   if (p.status == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
   return launch_result(gdn::launch_prepare(p, static_cast<cudaStream_t>(stream)), "gdn_prepare");
+}
+
+int gdn_spec_prepare(const gdn_spec_prepare_args* sa, void* stream) {
+  if (sa == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "args is NULL");
+  const gdn_prepare_args* a = &sa->base;
+  const int64_t width = a->K - 1, row = sa->conv_state_width, max_q = row - width + 1;
+  if (a->K < 2)
+    return fail(GDN_ERR_UNSUPPORTED, "gdn_spec_prepare needs conv_kernel >= 2 (a conv tail to carry)");
+  if (row < width || max_q < 1)
+    return fail(GDN_ERR_SHAPE, "spec conv row of " + S(row) + " entries is shorter than conv_kernel - 1 = " +
+                                   S(width));
+  if (a->has_initial_state != nullptr)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "spec conv update takes no has_initial_state");
+  gdn::PrepareLaunch p;
+  if (int rc = prepare_common(a, row, &p)) return rc;
+  for (auto pr : {std::make_pair((const void*)a->state_indices, "state_indices"),
+                  std::make_pair((const void*)sa->num_accepted, "num_accepted")})
+    if (int rc = require_ptr(pr.first, pr.second)) return rc;
+  if (a->T > a->N * max_q)
+    return fail(GDN_ERR_SHAPE, "spec conv update has " + S(a->T) + " tokens, more than requests * "
+                               "max_query_len = " + S(a->N * max_q));
+  if (row > 16)
+    return fail(GDN_ERR_UNSUPPORTED, "gdn_spec_prepare supports conv rows of at most 16 entries");
+  // [qwen3_5.cpp] spec metadata rules on the host mirrors: requests of at
+  // most max_q tokens, num_accepted in [1, max_q], one conv row per request
+  if (int rc = check_spec_host(a->cu_seqlens_host, nullptr, sa->num_accepted_host, a->N, max_q,
+                               a->T, a->conv_state_slots))
+    return rc;
+  if (int rc = check_spec_host(nullptr, a->state_indices_host, nullptr, a->N, 1, a->T,
+                               a->conv_state_slots))
+    return rc;
+  p.sidx = a->state_indices;
+  p.has_init = nullptr;
+  p.state_len = (int)row;
+  p.num_accepted = sa->num_accepted;
+  p.status = gdn::status_word();
+  if (p.status == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
+  return launch_result(gdn::launch_spec_prepare(p, static_cast<cudaStream_t>(stream)),
+                       "gdn_spec_prepare");
 }
 
 namespace {
@@ -392,43 +481,6 @@ int gdn_kda_varlen(const gdn_kda_args* a, void* stream) {
   p.status = gdn::status_word();
   if (p.status == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
   return launch_result(gdn::launch_kda(p, static_cast<cudaStream_t>(stream)), "gdn_kda_varlen");
-}
-
-// [qwen3_5.cpp] spec metadata validation, on the host mirrors: offsets span
-// the tokens, a request holds at most num_cols tokens (empty requests are
-// allowed, as [cpu_ops.cpp] GdnSpecDecodeKernel skips them), num_accepted in
-// [1, num_cols], slots below state_slots; and no live slot is named by two
-// requests' rows (their CTAs would race on it).
-int check_spec_host(const int32_t* cu, const int32_t* sidx, const int32_t* nat, int64_t n,
-                    int64_t cols, int64_t total, int64_t slots) {
-  if (cu != nullptr) {
-    if (cu[0] != 0 || cu[n] != total)
-      return fail(GDN_ERR_INVALID_ARGUMENT, "spec query offsets must span the spec tokens");
-    for (int64_t i = 0; i < n; ++i)
-      if (cu[i + 1] < cu[i] || cu[i + 1] - cu[i] > cols)
-        return fail(GDN_ERR_INVALID_ARGUMENT, "spec request " + S(i) + " has range " +
-                                                  S(cu[i]) + ".." + S(cu[i + 1]) +
-                                                  ", not 0.." + S(cols) + " tokens");
-  }
-  if (nat != nullptr)
-    for (int64_t i = 0; i < n; ++i)
-      if (nat[i] < 1 || nat[i] > cols)
-        return fail(GDN_ERR_INVALID_ARGUMENT, "num_accepted_tokens must be in [1, num_spec + 1]");
-  if (sidx != nullptr) {
-    std::vector<int64_t> owner(static_cast<size_t>(slots), -1);
-    for (int64_t i = 0; i < n; ++i)
-      for (int64_t c = 0; c < cols; ++c) {
-        const int32_t slot = sidx[i * cols + c];
-        if (slot < 0) continue;
-        if (slot >= slots)
-          return fail(GDN_ERR_INVALID_ARGUMENT, "spec GDN state slot out of range");
-        if (owner[slot] >= 0 && owner[slot] != i)
-          return fail(GDN_ERR_INVALID_ARGUMENT, "spec GDN state slot " + S(slot) +
-                                                    " named by two requests");
-        owner[slot] = i;
-      }
-  }
-  return GDN_OK;
 }
 
 int gdn_spec_decode(const gdn_spec_decode_args* a, void* stream) {

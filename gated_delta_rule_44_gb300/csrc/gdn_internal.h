@@ -39,6 +39,8 @@ struct PrepareLaunch {
   const uint8_t* has_init;  // may be null
   float* conv_pool;
   int64_t slots;
+  int state_len;                // speculative prepare: conv row length per channel
+  const int32_t* num_accepted;  // speculative prepare: [N]
   void* q;
   void* k;
   void* v;
@@ -47,6 +49,10 @@ struct PrepareLaunch {
   unsigned* status;
 };
 cudaError_t launch_prepare(const PrepareLaunch& p, cudaStream_t s);
+// The prepare of a speculative step: sequence s's conv row (slot sidx[s],
+// state_len entries per channel) is read at offset num_accepted[s] - 1 and
+// shifted by one tap; has_init is ignored.
+cudaError_t launch_spec_prepare(const PrepareLaunch& p, cudaStream_t s);
 
 // One token per row (decode) or token-sequential over sequences (recurrent
 // prefill) -- the same register-resident row update.

@@ -4,7 +4,8 @@
 // Defines: [cpu.rs] (ferrum-kernels 0.8.0, src/ferrum_kernels/backend/cpu.rs)
 // linear_attention_prepare_varlen_f32 and linear_attention_decode_prepare_
 // batch_f32; [cpu_ops.cpp] (vllm.cpp, src/vt/cpu/cpu_ops.cpp)
-// CausalConv1dFwdKernel, CausalConv1dUpdateKernel and GdnPostConvKernel.
+// CausalConv1dFwdKernel, CausalConv1dUpdateKernel, CausalConv1dSpecUpdateKernel
+// and GdnPostConvKernel.
 //
 // Work decomposition.  A thread owns one 16-byte vector of channels (8 bf16 or
 // 4 f32) and walks the tokens of a tile in order, keeping the last K-1 raw
@@ -239,12 +240,14 @@ __global__ void __launch_bounds__(kThreads, 4) prepare_kernel(const PrepareLaunc
   // ---- interior tile: every token's window lies inside one sequence --------------
   // Groups of kG rows: the next group's loads are issued as this group's rows
   // are consumed; the L2 norms of a group's kG tokens share their shuffle
-  // rounds.  A warp's 256 channels never straddle q, k and v, so the norm is
-  // skipped on v warps.
+  // rounds.  The shuffles run on every warp that holds a q or k channel (a
+  // warp-uniform test: with 2*Hk*Dk below a multiple of the warp's channels a
+  // warp holds k and v lanes), and the scaling on q and k lanes only; warps of
+  // v channels alone skip both.
   if (seq_lo + W <= t_begin && t_end <= seq_hi) {
     constexpr int kG = 4;
     const int n = t_end - t_begin;
-    const bool do_norm = p.norm && is_qk;  // uniform across the warp
+    const bool norm_warp = p.norm && (c0 - lane * V) < 2 * qk_total;  // lane 0's channel
     const TA* xrow = x + (int64_t)t_begin * p.x_stride + c0;
     float win[WV][V];
 #pragma unroll
@@ -286,16 +289,17 @@ __global__ void __launch_bounds__(kThreads, 4) prepare_kernel(const PrepareLaunc
 #pragma unroll
           for (int i = 0; i < V; ++i) win[WV - 1][i] = xt[i];
       }
-      if (do_norm) {
+      if (norm_warp) {
         for (int m = 1; m < group; m <<= 1)
 #pragma unroll
           for (int u = 0; u < kG; ++u) ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], m);
+        if (is_qk)
 #pragma unroll
-        for (int u = 0; u < kG; ++u) {
-          const float inv = rsqrtf(ss[u] + 1e-6f);
+          for (int u = 0; u < kG; ++u) {
+            const float inv = rsqrtf(ss[u] + 1e-6f);
 #pragma unroll
-          for (int i = 0; i < V; ++i) y[u][i] *= inv;
-        }
+            for (int i = 0; i < V; ++i) y[u][i] *= inv;
+          }
       }
 #pragma unroll
       for (int u = 0; u < kG; ++u)
@@ -470,6 +474,256 @@ __global__ void __launch_bounds__(kThreads, 4) prepare_kernel(const PrepareLaunc
   }
 }
 
+// ---------------------------------------------------------------------------
+// Speculative prepare ([cpu_ops.cpp] CausalConv1dSpecUpdateKernel, then the
+// split, norm and gates above).  grid = (requests, channel blocks + 1).
+// Request i's conv row holds state_len raw inputs per channel; the window
+// before its first draft is row[off .. off+W-1], off = num_accepted[i] - 1,
+// and the row becomes row[off+1 .. off+keep] || drafts (keep = state_len -
+// drafts; entries past the row read 0).
+//
+// The CTA's rows (its channels x state_len floats, channel-major in HBM) are
+// staged in shared memory transposed -- entry j of channel c at
+// rows[j * kPitch + c] -- with coalesced 16-byte loads and stores, so that
+// each thread reads and rewrites its V channels' entry j as 16-byte vectors.
+// The pitch is padded by 4 floats to spread the transposing accesses over the
+// banks.  A thread only touches its own columns between the two barriers,
+// and the in-place shift walks j upwards (it reads entry off+1+j > j).
+template <typename TA, int KW>
+__global__ void __launch_bounds__(kThreads) spec_prepare_kernel(const PrepareLaunch p,
+                                                                int chan_blocks) {
+  constexpr int V = Act<TA>::kVec;
+  constexpr int W = KW - 1;
+  static_assert(W >= 1, "the speculative conv row needs a tail");
+  constexpr int kPitch = kThreads * V + 4;
+  extern __shared__ float4 rows4[];
+  float* rows = reinterpret_cast<float*>(rows4);
+  const int SL = p.state_len, max_q = SL - W + 1;
+  const int qk_total = p.Hk * p.Dk;
+  const int C = 2 * qk_total + p.Hv * p.Dv;
+  const int req = blockIdx.x;
+  const int lo = __ldg(p.cu + req), hi = __ldg(p.cu + req + 1);
+  if (__ldg(p.cu) != 0 || __ldg(p.cu + p.N) != p.T || lo < 0 || hi < lo || hi > p.T ||
+      hi - lo > max_q) {
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusBadSeqlens);
+    return;
+  }
+  const int len = hi - lo;
+  if (len == 0) return;  // an empty request reads and writes nothing
+
+  if (blockIdx.y == chan_blocks) {  // gates: g, beta per (token, value head)
+    const TA* __restrict__ a = static_cast<const TA*>(p.a);
+    const TA* __restrict__ b = static_cast<const TA*>(p.b);
+    for (int e = threadIdx.x; e < len * p.Hv; e += kThreads) {
+      const int t = lo + e / p.Hv, h = e % p.Hv;
+      const float av = Act<TA>::scalar(a + (int64_t)t * p.a_stride + h);
+      const float bv = Act<TA>::scalar(b + (int64_t)t * p.b_stride + h);
+      p.g[(int64_t)t * p.Hv + h] = -expf(__ldg(p.A_log + h)) * softplus_f(av + __ldg(p.dt_bias + h));
+      p.beta[(int64_t)t * p.Hv + h] = sigmoid_f(bv);
+    }
+    return;
+  }
+
+  int slot = __ldg(p.sidx + req);
+  const int accepted = __ldg(p.num_accepted + req);
+  if (slot >= p.slots || (slot >= 0 && (accepted < 1 || accepted > max_q))) {
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusBadIndex);
+    slot = -1;
+  }
+  const bool live = slot >= 0;  // uniform across the CTA
+  const int off = live ? accepted - 1 : 0;
+  const int cb = blockIdx.y * kThreads * V;
+  const int nch = min(kThreads * V, C - cb);
+  const int n4 = nch * SL / 4;  // nch is a multiple of V >= 4
+  float* grow = live ? p.conv_pool + ((int64_t)slot * C + cb) * SL : nullptr;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int col = (warp * 32 + lane) * V;  // this thread's first column in the block
+  const int c0 = cb + col;
+  const bool active = c0 < C;
+  // The first kPre drafts' inputs are requested before the rows, so their
+  // latency overlaps the staging.
+  constexpr int kPre = 4;
+  const TA* __restrict__ x = static_cast<const TA*>(p.x) + c0;
+  uint4 xpre[kPre];
+#pragma unroll
+  for (int u = 0; u < kPre; ++u)
+    xpre[u] = (active && u < len) ? Act<TA>::load_raw(x + (int64_t)(lo + u) * p.x_stride)
+                                  : make_uint4(0, 0, 0, 0);
+
+  if (live) {  // rows -> shared memory, transposed; kB loads in flight per thread
+    constexpr int kB = 4;
+    const float4* src = reinterpret_cast<const float4*>(grow);
+    for (int f0 = threadIdx.x; f0 < n4; f0 += kB * kThreads) {
+      float4 v[kB];
+#pragma unroll
+      for (int b = 0; b < kB; ++b) {
+        const int f4 = f0 + b * kThreads;
+        v[b] = f4 < n4 ? src[f4] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int b = 0; b < kB; ++b) {
+        const int f4 = f0 + b * kThreads;
+        if (f4 < n4) {
+          const float vv[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int f = 4 * f4 + u, c = f / SL;
+            rows[(f - c * SL) * kPitch + c] = vv[u];
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const bool is_qk = c0 < 2 * qk_total;
+  const bool norm_warp = p.norm && (c0 - lane * V) < 2 * qk_total;  // warp-uniform
+  const int group = p.Dk / V;                        // lanes per key head
+  const bool mine = live && active;
+
+  float wt[V][KW];
+#pragma unroll
+  for (int e = 0; e < V; ++e)
+#pragma unroll
+    for (int j = 0; j < KW; ++j) wt[e][j] = active ? __ldg(p.w + (int64_t)(c0 + e) * KW + j) : 0.0f;
+  TA* __restrict__ out_ptr;
+  int64_t out_stride;
+  if (c0 < qk_total) {
+    out_ptr = static_cast<TA*>(p.q) + c0;
+    out_stride = qk_total;
+  } else if (c0 < 2 * qk_total) {
+    out_ptr = static_cast<TA*>(p.k) + (c0 - qk_total);
+    out_stride = qk_total;
+  } else {
+    out_ptr = static_cast<TA*>(p.v) + (c0 - 2 * qk_total);
+    out_stride = (int64_t)p.Hv * p.Dv;
+  }
+
+  // entry j of this thread's channels, as V/4 float4 (j < SL)
+  auto entry = [&](int j) { return rows4 + (j * kPitch + col) / 4; };
+  float win[W][V];
+#pragma unroll
+  for (int j = 0; j < W; ++j) {
+#pragma unroll
+    for (int q4 = 0; q4 < V / 4; ++q4) {
+      const float4 v = mine ? entry(off + j)[q4] : make_float4(0.f, 0.f, 0.f, 0.f);
+      win[j][4 * q4] = v.x;
+      win[j][4 * q4 + 1] = v.y;
+      win[j][4 * q4 + 2] = v.z;
+      win[j][4 * q4 + 3] = v.w;
+    }
+  }
+  const int keep = SL - len;  // >= W - 1 >= 0
+  if (mine) {
+    for (int j = 0; j < keep; ++j) {
+      const int src = off + 1 + j;
+#pragma unroll
+      for (int q4 = 0; q4 < V / 4; ++q4)
+        entry(j)[q4] = src < SL ? entry(src)[q4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+
+  // one draft: conv + SiLU + norm + store, then the row and window updates
+  auto step = [&](int u, const float (&xt)[V]) {
+    const int t = lo + u;
+    float y[V];
+    float ss = 0.0f;
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+      float acc = 0.0f;
+#pragma unroll
+      for (int j = 0; j < W; ++j) acc = fmaf(win[j][e], wt[e][j], acc);
+      acc = fmaf(xt[e], wt[e][W], acc);
+      y[e] = silu_f(acc);
+      ss = fmaf(y[e], y[e], ss);
+    }
+    if (norm_warp) {
+      for (int m = 1; m < group; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+      if (is_qk) {
+        const float inv = rsqrtf(ss + 1e-6f);
+#pragma unroll
+        for (int e = 0; e < V; ++e) y[e] *= inv;
+      }
+    }
+    if (active) Act<TA>::store(out_ptr + (int64_t)t * out_stride, y);
+    if (mine)
+#pragma unroll
+      for (int q4 = 0; q4 < V / 4; ++q4)
+        entry(keep + u)[q4] = make_float4(xt[4 * q4], xt[4 * q4 + 1], xt[4 * q4 + 2], xt[4 * q4 + 3]);
+#pragma unroll
+    for (int j = 0; j + 1 < W; ++j)
+#pragma unroll
+      for (int e = 0; e < V; ++e) win[j][e] = win[j + 1][e];
+#pragma unroll
+    for (int e = 0; e < V; ++e) win[W - 1][e] = xt[e];
+  };
+#pragma unroll
+  for (int u = 0; u < kPre; ++u) {
+    if (u < len) {  // uniform across the CTA
+      float xt[V];
+      Act<TA>::unpack(xpre[u], xt);
+      step(u, xt);
+    }
+  }
+#pragma unroll 1
+  for (int u = kPre; u < len; ++u) {
+    float xt[V];
+    if (active) {
+      Act<TA>::load(x + (int64_t)(lo + u) * p.x_stride, xt);
+    } else {
+#pragma unroll
+      for (int e = 0; e < V; ++e) xt[e] = 0.0f;
+    }
+    step(u, xt);
+  }
+  __syncthreads();
+
+  if (live) {
+    float4* dst = reinterpret_cast<float4*>(grow);
+    for (int f4 = threadIdx.x; f4 < n4; f4 += kThreads) {
+      float vv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int f = 4 * f4 + u, c = f / SL;
+        vv[u] = rows[(f - c * SL) * kPitch + c];
+      }
+      dst[f4] = make_float4(vv[0], vv[1], vv[2], vv[3]);
+    }
+  }
+}
+
+template <typename TA, int KW>
+cudaError_t launch_spec_k(const PrepareLaunch& p, cudaStream_t s) {
+  constexpr int V = Act<TA>::kVec;
+  const int C = 2 * p.Hk * p.Dk + p.Hv * p.Dv;
+  const int chan_blocks = (C + kThreads * V - 1) / (kThreads * V);
+  const size_t smem = (size_t)p.state_len * (kThreads * V + 4) * sizeof(float);
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(spec_prepare_kernel<TA, KW>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  const dim3 grid(p.N, chan_blocks + 1);
+  if (grid.y > 65535) return cudaErrorInvalidConfiguration;
+  spec_prepare_kernel<TA, KW><<<grid, kThreads, smem, s>>>(p, chan_blocks);
+  note_launch();
+  return cudaGetLastError();
+}
+
+template <typename TA>
+cudaError_t launch_spec_dtype(const PrepareLaunch& p, cudaStream_t s) {
+  switch (p.K) {
+    case 2: return launch_spec_k<TA, 2>(p, s);
+    case 3: return launch_spec_k<TA, 3>(p, s);
+    case 4: return launch_spec_k<TA, 4>(p, s);
+    case 5: return launch_spec_k<TA, 5>(p, s);
+    case 6: return launch_spec_k<TA, 6>(p, s);
+    case 7: return launch_spec_k<TA, 7>(p, s);
+    case 8: return launch_spec_k<TA, 8>(p, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 template <typename TA, int KW>
 cudaError_t launch_k(const PrepareLaunch& p, cudaStream_t s) {
   constexpr int V = Act<TA>::kVec;
@@ -506,6 +760,12 @@ cudaError_t launch_dtype(const PrepareLaunch& p, cudaStream_t s) {
 
 cudaError_t launch_prepare(const PrepareLaunch& p, cudaStream_t s) {
   return p.bf16 ? launch_dtype<__nv_bfloat16>(p, s) : launch_dtype<float>(p, s);
+}
+
+cudaError_t launch_spec_prepare(const PrepareLaunch& p, cudaStream_t s) {
+  if (p.state_len < p.K - 1 || p.state_len > 16 || p.sidx == nullptr || p.num_accepted == nullptr)
+    return cudaErrorInvalidValue;
+  return p.bf16 ? launch_spec_dtype<__nv_bfloat16>(p, s) : launch_spec_dtype<float>(p, s);
 }
 
 }  // namespace gdn

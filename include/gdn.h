@@ -295,6 +295,50 @@ typedef struct gdn_kda_args {
 int gdn_kda_varlen(const gdn_kda_args* args, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * gdn_spec_prepare -- [cpu_ops.cpp] CausalConv1dSpecUpdateKernel followed by
+ * the split, norm and gates of gdn_prepare: the prepare step of a
+ * speculative decode (the input of gdn_spec_decode).
+ *
+ * base holds gdn_prepare's arguments with these changes: N is the number of
+ * requests, request i owning the draft tokens cu_seqlens[i] ..
+ * cu_seqlens[i+1]-1 (0 to max_q of them); state_indices [N] names each
+ * request's conv row (required; negative = none); has_initial_state must be
+ * NULL; conv_state is [conv_state_slots, C_conv, conv_state_width] with
+ * conv_state_width = (K-1) + (max_q - 1), the widened row of raw inputs.
+ * With off = num_accepted[i] - 1, the conv window before the first draft is
+ * row[off .. off+K-2], then the drafts themselves:
+ *   y[t,c] = silu( sum_{j<K} w[c,j] * (row[off..off+K-2] || x)[t' + j] )
+ * for the request's t'-th draft t.  The row then becomes
+ * row[off+1 .. off+keep] || drafts (entries past the row read 0),
+ * keep = conv_state_width - drafts: shifted by one tap per step, so that the
+ * next step's offset picks the window ending at its last accepted token.
+ * A negative row: outputs from a zero window, no row written.  An empty
+ * request: nothing.
+ *   - Host mirrors (base.cu_seqlens_host, base.state_indices_host,
+ *     num_accepted_host; optional) validate fully: offsets span 0..T, at most
+ *     max_q tokens per request, num_accepted in [1, max_q], rows below
+ *     conv_state_slots and distinct.  Without them the kernel raises the
+ *     device status word (gdn_read_device_status: GDN_ERR_DEVICE_CHECK) and
+ *     skips the request for bad offsets, or computes from a zero window and
+ *     writes no row for a bad row index or num_accepted.
+ *   - Errors as gdn_prepare, plus GDN_ERR_SHAPE for conv_state_width < K-1
+ *     or T > N * max_q, GDN_ERR_INVALID_ARGUMENT for a NULL state_indices or
+ *     num_accepted or a non-NULL has_initial_state, and GDN_ERR_UNSUPPORTED
+ *     for conv_state_width > 16.
+ *   - One CTA per (request, 1024/512-channel block) stages its conv rows in
+ *     shared memory, transposed so that each thread reads its channels'
+ *     entries as 16-byte vectors.
+ * ------------------------------------------------------------------------- */
+typedef struct gdn_spec_prepare_args {
+  gdn_prepare_args base;
+  int64_t conv_state_width;          /* (K-1) + (max_q - 1) */
+  const int32_t* num_accepted;       /* [N], device */
+  const int32_t* num_accepted_host;  /* optional host mirror */
+} gdn_spec_prepare_args;
+
+int gdn_spec_prepare(const gdn_spec_prepare_args* args, void* stream);
+
+/* ---------------------------------------------------------------------------
  * gdn_spec_decode -- [cpu_ops.cpp] GdnSpecDecodeKernel with the metadata rules
  * of [qwen3_5.cpp] (spec metadata validation): speculative multi-token decode.
  *
@@ -319,9 +363,10 @@ int gdn_kda_varlen(const gdn_kda_args* args, void* stream);
  *   - Host mirrors (optional, any subset) validate fully before launch:
  *     offsets span 0..T, request lengths in [0, num_cols], num_accepted in
  *     [1, num_cols], slots < state_slots, no slot shared by two requests.
- *     Without them the kernel flags GDN_DEVICE_BAD_SEQLENS (bad offsets) or
- *     GDN_DEVICE_BAD_INDEX (bad num_accepted or slot) in the device status
- *     word and skips the request or the store.
+ *     Without them the kernel raises the device status word
+ *     (gdn_read_device_status: GDN_ERR_DEVICE_CHECK) and skips the request
+ *     (bad offsets), zeroes its outputs (bad num_accepted or initial slot)
+ *     or skips the store (bad snapshot slot).
  *   - Errors: GDN_ERR_SHAPE for non-positive sizes, Hv % Hk != 0, short
  *     buffers or T > n_reqs * num_cols; GDN_ERR_INVALID_ARGUMENT for NULL or
  *     misaligned pointers and failed mirror checks ("num_accepted_tokens must

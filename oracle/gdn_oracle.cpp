@@ -244,8 +244,10 @@ int spec_prepare_impl(const R* x, int64_t x_stride, const R* w, R* conv_pool, in
                       int nthreads) {
   if (n_reqs <= 0 || tokens <= 0 || hk_n <= 0 || hv_n <= 0 || dk <= 0 || dv <= 0 || kw <= 0)
     return ORC_ERR_SHAPE;
+  // K >= 2: with no conv tail (K = 1) a request of max_q tokens would need
+  // keep = -1 entries of the old row
   const int64_t width = kw - 1, max_q = state_len - width + 1;
-  if (max_q < 1) return ORC_ERR_SHAPE;
+  if (kw < 2 || max_q < 1) return ORC_ERR_SHAPE;
   if (cu[0] != 0 || cu[n_reqs] != tokens) return ORC_ERR_INVALID;
   for (int64_t i = 0; i < n_reqs; ++i) {
     if (cu[i + 1] < cu[i] || cu[i + 1] - cu[i] > max_q) return ORC_ERR_INVALID;

@@ -110,8 +110,8 @@ int orc_prepare_varlen_f64(ORC_PREPARE_PARAMS(double));
  * written).  With off = num_accepted[i] - 1 the conv window before the first
  * draft is row[off .. off+K-2]; the row becomes row[off+1 .. off+keep] ||
  * drafts, keep = state_len - len.  Split, gates and norm as O1.
- * ORC_ERR_INVALID for bad cu_seqlens, a request longer than max_q,
- * num_accepted outside [1, max_q] or a slot >= conv_slots. */
+ * ORC_ERR_SHAPE for K < 2; ORC_ERR_INVALID for bad cu_seqlens, a request
+ * longer than max_q, num_accepted outside [1, max_q] or a slot >= conv_slots. */
 int orc_spec_prepare_f32(const float* mixed_qkv, int64_t x_stride, const float* conv_weight,
                          float* conv_pool, int64_t conv_slots, int64_t state_len,
                          const int32_t* conv_indices, const int32_t* num_accepted,

@@ -309,3 +309,48 @@ def test_spec_decode_rejections():
     assert rc == B.GDN_ERR_INVALID_ARGUMENT and msg == "spec GDN state slot out of range"
     rc, msg = call_spec(spec_args(state_indices_host=_host(0, 1, 2, 3, 2, -1)))
     assert rc == B.GDN_ERR_INVALID_ARGUMENT and "named by two requests" in msg
+
+
+def spec_prepare_args(T=6, N=2, max_q=3, K=4, width=None, **over):
+    C = 2 * 1 * 8 + 1 * 8
+    width = (K - 1) + (max_q - 1) if width is None else width
+    base = dict(T=T, N=N, K=K, state_indices=FAKE, conv_state_slots=4,
+                conv_state_len=4 * C * width)
+    base.update({k: v for k, v in over.items() if k in dict(B.gdn_prepare_args._fields_)})
+    a = B.gdn_spec_prepare_args(base=prepare_args(**base), conv_state_width=width,
+                                num_accepted=over.get("num_accepted", FAKE),
+                                num_accepted_host=over.get("num_accepted_host"))
+    return a
+
+
+def call_spec_prepare(args):
+    L = B.lib()
+    rc = L.gdn_spec_prepare(ctypes.byref(args), None)
+    return rc, L.gdn_last_error_message().decode()
+
+
+def test_spec_prepare_rejections():
+    rc, msg = call_spec_prepare(spec_prepare_args(width=2))   # shorter than K-1 = 3
+    assert rc == B.GDN_ERR_SHAPE and "shorter than conv_kernel - 1" in msg
+    rc, msg = call_spec_prepare(spec_prepare_args(K=1, width=2, conv_weight_len=24))
+    assert rc == B.GDN_ERR_UNSUPPORTED
+    rc, msg = call_spec_prepare(spec_prepare_args(has_initial_state=FAKE))
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT and "has_initial_state" in msg
+    assert call_spec_prepare(spec_prepare_args(state_indices=None))[0] == B.GDN_ERR_INVALID_ARGUMENT
+    assert call_spec_prepare(spec_prepare_args(num_accepted=None))[0] == B.GDN_ERR_INVALID_ARGUMENT
+    rc, msg = call_spec_prepare(spec_prepare_args(T=7))   # 7 > 2 requests x max_q 3
+    assert rc == B.GDN_ERR_SHAPE and "more than requests * max_query_len" in msg
+    rc, _ = call_spec_prepare(spec_prepare_args(max_q=15, conv_state_len=10**6))
+    assert rc == B.GDN_ERR_UNSUPPORTED                    # a row of 17 entries
+    rc, msg = call_spec_prepare(spec_prepare_args(conv_state_len=10))
+    assert rc == B.GDN_ERR_SHAPE and "conv_state length 10" in msg
+    # host mirrors
+    rc, msg = call_spec_prepare(spec_prepare_args(cu_seqlens_host=_host(0, 4, 6)))
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT and "not 0..3 tokens" in msg
+    rc, msg = call_spec_prepare(spec_prepare_args(num_accepted_host=_host(1, 4)))
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT
+    assert msg == "num_accepted_tokens must be in [1, num_spec + 1]"
+    rc, msg = call_spec_prepare(spec_prepare_args(state_indices_host=_host(1, 1)))
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT and "named by two requests" in msg
+    rc, msg = call_spec_prepare(spec_prepare_args(state_indices_host=_host(0, 4)))
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT and msg == "spec GDN state slot out of range"

@@ -108,7 +108,7 @@ def test_null_slot_and_empty_request():
     assert not np.array_equal(p[2], pool[2])
 
 
-@pytest.mark.parametrize("case", ["nat0", "nat_big", "too_long", "slot_big", "short_row"])
+@pytest.mark.parametrize("case", ["nat0", "nat_big", "too_long", "slot_big", "short_row", "k1"])
 def test_rejects_bad_metadata(case):
     r = np.random.default_rng(4)
     max_q = 3
@@ -126,10 +126,13 @@ def test_rejects_bad_metadata(case):
         cu = np.array([0, 4, 5], np.int32)
     elif case == "slot_big":
         idx[1] = 3
-    else:
+    elif case == "short_row":
         pool = np.zeros((3, C, K - 2))   # shorter than the K-1 tail
+    kw = K
+    if case == "k1":                     # no conv tail: nothing to carry
+        kw, w = 1, w[:, :1]
     with pytest.raises(oracle.OracleError):
-        oracle.spec_prepare(x, w, pool, a, b, A_log, dt_bias, cu, idx, nat, Hk, Hv, Dk, Dv, K,
+        oracle.spec_prepare(x, w, pool, a, b, A_log, dt_bias, cu, idx, nat, Hk, Hv, Dk, Dv, kw,
                             dtype=np.float64)
 
 
