@@ -460,6 +460,49 @@ def time_spec_prepare(dev, peaks, n_reqs=128, max_q=4, Hk=16, Hv=32, D=128, K=4,
             "achieved_gbs": round(gbs, 1), "hbm_frac_of_measured": round(gbs / peaks["hbm"], 4)}
 
 
+def time_packed_decode(dev, peaks, B_=256, Hk=16, Hv=32, D=128, K=4, slots=512, iters=10):
+    """gdn_packed_decode on decode_b256's shape: conv update, norm, gates and
+    the recurrence in one launch from a packed qkvz row and a b-then-a gate
+    row.  Algorithmic bytes: every live state row read and written once, the
+    conv tails read and written once, the raw rows (q, k, v channels), the
+    gate inputs, out (bf16) and the conv weights."""
+    import torch
+    from gated_delta_rule_44_gb300 import binding as B
+    gen = torch.Generator().manual_seed(37)
+    C = 2 * Hk * D + Hv * D
+    qkvz = torch.randn(B_, C + Hv * D, generator=gen).to(torch.bfloat16).to(dev)
+    wconv = (torch.randn(C, K, generator=gen) * 0.4).to(dev)
+    ba = torch.randn(B_, 2 * Hv, generator=gen).to(torch.bfloat16).to(dev)
+    a_raw, b_raw = B.packed_ba_views(ba, Hv)
+    A_log, dt_bias = torch.zeros(Hv, device=dev), torch.zeros(Hv, device=dev)
+    conv = torch.randn(slots, C, K - 1, generator=gen).to(dev)
+    pool = (torch.randn(slots, Hv, D, D, generator=gen) * 0.02).to(dev)
+    sidx = torch.randperm(slots, generator=gen)[:B_].to(torch.int32).to(dev)
+    out = torch.empty(B_, Hv, D, dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.current_stream(dev)
+
+    def call():
+        B.gdn_packed_decode(qkvz, wconv, a_raw, b_raw, A_log, dt_bias, sidx, conv, pool, out,
+                            Hk=Hk, Hv=Hv, Dk=D, Dv=D, K=K, stream=s)
+
+    for _ in range(3):
+        call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(s)
+    for _ in range(iters):
+        call()
+    e1.record(s)
+    torch.cuda.synchronize(dev)
+    us = e0.elapsed_time(e1) / iters * 1e3
+    nbytes = (B_ * Hv * D * D * 4 * 2 + B_ * C * 2 + 2 * B_ * C * (K - 1) * 4
+              + B_ * 2 * Hv * 2 + B_ * Hv * D * 2 + C * K * 4 + B_ * 4)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"tokens_per_s": round(B_ / (us * 1e-6), 1), "avg_us": round(us, 2),
+            "algorithmic_bytes": nbytes, "achieved_gbs": round(gbs, 1),
+            "hbm_frac_of_measured": round(gbs / peaks["hbm"], 4)}
+
+
 def time_e2e(w, dev, steps, warmup, algo):
     """Same step through the public API with the step's inputs in pinned host
     memory: every step copies its inputs host -> device and its output
@@ -647,6 +690,7 @@ def main():
         extra["kda_decode_b256"] = time_kda_decode(dev, peaks)
         extra["spec_decode_r128x4"] = time_spec_decode(dev, peaks)
         extra["spec_prepare_r128x4"] = time_spec_prepare(dev, peaks)
+        extra["packed_decode_b256"] = time_packed_decode(dev, peaks)
         line["extra_workloads"] = extra
     if rank == 0 and not args.no_e2e:
         line["e2e"] = time_e2e(w, dev, max(3, args.steps // 2), 3, args.algo)

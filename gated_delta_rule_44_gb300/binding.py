@@ -53,6 +53,20 @@ class gdn_prepare_args(ctypes.Structure):
                 ("beta_len", _i64)]
 
 
+class gdn_packed_decode_args(ctypes.Structure):
+    _fields_ = [("B", _i64), ("Hk", _i64), ("Hv", _i64), ("Dk", _i64), ("Dv", _i64), ("K", _i64),
+                ("act_dtype", _i32), ("apply_qk_l2norm", _i32), ("scale", _f32),
+                ("mixed_qkv", _vp), ("mixed_qkv_stride", _i64), ("mixed_qkv_len", _i64),
+                ("conv_weight", _vp), ("conv_weight_len", _i64),
+                ("a_raw", _vp), ("a_raw_stride", _i64), ("a_raw_len", _i64),
+                ("b_raw", _vp), ("b_raw_stride", _i64), ("b_raw_len", _i64),
+                ("A_log", _vp), ("A_log_len", _i64), ("dt_bias", _vp), ("dt_bias_len", _i64),
+                ("state_indices", _vp), ("state_indices_host", _vp),
+                ("conv_state", _vp), ("conv_state_len", _i64),
+                ("state", _vp), ("state_slots", _i64), ("state_len", _i64),
+                ("out", _vp), ("out_len", _i64)]
+
+
 class gdn_spec_prepare_args(ctypes.Structure):
     _fields_ = [("base", gdn_prepare_args), ("conv_state_width", _i64), ("num_accepted", _vp),
                 ("num_accepted_host", _vp)]
@@ -110,7 +124,7 @@ class gdn_gated_rmsnorm_args(ctypes.Structure):
 
 
 EXPORTED = ("gdn_prepare", "gdn_decode", "gdn_prefill_varlen", "gdn_kda_varlen",
-            "gdn_spec_prepare", "gdn_spec_decode", "gdn_gated_rmsnorm",
+            "gdn_spec_prepare", "gdn_spec_decode", "gdn_packed_decode", "gdn_gated_rmsnorm",
             "gdn_prefill_workspace_bytes",
             "gdn_prefill_resolve_algo", "gdn_status_string", "gdn_last_error_message",
             "gdn_read_device_status", "gdn_version", "gdn_launch_count")
@@ -135,7 +149,7 @@ def lib() -> ctypes.CDLL:
         if _lib is None:
             L = ctypes.CDLL(_build.build_library())
             for name in ("gdn_prepare", "gdn_decode", "gdn_prefill_varlen", "gdn_kda_varlen",
-                         "gdn_spec_prepare", "gdn_spec_decode", "gdn_gated_rmsnorm",
+                         "gdn_spec_prepare", "gdn_spec_decode", "gdn_packed_decode", "gdn_gated_rmsnorm",
                          "gdn_read_device_status", "gdn_version"):
                 getattr(L, name).restype = ctypes.c_int
             L.gdn_prepare.argtypes = [ctypes.POINTER(gdn_prepare_args), _vp]
@@ -145,6 +159,7 @@ def lib() -> ctypes.CDLL:
             L.gdn_kda_varlen.argtypes = [ctypes.POINTER(gdn_kda_args), _vp]
             L.gdn_spec_decode.argtypes = [ctypes.POINTER(gdn_spec_decode_args), _vp]
             L.gdn_spec_prepare.argtypes = [ctypes.POINTER(gdn_spec_prepare_args), _vp]
+            L.gdn_packed_decode.argtypes = [ctypes.POINTER(gdn_packed_decode_args), _vp]
             L.gdn_read_device_status.argtypes = [_vp]
             L.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
             L.gdn_prefill_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64, _i64, _i32, _i32]
@@ -253,6 +268,35 @@ def gdn_spec_prepare(mixed_qkv, conv_weight, a_raw, b_raw, A_log, dt_bias, cu_se
     a = gdn_spec_prepare_args(base=base, conv_state_width=conv_state.shape[2],
                               num_accepted=_p(num_accepted), num_accepted_host=nah_p)
     _check(lib().gdn_spec_prepare(ctypes.byref(a), _stream(stream)))
+
+
+def gdn_packed_decode(mixed_qkv, conv_weight, a_raw, b_raw, A_log, dt_bias, state_indices,
+                      conv_state, state, out, *, Hk, Hv, Dk, Dv, K, scale=-1.0,
+                      apply_qk_l2norm=True, state_indices_host=None, stream=None) -> None:
+    """include/gdn.h gdn_packed_decode.  mixed_qkv [B, >= C_conv] raw rows
+    (row stride taken from the tensor, so a [B, C_conv + Hv*Dv] qkvz tensor
+    works as is); a_raw, b_raw [B, >= Hv] views (see packed_ba_views);
+    conv_state and state are updated in place."""
+    B_ = mixed_qkv.shape[0]
+    sih, sih_p = _host_i32(state_indices_host)
+    a = gdn_packed_decode_args(
+        B=B_, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, K=K, act_dtype=_dt(mixed_qkv),
+        apply_qk_l2norm=int(apply_qk_l2norm), scale=float(scale),
+        mixed_qkv=_p(mixed_qkv), mixed_qkv_stride=mixed_qkv.stride(0), mixed_qkv_len=_n(mixed_qkv),
+        conv_weight=_p(conv_weight), conv_weight_len=_n(conv_weight),
+        a_raw=_p(a_raw), a_raw_stride=a_raw.stride(0), a_raw_len=_n(a_raw),
+        b_raw=_p(b_raw), b_raw_stride=b_raw.stride(0), b_raw_len=_n(b_raw),
+        A_log=_p(A_log), A_log_len=_n(A_log), dt_bias=_p(dt_bias), dt_bias_len=_n(dt_bias),
+        state_indices=_p(state_indices), state_indices_host=sih_p,
+        conv_state=_p(conv_state), conv_state_len=_n(conv_state), state=_p(state),
+        state_slots=state.shape[0], state_len=_n(state), out=_p(out), out_len=_n(out))
+    _check(lib().gdn_packed_decode(ctypes.byref(a), _stream(stream)))
+
+
+def packed_ba_views(ba: torch.Tensor, Hv: int):
+    """(a_raw, b_raw) views of a merged gate tensor [T, 2*Hv] whose rows hold
+    b then a ([cpu.rs] linear_attention_prepare_varlen_packed_qkvz_ba_f32)."""
+    return ba[:, Hv:2 * Hv], ba[:, :Hv]
 
 
 def gdn_decode(q, k, v, g, beta, state, out, *, scale=-1.0, state_indices=None,

@@ -393,6 +393,81 @@ int check_recurrence(int64_t tokens, int64_t Hk, int64_t Hv, int64_t Dk, int64_t
 
 }  // namespace
 
+int gdn_packed_decode(const gdn_packed_decode_args* a, void* stream) {
+  if (a == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "args is NULL");
+  if (int rc = check_act_dtype(a->act_dtype)) return rc;
+  if (a->B <= 0 || a->K <= 0)
+    return fail(GDN_ERR_SHAPE, "packed GDN decode shape must be positive, got batch=" + S(a->B) +
+                                   " conv_kernel=" + S(a->K));
+  if (int rc = check_recurrence_dims(a->B, a->Hk, a->Hv, a->Dk, a->Dv)) return rc;
+  const int64_t qk_total = a->Hk * a->Dk, C = 2 * qk_total + a->Hv * a->Dv;
+  const int64_t x_stride = a->mixed_qkv_stride > 0 ? a->mixed_qkv_stride : C;
+  const int64_t a_stride = a->a_raw_stride > 0 ? a->a_raw_stride : a->Hv;
+  const int64_t b_stride = a->b_raw_stride > 0 ? a->b_raw_stride : a->Hv;
+  if (x_stride < C || a_stride < a->Hv || b_stride < a->Hv)
+    return fail(GDN_ERR_SHAPE, "packed GDN decode row stride shorter than the row");
+  if (a->state_slots <= 0) return fail(GDN_ERR_SHAPE, "gated_delta_rule state must have at least one slot");
+  const LenRule rules[] = {
+      {"mixed_qkv", a->mixed_qkv_len, (a->B - 1) * x_stride + C},
+      {"conv_weight", a->conv_weight_len, C * a->K},
+      {"a_raw", a->a_raw_len, (a->B - 1) * a_stride + a->Hv},
+      {"b_raw", a->b_raw_len, (a->B - 1) * b_stride + a->Hv},
+      {"a_log", a->A_log_len, a->Hv},
+      {"dt_bias", a->dt_bias_len, a->Hv},
+      {"conv_state", a->conv_state_len, a->state_slots * C * (a->K - 1)},
+      {"state", a->state_len, a->state_slots * a->Hv * a->Dv * a->Dk},
+      {"out", a->out_len, a->B * a->Hv * a->Dv},
+  };
+  if (int rc = check_lengths("packed_gdn_decode", rules)) return rc;
+  for (auto pr : {std::make_pair((const void*)a->mixed_qkv, "mixed_qkv"),
+                  std::make_pair((const void*)a->conv_weight, "conv_weight"),
+                  std::make_pair((const void*)a->a_raw, "a_raw"),
+                  std::make_pair((const void*)a->b_raw, "b_raw"),
+                  std::make_pair((const void*)a->A_log, "A_log"),
+                  std::make_pair((const void*)a->dt_bias, "dt_bias"),
+                  std::make_pair((const void*)a->state_indices, "state_indices"),
+                  std::make_pair((const void*)a->conv_state, "conv_state"),
+                  std::make_pair((const void*)a->state, "state"),
+                  std::make_pair((const void*)a->out, "out")})
+    if (int rc = require_ptr(pr.first, pr.second)) return rc;
+  if (int rc = require_aligned(a->state, "state")) return rc;
+  if (!gdn::packed_decode_supported((int)a->Dk, (int)a->Dv, (int)a->K))
+    return fail(GDN_ERR_UNSUPPORTED, "gdn_packed_decode supports Dk in {64, 128}, Dv <= 128 and "
+                                     "conv_kernel in [2, 4]");
+  if (!fits_i32(a->B * a->Hv * a->Dv) || !fits_i32(C))
+    return fail(GDN_ERR_UNSUPPORTED, "packed GDN decode sizes exceed 32-bit indexing");
+  if (a->state_indices_host != nullptr)
+    if (int rc = check_indices_host(a->state_indices_host, a->B, a->state_slots)) return rc;
+  gdn::PackedDecodeLaunch p{};
+  p.B = (int)a->B;
+  p.Hk = (int)a->Hk;
+  p.Hv = (int)a->Hv;
+  p.Dk = (int)a->Dk;
+  p.Dv = (int)a->Dv;
+  p.K = (int)a->K;
+  p.bf16 = a->act_dtype == GDN_DTYPE_BF16;
+  p.norm = a->apply_qk_l2norm != 0;
+  p.scale = resolve_scale(a->scale, a->Dk);
+  p.x = a->mixed_qkv;
+  p.x_stride = x_stride;
+  p.w = a->conv_weight;
+  p.a = a->a_raw;
+  p.a_stride = a_stride;
+  p.b = a->b_raw;
+  p.b_stride = b_stride;
+  p.A_log = a->A_log;
+  p.dt_bias = a->dt_bias;
+  p.sidx = a->state_indices;
+  p.conv_pool = a->conv_state;
+  p.pool = a->state;
+  p.slots = a->state_slots;
+  p.out = a->out;
+  p.status = gdn::status_word();
+  if (p.status == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
+  return launch_result(gdn::launch_packed_decode(p, static_cast<cudaStream_t>(stream)),
+                       "gdn_packed_decode");
+}
+
 int gdn_decode(const gdn_decode_args* a, void* stream) {
   if (a == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "args is NULL");
   if (int rc = check_recurrence(a->B, a->Hk, a->Hv, a->Dk, a->Dv, a->act_dtype, a->q, a->q_len,

@@ -86,6 +86,32 @@ cudaError_t launch_kda(const RecurLaunch& p, cudaStream_t s);
 cudaError_t launch_spec_decode(const RecurLaunch& p, cudaStream_t s);
 bool recurrent_supported(int Dk);
 
+// Decode in one launch from the packed projections: conv update, SiLU, q/k
+// norm, gates and the recurrence (one token per row b; the conv pool and the
+// state pool share the slot sidx[b]).
+struct PackedDecodeLaunch {
+  int B, Hk, Hv, Dk, Dv, K;
+  bool bf16, norm;
+  float scale;
+  const void* x;  // raw (pre-conv) rows: q, k, v channels first
+  int64_t x_stride;
+  const float* w;
+  const void* a;
+  int64_t a_stride;
+  const void* b;
+  int64_t b_stride;
+  const float* A_log;
+  const float* dt_bias;
+  const int32_t* sidx;
+  float* conv_pool;  // [slots, C_conv, K-1]
+  float* pool;       // [slots, Hv, Dv, Dk]
+  int64_t slots;
+  void* out;
+  unsigned* status;
+};
+bool packed_decode_supported(int Dk, int Dv, int K);
+cudaError_t launch_packed_decode(const PackedDecodeLaunch& p, cudaStream_t s);
+
 // Chunked (C = 64) tensor-core prefill.
 struct ChunkedLaunch {
   RecurLaunch r;

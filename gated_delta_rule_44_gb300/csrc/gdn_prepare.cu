@@ -25,6 +25,7 @@
 #include <cuda_runtime.h>
 
 #include "gdn_internal.h"
+#include "gdn_math.cuh"
 
 namespace gdn {
 namespace {
@@ -32,38 +33,9 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 
-__device__ __forceinline__ float sigmoid_f(float x) {
-  if (x >= 0.0f) {
-    const float z = expf(-x);
-    return 1.0f / (1.0f + z);
-  }
-  const float z = expf(x);
-  return z / (1.0f + z);
-}
-
-__device__ __forceinline__ float softplus_f(float x) {
-  if (x > 20.0f) return x;
-  if (x < -20.0f) return expf(x);
-  return log1pf(expf(x));
-}
-
-// 1 / y: the hardware's approximate reciprocal refined by one Newton-Raphson
-// step, r <- r + r (1 - y r), which roughly doubles its correct bits (to
-// within about one ulp of the correctly rounded value).  A lone approximate
-// reciprocal is biased enough to shift bf16 roundings of whole tensors the
-// same way.  For finite y >= 1.
-__device__ __forceinline__ float recip_nr(float y) {
-  float r;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
-  return fmaf(r, fmaf(-y, r, 1.0f), r);
-}
-
-// silu(x) = x / (1 + e^{-x}).  e^{-x} is capped at e^80 (the result is then
-// below 1e-32 in magnitude either way) so that the reciprocal's operand stays
-// finite.
-__device__ __forceinline__ float silu_f(float x) {
-  return x * recip_nr(1.0f + __expf(fminf(-x, 80.0f)));
-}
+using math::sigmoid_f;
+using math::silu_f;
+using math::softplus_f;
 
 template <typename TA>
 struct Act;

@@ -252,6 +252,72 @@ int gdn_prefill_varlen(const gdn_prefill_args* args, void* stream);
 int gdn_prefill_varlen_noalloc(const gdn_prefill_args* args, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * gdn_packed_decode -- [cpu_ops.cpp] GdnPackedDecodeKernel with the conv
+ * update of [cpu_ops.cpp] CausalConv1dUpdateKernel folded in: a decode step in
+ * one launch from the packed projections.  The packed layouts of [cpu.rs]
+ * linear_attention_prepare_varlen_packed_qkvz_ba_f32 are described with row
+ * strides: mixed_qkv rows may carry z after the q, k, v channels
+ * (mixed_qkv_stride = C_conv + Hv*Dv), and a merged gate row of b then a
+ * gives b_raw = ba, a_raw = ba + Hv, both with stride 2*Hv.
+ *
+ * For each row b with slot s = state_indices[b] (the conv pool and the state
+ * pool share the slot, as their slot counts must match), per conv channel c:
+ *   y[c] = silu( sum_{j<K-1} conv_state[s,c,j] w[c,j] + x[b,c] w[c,K-1] )
+ * and conv_state[s,c,:] becomes (conv_state[s,c,1:], x[b,c]).  q, k, v split
+ * y as gdn_prepare does; q and k are L2-normalised (apply_qk_l2norm) in f32;
+ * per value head g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b);
+ * then the gated delta rule of gdn_decode on state[s] and out = S (scale q).
+ * No intermediate is rounded to act_dtype: only out is stored in it, so the
+ * result equals gdn_prepare followed by gdn_decode up to the bf16 rounding of
+ * q, k, v that those two calls store.  state_indices[b] = -1 marks a padding
+ * row (zero outputs, neither pool touched): a fixed-size batch padded this
+ * way can be captured once in a CUDA graph and replayed with new metadata.
+ *   - Layout: out [B, Hv, Dv] act_dtype; conv_state [state_slots, C_conv,
+ *     K-1] f32; state [state_slots, Hv, Dv, Dk] f32 (16-byte aligned);
+ *     conv_weight [C_conv, K] f32; A_log, dt_bias [Hv] f32.
+ *   - Errors: GDN_ERR_SHAPE for non-positive sizes, Hv % Hk != 0, short
+ *     buffers or strides; GDN_ERR_INVALID_ARGUMENT for NULL pointers, a
+ *     misaligned state or failed host-mirror index checks (-1 the only
+ *     negative, live slots distinct and in range); GDN_ERR_UNSUPPORTED
+ *     outside Dk in {64, 128}, Dv <= 128, K in [2, 4].  Without the host
+ *     mirror a bad slot raises the device status word and the row is padded.
+ *   - One CTA of 256 threads per (row, key head): it owns the conv channels
+ *     of its key head and of that head's value heads.
+ * ------------------------------------------------------------------------- */
+typedef struct gdn_packed_decode_args {
+  int64_t B, Hk, Hv, Dk, Dv, K;  /* rows, heads, dims, conv width */
+  int32_t act_dtype;             /* gdn_dtype of mixed_qkv, a_raw, b_raw, out */
+  int32_t apply_qk_l2norm;
+  float scale;                   /* < 0: 1/sqrt(Dk) */
+  const void* mixed_qkv;         /* [B, mixed_qkv_stride] raw (pre-conv) rows */
+  int64_t mixed_qkv_stride;      /* 0 = C_conv */
+  int64_t mixed_qkv_len;
+  const float* conv_weight;      /* [C_conv, K] */
+  int64_t conv_weight_len;
+  const void* a_raw;             /* [B, a_raw_stride] */
+  int64_t a_raw_stride;          /* 0 = Hv */
+  int64_t a_raw_len;
+  const void* b_raw;             /* [B, b_raw_stride] */
+  int64_t b_raw_stride;          /* 0 = Hv */
+  int64_t b_raw_len;
+  const float* A_log;            /* [Hv] */
+  int64_t A_log_len;
+  const float* dt_bias;          /* [Hv] */
+  int64_t dt_bias_len;
+  const int32_t* state_indices;  /* [B], device, required */
+  const int32_t* state_indices_host;  /* optional host mirror */
+  float* conv_state;             /* [state_slots, C_conv, K-1], updated in place */
+  int64_t conv_state_len;
+  float* state;                  /* [state_slots, Hv, Dv, Dk], updated in place */
+  int64_t state_slots;
+  int64_t state_len;
+  void* out;                     /* [B, Hv, Dv] */
+  int64_t out_len;
+} gdn_packed_decode_args;
+
+int gdn_packed_decode(const gdn_packed_decode_args* args, void* stream);
+
+/* ---------------------------------------------------------------------------
  * gdn_kda_varlen -- [cpu_ops.cpp] KdaHeadTokenStep / KdaGatedDeltaRuleKernel:
  * the gated delta rule with one log decay per KEY CHANNEL (KDA).
  *

@@ -354,3 +354,41 @@ def test_spec_prepare_rejections():
     assert rc == B.GDN_ERR_INVALID_ARGUMENT and "named by two requests" in msg
     rc, msg = call_spec_prepare(spec_prepare_args(state_indices_host=_host(0, 4)))
     assert rc == B.GDN_ERR_INVALID_ARGUMENT and msg == "spec GDN state slot out of range"
+
+
+def packed_args(Bn=4, Hk=1, Hv=2, Dk=64, Dv=64, K=4, **over):
+    C = 2 * Hk * Dk + Hv * Dv
+    a = dict(B=Bn, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, K=K, act_dtype=B.GDN_DTYPE_BF16,
+             apply_qk_l2norm=1, scale=-1.0, mixed_qkv=FAKE, mixed_qkv_stride=0,
+             mixed_qkv_len=Bn * C, conv_weight=FAKE, conv_weight_len=C * K, a_raw=FAKE,
+             a_raw_stride=0, a_raw_len=Bn * Hv, b_raw=FAKE, b_raw_stride=0, b_raw_len=Bn * Hv,
+             A_log=FAKE, A_log_len=Hv, dt_bias=FAKE, dt_bias_len=Hv, state_indices=FAKE,
+             state_indices_host=None, conv_state=FAKE, conv_state_len=8 * C * (K - 1),
+             state=FAKE, state_slots=8, state_len=8 * Hv * Dv * Dk, out=FAKE,
+             out_len=Bn * Hv * Dv)
+    a.update(over)
+    return B.gdn_packed_decode_args(**a)
+
+
+def call_packed(args):
+    L = B.lib()
+    rc = L.gdn_packed_decode(ctypes.byref(args), None)
+    return rc, L.gdn_last_error_message().decode()
+
+
+def test_packed_decode_rejections():
+    assert call_packed(packed_args(Bn=0))[0] == B.GDN_ERR_SHAPE
+    assert call_packed(packed_args(Hk=2, Hv=3))[0] == B.GDN_ERR_SHAPE   # Hv % Hk != 0
+    rc, msg = call_packed(packed_args(conv_state_len=5))
+    assert rc == B.GDN_ERR_SHAPE and msg.startswith("packed_gdn_decode conv_state length 5")
+    rc, msg = call_packed(packed_args(mixed_qkv_stride=100))
+    assert rc == B.GDN_ERR_SHAPE and "row stride shorter" in msg
+    assert call_packed(packed_args(state_indices=None))[0] == B.GDN_ERR_INVALID_ARGUMENT
+    assert call_packed(packed_args(state=FAKE + 4))[0] == B.GDN_ERR_INVALID_ARGUMENT
+    rc, msg = call_packed(packed_args(Dk=32, mixed_qkv_len=10**6, conv_weight_len=10**6,
+                                      conv_state_len=10**7, state_len=10**8))
+    assert rc == B.GDN_ERR_UNSUPPORTED and "Dk in {64, 128}" in msg
+    assert call_packed(packed_args(K=5, conv_weight_len=10**6,
+                                   conv_state_len=10**7))[0] == B.GDN_ERR_UNSUPPORTED
+    rc, msg = call_packed(packed_args(state_indices_host=_host(0, 1, 1, -1)))
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT and msg == "duplicate live GDN state index"
