@@ -228,9 +228,9 @@ def kernel_report(w, kernel_ms, peaks):
 
 # DRAM bytes (read + write) per library call, measured with ncu on a GB300
 # (dram__bytes_read.sum + dram__bytes_write.sum summed over the call's launches),
-# keyed by (call, workload), with the sha256 of the kernel source they were
-# measured on: once that source changes the figure no longer applies and the
-# line reports null.  mixed_hv64's prefill call is too large to capture under
+# keyed by (call, workload), with the sha256 of the kernel sources they were
+# measured on (concatenated in the order listed): once a source changes the
+# figure no longer applies and the line reports null.  mixed_hv64's prefill call is too large to capture under
 # ncu's replay, so its figure is prefill_4k's scaled by the token-heads processed
 # (x4; the workspace and operand traffic grow in proportion to them).
 MEASURED_TRAFFIC = {
@@ -253,12 +253,15 @@ def measured_traffic(call, workload):
     ent = MEASURED_TRAFFIC.get((call, workload))
     if ent is None:
         return None, "not captured"
-    nbytes, src, sha, how = ent
-    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "gated_delta_rule_44_gb300",
-                        "csrc", src)
-    with open(path, "rb") as fh:
-        if hashlib.sha256(fh.read()).hexdigest() != sha:
-            return None, f"{src} changed since the capture"
+    nbytes, srcs, sha, how = ent
+    h = hashlib.sha256()
+    for src in srcs:
+        path = os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                            "gated_delta_rule_44_gb300", "csrc", src)
+        with open(path, "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest() != sha:
+        return None, f"{' + '.join(srcs)} changed since the capture"
     return int(nbytes), how
 
 
