@@ -234,13 +234,13 @@ def kernel_report(w, kernel_ms, peaks):
 # ncu's replay, so its figure is prefill_4k's scaled by the token-heads processed
 # (x4; the workspace and operand traffic grow in proportion to them).
 MEASURED_TRAFFIC = {
-    ("prefill", "prefill_4k"): (336.6e6, "gdn_chunked.cu",
+    ("prefill", "prefill_4k"): (336.6e6, ("gdn_chunked.cu",),
                                 "b23b482a461b6295f59ccdde4aecbf2d60083a21e05f3d00931e1d35d8da1e23",
                                 "chunk_prep + chunk_scan of one call"),
-    ("prefill", "mixed_hv64"): (1346.4e6, "gdn_chunked.cu",
+    ("prefill", "mixed_hv64"): (1346.4e6, ("gdn_chunked.cu",),
                                 "b23b482a461b6295f59ccdde4aecbf2d60083a21e05f3d00931e1d35d8da1e23",
                                 "prefill_4k's call x 4 (token-heads)"),
-    ("decode", "decode_b256"): (1020.5e6, "gdn_recurrent.cu",
+    ("decode", "decode_b256"): (1020.5e6, ("gdn_recurrent.cu",),
                                 "272397006c3693aba64f42eeb21334046018f4b9d79527884faff6bfadd2b454",
                                 "one decode launch"),
 }
