@@ -234,15 +234,18 @@ def kernel_report(w, kernel_ms, peaks):
 # ncu's replay, so its figure is prefill_4k's scaled by the token-heads processed
 # (x4; the workspace and operand traffic grow in proportion to them).
 MEASURED_TRAFFIC = {
-    ("prefill", "prefill_4k"): (336.6e6, ("gdn_chunked.cu",),
-                                "b23b482a461b6295f59ccdde4aecbf2d60083a21e05f3d00931e1d35d8da1e23",
+    ("prefill", "prefill_4k"): (334.9e6, ("gdn_chunked.cu",),
+                                "f69b0fb7ef5d301362e9150d0b4840fd73b27cfc97ddb54b1766056768a045d6",
                                 "chunk_prep + chunk_scan of one call"),
-    ("prefill", "mixed_hv64"): (1346.4e6, ("gdn_chunked.cu",),
-                                "b23b482a461b6295f59ccdde4aecbf2d60083a21e05f3d00931e1d35d8da1e23",
+    ("prefill", "mixed_hv64"): (1339.7e6, ("gdn_chunked.cu",),
+                                "f69b0fb7ef5d301362e9150d0b4840fd73b27cfc97ddb54b1766056768a045d6",
                                 "prefill_4k's call x 4 (token-heads)"),
-    ("decode", "decode_b256"): (1020.5e6, ("gdn_recurrent.cu",),
-                                "272397006c3693aba64f42eeb21334046018f4b9d79527884faff6bfadd2b454",
+    ("decode", "decode_b256"): (1020.5e6, ("gdn_recurrent.cu", "gdn_rowstep.cuh"),
+                                "9d528dd5e8bb4395260e1fe9f6eae7d145f3766d373a1b1f37434df7f7f4bf2b",
                                 "one decode launch"),
+    ("decode", "mixed_hv64"): (4082.0e6, ("gdn_recurrent.cu", "gdn_rowstep.cuh"),
+                               "9d528dd5e8bb4395260e1fe9f6eae7d145f3766d373a1b1f37434df7f7f4bf2b",
+                               "decode_b256's launch x 4 (row-heads)"),
 }
 
 
