@@ -612,6 +612,24 @@ def rank_info():
     return ws, rank, local
 
 
+def slowest_rank_ms(ms, dist, device):
+    """The step time of the slowest rank, on every rank (ms itself at N = 1).
+    Each rank runs its own replica of the workload, so the whole job's step
+    takes as long as its slowest replica."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(tokens_per_rank, ws, ms):
+    """Tokens per second of all ranks together (weak scaling: every rank
+    processes tokens_per_rank tokens per step)."""
+    return tokens_per_rank * ws / (ms * 1e-3)
+
+
 def main_reference(args):
     ws, rank, _ = rank_info()
     if rank != 0:
@@ -663,12 +681,8 @@ def main():
     bus = getattr(props, "pci_bus_id", None)
     clocks = ClockSampler(bus) if rank == 0 else None
     res = time_workload(w, dev, args.steps, max(args.warmup, 3), args.algo, dist, clocks)
-    ms = res["ms_per_step"]
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = w.T * ws / (ms * 1e-3)
+    ms = slowest_rank_ms(res["ms_per_step"], dist, dev)
+    value = whole_job_value(w.T, ws, ms)
     dom, roof, kernels = roofline_entry(w, res["kernel_ms"], peaks)
     line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 4),
