@@ -420,6 +420,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
       }
       sgam[2 * lane + 1] = x;
       sgam[2 * lane] = x - b;
+      sg[2 * lane] = __expf(a);  // e^{g_j}: the step between neighbouring decays
+      sg[2 * lane + 1] = __expf(b);
     }
     __syncthreads();
     if (tid < 64) {
@@ -444,14 +446,29 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] = 0.0f;
       }
-      const float gi = sgam[i];
+      // Decays e^{gam_i - gam_j} (j <= i) along the row, leftward from the
+      // block's last column: e^{gam_i - gam_j} = e^{gam_i - gam_{j+1}} e^{g_{j+1}},
+      // one exponential per row and block instead of one per entry.  0 right
+      // of the diagonal, 1 on it.
+      float dec[32];
+      if (!upper) {
+        const int jr = hf * 32 + 31;
+        float cur = jr <= i ? __expf(sgam[i] - sgam[jr]) : 0.0f;
+        dec[31] = cur;
+#pragma unroll
+        for (int e = 30; e >= 0; --e) {
+          const int j = hf * 32 + e;
+          cur = j == i ? 1.0f : cur * sg[j + 1];
+          dec[e] = cur;
+        }
+      }
       if (quad < 2) {
         const float fi = sb[i] * skn[i];
         if (!upper) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int j = hf * 32 + e;
-            v[e] = j < i ? fi * skn[j] * __expf(gi - sgam[j]) * v[e] : 0.0f;
+            v[e] = j < i ? fi * skn[j] * dec[e] * v[e] : 0.0f;
           }
         }
 #pragma unroll
@@ -464,7 +481,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int j = hf * 32 + e;
-            v[e] = j <= i ? fi * skn[j] * __expf(gi - sgam[j]) * v[e] : 0.0f;
+            v[e] = fi * skn[j] * dec[e] * v[e];  // dec is 0 right of the diagonal
           }
         }
 #pragma unroll
