@@ -138,6 +138,9 @@ __device__ __forceinline__ void ld_bf16x8(const void* p, float* v) {
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
 }
+__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
 // Named barrier that also ANDs a predicate over the participating threads.
 __device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred) {
   uint32_t r;
@@ -254,6 +257,7 @@ struct PrepSmem {
   static constexpr uint32_t BYTES = GB + 7 * 64 * 4;
 };
 constexpr int kPrepThreads = 256;
+constexpr int kBarP = 1;  // chunk_prep: warp 0 and the 4 P warps -- the P image space is free
 
 // Shared memory rounded up to the 1024-byte alignment of swizzled tiles; the
 // pointer keeps the shared address space, so accesses compile to shared ones.
@@ -407,8 +411,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
       sg[tid] = g_next;
       sb[tid] = b_next;
     }
-    // The previous head's Ut store has read the image space the P images use.
-    if (tid == 0) bulk_wait_read();
     __syncthreads();
     if (warp == 0) {  // inclusive scan of g over the chunk (2 tokens per lane)
       const float a = sg[2 * lane], b = sg[2 * lane + 1];
@@ -435,6 +437,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
     {
       // Lanes 0..63 hold K K^T -> A (f32, shared); lanes 64..127 hold Q K^T -> P
       // (hi + lo images, staged in the Tw image space).  Row i, columns 32 hf ...
+      // The previous head's Ut store must have read the image space the P
+      // images use: warp 0 waits for it and releases the P warps, which block
+      // only right before their stores.
+      if (warp == 0) {
+        if (lane == 0) bulk_wait_read();
+        __syncwarp();
+        named_bar_arrive(kBarP, 5 * 32);
+      }
       // Rows 0..31 x columns 32..63 lie above the diagonal: all zero.
       const int i = (quad & 1) * 32 + lane;
       const bool upper = (quad & 1) == 0 && hf == 1;  // uniform across the warp
@@ -484,6 +494,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
             v[e] = fi * skn[j] * dec[e] * v[e];  // dec is 0 right of the diagonal
           }
         }
+        named_bar(kBarP, 5 * 32);
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
           const uint32_t off = swz128_offset(i, hf * 32 + e, 8192);
