@@ -509,14 +509,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
       bulk_commit();
     }
     if (tid < 64 && jh + 1 < G) load_gates(h + 1);  // consumed at the next head's start
-    // T = (I + A)^-1, A strictly lower triangular, by 32 x 32 blocks:
-    // (1) T11, T22 by forward substitution, warp b for block b, lane = column c:
-    //     x_i = [i == c] - sum_{m < i} A[32b+i][32b+m] x_m.
+    // T = (I + A)^-1, A strictly lower triangular, by blocks:
+    // (1) the four 16 x 16 diagonal blocks by forward substitution, two per
+    //     warp of warps 0..1 (lanes 0..15 and 16..31), lane = column c:
+    //     x_i = [i == c] - sum_{m < i} A[16b+i][16b+m] x_m;
+    // (1b) the 32 x 32 diagonal blocks from them: lower-left 16 x 16 block
+    //     X = -D1 (A10 D0) of each, D0 and D1 its two inverted diagonal blocks;
+    // (2), (3) below: the 64 x 64 inverse from the two 32 x 32 ones.
     if (warp < 2) {
-      const int b0 = 32 * warp, c = lane;
-      float x[32];
+      const int b0 = 16 * (2 * warp + (lane >> 4)), c = lane & 15;
+      float x[16];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < 16; ++i) {
         const float* arow = sA + (b0 + i) * S_ + b0;
         float a0 = i == c ? 1.0f : 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
 #pragma unroll
@@ -531,7 +535,35 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
       }
       __syncwarp();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) sA[(b0 + i) * S_ + b0 + c] = x[i];
+      for (int i = 0; i < 16; ++i) sA[(b0 + i) * S_ + b0 + c] = x[i];
+    }
+    __syncthreads();
+    {  // (1b) Z = A10 D0 into sY rows 16 B .. 16 B + 15: thread -> block B, row r, 2 columns
+      const int B = tid >> 7, r = (tid >> 3) & 15, c0 = (tid & 7) * 2;
+      const float* arow = sA + (32 * B + 16 + r) * S_ + 32 * B;
+      float z0 = 0.0f, z1 = 0.0f;
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        const float a = arow[m];
+        const float2 d = *reinterpret_cast<const float2*>(sA + (32 * B + m) * S_ + 32 * B + c0);
+        z0 = fmaf(a, d.x, z0);
+        z1 = fmaf(a, d.y, z1);
+      }
+      *reinterpret_cast<float2*>(sY + (16 * B + r) * SY + c0) = make_float2(z0, z1);
+    }
+    __syncthreads();
+    {  // X = -D1 Z into the lower-left 16 x 16 block of each 32 x 32 diagonal block
+      const int B = tid >> 7, r = (tid >> 3) & 15, c0 = (tid & 7) * 2;
+      const float* drow = sA + (32 * B + 16 + r) * S_ + 32 * B + 16;
+      float x0 = 0.0f, x1 = 0.0f;
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        const float d = drow[m];
+        const float2 z = *reinterpret_cast<const float2*>(sY + (16 * B + m) * SY + c0);
+        x0 = fmaf(d, z.x, x0);
+        x1 = fmaf(d, z.y, x1);
+      }
+      *reinterpret_cast<float2*>(sA + (32 * B + 16 + r) * S_ + 32 * B + c0) = make_float2(-x0, -x1);
     }
     __syncthreads();
     // (2) Y = A21 T11, (3) T21 = -T22 Y: thread -> row i, columns j0 .. j0 + 3.
