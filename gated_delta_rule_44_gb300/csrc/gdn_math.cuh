@@ -37,6 +37,16 @@ __device__ __forceinline__ float recip_nr(float y) {
   return fmaf(r, fmaf(-y, r, 1.0f), r);
 }
 
+// e^x as 2^{x log2(e)} on the hardware's approximate base-2 exponential
+// (flush-to-zero form: results below 2^-126 read 0).  About two ulp; used
+// where an exponential is evaluated per state column.
+__device__ __forceinline__ float exp_ex2(float x) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * kLog2e));
+  return y;
+}
+
 // silu(x) = x / (1 + e^{-x}).  e^{-x} is capped at e^80 (the result is then
 // below 1e-32 in magnitude either way) so that the reciprocal's operand stays
 // finite.

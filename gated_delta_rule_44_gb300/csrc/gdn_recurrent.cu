@@ -37,6 +37,7 @@
 #include <cuda_runtime.h>
 
 #include "gdn_internal.h"
+#include "gdn_math.cuh"
 #include "gdn_rowstep.cuh"
 
 namespace gdn {
@@ -110,7 +111,8 @@ __device__ __forceinline__ float row_step_kda(float4 (&s)[4], const float4 (&e)[
 }
 
 __device__ __forceinline__ float4 exp4(const float4& g) {
-  return make_float4(expf(g.x), expf(g.y), expf(g.z), expf(g.w));
+  return make_float4(math::exp_ex2(g.x), math::exp_ex2(g.y), math::exp_ex2(g.z),
+                     math::exp_ex2(g.w));
 }
 __device__ __forceinline__ float4 mul4(const float4& a, const float4& b) {
   return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w);
