@@ -119,8 +119,9 @@ __device__ __forceinline__ float4 mul4(const float4& a, const float4& b) {
 }
 
 // ---------------------------------------------------------------------------
-// Decode: grid.x = B * Hv * slices.
-template <typename TA, int DK, int PASSES>
+// Decode: grid.x = B * Hv * slices.  KDA: the one-token sequences of a KDA
+// call (T == N), with the per-key-channel decay and has_initial_state.
+template <typename TA, int DK, int PASSES, bool KDA>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const RecurLaunch p, int slices) {
   constexpr int LPR = DK / 16;
   constexpr int RPP = kThreads / LPR;  // rows per pass
@@ -132,6 +133,12 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const RecurLaunch p, i
   const int row0 = slice * (RPP * PASSES) + rg;
   TA* out = static_cast<TA*>(p.out) + ((int64_t)b * p.Hv + h) * p.Dv;
 
+  if constexpr (KDA) {  // row b must be sequence b
+    if (__ldg(p.cu + b) != b || __ldg(p.cu + b + 1) != b + 1) {
+      if (tid == 0) atomicOr(p.status, kStatusBadSeqlens);
+      return;
+    }
+  }
   int slot = p.sidx != nullptr ? __ldg(p.sidx + b) : b;
   if (slot < -1 || slot >= p.slots) {
     if (tid == 0) atomicOr(p.status, kStatusBadIndex);
@@ -148,6 +155,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const RecurLaunch p, i
   const int hk = h / (p.Hv / p.Hk);
   float* S = p.pool + ((int64_t)slot * p.Hv + h) * p.Dv * DK;
 
+  const bool init = !KDA || p.has_init == nullptr || __ldg(p.has_init + b) != 0;
   // Issue every state load of the slice first (memory-level parallelism).
   float4 st[PASSES][4];
 #pragma unroll
@@ -155,24 +163,40 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const RecurLaunch p, i
     const int r = row0 + ps * RPP;
 #pragma unroll
     for (int m = 0; m < 4; ++m)
-      st[ps][m] = r < p.Dv ? __ldcs(reinterpret_cast<const float4*>(S + (int64_t)r * DK + 4 * lr +
-                                                                      4 * LPR * m))
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
+      st[ps][m] = (init && r < p.Dv) ? __ldcs(reinterpret_cast<const float4*>(
+                                           S + (int64_t)r * DK + 4 * lr + 4 * LPR * m))
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   QK<TA, DK> qk;
   const TA* kp = static_cast<const TA*>(p.k) + ((int64_t)b * p.Hk + hk) * DK;
   const TA* qp = static_cast<const TA*>(p.q) + ((int64_t)b * p.Hk + hk) * DK;
   qk.load(kp, qp, lr);
   qk.finish(p.norm);
-  const float decay = expf(__ldg(p.g + (int64_t)b * p.Hv + h));
   const float beta = __ldg(p.beta + (int64_t)b * p.Hv + h);
   const TA* vp = static_cast<const TA*>(p.v) + ((int64_t)b * p.Hv + h) * p.Dv;
+  float decay = 0.0f;
+  float4 e[KDA ? 4 : 1], ek[KDA ? 4 : 1], eq[KDA ? 4 : 1];
+  if constexpr (KDA) {  // this lane's 16 columns of e^{g[b, h, :]}
+    const float* gr = p.g + ((int64_t)b * p.Hv + h) * DK;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      e[m] = exp4(__ldg(reinterpret_cast<const float4*>(gr + 4 * lr + 4 * LPR * m)));
+      ek[m] = mul4(e[m], qk.k[m]);
+      eq[m] = mul4(e[m], qk.q[m]);
+    }
+  } else {
+    decay = expf(__ldg(p.g + (int64_t)b * p.Hv + h));
+  }
 
 #pragma unroll
   for (int ps = 0; ps < PASSES; ++ps) {
     const int r = row0 + ps * RPP;
     const float vv = r < p.Dv ? ld_act<TA>(vp + r) : 0.0f;
-    const float o = row_step<LPR>(st[ps], qk.k, qk.q, qk.kq, decay, beta, vv);
+    float o;
+    if constexpr (KDA)
+      o = row_step_kda<LPR>(st[ps], e, ek, eq, qk.k, qk.kq, beta, vv);
+    else
+      o = row_step<LPR>(st[ps], qk.k, qk.q, qk.kq, decay, beta, vv);
     if (r < p.Dv) {
 #pragma unroll
       for (int m = 0; m < 4; ++m)
@@ -358,18 +382,22 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurLaunch p
   }
 }
 
-enum class Mode { kDecode, kRecurrent, kKda, kSpec };
+enum class Mode { kDecode, kRecurrent, kKda, kKdaDecode, kSpec };
 
 template <typename TA, int DK, int PASSES>
 cudaError_t launch_dk(const RecurLaunch& p, cudaStream_t s, Mode mode) {
   constexpr int rows_per_cta = (kThreads / (DK / 16)) * PASSES;
   const int slices = (p.Dv + rows_per_cta - 1) / rows_per_cta;
-  const int64_t blocks = (int64_t)(mode == Mode::kDecode ? p.T : p.N) * p.Hv * slices;
+  const bool per_row = mode == Mode::kDecode || mode == Mode::kKdaDecode;
+  const int64_t blocks = (int64_t)(per_row ? p.T : p.N) * p.Hv * slices;
   if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
   const unsigned grid = (unsigned)blocks;
   switch (mode) {
     case Mode::kDecode:
-      decode_kernel<TA, DK, PASSES><<<grid, kThreads, 0, s>>>(p, slices);
+      decode_kernel<TA, DK, PASSES, false><<<grid, kThreads, 0, s>>>(p, slices);
+      break;
+    case Mode::kKdaDecode:
+      decode_kernel<TA, DK, PASSES, true><<<grid, kThreads, 0, s>>>(p, slices);
       break;
     case Mode::kRecurrent:
       recurrent_kernel<TA, DK, PASSES, false, false><<<grid, kThreads, 0, s>>>(p, slices);
@@ -419,7 +447,9 @@ cudaError_t launch_recurrent(const RecurLaunch& p, cudaStream_t s) {
 
 cudaError_t launch_kda(const RecurLaunch& p, cudaStream_t s) {
   if (p.norm) return cudaErrorInvalidValue;
-  return launch_mode(p, s, Mode::kKda);
+  // T == N: every sequence holds exactly one token (cu_seqlens must be 0..N,
+  // which the decode form checks on the device), so run the decode form.
+  return launch_mode(p, s, p.T == p.N ? Mode::kKdaDecode : Mode::kKda);
 }
 
 cudaError_t launch_spec_decode(const RecurLaunch& p, cudaStream_t s) {

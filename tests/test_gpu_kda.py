@@ -62,3 +62,11 @@ def test_kda_padding_and_fresh_states(cuda_device):
 
 def test_kda_long_sequence(cuda_device):
     run([1000], 4, 8, 128, 128, torch.bfloat16, cuda_device, seed=5)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_kda_decode_form_padding_and_fresh_states(dtype, cuda_device):
+    # T == N runs the decode form: padding rows and has_initial_state = 0 there
+    run([1] * 9, 2, 4, 128, 96, dtype, cuda_device, seed=6,
+        sidx=torch.tensor([3, -1, 0, 8, 5, -1, 1, 2, 7], dtype=torch.int32),
+        has_init=[1, 1, 0, 1, 0, 1, 1, 1, 0], slots=10)
