@@ -17,8 +17,9 @@
 // shared memory, with the two norms and the ratio gates.  Phase 2 streams the
 // value heads' state rows through registers, one head at a time, with the
 // row update of the recurrent kernels (LPR = Dk/16 lanes per row, 256/LPR rows
-// per pass), and writes out = scale * o.  Nothing is rounded to the
-// activation type between the steps; only out is stored in it.
+// per pass), and writes out = scale * o.  The first head's rows are requested
+// before phase 1.  Nothing is rounded to the activation type between the
+// steps; only out is stored in it.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -60,6 +61,24 @@ __global__ void __launch_bounds__(kThreads) packed_decode_kernel(const PackedDec
     for (int e = tid; e < ratio * p.Dv; e += kThreads) st_act<TA>(out + e, 0.0f);
     return;
   }
+
+  // The first value head's state rows are requested before phase 1, so their
+  // latency overlaps the conv; later heads load at the top of their turn.
+  const int lr = tid % LPR, rg = tid / LPR;
+  float4 st[PASSES][4];
+  auto load_state = [&](int hh) {
+    const float* S = p.pool + ((int64_t)slot * p.Hv + h0 + hh) * p.Dv * DK;
+#pragma unroll
+    for (int ps = 0; ps < PASSES; ++ps) {
+      const int r = rg + ps * RPP;
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        st[ps][m] = r < p.Dv ? __ldcs(reinterpret_cast<const float4*>(S + (int64_t)r * DK + 4 * lr +
+                                                                        4 * LPR * m))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  load_state(0);
 
   // ---- phase 1: conv update of this CTA's channels, gates, norms -----------
   const int qk_total = p.Hk * DK;
@@ -105,7 +124,6 @@ __global__ void __launch_bounds__(kThreads) packed_decode_kernel(const PackedDec
   __syncthreads();
 
   // ---- phase 2: the value heads' rows ---------------------------------------
-  const int lr = tid % LPR, rg = tid / LPR;
   float4 q4[4], k4[4];
   {
     const float qi = inv_s[0], ki = inv_s[1];
@@ -125,16 +143,7 @@ __global__ void __launch_bounds__(kThreads) packed_decode_kernel(const PackedDec
 #pragma unroll 1
   for (int hh = 0; hh < ratio; ++hh) {
     float* S = p.pool + ((int64_t)slot * p.Hv + h0 + hh) * p.Dv * DK;
-    float4 st[PASSES][4];
-#pragma unroll
-    for (int ps = 0; ps < PASSES; ++ps) {
-      const int r = rg + ps * RPP;
-#pragma unroll
-      for (int m = 0; m < 4; ++m)
-        st[ps][m] = r < p.Dv ? __ldcs(reinterpret_cast<const float4*>(S + (int64_t)r * DK + 4 * lr +
-                                                                        4 * LPR * m))
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    if (hh > 0) load_state(hh);
     const float decay = decay_s[hh], beta = beta_s[hh];
     const float* v = y + 2 * DK + hh * p.Dv;
 #pragma unroll
