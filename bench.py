@@ -234,17 +234,17 @@ def kernel_report(w, kernel_ms, peaks):
 # ncu's replay, so its figure is prefill_4k's scaled by the token-heads processed
 # (x4; the workspace and operand traffic grow in proportion to them).
 MEASURED_TRAFFIC = {
-    ("prefill", "prefill_4k"): (334.9e6, ("gdn_chunked.cu",),
-                                "f69b0fb7ef5d301362e9150d0b4840fd73b27cfc97ddb54b1766056768a045d6",
+    ("prefill", "prefill_4k"): (334.6e6, ("gdn_chunked.cu",),
+                                "88d3a3e3bfad0885889fbce61c4d7fe02a9484fed34307f12f7a610d4853d718",
                                 "chunk_prep + chunk_scan of one call"),
-    ("prefill", "mixed_hv64"): (1339.7e6, ("gdn_chunked.cu",),
-                                "f69b0fb7ef5d301362e9150d0b4840fd73b27cfc97ddb54b1766056768a045d6",
+    ("prefill", "mixed_hv64"): (1338.4e6, ("gdn_chunked.cu",),
+                                "88d3a3e3bfad0885889fbce61c4d7fe02a9484fed34307f12f7a610d4853d718",
                                 "prefill_4k's call x 4 (token-heads)"),
-    ("decode", "decode_b256"): (1020.5e6, ("gdn_recurrent.cu", "gdn_rowstep.cuh"),
-                                "9d528dd5e8bb4395260e1fe9f6eae7d145f3766d373a1b1f37434df7f7f4bf2b",
+    ("decode", "decode_b256"): (1020.7e6, ("gdn_recurrent.cu", "gdn_rowstep.cuh", "gdn_math.cuh"),
+                                "de3417cacc701511f2613d0e4e3e1b0d51cd70dc165eb1d25a1d078ea99af60b",
                                 "one decode launch"),
-    ("decode", "mixed_hv64"): (4082.0e6, ("gdn_recurrent.cu", "gdn_rowstep.cuh"),
-                               "9d528dd5e8bb4395260e1fe9f6eae7d145f3766d373a1b1f37434df7f7f4bf2b",
+    ("decode", "mixed_hv64"): (4082.9e6, ("gdn_recurrent.cu", "gdn_rowstep.cuh", "gdn_math.cuh"),
+                               "de3417cacc701511f2613d0e4e3e1b0d51cd70dc165eb1d25a1d078ea99af60b",
                                "decode_b256's launch x 4 (row-heads)"),
 }
 
