@@ -9,6 +9,15 @@
  *   gdn_decode          the state recurrence for one token per sequence
  *   gdn_prefill_varlen  the state recurrence over packed variable-length
  *                       sequences (chunked, tensor-core form)
+ * and these variants of them:
+ *   gdn_packed_decode   prepare + decode of one token per row in one launch,
+ *                       from the packed projections
+ *   gdn_prefill_varlen_noalloc   gdn_prefill_varlen on a scratch array inside
+ *                       the library's device image
+ *   gdn_spec_prepare,   the prepare and the recurrence of a speculative
+ *   gdn_spec_decode     multi-token decode step (per-draft state snapshots)
+ *   gdn_kda_varlen      the recurrence with one decay per key channel (KDA)
+ *   gdn_gated_rmsnorm   the gated RMSNorm applied to the recurrence output
  *
  * Sources (page title, then the function that defines the operation):
  *   [cpu.rs]       ferrum-kernels 0.8.0, src/ferrum_kernels/backend/cpu.rs
