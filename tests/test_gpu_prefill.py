@@ -88,6 +88,8 @@ SMALL = [
     ([129, 128, 3, 200], 2, 2, 128, 128, torch.bfloat16, None, False, False),
     ([300, 5], 2, 4, 64, 64, torch.bfloat16, None, False, True),
     ([40, 9, 17], 2, 6, 16, 24, torch.float32, [1], False, True),
+    # eight value heads per key head: chunk_prep's loop over a key head's heads
+    ([100, 37, 64, 1], 1, 8, 128, 128, torch.bfloat16, [1], False, True),
 ]
 
 
