@@ -303,8 +303,11 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurLaunch p
   }
   b_cur = __ldg(p.beta + (int64_t)t0 * p.Hv + h);
 
+  // A speculative request has a few tokens only: it loads each token's
+  // operands after the previous token instead of keeping a second set in
+  // registers, which leaves room for a fourth CTA per SM.
   for (int t = t0; t < t1; ++t) {
-    if (t + 1 < t1) {
+    if (!SPEC && t + 1 < t1) {
       nxt.load(kbase + (int64_t)(t + 1) * qk_row, qbase + (int64_t)(t + 1) * qk_row, lr);
 #pragma unroll
       for (int ps = 0; ps < PASSES; ++ps) {
@@ -364,10 +367,23 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurLaunch p
         }
       }
     }
-    cur = nxt;
+    if constexpr (SPEC) {
+      if (t + 1 < t1) {
+        cur.load(kbase + (int64_t)(t + 1) * qk_row, qbase + (int64_t)(t + 1) * qk_row, lr);
 #pragma unroll
-    for (int ps = 0; ps < PASSES; ++ps) v_cur[ps] = v_nxt[ps];
-    b_cur = b_nxt;
+        for (int ps = 0; ps < PASSES; ++ps) {
+          const int r = row0 + ps * RPP;
+          v_cur[ps] = r < p.Dv ? ld_act<TA>(vbase + (int64_t)(t + 1) * v_row + r) : 0.f;
+        }
+        g_cur = __ldg(p.g + (int64_t)(t + 1) * p.Hv + h);
+        b_cur = __ldg(p.beta + (int64_t)(t + 1) * p.Hv + h);
+      }
+    } else {
+      cur = nxt;
+#pragma unroll
+      for (int ps = 0; ps < PASSES; ++ps) v_cur[ps] = v_nxt[ps];
+      b_cur = b_nxt;
+    }
   }
 
   if constexpr (!SPEC) {
