@@ -240,11 +240,11 @@ MEASURED_TRAFFIC = {
     ("prefill", "mixed_hv64"): (1338.4e6, ("gdn_chunked.cu",),
                                 "88d3a3e3bfad0885889fbce61c4d7fe02a9484fed34307f12f7a610d4853d718",
                                 "prefill_4k's call x 4 (token-heads)"),
-    ("decode", "decode_b256"): (1020.7e6, ("gdn_recurrent.cu", "gdn_rowstep.cuh", "gdn_math.cuh"),
-                                "de3417cacc701511f2613d0e4e3e1b0d51cd70dc165eb1d25a1d078ea99af60b",
+    ("decode", "decode_b256"): (1020.6e6, ("gdn_recurrent.cu", "gdn_rowstep.cuh", "gdn_math.cuh"),
+                                "3262d5358409cb7d1def5b51c482c5605b906b9de47fcf817c61b9bcc7218b0a",
                                 "one decode launch"),
-    ("decode", "mixed_hv64"): (4082.9e6, ("gdn_recurrent.cu", "gdn_rowstep.cuh", "gdn_math.cuh"),
-                               "de3417cacc701511f2613d0e4e3e1b0d51cd70dc165eb1d25a1d078ea99af60b",
+    ("decode", "mixed_hv64"): (4082.6e6, ("gdn_recurrent.cu", "gdn_rowstep.cuh", "gdn_math.cuh"),
+                               "3262d5358409cb7d1def5b51c482c5605b906b9de47fcf817c61b9bcc7218b0a",
                                "decode_b256's launch x 4 (row-heads)"),
 }
 
