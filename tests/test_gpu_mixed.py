@@ -109,3 +109,38 @@ def test_host_pipeline_matches_sequential_steps(cuda_device):
         assert torch.equal(r.cpu(), ho)
     assert torch.equal(d1["state_pool"], d2["state_pool"])
     assert torch.equal(d1["conv_pool"], d2["conv_pool"])
+
+
+def test_mixed_step_cuda_graph_replay(cuda_device):
+    """A whole mixed step (prepare, decode, chunked prefill) captured once in
+    a CUDA graph and replayed gives bit-identical outputs, state and conv pools
+    to the same steps run eagerly: the host validation, the status-word lookup
+    and the prefill's tensor maps are all settled before the capture."""
+    dev = cuda_device
+    w = W.make_workload("graph", 403, [1] * 6 + [100, 64, 3], 2, 4, 128, 128, slots=14,
+                        n_decode=6, prefill_new=False, state_std=0.3)
+    eager, graphed = H.to_dev(w, dev), H.to_dev(w, dev)
+    step_e = layer.GdnStep(w.T, w.N, w.n_decode, w.Hk, w.Hv, w.Dk, w.Dv, w.K, w.act_dtype, dev)
+    step_g = layer.GdnStep(w.T, w.N, w.n_decode, w.Hk, w.Hv, w.Dk, w.Dv, w.K, w.act_dtype, dev)
+
+    def run(step, d, stream=None):
+        return step.run(d["mixed_qkv"], d["a_raw"], d["b_raw"], d["conv_weight"], d["A_log"],
+                        d["dt_bias"], d["cu_seqlens"], d["state_indices"],
+                        d["has_initial_state"], d["state_pool"], d["conv_pool"],
+                        d["cu_seqlens_prefill"], stream=stream)
+
+    # a throw-away eager step on copies settles every lazy host-side resource
+    warm = H.to_dev(w, dev)
+    run(step_g, warm)
+    torch.cuda.synchronize()
+    del warm
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run(step_g, graphed, stream=torch.cuda.current_stream())
+    for _ in range(2):
+        run(step_e, eager)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(step_e.out, step_g.out)
+        assert torch.equal(eager["state_pool"], graphed["state_pool"])
+        assert torch.equal(eager["conv_pool"], graphed["conv_pool"])
