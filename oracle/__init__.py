@@ -149,6 +149,9 @@ def _declare(L):
     L.orc_gdn_chunked_f64.restype = ctypes.c_int
     L.orc_gdn_chunked_f64.argtypes = ([_vp] * 6 + [_i64, _vp, _vp, _vp] + [_i64] * 6
                                       + [ctypes.c_double, ctypes.c_int, _i64, _vp])
+    L.orc_kda_chunked_f64.restype = ctypes.c_int
+    L.orc_kda_chunked_f64.argtypes = ([_vp] * 6 + [_i64, _vp, _vp, _vp] + [_i64] * 6
+                                      + [ctypes.c_double, _i64, _vp])
     L.orc_validate_gated_delta_rule_shape.restype = ctypes.c_int
     L.orc_validate_gated_delta_rule_shape.argtypes = [_i64] * 13 + [ctypes.c_char_p,
                                                                     ctypes.c_size_t]
@@ -444,6 +447,24 @@ def gdn_chunked_f64(q, k, v, g, beta, state_pool, cu_seqlens, scale, chunk,
         _ptr(hi), _ptr(cu), cu.size - 1, T, Hk, Hv, Dk, Dv, float(scale), int(use_qk_l2norm),
         int(chunk), _ptr(out))
     _check(rc, "gdn_chunked_f64")
+    return out
+
+
+def kda_chunked_f64(q, k, v, g, beta, state_pool, cu_seqlens, scale, chunk,
+                    state_indices=None, has_initial_state=None):
+    """O9 (f64 only): the chunked form of the KDA recurrence; same contract as
+    kda_varlen (g [T, Hv, Dk])."""
+    q, k, v, g, beta, T, Hk, Dk, Hv, Dv = _recur_inputs(q, k, v, g, beta, np.float64)
+    pool = _inplace(state_pool, np.float64, "state_pool")
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    si = None if state_indices is None else np.ascontiguousarray(state_indices, dtype=np.int32)
+    hi = None if has_initial_state is None else np.ascontiguousarray(has_initial_state,
+                                                                     dtype=np.uint8)
+    out = np.zeros((T, Hv, Dv), np.float64)
+    rc = _load().orc_kda_chunked_f64(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(pool), pool.shape[0], _ptr(si),
+        _ptr(hi), _ptr(cu), cu.size - 1, T, Hk, Hv, Dk, Dv, float(scale), int(chunk), _ptr(out))
+    _check(rc, "kda_chunked_f64")
     return out
 
 

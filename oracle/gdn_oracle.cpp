@@ -555,6 +555,86 @@ void chunk_step(const std::vector<double>& Kc, const std::vector<double>& Qc,
     }
 }
 
+// ---- O9: chunked form of the KDA recurrence (f64) -----------------------------
+// Derived from [cpu_ops.cpp] KdaHeadTokenStep as O4 is from the scalar-decay
+// recurrence, with a log decay per key channel d.  For a chunk of L tokens with
+// state S0 [Dv,Dk] and gam_i[d] = sum_{t<=i} g_t[d]:
+//   A_ij  = beta_i sum_d k_i[d] k_j[d] exp(gam_i[d] - gam_j[d])      j < i
+//   T     = (I + A)^-1
+//   W_i   = sum_{j<=i} T_ij beta_j (k_j o exp(gam_j)),  Ut_i = sum_{j<=i} T_ij beta_j v_j
+//   U     = Ut - W S0^T
+//   O_i   = (q_i o exp(gam_i)) S0^T + sum_{j<=i} (sum_d q_i[d] k_j[d] exp(gam_i[d] - gam_j[d])) U_j
+//   S_L[:, d] = exp(gam_L[d]) S0[:, d] + sum_j U_j k_j[d] exp(gam_L[d] - gam_j[d])
+// with q already scaled.  Every exponent is <= 0: each pair's decay is taken
+// as its own difference, never as a product of a growing and a shrinking
+// factor.
+void kda_chunk_step(const std::vector<double>& Kc, const std::vector<double>& Qc,
+                    const std::vector<double>& Vc, const std::vector<double>& Gc,
+                    const std::vector<double>& bc, int64_t L, int64_t dk, int64_t dv,
+                    double* S, std::vector<double>& Oc) {
+  std::vector<double> gam(L * dk);
+  for (int64_t d = 0; d < dk; ++d) {
+    double run = 0.0;
+    for (int64_t i = 0; i < L; ++i) {
+      run += Gc[i * dk + d];
+      gam[i * dk + d] = run;
+    }
+  }
+  // sum_d X_i[d] Y_j[d] exp(gam_i[d] - gam_j[d])
+  auto ddot = [&](const std::vector<double>& X, int64_t i, const std::vector<double>& Y,
+                  int64_t j) {
+    double s = 0.0;
+    for (int64_t d = 0; d < dk; ++d)
+      s += X[i * dk + d] * Y[j * dk + d] * std::exp(gam[i * dk + d] - gam[j * dk + d]);
+    return s;
+  };
+  std::vector<double> A(L * L, 0.0);
+  for (int64_t i = 0; i < L; ++i)
+    for (int64_t j = 0; j < i; ++j) A[i * L + j] = bc[i] * ddot(Kc, i, Kc, j);
+  std::vector<double> T(L * L, 0.0);
+  for (int64_t col = 0; col < L; ++col)
+    for (int64_t i = 0; i < L; ++i) {
+      double s = (i == col) ? 1.0 : 0.0;
+      for (int64_t m = 0; m < i; ++m) s -= A[i * L + m] * T[m * L + col];
+      T[i * L + col] = s;
+    }
+  std::vector<double> W(L * dk, 0.0), U(L * dv, 0.0);
+  for (int64_t i = 0; i < L; ++i)
+    for (int64_t j = 0; j <= i; ++j) {
+      const double t = T[i * L + j] * bc[j];
+      for (int64_t d = 0; d < dk; ++d)
+        W[i * dk + d] += t * Kc[j * dk + d] * std::exp(gam[j * dk + d]);
+      for (int64_t d = 0; d < dv; ++d) U[i * dv + d] += t * Vc[j * dv + d];
+    }
+  for (int64_t i = 0; i < L; ++i)  // U = Ut - W S0^T
+    for (int64_t e = 0; e < dv; ++e) {
+      double s = 0.0;
+      for (int64_t d = 0; d < dk; ++d) s += W[i * dk + d] * S[e * dk + d];
+      U[i * dv + e] -= s;
+    }
+  Oc.assign(L * dv, 0.0);
+  for (int64_t i = 0; i < L; ++i) {
+    for (int64_t e = 0; e < dv; ++e) {
+      double s = 0.0;
+      for (int64_t d = 0; d < dk; ++d)
+        s += Qc[i * dk + d] * std::exp(gam[i * dk + d]) * S[e * dk + d];
+      Oc[i * dv + e] = s;
+    }
+    for (int64_t j = 0; j <= i; ++j) {
+      const double pij = ddot(Qc, i, Kc, j);
+      for (int64_t e = 0; e < dv; ++e) Oc[i * dv + e] += pij * U[j * dv + e];
+    }
+  }
+  const double* gl = &gam[(L - 1) * dk];
+  for (int64_t e = 0; e < dv; ++e)
+    for (int64_t d = 0; d < dk; ++d) {
+      double s = std::exp(gl[d]) * S[e * dk + d];
+      for (int64_t j = 0; j < L; ++j)
+        s += U[j * dv + e] * Kc[j * dk + d] * std::exp(gl[d] - gam[j * dk + d]);
+      S[e * dk + d] = s;
+    }
+}
+
 // Gated RMSNorm of the recurrence output, [cpu.rs] gated_rms_norm_f32 (SiLU
 // gate) with [cpu_ops.cpp] RmsNormGatedKernel's options: a sigmoid gate and a
 // gate tensor [T, H, D] whose token rows are z_stride elements apart.  Per
@@ -915,6 +995,50 @@ int orc_gdn_chunked_f64(const double* q, const double* k, const double* v, const
           bc[i] = beta[t * hv_n + h];
         }
         chunk_step(Kc, Qc, Vc, gc, bc, L, dk, dv, S, Oc);
+        for (int64_t i = 0; i < L; ++i)
+          for (int64_t d = 0; d < dv; ++d) out[((c0 + i) * hv_n + h) * dv + d] = Oc[i * dv + d];
+      }
+    }
+  return ORC_OK;
+}
+
+int orc_kda_chunked_f64(const double* q, const double* k, const double* v, const double* g,
+                        const double* beta, double* pool, int64_t slots, const int32_t* sidx,
+                        const uint8_t* has_init, const int32_t* cu, int64_t n_seqs,
+                        int64_t tokens, int64_t hk_n, int64_t hv_n, int64_t dk, int64_t dv,
+                        double scale, int64_t chunk, double* out) {
+  if (n_seqs <= 0 || tokens <= 0 || hk_n <= 0 || hv_n <= 0 || dk <= 0 || dv <= 0 || chunk <= 0)
+    return ORC_ERR_SHAPE;
+  if (hv_n % hk_n != 0) return ORC_ERR_SHAPE;
+  if (int rc = check_cu(cu, n_seqs, tokens, nullptr, 0)) return rc;
+  if (int rc = check_slots(sidx, n_seqs, slots, nullptr, 0)) return rc;
+  const int64_t ratio = hv_n / hk_n;
+  for (int64_t s = 0; s < n_seqs; ++s)
+    for (int64_t h = 0; h < hv_n; ++h) {
+      const int64_t slot = sidx != nullptr ? sidx[s] : s;
+      if (slot < 0) {
+        for (int64_t t = cu[s]; t < cu[s + 1]; ++t)
+          for (int64_t d = 0; d < dv; ++d) out[(t * hv_n + h) * dv + d] = 0.0;
+        continue;
+      }
+      double* S = pool + (slot * hv_n + h) * dv * dk;
+      if (has_init != nullptr && has_init[s] == 0)
+        for (int64_t e = 0; e < dv * dk; ++e) S[e] = 0.0;
+      const int64_t hk = h / ratio;
+      for (int64_t c0 = cu[s]; c0 < cu[s + 1]; c0 += chunk) {
+        const int64_t L = std::min<int64_t>(chunk, cu[s + 1] - c0);
+        std::vector<double> Kc(L * dk), Qc(L * dk), Vc(L * dv), Gc(L * dk), bc(L), Oc;
+        for (int64_t i = 0; i < L; ++i) {
+          const int64_t t = c0 + i;
+          for (int64_t d = 0; d < dk; ++d) {
+            Kc[i * dk + d] = k[(t * hk_n + hk) * dk + d];
+            Qc[i * dk + d] = q[(t * hk_n + hk) * dk + d] * scale;
+            Gc[i * dk + d] = g[(t * hv_n + h) * dk + d];
+          }
+          for (int64_t d = 0; d < dv; ++d) Vc[i * dv + d] = v[(t * hv_n + h) * dv + d];
+          bc[i] = beta[t * hv_n + h];
+        }
+        kda_chunk_step(Kc, Qc, Vc, Gc, bc, L, dk, dv, S, Oc);
         for (int64_t i = 0; i < L; ++i)
           for (int64_t d = 0; d < dv; ++d) out[((c0 + i) * hv_n + h) * dv + d] = Oc[i * dv + d];
       }

@@ -202,6 +202,17 @@ int orc_gdn_chunked_f64(const double* query, const double* key, const double* va
                         int64_t key_dim, int64_t value_dim, double scale, int use_qk_l2norm,
                         int64_t chunk, double* out);
 
+/* ---- O9: chunked form of the KDA recurrence, f64 only (self-check) -------
+ * Same contract as orc_kda_varlen_f64 (g [T, Hv, Dk], q and k used as
+ * given); chunk = tokens per chunk (>= 1). */
+int orc_kda_chunked_f64(const double* query, const double* key, const double* value,
+                        const double* g, const double* beta, double* state_pool,
+                        int64_t state_slots, const int32_t* state_indices,
+                        const uint8_t* has_initial_state, const int32_t* cu_seqlens,
+                        int64_t n_seqs, int64_t tokens, int64_t key_heads, int64_t value_heads,
+                        int64_t key_dim, int64_t value_dim, double scale, int64_t chunk,
+                        double* out);
+
 /* ---- O5 gated RMSNorm of the recurrence output ----------------------------
  * [cpu.rs] gated_rms_norm_f32 / validate_gated_rms_norm_shape, with
  * [cpu_ops.cpp] RmsNormGatedKernel's sigmoid-gate option and strided gate.

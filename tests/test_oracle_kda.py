@@ -12,7 +12,11 @@ Each pin checks a fact that does not re-type the recurrence:
     decay travels with it);
   * a channel whose decay is e^{-inf} forgets its column: after it, the state's
     column is that token's rank-1 update alone;
-  * the f32 instantiation tracks f64.
+  * the f32 instantiation tracks f64;
+  * the chunked form (O9) equals the token-by-token recurrence for any chunk
+    length, with ragged tails, padding, fresh states and decays down to
+    e^{-30} per token and channel; with one decay for every channel it is the
+    GDN chunked form (O4, itself pinned).
 """
 import numpy as np
 import pytest
@@ -97,3 +101,32 @@ def test_f32_tracks_f64():
     a = oracle.kda_varlen(q, k, v, g, beta, p1, cu, 0.2, state_indices=sidx, dtype=np.float64)
     b = oracle.kda_varlen(q, k, v, g, beta, p2, cu, 0.2, state_indices=sidx, dtype=np.float32)
     assert np.abs(a - b).max() / np.sqrt((a ** 2).mean()) < 1e-5
+
+
+@pytest.mark.parametrize("chunk", [1, 7, 16, 64])
+@pytest.mark.parametrize("strong", [False, True])
+def test_chunked_form_equals_recurrence(chunk, strong):
+    q, k, v, g, beta, pool, cu, sidx = _inputs(7 + chunk, seqs=(5, 1, 70, 33))
+    sidx = np.array([3, -1, 0, 4], np.int32)
+    has_init = np.array([1, 1, 0, 1], np.uint8)
+    if strong:
+        g = -np.random.default_rng(11).uniform(0.0, 30.0, size=g.shape)
+    p1, p2 = pool.copy(), pool.copy()
+    a = oracle.kda_varlen(q, k, v, g, beta, p1, cu, 0.3, state_indices=sidx,
+                          has_initial_state=has_init, dtype=np.float64)
+    b = oracle.kda_chunked_f64(q, k, v, g, beta, p2, cu, 0.3, chunk, state_indices=sidx,
+                               has_initial_state=has_init)
+    scale_o = np.sqrt((a ** 2).mean())
+    assert np.abs(a - b).max() <= 1e-10 * scale_o
+    assert np.abs(p1 - p2).max() <= 1e-10 * np.sqrt((p1 ** 2).mean())
+
+
+def test_chunked_form_with_uniform_decay_is_gdn_chunked():
+    q, k, v, g, beta, pool, cu, sidx = _inputs(9, seqs=(40, 3))
+    g_head = g[:, :, 0]
+    g_uniform = np.repeat(g_head[:, :, None], g.shape[2], axis=2)
+    p1, p2 = pool.copy(), pool.copy()
+    a = oracle.kda_chunked_f64(q, k, v, g_uniform, beta, p1, cu, 0.25, 16, state_indices=sidx)
+    b = oracle.gdn_chunked_f64(q, k, v, g_head, beta, p2, cu, 0.25, 16, state_indices=sidx)
+    np.testing.assert_allclose(a, b, rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(p1, p2, rtol=1e-11, atol=1e-13)

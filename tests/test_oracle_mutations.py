@@ -10,8 +10,8 @@ dropped factor in the chunked form, a gated norm over the sum instead of the
 mean, swapped gates or unstrided gate rows, a KDA decay taken from one channel
 or applied after the dot, a speculative decode that starts from the wrong
 column, stores each snapshot one column late or loses the state at a -1 column, a
-speculative conv window read one tap late or a conv row shifted by the
-request length instead of one tap.
+speculative conv window read one tap late, a conv row shifted by the
+request length instead of one tap, a chunked KDA form without its decay in W.
 """
 import os
 
@@ -108,6 +108,10 @@ MUTATIONS = [
      "for (int64_t j = 0; j < keep; ++j) next[j] = old_at(off + 1 + j);",
      "for (int64_t j = 0; j < keep; ++j) next[j] = old_at(off + len + j);",
      [lambda: SP.test_outputs_are_the_convolution_of_the_accepted_history(4)]),
+    ("kda_chunked_drops_decay_in_W",
+     "W[i * dk + d] += t * Kc[j * dk + d] * std::exp(gam[j * dk + d]);",
+     "W[i * dk + d] += t * Kc[j * dk + d];",
+     [lambda: KD.test_chunked_form_equals_recurrence(16, False)]),
     ("chunked_drops_decay_in_W",
      "const double tw = T[i * L + j] * bc[j] * std::exp(gam[j]);",
      "const double tw = T[i * L + j] * bc[j];",
