@@ -17,7 +17,7 @@ and head with no exchange), so scaling is weak and the value counts the tokens
 of all ranks over the slowest rank's time.
 
 --impl reference times the CPU oracle (the plain C++ restatement of the
-pages' CPU code) on a bounded sample of the same workload.
+pages' CPU code) over whole steps of the same workload on the host cores.
 """
 from __future__ import annotations
 
@@ -553,58 +553,58 @@ def time_e2e(w, dev, steps, warmup, algo):
 
 # ---- CPU oracle baseline -----------------------------------------------------------
 
-def oracle_sample(w, heads_sampled, nthreads):
-    """Time the oracle (prepare over every token + recurrence over every
-    sequence for `heads_sampled` of the Hv value heads) and extrapolate the
-    recurrence linearly in heads.  Returns (tokens/s, seconds spent, sample)."""
+def oracle_step(w, nthreads, state_pool, conv_pool):
+    """One whole step of the workload on the oracle, timed: the prepare over
+    every token, then the recurrence over every sequence (decode rows are
+    one-token sequences) and every value head, each parallel over its items on
+    `nthreads` host threads.  The pools are updated in place, as the GPU step
+    does.  Returns seconds."""
     import numpy as np
     import oracle
-    T = w.T
     f32 = lambda t: t.float().numpy()
-    pool = w.conv_pool.numpy().copy()
     t0 = time.perf_counter()
-    prep = oracle.prepare_varlen(f32(w.mixed_qkv), w.conv_weight.numpy(), pool, f32(w.a_raw),
+    prep = oracle.prepare_varlen(f32(w.mixed_qkv), w.conv_weight.numpy(), conv_pool, f32(w.a_raw),
                                  f32(w.b_raw), w.A_log.numpy(), w.dt_bias.numpy(),
                                  w.cu_seqlens.numpy(), w.Hk, w.Hv, w.Dk, w.Dv, w.K,
                                  state_indices=w.state_indices.numpy(),
                                  has_initial_state=w.has_initial_state.numpy(),
                                  dtype=np.float32, nthreads=nthreads)
-    t_prep = time.perf_counter() - t0
-    heads = list(range(heads_sampled))
-    seqs = list(range(w.N))
-    slots = [int(s) for s in w.state_indices.tolist()]
-    live = [i for i, s in enumerate(slots) if s >= 0]
-    cpool = np.stack([w.state_pool[slots[i]][: heads_sampled].numpy() for i in live]) \
-        if live else np.zeros((1, heads_sampled, w.Dv, w.Dk), np.float32)
-    # A pool holding only the sampled heads: present those heads as Hv' = heads_sampled.
-    remap = np.full(w.N, -1, np.int32)
-    for j, i in enumerate(live):
-        remap[i] = j
-    Hk_s = max(1, heads_sampled // (w.Hv // w.Hk))
-    t1 = time.perf_counter()
-    oracle.gdn_varlen(prep["q"][:, :Hk_s], prep["k"][:, :Hk_s], prep["v"][:, :heads_sampled],
-                      prep["g"][:, :heads_sampled], prep["beta"][:, :heads_sampled],
-                      np.ascontiguousarray(cpool), w.cu_seqlens.numpy(), 1.0 / np.sqrt(w.Dk),
-                      state_indices=remap, has_initial_state=w.has_initial_state.numpy(),
-                      dtype=np.float32, nthreads=nthreads)
-    t_rec = time.perf_counter() - t1
-    est = t_prep + t_rec * (w.Hv / heads_sampled)
-    sample = (f"oracle f32 prepare over all {T} tokens + recurrence over all {w.N} sequences "
-              f"for {heads_sampled} of {w.Hv} value heads (key heads {Hk_s}); step time "
-              f"extrapolated linearly in heads: {t_prep:.2f}s + {t_rec:.2f}s x "
-              f"{w.Hv / heads_sampled:g}")
-    return T / est, t_prep + t_rec, sample
+    oracle.gdn_varlen(prep["q"], prep["k"], prep["v"], prep["g"], prep["beta"], state_pool,
+                      w.cu_seqlens.numpy(), 1.0 / np.sqrt(w.Dk),
+                      state_indices=w.state_indices.numpy(),
+                      has_initial_state=w.has_initial_state.numpy(), dtype=np.float32,
+                      nthreads=nthreads)
+    return time.perf_counter() - t0
 
 
-def cpu_baseline(w, nthreads, budget_s=20.0):
-    heads = 1
-    tps, spent, sample = oracle_sample(w, heads, nthreads)
-    # grow the sample toward the budget (bounded: at most all heads)
-    while spent < budget_s / 3 and heads * 2 <= w.Hv:
-        heads *= 2
-        tps, spent, sample = oracle_sample(w, heads, nthreads)
-    return {"value": round(tps, 2), "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
-            "sample": sample, "seconds": round(spent, 2)}
+def oracle_pools(w):
+    """Private f32 copies of the workload's state and conv pools."""
+    import numpy as np
+    return (np.ascontiguousarray(w.state_pool.numpy(), dtype=np.float32).copy(),
+            np.ascontiguousarray(w.conv_pool.numpy(), dtype=np.float32).copy())
+
+
+def oracle_sample_text(w, nthreads, steps):
+    return (f"{steps} whole step(s) of the workload on the oracle (C++ f32, {nthreads} host "
+            f"threads, parallel over (sequence, value head)): prepare over all {w.T} tokens and "
+            f"the recurrence over all {w.N} sequences x {w.Hv} value heads; no extrapolation")
+
+
+def cpu_baseline(w, nthreads):
+    """The oracle as it stands, timed over one whole step of the workload."""
+    sp, cp = oracle_pools(w)
+    secs = oracle_step(w, nthreads, sp, cp)
+    return {"value": round(w.T / secs, 2), "unit": "tokens/s", "cores": nthreads,
+            "kind": "oracle", "sample": oracle_sample_text(w, nthreads, 1),
+            "seconds": round(secs, 2)}
+
+
+def workload_config(w, ws):
+    """The `config` object of the JSON line; both arms print this same dict."""
+    return {"workload": w.name, "tokens_per_step": w.T, "decodes": w.n_decode,
+            "prefill_seqlens": w.seqlens[w.n_decode:], "Hk": w.Hk, "Hv": w.Hv, "Dk": w.Dk,
+            "Dv": w.Dv, "conv_kernel": w.K, "state_slots": w.slots, "state_dtype": "f32",
+            "parallelism": f"replicas{ws}", "l2": "inputs larger than L2 (no flush)"}
 
 
 def rank_info():
@@ -633,6 +633,8 @@ def whole_job_value(tokens_per_rank, ws, ms):
 
 
 def main_reference(args):
+    """The oracle timed over W untimed then K timed whole steps of the same
+    workload on the host cores (rank 0 only)."""
     ws, rank, _ = rank_info()
     if rank != 0:
         return 0
@@ -641,20 +643,20 @@ def main_reference(args):
     oracle.build()
     w = W.named(args.workload)
     nthreads = os.cpu_count() or 1
-    vals = []
-    samp = ""
-    for i in range(args.warmup + args.steps):
-        tps, spent, samp = oracle_sample(w, 1, nthreads)
-        if i >= args.warmup:
-            vals.append(tps)
-    v = statistics.mean(vals)
+    sp, cp = oracle_pools(w)
+    for _ in range(args.warmup):
+        oracle_step(w, nthreads, sp, cp)
+    secs = [oracle_step(w, nthreads, sp, cp) for _ in range(args.steps)]
+    total = sum(secs)
+    v = w.T * args.steps / total
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 2), "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(w.T / v * 1e3, 3), "higher_is_better": True,
+            "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": args.workload, "tokens_per_step": w.T},
+            "config": workload_config(w, ws),
             "cpu_baseline": {"value": round(v, 2), "unit": "tokens/s", "cores": nthreads,
-                             "kind": "oracle", "sample": samp},
+                             "kind": "oracle",
+                             "sample": oracle_sample_text(w, nthreads, args.steps)},
             "e2e": {"value": round(v, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -690,12 +692,8 @@ def main():
             "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": args.workload, "tokens_per_step": w.T, "decodes": w.n_decode,
-                       "prefill_seqlens": w.seqlens[w.n_decode:], "Hk": w.Hk, "Hv": w.Hv,
-                       "Dk": w.Dk, "Dv": w.Dv, "conv_kernel": w.K, "state_slots": w.slots,
-                       "state_dtype": "f32", "parallelism": f"replicas{ws}",
-                       "l2": "inputs larger than L2 (no flush)",
-                       "prefill_algo": B.gdn_prefill_resolve_algo(w.Dk, w.Dv, 1, args.algo)},
+            "config": workload_config(w, ws),
+            "prefill_algo": B.gdn_prefill_resolve_algo(w.Dk, w.Dv, 1, args.algo),
             "roofline": roof, "kernels": kernels, "gpu_launches": res["launches"],
             "clocks": res["clocks"]}
     if rank == 0 and not args.no_extra:

@@ -123,11 +123,20 @@ class gdn_gated_rmsnorm_args(ctypes.Structure):
                 ("weight_len", _i64), ("out", _vp), ("out_len", _i64)]
 
 
+class gdn_mixed_meta(ctypes.Structure):
+    _fields_ = [("num_decodes", _i64), ("num_prefills", _i64), ("num_decode_tokens", _i64),
+                ("num_prefill_tokens", _i64), ("num_actual_tokens", _i64), ("state_slots", _i64),
+                ("allow_inert_padding", _i32), ("cu_seqlens_host", _vp),
+                ("state_indices_host", _vp), ("has_initial_state_host", _vp),
+                ("cu_seqlens_prefill_host", _vp), ("prefill_state_indices_host", _vp),
+                ("prefill_has_initial_state_host", _vp)]
+
+
 EXPORTED = ("gdn_prepare", "gdn_decode", "gdn_prefill_varlen", "gdn_kda_varlen",
             "gdn_spec_prepare", "gdn_spec_decode", "gdn_packed_decode", "gdn_gated_rmsnorm",
             "gdn_prefill_workspace_bytes",
             "gdn_prefill_resolve_algo", "gdn_status_string", "gdn_last_error_message",
-            "gdn_read_device_status", "gdn_version", "gdn_launch_count")
+            "gdn_read_device_status", "gdn_version", "gdn_launch_count", "gdn_validate_mixed")
 
 
 class GdnError(RuntimeError):
@@ -150,7 +159,7 @@ def lib() -> ctypes.CDLL:
             L = ctypes.CDLL(_build.build_library())
             for name in ("gdn_prepare", "gdn_decode", "gdn_prefill_varlen", "gdn_kda_varlen",
                          "gdn_spec_prepare", "gdn_spec_decode", "gdn_packed_decode", "gdn_gated_rmsnorm",
-                         "gdn_read_device_status", "gdn_version"):
+                         "gdn_read_device_status", "gdn_version", "gdn_validate_mixed"):
                 getattr(L, name).restype = ctypes.c_int
             L.gdn_prepare.argtypes = [ctypes.POINTER(gdn_prepare_args), _vp]
             L.gdn_decode.argtypes = [ctypes.POINTER(gdn_decode_args), _vp]
@@ -161,6 +170,7 @@ def lib() -> ctypes.CDLL:
             L.gdn_spec_prepare.argtypes = [ctypes.POINTER(gdn_spec_prepare_args), _vp]
             L.gdn_packed_decode.argtypes = [ctypes.POINTER(gdn_packed_decode_args), _vp]
             L.gdn_read_device_status.argtypes = [_vp]
+            L.gdn_validate_mixed.argtypes = [ctypes.POINTER(gdn_mixed_meta)]
             L.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
             L.gdn_prefill_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64, _i64, _i32, _i32]
             L.gdn_prefill_resolve_algo.restype = _i32
@@ -398,6 +408,47 @@ def gdn_prefill_varlen(q, k, v, g, beta, state, cu_seqlens, out, *, scale=-1.0,
         state_indices_host=sih_p, out=_p(out), out_len=_n(out), workspace=_p(workspace),
         workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size())
     _check(lib().gdn_prefill_varlen(ctypes.byref(a), _stream(stream)))
+
+
+def _host_u8(t: Optional[torch.Tensor]):
+    if t is None:
+        return None, None
+    h = t.detach().to("cpu", torch.uint8).contiguous()
+    return h, h.data_ptr()
+
+
+def gdn_validate_mixed(*, num_decodes, num_prefills, num_actual_tokens, state_slots,
+                       cu_seqlens_host, state_indices_host, cu_seqlens_prefill_host,
+                       has_initial_state_host=None, prefill_state_indices_host=None,
+                       prefill_has_initial_state_host=None, num_decode_tokens=None,
+                       num_prefill_tokens=None, allow_inert_padding=True) -> None:
+    """include/gdn.h gdn_validate_mixed on host copies of a mixed step's
+    metadata (tensors on any device; they are copied to the host).  Raises
+    GdnError on the first broken rule; launches nothing."""
+    nd_tok = num_decodes if num_decode_tokens is None else num_decode_tokens
+    np_tok = (num_actual_tokens - nd_tok) if num_prefill_tokens is None else num_prefill_tokens
+    cu, cu_p = _host_i32(cu_seqlens_host)
+    si, si_p = _host_i32(state_indices_host)
+    hi, hi_p = _host_u8(has_initial_state_host)
+    cp, cp_p = _host_i32(cu_seqlens_prefill_host)
+    ps, ps_p = _host_i32(prefill_state_indices_host)
+    ph, ph_p = _host_u8(prefill_has_initial_state_host)
+    nreq = num_decodes + num_prefills
+    for name, t, n in (("cu_seqlens", cu, nreq + 1), ("state_indices", si, nreq),
+                       ("has_initial_state", hi, nreq), ("cu_seqlens_prefill", cp, num_prefills + 1),
+                       ("prefill_state_indices", ps, num_prefills),
+                       ("prefill_has_initial_state", ph, num_prefills)):
+        if t is not None and t.numel() < n:
+            raise GdnError(GDN_ERR_SHAPE, "GDN_ERR_SHAPE",
+                           f"{name} holds {t.numel()} entries, the step needs {n}")
+    m = gdn_mixed_meta(num_decodes=num_decodes, num_prefills=num_prefills,
+                       num_decode_tokens=nd_tok, num_prefill_tokens=np_tok,
+                       num_actual_tokens=num_actual_tokens, state_slots=state_slots,
+                       allow_inert_padding=int(bool(allow_inert_padding)),
+                       cu_seqlens_host=cu_p, state_indices_host=si_p, has_initial_state_host=hi_p,
+                       cu_seqlens_prefill_host=cp_p, prefill_state_indices_host=ps_p,
+                       prefill_has_initial_state_host=ph_p)
+    _check(lib().gdn_validate_mixed(ctypes.byref(m)))
 
 
 def gdn_read_device_status(stream=None) -> None:

@@ -78,12 +78,15 @@ int check_recurrence_dims(int64_t tokens, int64_t hk, int64_t hv, int64_t dk, in
   return GDN_OK;
 }
 
-// [cpu.rs] recurrent_gated_delta_rule_varlen_f32 cu_seqlens rules.
+// [cpu.rs] recurrent_gated_delta_rule_varlen_f32 (and
+// linear_attention_prepare_varlen_f32) cu_seqlens rules.  The page prints
+// cu.first() / cu.last(), Rust Options, with {:?}: "Some(v)".
 int check_cu_host(const int32_t* cu, int64_t n, int64_t total, const char* who) {
   if (cu[0] != 0 || cu[n] != total)
     return fail(GDN_ERR_INVALID_ARGUMENT,
                 std::string(who) + " cu_seqlens must start at 0 and end at total_tokens " +
-                    S(total) + ", got first=" + S(cu[0]) + " last=" + S(cu[n]));
+                    S(total) + ", got first=Some(" + S(cu[0]) + ") last=Some(" + S(cu[n]) +
+                    ")");
   for (int64_t s = 0; s < n; ++s)
     if (cu[s + 1] <= cu[s])
       return fail(GDN_ERR_INVALID_ARGUMENT, std::string(who) + " sequence " + S(s) +
@@ -147,6 +150,12 @@ int check_spec_host(const int32_t* cu, const int32_t* sidx, const int32_t* nat, 
 }
 
 bool fits_i32(int64_t v) { return v >= 0 && v <= INT32_MAX; }
+
+}  // namespace
+
+int gdn::report_error(int code, const char* msg) { return fail(code, msg); }
+
+namespace {
 
 int launch_result(cudaError_t e, const char* what) {
   if (e != cudaSuccess)
@@ -653,6 +662,78 @@ int gdn_gated_rmsnorm(const gdn_gated_rmsnorm_args* a, void* stream) {
   p.out = a->out;
   return launch_result(gdn::launch_gated_rmsnorm(p, static_cast<cudaStream_t>(stream)),
                        "gdn_gated_rmsnorm");
+}
+
+// [qwen3_5.cpp] ValidateGdnAttentionMetadata, the non-speculative part, in
+// the page's order and with its messages (without the "qwen3_5: " prefix).
+// The causal-conv chunk metadata it also checks has no counterpart here: the
+// prepare kernel derives its tiles from cu_seqlens itself.
+int gdn_validate_mixed(const gdn_mixed_meta* m) {
+  if (m == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "meta is NULL");
+  const int64_t nd = m->num_decodes, np = m->num_prefills;
+  const int64_t nd_tok = m->num_decode_tokens, np_tok = m->num_prefill_tokens;
+  const int64_t nreq = nd + np;
+  if (nd < 0 || np < 0 || nd_tok < 0 || np_tok < 0 || m->num_actual_tokens < 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "negative GDN metadata count");
+  if (nd_tok != nd)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "non-spec decode requires one token per request");
+  if (m->num_actual_tokens != nd_tok + np_tok)
+    return fail(GDN_ERR_INVALID_ARGUMENT,
+                "GDN decode+prefill+spec tokens must equal actual tokens");
+  if (nreq == 0) {
+    if (m->num_actual_tokens != 0)
+      return fail(GDN_ERR_INVALID_ARGUMENT, "GDN tokens require state metadata");
+    return succeed();
+  }
+  if (m->state_indices_host == nullptr)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "missing non-spec GDN state indices");
+  if (m->state_slots < 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "GDN state cache has invalid slot count");
+  const int32_t* idx = m->state_indices_host;
+  if (int rc = check_indices_host(idx, nreq, m->state_slots)) return rc;
+  if (!m->allow_inert_padding)
+    for (int64_t i = 0; i < nreq; ++i)
+      if (idx[i] < 0)
+        return fail(GDN_ERR_INVALID_ARGUMENT, "live GDN state index must be non-negative");
+  if (np == 0) return succeed();
+  if (m->cu_seqlens_host == nullptr || m->cu_seqlens_prefill_host == nullptr)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "incomplete GDN prefill metadata");
+  const int32_t* qsl = m->cu_seqlens_host;
+  const int32_t* pqsl = m->cu_seqlens_prefill_host;
+  const int32_t* pidx = m->prefill_state_indices_host != nullptr
+                            ? m->prefill_state_indices_host
+                            : idx + nd;
+  const uint8_t* init = m->has_initial_state_host;
+  const uint8_t* pinit = m->prefill_has_initial_state_host != nullptr
+                             ? m->prefill_has_initial_state_host
+                             : (init != nullptr ? init + nd : nullptr);
+  if (qsl[0] != 0 || qsl[nreq] != nd_tok + np_tok)
+    return fail(GDN_ERR_INVALID_ARGUMENT,
+                "non-spec GDN query offsets must span the non-spec tokens");
+  for (int64_t i = 0; i < nreq; ++i)
+    if (qsl[i + 1] <= qsl[i])
+      return fail(GDN_ERR_INVALID_ARGUMENT,
+                  "non-spec GDN query offsets must be strictly increasing");
+  if (qsl[nd] != nd_tok)
+    return fail(GDN_ERR_INVALID_ARGUMENT,
+                "non-spec GDN decode prefix does not match token count");
+  for (int64_t i = 0; i < np; ++i) {
+    if (pidx[i] != idx[nd + i])
+      return fail(GDN_ERR_INVALID_ARGUMENT, "prefill state indices must match non-spec suffix");
+    if (pidx[i] < 0)
+      return fail(GDN_ERR_INVALID_ARGUMENT, "prefill GDN state index must be non-negative");
+    if (pqsl[i] != qsl[nd + i] - nd_tok)
+      return fail(GDN_ERR_INVALID_ARGUMENT,
+                  "prefill query offsets must match rebased non-spec suffix");
+    const uint8_t a = init != nullptr ? init[nd + i] : 1;
+    const uint8_t b = pinit != nullptr ? pinit[i] : 1;
+    if ((a != 0) != (b != 0))
+      return fail(GDN_ERR_INVALID_ARGUMENT,
+                  "prefill initial-state mask must match non-spec suffix");
+  }
+  if (pqsl[np] != np_tok)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "prefill query offsets must span prefill tokens");
+  return succeed();
 }
 
 int32_t gdn_prefill_resolve_algo(int64_t Dk, int64_t Dv, int32_t act_dtype, int32_t algo) {

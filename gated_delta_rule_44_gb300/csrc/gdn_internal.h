@@ -22,6 +22,10 @@ void note_launch();
 // nullptr if the symbol could not be resolved.
 unsigned* status_word();
 
+// Records `msg` as the calling thread's gdn_last_error_message() and returns
+// `code` (for sources outside the API translation unit).
+int report_error(int code, const char* msg);
+
 struct PrepareLaunch {
   int T, N, Hk, Hv, Dk, Dv, K;
   bool bf16, norm;

@@ -23,6 +23,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "gdn_internal.h"
 #include "gdn_math.cuh"
 #include "gdn_rowstep.cuh"
@@ -110,7 +112,12 @@ __global__ void __launch_bounds__(kThreads) packed_decode_kernel(const PackedDec
     const float bv = ld_act<TA>(static_cast<const TA*>(p.b) + (int64_t)b * p.b_stride + h);
     const float g = -expf(__ldg(p.A_log + h)) * math::softplus_f(av + __ldg(p.dt_bias + h));
     decay_s[tid] = expf(g);
-    beta_s[tid] = math::sigmoid_f(bv);
+    // [cpu_ops.cpp] GdnPackedDecodeKernel rounds beta through b's storage type
+    // (nearest even), as the unfused path stores it; f32 keeps it exact.
+    float beta = math::sigmoid_f(bv);
+    if constexpr (std::is_same<TA, __nv_bfloat16>::value)
+      beta = __bfloat162float(__float2bfloat16_rn(beta));
+    beta_s[tid] = beta;
   }
   __syncthreads();
   if (tid < 64) {  // warp 0: |q|^2, warp 1: |k|^2

@@ -33,7 +33,10 @@ unsigned* status_word() {
   std::lock_guard<std::mutex> lock(g_mu);
   if (g_addr[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) {
+      cudaGetLastError();  // clear the non-sticky error so a later call's check does not see it
+      return nullptr;
+    }
     g_addr[dev] = static_cast<unsigned*>(p);
   }
   return g_addr[dev];

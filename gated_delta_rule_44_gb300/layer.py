@@ -47,23 +47,59 @@ class GdnStep:
         ws = B.gdn_prefill_workspace_bytes(Tp, Np, Hv, Dk, Dv, dt, algo) if Np > 0 else 0
         self.workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev) if ws else None
 
+    def validate(self, cu_seqlens_host, state_indices_host, cu_seqlens_prefill_host,
+                 has_initial_state_host=None, state_slots=None) -> None:
+        """Checks host copies of the step's metadata against the mixed-step
+        contract ([qwen3_5.cpp] ValidateGdnAttentionMetadata, via the C ABI's
+        gdn_validate_mixed): decode rows first and single-token,
+        cu_seqlens[n_decode] == n_decode, the prefill cu_seqlens equal to the
+        suffix of cu_seqlens rebased to 0, the prefill indices the suffix of
+        state_indices.  Raises GdnError; launches nothing."""
+        nd = self.n_decode
+        if state_slots is None:
+            state_slots = (int(state_indices_host.max().item()) + 1
+                           if state_indices_host.numel() else 0)
+        B.gdn_validate_mixed(num_decodes=nd, num_prefills=self.N - nd,
+                             num_actual_tokens=self.T, state_slots=state_slots,
+                             cu_seqlens_host=cu_seqlens_host,
+                             state_indices_host=state_indices_host,
+                             has_initial_state_host=has_initial_state_host,
+                             cu_seqlens_prefill_host=(cu_seqlens_prefill_host
+                                                      if self.N > nd else None))
+
     def run(self, mixed_qkv, a_raw, b_raw, conv_weight, A_log, dt_bias, cu_seqlens, state_indices,
             has_initial_state, state_pool, conv_pool, cu_seqlens_prefill=None,
             stream: Optional[torch.cuda.Stream] = None,
-            out: Optional[torch.Tensor] = None) -> torch.Tensor:
+            out: Optional[torch.Tensor] = None, cu_seqlens_host=None, state_indices_host=None,
+            has_initial_state_host=None, cu_seqlens_prefill_host=None) -> torch.Tensor:
         """One step; writes the output to ``out`` (default: this object's own
-        buffer) and returns it."""
+        buffer) and returns it.  When host copies of the metadata are passed
+        (``*_host``), the step's metadata contract is checked before anything
+        is launched (see ``validate``) and the calls get the host mirrors for
+        their own index and cu_seqlens checks."""
         nd, ndt = self.n_decode, self.nd_tok
         out = self.out if out is None else out
+        if cu_seqlens_host is not None or state_indices_host is not None:
+            if cu_seqlens_host is None or state_indices_host is None or (
+                    self.N > nd and cu_seqlens_prefill_host is None):
+                raise B.GdnError(B.GDN_ERR_INVALID_ARGUMENT, "GDN_ERR_INVALID_ARGUMENT",
+                                 "incomplete GDN prefill metadata")
+            self.validate(cu_seqlens_host, state_indices_host, cu_seqlens_prefill_host,
+                          has_initial_state_host, state_slots=state_pool.shape[0])
+        host = cu_seqlens_host is not None
         B.gdn_prepare(mixed_qkv, conv_weight, a_raw, b_raw, A_log, dt_bias, cu_seqlens, conv_pool,
                       self.q, self.k, self.v, self.g, self.beta, Hk=self.Hk, Hv=self.Hv,
                       Dk=self.Dk, Dv=self.Dv, K=self.K, state_indices=state_indices,
                       has_initial_state=has_initial_state, apply_qk_l2norm=self.norm,
+                      cu_seqlens_host=cu_seqlens_host if host else None,
+                      state_indices_host=state_indices_host if host else None,
                       stream=stream)
         if nd > 0:
             B.gdn_decode(self.q[:ndt], self.k[:ndt], self.v[:ndt], self.g[:ndt],
                          self.beta[:ndt], state_pool, out[:ndt], scale=self.scale,
-                         state_indices=state_indices[:nd], stream=stream)
+                         state_indices=state_indices[:nd],
+                         state_indices_host=state_indices_host[:nd] if host else None,
+                         stream=stream)
         if self.N > nd:
             B.gdn_prefill_varlen(self.q[ndt:], self.k[ndt:], self.v[ndt:], self.g[ndt:],
                                  self.beta[ndt:], state_pool, cu_seqlens_prefill,
@@ -71,6 +107,8 @@ class GdnStep:
                                  state_indices=state_indices[nd:],
                                  has_initial_state=(None if has_initial_state is None
                                                     else has_initial_state[nd:]),
+                                 cu_seqlens_host=cu_seqlens_prefill_host if host else None,
+                                 state_indices_host=state_indices_host[nd:] if host else None,
                                  algo=self.algo, workspace=self.workspace, stream=stream)
         return out
 
@@ -140,11 +178,18 @@ def mixed_step(mixed_qkv, a_raw, b_raw, conv_weight, A_log, dt_bias, cu_seqlens,
                has_initial_state, state_pool, conv_pool, *, n_decode: int, Hk: int, Hv: int,
                Dk: int, Dv: int, K: int, cu_seqlens_prefill=None, scale: float = -1.0,
                algo: int = B.GDN_PREFILL_AUTO, stream=None) -> torch.Tensor:
-    """Allocating one-shot form of GdnStep.run; returns out [T, Hv, Dv]."""
+    """Allocating one-shot form of GdnStep.run; returns out [T, Hv, Dv].  It
+    copies the metadata to the host (a synchronisation) and checks the
+    mixed-step contract before launching anything."""
     T = mixed_qkv.shape[0]
     N = cu_seqlens.numel() - 1
     step = GdnStep(T, N, n_decode, Hk, Hv, Dk, Dv, K, mixed_qkv.dtype, mixed_qkv.device,
                    scale=scale, algo=algo)
+    host = {"cu_seqlens_host": cu_seqlens.cpu(), "state_indices_host": state_indices.cpu(),
+            "has_initial_state_host": (None if has_initial_state is None
+                                       else has_initial_state.cpu()),
+            "cu_seqlens_prefill_host": (None if cu_seqlens_prefill is None
+                                        else cu_seqlens_prefill.cpu())}
     return step.run(mixed_qkv, a_raw, b_raw, conv_weight, A_log, dt_bias, cu_seqlens,
                     state_indices, has_initial_state, state_pool, conv_pool,
-                    cu_seqlens_prefill=cu_seqlens_prefill, stream=stream).clone()
+                    cu_seqlens_prefill=cu_seqlens_prefill, stream=stream, **host).clone()

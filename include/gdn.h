@@ -18,6 +18,8 @@
  *   gdn_spec_decode     multi-token decode step (per-draft state snapshots)
  *   gdn_kda_varlen      the recurrence with one decay per key channel (KDA)
  *   gdn_gated_rmsnorm   the gated RMSNorm applied to the recurrence output
+ * and a host-only check of a mixed step's metadata:
+ *   gdn_validate_mixed  decode rows first, prefill cu_seqlens rebased
  *
  * Sources (page title, then the function that defines the operation):
  *   [cpu.rs]       ferrum-kernels 0.8.0, src/ferrum_kernels/backend/cpu.rs
@@ -251,10 +253,13 @@ int gdn_prefill_varlen(const gdn_prefill_args* args, void* stream);
  *   - Limit: sizes whose gdn_prefill_workspace_bytes() exceeds 64 MiB
  *     (67108864 bytes) are rejected with GDN_ERR_INVALID_ARGUMENT before
  *     anything is launched; sizes that need no scratch run as usual.
- *   - Every GPU that loads the library holds the 64 MiB until process exit.
- *   - The first call on each device (with that device current) looks up the
- *     array's device address once; make that first call before any stream
- *     capture.  A failed look-up returns GDN_ERR_CUDA.
+ *   - Every GPU that loads the array's module holds the 64 MiB until process
+ *     exit.  Under CUDA's default lazy module loading that memory is committed
+ *     by the first call on each device, which is therefore the set-up step
+ *     that can fail (e.g. when the device is out of memory): it returns
+ *     GDN_ERR_CUDA with the CUDA error in gdn_last_error_message().
+ *   - That first call on each device (with that device current) also looks up
+ *     the array's device address once; make it before any stream capture.
  *   - All calls share the one array, and it keeps the last call's contents
  *     (nothing in it needs to start at zero): calls whose GPU work overlaps
  *     (on different streams or from different host threads) race on it. */
@@ -519,6 +524,53 @@ typedef struct gdn_gated_rmsnorm_args {
 } gdn_gated_rmsnorm_args;
 
 int gdn_gated_rmsnorm(const gdn_gated_rmsnorm_args* args, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * gdn_validate_mixed -- [qwen3_5.cpp] ValidateGdnAttentionMetadata (its
+ * non-speculative part): the metadata contract of one mixed step, checked on
+ * host copies before anything is launched.
+ *
+ * A mixed step packs num_decodes single-token sequences first, then
+ * num_prefills prefill sequences ([qwen3_5.cpp] SubView of the decode prefix
+ * and the prefill suffix).  One gdn_prepare runs over all
+ * num_actual_tokens tokens, gdn_decode over rows [0, num_decodes) and
+ * gdn_prefill_varlen over the rest with cu_seqlens_prefill, which must be the
+ * suffix of cu_seqlens rebased to 0.  Rules, in the page's order (messages are
+ * the page's, without its "qwen3_5: " prefix):
+ *   counts >= 0; num_decode_tokens == num_decodes;
+ *   num_actual_tokens == num_decode_tokens + num_prefill_tokens;
+ *   state_indices_host follows the index rules of the general section, and
+ *   holds no -1 unless allow_inert_padding;
+ *   cu_seqlens_host[0] == 0, cu_seqlens_host[nreq] == num_actual_tokens,
+ *   strictly increasing, cu_seqlens_host[num_decodes] == num_decode_tokens;
+ *   for prefill i: prefill_state_indices_host[i] == state_indices_host[nd+i]
+ *   and >= 0, cu_seqlens_prefill_host[i] == cu_seqlens_host[nd+i] - nd_tok,
+ *   prefill_has_initial_state_host[i] == has_initial_state_host[nd+i];
+ *   cu_seqlens_prefill_host[num_prefills] == num_prefill_tokens.
+ * Every pointer is a HOST pointer; the arrays are read, never written.
+ * prefill_state_indices_host / prefill_has_initial_state_host may be NULL
+ * when the prefill calls take the suffix views of the full arrays (as this
+ * library's step helper does); has_initial_state_host NULL means all 1.
+ * Returns GDN_OK or GDN_ERR_INVALID_ARGUMENT with the message; launches
+ * nothing and needs no GPU.
+ * ------------------------------------------------------------------------- */
+typedef struct gdn_mixed_meta {
+  int64_t num_decodes;                           /* leading single-token sequences */
+  int64_t num_prefills;                          /* sequences after them */
+  int64_t num_decode_tokens;                     /* tokens of the decode rows */
+  int64_t num_prefill_tokens;                    /* tokens of the prefill rows */
+  int64_t num_actual_tokens;                     /* T of the step */
+  int64_t state_slots;                           /* slots of the state pool */
+  int32_t allow_inert_padding;                   /* 1: -1 allowed among decode rows */
+  const int32_t* cu_seqlens_host;                /* [nreq + 1] */
+  const int32_t* state_indices_host;             /* [nreq] */
+  const uint8_t* has_initial_state_host;         /* [nreq] or NULL */
+  const int32_t* cu_seqlens_prefill_host;        /* [num_prefills + 1], rebased */
+  const int32_t* prefill_state_indices_host;     /* [num_prefills] or NULL */
+  const uint8_t* prefill_has_initial_state_host; /* [num_prefills] or NULL */
+} gdn_mixed_meta;
+
+int gdn_validate_mixed(const gdn_mixed_meta* meta);
 
 /* Scratch bytes gdn_prefill_varlen needs for these sizes and algorithm (0 for
  * the recurrent algorithm).  Depends only on the arguments. */

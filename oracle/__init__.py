@@ -163,6 +163,9 @@ def _declare(L):
         [_i64] * 18 + [ctypes.c_char_p, ctypes.c_size_t])
     L.orc_validate_cu_seqlens.restype = ctypes.c_int
     L.orc_validate_cu_seqlens.argtypes = [_vp, _i64, _i64, ctypes.c_char_p, ctypes.c_size_t]
+    L.orc_validate_prepare_cu_seqlens.restype = ctypes.c_int
+    L.orc_validate_prepare_cu_seqlens.argtypes = [_vp, _i64, _i64, ctypes.c_char_p,
+                                                  ctypes.c_size_t]
     for suf, ct in (("f32", ctypes.c_float), ("f64", ctypes.c_double)):
         fn = getattr(L, f"orc_gated_rmsnorm_{suf}")
         fn.restype = ctypes.c_int
@@ -252,6 +255,13 @@ def validate_cu_seqlens(cu, batch, total):
     c = np.ascontiguousarray(cu, dtype=np.int32)
     b = _msgbuf()
     rc = _load().orc_validate_cu_seqlens(_ptr(c), int(batch), int(total), b, 512)
+    return rc, b.value.decode()
+
+
+def validate_prepare_cu_seqlens(cu, batch, total):
+    c = np.ascontiguousarray(cu, dtype=np.int32)
+    b = _msgbuf()
+    rc = _load().orc_validate_prepare_cu_seqlens(_ptr(c), int(batch), int(total), b, 512)
     return rc, b.value.decode()
 
 

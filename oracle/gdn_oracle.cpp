@@ -83,22 +83,25 @@ R softplus_(R x) {
 }
 
 // ---- [cpu.rs] recurrent_gated_delta_rule_varlen_f32 cu_seqlens rules -------
-int check_cu(const int32_t* cu, int64_t batch, int64_t total, char* msg, size_t cap) {
+// The page formats cu.first() and cu.last(), which are Rust Options, with
+// {:?}: a present value prints as "Some(v)".
+int check_cu(const int32_t* cu, int64_t batch, int64_t total, char* msg, size_t cap,
+             const char* who = "gated_delta_rule_varlen") {
   if (cu == nullptr) {
     set_msg(msg, cap, "cu_seqlens is NULL");
     return ORC_ERR_INVALID;
   }
   if (cu[0] != 0 || static_cast<int64_t>(cu[batch]) != total) {
     set_msg(msg, cap,
-            "gated_delta_rule_varlen cu_seqlens must start at 0 and end at total_tokens " +
-                std::to_string(total) + ", got first=" + std::to_string(cu[0]) +
-                " last=" + std::to_string(cu[batch]));
+            std::string(who) + " cu_seqlens must start at 0 and end at total_tokens " +
+                std::to_string(total) + ", got first=Some(" + std::to_string(cu[0]) +
+                ") last=Some(" + std::to_string(cu[batch]) + ")");
     return ORC_ERR_INVALID;
   }
   for (int64_t s = 0; s < batch; ++s) {
     if (cu[s + 1] <= cu[s]) {
       set_msg(msg, cap,
-              "gated_delta_rule_varlen sequence " + std::to_string(s) +
+              std::string(who) + " sequence " + std::to_string(s) +
                   " has empty or non-monotonic range " + std::to_string(cu[s]) + ".." +
                   std::to_string(cu[s + 1]));
       return ORC_ERR_INVALID;
@@ -812,6 +815,17 @@ int orc_validate_cu_seqlens(const int32_t* cu, int64_t batch, int64_t total, cha
     return ORC_ERR_SHAPE;
   }
   return check_cu(cu, batch, total, msg, cap);
+}
+
+// [cpu.rs] linear_attention_prepare_varlen_f32: the same cu_seqlens rules
+// under the prepare's label.
+int orc_validate_prepare_cu_seqlens(const int32_t* cu, int64_t batch, int64_t total, char* msg,
+                                    size_t cap) {
+  if (batch <= 0 || total <= 0) {
+    set_msg(msg, cap, "linear_attention_prepare_varlen shape must be positive");
+    return ORC_ERR_SHAPE;
+  }
+  return check_cu(cu, batch, total, msg, cap, "linear_attention_prepare_varlen");
 }
 
 int orc_validate_state_indices(const int32_t* indices, int64_t n, int64_t slots,

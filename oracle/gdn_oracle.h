@@ -75,6 +75,10 @@ int orc_validate_linear_attention_decode_prepare_shape(
  * at total_tokens, every range non-empty and increasing. */
 int orc_validate_cu_seqlens(const int32_t* cu_seqlens, int64_t batch, int64_t total_tokens,
                             char* msg, size_t msg_cap);
+/* [cpu.rs] linear_attention_prepare_varlen_f32: the same rules and messages
+ * under the label "linear_attention_prepare_varlen". */
+int orc_validate_prepare_cu_seqlens(const int32_t* cu_seqlens, int64_t batch,
+                                    int64_t total_tokens, char* msg, size_t msg_cap);
 /* [qwen3_5.cpp] ValidateGdnStateIndices: -1 is the only negative value, a live
  * slot is < state_slots, no duplicate live slot.  Both the O(n) seen-set pass
  * and (when force_full != 0) the O(n^2) pairwise re-check run. */

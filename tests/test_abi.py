@@ -116,7 +116,7 @@ def test_prefill_cu_seqlens_messages():
     rc, msg = call_prefill(prefill_args(cu_seqlens_host=ctypes.addressof(cu)))
     assert rc == B.GDN_ERR_INVALID_ARGUMENT
     assert msg == ("gated_delta_rule_varlen cu_seqlens must start at 0 and end at total_tokens 10,"
-                   " got first=0 last=9")
+                   " got first=Some(0) last=Some(9)")
     cu = (ctypes.c_int32 * 3)(0, 0, 10)
     rc, msg = call_prefill(prefill_args(cu_seqlens_host=ctypes.addressof(cu)))
     assert rc == B.GDN_ERR_INVALID_ARGUMENT
@@ -177,6 +177,21 @@ def test_prepare_messages():
     assert rc == B.GDN_ERR_INVALID_ARGUMENT  # 28 bf16 = 56 bytes: rows not 16-byte aligned
     rc, msg = call_prepare(prepare_args(act_dtype=5))
     assert rc == B.GDN_ERR_DTYPE
+
+
+def test_prepare_cu_seqlens_messages():
+    """The prepare's host-mirror cu_seqlens rules carry the label of [cpu.rs]
+    linear_attention_prepare_varlen_f32 and print the bounds in Rust's Option
+    Debug form, as the page's format string does."""
+    cu = (ctypes.c_int32 * 3)(1, 2, 7)
+    rc, msg = call_prepare(prepare_args(T=7, N=2, cu_seqlens_host=ctypes.addressof(cu)))
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT
+    assert msg == ("linear_attention_prepare_varlen cu_seqlens must start at 0 and end at"
+                   " total_tokens 7, got first=Some(1) last=Some(7)")
+    cu = (ctypes.c_int32 * 3)(0, 0, 7)
+    rc, msg = call_prepare(prepare_args(T=7, N=2, cu_seqlens_host=ctypes.addressof(cu)))
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT
+    assert msg == "linear_attention_prepare_varlen sequence 0 has empty or non-monotonic range 0..0"
 
 
 def test_valid_call_without_gpu_stops_before_launch():

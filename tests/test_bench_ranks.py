@@ -64,3 +64,25 @@ def test_reference_arm_prints_on_rank_zero_only(monkeypatch, capsys):
     monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--gpus", "2"])
     assert bench.main() == 0
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_times_whole_oracle_steps(monkeypatch, capsys):
+    """The reference arm runs W + K whole oracle steps of the workload (no
+    extrapolation): its timed steps fit inside the wall time of the call, and
+    it prints the same config object as the GPU arm."""
+    import time
+    from gated_delta_rule_44_gb300 import workloads as W
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--workload",
+                                      "tiny_f32", "--steps", "3", "--warmup", "1"])
+    t0 = time.perf_counter()
+    assert bench.main() == 0
+    wall = time.perf_counter() - t0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    w = W.named("tiny_f32")
+    assert line["impl"] == "reference" and line["steps"] == 3 and line["warmup"] == 1
+    assert line["config"] == bench.workload_config(w, 1)
+    assert line["ms_per_step"] * 3 / 1e3 <= wall
+    assert line["value"] == pytest.approx(w.T / (line["ms_per_step"] / 1e3), rel=1e-3)
+    assert "no extrapolation" in line["cpu_baseline"]["sample"]

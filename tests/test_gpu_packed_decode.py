@@ -2,8 +2,10 @@
 projections: [cpu_ops.cpp] GdnPackedDecodeKernel with the conv update of
 CausalConv1dUpdateKernel folded in; packed layouts of [cpu.rs]
 linear_attention_prepare_varlen_packed_qkvz_ba_f32) against the oracle's
-prepare (O1) followed by its decode (O3), computed in f64 with nothing rounded
-in between, through the C ABI.  Covers the decode_b256 shape, GQA ratios 1, 2
+prepare (O1) followed by its decode (O3), computed in f64, through the C ABI.
+Between the two steps the reference rounds beta through b's storage type (bf16,
+nearest even) where the page's kernel does so, "exactly at the upstream
+store/load boundary"; nothing else is rounded in between.  Covers the decode_b256 shape, GQA ratios 1, 2
 and 4, Dk 64 and 128, ragged Dv, conv widths 2..4, padding rows, f32 and bf16,
 and a CUDA graph captured once and replayed with new metadata."""
 import numpy as np
@@ -47,7 +49,8 @@ def gpu(d, dev, conv_d, state_d, idx=None, stream=None):
 
 
 def reference(d, conv, state):
-    """O1 (one-token sequences) then O3, f64, nothing rounded in between."""
+    """O1 (one-token sequences) then O3, f64; beta rounded through b's dtype
+    in between ([cpu_ops.cpp] GdnPackedDecodeKernel), nothing else."""
     Hk, Hv, Dk, Dv, K = d["dims"]
     Bn, C = d["qkvz"].shape[0], d["C"]
     x = H.f32(d["qkvz"])[:, :C].astype(np.float64)
@@ -56,6 +59,8 @@ def reference(d, conv, state):
                                  d["A_log"].numpy(), d["dt_bias"].numpy(),
                                  np.arange(Bn + 1, dtype=np.int32), Hk, Hv, Dk, Dv, K,
                                  state_indices=d["idx"].numpy(), dtype=np.float64)
+    if d["ba"].dtype == torch.bfloat16:
+        prep["beta"] = H.bf16_round(prep["beta"])
     out = oracle.gdn_decode(prep["q"], prep["k"], prep["v"], prep["g"], prep["beta"], state,
                             1.0 / np.sqrt(Dk), state_indices=d["idx"].numpy(), dtype=np.float64)
     return out

@@ -110,6 +110,14 @@ def test_cu_seqlens_messages():
     assert rc == oracle.ORC_ERR_INVALID
 
 
+def test_prepare_cu_seqlens_messages():
+    rc, msg = oracle.validate_prepare_cu_seqlens([1, 3, 7], 2, 7)
+    assert rc == oracle.ORC_ERR_INVALID and msg == G["prep_cu_bounds"]
+    rc, msg = oracle.validate_prepare_cu_seqlens([0, 0, 7], 2, 7)
+    assert rc == oracle.ORC_ERR_INVALID and msg == G["prep_cu_empty"]
+    assert oracle.validate_prepare_cu_seqlens([0, 3, 7], 2, 7) == (0, "")
+
+
 @pytest.mark.parametrize("idx,slots,ok,frag", [
     ([0, 1, 2], 3, True, ""),
     ([-1, 2, -1, 0], 3, True, ""),
