@@ -6,14 +6,14 @@ mixed-step helper and the seeded synthetic workloads.  The library is loaded
 on first use; there is no CPU fallback.
 """
 from .binding import (GDN_DTYPE_BF16, GDN_DTYPE_F32, GDN_PREFILL_AUTO, GDN_PREFILL_CHUNKED,
-                      GDN_PREFILL_RECURRENT, GdnError, gdn_decode, gdn_prefill_resolve_algo,
+                      GDN_PREFILL_FUSED, GDN_PREFILL_RECURRENT, GdnError, gdn_decode, gdn_prefill_resolve_algo,
                       gdn_prefill_varlen, gdn_prefill_workspace_bytes, gdn_prepare,
                       gdn_read_device_status, gdn_version, lib)
 from .layer import GdnStep, mixed_step
 
 __all__ = [
     "GDN_DTYPE_BF16", "GDN_DTYPE_F32", "GDN_PREFILL_AUTO", "GDN_PREFILL_CHUNKED",
-    "GDN_PREFILL_RECURRENT", "GdnError", "GdnStep", "gdn_decode", "gdn_prefill_resolve_algo",
+    "GDN_PREFILL_FUSED", "GDN_PREFILL_RECURRENT", "GdnError", "GdnStep", "gdn_decode", "gdn_prefill_resolve_algo",
     "gdn_prefill_varlen", "gdn_prefill_workspace_bytes", "gdn_prepare", "gdn_read_device_status",
     "gdn_version", "lib", "mixed_step",
 ]

@@ -30,6 +30,7 @@ GDN_DTYPE_BF16 = 1
 GDN_PREFILL_AUTO = 0
 GDN_PREFILL_CHUNKED = 1
 GDN_PREFILL_RECURRENT = 2
+GDN_PREFILL_FUSED = 3
 
 _i64 = ctypes.c_int64
 _i32 = ctypes.c_int32

@@ -738,8 +738,8 @@ int gdn_validate_mixed(const gdn_mixed_meta* m) {
 
 int32_t gdn_prefill_resolve_algo(int64_t Dk, int64_t Dv, int32_t act_dtype, int32_t algo) {
   if (algo != GDN_PREFILL_AUTO) return algo;
-  return gdn::chunked_supported((int)Dk, (int)Dv, act_dtype == GDN_DTYPE_BF16)
-             ? GDN_PREFILL_CHUNKED
+  return gdn::fused_supported((int)Dk, (int)Dv, act_dtype == GDN_DTYPE_BF16)
+             ? GDN_PREFILL_FUSED
              : GDN_PREFILL_RECURRENT;
 }
 
@@ -761,7 +761,7 @@ int gdn_prefill_varlen(const gdn_prefill_args* a, void* stream) {
     return fail(GDN_ERR_SHAPE, "gated_delta_rule_varlen shape must be positive, got batch=" +
                                    S(a->N) + " total_tokens=" + S(a->T));
   if (require_ptr(a->cu_seqlens, "cu_seqlens")) return GDN_ERR_INVALID_ARGUMENT;
-  if (a->algo < GDN_PREFILL_AUTO || a->algo > GDN_PREFILL_RECURRENT)
+  if (a->algo < GDN_PREFILL_AUTO || a->algo > GDN_PREFILL_FUSED)
     return fail(GDN_ERR_INVALID_ARGUMENT, "unknown prefill algo " + S(a->algo));
   if (a->cu_seqlens_host != nullptr)
     if (int rc = check_cu_host(a->cu_seqlens_host, a->N, a->T, "gated_delta_rule_varlen"))
@@ -810,6 +810,14 @@ int gdn_prefill_varlen(const gdn_prefill_args* a, void* stream) {
     if (p.status == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
     gdn::ChunkedLaunch c{p, a->workspace, a->workspace_bytes};
     return launch_result(gdn::launch_chunked(c, st), "gdn_prefill_varlen(chunked)");
+  }
+  if (algo == GDN_PREFILL_FUSED) {
+    if (!gdn::fused_supported((int)a->Dk, (int)a->Dv, p.bf16))
+      return fail(GDN_ERR_UNSUPPORTED,
+                  "the fused chunked prefill supports bf16 activations with Dk = Dv = 128");
+    p.status = gdn::status_word();
+    if (p.status == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
+    return launch_result(gdn::launch_fused(p, st), "gdn_prefill_varlen(fused)");
   }
   if (!gdn::recurrent_supported((int)a->Dk))
     return fail(GDN_ERR_UNSUPPORTED, "the recurrent prefill supports Dk in {16, 32, 64, 128, 256}");

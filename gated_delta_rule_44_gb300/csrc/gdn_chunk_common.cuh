@@ -1,0 +1,156 @@
+// gdn_chunk_common.cuh -- pieces shared by the two chunked (C = 64) prefill
+// implementations: bf16 packing and hi + lo splitting of f32 operands, named
+// barriers, bulk copies, and the TMA tensor maps of the q, k, v tiles.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "tcgen05.cuh"
+
+namespace gdn {
+namespace chunk {
+
+constexpr int kC = 64;   // chunk length
+constexpr int kD = 128;  // Dk = Dv
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Stores 8 floats as bf16 into one 16-byte chunk.
+__device__ __forceinline__ void st_bf16x8(void* p, const float* v) {
+  *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                            pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+}
+
+// x rounded to nearest with 8 significant bits (Veltkamp's splitting with the
+// factor 2^16 + 1), so exactly a bf16 value; x - hi is exact in f32.  Plain
+// f32 arithmetic: it runs on the FMA pipe instead of the (quarter-rate)
+// conversion unit.  Valid for |x| < FLT_MAX / 65537.
+__device__ __forceinline__ float split_hi(float x) {
+  const float c = __fmul_rn(x, 65537.0f);
+  return __fsub_rn(c, __fsub_rn(c, x));
+}
+
+// The bf16 bits of hi (its upper half) and bf16(x - hi) of two values, packed
+// as two bf16x2 words: hi + lo carries about 16 significant bits of x.
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hw, uint32_t& lw) {
+  const float ha = split_hi(a), hb = split_hi(b);
+  hw = __byte_perm(__float_as_uint(ha), __float_as_uint(hb), 0x7632);  // upper halves
+  lw = pack_bf16x2(__fsub_rn(a, ha), __fsub_rn(b, hb));
+}
+
+// hi and lo images of 8 values, each into one 16-byte chunk.
+__device__ __forceinline__ void st_split8(void* hi, void* lo, const float* v) {
+  uint32_t hw[4], lw[4];
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) split2(v[e], v[e + 1], hw[e / 2], lw[e / 2]);
+  *reinterpret_cast<uint4*>(hi) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  *reinterpret_cast<uint4*>(lo) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+}
+
+__device__ __forceinline__ void ld_bf16x8(const void* p, float* v) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+__device__ __forceinline__ void named_bar(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Named barrier that also ANDs a predicate over the participating threads.
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(mbar)
+      : "memory");
+}
+
+// Bulk copy shared -> global (one thread), tracked by its bulk async-group.
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile(
+      "cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(
+          reinterpret_cast<uint64_t>(dst)),
+      "r"(src), "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+}
+// Waits until this thread's bulk copies have read their shared-memory sources.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+}
+// Waits until this thread's bulk copies are complete.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
+}
+
+// Shared memory rounded up to the 1024-byte alignment of swizzled tiles; the
+// pointer keeps the shared address space, so accesses compile to shared ones.
+__device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
+  return raw + ((1024u - (umma::smem_u32(raw) & 1023u)) & 1023u);
+}
+
+// ---- host: TMA tensor maps --------------------------------------------------------
+
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// [rows, heads, 128] bf16 tensor; box = 64 rows x 1 head x 64 elements, SW128.
+// Rows past `rows` read as zeros.
+inline bool make_map(CUtensorMap* m, const void* ptr, int rows, int heads) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(heads),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2,
+                           static_cast<cuuint64_t>(heads) * kD * 2};
+  cuuint32_t box[3] = {64, 1, 64};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace chunk
+}  // namespace gdn

@@ -1,0 +1,804 @@
+// gdn_fused.cu -- chunked (C = 64) WY/UT-form varlen prefill in ONE launch:
+// one CTA per (sequence, value head) carries the f32 state through the
+// sequence's chunks while its own warps prepare the next chunk, so nothing of
+// a chunk but its output ever leaves the SM.
+//
+// Defines the recurrence of [cpu.rs] (ferrum-kernels 0.8.0, src/ferrum_kernels/
+// backend/cpu.rs) recurrent_gated_delta_rule_varlen_f32 / [cpu_ops.cpp]
+// (vllm.cpp, src/vt/cpu/cpu_ops.cpp) GdnPrefillKernel, evaluated chunk by
+// chunk in the form derived from it (the pages name a chunked GPU form but do
+// not print it).  For one chunk of L <= 64 tokens with state S = [Dv, Dk] at
+// its start (gam_i = sum_{t <= i} g_t):
+//   A_ij = beta_i e^{gam_i - gam_j} k_i.k_j (j < i),   T = (I + A)^-1
+//   W    = T diag(beta e^gam) K,   Ut = T diag(beta) V,   U = Ut - W S^T
+//   O    = diag(e^gam) scale Q S^T + P U,   P_ij = scale e^{gam_i - gam_j} q_i.k_j (j <= i)
+//   S'   = e^{gam_L} S + U^T diag(e^{gam_L - gam}) K
+// with every exponent <= 0.
+//
+// Orientation.  The state-side products run transposed, with TMEM lanes = the
+// value dimension dv, so that one thread owns one row S[dv, :]:
+//   G    = [K; Q] K^T                 (M = 128 token rows, N = 64)     prep
+//   W^T  = K^T Tw^T                   (M = 128 dk, N = 64 tokens)      prep
+//   D1   = V^T Tu^T - S W^T | S Q^T   (M = 128 dv, N = 64 + 64)
+//          so D1[:, 0:64] = U^T and D1[:, 64:128] = (Q S^T)^T directly
+//   dS   = U'^T K   onto  e^{gam_L} S (M = 128 dv, N = 128 dk), U' = diag(fu) U
+//   D3   = U^T P^T  onto  (fo Q S^T)^T (M = 128 dv, N = 64 tokens)
+// U'^T and U^T enter the tensor core from TMEM (A operand in tensor memory),
+// the f32 state lives in TMEM as dS's accumulator, its hi + lo bf16 images in
+// shared memory as D1's A operand.
+//
+// Precision.  q, k, v are exact bf16 inputs.  T, S, U', U and P enter the
+// tensor core as hi + lo bf16 pairs (hi = x rounded to 8 significant bits, lo
+// = bf16(x - hi)), about 16 significant bits; W as one bf16 value (it reaches
+// the output only through the W S^T correction).  Products of two split
+// operands take hi*hi + hi*lo + lo*hi.
+//
+// Roles (14 warps):
+//   warp 0      TMA loads: K, Q of chunk c into stage c % 2; V of chunk c into
+//               the region W^T(c - 1) held once D1(c - 1) has read it
+//   warp 1      every MMA, issued in dependency order as their inputs appear
+//   warps 2-9   prep of chunk c: norms, gates, A and P from G, T by 16 x 16
+//               blocks, the Tw / Tu / P images, the W^T image
+//   warps 10-13 the state chain of chunk c: U from D1 (U', U into TMEM and
+//               fo Q S^T into D3), the state update S' and its images, the
+//               output rows
+// Prep of chunk c + 1 overlaps the chain of chunk c.  Every hand-off is an
+// mbarrier; every wait is bounded and, once any wait gives up, every role
+// leaves at its next wait, in-flight copies and MMAs are drained (bounded) and
+// the TMEM is freed.
+//
+// Partial chunks: g and beta of rows past the chunk end are taken as 0, so
+// those rows of W, Ut, U and U' are exactly zero and their K, Q, V rows (the
+// next sequence's tokens, or zeros past the tensor end) never contribute.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "gdn_chunk_common.cuh"
+#include "gdn_internal.h"
+#include "tcgen05.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace umma;
+using namespace chunk;
+
+constexpr long long kWaitBudget = 2000000000LL;  // ~1 s of SM clock per wait
+
+struct FusedSmem {
+  static constexpr uint32_t KQ = 0;             // 2 stages x [K box0 | Q box0 | K box1 | Q box1]
+  static constexpr uint32_t kStage = 32768;
+  static constexpr uint32_t SH = 65536;         // S hi image [128 dv][128 dk], K-major, 2 x 16 KB
+  static constexpr uint32_t SL = SH + 32768;    // S lo image
+  static constexpr uint32_t WV = SL + 32768;    // W^T image [128 dk][64 tok] MN-major, or V [V0|V1]
+  static constexpr uint32_t PI = WV + 16384;    // P hi [64 i][64 j] K-major, then P lo
+  static constexpr uint32_t TI = PI + 16384;    // Tw hi, Tw lo, Tu hi, Tu lo (8 KB each); Y aliases
+  static constexpr uint32_t AT = TI + 32768;    // A, then T in place, f32 [64][68]
+  static constexpr uint32_t kAStride = 68;
+  static constexpr uint32_t kYStride = 36;      // Y = A21 T11, f32 [32][36] at TI
+  static constexpr uint32_t GB = AT + 64 * kAStride * 4;  // g, beta, gam, kn, qn, wj, uj
+  static constexpr uint32_t FAC = GB + 7 * 64 * 4;        // 2 x {fo[64], fu[64], e^{gam_L}, 0, 0, 0}
+  static constexpr uint32_t kFac = 132;                   // floats per factor buffer
+  static constexpr uint32_t BYTES = FAC + 2 * kFac * 4;
+};
+static_assert(FusedSmem::BYTES + 1024 + 1024 <= 232448, "shared memory per CTA");
+static_assert(32 * FusedSmem::kYStride * 4 <= 8192, "Y fits in the Tw hi image space");
+
+// TMEM columns (512 allocated).
+constexpr uint32_t kTG = 0;     // G = [K;Q] K^T, then W^T (64)
+constexpr uint32_t kTD1 = 64;   // D1: U^T | (Q S^T)^T (128)
+constexpr uint32_t kTS = 192;   // f32 state S[dv][dk], dS accumulates onto it (128)
+constexpr uint32_t kTD3 = 320;  // output accumulator O^T (64)
+constexpr uint32_t kTU2 = 384;  // U'^T hi | lo as packed bf16 pairs (32 + 32)
+constexpr uint32_t kTU = 448;   // U^T hi | lo (32 + 32)
+
+constexpr int kThreads = 448;
+constexpr int kPrepThreads = 256;
+constexpr int kScanThreads = 128;
+constexpr int kBarPrep = 1;
+constexpr int kBarScan = 2;
+
+enum Mb : int {
+  kMbKq0 = 0, kMbKq1, kMbKqFree0, kMbKqFree1, kMbV, kMbG, kMbGFree, kMbTwTu, kMbWu, kMbWImg,
+  kMbPImg, kMbFac, kMbD1, kMbD1Free, kMbUReady, kMbSImg, kMbD2, kMbD3, kMbEnd, kNumMb
+};
+
+// D (+)= A[tmem] * B[smem]: the A operand in tensor memory (M = 128 lanes, K
+// packed two bf16 per 32-bit column, the even element in the low half).
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+      : "memory");
+}
+
+// 32 lanes x 8 columns of 32-bit values from registers.
+__device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+      : "memory");
+}
+
+// Bounded wait that also gives up as soon as another role has given up.
+__device__ __forceinline__ bool wait_mb(uint32_t mb, uint32_t parity, volatile int* abort,
+                                        unsigned* status) {
+  if (mbar_try_wait(mb, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(mb, parity)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > kWaitBudget) {
+      if (atomicExch(const_cast<int*>(abort), 1) == 0) atomicOr(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_v, const RecurLaunch p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = aligned_smem(smem_raw);
+  __shared__ uint64_t mbs[kNumMb];
+  __shared__ uint32_t tslot;
+  __shared__ int s_abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.x % p.Hv, s = blockIdx.x / p.Hv;
+  const int hk = h / (p.Hv / p.Hk);
+
+  const int lo = __ldg(p.cu + s), hi = __ldg(p.cu + s + 1);
+  if (lo < 0 || hi <= lo || hi > p.T || __ldg(p.cu) != 0 || __ldg(p.cu + p.N) != p.T) {
+    if (tid == 0) atomicOr(p.status, kStatusBadSeqlens);
+    return;
+  }
+  int slot = p.sidx != nullptr ? __ldg(p.sidx + s) : s;
+  if (slot < -1 || slot >= p.slots) {
+    if (tid == 0) atomicOr(p.status, kStatusBadIndex);
+    slot = -1;
+  }
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+  if (slot < 0) {  // padded sequence: zero outputs, pool untouched
+    for (int idx = tid; idx < (hi - lo) * 16; idx += kThreads) {
+      const int t = lo + idx / 16, q16 = idx % 16;
+      *reinterpret_cast<uint4*>(out + ((int64_t)t * p.Hv + h) * kD + q16 * 8) =
+          make_uint4(0, 0, 0, 0);
+    }
+    return;
+  }
+  const int nch = (hi - lo + kC - 1) / kC;
+  const uint32_t base = smem_u32(sm);
+  auto MB = [&](int i) { return smem_u32(&mbs[i]); };
+  volatile int* abort = &s_abort;
+
+  if (tid == 0) {
+    for (int i = 0; i < kNumMb; ++i) mbar_init(MB(i), 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(smem_u32(&tslot), 512);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = tslot;
+  float* fac = reinterpret_cast<float*>(sm + FusedSmem::FAC);
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- loader
+    if (lane == 0) {
+      int last_kq[2] = {-1, -1}, n_v = 0;
+      auto load_kq = [&](int c) {
+        const uint32_t st = base + FusedSmem::KQ + (c & 1) * FusedSmem::kStage;
+        const uint32_t mb = MB(kMbKq0 + (c & 1));
+        const int t0 = lo + c * kC;
+        mbar_expect_tx(mb, 4 * 8192);
+        tma_load_3d(st + 0, &tm_k, mb, 0, hk, t0);
+        tma_load_3d(st + 8192, &tm_q, mb, 0, hk, t0);
+        tma_load_3d(st + 16384, &tm_k, mb, 64, hk, t0);
+        tma_load_3d(st + 24576, &tm_q, mb, 64, hk, t0);
+        last_kq[c & 1] = c;
+      };
+      auto load_v = [&](int c) {
+        const uint32_t mb = MB(kMbV);
+        const int t0 = lo + c * kC;
+        mbar_expect_tx(mb, 2 * 8192);
+        tma_load_3d(base + FusedSmem::WV, &tm_v, mb, 0, h, t0);
+        tma_load_3d(base + FusedSmem::WV + 8192, &tm_v, mb, 64, h, t0);
+        n_v = c + 1;
+      };
+      load_kq(0);
+      if (nch > 1) load_kq(1);
+      load_v(0);
+      for (int c = 1; c < nch; ++c) {
+        // V(c) replaces W^T(c - 1) once D1(c - 1) has read it.
+        if (!wait_mb(MB(kMbD1), (c - 1) & 1, abort, p.status)) break;
+        load_v(c);
+        if (c + 1 < nch) {  // stage (c + 1) % 2 is free once D2(c - 1) has read K(c - 1)
+          if (!wait_mb(MB(kMbKqFree0 + ((c + 1) & 1)), ((c - 1) >> 1) & 1, abort, p.status))
+            break;
+          load_kq(c + 1);
+        }
+      }
+      __syncwarp(1u);
+      if (*abort) {  // let the copies in flight land before the CTA exits
+        for (int st = 0; st < 2; ++st)
+          if (last_kq[st] >= 0) mbar_wait(MB(kMbKq0 + st), (last_kq[st] >> 1) & 1, kWaitBudget);
+        if (n_v > 0) mbar_wait(MB(kMbV), (n_v - 1) & 1, kWaitBudget);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id_g = idesc_bf16_f32(128, 64, false, false);
+      const uint32_t id_wu = idesc_bf16_f32(128, 64, true, false);
+      const uint32_t id_d1w = idesc_bf16_f32(128, 64, false, true);
+      const uint32_t id_d1q = idesc_bf16_f32(128, 64, false, false);
+      const uint32_t id_d2 = idesc_bf16_f32(128, 128, false, true);
+      const uint32_t id_d3 = idesc_bf16_f32(128, 64, false, false);
+      int cg = 0, cwu = 0, cd1 = 0, cd23 = 0;
+      long long last = clock64();
+      while (cd23 < nch) {
+        if (*abort) break;
+        bool went = false;
+        if (cd23 < cd1 && mbar_try_wait(MB(kMbUReady), cd23 & 1) &&
+            mbar_try_wait(MB(kMbPImg), cd23 & 1)) {
+          fence_after_sync();
+          const int c = cd23;
+          const uint32_t st = base + FusedSmem::KQ + (c & 1) * FusedSmem::kStage;
+          // dS = U'^T K onto e^{gam_L} S  (A = U'^T hi, lo from TMEM; B = K MN-major)
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int kk = 0; kk < kC; kk += 16)
+              mma_bf16_ta(tmem + kTS, tmem + kTU2 + part * 32 + kk / 2,
+                          desc_sw128(st + (kk / 8) * 1024, 16384, 1024), id_d2, true);
+          mma_commit(MB(kMbD2));
+          mma_commit(MB(kMbKqFree0 + (c & 1)));
+          // O^T += U^T P^T: hi*hi, hi*lo, lo*hi  (A = U^T from TMEM; B = P, K-major)
+#pragma unroll
+          for (int pr = 0; pr < 3; ++pr) {
+            const uint32_t ua = kTU + (pr == 2 ? 32 : 0);
+            const uint32_t pb = base + FusedSmem::PI + (pr == 1 ? 8192 : 0);
+#pragma unroll
+            for (int kk = 0; kk < kC; kk += 16)
+              mma_bf16_ta(tmem + kTD3, tmem + ua + kk / 2, desc_sw128(pb + kk * 2, 16, 1024),
+                          id_d3, true);
+          }
+          mma_commit(MB(kMbD3));
+          ++cd23;
+          went = true;
+        } else if (cd1 < cwu && mbar_try_wait(MB(kMbWImg), cd1 & 1) &&
+                   mbar_try_wait(MB(kMbSImg), cd1 & 1)) {
+          fence_after_sync();
+          const int c = cd1;
+          const uint32_t st = base + FusedSmem::KQ + (c & 1) * FusedSmem::kStage;
+          // D1[:, 0:64] += S (-W)^T onto Ut^T;  D1[:, 64:128] = S Q^T.  A = S hi, lo.
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int kk = 0; kk < kD; kk += 16) {
+              const uint64_t a = desc_sw128(base + (part ? FusedSmem::SL : FusedSmem::SH) +
+                                                (kk / 64) * 16384 + (kk % 64) * 2,
+                                            16, 1024);
+              mma_bf16(tmem + kTD1, a, desc_sw128(base + FusedSmem::WV + (kk / 8) * 1024, 8192, 1024),
+                       id_d1w, true);
+              mma_bf16(tmem + kTD1 + 64, a,
+                       desc_sw128(st + 8192 + (kk / 64) * 16384 + (kk % 64) * 2, 16, 1024),
+                       id_d1q, part > 0 || kk > 0);
+            }
+          mma_commit(MB(kMbD1));
+          ++cd1;
+          went = true;
+        } else if (cwu < cg && mbar_try_wait(MB(kMbTwTu), cwu & 1) &&
+                   mbar_try_wait(MB(kMbV), cwu & 1) &&
+                   (cwu == 0 || mbar_try_wait(MB(kMbD1Free), (cwu - 1) & 1))) {
+          fence_after_sync();
+          const int c = cwu;
+          const uint32_t st = base + FusedSmem::KQ + (c & 1) * FusedSmem::kStage;
+          // W^T = K^T Tw^T (A = K, MN-major, M = dk), hi + lo of Tw.
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int kk = 0; kk < kC; kk += 16)
+              mma_bf16(tmem + kTG, desc_sw128(st + (kk / 8) * 1024, 16384, 1024),
+                       desc_sw128(base + FusedSmem::TI + part * 8192 + kk * 2, 16, 1024), id_wu,
+                       part > 0 || kk > 0);
+          // Ut^T = V^T Tu^T into D1[:, 0:64] (A = V, MN-major, M = dv).
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int kk = 0; kk < kC; kk += 16)
+              mma_bf16(tmem + kTD1, desc_sw128(base + FusedSmem::WV + (kk / 8) * 1024, 8192, 1024),
+                       desc_sw128(base + FusedSmem::TI + 16384 + part * 8192 + kk * 2, 16, 1024),
+                       id_wu, part > 0 || kk > 0);
+          mma_commit(MB(kMbWu));
+          ++cwu;
+          went = true;
+        } else if (cg < nch && mbar_try_wait(MB(kMbKq0 + (cg & 1)), (cg >> 1) & 1) &&
+                   (cg == 0 || mbar_try_wait(MB(kMbGFree), (cg - 1) & 1))) {
+          fence_after_sync();
+          const uint32_t st = base + FusedSmem::KQ + (cg & 1) * FusedSmem::kStage;
+          // G = [K; Q] K^T  (M = 128, N = 64, K = 128)
+#pragma unroll
+          for (int kk = 0; kk < kD; kk += 16) {
+            const uint32_t off = (kk / 64) * 16384 + (kk % 64) * 2;
+            mma_bf16(tmem + kTG, desc_sw128(st + off, 16, 1024), desc_sw128(st + off, 16, 1024),
+                     id_g, kk > 0);
+          }
+          mma_commit(MB(kMbG));
+          ++cg;
+          went = true;
+        }
+        if (went) {
+          last = clock64();
+        } else if (clock64() - last > kWaitBudget) {
+          if (atomicExch(const_cast<int*>(abort), 1) == 0) atomicOr(p.status, kStatusTimeout);
+          break;
+        }
+      }
+    }
+  } else if (warp < 10) {
+    // ---------------------------------------------------------------- prep
+    const int ptid = tid - 64, pw = warp - 2;
+    const int quad = warp & 3, hf = pw >> 2;
+    float* sg = reinterpret_cast<float*>(sm + FusedSmem::GB);
+    float* sb = sg + 64;
+    float* sgam = sb + 64;
+    float* skn = sgam + 64;
+    float* sqn = skn + 64;
+    float* swj = sqn + 64;
+    float* suj = swj + 64;
+    float* sA = reinterpret_cast<float*>(sm + FusedSmem::AT);
+    float* sY = reinterpret_cast<float*>(sm + FusedSmem::TI);
+    constexpr int S_ = FusedSmem::kAStride;
+    constexpr int SY = FusedSmem::kYStride;
+    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    float g_next = 0.0f, b_next = 0.0f;
+    auto load_gates = [&](int c) {  // ptid < 64
+      const int t0 = lo + c * kC, L = min(kC, hi - t0);
+      if (ptid < L) {
+        g_next = __ldg(p.g + (int64_t)(t0 + ptid) * p.Hv + h);
+        b_next = __ldg(p.beta + (int64_t)(t0 + ptid) * p.Hv + h);
+      } else {
+        g_next = b_next = 0.0f;
+      }
+    };
+    if (ptid < 64) load_gates(0);
+    for (int c = 0; c < nch; ++c) {
+      const uint8_t* sst = sm + FusedSmem::KQ + (c & 1) * FusedSmem::kStage;
+      float* F = fac + (c & 1) * FusedSmem::kFac;
+      bool ok = true;
+      if (ptid < 64) {
+        sg[ptid] = g_next;
+        sb[ptid] = b_next;
+      }
+      ok = wait_mb(MB(kMbKq0 + (c & 1)), (c >> 1) & 1, abort, p.status) && ok;
+      if (ptid < 128) {  // inverse row norms: rows of K (ptid < 64), of Q (64..127)
+        const int r = ptid & 63;
+        float ss = 0.0f;
+        if (p.norm) {
+          const uint8_t* row = sst + (ptid < 64 ? 0 : 8192) + r * 128;
+#pragma unroll
+          for (int box = 0; box < 2; ++box)
+#pragma unroll
+            for (int q16 = 0; q16 < 8; ++q16) {
+              float v[8];
+              ld_bf16x8(row + box * 16384 + ((q16 ^ (r & 7)) << 4), v);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
+            }
+        }
+        (ptid < 64 ? skn : sqn)[r] = p.norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+      }
+      named_bar(kBarPrep, kPrepThreads);
+      if (pw == 0) {  // inclusive scan of g over the chunk (2 tokens per lane)
+        const float a = sg[2 * lane], b = sg[2 * lane + 1];
+        float x = a + b;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        sgam[2 * lane + 1] = x;
+        sgam[2 * lane] = x - b;
+        sg[2 * lane] = __expf(a);  // e^{g_j}: the step between neighbouring decays
+        sg[2 * lane + 1] = __expf(b);
+      }
+      // FAC[c % 2] was last read by the chain's U step of chunk c - 2 and its
+      // state update of chunk c - 1 ... and fac(c) must not complete before the
+      // chain has taken fac(c - 1): both hold once the chain has published the
+      // state images of chunk c - 1.
+      if (c >= 1) ok = wait_mb(MB(kMbSImg), (c - 1) & 1, abort, p.status) && ok;
+      named_bar(kBarPrep, kPrepThreads);
+      if (ptid < 64) {
+        swj[ptid] = sb[ptid] * skn[ptid] * __expf(sgam[ptid]);
+        suj[ptid] = sb[ptid];
+        F[ptid] = p.scale * sqn[ptid] * __expf(sgam[ptid]);              // fo
+        F[64 + ptid] = __expf(sgam[kC - 1] - sgam[ptid]) * skn[ptid];    // fu
+        if (ptid < 4) F[128 + ptid] = ptid == 0 ? __expf(sgam[kC - 1]) : 0.0f;  // e^{gam_L}
+      }
+      named_bar(kBarPrep, kPrepThreads);
+      if (ptid == 0) mbar_arrive(MB(kMbFac));
+      if (ptid < 64 && c + 1 < nch) load_gates(c + 1);  // consumed next chunk
+      ok = wait_mb(MB(kMbG), c & 1, abort, p.status) && ok;
+      fence_after_sync();
+      // Lanes 0..63 of G hold K K^T -> A (f32, shared); lanes 64..127 hold
+      // Q K^T -> P (kept in registers until the previous chunk's D3 has read
+      // the P images).  Row i, columns 32 hf ... 32 hf + 31.
+      const int i = (quad & 1) * 32 + lane;
+      const bool upper = (quad & 1) == 0 && hf == 1;  // rows 0..31 x columns 32..63: zero
+      float pv[32];
+      {
+        float v[32];
+        if (!upper) {
+          tmem_ld32(tmem + kTG + lane_addr + hf * 32, v);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0.0f;
+        }
+        // Decays e^{gam_i - gam_j} (j <= i) as a running product leftward from
+        // the block's last column; 0 right of the diagonal, 1 on it.
+        float dec[32];
+        if (!upper) {
+          const int jr = hf * 32 + 31;
+          float cur = jr <= i ? __expf(sgam[i] - sgam[jr]) : 0.0f;
+          dec[31] = cur;
+#pragma unroll
+          for (int e = 30; e >= 0; --e) {
+            const int j = hf * 32 + e;
+            cur = j == i ? 1.0f : cur * sg[j + 1];
+            dec[e] = cur;
+          }
+        }
+        if (quad < 2) {
+          const float fi = sb[i] * skn[i];
+          if (!upper) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int j = hf * 32 + e;
+              v[e] = j < i ? fi * skn[j] * dec[e] * v[e] : 0.0f;
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(sA + i * S_ + hf * 32 + e) =
+                make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) pv[e] = 0.0f;
+        } else {
+          const float fi = p.scale * sqn[i];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int j = hf * 32 + e;
+            pv[e] = upper ? 0.0f : fi * skn[j] * dec[e] * v[e];
+          }
+        }
+      }
+      fence_before_sync();
+      named_bar(kBarPrep, kPrepThreads);  // A complete; G read (W^T may reuse its columns)
+      // T = (I + A)^-1 by blocks: the four 16 x 16 diagonal blocks by forward
+      // substitution (prep warps 0..1, lane = column), the two 32 x 32
+      // diagonal blocks from them (X = -D1 A10 D0), then T21 = -T22 (A21 T11).
+      if (pw < 2) {
+        const int b0 = 16 * (2 * pw + (lane >> 4)), cc = lane & 15;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          const float* arow = sA + (b0 + r) * S_ + b0;
+          float a0 = r == cc ? 1.0f : 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+#pragma unroll
+          for (int m = 0; m < r; m += 4) {
+            const float4 av = *reinterpret_cast<const float4*>(arow + m);
+            a0 = fmaf(-av.x, x[m], a0);
+            if (m + 1 < r) a1 = fmaf(-av.y, x[m + 1], a1);
+            if (m + 2 < r) a2 = fmaf(-av.z, x[m + 2], a2);
+            if (m + 3 < r) a3 = fmaf(-av.w, x[m + 3], a3);
+          }
+          x[r] = (a0 + a1) + (a2 + a3);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int r = 0; r < 16; ++r) sA[(b0 + r) * S_ + b0 + cc] = x[r];
+      }
+      named_bar(kBarPrep, kPrepThreads);
+      {  // Z = A10 D0 into sY rows 16 B .. 16 B + 15
+        const int Bq = ptid >> 7, r = (ptid >> 3) & 15, c0 = (ptid & 7) * 2;
+        const float* arow = sA + (32 * Bq + 16 + r) * S_ + 32 * Bq;
+        float z0 = 0.0f, z1 = 0.0f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          const float a = arow[m];
+          const float2 d = *reinterpret_cast<const float2*>(sA + (32 * Bq + m) * S_ + 32 * Bq + c0);
+          z0 = fmaf(a, d.x, z0);
+          z1 = fmaf(a, d.y, z1);
+        }
+        *reinterpret_cast<float2*>(sY + (16 * Bq + r) * SY + c0) = make_float2(z0, z1);
+      }
+      named_bar(kBarPrep, kPrepThreads);
+      {  // X = -D1 Z into the lower-left 16 x 16 block of each 32 x 32 diagonal block
+        const int Bq = ptid >> 7, r = (ptid >> 3) & 15, c0 = (ptid & 7) * 2;
+        const float* drow = sA + (32 * Bq + 16 + r) * S_ + 32 * Bq + 16;
+        float x0 = 0.0f, x1 = 0.0f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          const float d = drow[m];
+          const float2 z = *reinterpret_cast<const float2*>(sY + (16 * Bq + m) * SY + c0);
+          x0 = fmaf(d, z.x, x0);
+          x1 = fmaf(d, z.y, x1);
+        }
+        *reinterpret_cast<float2*>(sA + (32 * Bq + 16 + r) * S_ + 32 * Bq + c0) =
+            make_float2(-x0, -x1);
+      }
+      named_bar(kBarPrep, kPrepThreads);
+      const int bi = ptid >> 3, bj = (ptid & 7) * 4;
+      {  // Y = A21 T11
+        const float* arow = sA + (32 + bi) * S_;
+        float y[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int k = 0; k < 32; k += 4) {
+          const float4 a = *reinterpret_cast<const float4*>(arow + k);
+          const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 t = *reinterpret_cast<const float4*>(sA + (k + q) * S_ + bj);
+            y[0] = fmaf(av[q], t.x, y[0]);
+            y[1] = fmaf(av[q], t.y, y[1]);
+            y[2] = fmaf(av[q], t.z, y[2]);
+            y[3] = fmaf(av[q], t.w, y[3]);
+          }
+        }
+        *reinterpret_cast<float4*>(sY + bi * SY + bj) = make_float4(y[0], y[1], y[2], y[3]);
+      }
+      named_bar(kBarPrep, kPrepThreads);
+      {  // T21 = -T22 Y
+        const float* trow = sA + (32 + bi) * S_ + 32;
+        float y[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int k = 0; k < 32; k += 4) {
+          const float4 a = *reinterpret_cast<const float4*>(trow + k);
+          const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 t = *reinterpret_cast<const float4*>(sY + (k + q) * SY + bj);
+            y[0] = fmaf(av[q], t.x, y[0]);
+            y[1] = fmaf(av[q], t.y, y[1]);
+            y[2] = fmaf(av[q], t.z, y[2]);
+            y[3] = fmaf(av[q], t.w, y[3]);
+          }
+        }
+        *reinterpret_cast<float4*>(sA + (32 + bi) * S_ + bj) =
+            make_float4(-y[0], -y[1], -y[2], -y[3]);
+      }
+      // The P images: once D3 of the previous chunk has read them.
+      if (c >= 1) ok = wait_mb(MB(kMbD3), (c - 1) & 1, abort, p.status) && ok;
+      if (quad >= 2) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          const uint32_t off = swz128_offset(i, hf * 32 + e, 8192);
+          st_split8(sm + FusedSmem::PI + off, sm + FusedSmem::PI + 8192 + off, pv + e);
+        }
+      }
+      named_bar(kBarPrep, kPrepThreads);  // T complete, Y dead
+      // Tw = T diag(beta e^gam kn), Tu = T diag(beta) as hi + lo images.
+      for (int item = ptid; item < 64 * 8; item += kPrepThreads) {
+        const int r = item >> 3, q = item & 7;
+        float tw[8], tu[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float t = sA[r * S_ + 8 * q + e];
+          tw[e] = t * swj[8 * q + e];
+          tu[e] = t * suj[8 * q + e];
+        }
+        const uint32_t off = swz128_offset(r, 8 * q, 8192);
+        st_split8(sm + FusedSmem::TI + off, sm + FusedSmem::TI + 8192 + off, tw);
+        st_split8(sm + FusedSmem::TI + 16384 + off, sm + FusedSmem::TI + 24576 + off, tu);
+      }
+      fence_proxy_async();
+      ok = named_bar_and(kBarPrep, kPrepThreads, ok);
+      if (ptid == 0) {
+        mbar_arrive(MB(kMbTwTu));
+        mbar_arrive(MB(kMbPImg));
+      }
+      if (!ok) break;
+      // W^T (TMEM lanes = dk, 64 token columns) -> the -W^T image, MN-major B of D1.
+      ok = wait_mb(MB(kMbWu), c & 1, abort, p.status) && ok;
+      fence_after_sync();
+      {
+        float w[32];
+        tmem_ld32(tmem + kTG + lane_addr + hf * 32, w);
+        tmem_ld_wait();
+        const int dk = quad * 32 + lane;
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          float nv[8];
+#pragma unroll
+          for (int x = 0; x < 8; ++x) nv[x] = -w[e + x];
+          st_bf16x8(sm + FusedSmem::WV + swz128_offset(dk, hf * 32 + e, 16384), nv);
+        }
+      }
+      fence_proxy_async();
+      fence_before_sync();
+      ok = named_bar_and(kBarPrep, kPrepThreads, ok);
+      if (ptid == 0) {
+        mbar_arrive(MB(kMbWImg));
+        mbar_arrive(MB(kMbGFree));
+      }
+      if (!ok) break;
+    }
+  } else {
+    // ---------------------------------------------------------------- state chain
+    const int quad = warp & 3;
+    const int dv = quad * 32 + lane;
+    const bool lead = warp == 10 && lane == 0;
+    const uint32_t la = static_cast<uint32_t>(quad * 32) << 16;
+    float* prow = p.pool + (((int64_t)slot * p.Hv + h) * kD + dv) * kD;
+    const bool init = p.has_init == nullptr || __ldg(p.has_init + s) != 0;
+    bool ok = wait_mb(MB(kMbFac), 0, abort, p.status);
+    {
+      const float eL = fac[128];
+      for (int j = 0; j < kD; j += 16) {
+        float v[16];
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+          float4 f = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          if (init) f = *reinterpret_cast<const float4*>(prow + j + e);
+          v[e] = f.x;
+          v[e + 1] = f.y;
+          v[e + 2] = f.z;
+          v[e + 3] = f.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 16; e += 8) {
+          const uint32_t off = swz128_offset(dv, j + e, 16384);
+          st_split8(sm + FusedSmem::SH + off, sm + FusedSmem::SL + off, v + e);
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] *= eL;
+        tmem_st16(tmem + kTS + la + j, v);
+      }
+      tmem_st_wait();
+      fence_proxy_async();
+      fence_before_sync();
+    }
+    ok = named_bar_and(kBarScan, kScanThreads, ok);
+    if (lead) mbar_arrive(MB(kMbSImg));
+    for (int c = 0; c < nch && ok; ++c) {
+      const int t0 = lo + c * kC;
+      const int L = min(kC, hi - t0);
+      const float* F = fac + (c & 1) * FusedSmem::kFac;
+      // U^T = D1[:, 0:64] (Ut^T - W S^T); U'^T = U^T diag(fu) and U^T into TMEM
+      // as hi + lo bf16 pairs; fo (Q S^T)^T into D3 for the P U accumulation.
+      ok = wait_mb(MB(kMbD1), c & 1, abort, p.status) && ok;
+      fence_after_sync();
+#pragma unroll 1
+      for (int j = 0; j < kC; j += 16) {
+        float u[16], qs[16];
+        tmem_ld16(tmem + kTD1 + la + j, u);
+        tmem_ld16(tmem + kTD1 + 64 + la + j, qs);
+        tmem_ld_wait();
+        uint32_t u2h[8], u2l[8], uh[8], ul[8];
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+          split2(u[e] * F[64 + j + e], u[e + 1] * F[64 + j + e + 1], u2h[e / 2], u2l[e / 2]);
+          split2(u[e], u[e + 1], uh[e / 2], ul[e / 2]);
+          qs[e] *= F[j + e];
+          qs[e + 1] *= F[j + e + 1];
+        }
+        tmem_st8u(tmem + kTU2 + la + j / 2, u2h);
+        tmem_st8u(tmem + kTU2 + 32 + la + j / 2, u2l);
+        tmem_st8u(tmem + kTU + la + j / 2, uh);
+        tmem_st8u(tmem + kTU + 32 + la + j / 2, ul);
+        tmem_st16(tmem + kTD3 + la + j, qs);
+      }
+      tmem_st_wait();
+      fence_before_sync();
+      ok = named_bar_and(kBarScan, kScanThreads, ok);
+      if (lead) {
+        mbar_arrive(MB(kMbUReady));
+        mbar_arrive(MB(kMbD1Free));
+      }
+      if (!ok) break;
+      // S' = e^{gam_L} S + dS (in TMEM): its images for D1 of the next chunk,
+      // then S' e^{gam_L'} back (the next dS accumulates onto it); the last
+      // chunk's S' goes to the pool.
+      ok = wait_mb(MB(kMbD2), c & 1, abort, p.status) && ok;
+      const bool last = c + 1 == nch;
+      float eLn = 0.0f;
+      if (!last) {
+        ok = wait_mb(MB(kMbFac), (c + 1) & 1, abort, p.status) && ok;
+        eLn = fac[((c + 1) & 1) * FusedSmem::kFac + 128];
+      }
+      fence_after_sync();
+#pragma unroll 1
+      for (int j = 0; j < kD; j += 16) {
+        float v[16];
+        tmem_ld16(tmem + kTS + la + j, v);
+        tmem_ld_wait();
+        if (last) {
+#pragma unroll
+          for (int e = 0; e < 16; e += 4)
+            *reinterpret_cast<float4*>(prow + j + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; e += 8) {
+            const uint32_t off = swz128_offset(dv, j + e, 16384);
+            st_split8(sm + FusedSmem::SH + off, sm + FusedSmem::SL + off, v + e);
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] *= eLn;
+          tmem_st16(tmem + kTS + la + j, v);
+        }
+      }
+      if (!last) {
+        tmem_st_wait();
+        fence_proxy_async();
+      }
+      fence_before_sync();
+      ok = named_bar_and(kBarScan, kScanThreads, ok);
+      if (lead && !last) mbar_arrive(MB(kMbSImg));
+      if (!ok) break;
+      // Output rows of the chunk: O^T[dv, i] = D3 (fo Q S^T + P U).
+      ok = wait_mb(MB(kMbD3), c & 1, abort, p.status) && ok;
+      fence_after_sync();
+      __nv_bfloat16* ocol = out + ((int64_t)t0 * p.Hv + h) * kD + dv;
+#pragma unroll 1
+      for (int j = 0; j < kC; j += 16) {
+        float o[16];
+        tmem_ld16(tmem + kTD3 + la + j, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          if (j + e < L) ocol[(int64_t)(j + e) * p.Hv * kD] = __float2bfloat16_rn(o[e]);
+      }
+      fence_before_sync();
+    }
+  }
+
+  // ---- teardown: every thread arrives here exactly once --------------------
+  fence_before_sync();
+  __syncthreads();
+  if (*abort) {  // drain the MMAs in flight (their copies were drained by the loader)
+    if (warp == 1 && lane == 0) {
+      mma_commit(MB(kMbEnd));
+      mbar_wait(MB(kMbEnd), 0, kWaitBudget);
+    }
+    __syncthreads();
+  }
+  fence_after_sync();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+bool fused_supported(int Dk, int Dv, bool bf16) { return bf16 && Dk == kD && Dv == kD; }
+
+cudaError_t launch_fused(const RecurLaunch& p, cudaStream_t s) {
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, p.q, p.T, p.Hk) || !make_map(&tk, p.k, p.T, p.Hk) ||
+      !make_map(&tv, p.v, p.T, p.Hv))
+    return cudaErrorInvalidValue;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(fused_prefill_kernel,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    FusedSmem::BYTES + 1024);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const int64_t blocks = static_cast<int64_t>(p.N) * p.Hv;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  fused_prefill_kernel<<<static_cast<unsigned>(blocks), kThreads, FusedSmem::BYTES + 1024, s>>>(
+      tq, tk, tv, p);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

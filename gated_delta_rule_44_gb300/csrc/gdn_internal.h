@@ -124,6 +124,10 @@ struct ChunkedLaunch {
 };
 bool chunked_supported(int Dk, int Dv, bool bf16);
 
+// The same chunked form in one persistent launch (no workspace).
+bool fused_supported(int Dk, int Dv, bool bf16);
+cudaError_t launch_fused(const RecurLaunch& p, cudaStream_t s);
+
 // Gated RMSNorm of the recurrence output.
 struct NormLaunch {
   int64_t rows;   // tokens * heads

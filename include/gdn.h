@@ -89,9 +89,13 @@ typedef enum gdn_dtype {
 
 /* Which recurrence kernel gdn_prefill_varlen runs. */
 typedef enum gdn_prefill_algo {
-  GDN_PREFILL_AUTO = 0,      /* chunked when supported (bf16, Dk = Dv = 128), else recurrent */
-  GDN_PREFILL_CHUNKED = 1,   /* chunk-64 WY/UT form on tcgen05 tensor cores */
-  GDN_PREFILL_RECURRENT = 2  /* token-sequential recurrence on CUDA cores */
+  GDN_PREFILL_AUTO = 0,      /* fused chunked when supported (bf16, Dk = Dv = 128), else recurrent */
+  GDN_PREFILL_CHUNKED = 1,   /* chunk-64 WY/UT form on tcgen05 tensor cores, two launches that
+                                hand each chunk over through a caller workspace */
+  GDN_PREFILL_RECURRENT = 2, /* token-sequential recurrence on CUDA cores */
+  GDN_PREFILL_FUSED = 3      /* the chunk-64 form in one launch, one CTA per (sequence, value
+                                head) preparing the next chunk while it carries the state;
+                                needs no workspace */
 } gdn_prefill_algo;
 
 /* ---------------------------------------------------------------------------

@@ -161,6 +161,9 @@ def _declare(L):
     L.orc_validate_linear_attention_decode_prepare_shape.restype = ctypes.c_int
     L.orc_validate_linear_attention_decode_prepare_shape.argtypes = (
         [_i64] * 18 + [ctypes.c_char_p, ctypes.c_size_t])
+    L.orc_gdn_deviation_bound_f64.restype = ctypes.c_int
+    L.orc_gdn_deviation_bound_f64.argtypes = ([_vp] * 9 + [_i64, _vp, _vp, _vp] + [_i64] * 6
+                                              + [ctypes.c_double, _vp, ctypes.c_int])
     L.orc_validate_cu_seqlens.restype = ctypes.c_int
     L.orc_validate_cu_seqlens.argtypes = [_vp, _i64, _i64, ctypes.c_char_p, ctypes.c_size_t]
     L.orc_validate_prepare_cu_seqlens.restype = ctypes.c_int
@@ -354,6 +357,29 @@ def _recur_inputs(q, k, v, g, beta, dtype):
     T, Hk, Dk = q.shape
     _, Hv, Dv = v.shape
     return q, k, v, g, beta, T, Hk, Dk, Hv, Dv
+
+
+def gdn_deviation_bound(q, k, v, g, beta, dq, dk, dv, state_pool, cu_seqlens, scale,
+                        state_indices=None, has_initial_state=None, nthreads=0):
+    """Test aid: a first-order bound [T, Hv, Dv] on how far each output of O2
+    moves when the stored q, k, v move by at most dq, dk, dv (f64; the state
+    pool is only read)."""
+    q, k, v, g, beta, T, Hk, Dk, Hv, Dv = _recur_inputs(q, k, v, g, beta, np.float64)
+    dq = _arr(dq, np.float64, "dq")
+    dk = _arr(dk, np.float64, "dk")
+    dv = _arr(dv, np.float64, "dv")
+    pool = np.ascontiguousarray(state_pool, dtype=np.float64)
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    si = None if state_indices is None else np.ascontiguousarray(state_indices, dtype=np.int32)
+    hi = None if has_initial_state is None else np.ascontiguousarray(has_initial_state,
+                                                                     dtype=np.uint8)
+    bound = np.zeros((T, Hv, Dv), np.float64)
+    rc = _load().orc_gdn_deviation_bound_f64(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(dq), _ptr(dk), _ptr(dv),
+        _ptr(pool), pool.shape[0], _ptr(si), _ptr(hi), _ptr(cu), cu.size - 1, T, Hk, Hv, Dk, Dv,
+        float(scale), _ptr(bound), int(nthreads))
+    _check(rc, "gdn_deviation_bound")
+    return bound
 
 
 def gdn_varlen(q, k, v, g, beta, state_pool, cu_seqlens, scale, state_indices=None,

@@ -416,6 +416,64 @@ int varlen_impl(const R* q, const R* k, const R* v, const R* g, const R* beta, R
   return ORC_OK;
 }
 
+// ---- Deviation bound of O2 under moved inputs (test aid, f64) ---------------
+// When the stored q, k, v of the recurrence move by at most dq, dk, dv
+// (elementwise), how far can each output move, to first order?  O2 is
+//   S_t = a S_{t-1} (I - b k k^T) + b v k^T,   o_t = scale S_t q,   a = e^g, b = beta,
+// so, to first order in the moves, row c of the state moves by
+//   dS_t[c] = a dS_{t-1}[c] (I - b k k^T) + b dv_c k^T - a b (S_{t-1}[c].dk) k^T
+//             + b (v_c - a S_{t-1}[c].k) dk^T
+// and the output by do_t[c] = scale (dS_t[c].q + S_t[c].dq).  With
+// |I - b k k^T|_2 = max(1, |1 - b |k|^2|) this gives the row-norm bound
+//   r_t[c] = a r_{t-1}[c] max(1, |1 - b|k|^2|)
+//            + b (dv_c |k| + a sum_d |S_{t-1}[c][d]| dk_d |k| + |v_c - a S_{t-1}[c].k| |dk|)
+//   |do_t[c]| <= scale (r_t[c] |q| + sum_d |S_t[c][d]| dq_d),
+// run alongside the recurrence itself (same loop order as head_chain, no
+// in-loop norm).  The state pool is read, not written.
+void deviation_chain(const double* q, const double* k, const double* v, const double* g,
+                     const double* beta, const double* dq, const double* dk_, const double* dv_,
+                     std::vector<double>& S, int64_t t0, int64_t t1, int64_t h, int64_t hk,
+                     int64_t hk_n, int64_t hv_n, int64_t dk, int64_t dv, double scale,
+                     double* bound) {
+  std::vector<double> r(dv, 0.0);
+  for (int64_t t = t0; t < t1; ++t) {
+    const double* qt = q + (t * hk_n + hk) * dk;
+    const double* kt = k + (t * hk_n + hk) * dk;
+    const double* dqt = dq + (t * hk_n + hk) * dk;
+    const double* dkt = dk_ + (t * hk_n + hk) * dk;
+    double nq = 0.0, nk = 0.0, ndk = 0.0;
+    for (int64_t d = 0; d < dk; ++d) {
+      nq += qt[d] * qt[d];
+      nk += kt[d] * kt[d];
+      ndk += dkt[d] * dkt[d];
+    }
+    const double a = std::exp(g[t * hv_n + h]), b = beta[t * hv_n + h];
+    const double shrink = std::max(1.0, std::fabs(1.0 - b * nk));
+    nq = std::sqrt(nq);
+    nk = std::sqrt(nk);
+    ndk = std::sqrt(ndk);
+    for (int64_t c = 0; c < dv; ++c) {
+      double* row = S.data() + c * dk;
+      double sk = 0.0, kv = 0.0;
+      for (int64_t d = 0; d < dk; ++d) {
+        sk += std::fabs(row[d]) * dkt[d];
+        row[d] *= a;
+        kv += row[d] * kt[d];
+      }
+      const double vc = v[(t * hv_n + h) * dv + c];
+      const double delta = (vc - kv) * b;
+      double sq = 0.0;
+      for (int64_t d = 0; d < dk; ++d) {
+        row[d] += delta * kt[d];
+        sq += std::fabs(row[d]) * dqt[d];
+      }
+      r[c] = a * r[c] * shrink +
+             b * (dv_[(t * hv_n + h) * dv + c] * nk + a * sk * nk + std::fabs(vc - kv) * ndk);
+      bound[(t * hv_n + h) * dv + c] = scale * (r[c] * nq + sq);
+    }
+  }
+}
+
 // ---- O7: speculative multi-token decode ([cpu_ops.cpp] GdnSpecDecodeKernel) --
 // Request i owns tokens [cu[i], cu[i+1]) and a row of num_cols pool slots.  Its
 // state starts from slot sidx[i][num_accepted[i] - 1] (the snapshot after the
@@ -913,6 +971,38 @@ int orc_gdn_varlen_f64(ORC_RECUR_PARAMS(double)) {
                              has_initial_state, cu_seqlens, n_seqs, tokens, key_heads,
                              value_heads, key_dim, value_dim, scale, use_qk_l2norm, items,
                              n_items, out, nthreads);
+}
+
+int orc_gdn_deviation_bound_f64(const double* q, const double* k, const double* v,
+                                const double* g, const double* beta, const double* dq,
+                                const double* dk, const double* dv, const double* state_pool,
+                                int64_t state_slots, const int32_t* state_indices,
+                                const uint8_t* has_initial_state, const int32_t* cu_seqlens,
+                                int64_t n_seqs, int64_t tokens, int64_t key_heads,
+                                int64_t value_heads, int64_t key_dim, int64_t value_dim,
+                                double scale, double* bound, int nthreads) {
+  if (n_seqs <= 0 || tokens <= 0 || key_heads <= 0 || value_heads <= 0 || key_dim <= 0 ||
+      value_dim <= 0 || value_heads % key_heads != 0)
+    return ORC_ERR_SHAPE;
+  if (int rc = check_cu(cu_seqlens, n_seqs, tokens, nullptr, 0)) return rc;
+  if (int rc = check_slots(state_indices, n_seqs, state_slots, nullptr, 0)) return rc;
+  const int64_t ratio = value_heads / key_heads, state_len = value_dim * key_dim;
+  parallel_items(n_seqs * value_heads, nthreads, [&](int64_t item) {
+    const int64_t s = item / value_heads, h = item % value_heads;
+    const int64_t slot = state_indices != nullptr ? state_indices[s] : s;
+    if (slot < 0) {  // padded: outputs are zeros on both sides
+      for (int64_t t = cu_seqlens[s]; t < cu_seqlens[s + 1]; ++t)
+        for (int64_t c = 0; c < value_dim; ++c) bound[(t * value_heads + h) * value_dim + c] = 0.0;
+      return;
+    }
+    std::vector<double> S(state_len, 0.0);
+    if (has_initial_state == nullptr || has_initial_state[s] != 0)
+      for (int64_t e = 0; e < state_len; ++e)
+        S[e] = state_pool[(slot * value_heads + h) * state_len + e];
+    deviation_chain(q, k, v, g, beta, dq, dk, dv, S, cu_seqlens[s], cu_seqlens[s + 1], h,
+                    h / ratio, key_heads, value_heads, key_dim, value_dim, scale, bound);
+  });
+  return ORC_OK;
 }
 
 int orc_kda_varlen_f32(ORC_RECUR_PARAMS(float)) {

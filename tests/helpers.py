@@ -18,6 +18,16 @@ f32 tensors (state, g, beta) use the plain metric.  Every bf16 comparison also
 reports and bounds rms(gpu - ref)/rms(ref), the plain metric averaged, so that
 a systematic one-quantum bias cannot hide under the exemption.
 
+End to end (prepare, then the recurrence, from raw inputs) the same holds one
+step earlier: q, k and v are stored in bf16 between the two steps, and where
+the path's and the oracle's f32 values straddle a rounding boundary the two
+stored values differ by one step, which the recurrence carries into the
+outputs (measured on the oracle alone: flipping the near-boundary q or k
+values of a D = 128 head moves outputs by up to 3e-2 of their rms).
+stored_flip_bound bounds this from the oracle's own values, with the
+oracle's first-order deviation bound of the recurrence, and the end-to-end
+tests add it to the exemption.
+
 Oracle inputs come only from the workload generator (bf16 values widened
 exactly to f32) or from the oracle's own earlier steps (rounded to bf16 where
 the path stores bf16), never from the CUDA path.
@@ -52,15 +62,20 @@ def bf16_quantum(xq: np.ndarray) -> np.ndarray:
     return np.where(a > 0, np.exp2(e - 7), 0.0)
 
 
-def rel_err_stored_bf16(gpu, ref) -> float:
-    """max(|gpu - bf16(ref)| - one bf16 quantum, 0) / rms(ref)."""
+def rel_err_stored_bf16(gpu, ref, extra=None) -> float:
+    """max(|gpu - bf16(ref)| - one bf16 quantum - extra, 0) / rms(ref); `extra`
+    (same shape, default 0) is a per-element allowance such as
+    stored_flip_bound's."""
     gpu = np.asarray(gpu, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert gpu.shape == ref.shape, (gpu.shape, ref.shape)
     if ref.size == 0:
         return 0.0
     rq = bf16_round(ref)
-    excess = np.maximum(np.abs(gpu - rq) - bf16_quantum(rq), 0.0)
+    excess = np.abs(gpu - rq) - bf16_quantum(rq)
+    if extra is not None:
+        excess -= np.asarray(extra, dtype=np.float64)
+    excess = np.maximum(excess, 0.0)
     rms = float(np.sqrt((ref ** 2).mean()))
     return float(excess.max()) / rms if rms > 0 else float(excess.max())
 
@@ -90,13 +105,54 @@ def rms_rel_err(gpu, ref) -> float:
     return d / rms if rms > 0 else d
 
 
-def assert_close(gpu, ref, tol, what="", stored_bf16=False):
+def bf16_flip(x):
+    """For each value x, its bf16 rounding r, the neighbouring bf16 value nb on
+    the side of x, and |x - (r + nb) / 2|, its distance from the rounding
+    boundary between them (computed on the bf16 bit patterns, so binade
+    edges are exact).  Zeros and exact bf16 values get nb = r."""
+    x = np.asarray(x, dtype=np.float64)
+    r = bf16_round(x)
+    bits = (r.astype(np.float32).view(np.uint32) >> 16).astype(np.int64)
+    up = x > r                       # x lies above its rounding
+    away = np.where(r > 0, up, ~up)  # toward larger magnitude
+    step = np.where(x == r, 0, np.where(away, 1, -1))
+    step = np.where(r == 0, 0, step)
+    nb = ((bits + step).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    dist = np.abs(x - 0.5 * (r + nb))
+    return r, nb, dist
+
+
+def stored_flip_bound(prep, cu_seqlens, scale, state_pool, state_indices=None,
+                      has_initial_state=None, margin=1.0 / 32):
+    """Allowance for outputs computed end to end from raw inputs, where q, k
+    and v are stored in bf16 between the prepare and the recurrence by two
+    different f32 evaluations of the same prepare (the path's and the
+    oracle's).  Where the oracle's f32 value lies within `margin` of a bf16
+    step of a rounding boundary, the other evaluation may store the
+    neighbouring value; every other stored value is the same on both sides.
+    Returns the oracle's first-order bound (oracle.gdn_deviation_bound) on
+    how far those one-step moves can carry each output of the recurrence."""
+    rounded, moves = {}, {}
+    for key in ("q", "k", "v"):
+        r, nb, dist = bf16_flip(prep[key])
+        step = np.abs(nb - r)
+        rounded[key] = r
+        moves[key] = np.where((step > 0) & (dist <= margin * step), step, 0.0)
+    return oracle.gdn_deviation_bound(
+        rounded["q"], rounded["k"], rounded["v"], prep["g"], prep["beta"], moves["q"],
+        moves["k"], moves["v"], state_pool, cu_seqlens, scale, state_indices=state_indices,
+        has_initial_state=has_initial_state)
+
+
+def assert_close(gpu, ref, tol, what="", stored_bf16=False, extra=None):
     """Plain metric for f32 tensors; the storage-rounding metric (see the module
     docstring) for tensors the path stores in bf16, which must also keep
-    rms(err)/rms(ref) within the tolerance.  Returns the error."""
+    rms(err)/rms(ref) within the tolerance.  `extra`: a per-element allowance
+    added to the one-quantum exemption (stored_flip_bound).  Returns the
+    error."""
     assert np.all(np.isfinite(np.asarray(gpu, dtype=np.float64))), f"{what}: non-finite"
     if stored_bf16:
-        e = rel_err_stored_bf16(gpu, ref)
+        e = rel_err_stored_bf16(gpu, ref, extra)
         e_plain = rel_err(gpu, ref)
         e_rms = rms_rel_err(gpu, ref)
         print(f"{what}: max(|err| - 1 bf16 quantum)/rms(ref) {e:.3e}, plain max|err|/rms "

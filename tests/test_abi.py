@@ -128,10 +128,15 @@ def test_prefill_cu_seqlens_messages():
 
 def test_prefill_workspace_rules():
     algo = B.gdn_prefill_resolve_algo(128, 128, B.GDN_DTYPE_BF16, B.GDN_PREFILL_AUTO)
-    assert algo in (B.GDN_PREFILL_CHUNKED, B.GDN_PREFILL_RECURRENT)
+    assert algo == B.GDN_PREFILL_FUSED
     assert B.gdn_prefill_resolve_algo(32, 32, B.GDN_DTYPE_F32, B.GDN_PREFILL_AUTO) == \
         B.GDN_PREFILL_RECURRENT
     assert B.gdn_prefill_workspace_bytes(100, 2, 4, 32, 32, B.GDN_DTYPE_F32) == 0
+    # the fused form needs no workspace; an unknown algorithm is rejected
+    assert B.gdn_prefill_workspace_bytes(4096, 1, 32, 128, 128, B.GDN_DTYPE_BF16) == 0
+    assert call_prefill(prefill_args(algo=4))[0] == B.GDN_ERR_INVALID_ARGUMENT
+    rc, msg = call_prefill(prefill_args(Dk=64, Dv=64, algo=B.GDN_PREFILL_FUSED))
+    assert rc == B.GDN_ERR_UNSUPPORTED and "fused" in msg
     need = B.gdn_prefill_workspace_bytes(4096, 1, 32, 128, 128, B.GDN_DTYPE_BF16,
                                          B.GDN_PREFILL_CHUNKED)
     if need > 0:

@@ -1,7 +1,8 @@
 """GPU parity of gdn_prefill_varlen against the oracle's sequential recurrence (O2).
 
-Both algorithms (chunked tensor-core form where supported, token-sequential
-recurrent form everywhere) are checked on: ragged varlen batches whose lengths
+Every algorithm (the chunked tensor-core form in one fused launch and in two
+launches with a workspace, where supported, and the token-sequential recurrent
+form everywhere) is checked on: ragged varlen batches whose lengths
 straddle the chunk size (1, 63, 64, 65, 127, 128, 129, ...), padding slots,
 has_initial_state mixes, GQA ratios, f32 and bf16, in-kernel q/k norm, the
 weak-decay twins (slow decay, so a wrong carried state is not hidden), and the
@@ -21,14 +22,15 @@ from gated_delta_rule_44_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
-ALGOS = (B.GDN_PREFILL_RECURRENT, B.GDN_PREFILL_CHUNKED)
+ALGOS = (B.GDN_PREFILL_RECURRENT, B.GDN_PREFILL_CHUNKED, B.GDN_PREFILL_FUSED)
 
 
 def algo_ok(algo, w):
+    """The tensor-core algorithms are built for bf16 with Dk = Dv = 128."""
     if algo == B.GDN_PREFILL_RECURRENT:
         return True
     dt = B.GDN_DTYPE_BF16 if w.act_dtype == torch.bfloat16 else B.GDN_DTYPE_F32
-    return B.gdn_prefill_resolve_algo(w.Dk, w.Dv, dt, B.GDN_PREFILL_AUTO) == B.GDN_PREFILL_CHUNKED
+    return B.gdn_prefill_resolve_algo(w.Dk, w.Dv, dt, B.GDN_PREFILL_AUTO) == B.GDN_PREFILL_FUSED
 
 
 def run_prefill(w, dev, algo, seqs=None, heads=None, norm=False, scale=-1.0, host=True):
