@@ -693,7 +693,8 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": workload_config(w, ws),
-            "prefill_algo": B.gdn_prefill_resolve_algo(w.Dk, w.Dv, 1, args.algo),
+            "prefill_algo": B.gdn_prefill_resolve_algo(w.N - w.n_decode, w.Hv, w.Dk, w.Dv, 1,
+                                                       args.algo),
             "roofline": roof, "kernels": kernels, "gpu_launches": res["launches"],
             "clocks": res["clocks"]}
     if rank == 0 and not args.no_extra:

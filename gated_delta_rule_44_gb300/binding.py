@@ -137,7 +137,8 @@ EXPORTED = ("gdn_prepare", "gdn_decode", "gdn_prefill_varlen", "gdn_kda_varlen",
             "gdn_spec_prepare", "gdn_spec_decode", "gdn_packed_decode", "gdn_gated_rmsnorm",
             "gdn_prefill_workspace_bytes",
             "gdn_prefill_resolve_algo", "gdn_status_string", "gdn_last_error_message",
-            "gdn_read_device_status", "gdn_version", "gdn_launch_count", "gdn_validate_mixed")
+            "gdn_read_device_status", "gdn_version", "gdn_launch_count", "gdn_validate_mixed",
+            "gdn_check_wait_timeout")
 
 
 class GdnError(RuntimeError):
@@ -172,10 +173,12 @@ def lib() -> ctypes.CDLL:
             L.gdn_packed_decode.argtypes = [ctypes.POINTER(gdn_packed_decode_args), _vp]
             L.gdn_read_device_status.argtypes = [_vp]
             L.gdn_validate_mixed.argtypes = [ctypes.POINTER(gdn_mixed_meta)]
+            L.gdn_check_wait_timeout.restype = ctypes.c_int
+            L.gdn_check_wait_timeout.argtypes = [ctypes.c_longlong, _vp]
             L.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
             L.gdn_prefill_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64, _i64, _i32, _i32]
             L.gdn_prefill_resolve_algo.restype = _i32
-            L.gdn_prefill_resolve_algo.argtypes = [_i64, _i64, _i32, _i32]
+            L.gdn_prefill_resolve_algo.argtypes = [_i64, _i64, _i64, _i64, _i32, _i32]
             L.gdn_status_string.restype = ctypes.c_char_p
             L.gdn_status_string.argtypes = [ctypes.c_int]
             L.gdn_last_error_message.restype = ctypes.c_char_p
@@ -384,8 +387,9 @@ def gdn_prefill_workspace_bytes(T, N, Hv, Dk, Dv, act_dtype=GDN_DTYPE_BF16,
     return int(lib().gdn_prefill_workspace_bytes(T, N, Hv, Dk, Dv, act_dtype, algo))
 
 
-def gdn_prefill_resolve_algo(Dk, Dv, act_dtype=GDN_DTYPE_BF16, algo=GDN_PREFILL_AUTO) -> int:
-    return int(lib().gdn_prefill_resolve_algo(Dk, Dv, act_dtype, algo))
+def gdn_prefill_resolve_algo(N, Hv, Dk, Dv, act_dtype=GDN_DTYPE_BF16,
+                             algo=GDN_PREFILL_AUTO) -> int:
+    return int(lib().gdn_prefill_resolve_algo(N, Hv, Dk, Dv, act_dtype, algo))
 
 
 def gdn_prefill_varlen(q, k, v, g, beta, state, cu_seqlens, out, *, scale=-1.0,
@@ -455,6 +459,12 @@ def gdn_validate_mixed(*, num_decodes, num_prefills, num_actual_tokens, state_sl
 def gdn_read_device_status(stream=None) -> None:
     """Synchronises the stream and raises GdnError if a kernel flagged an error."""
     _check(lib().gdn_read_device_status(_stream(stream)))
+
+
+def gdn_check_wait_timeout(budget_cycles: int, stream=None) -> None:
+    """include/gdn.h gdn_check_wait_timeout: one bounded device wait that runs
+    out on purpose; gdn_read_device_status then raises GDN_ERR_TIMEOUT."""
+    _check(lib().gdn_check_wait_timeout(int(budget_cycles), _stream(stream)))
 
 
 def gdn_version() -> int:

@@ -736,16 +736,28 @@ int gdn_validate_mixed(const gdn_mixed_meta* m) {
   return succeed();
 }
 
-int32_t gdn_prefill_resolve_algo(int64_t Dk, int64_t Dv, int32_t act_dtype, int32_t algo) {
+// AUTO: the tensor-core forms for bf16 with Dk = Dv = 128, else the recurrent
+// one.  The fused form keeps one (sequence, value head) chain per SM and
+// prepares its chunks inside it; with fewer chains than SMs the two-launch
+// form, which prepares every chunk of every chain in parallel first, is the
+// faster of the two.
+int32_t gdn_prefill_resolve_algo(int64_t N, int64_t Hv, int64_t Dk, int64_t Dv, int32_t act_dtype,
+                                 int32_t algo) {
   if (algo != GDN_PREFILL_AUTO) return algo;
-  return gdn::fused_supported((int)Dk, (int)Dv, act_dtype == GDN_DTYPE_BF16)
-             ? GDN_PREFILL_FUSED
-             : GDN_PREFILL_RECURRENT;
+  if (!gdn::fused_supported((int)Dk, (int)Dv, act_dtype == GDN_DTYPE_BF16))
+    return GDN_PREFILL_RECURRENT;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    sms = 152;
+  }
+  return N * Hv >= sms ? GDN_PREFILL_FUSED : GDN_PREFILL_CHUNKED;
 }
 
 size_t gdn_prefill_workspace_bytes(int64_t T, int64_t N, int64_t Hv, int64_t Dk, int64_t Dv,
                                    int32_t act_dtype, int32_t algo) {
-  if (gdn_prefill_resolve_algo(Dk, Dv, act_dtype, algo) != GDN_PREFILL_CHUNKED) return 0;
+  if (gdn_prefill_resolve_algo(N, Hv, Dk, Dv, act_dtype, algo) != GDN_PREFILL_CHUNKED) return 0;
   if (T <= 0 || N <= 0 || Hv <= 0) return 0;
   return gdn::chunked_workspace_bytes(T, N, Hv, Dk, Dv);
 }
@@ -770,7 +782,7 @@ int gdn_prefill_varlen(const gdn_prefill_args* a, void* stream) {
     if (int rc = check_indices_host(a->state_indices_host, a->N, a->state_slots)) return rc;
   if (a->state_indices == nullptr && a->N > a->state_slots)
     return fail(GDN_ERR_SHAPE, "gated_delta_rule state has fewer slots than sequences");
-  const int32_t algo = gdn_prefill_resolve_algo(a->Dk, a->Dv, a->act_dtype, a->algo);
+  const int32_t algo = gdn_prefill_resolve_algo(a->N, a->Hv, a->Dk, a->Dv, a->act_dtype, a->algo);
   gdn::RecurLaunch p{};
   p.T = (int)a->T;
   p.N = (int)a->N;

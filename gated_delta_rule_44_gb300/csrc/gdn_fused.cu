@@ -22,7 +22,8 @@
 //   D1   = V^T Tu^T - S W^T | S Q^T   (M = 128 dv, N = 64 + 64)
 //          so D1[:, 0:64] = U^T and D1[:, 64:128] = (Q S^T)^T directly
 //   dS   = U'^T K   onto  e^{gam_L} S (M = 128 dv, N = 128 dk), U' = diag(fu) U
-//   D3   = U^T P^T  onto  (fo Q S^T)^T (M = 128 dv, N = 64 tokens)
+//   O^T  = U^T P^T  onto  (fo Q S^T)^T, in place in D1's second half
+//          (M = 128 dv, N = 64 tokens)
 // U'^T and U^T enter the tensor core from TMEM (A operand in tensor memory),
 // the f32 state lives in TMEM as dS's accumulator, its hi + lo bf16 images in
 // shared memory as D1's A operand.
@@ -38,10 +39,10 @@
 //               the region W^T(c - 1) held once D1(c - 1) has read it
 //   warp 1      every MMA, issued in dependency order as their inputs appear
 //   warps 2-9   prep of chunk c: norms, gates, A and P from G, T by 16 x 16
-//               blocks, the Tw / Tu / P images, the W^T image
-//   warps 10-13 the state chain of chunk c: U from D1 (U', U into TMEM and
-//               fo Q S^T into D3), the state update S' and its images, the
-//               output rows
+//               blocks, the Tw / Tu / P images
+//   warps 10-13 the state chain of chunk c: the W^T image, U from D1 (U', U
+//               into TMEM, fo Q S^T in place), the state update S' and its
+//               images, the output rows
 // Prep of chunk c + 1 overlaps the chain of chunk c.  Every hand-off is an
 // mbarrier; every wait is bounded and, once any wait gives up, every role
 // leaves at its next wait, in-flight copies and MMAs are drained (bounded) and
@@ -83,16 +84,18 @@ struct FusedSmem {
   static constexpr uint32_t GB = AT + 64 * kAStride * 4;  // g, beta, gam, kn, qn, wj, uj
   static constexpr uint32_t FAC = GB + 7 * 64 * 4;        // 2 x {fo[64], fu[64], e^{gam_L}, 0, 0, 0}
   static constexpr uint32_t kFac = 132;                   // floats per factor buffer
-  static constexpr uint32_t BYTES = FAC + 2 * kFac * 4;
+  static constexpr uint32_t OST = FAC + 2 * kFac * 4;     // output staging [32 tok][128 dv] bf16
+  static constexpr uint32_t BYTES = OST + 32 * 128 * 2;
 };
 static_assert(FusedSmem::BYTES + 1024 + 1024 <= 232448, "shared memory per CTA");
 static_assert(32 * FusedSmem::kYStride * 4 <= 8192, "Y fits in the Tw hi image space");
 
 // TMEM columns (512 allocated).
-constexpr uint32_t kTG = 0;     // G = [K;Q] K^T, then W^T (64)
-constexpr uint32_t kTD1 = 64;   // D1: U^T | (Q S^T)^T (128)
-constexpr uint32_t kTS = 192;   // f32 state S[dv][dk], dS accumulates onto it (128)
-constexpr uint32_t kTD3 = 320;  // output accumulator O^T (64)
+constexpr uint32_t kTG = 0;     // G = [K;Q] K^T (64)
+constexpr uint32_t kTW = 64;    // W^T (64)
+constexpr uint32_t kTD1 = 128;  // D1: U^T | (Q S^T)^T, the second half then fo-scaled and the
+                                // output accumulator O^T (128)
+constexpr uint32_t kTS = 256;   // f32 state S[dv][dk], dS accumulates onto it (128)
 constexpr uint32_t kTU2 = 384;  // U'^T hi | lo as packed bf16 pairs (32 + 32)
 constexpr uint32_t kTU = 448;   // U^T hi | lo (32 + 32)
 
@@ -103,8 +106,8 @@ constexpr int kBarPrep = 1;
 constexpr int kBarScan = 2;
 
 enum Mb : int {
-  kMbKq0 = 0, kMbKq1, kMbKqFree0, kMbKqFree1, kMbV, kMbG, kMbGFree, kMbTwTu, kMbWu, kMbWImg,
-  kMbPImg, kMbFac, kMbD1, kMbD1Free, kMbUReady, kMbSImg, kMbD2, kMbD3, kMbEnd, kNumMb
+  kMbKq0 = 0, kMbKq1, kMbKqFree0, kMbKqFree1, kMbV, kMbG, kMbGRead, kMbTwTu, kMbWu, kMbWImg,
+  kMbPImg, kMbFac, kMbD1, kMbD1Free, kMbUReady, kMbSImg, kMbD2, kMbD3, kMbOFree, kMbEnd, kNumMb
 };
 
 // D (+)= A[tmem] * B[smem]: the A operand in tensor memory (M = 128 lanes, K
@@ -124,6 +127,26 @@ __device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&v)[8]
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr),
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+      : "memory");
+}
+
+// 32 lanes x 32 columns of 32-bit values from registers.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(
+          taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
       : "memory");
 }
 
@@ -242,13 +265,15 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
       const uint32_t id_d1q = idesc_bf16_f32(128, 64, false, false);
       const uint32_t id_d2 = idesc_bf16_f32(128, 128, false, true);
       const uint32_t id_d3 = idesc_bf16_f32(128, 64, false, false);
+      // Chunks whose MMAs of each group have been issued, in priority order:
+      // D2 + D3 (the state chain and the output), D1, the prep's W / Ut, G.
       int cg = 0, cwu = 0, cd1 = 0, cd23 = 0;
       long long last = clock64();
       while (cd23 < nch) {
         if (*abort) break;
         bool went = false;
-        if (cd23 < cd1 && mbar_try_wait(MB(kMbUReady), cd23 & 1) &&
-            mbar_try_wait(MB(kMbPImg), cd23 & 1)) {
+        if (cd23 < cd1 && mbar_test_wait(MB(kMbUReady), cd23 & 1) &&
+            mbar_test_wait(MB(kMbPImg), cd23 & 1)) {
           fence_after_sync();
           const int c = cd23;
           const uint32_t st = base + FusedSmem::KQ + (c & 1) * FusedSmem::kStage;
@@ -261,25 +286,28 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
                           desc_sw128(st + (kk / 8) * 1024, 16384, 1024), id_d2, true);
           mma_commit(MB(kMbD2));
           mma_commit(MB(kMbKqFree0 + (c & 1)));
-          // O^T += U^T P^T: hi*hi, hi*lo, lo*hi  (A = U^T from TMEM; B = P, K-major)
+          // O^T += U^T P^T onto fo (Q S^T)^T: hi*hi, hi*lo, lo*hi (A = U^T from TMEM;
+          // B = P, K-major)
 #pragma unroll
           for (int pr = 0; pr < 3; ++pr) {
             const uint32_t ua = kTU + (pr == 2 ? 32 : 0);
             const uint32_t pb = base + FusedSmem::PI + (pr == 1 ? 8192 : 0);
 #pragma unroll
             for (int kk = 0; kk < kC; kk += 16)
-              mma_bf16_ta(tmem + kTD3, tmem + ua + kk / 2, desc_sw128(pb + kk * 2, 16, 1024),
-                          id_d3, true);
+              mma_bf16_ta(tmem + kTD1 + 64, tmem + ua + kk / 2,
+                          desc_sw128(pb + kk * 2, 16, 1024), id_d3, true);
           }
           mma_commit(MB(kMbD3));
           ++cd23;
           went = true;
-        } else if (cd1 < cwu && mbar_try_wait(MB(kMbWImg), cd1 & 1) &&
-                   mbar_try_wait(MB(kMbSImg), cd1 & 1)) {
+        } else if (cd1 < cwu && mbar_test_wait(MB(kMbWImg), cd1 & 1) &&
+                   mbar_test_wait(MB(kMbSImg), cd1 & 1) &&
+                   (cd1 == 0 || mbar_test_wait(MB(kMbOFree), (cd1 - 1) & 1))) {
           fence_after_sync();
           const int c = cd1;
           const uint32_t st = base + FusedSmem::KQ + (c & 1) * FusedSmem::kStage;
-          // D1[:, 0:64] += S (-W)^T onto Ut^T;  D1[:, 64:128] = S Q^T.  A = S hi, lo.
+          // D1[:, 0:64] += S (-W)^T onto Ut^T;  D1[:, 64:128] = S Q^T (the previous
+          // chunk's output rows have been read).  A = S hi, lo.
 #pragma unroll
           for (int part = 0; part < 2; ++part)
 #pragma unroll
@@ -287,8 +315,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
               const uint64_t a = desc_sw128(base + (part ? FusedSmem::SL : FusedSmem::SH) +
                                                 (kk / 64) * 16384 + (kk % 64) * 2,
                                             16, 1024);
-              mma_bf16(tmem + kTD1, a, desc_sw128(base + FusedSmem::WV + (kk / 8) * 1024, 8192, 1024),
-                       id_d1w, true);
+              mma_bf16(tmem + kTD1, a,
+                       desc_sw128(base + FusedSmem::WV + (kk / 8) * 1024, 8192, 1024), id_d1w,
+                       true);
               mma_bf16(tmem + kTD1 + 64, a,
                        desc_sw128(st + 8192 + (kk / 64) * 16384 + (kk % 64) * 2, 16, 1024),
                        id_d1q, part > 0 || kk > 0);
@@ -296,9 +325,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
           mma_commit(MB(kMbD1));
           ++cd1;
           went = true;
-        } else if (cwu < cg && mbar_try_wait(MB(kMbTwTu), cwu & 1) &&
-                   mbar_try_wait(MB(kMbV), cwu & 1) &&
-                   (cwu == 0 || mbar_try_wait(MB(kMbD1Free), (cwu - 1) & 1))) {
+        } else if (cwu < cg && mbar_test_wait(MB(kMbTwTu), cwu & 1) &&
+                   mbar_test_wait(MB(kMbV), cwu & 1) &&
+                   (cwu == 0 || mbar_test_wait(MB(kMbD1Free), (cwu - 1) & 1))) {
           fence_after_sync();
           const int c = cwu;
           const uint32_t st = base + FusedSmem::KQ + (c & 1) * FusedSmem::kStage;
@@ -307,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
           for (int part = 0; part < 2; ++part)
 #pragma unroll
             for (int kk = 0; kk < kC; kk += 16)
-              mma_bf16(tmem + kTG, desc_sw128(st + (kk / 8) * 1024, 16384, 1024),
+              mma_bf16(tmem + kTW, desc_sw128(st + (kk / 8) * 1024, 16384, 1024),
                        desc_sw128(base + FusedSmem::TI + part * 8192 + kk * 2, 16, 1024), id_wu,
                        part > 0 || kk > 0);
           // Ut^T = V^T Tu^T into D1[:, 0:64] (A = V, MN-major, M = dv).
@@ -321,8 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
           mma_commit(MB(kMbWu));
           ++cwu;
           went = true;
-        } else if (cg < nch && mbar_try_wait(MB(kMbKq0 + (cg & 1)), (cg >> 1) & 1) &&
-                   (cg == 0 || mbar_try_wait(MB(kMbGFree), (cg - 1) & 1))) {
+        } else if (cg < nch && mbar_test_wait(MB(kMbKq0 + (cg & 1)), (cg >> 1) & 1) &&
+                   (cg == 0 || mbar_test_wait(MB(kMbGRead), (cg - 1) & 1))) {
           fence_after_sync();
           const uint32_t st = base + FusedSmem::KQ + (cg & 1) * FusedSmem::kStage;
           // G = [K; Q] K^T  (M = 128, N = 64, K = 128)
@@ -371,6 +400,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
       }
     };
     if (ptid < 64) load_gates(0);
+    float pv[32];  // this thread's P values (P-row warps) until the images go out
+    const int i = (quad & 1) * 32 + lane;
     for (int c = 0; c < nch; ++c) {
       const uint8_t* sst = sm + FusedSmem::KQ + (c & 1) * FusedSmem::kStage;
       float* F = fac + (c & 1) * FusedSmem::kFac;
@@ -430,11 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
       ok = wait_mb(MB(kMbG), c & 1, abort, p.status) && ok;
       fence_after_sync();
       // Lanes 0..63 of G hold K K^T -> A (f32, shared); lanes 64..127 hold
-      // Q K^T -> P (kept in registers until the previous chunk's D3 has read
-      // the P images).  Row i, columns 32 hf ... 32 hf + 31.
-      const int i = (quad & 1) * 32 + lane;
+      // Q K^T -> P.  Row i, columns 32 hf ... 32 hf + 31.
       const bool upper = (quad & 1) == 0 && hf == 1;  // rows 0..31 x columns 32..63: zero
-      float pv[32];
       {
         float v[32];
         if (!upper) {
@@ -483,12 +511,14 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
         }
       }
       fence_before_sync();
-      named_bar(kBarPrep, kPrepThreads);  // A complete; G read (W^T may reuse its columns)
+      named_bar(kBarPrep, kPrepThreads);  // A complete; G read: the next chunk's G may go
+      if (ptid == 0) mbar_arrive(MB(kMbGRead));
       // T = (I + A)^-1 by blocks: the four 16 x 16 diagonal blocks by forward
-      // substitution (prep warps 0..1, lane = column), the two 32 x 32
-      // diagonal blocks from them (X = -D1 A10 D0), then T21 = -T22 (A21 T11).
-      if (pw < 2) {
-        const int b0 = 16 * (2 * pw + (lane >> 4)), cc = lane & 15;
+      // substitution (the two A-row warps of column half 0, lane = column),
+      // the two 32 x 32 diagonal blocks from them (X = -D1 A10 D0), then
+      // T21 = -T22 (A21 T11).
+      if (quad < 2 && hf == 0) {
+        const int b0 = 16 * (2 * quad + (lane >> 4)), cc = lane & 15;
         float x[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
@@ -508,6 +538,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
 #pragma unroll
         for (int r = 0; r < 16; ++r) sA[(b0 + r) * S_ + b0 + cc] = x[r];
       }
+      // Y lives in the Tw / Tu image space: the previous chunk's W and Ut
+      // MMAs must have read it.
+      if (c >= 1) ok = wait_mb(MB(kMbWu), (c - 1) & 1, abort, p.status) && ok;
       named_bar(kBarPrep, kPrepThreads);
       {  // Z = A10 D0 into sY rows 16 B .. 16 B + 15
         const int Bq = ptid >> 7, r = (ptid >> 3) & 15, c0 = (ptid & 7) * 2;
@@ -577,18 +610,20 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
         *reinterpret_cast<float4*>(sA + (32 + bi) * S_ + bj) =
             make_float4(-y[0], -y[1], -y[2], -y[3]);
       }
-      // The P images: once D3 of the previous chunk has read them.
-      if (c >= 1) ok = wait_mb(MB(kMbD3), (c - 1) & 1, abort, p.status) && ok;
+      named_bar(kBarPrep, kPrepThreads);  // T complete, Y dead
+      // The P-row warps store the P images (once D3 of the previous chunk has
+      // read them); the A-row warps store Tw = T diag(beta e^gam kn) and
+      // Tu = T diag(beta) as hi + lo images.
       if (quad >= 2) {
+        if (c >= 1) ok = wait_mb(MB(kMbD3), (c - 1) & 1, abort, p.status) && ok;
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
           const uint32_t off = swz128_offset(i, hf * 32 + e, 8192);
           st_split8(sm + FusedSmem::PI + off, sm + FusedSmem::PI + 8192 + off, pv + e);
         }
       }
-      named_bar(kBarPrep, kPrepThreads);  // T complete, Y dead
-      // Tw = T diag(beta e^gam kn), Tu = T diag(beta) as hi + lo images.
-      for (int item = ptid; item < 64 * 8; item += kPrepThreads) {
+      const int atid = (quad & 1) * 32 + lane + hf * 64;  // 0..127 over the A-row warps
+      for (int item = atid; item < 64 * 8 && quad < 2; item += 128) {
         const int r = item >> 3, q = item & 7;
         float tw[8], tu[8];
 #pragma unroll
@@ -606,30 +641,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
       if (ptid == 0) {
         mbar_arrive(MB(kMbTwTu));
         mbar_arrive(MB(kMbPImg));
-      }
-      if (!ok) break;
-      // W^T (TMEM lanes = dk, 64 token columns) -> the -W^T image, MN-major B of D1.
-      ok = wait_mb(MB(kMbWu), c & 1, abort, p.status) && ok;
-      fence_after_sync();
-      {
-        float w[32];
-        tmem_ld32(tmem + kTG + lane_addr + hf * 32, w);
-        tmem_ld_wait();
-        const int dk = quad * 32 + lane;
-#pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          float nv[8];
-#pragma unroll
-          for (int x = 0; x < 8; ++x) nv[x] = -w[e + x];
-          st_bf16x8(sm + FusedSmem::WV + swz128_offset(dk, hf * 32 + e, 16384), nv);
-        }
-      }
-      fence_proxy_async();
-      fence_before_sync();
-      ok = named_bar_and(kBarPrep, kPrepThreads, ok);
-      if (ptid == 0) {
-        mbar_arrive(MB(kMbWImg));
-        mbar_arrive(MB(kMbGFree));
       }
       if (!ok) break;
     }
@@ -670,33 +681,63 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
     }
     ok = named_bar_and(kBarScan, kScanThreads, ok);
     if (lead) mbar_arrive(MB(kMbSImg));
+    // Per chunk: the W^T image (D1 waits), U (D2 and D3 wait), the state update
+    // (the next D1 waits), the output rows (the next D1's Q half waits).
     for (int c = 0; c < nch && ok; ++c) {
       const int t0 = lo + c * kC;
       const int L = min(kC, hi - t0);
       const float* F = fac + (c & 1) * FusedSmem::kFac;
+      // W^T (TMEM lanes = dk, 64 token columns) -> the -W^T image, the MN-major
+      // B operand of this chunk's D1 (V, which shared the space, is consumed).
+      ok = wait_mb(MB(kMbWu), c & 1, abort, p.status) && ok;
+      fence_after_sync();
+#pragma unroll 1
+      for (int j0 = 0; j0 < kC; j0 += 32) {
+        float w[32];
+        tmem_ld32(tmem + kTW + la + j0, w);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          float nv[8];
+#pragma unroll
+          for (int x = 0; x < 8; ++x) nv[x] = -w[e + x];
+          st_bf16x8(sm + FusedSmem::WV + swz128_offset(dv, j0 + e, 16384), nv);
+        }
+      }
+      fence_proxy_async();
+      fence_before_sync();
+      ok = named_bar_and(kBarScan, kScanThreads, ok);
+      if (lead) mbar_arrive(MB(kMbWImg));
+      if (!ok) break;
       // U^T = D1[:, 0:64] (Ut^T - W S^T); U'^T = U^T diag(fu) and U^T into TMEM
-      // as hi + lo bf16 pairs; fo (Q S^T)^T into D3 for the P U accumulation.
+      // as hi + lo bf16 pairs; D1[:, 64:128] scaled in place to fo (Q S^T)^T,
+      // onto which P U accumulates.  Two rounds of 32 token columns.
       ok = wait_mb(MB(kMbD1), c & 1, abort, p.status) && ok;
       fence_after_sync();
 #pragma unroll 1
-      for (int j = 0; j < kC; j += 16) {
-        float u[16], qs[16];
-        tmem_ld16(tmem + kTD1 + la + j, u);
-        tmem_ld16(tmem + kTD1 + 64 + la + j, qs);
+      for (int j0 = 0; j0 < kC; j0 += 32) {
+        float u[32], qs[32];
+        tmem_ld32(tmem + kTD1 + la + j0, u);
+        tmem_ld32(tmem + kTD1 + 64 + la + j0, qs);
         tmem_ld_wait();
-        uint32_t u2h[8], u2l[8], uh[8], ul[8];
 #pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          split2(u[e] * F[64 + j + e], u[e + 1] * F[64 + j + e + 1], u2h[e / 2], u2l[e / 2]);
-          split2(u[e], u[e + 1], uh[e / 2], ul[e / 2]);
-          qs[e] *= F[j + e];
-          qs[e + 1] *= F[j + e + 1];
+        for (int j1 = 0; j1 < 32; j1 += 16) {
+          const int j = j0 + j1;
+          uint32_t u2h[8], u2l[8], uh[8], ul[8];
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            split2(u[j1 + e] * F[64 + j + e], u[j1 + e + 1] * F[64 + j + e + 1], u2h[e / 2],
+                   u2l[e / 2]);
+            split2(u[j1 + e], u[j1 + e + 1], uh[e / 2], ul[e / 2]);
+          }
+          tmem_st8u(tmem + kTU2 + la + j / 2, u2h);
+          tmem_st8u(tmem + kTU2 + 32 + la + j / 2, u2l);
+          tmem_st8u(tmem + kTU + la + j / 2, uh);
+          tmem_st8u(tmem + kTU + 32 + la + j / 2, ul);
         }
-        tmem_st8u(tmem + kTU2 + la + j / 2, u2h);
-        tmem_st8u(tmem + kTU2 + 32 + la + j / 2, u2l);
-        tmem_st8u(tmem + kTU + la + j / 2, uh);
-        tmem_st8u(tmem + kTU + 32 + la + j / 2, ul);
-        tmem_st16(tmem + kTD3 + la + j, qs);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) qs[e] *= F[j0 + e];
+        tmem_st32(tmem + kTD1 + 64 + la + j0, qs);
       }
       tmem_st_wait();
       fence_before_sync();
@@ -718,23 +759,24 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
       }
       fence_after_sync();
 #pragma unroll 1
-      for (int j = 0; j < kD; j += 16) {
-        float v[16];
-        tmem_ld16(tmem + kTS + la + j, v);
+      for (int j0 = 0; j0 < kD; j0 += 32) {
+        float v[32];
+        tmem_ld32(tmem + kTS + la + j0, v);
         tmem_ld_wait();
         if (last) {
 #pragma unroll
-          for (int e = 0; e < 16; e += 4)
-            *reinterpret_cast<float4*>(prow + j + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(prow + j0 + e) =
+                make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
         } else {
 #pragma unroll
-          for (int e = 0; e < 16; e += 8) {
-            const uint32_t off = swz128_offset(dv, j + e, 16384);
+          for (int e = 0; e < 32; e += 8) {
+            const uint32_t off = swz128_offset(dv, j0 + e, 16384);
             st_split8(sm + FusedSmem::SH + off, sm + FusedSmem::SL + off, v + e);
           }
 #pragma unroll
-          for (int e = 0; e < 16; ++e) v[e] *= eLn;
-          tmem_st16(tmem + kTS + la + j, v);
+          for (int e = 0; e < 32; ++e) v[e] *= eLn;
+          tmem_st32(tmem + kTS + la + j0, v);
         }
       }
       if (!last) {
@@ -745,20 +787,38 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
       ok = named_bar_and(kBarScan, kScanThreads, ok);
       if (lead && !last) mbar_arrive(MB(kMbSImg));
       if (!ok) break;
-      // Output rows of the chunk: O^T[dv, i] = D3 (fo Q S^T + P U).
+      // Output rows of the chunk: O^T[dv, i] = fo Q S^T + P U, then the
+      // columns are free for the next chunk's D1.
       ok = wait_mb(MB(kMbD3), c & 1, abort, p.status) && ok;
       fence_after_sync();
-      __nv_bfloat16* ocol = out + ((int64_t)t0 * p.Hv + h) * kD + dv;
+      {
+        // 32 tokens at a time through the staging rows: each thread writes its
+        // dv of every token, then the rows leave as 16-byte vectors.
+        __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + FusedSmem::OST);
+        const int stid = tid - 320;  // 0..127
 #pragma unroll 1
-      for (int j = 0; j < kC; j += 16) {
-        float o[16];
-        tmem_ld16(tmem + kTD3 + la + j, o);
-        tmem_ld_wait();
+        for (int j0 = 0; j0 < kC && j0 < L; j0 += 32) {
+          float o[32];
+          tmem_ld32(tmem + kTD1 + 64 + la + j0, o);
+          tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          if (j + e < L) ocol[(int64_t)(j + e) * p.Hv * kD] = __float2bfloat16_rn(o[e]);
+          for (int e = 0; e < 32; ++e) ost[e * kD + dv] = __float2bfloat16_rn(o[e]);
+          named_bar(kBarScan, kScanThreads);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int idx = q * kScanThreads + stid;  // 16-byte vector: token idx / 16
+            const int r = idx >> 4, c16 = idx & 15;
+            if (j0 + r < L)
+              *reinterpret_cast<uint4*>(out + ((int64_t)(t0 + j0 + r) * p.Hv + h) * kD + c16 * 8) =
+                  *reinterpret_cast<const uint4*>(ost + r * kD + c16 * 8);
+          }
+          named_bar(kBarScan, kScanThreads);
+        }
       }
       fence_before_sync();
+      ok = named_bar_and(kBarScan, kScanThreads, ok);
+      if (lead) mbar_arrive(MB(kMbOFree));
+      if (!ok) break;
     }
   }
 

@@ -9,8 +9,11 @@
 #include <atomic>
 #include <cstdint>
 #include <mutex>
+#include <string>
 
+#include "../../include/gdn.h"
 #include "gdn_internal.h"
+#include "tcgen05.cuh"
 
 namespace {
 __device__ unsigned g_status_word;
@@ -43,3 +46,34 @@ unsigned* status_word() {
 }
 
 }  // namespace gdn
+
+namespace {
+
+// One thread waits, with the library's bounded wait, on an mbarrier that
+// nothing ever arrives on; when the budget runs out it records the timeout in
+// the status word, exactly as the kernels do when one of their waits gives
+// up.  Nothing else is issued, so nothing is in flight when it returns.
+__global__ void wait_timeout_kernel(unsigned* status, long long budget) {
+  __shared__ uint64_t mbar;
+  const uint32_t mb = gdn::umma::smem_u32(&mbar);
+  gdn::umma::mbar_init(mb, 1);
+  gdn::umma::fence_mbar_init();
+  if (!gdn::umma::mbar_wait(mb, 0, budget)) atomicOr(status, gdn::kStatusTimeout);
+}
+
+}  // namespace
+
+extern "C" int gdn_check_wait_timeout(long long budget_cycles, void* stream) {
+  if (budget_cycles <= 0 || budget_cycles > 2000000000LL)
+    return gdn::report_error(GDN_ERR_INVALID_ARGUMENT,
+                             "budget_cycles must be in (0, 2e9] (about one second)");
+  unsigned* w = gdn::status_word();
+  if (w == nullptr) return gdn::report_error(GDN_ERR_CUDA, "device status word unavailable");
+  wait_timeout_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(w, budget_cycles);
+  gdn::note_launch();
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess)
+    return gdn::report_error(GDN_ERR_CUDA,
+                             (std::string("gdn_check_wait_timeout: ") + cudaGetErrorString(e)).c_str());
+  return gdn::report_error(GDN_OK, "");
+}

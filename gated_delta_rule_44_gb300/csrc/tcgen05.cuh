@@ -182,6 +182,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t mbar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test of a phase (try_wait may suspend the thread for a while
+// before it returns false; test_wait returns at once): for polling several
+// barriers from one thread.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t mbar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(mbar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait: gives up after ~`budget` cycles and returns false.
 __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, long long budget) {
   if (mbar_try_wait(mbar, parity)) return true;

@@ -89,7 +89,8 @@ typedef enum gdn_dtype {
 
 /* Which recurrence kernel gdn_prefill_varlen runs. */
 typedef enum gdn_prefill_algo {
-  GDN_PREFILL_AUTO = 0,      /* fused chunked when supported (bf16, Dk = Dv = 128), else recurrent */
+  GDN_PREFILL_AUTO = 0,      /* a chunked form when supported (bf16, Dk = Dv = 128), else
+                                recurrent: see gdn_prefill_resolve_algo */
   GDN_PREFILL_CHUNKED = 1,   /* chunk-64 WY/UT form on tcgen05 tensor cores, two launches that
                                 hand each chunk over through a caller workspace */
   GDN_PREFILL_RECURRENT = 2, /* token-sequential recurrence on CUDA cores */
@@ -577,12 +578,18 @@ typedef struct gdn_mixed_meta {
 int gdn_validate_mixed(const gdn_mixed_meta* meta);
 
 /* Scratch bytes gdn_prefill_varlen needs for these sizes and algorithm (0 for
- * the recurrent algorithm).  Depends only on the arguments. */
+ * the recurrent and fused algorithms).  With GDN_PREFILL_AUTO it depends on
+ * the current device too (gdn_prefill_resolve_algo). */
 size_t gdn_prefill_workspace_bytes(int64_t T, int64_t N, int64_t Hv, int64_t Dk, int64_t Dv,
                                    int32_t act_dtype, int32_t algo);
 
-/* The algorithm GDN_PREFILL_AUTO resolves to for these sizes. */
-int32_t gdn_prefill_resolve_algo(int64_t Dk, int64_t Dv, int32_t act_dtype, int32_t algo);
+/* The algorithm GDN_PREFILL_AUTO resolves to for these sizes on the current
+ * device: for bf16 with Dk = Dv = 128 the fused form when there are at least
+ * as many (sequence, value head) chains (N * Hv) as SMs, else the two-launch
+ * chunked form; the recurrent form otherwise.  Other values of algo are
+ * returned as given. */
+int32_t gdn_prefill_resolve_algo(int64_t N, int64_t Hv, int64_t Dk, int64_t Dv, int32_t act_dtype,
+                                 int32_t algo);
 
 /* Static text for a status code. */
 const char* gdn_status_string(int status);
@@ -593,6 +600,16 @@ const char* gdn_last_error_message(void);
 /* Synchronises `stream`, then returns (and clears) the current device's
  * status word: GDN_OK, GDN_ERR_DEVICE_CHECK or GDN_ERR_TIMEOUT. */
 int gdn_read_device_status(void* stream);
+
+/* Diagnostic of the device-side failure path (the pages have no
+ * counterpart): launches one thread that waits, with the same bounded wait
+ * every kernel here uses, on an mbarrier that nothing ever arrives on.  After
+ * about budget_cycles SM clocks (at most 2e9, about a second) the wait gives
+ * up and records GDN_ERR_TIMEOUT in the device status word, as a kernel
+ * whose copy or MMA never completed would; nothing else is in flight, and the
+ * context stays usable.  Read the result with gdn_read_device_status().
+ * Returns GDN_ERR_INVALID_ARGUMENT for a budget outside (0, 2e9]. */
+int gdn_check_wait_timeout(long long budget_cycles, void* stream);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int gdn_version(void);

@@ -163,7 +163,7 @@ def _declare(L):
         [_i64] * 18 + [ctypes.c_char_p, ctypes.c_size_t])
     L.orc_gdn_deviation_bound_f64.restype = ctypes.c_int
     L.orc_gdn_deviation_bound_f64.argtypes = ([_vp] * 9 + [_i64, _vp, _vp, _vp] + [_i64] * 6
-                                              + [ctypes.c_double, _vp, ctypes.c_int])
+                                              + [ctypes.c_double, _vp, _vp, ctypes.c_int])
     L.orc_validate_cu_seqlens.restype = ctypes.c_int
     L.orc_validate_cu_seqlens.argtypes = [_vp, _i64, _i64, ctypes.c_char_p, ctypes.c_size_t]
     L.orc_validate_prepare_cu_seqlens.restype = ctypes.c_int
@@ -360,10 +360,12 @@ def _recur_inputs(q, k, v, g, beta, dtype):
 
 
 def gdn_deviation_bound(q, k, v, g, beta, dq, dk, dv, state_pool, cu_seqlens, scale,
-                        state_indices=None, has_initial_state=None, nthreads=0):
+                        state_indices=None, has_initial_state=None, nthreads=0,
+                        with_state=False):
     """Test aid: a first-order bound [T, Hv, Dv] on how far each output of O2
     moves when the stored q, k, v move by at most dq, dk, dv (f64; the state
-    pool is only read)."""
+    pool is only read).  With with_state, also a bound [slots, Hv, Dv] on every
+    element of each row of the live sequences' final states (0 elsewhere)."""
     q, k, v, g, beta, T, Hk, Dk, Hv, Dv = _recur_inputs(q, k, v, g, beta, np.float64)
     dq = _arr(dq, np.float64, "dq")
     dk = _arr(dk, np.float64, "dk")
@@ -374,12 +376,13 @@ def gdn_deviation_bound(q, k, v, g, beta, dq, dk, dv, state_pool, cu_seqlens, sc
     hi = None if has_initial_state is None else np.ascontiguousarray(has_initial_state,
                                                                      dtype=np.uint8)
     bound = np.zeros((T, Hv, Dv), np.float64)
+    sbound = np.zeros((pool.shape[0], Hv, Dv), np.float64) if with_state else None
     rc = _load().orc_gdn_deviation_bound_f64(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(dq), _ptr(dk), _ptr(dv),
         _ptr(pool), pool.shape[0], _ptr(si), _ptr(hi), _ptr(cu), cu.size - 1, T, Hk, Hv, Dk, Dv,
-        float(scale), _ptr(bound), int(nthreads))
+        float(scale), _ptr(bound), _ptr(sbound), int(nthreads))
     _check(rc, "gdn_deviation_bound")
-    return bound
+    return (bound, sbound) if with_state else bound
 
 
 def gdn_varlen(q, k, v, g, beta, state_pool, cu_seqlens, scale, state_indices=None,

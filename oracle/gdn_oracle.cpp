@@ -429,12 +429,14 @@ int varlen_impl(const R* q, const R* k, const R* v, const R* g, const R* beta, R
 //            + b (dv_c |k| + a sum_d |S_{t-1}[c][d]| dk_d |k| + |v_c - a S_{t-1}[c].k| |dk|)
 //   |do_t[c]| <= scale (r_t[c] |q| + sum_d |S_t[c][d]| dq_d),
 // run alongside the recurrence itself (same loop order as head_chain, no
-// in-loop norm).  The state pool is read, not written.
+// in-loop norm).  The state pool is read, not written.  The final r[c] bounds
+// every element of row c of the final state (|x_d| <= |x|), written to
+// state_bound when it is given.
 void deviation_chain(const double* q, const double* k, const double* v, const double* g,
                      const double* beta, const double* dq, const double* dk_, const double* dv_,
                      std::vector<double>& S, int64_t t0, int64_t t1, int64_t h, int64_t hk,
                      int64_t hk_n, int64_t hv_n, int64_t dk, int64_t dv, double scale,
-                     double* bound) {
+                     double* bound, double* state_bound) {
   std::vector<double> r(dv, 0.0);
   for (int64_t t = t0; t < t1; ++t) {
     const double* qt = q + (t * hk_n + hk) * dk;
@@ -472,6 +474,8 @@ void deviation_chain(const double* q, const double* k, const double* v, const do
       bound[(t * hv_n + h) * dv + c] = scale * (r[c] * nq + sq);
     }
   }
+  if (state_bound != nullptr)
+    for (int64_t c = 0; c < dv; ++c) state_bound[c] = r[c];
 }
 
 // ---- O7: speculative multi-token decode ([cpu_ops.cpp] GdnSpecDecodeKernel) --
@@ -980,7 +984,8 @@ int orc_gdn_deviation_bound_f64(const double* q, const double* k, const double* 
                                 const uint8_t* has_initial_state, const int32_t* cu_seqlens,
                                 int64_t n_seqs, int64_t tokens, int64_t key_heads,
                                 int64_t value_heads, int64_t key_dim, int64_t value_dim,
-                                double scale, double* bound, int nthreads) {
+                                double scale, double* bound, double* state_bound,
+                                int nthreads) {
   if (n_seqs <= 0 || tokens <= 0 || key_heads <= 0 || value_heads <= 0 || key_dim <= 0 ||
       value_dim <= 0 || value_heads % key_heads != 0)
     return ORC_ERR_SHAPE;
@@ -1000,7 +1005,10 @@ int orc_gdn_deviation_bound_f64(const double* q, const double* k, const double* 
       for (int64_t e = 0; e < state_len; ++e)
         S[e] = state_pool[(slot * value_heads + h) * state_len + e];
     deviation_chain(q, k, v, g, beta, dq, dk, dv, S, cu_seqlens[s], cu_seqlens[s + 1], h,
-                    h / ratio, key_heads, value_heads, key_dim, value_dim, scale, bound);
+                    h / ratio, key_heads, value_heads, key_dim, value_dim, scale, bound,
+                    state_bound != nullptr
+                        ? state_bound + (slot * value_heads + h) * value_dim
+                        : nullptr);
   });
   return ORC_OK;
 }

@@ -74,7 +74,9 @@ int orc_validate_linear_attention_decode_prepare_shape(
 /* Test aid, f64: a first-order bound on how far each output of O2 can move
  * when the stored q, k, v move by at most dq, dk, dv (elementwise, same
  * shapes as q, k, v).  q and k are taken as stored (no in-loop norm); the
- * state pool is only read.  bound [T, Hv, Dv]. */
+ * state pool is only read.  bound [T, Hv, Dv]; state_bound (optional,
+ * [slots, Hv, Dv]) bounds every element of each row of each live sequence's
+ * final state. */
 int orc_gdn_deviation_bound_f64(const double* q, const double* k, const double* v,
                                 const double* g, const double* beta, const double* dq,
                                 const double* dk, const double* dv, const double* state_pool,
@@ -82,7 +84,8 @@ int orc_gdn_deviation_bound_f64(const double* q, const double* k, const double* 
                                 const uint8_t* has_initial_state, const int32_t* cu_seqlens,
                                 int64_t n_seqs, int64_t tokens, int64_t key_heads,
                                 int64_t value_heads, int64_t key_dim, int64_t value_dim,
-                                double scale, double* bound, int nthreads);
+                                double scale, double* bound, double* state_bound,
+                                int nthreads);
 /* [cpu.rs] recurrent_gated_delta_rule_varlen_f32: cu_seqlens starts at 0, ends
  * at total_tokens, every range non-empty and increasing. */
 int orc_validate_cu_seqlens(const int32_t* cu_seqlens, int64_t batch, int64_t total_tokens,

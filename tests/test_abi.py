@@ -127,13 +127,18 @@ def test_prefill_cu_seqlens_messages():
 
 
 def test_prefill_workspace_rules():
-    algo = B.gdn_prefill_resolve_algo(128, 128, B.GDN_DTYPE_BF16, B.GDN_PREFILL_AUTO)
-    assert algo == B.GDN_PREFILL_FUSED
-    assert B.gdn_prefill_resolve_algo(32, 32, B.GDN_DTYPE_F32, B.GDN_PREFILL_AUTO) == \
+    # many chains: the fused form; few: the two-launch chunked form (no GPU
+    # here: the SM count defaults to 152)
+    assert B.gdn_prefill_resolve_algo(4, 64, 128, 128, B.GDN_DTYPE_BF16) == B.GDN_PREFILL_FUSED
+    assert B.gdn_prefill_resolve_algo(1, 32, 128, 128, B.GDN_DTYPE_BF16) == B.GDN_PREFILL_CHUNKED
+    assert B.gdn_prefill_resolve_algo(4, 64, 32, 32, B.GDN_DTYPE_F32) == \
         B.GDN_PREFILL_RECURRENT
+    assert B.gdn_prefill_resolve_algo(1, 32, 128, 128, B.GDN_DTYPE_BF16,
+                                      B.GDN_PREFILL_FUSED) == B.GDN_PREFILL_FUSED
     assert B.gdn_prefill_workspace_bytes(100, 2, 4, 32, 32, B.GDN_DTYPE_F32) == 0
     # the fused form needs no workspace; an unknown algorithm is rejected
-    assert B.gdn_prefill_workspace_bytes(4096, 1, 32, 128, 128, B.GDN_DTYPE_BF16) == 0
+    assert B.gdn_prefill_workspace_bytes(8192, 4, 64, 128, 128, B.GDN_DTYPE_BF16) == 0
+    assert B.gdn_prefill_workspace_bytes(4096, 1, 32, 128, 128, B.GDN_DTYPE_BF16) > 0
     assert call_prefill(prefill_args(algo=4))[0] == B.GDN_ERR_INVALID_ARGUMENT
     rc, msg = call_prefill(prefill_args(Dk=64, Dv=64, algo=B.GDN_PREFILL_FUSED))
     assert rc == B.GDN_ERR_UNSUPPORTED and "fused" in msg

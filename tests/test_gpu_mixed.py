@@ -35,9 +35,9 @@ def run_mixed(w, dev, seqs, heads):
     # Where the path's and the oracle's f32 q, k, v may round to neighbouring
     # bf16 values, the outputs may differ by that step carried through the
     # recurrence: the oracle bounds it (tests/helpers.py, stored_flip_bound).
-    extra = H.stored_flip_bound(ref_prep, w.cu_seqlens.numpy(), 1.0 / np.sqrt(w.Dk), cpool,
-                                state_indices=remap,
-                                has_initial_state=w.has_initial_state.numpy())
+    extra, extra_state = H.stored_flip_bound(ref_prep, w.cu_seqlens.numpy(), 1.0 / np.sqrt(w.Dk),
+                                             cpool, state_indices=remap,
+                                             has_initial_state=w.has_initial_state.numpy())
     # the path stores q, k, v in bf16 between the two steps, as the pages do
     for key in ("q", "k", "v"):
         ref_prep[key] = H.bf16_round(ref_prep[key]).astype(np.float32)
@@ -55,7 +55,8 @@ def run_mixed(w, dev, seqs, heads):
     gp = d["state_pool"]
     live = [s for s in seqs if remap[s] >= 0]
     e_state = H.assert_close_blocks(
-        ((H.f32(gp[int(w.state_indices[s])][heads]), cpool[remap[s]][heads]) for s in live),
+        ((H.f32(gp[int(w.state_indices[s])][heads]), cpool[remap[s]][heads],
+          extra_state[remap[s]][heads][..., None]) for s in live),
         tol, "state")
     np.testing.assert_array_equal(H.f32(d["conv_pool"]), ref_conv)
     return e_out, e_state

@@ -30,7 +30,7 @@ def algo_ok(algo, w):
     if algo == B.GDN_PREFILL_RECURRENT:
         return True
     dt = B.GDN_DTYPE_BF16 if w.act_dtype == torch.bfloat16 else B.GDN_DTYPE_F32
-    return B.gdn_prefill_resolve_algo(w.Dk, w.Dv, dt, B.GDN_PREFILL_AUTO) == B.GDN_PREFILL_FUSED
+    return B.gdn_prefill_resolve_algo(w.N, w.Hv, w.Dk, w.Dv, dt) != B.GDN_PREFILL_RECURRENT
 
 
 def run_prefill(w, dev, algo, seqs=None, heads=None, norm=False, scale=-1.0, host=True):

@@ -48,14 +48,15 @@ def _prepared(weak, seed, D=16, seqlens=(70, 1, 130)):
     return w, {k: v.astype(np.float64) for k, v in prep.items()}
 
 
-def _run(w, prep, **over):
+def _run(w, prep, with_pool=False, **over):
     import oracle
     x = dict(prep, **over)
     pool = w.state_pool.numpy().astype(np.float64).copy()
-    return oracle.gdn_varlen(x["q"], x["k"], x["v"], x["g"], x["beta"], pool,
-                             w.cu_seqlens.numpy(), 1.0 / np.sqrt(w.Dk),
-                             state_indices=w.state_indices.numpy(),
-                             has_initial_state=w.has_initial_state.numpy(), dtype=np.float64)
+    out = oracle.gdn_varlen(x["q"], x["k"], x["v"], x["g"], x["beta"], pool,
+                            w.cu_seqlens.numpy(), 1.0 / np.sqrt(w.Dk),
+                            state_indices=w.state_indices.numpy(),
+                            has_initial_state=w.has_initial_state.numpy(), dtype=np.float64)
+    return (out, pool) if with_pool else out
 
 
 @pytest.mark.parametrize("weak", [False, True])
@@ -75,18 +76,23 @@ def test_deviation_bound_holds_and_is_tight(weak, which):
         m = np.where(rng.random(x.shape) < 0.03, step, 0.0) if key in which else np.zeros_like(x)
         moves[key] = m
         over[key] = x + m * rng.choice([-1.0, 1.0], size=x.shape)
-    o1 = _run(w, prep)
-    o2 = _run(w, prep, **over)
-    bound = oracle.gdn_deviation_bound(prep["q"], prep["k"], prep["v"], prep["g"], prep["beta"],
-                                       moves["q"], moves["k"], moves["v"],
-                                       w.state_pool.numpy().astype(np.float64),
-                                       w.cu_seqlens.numpy(), 1.0 / np.sqrt(w.Dk),
-                                       state_indices=w.state_indices.numpy(),
-                                       has_initial_state=w.has_initial_state.numpy())
+    o1, s1 = _run(w, prep, with_pool=True)
+    o2, s2 = _run(w, prep, with_pool=True, **over)
+    bound, sbound = oracle.gdn_deviation_bound(
+        prep["q"], prep["k"], prep["v"], prep["g"], prep["beta"], moves["q"], moves["k"],
+        moves["v"], w.state_pool.numpy().astype(np.float64), w.cu_seqlens.numpy(),
+        1.0 / np.sqrt(w.Dk), state_indices=w.state_indices.numpy(),
+        has_initial_state=w.has_initial_state.numpy(), with_state=True)
     moved = np.abs(o2 - o1)
     assert np.all(moved <= bound * 1.01 + 1e-15)
     live = bound > 1e-12
     assert (moved[live] / bound[live]).max() > 0.2
+    # the final states: every element of a row within the row's bound
+    smoved = np.abs(s2 - s1)
+    assert np.all(smoved <= sbound[..., None] * 1.01 + 1e-15)
+    if which != "q":  # q does not enter the state
+        rows = sbound > 1e-12
+        assert (smoved.max(axis=-1)[rows] / sbound[rows]).max() > 0.05
 
 
 def test_deviation_bound_is_zero_without_moves_and_linear_in_them():
