@@ -73,6 +73,11 @@ class gdn_spec_prepare_args(ctypes.Structure):
                 ("num_accepted_host", _vp)]
 
 
+class gdn_out_norm(ctypes.Structure):
+    _fields_ = [("z", _vp), ("z_len", _i64), ("z_token_stride", _i64), ("weight", _vp),
+                ("weight_len", _i64), ("eps", _f32), ("sigmoid_gate", _i32)]
+
+
 class gdn_decode_args(ctypes.Structure):
     _fields_ = [("B", _i64), ("Hk", _i64), ("Hv", _i64), ("Dk", _i64), ("Dv", _i64),
                 ("act_dtype", _i32), ("use_qk_l2norm", _i32), ("scale", _f32),
@@ -80,7 +85,7 @@ class gdn_decode_args(ctypes.Structure):
                 ("v_len", _i64), ("g", _vp), ("g_len", _i64), ("beta", _vp), ("beta_len", _i64),
                 ("state", _vp), ("state_slots", _i64), ("state_len", _i64),
                 ("state_indices", _vp), ("state_indices_host", _vp),
-                ("out", _vp), ("out_len", _i64)]
+                ("out", _vp), ("out_len", _i64), ("out_norm", ctypes.POINTER(gdn_out_norm))]
 
 
 class gdn_prefill_args(ctypes.Structure):
@@ -92,7 +97,8 @@ class gdn_prefill_args(ctypes.Structure):
                 ("cu_seqlens", _vp), ("state_indices", _vp), ("has_initial_state", _vp),
                 ("cu_seqlens_host", _vp), ("state_indices_host", _vp),
                 ("out", _vp), ("out_len", _i64), ("workspace", _vp),
-                ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t),
+                ("out_norm", ctypes.POINTER(gdn_out_norm))]
 
 
 class gdn_kda_args(ctypes.Structure):
@@ -313,18 +319,33 @@ def packed_ba_views(ba: torch.Tensor, Hv: int):
     return ba[:, Hv:2 * Hv], ba[:, :Hv]
 
 
+def _out_norm(norm_z, norm_weight, norm_eps, norm_sigmoid, tokens, Hv, Dv):
+    """The gdn_out_norm option: None, or (struct, pointer) with z's row stride
+    taken from the tensor (a [T, Hv, Dv] gate or a [T, >= Hv*Dv] slice)."""
+    if norm_weight is None:
+        return None, None
+    zs = norm_z.stride(0)
+    n = gdn_out_norm(z=_p(norm_z), z_len=max(tokens - 1, 0) * zs + Hv * Dv, z_token_stride=zs,
+                     weight=_p(norm_weight), weight_len=_n(norm_weight), eps=float(norm_eps),
+                     sigmoid_gate=int(bool(norm_sigmoid)))
+    return n, ctypes.pointer(n)
+
+
 def gdn_decode(q, k, v, g, beta, state, out, *, scale=-1.0, state_indices=None,
-               state_indices_host=None, use_qk_l2norm=False, stream=None) -> None:
-    """include/gdn.h gdn_decode; `state` [slots,Hv,Dv,Dk] f32 updated in place."""
+               state_indices_host=None, use_qk_l2norm=False, norm_z=None, norm_weight=None,
+               norm_eps=1e-6, norm_sigmoid=False, stream=None) -> None:
+    """include/gdn.h gdn_decode; `state` [slots,Hv,Dv,Dk] f32 updated in place.
+    With norm_weight (and norm_z) the gated RMSNorm is applied to `out`."""
     B, Hk, Dk = q.shape
     _, Hv, Dv = v.shape
     sih, sih_p = _host_i32(state_indices_host)
+    nrm, nrm_p = _out_norm(norm_z, norm_weight, norm_eps, norm_sigmoid, B, Hv, Dv)
     a = gdn_decode_args(
         B=B, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, act_dtype=_dt(q), use_qk_l2norm=int(use_qk_l2norm),
         scale=float(scale), q=_p(q), q_len=_n(q), k=_p(k), k_len=_n(k), v=_p(v), v_len=_n(v),
         g=_p(g), g_len=_n(g), beta=_p(beta), beta_len=_n(beta), state=_p(state),
         state_slots=state.shape[0], state_len=_n(state), state_indices=_p(state_indices),
-        state_indices_host=sih_p, out=_p(out), out_len=_n(out))
+        state_indices_host=sih_p, out=_p(out), out_len=_n(out), out_norm=nrm_p)
     _check(lib().gdn_decode(ctypes.byref(a), _stream(stream)))
 
 
@@ -395,14 +416,17 @@ def gdn_prefill_resolve_algo(N, Hv, Dk, Dv, act_dtype=GDN_DTYPE_BF16,
 def gdn_prefill_varlen(q, k, v, g, beta, state, cu_seqlens, out, *, scale=-1.0,
                        state_indices=None, has_initial_state=None, cu_seqlens_host=None,
                        state_indices_host=None, use_qk_l2norm=False, algo=GDN_PREFILL_AUTO,
-                       workspace=None, stream=None) -> None:
+                       workspace=None, norm_z=None, norm_weight=None, norm_eps=1e-6,
+                       norm_sigmoid=False, stream=None) -> None:
     """include/gdn.h gdn_prefill_varlen; `state` updated in place.  `workspace`
-    is a uint8 device tensor of at least gdn_prefill_workspace_bytes() bytes."""
+    is a uint8 device tensor of at least gdn_prefill_workspace_bytes() bytes.
+    With norm_weight (and norm_z) the gated RMSNorm is applied to `out`."""
     T, Hk, Dk = q.shape
     _, Hv, Dv = v.shape
     N = cu_seqlens.numel() - 1
     cuh, cuh_p = _host_i32(cu_seqlens_host)
     sih, sih_p = _host_i32(state_indices_host)
+    nrm, nrm_p = _out_norm(norm_z, norm_weight, norm_eps, norm_sigmoid, T, Hv, Dv)
     a = gdn_prefill_args(
         T=T, N=N, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, act_dtype=_dt(q), use_qk_l2norm=int(use_qk_l2norm),
         scale=float(scale), algo=int(algo), q=_p(q), q_len=_n(q), k=_p(k), k_len=_n(k),
@@ -411,7 +435,8 @@ def gdn_prefill_varlen(q, k, v, g, beta, state, cu_seqlens, out, *, scale=-1.0,
         cu_seqlens=_p(cu_seqlens), state_indices=_p(state_indices),
         has_initial_state=_p(has_initial_state), cu_seqlens_host=cuh_p,
         state_indices_host=sih_p, out=_p(out), out_len=_n(out), workspace=_p(workspace),
-        workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size())
+        workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
+        out_norm=nrm_p)
     _check(lib().gdn_prefill_varlen(ctypes.byref(a), _stream(stream)))
 
 

@@ -95,6 +95,58 @@ int check_cu_host(const int32_t* cu, int64_t n, int64_t total, const char* who) 
   return GDN_OK;
 }
 
+// The output-norm option of gdn_decode / gdn_prefill_varlen: the rules of
+// gdn_gated_rmsnorm ([cpu.rs] validate_gated_rms_norm_shape) for `tokens` rows
+// of Hv * Dv values; fills the launch's norm fields.
+int check_out_norm(const gdn_out_norm* n, int64_t tokens, int64_t Hv, int64_t Dv, int32_t act_dtype,
+                   gdn::RecurLaunch& p) {
+  p.onorm_w = nullptr;
+  if (n == nullptr) return GDN_OK;
+  const int64_t row = Hv * Dv;
+  if (n->z_token_stride < row)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gated_rms_norm z token stride shorter than heads * dim");
+  const LenRule rules[] = {
+      {"z", n->z_len, (tokens - 1) * n->z_token_stride + row},
+      {"weight", n->weight_len, Dv},
+  };
+  if (int rc = check_lengths("gated_rms_norm", rules)) return rc;
+  for (auto pr : {std::make_pair(n->z, "out_norm z"), std::make_pair(n->weight, "out_norm weight")}) {
+    if (int rc = require_ptr(pr.first, pr.second)) return rc;
+    if (int rc = require_aligned(pr.first, pr.second)) return rc;
+  }
+  const int64_t es = elem_size(act_dtype), vec = 16 / es;
+  if ((n->z_token_stride * es) % 16 != 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gated_rms_norm z token stride must be a multiple of 16 bytes");
+  if (Dv % vec != 0 || Dv > 128 * vec)
+    return fail(GDN_ERR_UNSUPPORTED, "the output norm supports Dv a multiple of " + S(vec) +
+                                         " and at most " + S(128 * vec));
+  if (!(n->eps >= 0.0f)) return fail(GDN_ERR_INVALID_ARGUMENT, "gated_rms_norm eps must be >= 0");
+  p.onorm_z = n->z;
+  p.onorm_z_stride = n->z_token_stride;
+  p.onorm_w = n->weight;
+  p.onorm_eps = n->eps;
+  p.onorm_sigmoid = n->sigmoid_gate != 0;
+  return GDN_OK;
+}
+
+// The output norm as its own kernel, over the output in place (for the
+// prefill forms that do not fuse it).
+cudaError_t launch_out_norm_pass(const gdn::RecurLaunch& p, cudaStream_t st) {
+  gdn::NormLaunch n{};
+  n.rows = (int64_t)p.T * p.Hv;
+  n.heads = p.Hv;
+  n.dim = p.Dv;
+  n.bf16 = p.bf16;
+  n.sigmoid_gate = p.onorm_sigmoid;
+  n.eps = p.onorm_eps;
+  n.core = p.out;
+  n.z = p.onorm_z;
+  n.z_stride = p.onorm_z_stride;
+  n.weight = p.onorm_w;
+  n.out = p.out;
+  return gdn::launch_gated_rmsnorm(n, st);
+}
+
 // [qwen3_5.cpp] ValidateGdnStateIndices: -1 is the only allowed negative, live
 // slots in range and distinct (O(n) seen-set).
 int check_indices_host(const int32_t* idx, int64_t n, int64_t slots) {
@@ -511,9 +563,17 @@ int gdn_decode(const gdn_decode_args* a, void* stream) {
   p.sidx = a->state_indices;
   p.has_init = nullptr;
   p.out = a->out;
+  if (int rc = check_out_norm(a->out_norm, a->B, a->Hv, a->Dv, a->act_dtype, p)) return rc;
   p.status = gdn::status_word();
   if (p.status == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
-  return launch_result(gdn::launch_decode(p, static_cast<cudaStream_t>(stream)), "gdn_decode");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (p.onorm_w == nullptr || gdn::decode_norm_in_kernel(p.Dk, p.Dv))
+    return launch_result(gdn::launch_decode(p, st), "gdn_decode");
+  // a row wider than one cluster of slices: the norm as a second kernel
+  gdn::RecurLaunch plain = p;
+  plain.onorm_w = nullptr;
+  if (int rc = launch_result(gdn::launch_decode(plain, st), "gdn_decode")) return rc;
+  return launch_result(launch_out_norm_pass(p, st), "gdn_decode(output norm)");
 }
 
 int gdn_kda_varlen(const gdn_kda_args* a, void* stream) {
@@ -804,6 +864,7 @@ int gdn_prefill_varlen(const gdn_prefill_args* a, void* stream) {
   p.sidx = a->state_indices;
   p.has_init = a->has_initial_state;
   p.out = a->out;
+  if (int rc = check_out_norm(a->out_norm, a->T, a->Hv, a->Dv, a->act_dtype, p)) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (algo == GDN_PREFILL_CHUNKED) {
     if (!gdn::chunked_supported((int)a->Dk, (int)a->Dv, p.bf16))
@@ -821,9 +882,11 @@ int gdn_prefill_varlen(const gdn_prefill_args* a, void* stream) {
     p.status = gdn::status_word();
     if (p.status == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
     gdn::ChunkedLaunch c{p, a->workspace, a->workspace_bytes};
-    return launch_result(gdn::launch_chunked(c, st), "gdn_prefill_varlen(chunked)");
+    if (int rc = launch_result(gdn::launch_chunked(c, st), "gdn_prefill_varlen(chunked)")) return rc;
+    if (p.onorm_w == nullptr) return GDN_OK;
+    return launch_result(launch_out_norm_pass(p, st), "gdn_prefill_varlen(output norm)");
   }
-  if (algo == GDN_PREFILL_FUSED) {
+  if (algo == GDN_PREFILL_FUSED) {  // applies the output norm itself
     if (!gdn::fused_supported((int)a->Dk, (int)a->Dv, p.bf16))
       return fail(GDN_ERR_UNSUPPORTED,
                   "the fused chunked prefill supports bf16 activations with Dk = Dv = 128");
@@ -835,7 +898,10 @@ int gdn_prefill_varlen(const gdn_prefill_args* a, void* stream) {
     return fail(GDN_ERR_UNSUPPORTED, "the recurrent prefill supports Dk in {16, 32, 64, 128, 256}");
   p.status = gdn::status_word();
   if (p.status == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
-  return launch_result(gdn::launch_recurrent(p, st), "gdn_prefill_varlen(recurrent)");
+  if (int rc = launch_result(gdn::launch_recurrent(p, st), "gdn_prefill_varlen(recurrent)"))
+    return rc;
+  if (p.onorm_w == nullptr) return GDN_OK;
+  return launch_result(launch_out_norm_pass(p, st), "gdn_prefill_varlen(output norm)");
 }
 
 }  // extern "C"

@@ -60,6 +60,7 @@
 
 #include "gdn_chunk_common.cuh"
 #include "gdn_internal.h"
+#include "gdn_math.cuh"
 #include "tcgen05.cuh"
 
 namespace gdn {
@@ -793,9 +794,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
       fence_after_sync();
       {
         // 32 tokens at a time through the staging rows: each thread writes its
-        // dv of every token, then the rows leave as 16-byte vectors.
+        // dv of every token, then the rows leave as 16-byte vectors.  A token
+        // row is 16 consecutive lanes, so the output norm's sum of squares is
+        // four shuffles within the half-warp.
         __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + FusedSmem::OST);
         const int stid = tid - 320;  // 0..127
+        const bool onorm = p.onorm_w != nullptr;
 #pragma unroll 1
         for (int j0 = 0; j0 < kC && j0 < L; j0 += 32) {
           float o[32];
@@ -808,9 +812,30 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
           for (int q = 0; q < 4; ++q) {
             const int idx = q * kScanThreads + stid;  // 16-byte vector: token idx / 16
             const int r = idx >> 4, c16 = idx & 15;
-            if (j0 + r < L)
-              *reinterpret_cast<uint4*>(out + ((int64_t)(t0 + j0 + r) * p.Hv + h) * kD + c16 * 8) =
-                  *reinterpret_cast<const uint4*>(ost + r * kD + c16 * 8);
+            __nv_bfloat16* dst = out + ((int64_t)(t0 + j0 + r) * p.Hv + h) * kD + c16 * 8;
+            if (onorm) {
+              float x[8];
+              ld_bf16x8(ost + r * kD + c16 * 8, x);
+              float ss = 0.0f;
+#pragma unroll
+              for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+#pragma unroll
+              for (int m = 8; m > 0; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+              if (j0 + r < L) {
+                const float inv = math::rms_inv(ss, 1.0f / kD, p.onorm_eps);
+                float z[8], w[8];
+                ld_bf16x8(static_cast<const __nv_bfloat16*>(p.onorm_z) +
+                              (int64_t)(t0 + j0 + r) * p.onorm_z_stride + (int64_t)h * kD + c16 * 8,
+                          z);
+                ld_bf16x8(static_cast<const __nv_bfloat16*>(p.onorm_w) + c16 * 8, w);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  x[e] = x[e] * inv * w[e] * math::norm_gate(z[e], p.onorm_sigmoid);
+                st_bf16x8(dst, x);
+              }
+            } else if (j0 + r < L) {
+              *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(ost + r * kD + c16 * 8);
+            }
           }
           named_bar(kBarScan, kScanThreads);
         }

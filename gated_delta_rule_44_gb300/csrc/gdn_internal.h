@@ -78,6 +78,14 @@ struct RecurLaunch {
   int num_cols;                 // speculative decode only
   void* out;
   unsigned* status;
+  // Gated RMSNorm of the output rows (on when onorm_w != nullptr): out =
+  // core / sqrt(mean(core^2) + eps) * w * act(z), core rounded to the
+  // activation type first.
+  const void* onorm_z;
+  int64_t onorm_z_stride;  // elements between token rows of z
+  const void* onorm_w;
+  float onorm_eps;
+  bool onorm_sigmoid;
 };
 cudaError_t launch_decode(const RecurLaunch& p, cudaStream_t s);
 cudaError_t launch_recurrent(const RecurLaunch& p, cudaStream_t s);
@@ -89,6 +97,9 @@ cudaError_t launch_kda(const RecurLaunch& p, cudaStream_t s);
 // stored into sidx[s * num_cols + j] (negative: skipped); p.norm false.
 cudaError_t launch_spec_decode(const RecurLaunch& p, cudaStream_t s);
 bool recurrent_supported(int Dk);
+// Whether gdn_decode applies the output norm inside the recurrence kernel
+// (the row's value-dimension slices fit one cluster of at most 8 CTAs).
+bool decode_norm_in_kernel(int Dk, int Dv);
 
 // Decode in one launch from the packed projections: conv update, SiLU, q/k
 // norm, gates and the recurrence (one token per row b; the conv pool and the

@@ -1,5 +1,7 @@
 // gdn_math.cuh -- the scalar gate and activation functions of the prepare
-// step, shared by the prepare kernels and the packed decode kernel.
+// step, shared by the prepare kernels and the packed decode kernel, and the
+// gate and scale of the gated output norm, shared by the norm kernel and the
+// kernels that apply the norm where they store their output.
 //
 // [cpu.rs] (ferrum-kernels 0.8.0, src/ferrum_kernels/backend/cpu.rs) sigmoid,
 // softplus and silu: a two-branch sigmoid, softplus equal to x above 20 and to
@@ -52,6 +54,19 @@ __device__ __forceinline__ float exp_ex2(float x) {
 // finite.
 __device__ __forceinline__ float silu_f(float x) {
   return x * recip_nr(1.0f + __expf(fminf(-x, 80.0f)));
+}
+
+// The gate of the gated RMSNorm ([cpu.rs] gated_rms_norm_f32: silu(z);
+// [cpu_ops.cpp] RmsNormGatedKernel's option: sigmoid(z)), with sigmoid(z) =
+// 1 / (1 + e^{-z}) on the refined reciprocal (e^{-z} capped at e^80).
+__device__ __forceinline__ float norm_gate(float z, bool sigmoid_gate) {
+  const float sg = recip_nr(1.0f + __expf(fminf(-z, 80.0f)));
+  return sigmoid_gate ? sg : z * sg;
+}
+
+// 1 / sqrt(mean + eps) of a row of n values whose squares sum to ss.
+__device__ __forceinline__ float rms_inv(float ss, float inv_n, float eps) {
+  return rsqrtf(fmaf(ss, inv_n, eps));
 }
 
 }  // namespace math

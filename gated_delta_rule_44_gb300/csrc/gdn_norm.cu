@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include "gdn_internal.h"
+#include "gdn_math.cuh"
 
 namespace gdn {
 namespace {
@@ -61,20 +62,6 @@ struct Vec<float> {
     *reinterpret_cast<float4*>(p) = make_float4(o[0], o[1], o[2], o[3]);
   }
 };
-
-// 1 / y: the approximate reciprocal refined by one Newton-Raphson step,
-// r <- r + r (1 - y r).  For finite y >= 1.
-__device__ __forceinline__ float recip_nr(float y) {
-  float r;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
-  return fmaf(r, fmaf(-y, r, 1.0f), r);
-}
-
-// sigmoid(x) = 1 / (1 + e^{-x}); e^{-x} capped at e^80 so that the operand
-// stays finite (the sigmoid is then below 1e-34 either way).
-__device__ __forceinline__ float sigmoid_f(float x) {
-  return recip_nr(1.0f + __expf(fminf(-x, 80.0f)));
-}
 
 template <typename TA, int NV>
 __global__ void __launch_bounds__(kThreads) gated_rmsnorm_kernel(const NormLaunch p, int lpr) {
@@ -124,18 +111,15 @@ __global__ void __launch_bounds__(kThreads) gated_rmsnorm_kernel(const NormLaunc
       for (int e = 0; e < V; ++e) ss = fmaf(x[j][e], x[j][e], ss);
     }
     for (int m = 1; m < lpr; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-    const float inv = rsqrtf(fmaf(ss, inv_dim, p.eps));
+    const float inv = math::rms_inv(ss, inv_dim, p.eps);
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
       const int vi = sub + j * lpr;
       if (live && vi < nvec) {
         float o[V];
 #pragma unroll
-        for (int e = 0; e < V; ++e) {
-          const float sg = sigmoid_f(zz[j][e]);
-          const float act = p.sigmoid_gate ? sg : zz[j][e] * sg;
-          o[e] = x[j][e] * inv * w[j][e] * act;
-        }
+        for (int e = 0; e < V; ++e)
+          o[e] = x[j][e] * inv * w[j][e] * math::norm_gate(zz[j][e], p.sigmoid_gate);
         Vec<TA>::store(out8 + (row * p.dim + static_cast<int64_t>(vi) * V) * es, o);
       }
     }

@@ -47,6 +47,37 @@ using namespace rows;
 
 constexpr int kThreads = 128;
 
+// The stored value of x: x rounded to the activation type.
+template <typename TA>
+__device__ __forceinline__ float round_act(float x);
+template <>
+__device__ __forceinline__ float round_act<float>(float x) {
+  return x;
+}
+template <>
+__device__ __forceinline__ float round_act<__nv_bfloat16>(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// Every thread of every CTA of the cluster arrives, then waits: shared-memory
+// writes before it are visible to the cluster's CTAs after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n"
+      "barrier.cluster.wait.acquire.aligned;\n" ::
+          : "memory");
+}
+
+// *p in the shared memory of the cluster's CTA of rank `rank`.
+__device__ __forceinline__ float ld_cluster(const float* p, int rank) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
+  return v;
+}
+
 // q and k columns of one lane (16 each), optionally L2-normalised, plus k.q.
 template <typename TA, int DK>
 struct QK {
@@ -121,7 +152,12 @@ __device__ __forceinline__ float4 mul4(const float4& a, const float4& b) {
 // ---------------------------------------------------------------------------
 // Decode: grid.x = B * Hv * slices.  KDA: the one-token sequences of a KDA
 // call (T == N), with the per-key-channel decay and has_initial_state.
-template <typename TA, int DK, int PASSES, bool KDA>
+// ONORM: the gated RMSNorm of each output row is applied before the store.
+// The row's value-dimension slices are the CTAs of one thread-block cluster
+// (slices <= 8): each sums the squares of its rows' stored outputs, the sums
+// are exchanged through distributed shared memory and added in rank order,
+// so every CTA of the row gets the same norm.
+template <typename TA, int DK, int PASSES, bool KDA, bool ONORM>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const RecurLaunch p, int slices) {
   constexpr int LPR = DK / 16;
   constexpr int RPP = kThreads / LPR;  // rows per pass
@@ -188,6 +224,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const RecurLaunch p, i
     decay = expf(__ldg(p.g + (int64_t)b * p.Hv + h));
   }
 
+  float core[PASSES];  // ONORM: this row's output as stored, before the norm
+  float ss = 0.0f;
 #pragma unroll
   for (int ps = 0; ps < PASSES; ++ps) {
     const int r = row0 + ps * RPP;
@@ -197,11 +235,46 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const RecurLaunch p, i
       o = row_step_kda<LPR>(st[ps], e, ek, eq, qk.k, qk.kq, beta, vv);
     else
       o = row_step<LPR>(st[ps], qk.k, qk.q, qk.kq, decay, beta, vv);
+    core[ps] = 0.0f;
     if (r < p.Dv) {
 #pragma unroll
       for (int m = 0; m < 4; ++m)
         __stcs(reinterpret_cast<float4*>(S + (int64_t)r * DK + 4 * lr + 4 * LPR * m), st[ps][m]);
-      if (lr == 0) st_act<TA>(out + r, o * p.scale);
+      if constexpr (ONORM) {
+        core[ps] = round_act<TA>(o * p.scale);
+        if (lr == 0) ss = fmaf(core[ps], core[ps], ss);
+      } else {
+        if (lr == 0) st_act<TA>(out + r, o * p.scale);
+      }
+    }
+  }
+  if constexpr (ONORM) {
+    __shared__ float wpart[kThreads / 32];
+    __shared__ float cpart;
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+    if ((tid & 31) == 0) wpart[tid >> 5] = ss;
+    __syncthreads();
+    float tot = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) tot += wpart[w];
+    if (slices > 1) {
+      if (tid == 0) cpart = tot;
+      cluster_sync_all();
+      tot = 0.0f;
+      for (int rk = 0; rk < slices; ++rk) tot += ld_cluster(&cpart, rk);
+      cluster_sync_all();  // every CTA has read the others' sums before any exits
+    }
+    const float inv = math::rms_inv(tot, 1.0f / static_cast<float>(p.Dv), p.onorm_eps);
+    const TA* zr = static_cast<const TA*>(p.onorm_z) + (int64_t)b * p.onorm_z_stride +
+                   (int64_t)h * p.Dv;
+    const TA* wr = static_cast<const TA*>(p.onorm_w);
+#pragma unroll
+    for (int ps = 0; ps < PASSES; ++ps) {
+      const int r = row0 + ps * RPP;
+      if (lr == 0 && r < p.Dv)
+        st_act<TA>(out + r, core[ps] * inv * ld_act<TA>(wr + r) *
+                                math::norm_gate(ld_act<TA>(zr + r), p.onorm_sigmoid));
     }
   }
 }
@@ -400,9 +473,17 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurLaunch p
 
 enum class Mode { kDecode, kRecurrent, kKda, kKdaDecode, kSpec };
 
+constexpr int kMaxNormCluster = 8;
+
+// Rows of the value dimension one CTA holds: PASSES chosen so that a CTA
+// holds 64 rows at Dk = 128 (32 floats of state per thread).
+constexpr int passes_for(int dk) { return dk <= 32 ? 1 : dk == 64 ? 2 : 4; }
+constexpr int rows_per_cta_for(int dk) { return (kThreads / (dk / 16)) * passes_for(dk); }
+
 template <typename TA, int DK, int PASSES>
 cudaError_t launch_dk(const RecurLaunch& p, cudaStream_t s, Mode mode) {
   constexpr int rows_per_cta = (kThreads / (DK / 16)) * PASSES;
+  static_assert(rows_per_cta == rows_per_cta_for(DK), "one place for the slice rule");
   const int slices = (p.Dv + rows_per_cta - 1) / rows_per_cta;
   const bool per_row = mode == Mode::kDecode || mode == Mode::kKdaDecode;
   const int64_t blocks = (int64_t)(per_row ? p.T : p.N) * p.Hv * slices;
@@ -410,10 +491,30 @@ cudaError_t launch_dk(const RecurLaunch& p, cudaStream_t s, Mode mode) {
   const unsigned grid = (unsigned)blocks;
   switch (mode) {
     case Mode::kDecode:
-      decode_kernel<TA, DK, PASSES, false><<<grid, kThreads, 0, s>>>(p, slices);
+      if (p.onorm_w != nullptr) {
+        if (slices > kMaxNormCluster) return cudaErrorInvalidConfiguration;
+        // the row's slices as one cluster, so that they can share their sums
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(slices);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e =
+            cudaLaunchKernelEx(&cfg, decode_kernel<TA, DK, PASSES, false, true>, p, slices);
+        note_launch();
+        return e != cudaSuccess ? e : cudaGetLastError();
+      }
+      decode_kernel<TA, DK, PASSES, false, false><<<grid, kThreads, 0, s>>>(p, slices);
       break;
     case Mode::kKdaDecode:
-      decode_kernel<TA, DK, PASSES, true><<<grid, kThreads, 0, s>>>(p, slices);
+      decode_kernel<TA, DK, PASSES, true, false><<<grid, kThreads, 0, s>>>(p, slices);
       break;
     case Mode::kRecurrent:
       recurrent_kernel<TA, DK, PASSES, false, false><<<grid, kThreads, 0, s>>>(p, slices);
@@ -447,6 +548,12 @@ cudaError_t launch_any(const RecurLaunch& p, cudaStream_t s, Mode mode) {
 
 bool recurrent_supported(int Dk) {
   return Dk == 16 || Dk == 32 || Dk == 64 || Dk == 128 || Dk == 256;
+}
+
+bool decode_norm_in_kernel(int Dk, int Dv) {
+  if (!recurrent_supported(Dk) || Dv < 1) return false;
+  const int rows = rows_per_cta_for(Dk);
+  return (Dv + rows - 1) / rows <= kMaxNormCluster;
 }
 
 static cudaError_t launch_mode(const RecurLaunch& p, cudaStream_t s, Mode mode) {

@@ -162,6 +162,31 @@ typedef struct gdn_prepare_args {
 int gdn_prepare(const gdn_prepare_args* args, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * gdn_out_norm -- an optional gated RMSNorm of the recurrence output, applied
+ * where gdn_decode / gdn_prefill_varlen store it: [cpu.rs] gated_rms_norm_f32,
+ * [cpu_ops.cpp] RmsNormGatedKernel.  Per (token, value head) row of Dv values
+ *   out = core / sqrt(mean_d(core^2) + eps) * weight[d] * act(z[d])
+ * where core is the recurrence output rounded to act_dtype (what the unfused
+ * pipeline stores and the norm reads back) and act = silu (sigmoid_gate = 0)
+ * or sigmoid.  z: token rows of at least Hv * Dv values in act_dtype,
+ * z_token_stride elements apart (16-byte aligned rows); weight: [Dv] in
+ * act_dtype.  The decode computes it inside the recurrence kernel (the CTAs of
+ * a row's value-dimension slices exchange their partial sums within a thread-
+ * block cluster); so does the fused chunked prefill; the other prefill forms
+ * run the norm as a second kernel over the output in place.  Same rules as
+ * gdn_gated_rmsnorm (lengths, alignment, Dv <= 1024 for bf16).
+ * ------------------------------------------------------------------------- */
+typedef struct gdn_out_norm {
+  const void* z;           /* [tokens, z_token_stride] act_dtype */
+  int64_t z_len;
+  int64_t z_token_stride;  /* elements between token rows of z (>= Hv * Dv) */
+  const void* weight;      /* [Dv] act_dtype */
+  int64_t weight_len;
+  float eps;
+  int32_t sigmoid_gate;    /* 1: sigmoid gate instead of silu */
+} gdn_out_norm;
+
+/* ---------------------------------------------------------------------------
  * gdn_decode -- [cpu_ops.cpp] GdnDecodeKernel / GdnHeadTokenStep;
  * [cpu.rs] recurrent_gated_delta_rule_batch_f32.
  *
@@ -195,6 +220,7 @@ typedef struct gdn_decode_args {
   const int32_t* state_indices_host; /* optional host copy: full validation */
   void* out;                /* [B, Hv, Dv] */
   int64_t out_len;
+  const gdn_out_norm* out_norm;  /* NULL, or the gated RMSNorm applied to out */
 } gdn_decode_args;
 
 int gdn_decode(const gdn_decode_args* args, void* stream);
@@ -242,6 +268,7 @@ typedef struct gdn_prefill_args {
   int64_t out_len;
   void* workspace;          /* device scratch, see gdn_prefill_workspace_bytes */
   size_t workspace_bytes;
+  const gdn_out_norm* out_norm;  /* NULL, or the gated RMSNorm applied to out */
 } gdn_prefill_args;
 
 int gdn_prefill_varlen(const gdn_prefill_args* args, void* stream);

@@ -417,3 +417,45 @@ def test_packed_decode_rejections():
                                    conv_state_len=10**7))[0] == B.GDN_ERR_UNSUPPORTED
     rc, msg = call_packed(packed_args(state_indices_host=_host(0, 1, 1, -1)))
     assert rc == B.GDN_ERR_INVALID_ARGUMENT and msg == "duplicate live GDN state index"
+
+
+def out_norm(T, Hv, Dv, **over):
+    n = dict(z=FAKE, z_len=T * Hv * Dv, z_token_stride=Hv * Dv, weight=FAKE, weight_len=Dv,
+             eps=1e-6, sigmoid_gate=0)
+    n.update(over)
+    return B.gdn_out_norm(**n)
+
+
+def test_out_norm_option_rejections():
+    """The output-norm option of gdn_decode / gdn_prefill_varlen follows the
+    gated_rms_norm rules ([cpu.rs] validate_gated_rms_norm_shape) for the
+    call's output rows."""
+    def dec(**over):
+        n = out_norm(2, 2, 64, **over)
+        return call_decode(decode_args(out_norm=ctypes.pointer(n)))
+
+    rc, msg = dec(z_len=2 * 2 * 64 - 1)
+    assert rc == B.GDN_ERR_SHAPE and msg == "gated_rms_norm z length 255 < expected 256"
+    rc, msg = dec(weight_len=63)
+    assert rc == B.GDN_ERR_SHAPE and msg == "gated_rms_norm weight length 63 < expected 64"
+    assert dec(z_token_stride=100)[0] == B.GDN_ERR_INVALID_ARGUMENT       # < Hv * Dv
+    assert dec(z_token_stride=132, z_len=10**6)[0] == B.GDN_ERR_INVALID_ARGUMENT  # 264 B rows
+    assert dec(z=None)[0] == B.GDN_ERR_INVALID_ARGUMENT
+    assert dec(weight=FAKE + 2)[0] == B.GDN_ERR_INVALID_ARGUMENT
+    assert dec(eps=-1.0)[0] == B.GDN_ERR_INVALID_ARGUMENT
+    n = out_norm(2, 2, 12)
+    rc, msg = call_decode(decode_args(Dv=12, v_len=48, out_len=48, state_len=4 * 2 * 12 * 128,
+                                      out_norm=ctypes.pointer(n)))
+    assert rc == B.GDN_ERR_UNSUPPORTED and "multiple of 8" in msg
+    # the prefill: z rows for every token
+    n = out_norm(10, 2, 128, z_len=9 * 256 + 255)
+    rc, msg = call_prefill(prefill_args(out_norm=ctypes.pointer(n)))
+    assert rc == B.GDN_ERR_SHAPE and msg == "gated_rms_norm z length 2559 < expected 2560"
+
+
+def test_out_norm_valid_call_without_gpu_stops_before_launch():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("this machine has a GPU")
+    n = out_norm(2, 2, 64, z_token_stride=136, z_len=136 + 128)
+    assert call_decode(decode_args(out_norm=ctypes.pointer(n)))[0] == B.GDN_ERR_CUDA
