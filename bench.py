@@ -314,6 +314,66 @@ def time_gated_rmsnorm(w, dev, peaks, iters=20):
             "achieved_gbs": round(gbs, 1), "hbm_frac_of_measured": round(gbs / peaks["hbm"], 4)}
 
 
+def time_out_norm_routes(w, dev, algo, iters=10):
+    """The step's recurrence calls (decode rows, then the prefill) followed by
+    the gated RMSNorm of their output, two ways: the norm as its own call
+    after them, and the norm fused into their stores (the out_norm option).
+    Gate rows z [T, Hv*Dv] and weight [Dv] bf16, seeded; q, k, v, g, beta are
+    the step's own prepare outputs.  Reports each route's average time."""
+    import torch
+    from gated_delta_rule_44_gb300 import binding as B
+    from gated_delta_rule_44_gb300.layer import GdnStep
+    d = dev_inputs(w, dev)
+    step = GdnStep(w.T, w.N, w.n_decode, w.Hk, w.Hv, w.Dk, w.Dv, w.K, w.act_dtype, dev, algo=algo)
+    s = torch.cuda.current_stream(dev)
+    B.gdn_prepare(d["mixed_qkv"], d["conv_weight"], d["a_raw"], d["b_raw"], d["A_log"],
+                  d["dt_bias"], d["cu_seqlens"], d["conv_pool"], step.q, step.k, step.v, step.g,
+                  step.beta, Hk=step.Hk, Hv=step.Hv, Dk=step.Dk, Dv=step.Dv, K=step.K,
+                  state_indices=d["state_indices"], has_initial_state=d["has_initial_state"],
+                  stream=s)
+    g = torch.Generator().manual_seed(23)
+    z = torch.randn(w.T, w.Hv * w.Dv, generator=g).to(torch.bfloat16).to(dev)
+    wt = (torch.rand(w.Dv, generator=g) + 0.5).to(torch.bfloat16).to(dev)
+    normed = torch.empty_like(step.out)
+    nd, ndt = step.n_decode, step.nd_tok
+
+    def calls(fused):
+        kw = {}
+        if nd > 0:
+            if fused:
+                kw = dict(norm_z=z[:ndt], norm_weight=wt)
+            B.gdn_decode(step.q[:ndt], step.k[:ndt], step.v[:ndt], step.g[:ndt],
+                         step.beta[:ndt], d["state_pool"], step.out[:ndt],
+                         state_indices=d["state_indices"][:nd], stream=s, **kw)
+        if step.N > nd:
+            if fused:
+                kw = dict(norm_z=z[ndt:], norm_weight=wt)
+            B.gdn_prefill_varlen(step.q[ndt:], step.k[ndt:], step.v[ndt:], step.g[ndt:],
+                                 step.beta[ndt:], d["state_pool"], d["cu_seqlens_prefill"],
+                                 step.out[ndt:], state_indices=d["state_indices"][nd:],
+                                 has_initial_state=d["has_initial_state"][nd:], algo=step.algo,
+                                 workspace=step.workspace, stream=s, **kw)
+        if not fused:
+            B.gdn_gated_rmsnorm(step.out, z, wt, normed, stream=s)
+
+    res = {}
+    for fused in (False, True):
+        for _ in range(3):
+            calls(fused)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(s)
+        for _ in range(iters):
+            calls(fused)
+        e1.record(s)
+        torch.cuda.synchronize(dev)
+        res["fused_us" if fused else "separate_us"] = round(e0.elapsed_time(e1) / iters * 1e3, 2)
+    B.gdn_read_device_status(s)
+    del d, step
+    torch.cuda.empty_cache()
+    return {"calls": "decode + prefill + gated RMSNorm of the output", **res}
+
+
 def time_kda_decode(dev, peaks, B_=256, Hk=16, Hv=32, D=128, slots=512, iters=10):
     """gdn_kda_varlen on decode_b256's shape (256 one-token sequences, a
     512-slot f32 pool, bf16 activations).  Algorithmic bytes: every live state
@@ -708,6 +768,7 @@ def main():
                            "kernels": kx}
             del wx
         extra["gated_rmsnorm"] = time_gated_rmsnorm(w, dev, peaks)
+        extra["out_norm_routes"] = time_out_norm_routes(w, dev, args.algo)
         extra["kda_decode_b256"] = time_kda_decode(dev, peaks)
         extra["spec_decode_r128x4"] = time_spec_decode(dev, peaks)
         extra["spec_prepare_r128x4"] = time_spec_prepare(dev, peaks)

@@ -248,7 +248,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
   // TMEM: columns 0..63 [K; Q] K^T (kept for every value head), 64..191 the
   // M = 64 results W, then Ut, of the current head.
   const uint32_t tm_g = tmem, tm_wu = tmem + 64;
-  bool ok = mbar_wait(mb_tma, 0, kWaitBudget);
+  const bool ok_kq = __syncthreads_and(mbar_wait(mb_tma, 0, kWaitBudget));
+  if (!ok_kq) {  // the K, Q tiles did not land: touch none of their bytes
+    if (tid == 0) {
+      atomicOr(p.status, kStatusTimeout);
+      // wait (bounded) for the copies still in flight before the CTA exits
+      mbar_wait(mb_tma, 0, kWaitBudget);
+      mbar_wait(mb_v, 0, kWaitBudget);  // the first V load
+    }
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+    return;
+  }
   if (L < kC) {  // zero K and Q rows past the chunk end
     for (int i = tid; i < (kC - L) * 8; i += kPrepThreads) {
       const int r = L + i / 8, q16 = i % 8;
@@ -258,15 +269,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
     }
     fence_proxy_async();
   }
-  if (!__syncthreads_and(ok)) {
-    if (tid == 0) {
-      atomicOr(p.status, kStatusTimeout);
-      mbar_wait(mb_v, 0, kWaitBudget);  // the first V load
-    }
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
-    return;
-  }
+  __syncthreads();
   fence_after_sync();
   // [K; Q] K^T  (M = 128, N = 64, K = 128): A is the 128-row K-major tile
   // [K; Q] (boxes 16 KB apart), B the K tile (its first 64 rows).  Shared by
@@ -298,7 +301,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
     }
     (tid < 64 ? skn : sqn)[r] = p.norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
   }
-  ok = mbar_wait(mb_mma, 0, kWaitBudget);
+  bool ok = mbar_wait(mb_mma, 0, kWaitBudget);
   uint32_t mma_phase = 1;
   fence_after_sync();
   __syncthreads();  // publishes skn, sqn; the Q tile is free from here on
