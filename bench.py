@@ -316,8 +316,9 @@ def time_gated_rmsnorm(w, dev, peaks, iters=20):
 
 def time_out_norm_routes(w, dev, algo, iters=10):
     """The step's recurrence calls (decode rows, then the prefill) followed by
-    the gated RMSNorm of their output, two ways: the norm as its own call
-    after them, and the norm fused into their stores (the out_norm option).
+    the gated RMSNorm of their output, three ways: the norm as its own call
+    after them; the out_norm option of the calls (the norm kernel after each);
+    and the option with the decode's norm inside the decode kernel.
     Gate rows z [T, Hv*Dv] and weight [Dv] bf16, seeded; q, k, v, g, beta are
     the step's own prepare outputs.  Reports each route's average time."""
     import torch
@@ -337,11 +338,13 @@ def time_out_norm_routes(w, dev, algo, iters=10):
     normed = torch.empty_like(step.out)
     nd, ndt = step.n_decode, step.nd_tok
 
-    def calls(fused):
+    def calls(route):
+        fused = route != "separate_us"
         kw = {}
         if nd > 0:
             if fused:
-                kw = dict(norm_z=z[:ndt], norm_weight=wt)
+                kw = dict(norm_z=z[:ndt], norm_weight=wt,
+                          norm_in_kernel=route == "decode_in_kernel_us")
             B.gdn_decode(step.q[:ndt], step.k[:ndt], step.v[:ndt], step.g[:ndt],
                          step.beta[:ndt], d["state_pool"], step.out[:ndt],
                          state_indices=d["state_indices"][:nd], stream=s, **kw)
@@ -357,17 +360,17 @@ def time_out_norm_routes(w, dev, algo, iters=10):
             B.gdn_gated_rmsnorm(step.out, z, wt, normed, stream=s)
 
     res = {}
-    for fused in (False, True):
+    for route in ("separate_us", "out_norm_option_us", "decode_in_kernel_us"):
         for _ in range(3):
-            calls(fused)
+            calls(route)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(dev)
         e0.record(s)
         for _ in range(iters):
-            calls(fused)
+            calls(route)
         e1.record(s)
         torch.cuda.synchronize(dev)
-        res["fused_us" if fused else "separate_us"] = round(e0.elapsed_time(e1) / iters * 1e3, 2)
+        res[route] = round(e0.elapsed_time(e1) / iters * 1e3, 2)
     B.gdn_read_device_status(s)
     del d, step
     torch.cuda.empty_cache()
@@ -412,6 +415,51 @@ def time_kda_decode(dev, peaks, B_=256, Hk=16, Hv=32, D=128, slots=512, iters=10
     return {"tokens_per_s": round(B_ / (us * 1e-6), 1), "avg_us": round(us, 2),
             "algorithmic_bytes": nbytes, "achieved_gbs": round(gbs, 1),
             "hbm_frac_of_measured": round(gbs / peaks["hbm"], 4)}
+
+
+def time_kda_prefill(dev, peaks, T=4096, Hk=16, Hv=32, D=128, iters=5):
+    """gdn_kda_varlen on the single-sequence prefill shape (one 4096-token
+    sequence, 16 / 32 heads of 128, bf16, g = -U(0, 0.3) per key channel),
+    both forms: the chunked tensor-core one (its two launches) and the
+    recurrent one.  Algorithmic FLOPs: the chunk-64 form's contractions, as
+    for the scalar-decay prefill."""
+    import torch
+    from gated_delta_rule_44_gb300 import binding as B
+    from gated_delta_rule_44_gb300 import roofline as R
+    gen = torch.Generator().manual_seed(29)
+    q = (torch.randn(T, Hk, D, generator=gen) / D ** 0.5).to(torch.bfloat16).to(dev)
+    k = (torch.randn(T, Hk, D, generator=gen) / D ** 0.5).to(torch.bfloat16).to(dev)
+    v = torch.randn(T, Hv, D, generator=gen).to(torch.bfloat16).to(dev)
+    g = (-torch.rand(T, Hv, D, generator=gen) * 0.3).to(dev)
+    beta = (torch.rand(T, Hv, generator=gen) * 0.8 + 0.1).to(dev)
+    pool = (torch.randn(1, Hv, D, D, generator=gen) * 0.02).to(dev)
+    cu = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    out = torch.empty(T, Hv, D, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(B.gdn_kda_workspace_bytes(T, 1, Hv, D, D, 1, B.GDN_PREFILL_CHUNKED),
+                     dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream(dev)
+    res = {"shape": [T, Hk, Hv, D]}
+    for name, algo in (("chunked", B.GDN_PREFILL_CHUNKED), ("recurrent", B.GDN_PREFILL_RECURRENT)):
+        def call():
+            B.gdn_kda_varlen(q, k, v, g, beta, pool, cu, out, algo=algo,
+                             workspace=ws if algo == B.GDN_PREFILL_CHUNKED else None, stream=s)
+        for _ in range(3):
+            call()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(s)
+        for _ in range(iters):
+            call()
+        e1.record(s)
+        torch.cuda.synchronize(dev)
+        us = e0.elapsed_time(e1) / iters * 1e3
+        res[name] = {"avg_us": round(us, 2), "tokens_per_s": round(T / (us * 1e-6), 1)}
+    B.gdn_read_device_status(s)
+    flops = R.prefill_flops([T], Hv, D, D)
+    tf = flops / (res["chunked"]["avg_us"] * 1e-6) / 1e12
+    res["chunked"].update({"algorithmic_flops": flops, "achieved_tflops": round(tf, 2),
+                           "tensor_frac_of_measured": round(tf / peaks["bf16"], 4)})
+    return res
 
 
 def time_spec_decode(dev, peaks, n_reqs=128, num_cols=4, Hk=16, Hv=32, D=128, slots=1024,
@@ -770,6 +818,7 @@ def main():
         extra["gated_rmsnorm"] = time_gated_rmsnorm(w, dev, peaks)
         extra["out_norm_routes"] = time_out_norm_routes(w, dev, args.algo)
         extra["kda_decode_b256"] = time_kda_decode(dev, peaks)
+        extra["kda_prefill_4k"] = time_kda_prefill(dev, peaks)
         extra["spec_decode_r128x4"] = time_spec_decode(dev, peaks)
         extra["spec_prepare_r128x4"] = time_spec_prepare(dev, peaks)
         extra["packed_decode_b256"] = time_packed_decode(dev, peaks)

@@ -75,7 +75,7 @@ class gdn_spec_prepare_args(ctypes.Structure):
 
 class gdn_out_norm(ctypes.Structure):
     _fields_ = [("z", _vp), ("z_len", _i64), ("z_token_stride", _i64), ("weight", _vp),
-                ("weight_len", _i64), ("eps", _f32), ("sigmoid_gate", _i32)]
+                ("weight_len", _i64), ("eps", _f32), ("sigmoid_gate", _i32), ("in_kernel", _i32)]
 
 
 class gdn_decode_args(ctypes.Structure):
@@ -109,7 +109,8 @@ class gdn_kda_args(ctypes.Structure):
                 ("state", _vp), ("state_slots", _i64), ("state_len", _i64),
                 ("cu_seqlens", _vp), ("state_indices", _vp), ("has_initial_state", _vp),
                 ("cu_seqlens_host", _vp), ("state_indices_host", _vp),
-                ("out", _vp), ("out_len", _i64)]
+                ("out", _vp), ("out_len", _i64), ("algo", _i32), ("workspace", _vp),
+                ("workspace_bytes", ctypes.c_size_t)]
 
 
 class gdn_spec_decode_args(ctypes.Structure):
@@ -142,7 +143,8 @@ class gdn_mixed_meta(ctypes.Structure):
 EXPORTED = ("gdn_prepare", "gdn_decode", "gdn_prefill_varlen", "gdn_kda_varlen",
             "gdn_spec_prepare", "gdn_spec_decode", "gdn_packed_decode", "gdn_gated_rmsnorm",
             "gdn_prefill_workspace_bytes",
-            "gdn_prefill_resolve_algo", "gdn_status_string", "gdn_last_error_message",
+            "gdn_prefill_resolve_algo", "gdn_kda_resolve_algo", "gdn_kda_workspace_bytes",
+            "gdn_status_string", "gdn_last_error_message",
             "gdn_read_device_status", "gdn_version", "gdn_launch_count", "gdn_validate_mixed",
             "gdn_check_wait_timeout")
 
@@ -185,6 +187,10 @@ def lib() -> ctypes.CDLL:
             L.gdn_prefill_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64, _i64, _i32, _i32]
             L.gdn_prefill_resolve_algo.restype = _i32
             L.gdn_prefill_resolve_algo.argtypes = [_i64, _i64, _i64, _i64, _i32, _i32]
+            L.gdn_kda_resolve_algo.restype = _i32
+            L.gdn_kda_resolve_algo.argtypes = [_i64, _i64, _i64, _i64, _i32, _i32]
+            L.gdn_kda_workspace_bytes.restype = ctypes.c_size_t
+            L.gdn_kda_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64, _i64, _i32, _i32]
             L.gdn_status_string.restype = ctypes.c_char_p
             L.gdn_status_string.argtypes = [ctypes.c_int]
             L.gdn_last_error_message.restype = ctypes.c_char_p
@@ -319,7 +325,7 @@ def packed_ba_views(ba: torch.Tensor, Hv: int):
     return ba[:, Hv:2 * Hv], ba[:, :Hv]
 
 
-def _out_norm(norm_z, norm_weight, norm_eps, norm_sigmoid, tokens, Hv, Dv):
+def _out_norm(norm_z, norm_weight, norm_eps, norm_sigmoid, tokens, Hv, Dv, in_kernel=False):
     """The gdn_out_norm option: None, or (struct, pointer) with z's row stride
     taken from the tensor (a [T, Hv, Dv] gate or a [T, >= Hv*Dv] slice)."""
     if norm_weight is None:
@@ -327,19 +333,19 @@ def _out_norm(norm_z, norm_weight, norm_eps, norm_sigmoid, tokens, Hv, Dv):
     zs = norm_z.stride(0)
     n = gdn_out_norm(z=_p(norm_z), z_len=max(tokens - 1, 0) * zs + Hv * Dv, z_token_stride=zs,
                      weight=_p(norm_weight), weight_len=_n(norm_weight), eps=float(norm_eps),
-                     sigmoid_gate=int(bool(norm_sigmoid)))
+                     sigmoid_gate=int(bool(norm_sigmoid)), in_kernel=int(bool(in_kernel)))
     return n, ctypes.pointer(n)
 
 
 def gdn_decode(q, k, v, g, beta, state, out, *, scale=-1.0, state_indices=None,
                state_indices_host=None, use_qk_l2norm=False, norm_z=None, norm_weight=None,
-               norm_eps=1e-6, norm_sigmoid=False, stream=None) -> None:
+               norm_eps=1e-6, norm_sigmoid=False, norm_in_kernel=False, stream=None) -> None:
     """include/gdn.h gdn_decode; `state` [slots,Hv,Dv,Dk] f32 updated in place.
     With norm_weight (and norm_z) the gated RMSNorm is applied to `out`."""
     B, Hk, Dk = q.shape
     _, Hv, Dv = v.shape
     sih, sih_p = _host_i32(state_indices_host)
-    nrm, nrm_p = _out_norm(norm_z, norm_weight, norm_eps, norm_sigmoid, B, Hv, Dv)
+    nrm, nrm_p = _out_norm(norm_z, norm_weight, norm_eps, norm_sigmoid, B, Hv, Dv, norm_in_kernel)
     a = gdn_decode_args(
         B=B, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, act_dtype=_dt(q), use_qk_l2norm=int(use_qk_l2norm),
         scale=float(scale), q=_p(q), q_len=_n(q), k=_p(k), k_len=_n(k), v=_p(v), v_len=_n(v),
@@ -349,22 +355,40 @@ def gdn_decode(q, k, v, g, beta, state, out, *, scale=-1.0, state_indices=None,
     _check(lib().gdn_decode(ctypes.byref(a), _stream(stream)))
 
 
+def gdn_kda_resolve_algo(T, N, Dk, Dv, act_dtype=GDN_DTYPE_BF16, algo=GDN_PREFILL_AUTO) -> int:
+    return int(lib().gdn_kda_resolve_algo(T, N, Dk, Dv, act_dtype, algo))
+
+
+def gdn_kda_workspace_bytes(T, N, Hv, Dk, Dv, act_dtype=GDN_DTYPE_BF16,
+                            algo=GDN_PREFILL_AUTO) -> int:
+    return int(lib().gdn_kda_workspace_bytes(T, N, Hv, Dk, Dv, act_dtype, algo))
+
+
 def gdn_kda_varlen(q, k, v, g, beta, state, cu_seqlens, out, *, scale=-1.0, state_indices=None,
                    has_initial_state=None, cu_seqlens_host=None, state_indices_host=None,
-                   stream=None) -> None:
-    """include/gdn.h gdn_kda_varlen; g [T, Hv, Dk] f32; `state` updated in place."""
+                   algo=GDN_PREFILL_AUTO, workspace=None, stream=None) -> None:
+    """include/gdn.h gdn_kda_varlen; g [T, Hv, Dk] f32; `state` updated in place.
+    `workspace`: a uint8 device tensor of at least gdn_kda_workspace_bytes()
+    bytes; when None and the resolved algorithm needs one, one is allocated
+    here for the call."""
     T, Hk, Dk = q.shape
     _, Hv, Dv = v.shape
     N = cu_seqlens.numel() - 1
     cuh, cuh_p = _host_i32(cu_seqlens_host)
     sih, sih_p = _host_i32(state_indices_host)
+    if workspace is None:
+        nbytes = gdn_kda_workspace_bytes(T, N, Hv, Dk, Dv, _dt(q), algo)
+        if nbytes:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     a = gdn_kda_args(
         T=T, N=N, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, act_dtype=_dt(q), scale=float(scale),
         q=_p(q), q_len=_n(q), k=_p(k), k_len=_n(k), v=_p(v), v_len=_n(v), g=_p(g), g_len=_n(g),
         beta=_p(beta), beta_len=_n(beta), state=_p(state), state_slots=state.shape[0],
         state_len=_n(state), cu_seqlens=_p(cu_seqlens), state_indices=_p(state_indices),
         has_initial_state=_p(has_initial_state), cu_seqlens_host=cuh_p,
-        state_indices_host=sih_p, out=_p(out), out_len=_n(out))
+        state_indices_host=sih_p, out=_p(out), out_len=_n(out), algo=int(algo),
+        workspace=_p(workspace),
+        workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size())
     _check(lib().gdn_kda_varlen(ctypes.byref(a), _stream(stream)))
 
 

@@ -20,7 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libgdn.so")
 
 SOURCES = ["gdn_api.cpp", "gdn_status.cu", "gdn_prepare.cu", "gdn_recurrent.cu", "gdn_fused.cu",
-           "gdn_chunked.cu", "gdn_noalloc.cu", "gdn_norm.cu", "gdn_packed.cu"]
+           "gdn_chunked.cu", "gdn_kda_chunked.cu", "gdn_noalloc.cu", "gdn_norm.cu", "gdn_packed.cu"]
 HEADERS = ["gdn_internal.h", "tcgen05.cuh", "gdn_math.cuh", "gdn_rowstep.cuh", "gdn_chunk_common.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

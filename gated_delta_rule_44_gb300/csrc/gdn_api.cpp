@@ -126,6 +126,7 @@ int check_out_norm(const gdn_out_norm* n, int64_t tokens, int64_t Hv, int64_t Dv
   p.onorm_w = n->weight;
   p.onorm_eps = n->eps;
   p.onorm_sigmoid = n->sigmoid_gate != 0;
+  p.onorm_in_kernel = n->in_kernel != 0;
   return GDN_OK;
 }
 
@@ -567,9 +568,9 @@ int gdn_decode(const gdn_decode_args* a, void* stream) {
   p.status = gdn::status_word();
   if (p.status == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (p.onorm_w == nullptr || gdn::decode_norm_in_kernel(p.Dk, p.Dv))
+  if (p.onorm_w == nullptr || (p.onorm_in_kernel && gdn::decode_norm_in_kernel(p.Dk, p.Dv)))
     return launch_result(gdn::launch_decode(p, st), "gdn_decode");
-  // a row wider than one cluster of slices: the norm as a second kernel
+  // the norm as a second kernel over the output in place
   gdn::RecurLaunch plain = p;
   plain.onorm_w = nullptr;
   if (int rc = launch_result(gdn::launch_decode(plain, st), "gdn_decode")) return rc;
@@ -601,6 +602,21 @@ int gdn_kda_varlen(const gdn_kda_args* a, void* stream) {
     return fail(GDN_ERR_UNSUPPORTED, "gdn_kda_varlen supports Dk in {16, 32, 64, 128, 256}");
   if (!fits_i32(a->T * a->Hv * a->Dk))
     return fail(GDN_ERR_UNSUPPORTED, "kda_gated_delta_rule sizes exceed 32-bit indexing");
+  if (a->algo != GDN_PREFILL_AUTO && a->algo != GDN_PREFILL_CHUNKED &&
+      a->algo != GDN_PREFILL_RECURRENT)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "unknown or unsupported KDA algo " + S(a->algo));
+  const int32_t algo = gdn_kda_resolve_algo(a->T, a->N, a->Dk, a->Dv, a->act_dtype, a->algo);
+  if (algo == GDN_PREFILL_CHUNKED) {
+    if (!gdn::kda_chunked_supported((int)a->Dk, (int)a->Dv, a->act_dtype == GDN_DTYPE_BF16))
+      return fail(GDN_ERR_UNSUPPORTED,
+                  "the chunked KDA prefill supports bf16 activations with Dk = Dv = 128");
+    const size_t need = gdn::kda_chunked_workspace_bytes(a->T, a->N, a->Hv, a->Dk, a->Dv);
+    if (a->workspace == nullptr || a->workspace_bytes < need)
+      return fail(GDN_ERR_INVALID_ARGUMENT, "gdn_kda_varlen workspace needs " + S((int64_t)need) +
+                                                " bytes, got " + S((int64_t)a->workspace_bytes));
+    if ((reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0)
+      return fail(GDN_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
+  }
   gdn::RecurLaunch p{};
   p.T = (int)a->T;
   p.N = (int)a->N;
@@ -624,7 +640,27 @@ int gdn_kda_varlen(const gdn_kda_args* a, void* stream) {
   p.out = a->out;
   p.status = gdn::status_word();
   if (p.status == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
+  if (algo == GDN_PREFILL_CHUNKED) {
+    gdn::ChunkedLaunch c{p, a->workspace, a->workspace_bytes};
+    return launch_result(gdn::launch_kda_chunked(c, static_cast<cudaStream_t>(stream)),
+                         "gdn_kda_varlen(chunked)");
+  }
   return launch_result(gdn::launch_kda(p, static_cast<cudaStream_t>(stream)), "gdn_kda_varlen");
+}
+
+int32_t gdn_kda_resolve_algo(int64_t T, int64_t N, int64_t Dk, int64_t Dv, int32_t act_dtype,
+                             int32_t algo) {
+  if (algo != GDN_PREFILL_AUTO) return algo;
+  return T > N && gdn::kda_chunked_supported((int)Dk, (int)Dv, act_dtype == GDN_DTYPE_BF16)
+             ? GDN_PREFILL_CHUNKED
+             : GDN_PREFILL_RECURRENT;
+}
+
+size_t gdn_kda_workspace_bytes(int64_t T, int64_t N, int64_t Hv, int64_t Dk, int64_t Dv,
+                               int32_t act_dtype, int32_t algo) {
+  if (gdn_kda_resolve_algo(T, N, Dk, Dv, act_dtype, algo) != GDN_PREFILL_CHUNKED) return 0;
+  if (T <= 0 || N <= 0 || Hv <= 0) return 0;
+  return gdn::kda_chunked_workspace_bytes(T, N, Hv, Dk, Dv);
 }
 
 int gdn_spec_decode(const gdn_spec_decode_args* a, void* stream) {
@@ -886,13 +922,15 @@ int gdn_prefill_varlen(const gdn_prefill_args* a, void* stream) {
     if (p.onorm_w == nullptr) return GDN_OK;
     return launch_result(launch_out_norm_pass(p, st), "gdn_prefill_varlen(output norm)");
   }
-  if (algo == GDN_PREFILL_FUSED) {  // applies the output norm itself
+  if (algo == GDN_PREFILL_FUSED) {
     if (!gdn::fused_supported((int)a->Dk, (int)a->Dv, p.bf16))
       return fail(GDN_ERR_UNSUPPORTED,
                   "the fused chunked prefill supports bf16 activations with Dk = Dv = 128");
     p.status = gdn::status_word();
     if (p.status == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
-    return launch_result(gdn::launch_fused(p, st), "gdn_prefill_varlen(fused)");
+    if (int rc = launch_result(gdn::launch_fused(p, st), "gdn_prefill_varlen(fused)")) return rc;
+    if (p.onorm_w == nullptr) return GDN_OK;
+    return launch_result(launch_out_norm_pass(p, st), "gdn_prefill_varlen(output norm)");
   }
   if (!gdn::recurrent_supported((int)a->Dk))
     return fail(GDN_ERR_UNSUPPORTED, "the recurrent prefill supports Dk in {16, 32, 64, 128, 256}");

@@ -120,6 +120,61 @@ __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
   return raw + ((1024u - (umma::smem_u32(raw) & 1023u)) & 1023u);
 }
 
+// Sequence and chunk-in-sequence of global chunk `gc`, from cu_seqlens (warp 0).
+// Returns false when gc is past the last chunk or cu_seqlens is malformed.
+__device__ inline bool locate_chunk(const int32_t* __restrict__ cu, int N, int T, int gc, int& s_out,
+                             int& j_out, bool& bad) {
+  const int lane = threadIdx.x & 31;
+  int base = 0;
+  bad = false;
+  for (int s0 = 0; s0 < N; s0 += 32) {
+    const int s = s0 + lane;
+    int nc = 0;
+    if (s < N) {
+      const int lo = __ldg(cu + s), hi = __ldg(cu + s + 1);
+      if (lo < 0 || hi <= lo || hi > T) bad = true;
+      nc = hi > lo ? (hi - lo + kC - 1) / kC : 0;
+    }
+    int incl = nc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int excl = incl - nc;
+    const unsigned hit =
+        __ballot_sync(0xffffffffu, nc > 0 && gc >= base + excl && gc < base + incl);
+    bad = __any_sync(0xffffffffu, bad);
+    if (hit) {
+      const int src = __ffs(hit) - 1;
+      s_out = s0 + src;
+      j_out = gc - base - __shfl_sync(0xffffffffu, excl, src);
+      return !bad;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return false;
+}
+
+// First global chunk of sequence s (sum of earlier sequences' chunk counts);
+// `bad` reports an empty or decreasing earlier range (warp 0).
+__device__ inline int chunk_base(const int32_t* __restrict__ cu, int s, bool& bad) {
+  int b = 0;
+  bool nb = false;
+  for (int i = threadIdx.x & 31; i < s; i += 32) {
+    const int len = __ldg(cu + i + 1) - __ldg(cu + i);
+    nb |= len <= 0;
+    b += len > 0 ? (len + kC - 1) / kC : 0;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) b += __shfl_xor_sync(0xffffffffu, b, o);
+  bad = __any_sync(0xffffffffu, nb);
+  return b;
+}
+
+// Upper bound on the chunks of T tokens in N non-empty sequences.
+inline int64_t max_chunks(int64_t T, int64_t N) { return T / kC + N; }
+
 // ---- host: TMA tensor maps --------------------------------------------------------
 
 inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

@@ -60,7 +60,6 @@
 
 #include "gdn_chunk_common.cuh"
 #include "gdn_internal.h"
-#include "gdn_math.cuh"
 #include "tcgen05.cuh"
 
 namespace gdn {
@@ -110,46 +109,6 @@ enum Mb : int {
   kMbKq0 = 0, kMbKq1, kMbKqFree0, kMbKqFree1, kMbV, kMbG, kMbGRead, kMbTwTu, kMbWu, kMbWImg,
   kMbPImg, kMbFac, kMbD1, kMbD1Free, kMbUReady, kMbSImg, kMbD2, kMbD3, kMbOFree, kMbEnd, kNumMb
 };
-
-// D (+)= A[tmem] * B[smem]: the A operand in tensor memory (M = 128 lanes, K
-// packed two bf16 per 32-bit column, the even element in the low half).
-__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, bool accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
-      : "memory");
-}
-
-// 32 lanes x 8 columns of 32-bit values from registers.
-__device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&v)[8]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-      : "memory");
-}
-
-// 32 lanes x 32 columns of 32-bit values from registers.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(
-          taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
-      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
-      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
-      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
-      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
-      : "memory");
-}
 
 // Bounded wait that also gives up as soon as another role has given up.
 __device__ __forceinline__ bool wait_mb(uint32_t mb, uint32_t parity, volatile int* abort,
@@ -794,12 +753,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
       fence_after_sync();
       {
         // 32 tokens at a time through the staging rows: each thread writes its
-        // dv of every token, then the rows leave as 16-byte vectors.  A token
-        // row is 16 consecutive lanes, so the output norm's sum of squares is
-        // four shuffles within the half-warp.
+        // dv of every token, then the rows leave as 16-byte vectors.
         __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + FusedSmem::OST);
         const int stid = tid - 320;  // 0..127
-        const bool onorm = p.onorm_w != nullptr;
+        const int c16 = stid & 15;   // this thread's 16-byte vector of every row it copies
 #pragma unroll 1
         for (int j0 = 0; j0 < kC && j0 < L; j0 += 32) {
           float o[32];
@@ -810,30 +767,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
           named_bar(kBarScan, kScanThreads);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const int idx = q * kScanThreads + stid;  // 16-byte vector: token idx / 16
-            const int r = idx >> 4, c16 = idx & 15;
+            const int r = (q * kScanThreads + stid) >> 4;  // the vector's token row
             __nv_bfloat16* dst = out + ((int64_t)(t0 + j0 + r) * p.Hv + h) * kD + c16 * 8;
-            if (onorm) {
-              float x[8];
-              ld_bf16x8(ost + r * kD + c16 * 8, x);
-              float ss = 0.0f;
-#pragma unroll
-              for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
-#pragma unroll
-              for (int m = 8; m > 0; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-              if (j0 + r < L) {
-                const float inv = math::rms_inv(ss, 1.0f / kD, p.onorm_eps);
-                float z[8], w[8];
-                ld_bf16x8(static_cast<const __nv_bfloat16*>(p.onorm_z) +
-                              (int64_t)(t0 + j0 + r) * p.onorm_z_stride + (int64_t)h * kD + c16 * 8,
-                          z);
-                ld_bf16x8(static_cast<const __nv_bfloat16*>(p.onorm_w) + c16 * 8, w);
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                  x[e] = x[e] * inv * w[e] * math::norm_gate(z[e], p.onorm_sigmoid);
-                st_bf16x8(dst, x);
-              }
-            } else if (j0 + r < L) {
+            if (j0 + r < L) {
               *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(ost + r * kD + c16 * 8);
             }
           }

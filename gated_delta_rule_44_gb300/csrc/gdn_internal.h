@@ -86,6 +86,7 @@ struct RecurLaunch {
   const void* onorm_w;
   float onorm_eps;
   bool onorm_sigmoid;
+  bool onorm_in_kernel;  // decode: inside the recurrence kernel where it fits
 };
 cudaError_t launch_decode(const RecurLaunch& p, cudaStream_t s);
 cudaError_t launch_recurrent(const RecurLaunch& p, cudaStream_t s);
@@ -98,7 +99,8 @@ cudaError_t launch_kda(const RecurLaunch& p, cudaStream_t s);
 cudaError_t launch_spec_decode(const RecurLaunch& p, cudaStream_t s);
 bool recurrent_supported(int Dk);
 // Whether gdn_decode applies the output norm inside the recurrence kernel
-// (the row's value-dimension slices fit one cluster of at most 8 CTAs).
+// (the row's value-dimension slices, 64 rows each at Dk = 128, fit one CTA
+// of at most 4 x 128 threads).
 bool decode_norm_in_kernel(int Dk, int Dv);
 
 // Decode in one launch from the packed projections: conv update, SiLU, q/k
@@ -134,6 +136,12 @@ struct ChunkedLaunch {
   size_t workspace_bytes;
 };
 bool chunked_supported(int Dk, int Dv, bool bf16);
+
+// The chunked form of the KDA recurrence (g [T, Hv, Dk]; p.norm false): two
+// launches over a caller workspace of kda_chunked_workspace_bytes().
+bool kda_chunked_supported(int Dk, int Dv, bool bf16);
+size_t kda_chunked_workspace_bytes(int64_t T, int64_t N, int64_t Hv, int64_t Dk, int64_t Dv);
+cudaError_t launch_kda_chunked(const ChunkedLaunch& c, cudaStream_t s);
 
 // The same chunked form in one persistent launch (no workspace).
 bool fused_supported(int Dk, int Dv, bool bf16);

@@ -1,0 +1,840 @@
+// gdn_kda_chunked.cu -- chunked (C = 64) varlen prefill of the KDA recurrence
+// (one log decay per KEY CHANNEL) on tcgen05 tensor cores.
+//
+// [cpu_ops.cpp] (vllm.cpp, src/vt/cpu/cpu_ops.cpp) KdaHeadTokenStep /
+// KdaGatedDeltaRuleKernel define the recurrence token by token, per (sequence,
+// value head) with state S = [Dv, Dk]:
+//   S[:, d] *= e^{g_t[d]};  u = beta_t (v_t - S k_t);  S += u k_t^T;  o_t = S (scale q_t)
+// and the KdaChunkPrefillKernel comment names a chunked GPU form without
+// printing it.  The chunk form below is derived from the recurrence.  For one
+// chunk of L <= 64 tokens with state S0 at its start, E_t = e^{g_t} (per
+// channel) and products of E over token ranges, every one a decay from an
+// earlier token to a later one (so none exceeds 1 when g <= 0):
+//   A_ts = beta_t sum_d k_t[d] k_s[d] prod_{s<u<=t} E_u[d]     (s < t)
+//   P_ts = scale  sum_d q_t[d] k_s[d] prod_{s<u<=t} E_u[d]     (s <= t)
+//   T = (I + A)^-1,  Tb = T diag(beta)
+//   Ke_t = k_t . prod_{u<=t} E_u,  Qe_t = q_t . prod_{u<=t} E_u,  Kd_s = k_s . prod_{u>s} E_u
+//   W = Tb Ke,  Ut = Tb V,  U = Ut - W S0^T
+//   O = scale Qe S0^T + P U
+//   S_L = S0 diag(prod_u E_u) + U^T Kd
+//
+// A and P.  The decay inside each dot product depends on the channel, so it
+// cannot be taken out as in the scalar-decay form.  They are computed on CUDA
+// cores in f32 from operands scaled about 16-token sub-chunk boundaries: for
+// t in sub-chunk I and s in an earlier sub-chunk J,
+//   prod_{s<u<=t} E_u = Fwd_t . Mid_IJ . Bwd_s
+// with Fwd_t the product from the start of I to t, Bwd_s the product from s + 1
+// to the end of J and Mid_IJ the products of the whole sub-chunks between them
+// (each factor a decay, <= 1).  Pairs inside one sub-chunk take running
+// products of E from s to t.
+//
+// Two launches on the caller's stream:
+//  1. kda_prep (one CTA per (chunk, value head), all chunks in parallel): E, A
+//     and P (f32), T by 16 x 16 blocks, W^T = Ke^T Tb^T (tcgen05); writes the
+//     chunk's blob: the -W^T, P, Tb, Qe and Kd images (hi + lo bf16 pairs but
+//     W) in the shared-memory layouts the second kernel feeds to the tensor
+//     core, and prod_u E_u.
+//  2. kda_scan (one CTA per (sequence, value head), its chunks in order): per
+//     chunk, loads the blob and V, then
+//        D1 = [Ut^T - S W^T | S Qe^T]   (M = 128 dv; Ut^T = V^T Tb^T on the tensor core)
+//        U^T (hi + lo) into TMEM; D2: S += U^T Kd;  D3: O^T += U^T P^T
+//        S' images for the next D1; S' diag(prod E of the next chunk) in TMEM,
+//        onto which the next D2 accumulates; the output rows.
+//
+// Precision: as the scalar-decay chunked form -- T, S, U, P, Qe and Kd enter
+// the tensor core as hi + lo bf16 pairs (hi = x rounded to 8 significant bits,
+// lo = bf16(x - hi)) with products hi*hi + hi*lo + lo*hi; W and Ke as single
+// bf16 values (W reaches the output only through the W S^T correction).
+//
+// Partial chunks: g and beta of rows past the chunk end are taken as 0, so
+// those rows of T are unit rows, their Tb, W, Ut and U rows are zero, and the
+// K, Q, V rows there (the next sequence's tokens, or zeros past the tensor
+// end) never reach a stored value.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "gdn_chunk_common.cuh"
+#include "gdn_internal.h"
+#include "tcgen05.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace umma;
+using namespace chunk;
+
+constexpr long long kWaitBudget = 2000000000LL;  // ~1 s of SM clock per wait
+
+// Blob of one (chunk, value head) in the workspace.
+constexpr uint32_t kBW = 0;          // -W^T image [128 dk][64 tok], MN-major B operand (16 KB)
+constexpr uint32_t kBP = 16384;      // P hi, P lo: K-major [64 i][64 j] (8 KB each)
+constexpr uint32_t kBT = 32768;      // Tb hi, Tb lo: K-major [64 i][64 s] (8 KB each)
+constexpr uint32_t kBQ = 49152;      // Qe hi, Qe lo: K-major [64 tok][128 dk] (16 KB each)
+constexpr uint32_t kBK = 81920;      // Kd hi, Kd lo: same layout (16 KB each)
+constexpr uint32_t kBImg = 114688;   // the images above: copied to the scan's stage as they are
+constexpr uint32_t kBE = 114688;     // prod_u E_u per channel, f32 [128]
+constexpr uint32_t kBlob = 115712;   // 113 KB
+
+// bf16 element (t, d) of a [64 tok][128] tile stored as two SW128 boxes of 64 columns.
+__device__ __forceinline__ float tile_at(const uint8_t* tile, int t, int d) {
+  return __bfloat162float(
+      *reinterpret_cast<const __nv_bfloat16*>(tile + swz128_offset(t, d, 8192)));
+}
+
+__device__ __forceinline__ void st_bf16(uint8_t* p, float x) {
+  *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(x);
+}
+
+// hi + lo bf16 pair of x into two images at the same offset.
+__device__ __forceinline__ void st_split1(uint8_t* hi, uint8_t* lo, float x) {
+  const float h = split_hi(x);
+  *reinterpret_cast<uint16_t*>(hi) = static_cast<uint16_t>(__float_as_uint(h) >> 16);
+  *reinterpret_cast<__nv_bfloat16*>(lo) = __float2bfloat16_rn(__fsub_rn(x, h));
+}
+
+// ---------------------------------------------------------------------------
+// Kernel 1: per (chunk, value head).  8 warps.
+struct KPrep {
+  static constexpr uint32_t K = 0;           // K tile [64 tok][128 dk], 2 SW128 boxes (TMA)
+  static constexpr uint32_t Q = 16384;       // Q tile
+  static constexpr uint32_t E = 32768;       // e^{g}, f32 [64][128]; then the P hi, lo images
+  static constexpr uint32_t OP = 65536;      // f32 operands of A and P, rows kLd floats apart:
+  static constexpr uint32_t kLd = 132;
+  static constexpr uint32_t KL = OP;                    //   k_t Fwd_t  [64]
+  static constexpr uint32_t QL = OP + 64 * kLd * 4;     //   q_t Fwd_t  [64]
+  static constexpr uint32_t KR = OP + 128 * kLd * 4;    //   k_s Bwd_s  [48]
+  static constexpr uint32_t KE = OP;                    // then: Ke image (16 KB), later -W^T
+  static constexpr uint32_t QE = OP + 16384;            //       Qe hi, lo (16 KB each)
+  static constexpr uint32_t KD = OP + 49152;            //       Kd hi, lo (16 KB each)
+  static constexpr uint32_t TB = OP + 93184;            // Tb hi, lo images (8 KB each)
+  static constexpr uint32_t AT = TB + 16384;            // A, then T in place, f32 [64][kAs]
+  static constexpr uint32_t kAs = 68;
+  static constexpr uint32_t PM = AT + 64 * kAs * 4;     // P, f32 [64][kAs]
+  static constexpr uint32_t Z = PM + 64 * kAs * 4;      // T solve scratch [3][16][16]
+  static constexpr uint32_t BLK = Z + 3 * 256 * 4;      // sub-chunk products [4][128]
+  static constexpr uint32_t MID = BLK + 4 * 128 * 4;    // Mid_20, Mid_31, Mid_30 [3][128]
+  static constexpr uint32_t BETA = MID + 3 * 128 * 4;   // [64]
+  static constexpr uint32_t EL = BETA + 64 * 4;         // prod_u E_u [128]
+  static constexpr uint32_t BYTES = EL + 128 * 4;
+};
+static_assert(KPrep::KR + 48 * KPrep::kLd * 4 <= KPrep::TB, "operands fit before Tb");
+static_assert(KPrep::KD + 32768 <= KPrep::TB, "images fit before Tb");
+static_assert(KPrep::BYTES + 1024 <= 232448, "shared memory per CTA");
+constexpr int kPrepThreads = 256;
+
+__global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const RecurLaunch p, uint8_t* __restrict__ ws) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = aligned_smem(smem_raw);
+  __shared__ uint64_t mbar_tma, mbar_mma;
+  __shared__ uint32_t tslot;
+  __shared__ int s_seq, s_chunk, s_ok;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gc = blockIdx.x, h = blockIdx.y;
+  const int hk = h / (p.Hv / p.Hk);
+
+  if (warp == 0) {
+    int s = 0, j = 0;
+    bool bad = false;
+    const bool ok = locate_chunk(p.cu, p.N, p.T, gc, s, j, bad);
+    if (lane == 0) {
+      s_seq = s;
+      s_chunk = j;
+      s_ok = ok ? 1 : 0;
+      if (bad && gc == 0 && h == 0) atomicOr(p.status, kStatusBadSeqlens);
+    }
+  }
+  __syncthreads();
+  if (!s_ok) return;  // uniform: past the last chunk (or malformed cu_seqlens)
+  const int t0 = __ldg(p.cu + s_seq) + kC * s_chunk;
+  const int L = min(kC, __ldg(p.cu + s_seq + 1) - t0);
+  const uint32_t base = smem_u32(sm);
+  const uint32_t mb_tma = smem_u32(&mbar_tma), mb_mma = smem_u32(&mbar_mma);
+  uint8_t* blob = ws + ((int64_t)gc * p.Hv + h) * kBlob;
+
+  if (tid == 0) {
+    mbar_init(mb_tma, 1);
+    mbar_init(mb_mma, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    mbar_expect_tx(mb_tma, 4 * 8192);
+    tma_load_3d(base + KPrep::K, &tm_k, mb_tma, 0, hk, t0);
+    tma_load_3d(base + KPrep::K + 8192, &tm_k, mb_tma, 64, hk, t0);
+    tma_load_3d(base + KPrep::Q, &tm_q, mb_tma, 0, hk, t0);
+    tma_load_3d(base + KPrep::Q + 8192, &tm_q, mb_tma, 64, hk, t0);
+  }
+  if (warp == 0) tmem_alloc(smem_u32(&tslot), 64);
+
+  const uint8_t* sK = sm + KPrep::K;
+  const uint8_t* sQ = sm + KPrep::Q;
+  float* sE = reinterpret_cast<float*>(sm + KPrep::E);
+  float* sKL = reinterpret_cast<float*>(sm + KPrep::KL);
+  float* sQL = reinterpret_cast<float*>(sm + KPrep::QL);
+  float* sKR = reinterpret_cast<float*>(sm + KPrep::KR);
+  float* sA = reinterpret_cast<float*>(sm + KPrep::AT);
+  float* sP = reinterpret_cast<float*>(sm + KPrep::PM);
+  float* sZ = reinterpret_cast<float*>(sm + KPrep::Z);
+  float* sBlk = reinterpret_cast<float*>(sm + KPrep::BLK);
+  float* sMid = reinterpret_cast<float*>(sm + KPrep::MID);
+  float* sBeta = reinterpret_cast<float*>(sm + KPrep::BETA);
+  float* sEL = reinterpret_cast<float*>(sm + KPrep::EL);
+  constexpr int LD = KPrep::kLd, AS = KPrep::kAs;
+  const int d = tid & 127, half = tid >> 7;
+
+  // E = e^{g} (g taken as 0 past the chunk end), beta (0 past the end).
+  for (int r = 0; r < 32; ++r) {
+    const int t = half * 32 + r;
+    const float gv = t < L ? __ldg(p.g + ((int64_t)(t0 + t) * p.Hv + h) * kD + d) : 0.0f;
+    sE[t * kD + d] = expf(gv);
+  }
+  if (tid < 64) sBeta[tid] = tid < L ? __ldg(p.beta + (int64_t)(t0 + tid) * p.Hv + h) : 0.0f;
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = tslot;
+  bool ok = __syncthreads_and(mbar_wait(mb_tma, 0, kWaitBudget));
+  if (!ok) {  // the K, Q tiles did not land: touch none of their bytes
+    if (tid == 0) {
+      atomicOr(p.status, kStatusTimeout);
+      mbar_wait(mb_tma, 0, kWaitBudget);  // let the copies in flight finish
+    }
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 64);
+    return;
+  }
+
+  // Scaled operands: thread (d, half) owns sub-chunks 2 half and 2 half + 1 of
+  // channel d.  Fwd runs from the sub-chunk start to t, Bwd from s + 1 to the
+  // sub-chunk end.
+  for (int bb = 0; bb < 2; ++bb) {
+    const int b = 2 * half + bb;
+    float f = 1.0f;
+    for (int r = 0; r < 16; ++r) {
+      const int t = 16 * b + r;
+      f *= sE[t * kD + d];
+      sKL[t * LD + d] = tile_at(sK, t, d) * f;
+      sQL[t * LD + d] = tile_at(sQ, t, d) * f;
+    }
+    sBlk[b * kD + d] = f;
+    if (b < 3) {
+      float w = 1.0f;
+      for (int r = 15; r >= 0; --r) {
+        const int t = 16 * b + r;
+        sKR[t * LD + d] = tile_at(sK, t, d) * w;
+        w *= sE[t * kD + d];
+      }
+    }
+  }
+  __syncthreads();
+  if (tid < 128) {  // products of the whole sub-chunks between I and J
+    sMid[d] = sBlk[1 * kD + d];                          // (I, J) = (2, 0)
+    sMid[kD + d] = sBlk[2 * kD + d];                     // (3, 1)
+    sMid[2 * kD + d] = sBlk[1 * kD + d] * sBlk[2 * kD + d];  // (3, 0)
+  }
+  __syncthreads();
+
+  // Off-diagonal sub-blocks (t in I, s in J < I): warp w < 6 takes the pair
+  // (I, J) = (1,0), (2,0), (2,1), (3,0), (3,1), (3,2); lane r < 16 row 16 I + r
+  // of A, lane r >= 16 the same row of P; 16 columns each.
+  if (warp < 6) {
+    const int I = warp < 1 ? 1 : warp < 3 ? 2 : 3;
+    const int J = warp - I * (I - 1) / 2;
+    const int mi = I - J == 2 ? J : I - J == 3 ? 2 : -1;
+    const int t = 16 * I + (lane & 15);
+    const float* lrow = (lane < 16 ? sKL : sQL) + t * LD;
+    const float* mrow = sMid + (mi < 0 ? 0 : mi) * kD;
+    const float* kr = sKR + 16 * J * LD;
+    float acc[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) acc[c] = 0.0f;
+#pragma unroll 2
+    for (int dd = 0; dd < kD; dd += 4) {
+      float4 a = *reinterpret_cast<const float4*>(lrow + dd);
+      if (mi >= 0) {
+        const float4 m = *reinterpret_cast<const float4*>(mrow + dd);
+        a.x *= m.x;
+        a.y *= m.y;
+        a.z *= m.z;
+        a.w *= m.w;
+      }
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float4 kv = *reinterpret_cast<const float4*>(kr + c * LD + dd);
+        acc[c] = fmaf(a.x, kv.x, acc[c]);
+        acc[c] = fmaf(a.y, kv.y, acc[c]);
+        acc[c] = fmaf(a.z, kv.z, acc[c]);
+        acc[c] = fmaf(a.w, kv.w, acc[c]);
+      }
+    }
+    const float f = lane < 16 ? sBeta[t] : p.scale;
+    float* dst = (lane < 16 ? sA : sP) + t * AS + 16 * J;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) dst[c] = f * acc[c];
+  }
+
+  // Diagonal sub-blocks: thread (b, s, dq) carries R = k_s . prod_{s<u<=t} E_u
+  // over 32 channels from t = s to the end of the sub-chunk; the four channel
+  // quarters are added by shuffles.
+  {
+    const int b = tid >> 6, s = (tid >> 2) & 15, dq = tid & 3;
+    float a[16], pp[16];
+#pragma unroll
+    for (int tt = 0; tt < 16; ++tt) a[tt] = pp[tt] = 0.0f;
+#pragma unroll 1
+    for (int dc = 0; dc < 4; ++dc) {
+      const int d0 = 32 * dq + 8 * dc;
+      float R[8];
+      ld_bf16x8(sK + swz128_offset(16 * b + s, d0, 8192), R);
+#pragma unroll
+      for (int tt = 0; tt < 16; ++tt) {
+        if (tt >= s) {
+          const int t = 16 * b + tt;
+          float kt[8], qt[8];
+          ld_bf16x8(sK + swz128_offset(t, d0, 8192), kt);
+          ld_bf16x8(sQ + swz128_offset(t, d0, 8192), qt);
+          if (tt > s) {
+            const float4 e0 = *reinterpret_cast<const float4*>(sE + t * kD + d0);
+            const float4 e1 = *reinterpret_cast<const float4*>(sE + t * kD + d0 + 4);
+            R[0] *= e0.x;
+            R[1] *= e0.y;
+            R[2] *= e0.z;
+            R[3] *= e0.w;
+            R[4] *= e1.x;
+            R[5] *= e1.y;
+            R[6] *= e1.z;
+            R[7] *= e1.w;
+          }
+          float sa = 0.0f, sp = 0.0f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            sa = fmaf(kt[e], R[e], sa);
+            sp = fmaf(qt[e], R[e], sp);
+          }
+          a[tt] += sa;
+          pp[tt] += sp;
+        }
+      }
+    }
+#pragma unroll
+    for (int tt = 0; tt < 16; ++tt) {
+      a[tt] += __shfl_xor_sync(0xffffffffu, a[tt], 1);
+      a[tt] += __shfl_xor_sync(0xffffffffu, a[tt], 2);
+      pp[tt] += __shfl_xor_sync(0xffffffffu, pp[tt], 1);
+      pp[tt] += __shfl_xor_sync(0xffffffffu, pp[tt], 2);
+    }
+    if (dq == 0) {
+#pragma unroll
+      for (int tt = 0; tt < 16; ++tt) {
+        const int t = 16 * b + tt;
+        if (tt > s) sA[t * AS + 16 * b + s] = sBeta[t] * a[tt];
+        if (tt >= s) sP[t * AS + 16 * b + s] = p.scale * pp[tt];
+      }
+    }
+  }
+  __syncthreads();  // A and P complete; the f32 operands are dead
+
+  // Images over the operand space: thread (d, 0) runs prod_{u<=t} E_u forward
+  // (Ke, Qe and prod_u E_u), thread (d, 1) prod_{u>s} E_u backward (Kd).
+  if (half == 0) {
+    float pre = 1.0f;
+    for (int t = 0; t < kC; ++t) {
+      pre *= sE[t * kD + d];
+      const uint32_t off = swz128_offset(t, d, 8192);
+      st_bf16(sm + KPrep::KE + off, tile_at(sK, t, d) * pre);
+      st_split1(sm + KPrep::QE + off, sm + KPrep::QE + 16384 + off, tile_at(sQ, t, d) * pre);
+    }
+    sEL[d] = pre;
+  } else {
+    float suf = 1.0f;
+    for (int t = kC - 1; t >= 0; --t) {
+      const uint32_t off = swz128_offset(t, d, 8192);
+      st_split1(sm + KPrep::KD + off, sm + KPrep::KD + 16384 + off, tile_at(sK, t, d) * suf);
+      suf *= sE[t * kD + d];
+    }
+  }
+
+  // T = (I + A)^-1.  The four 16 x 16 diagonal blocks by forward substitution
+  // (lane = column; a block's 16 columns are one half-warp) ...
+  if (tid < 64) {
+    const int b0 = 16 * (tid >> 4), c = tid & 15;
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const float* arow = sA + (b0 + r) * AS + b0;
+      float acc = r == c ? 1.0f : 0.0f;
+#pragma unroll
+      for (int m = 0; m < r; ++m) acc = fmaf(-arow[m], x[m], acc);
+      x[r] = acc;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < 16; ++r) sA[(b0 + r) * AS + b0 + c] = x[r];
+  }
+  __syncthreads();
+  // ... then block row I from the rows above it:
+  //   Z_IJ = sum_{J <= K < I} A_IK T_KJ,  T_IJ = -T_II Z_IJ.
+  {
+    const int r = tid >> 4, c = tid & 15;
+    for (int I = 1; I < 4; ++I) {
+      for (int J = 0; J < I; ++J) {
+        float z = 0.0f;
+        for (int K = J; K < I; ++K) {
+          const float* arow = sA + (16 * I + r) * AS + 16 * K;
+#pragma unroll
+          for (int m = 0; m < 16; ++m) z = fmaf(arow[m], sA[(16 * K + m) * AS + 16 * J + c], z);
+        }
+        sZ[J * 256 + r * 16 + c] = z;
+      }
+      __syncthreads();
+      for (int J = 0; J < I; ++J) {
+        const float* trow = sA + (16 * I + r) * AS + 16 * I;
+        float y = 0.0f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) y = fmaf(trow[m], sZ[J * 256 + m * 16 + c], y);
+        sA[(16 * I + r) * AS + 16 * J + c] = -y;
+      }
+      __syncthreads();
+    }
+  }
+
+  // Tb = T diag(beta) and P as hi + lo images (zero above the diagonal); the P
+  // images take the space of E, which is dead.
+  for (int item = tid; item < 64 * 8; item += kPrepThreads) {
+    const int i = item >> 3, q = item & 7;
+    float tv[8], pv[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int sc = 8 * q + e;
+      tv[e] = sc <= i ? sA[i * AS + sc] * sBeta[sc] : 0.0f;
+      pv[e] = sc <= i ? sP[i * AS + sc] : 0.0f;
+    }
+    const uint32_t off = swz128_offset(i, 8 * q, 8192);
+    st_split8(sm + KPrep::TB + off, sm + KPrep::TB + 8192 + off, tv);
+    st_split8(sm + KPrep::E + off, sm + KPrep::E + 8192 + off, pv);
+  }
+  fence_proxy_async();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (tid == 0) {
+    // W^T = Ke^T Tb^T (M = 128 dk, N = 64 tokens, K = 64 tokens): A = Ke MN-major,
+    // B = Tb hi, lo (K-major).
+    const uint32_t idesc = idesc_bf16_f32(128, 64, true, false);
+#pragma unroll
+    for (int part = 0; part < 2; ++part)
+#pragma unroll
+      for (int kk = 0; kk < kC; kk += 16)
+        mma_bf16(tmem, desc_sw128(base + KPrep::KE + (kk / 8) * 1024, 8192, 1024),
+                 desc_sw128(base + KPrep::TB + part * 8192 + kk * 2, 16, 1024), idesc,
+                 part > 0 || kk > 0);
+    mma_commit(mb_mma);
+  } else if (tid == 32) {  // the images that are final go out meanwhile
+    bulk_s2g(blob + kBP, base + KPrep::E, 16384);
+    bulk_s2g(blob + kBT, base + KPrep::TB, 16384);
+    bulk_s2g(blob + kBQ, base + KPrep::QE, 32768);
+    bulk_s2g(blob + kBK, base + KPrep::KD, 32768);
+    bulk_s2g(blob + kBE, base + KPrep::EL, 512);
+    bulk_commit();
+  }
+  ok = __syncthreads_and(mbar_wait(mb_mma, 0, kWaitBudget));  // uniform: tcgen05.ld is warp-wide
+  fence_after_sync();
+  if (ok && warp < 4) {  // -W^T image over Ke (the MMA has read Ke)
+    const uint32_t la = static_cast<uint32_t>(warp * 32) << 16;
+    const int dk = tid;
+#pragma unroll 1
+    for (int j0 = 0; j0 < kC; j0 += 32) {
+      float w[32];
+      tmem_ld32(tmem + la + j0, w);
+      tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 32; e += 8) {
+        float nv[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) nv[x] = -w[e + x];
+        st_bf16x8(sm + KPrep::KE + swz128_offset(dk, j0 + e, 16384), nv);
+      }
+    }
+  }
+  fence_proxy_async();
+  fence_before_sync();
+  ok = __syncthreads_and(ok);
+  if (tid == 32) {
+    if (ok) {
+      bulk_s2g(blob + kBW, base + KPrep::KE, 16384);
+      bulk_commit();
+    }
+    bulk_wait_all();  // the blob is complete (and the shared memory read) before exit
+  }
+  if (!ok && tid == 0) {
+    atomicOr(p.status, kStatusTimeout);
+    mbar_wait(mb_mma, 0, kWaitBudget);  // the MMA in flight
+  }
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 64);
+}
+
+// ---------------------------------------------------------------------------
+// Kernel 2: per (sequence, value head), its chunks in order.  4 warps; thread
+// dv owns TMEM lane dv (row dv of the state).
+struct KScan {
+  static constexpr uint32_t SH = 0;                 // S hi image [128 dv][128 dk], K-major
+  static constexpr uint32_t SL = 32768;             // S lo image
+  static constexpr uint32_t ST = 65536;             // the chunk's blob images (kBImg bytes)
+  static constexpr uint32_t V = ST + kBImg;         // V tile [64 tok][128 dv], 2 SW128 boxes
+  static constexpr uint32_t OST = V + 16384;        // output staging [32 tok][128 dv] bf16
+  static constexpr uint32_t ELB = OST + 8192;       // prod_u E_u of two chunks, f32 [2][128]
+  static constexpr uint32_t BYTES = ELB + 1024;
+};
+static_assert(KScan::V % 1024 == 0, "swizzled tiles are 1024-byte aligned");
+static_assert(KScan::BYTES + 1024 <= 232448, "shared memory per CTA");
+constexpr uint32_t kSD1 = 0;    // TMEM: D1 = [U^T | O^T] (128 columns)
+constexpr uint32_t kSS = 128;   //       the f32 state S[dv][dk] (128)
+constexpr uint32_t kSU = 256;   //       U^T hi | lo as packed bf16 pairs (32 + 32)
+constexpr int kScanThreads = 128;
+
+__global__ void __launch_bounds__(kScanThreads, 1) kda_scan_kernel(
+    const __grid_constant__ CUtensorMap tm_v, const RecurLaunch p, const uint8_t* __restrict__ ws) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = aligned_smem(smem_raw);
+  __shared__ uint64_t mbar_ld, mbar_el, mbar_mma;
+  __shared__ uint32_t tslot;
+  __shared__ int s_gc0, s_bad;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.x % p.Hv, s = blockIdx.x / p.Hv;
+
+  const int lo = __ldg(p.cu + s), hi = __ldg(p.cu + s + 1);
+  if (lo < 0 || hi <= lo || hi > p.T || __ldg(p.cu) != 0 || __ldg(p.cu + p.N) != p.T) {
+    if (tid == 0) atomicOr(p.status, kStatusBadSeqlens);
+    return;
+  }
+  int slot = p.sidx != nullptr ? __ldg(p.sidx + s) : s;
+  if (slot < -1 || slot >= p.slots) {
+    if (tid == 0) atomicOr(p.status, kStatusBadIndex);
+    slot = -1;
+  }
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+  if (slot < 0) {  // padded sequence: zero outputs, pool untouched
+    for (int idx = tid; idx < (hi - lo) * 16; idx += kScanThreads) {
+      const int t = lo + idx / 16, q16 = idx % 16;
+      *reinterpret_cast<uint4*>(out + ((int64_t)t * p.Hv + h) * kD + q16 * 8) =
+          make_uint4(0, 0, 0, 0);
+    }
+    return;
+  }
+  if (warp == 0) {
+    bool bad = false;
+    const int b = chunk_base(p.cu, s, bad);
+    if (lane == 0) {
+      s_gc0 = b;
+      s_bad = bad ? 1 : 0;
+    }
+  }
+  const uint32_t base = smem_u32(sm);
+  const uint32_t mb_ld = smem_u32(&mbar_ld), mb_el = smem_u32(&mbar_el),
+                 mb_mma = smem_u32(&mbar_mma);
+  if (tid == 0) {
+    mbar_init(mb_ld, 1);
+    mbar_init(mb_el, 1);
+    mbar_init(mb_mma, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(smem_u32(&tslot), 512);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = tslot;
+  if (s_bad) {  // an earlier sequence's range is empty or decreasing
+    if (tid == 0) atomicOr(p.status, kStatusBadSeqlens);
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+    return;
+  }
+  const int nch = (hi - lo + kC - 1) / kC;
+  auto blob = [&](int c) { return ws + ((int64_t)(s_gc0 + c) * p.Hv + h) * kBlob; };
+  const float* elb = reinterpret_cast<const float*>(sm + KScan::ELB);
+  const int dv = tid;
+  const uint32_t la = static_cast<uint32_t>(warp * 32) << 16;
+  float* prow = p.pool + (((int64_t)slot * p.Hv + h) * kD + dv) * kD;
+  const bool init = p.has_init == nullptr || __ldg(p.has_init + s) != 0;
+  // Copies and MMAs issued but not yet seen complete (thread 0's books, for a
+  // clean exit after a wait that gave up).
+  int pend_ld = -1, pend_el = -1, n_mma = 0;
+  bool pend_mma = false;
+
+  if (tid == 0) {
+    mbar_expect_tx(mb_el, 512);
+    bulk_g2s(base + KScan::ELB, blob(0) + kBE, 512, mb_el);
+    pend_el = 0;
+  }
+  bool ok = mbar_wait(mb_el, 0, kWaitBudget);
+  if (tid == 0 && ok) pend_el = -1;
+  // Initial state: its hi + lo images, and S0 diag(prod E) in TMEM.
+  for (int j = 0; j < kD; j += 16) {
+    float v[16];
+#pragma unroll
+    for (int e = 0; e < 16; e += 4) {
+      float4 f = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (init) f = *reinterpret_cast<const float4*>(prow + j + e);
+      v[e] = f.x;
+      v[e + 1] = f.y;
+      v[e + 2] = f.z;
+      v[e + 3] = f.w;
+    }
+#pragma unroll
+    for (int e = 0; e < 16; e += 8) {
+      const uint32_t off = swz128_offset(dv, j + e, 16384);
+      st_split8(sm + KScan::SH + off, sm + KScan::SL + off, v + e);
+    }
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] *= elb[j + e];
+    tmem_st16(tmem + kSS + la + j, v);
+  }
+  tmem_st_wait();
+  fence_proxy_async();
+  fence_before_sync();
+  ok = __syncthreads_and(ok);
+
+  const uint32_t id_ut = idesc_bf16_f32(128, 64, true, false);
+  const uint32_t id_w = idesc_bf16_f32(128, 64, false, true);
+  const uint32_t id_q = idesc_bf16_f32(128, 64, false, false);
+  const uint32_t id_d2 = idesc_bf16_f32(128, 128, false, true);
+  const uint32_t id_d3 = idesc_bf16_f32(128, 64, false, false);
+  __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + KScan::OST);
+
+  for (int c = 0; c < nch && ok; ++c) {
+    const int t0 = lo + c * kC;
+    const int L = min(kC, hi - t0);
+    const bool last = c + 1 == nch;
+    if (tid == 0) {
+      fence_after_sync();
+      const uint8_t* b = blob(c);
+      mbar_expect_tx(mb_ld, kBImg + 2 * 8192);
+      for (uint32_t off = 0; off < kBImg; off += 16384)
+        bulk_g2s(base + KScan::ST + off, b + off, 16384, mb_ld);
+      tma_load_3d(base + KScan::V, &tm_v, mb_ld, 0, h, t0);
+      tma_load_3d(base + KScan::V + 8192, &tm_v, mb_ld, 64, h, t0);
+      pend_ld = c;
+      if (!last) {  // prod E of the next chunk, for the state update of this one
+        mbar_expect_tx(mb_el, 512);
+        bulk_g2s(base + KScan::ELB + ((c + 1) & 1) * 512, blob(c + 1) + kBE, 512, mb_el);
+        pend_el = c + 1;
+      }
+    }
+    ok = __syncthreads_and(mbar_wait(mb_ld, c & 1, kWaitBudget));
+    if (!ok) break;
+    if (tid == 0) {
+      pend_ld = -1;
+      fence_after_sync();
+      // Ut^T = V^T Tb^T into D1[:, 0:64]  (A = V MN-major, M = dv; B = Tb hi, lo)
+#pragma unroll
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int kk = 0; kk < kC; kk += 16)
+          mma_bf16(tmem + kSD1, desc_sw128(base + KScan::V + (kk / 8) * 1024, 8192, 1024),
+                   desc_sw128(base + KScan::ST + kBT + part * 8192 + kk * 2, 16, 1024), id_ut,
+                   part > 0 || kk > 0);
+      // D1[:, 0:64] += S (-W)^T  (A = S hi, lo; B = the -W^T image, MN-major)
+#pragma unroll
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int kk = 0; kk < kD; kk += 16)
+          mma_bf16(tmem + kSD1,
+                   desc_sw128(base + (part ? KScan::SL : KScan::SH) + (kk / 64) * 16384 +
+                                  (kk % 64) * 2,
+                              16, 1024),
+                   desc_sw128(base + KScan::ST + kBW + (kk / 8) * 1024, 8192, 1024), id_w, true);
+      // D1[:, 64:128] = S Qe^T: S hi Qe hi, S lo Qe hi, S hi Qe lo
+#pragma unroll
+      for (int pr = 0; pr < 3; ++pr) {
+        const uint32_t sa = pr == 1 ? KScan::SL : KScan::SH;
+        const uint32_t qo = pr == 2 ? 16384 : 0;
+#pragma unroll
+        for (int kk = 0; kk < kD; kk += 16)
+          mma_bf16(tmem + kSD1 + 64,
+                   desc_sw128(base + sa + (kk / 64) * 16384 + (kk % 64) * 2, 16, 1024),
+                   desc_sw128(base + KScan::ST + kBQ + qo + (kk / 64) * 8192 + (kk % 64) * 2, 16,
+                              1024),
+                   id_q, pr > 0 || kk > 0);
+      }
+      mma_commit(mb_mma);
+      pend_mma = true;
+    }
+    ok = mbar_wait(mb_mma, n_mma & 1, kWaitBudget);
+    ++n_mma;
+    if (tid == 0 && ok) pend_mma = false;
+    ok = __syncthreads_and(ok);  // uniform: tcgen05.ld / st are warp-wide
+    if (!ok) break;
+    fence_after_sync();
+    // U^T = D1[:, 0:64] as hi + lo pairs into TMEM; D1[:, 64:128] scaled in
+    // place: O^T starts as scale (Qe S^T)^T, onto which P U accumulates.
+    {
+#pragma unroll 1
+      for (int j0 = 0; j0 < kC; j0 += 32) {
+        float u[32], qs[32];
+        tmem_ld32(tmem + kSD1 + la + j0, u);
+        tmem_ld32(tmem + kSD1 + 64 + la + j0, qs);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j1 = 0; j1 < 32; j1 += 16) {
+          uint32_t uh[8], ul[8];
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) split2(u[j1 + e], u[j1 + e + 1], uh[e / 2], ul[e / 2]);
+          tmem_st8u(tmem + kSU + la + (j0 + j1) / 2, uh);
+          tmem_st8u(tmem + kSU + 32 + la + (j0 + j1) / 2, ul);
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) qs[e] *= p.scale;
+        tmem_st32(tmem + kSD1 + 64 + la + j0, qs);
+      }
+      tmem_st_wait();
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+      fence_after_sync();
+      // S += U^T Kd: U hi Kd hi, U lo Kd hi, U hi Kd lo (A = U^T from TMEM; B = Kd MN-major)
+#pragma unroll
+      for (int pr = 0; pr < 3; ++pr) {
+        const uint32_t ua = pr == 1 ? 32 : 0;
+        const uint32_t ko = pr == 2 ? 16384 : 0;
+#pragma unroll
+        for (int kk = 0; kk < kC; kk += 16)
+          mma_bf16_ta(tmem + kSS, tmem + kSU + ua + kk / 2,
+                      desc_sw128(base + KScan::ST + kBK + ko + (kk / 8) * 1024, 8192, 1024), id_d2,
+                      true);
+      }
+      // O^T += U^T P^T: U hi P hi, U hi P lo, U lo P hi (B = P, K-major)
+#pragma unroll
+      for (int pr = 0; pr < 3; ++pr) {
+        const uint32_t ua = pr == 2 ? 32 : 0;
+        const uint32_t po = pr == 1 ? 8192 : 0;
+#pragma unroll
+        for (int kk = 0; kk < kC; kk += 16)
+          mma_bf16_ta(tmem + kSD1 + 64, tmem + kSU + ua + kk / 2,
+                      desc_sw128(base + KScan::ST + kBP + po + kk * 2, 16, 1024), id_d3, true);
+      }
+      mma_commit(mb_mma);
+      pend_mma = true;
+    }
+    ok = mbar_wait(mb_mma, n_mma & 1, kWaitBudget);
+    ++n_mma;
+    if (tid == 0 && ok) pend_mma = false;
+    if (!last) {
+      const bool el_ok = mbar_wait(mb_el, (c + 1) & 1, kWaitBudget);
+      if (tid == 0 && el_ok) pend_el = -1;
+      ok = el_ok && ok;
+    }
+    ok = __syncthreads_and(ok);
+    if (!ok) break;
+    fence_after_sync();
+    // S' = S0 diag(prod E) + U^T Kd: its images for the next D1 and S' diag(prod
+    // E of the next chunk) back into TMEM; the last chunk's S' goes to the pool.
+    const float* eln = elb + ((c + 1) & 1) * 128;
+#pragma unroll 1
+    for (int j0 = 0; j0 < kD; j0 += 32) {
+      float v[32];
+      tmem_ld32(tmem + kSS + la + j0, v);
+      tmem_ld_wait();
+      if (last) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(prow + j0 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          const uint32_t off = swz128_offset(dv, j0 + e, 16384);
+          st_split8(sm + KScan::SH + off, sm + KScan::SL + off, v + e);
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] *= eln[j0 + e];
+        tmem_st32(tmem + kSS + la + j0, v);
+      }
+    }
+    // Output rows: 32 tokens at a time through the staging rows.
+#pragma unroll 1
+    for (int j0 = 0; j0 < L; j0 += 32) {
+      float o[32];
+      tmem_ld32(tmem + kSD1 + 64 + la + j0, o);
+      tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) ost[e * kD + dv] = __float2bfloat16_rn(o[e]);
+      __syncthreads();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int idx = q * kScanThreads + tid;  // 16-byte vector: token idx / 16
+        const int r = idx >> 4, c16 = idx & 15;
+        if (j0 + r < L)
+          *reinterpret_cast<uint4*>(out + ((int64_t)(t0 + j0 + r) * p.Hv + h) * kD + c16 * 8) =
+              *reinterpret_cast<const uint4*>(ost + r * kD + c16 * 8);
+      }
+      __syncthreads();
+    }
+    if (!last) tmem_st_wait();
+    fence_proxy_async();
+    fence_before_sync();
+    __syncthreads();
+  }
+
+  // teardown: copies and MMAs still in flight (after a wait that gave up) land
+  // first, then the TMEM is freed.
+  if (!ok && tid == 0) {
+    atomicOr(p.status, kStatusTimeout);
+    if (pend_ld >= 0) mbar_wait(mb_ld, pend_ld & 1, kWaitBudget);
+    if (pend_el >= 0) mbar_wait(mb_el, pend_el & 1, kWaitBudget);
+    if (pend_mma) mbar_wait(mb_mma, (n_mma - 1) & 1, kWaitBudget);
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+bool kda_chunked_supported(int Dk, int Dv, bool bf16) { return bf16 && Dk == kD && Dv == kD; }
+
+size_t kda_chunked_workspace_bytes(int64_t T, int64_t N, int64_t Hv, int64_t Dk, int64_t Dv) {
+  if (Dk != kD || Dv != kD) return 0;
+  return static_cast<size_t>(max_chunks(T, N) * Hv) * kBlob;
+}
+
+cudaError_t launch_kda_chunked(const ChunkedLaunch& c, cudaStream_t s) {
+  const RecurLaunch& p = c.r;
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, p.q, p.T, p.Hk) || !make_map(&tk, p.k, p.T, p.Hk) ||
+      !make_map(&tv, p.v, p.T, p.Hv))
+    return cudaErrorInvalidValue;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(kda_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    KPrep::BYTES + 1024);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(kda_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      KScan::BYTES + 1024);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  uint8_t* ws = static_cast<uint8_t*>(c.workspace);
+  const int64_t nch = max_chunks(p.T, p.N);
+  if (nch > 0x7fffffff || p.Hv > 65535) return cudaErrorInvalidConfiguration;
+  kda_prep_kernel<<<dim3(static_cast<unsigned>(nch), p.Hv), kPrepThreads, KPrep::BYTES + 1024,
+                    s>>>(tq, tk, p, ws);
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t blocks = static_cast<int64_t>(p.N) * p.Hv;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  kda_scan_kernel<<<static_cast<unsigned>(blocks), kScanThreads, KScan::BYTES + 1024, s>>>(tv, p,
+                                                                                           ws);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -59,25 +59,6 @@ __device__ __forceinline__ float round_act<__nv_bfloat16>(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
 }
 
-// Every thread of every CTA of the cluster arrives, then waits: shared-memory
-// writes before it are visible to the cluster's CTAs after it.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n"
-      "barrier.cluster.wait.acquire.aligned;\n" ::
-          : "memory");
-}
-
-// *p in the shared memory of the cluster's CTA of rank `rank`.
-__device__ __forceinline__ float ld_cluster(const float* p, int rank) {
-  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
-  return v;
-}
-
 // q and k columns of one lane (16 each), optionally L2-normalised, plus k.q.
 template <typename TA, int DK>
 struct QK {
@@ -150,21 +131,26 @@ __device__ __forceinline__ float4 mul4(const float4& a, const float4& b) {
 }
 
 // ---------------------------------------------------------------------------
-// Decode: grid.x = B * Hv * slices.  KDA: the one-token sequences of a KDA
-// call (T == N), with the per-key-channel decay and has_initial_state.
-// ONORM: the gated RMSNorm of each output row is applied before the store.
-// The row's value-dimension slices are the CTAs of one thread-block cluster
-// (slices <= 8): each sums the squares of its rows' stored outputs, the sums
-// are exchanged through distributed shared memory and added in rank order,
-// so every CTA of the row gets the same norm.
-template <typename TA, int DK, int PASSES, bool KDA, bool ONORM>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const RecurLaunch p, int slices) {
+// Decode: grid.x = B * Hv * slices, one 128-thread CTA per value-dimension
+// slice.  KDA: the one-token sequences of a KDA call (T == N), with the
+// per-key-channel decay and has_initial_state.
+// NS > 0: the gated RMSNorm of each output row is applied before the store.
+// Then one CTA holds all slices of a (row, head), NS groups of 128 threads
+// (NS = the slice count rounded up to a power of two, <= 4; groups past the
+// last slice own no rows); the squares of the stored outputs are summed per
+// warp and the warp sums added in order, so the whole row gets one norm.
+// (NS > 0 caps the registers at 128 a thread, 512 threads an SM as the plain
+// decode's four CTAs of 128: the state stream needs the warps in flight.)
+template <typename TA, int DK, int PASSES, bool KDA, int NS>
+__global__ void __launch_bounds__(kThreads * (NS > 0 ? NS : 1), 4 / (NS > 0 ? NS : 4))
+    decode_kernel(const RecurLaunch p, int slices) {
+  constexpr bool ONORM = NS > 0;
   constexpr int LPR = DK / 16;
   constexpr int RPP = kThreads / LPR;  // rows per pass
-  const int tid = threadIdx.x;
+  const int tid = ONORM ? threadIdx.x % kThreads : threadIdx.x;
   const int lr = tid % LPR, rg = tid / LPR;
-  const int slice = blockIdx.x % slices;
-  const int bh = blockIdx.x / slices;
+  const int slice = ONORM ? threadIdx.x / kThreads : blockIdx.x % slices;
+  const int bh = ONORM ? blockIdx.x : blockIdx.x / slices;
   const int h = bh % p.Hv, b = bh / p.Hv;
   const int row0 = slice * (RPP * PASSES) + rg;
   TA* out = static_cast<TA*>(p.out) + ((int64_t)b * p.Hv + h) * p.Dv;
@@ -202,6 +188,20 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const RecurLaunch p, i
       st[ps][m] = (init && r < p.Dv) ? __ldcs(reinterpret_cast<const float4*>(
                                            S + (int64_t)r * DK + 4 * lr + 4 * LPR * m))
                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  // ONORM: the row's gate and weight values, requested with the state so that
+  // their latency is not paid again after the reduction.
+  float zv[ONORM ? PASSES : 1], wv[ONORM ? PASSES : 1];
+  if constexpr (ONORM) {
+    const TA* zr = static_cast<const TA*>(p.onorm_z) + (int64_t)b * p.onorm_z_stride +
+                   (int64_t)h * p.Dv;
+#pragma unroll
+    for (int ps = 0; ps < PASSES; ++ps) {
+      const int r = row0 + ps * RPP;
+      const bool mine = lr == 0 && r < p.Dv;
+      zv[ps] = mine ? ld_act<TA>(zr + r) : 0.0f;
+      wv[ps] = mine ? ld_act<TA>(static_cast<const TA*>(p.onorm_w) + r) : 0.0f;
+    }
   }
   QK<TA, DK> qk;
   const TA* kp = static_cast<const TA*>(p.k) + ((int64_t)b * p.Hk + hk) * DK;
@@ -249,32 +249,21 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const RecurLaunch p, i
     }
   }
   if constexpr (ONORM) {
-    __shared__ float wpart[kThreads / 32];
-    __shared__ float cpart;
+    constexpr int kWarps = kThreads * (ONORM ? NS : 1) / 32;
+    __shared__ float wpart[kWarps];
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-    if ((tid & 31) == 0) wpart[tid >> 5] = ss;
+    if ((threadIdx.x & 31) == 0) wpart[threadIdx.x >> 5] = ss;
     __syncthreads();
     float tot = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) tot += wpart[w];
-    if (slices > 1) {
-      if (tid == 0) cpart = tot;
-      cluster_sync_all();
-      tot = 0.0f;
-      for (int rk = 0; rk < slices; ++rk) tot += ld_cluster(&cpart, rk);
-      cluster_sync_all();  // every CTA has read the others' sums before any exits
-    }
+    for (int w = 0; w < kWarps; ++w) tot += wpart[w];
     const float inv = math::rms_inv(tot, 1.0f / static_cast<float>(p.Dv), p.onorm_eps);
-    const TA* zr = static_cast<const TA*>(p.onorm_z) + (int64_t)b * p.onorm_z_stride +
-                   (int64_t)h * p.Dv;
-    const TA* wr = static_cast<const TA*>(p.onorm_w);
 #pragma unroll
     for (int ps = 0; ps < PASSES; ++ps) {
       const int r = row0 + ps * RPP;
       if (lr == 0 && r < p.Dv)
-        st_act<TA>(out + r, core[ps] * inv * ld_act<TA>(wr + r) *
-                                math::norm_gate(ld_act<TA>(zr + r), p.onorm_sigmoid));
+        st_act<TA>(out + r, core[ps] * inv * wv[ps] * math::norm_gate(zv[ps], p.onorm_sigmoid));
     }
   }
 }
@@ -473,7 +462,9 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(const RecurLaunch p
 
 enum class Mode { kDecode, kRecurrent, kKda, kKdaDecode, kSpec };
 
-constexpr int kMaxNormCluster = 8;
+// Slices of one row in one CTA (512 threads: 128 registers a thread, as the
+// plain decode; wider rows take the norm kernel after the decode).
+constexpr int kMaxNormSlices = 4;
 
 // Rows of the value dimension one CTA holds: PASSES chosen so that a CTA
 // holds 64 rows at Dk = 128 (32 floats of state per thread).
@@ -491,30 +482,22 @@ cudaError_t launch_dk(const RecurLaunch& p, cudaStream_t s, Mode mode) {
   const unsigned grid = (unsigned)blocks;
   switch (mode) {
     case Mode::kDecode:
-      if (p.onorm_w != nullptr) {
-        if (slices > kMaxNormCluster) return cudaErrorInvalidConfiguration;
-        // the row's slices as one cluster, so that they can share their sums
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(grid);
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = 0;
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(slices);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        const cudaError_t e =
-            cudaLaunchKernelEx(&cfg, decode_kernel<TA, DK, PASSES, false, true>, p, slices);
-        note_launch();
-        return e != cudaSuccess ? e : cudaGetLastError();
+      if (p.onorm_w != nullptr) {  // one CTA per (row, head) holding all its slices
+        const unsigned rows = static_cast<unsigned>(grid / slices);
+        if (slices == 1)
+          decode_kernel<TA, DK, PASSES, false, 1><<<rows, kThreads, 0, s>>>(p, slices);
+        else if (slices == 2)
+          decode_kernel<TA, DK, PASSES, false, 2><<<rows, 2 * kThreads, 0, s>>>(p, slices);
+        else if (slices <= kMaxNormSlices)
+          decode_kernel<TA, DK, PASSES, false, 4><<<rows, 4 * kThreads, 0, s>>>(p, slices);
+        else
+          return cudaErrorInvalidConfiguration;
+        break;
       }
-      decode_kernel<TA, DK, PASSES, false, false><<<grid, kThreads, 0, s>>>(p, slices);
+      decode_kernel<TA, DK, PASSES, false, 0><<<grid, kThreads, 0, s>>>(p, slices);
       break;
     case Mode::kKdaDecode:
-      decode_kernel<TA, DK, PASSES, true, false><<<grid, kThreads, 0, s>>>(p, slices);
+      decode_kernel<TA, DK, PASSES, true, 0><<<grid, kThreads, 0, s>>>(p, slices);
       break;
     case Mode::kRecurrent:
       recurrent_kernel<TA, DK, PASSES, false, false><<<grid, kThreads, 0, s>>>(p, slices);
@@ -553,7 +536,7 @@ bool recurrent_supported(int Dk) {
 bool decode_norm_in_kernel(int Dk, int Dv) {
   if (!recurrent_supported(Dk) || Dv < 1) return false;
   const int rows = rows_per_cta_for(Dk);
-  return (Dv + rows - 1) / rows <= kMaxNormCluster;
+  return (Dv + rows - 1) / rows <= kMaxNormSlices;
 }
 
 static cudaError_t launch_mode(const RecurLaunch& p, cudaStream_t s, Mode mode) {

@@ -170,11 +170,13 @@ int gdn_prepare(const gdn_prepare_args* args, void* stream);
  * pipeline stores and the norm reads back) and act = silu (sigmoid_gate = 0)
  * or sigmoid.  z: token rows of at least Hv * Dv values in act_dtype,
  * z_token_stride elements apart (16-byte aligned rows); weight: [Dv] in
- * act_dtype.  The decode computes it inside the recurrence kernel (the CTAs of
- * a row's value-dimension slices exchange their partial sums within a thread-
- * block cluster); so does the fused chunked prefill; the other prefill forms
- * run the norm as a second kernel over the output in place.  Same rules as
- * gdn_gated_rmsnorm (lengths, alignment, Dv <= 1024 for bf16).
+ * act_dtype.  By default the call runs the norm as a second kernel over the
+ * output in place (on GB300 that is faster than folding it into the
+ * recurrence kernels, whose tails then wait on a row-wide reduction).  With
+ * in_kernel = 1 gdn_decode applies it inside the decode kernel when one CTA
+ * can hold the whole row (Dv <= 256 at Dk = 64 or 128, Dv <= 128 at Dk = 256,
+ * Dv <= 512 at Dk <= 32); the prefill always uses the second kernel.  Same
+ * rules as gdn_gated_rmsnorm (lengths, alignment, Dv <= 1024 for bf16).
  * ------------------------------------------------------------------------- */
 typedef struct gdn_out_norm {
   const void* z;           /* [tokens, z_token_stride] act_dtype */
@@ -184,6 +186,7 @@ typedef struct gdn_out_norm {
   int64_t weight_len;
   float eps;
   int32_t sigmoid_gate;    /* 1: sigmoid gate instead of silu */
+  int32_t in_kernel;       /* 1: inside the decode kernel where it fits (see above) */
 } gdn_out_norm;
 
 /* ---------------------------------------------------------------------------
@@ -373,8 +376,13 @@ int gdn_packed_decode(const gdn_packed_decode_args* args, void* stream);
  * q and k are used as given (no L2 norm).  Decode is the case of N one-token
  * sequences.  State pool, state_indices (-1 = padding), has_initial_state,
  * cu_seqlens and their host mirrors as in gdn_prefill_varlen; g 16-byte
- * aligned.  Runs on CUDA cores, a CTA per (sequence, head, row slice).
- * Supported: Dk in {16, 32, 64, 128, 256}; any Dv >= 1.
+ * aligned.
+ * algo (gdn_prefill_algo; see gdn_kda_resolve_algo): RECURRENT runs on CUDA
+ * cores, a CTA per (sequence, head, row slice); CHUNKED is the chunk-64 form
+ * on tcgen05 tensor cores (bf16, Dk = Dv = 128), two launches that hand each
+ * chunk over through a caller workspace of gdn_kda_workspace_bytes() bytes
+ * (256-byte aligned); FUSED is not offered for KDA.
+ * Supported: Dk in {16, 32, 64, 128, 256}; any Dv >= 1 (recurrent).
  * Errors as gdn_prefill_varlen (g: "kda_gated_delta_rule g length N <
  * expected T*Hv*Dk").
  * ------------------------------------------------------------------------- */
@@ -402,9 +410,25 @@ typedef struct gdn_kda_args {
   const int32_t* state_indices_host;
   void* out;                /* [T, Hv, Dv] */
   int64_t out_len;
+  int32_t algo;             /* gdn_prefill_algo: AUTO, CHUNKED or RECURRENT */
+  void* workspace;          /* device scratch, see gdn_kda_workspace_bytes */
+  size_t workspace_bytes;
 } gdn_kda_args;
 
 int gdn_kda_varlen(const gdn_kda_args* args, void* stream);
+
+/* The algorithm gdn_kda_varlen runs for `algo`: AUTO picks CHUNKED when some
+ * sequence holds more than one token (T > N) and the chunked form supports the
+ * shape (bf16, Dk = Dv = 128), else RECURRENT.  Other values are returned as
+ * given. */
+int32_t gdn_kda_resolve_algo(int64_t T, int64_t N, int64_t Dk, int64_t Dv, int32_t act_dtype,
+                             int32_t algo);
+
+/* Workspace bytes gdn_kda_varlen needs for these sizes and `algo` (0 when the
+ * resolved algorithm is the recurrent one): one 113 KB blob per (chunk, value
+ * head), for at most T / 64 + N chunks. */
+size_t gdn_kda_workspace_bytes(int64_t T, int64_t N, int64_t Hv, int64_t Dk, int64_t Dv,
+                               int32_t act_dtype, int32_t algo);
 
 /* ---------------------------------------------------------------------------
  * gdn_spec_prepare -- [cpu_ops.cpp] CausalConv1dSpecUpdateKernel followed by

@@ -285,6 +285,37 @@ def test_kda_rejections():
     assert rc == B.GDN_ERR_INVALID_ARGUMENT and "empty or non-monotonic" in msg
 
 
+def test_kda_algo_rules():
+    """AUTO takes the chunked tensor-core form for bf16 with Dk = Dv = 128 when
+    some sequence holds more than one token; it needs a caller workspace of one
+    blob per (chunk, value head)."""
+    R = B.gdn_kda_resolve_algo
+    assert R(100, 2, 128, 128) == B.GDN_PREFILL_CHUNKED
+    assert R(2, 2, 128, 128) == B.GDN_PREFILL_RECURRENT            # one token each
+    assert R(100, 2, 128, 64) == B.GDN_PREFILL_RECURRENT
+    assert R(100, 2, 128, 128, B.GDN_DTYPE_F32) == B.GDN_PREFILL_RECURRENT
+    assert R(100, 2, 128, 128, algo=B.GDN_PREFILL_RECURRENT) == B.GDN_PREFILL_RECURRENT
+    blob = B.gdn_kda_workspace_bytes(64, 1, 1, 128, 128) // (64 // 64 + 1)
+    assert blob == 113 * 1024
+    assert B.gdn_kda_workspace_bytes(4096, 3, 32, 128, 128) == (4096 // 64 + 3) * 32 * blob
+    assert B.gdn_kda_workspace_bytes(100, 2, 4, 128, 64) == 0
+    big = dict(T=130, N=2, Dv=128, v_len=130 * 2 * 128, out_len=130 * 2 * 128,
+               q_len=130 * 128, k_len=130 * 128, g_len=130 * 2 * 128, beta_len=260,
+               state_len=4 * 2 * 128 * 128)
+    rc, msg = call_kda(kda_args(**big))
+    need = B.gdn_kda_workspace_bytes(130, 2, 2, 128, 128)
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT
+    assert msg == f"gdn_kda_varlen workspace needs {need} bytes, got 0"
+    rc, _ = call_kda(kda_args(**big, workspace=FAKE, workspace_bytes=need - 1))
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT
+    rc, msg = call_kda(kda_args(**big, workspace=FAKE + 16, workspace_bytes=need))
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT and msg == "workspace must be 256-byte aligned"
+    rc, msg = call_kda(kda_args(**big, algo=B.GDN_PREFILL_FUSED))
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT and "KDA algo 3" in msg
+    rc, msg = call_kda(kda_args(algo=B.GDN_PREFILL_CHUNKED))                # Dv = 64
+    assert rc == B.GDN_ERR_UNSUPPORTED and "Dk = Dv = 128" in msg
+
+
 def spec_args(T=5, n_reqs=2, num_cols=3, Hk=1, Hv=2, Dk=128, Dv=64, **over):
     a = dict(T=T, n_reqs=n_reqs, num_cols=num_cols, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv,
              act_dtype=B.GDN_DTYPE_BF16, scale=-1.0, q=FAKE, q_len=T * Hk * Dk, k=FAKE,

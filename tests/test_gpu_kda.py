@@ -1,7 +1,10 @@
 """GPU parity of gdn_kda_varlen (the gated delta rule with one log decay per
 key channel, [cpu_ops.cpp] KdaHeadTokenStep / KdaGatedDeltaRuleKernel) against
 the oracle's KDA chain, through the C ABI: varlen prefill, decode (one-token
-sequences), padding slots, fresh states, bf16 and f32, every supported Dk."""
+sequences), padding slots, fresh states, bf16 and f32, every supported Dk; the
+chunked tensor-core form at chunk-boundary lengths, strong and weak decays,
+GQA, padding and fresh states, and the single-sequence prefill shape at full
+size (4096 tokens, 16 / 32 heads of 128)."""
 import numpy as np
 import pytest
 import torch
@@ -13,7 +16,8 @@ from gated_delta_rule_44_gb300 import binding as B
 pytestmark = pytest.mark.gpu
 
 
-def run(seqs, Hk, Hv, Dk, Dv, dtype, dev, seed, sidx=None, has_init=None, slots=None):
+def run(seqs, Hk, Hv, Dk, Dv, dtype, dev, seed, sidx=None, has_init=None, slots=None,
+        algo=B.GDN_PREFILL_AUTO, g_scale=0.3):
     g0 = torch.Generator().manual_seed(seed)
     T, N = sum(seqs), len(seqs)
     slots = slots or N + 2
@@ -21,7 +25,7 @@ def run(seqs, Hk, Hv, Dk, Dv, dtype, dev, seed, sidx=None, has_init=None, slots=
     q = (torch.randn(T, Hk, Dk, generator=g0) / np.sqrt(Dk)).to(dtype)
     k = (torch.randn(T, Hk, Dk, generator=g0) / np.sqrt(Dk)).to(dtype)
     v = torch.randn(T, Hv, Dv, generator=g0).to(dtype)
-    g = -torch.rand(T, Hv, Dk, generator=g0) * 0.3          # log decay per key channel
+    g = -torch.rand(T, Hv, Dk, generator=g0) * g_scale      # log decay per key channel
     beta = torch.rand(T, Hv, generator=g0) * 0.8 + 0.1
     pool = torch.randn(slots, Hv, Dv, Dk, generator=g0) * 0.1
     if sidx is None:
@@ -32,7 +36,7 @@ def run(seqs, Hk, Hv, Dk, Dv, dtype, dev, seed, sidx=None, has_init=None, slots=
     B.gdn_kda_varlen(q.to(dev), k.to(dev), v.to(dev), g.to(dev), beta.to(dev), pool_d,
                      cu.to(dev), out, scale=-1.0, state_indices=sidx.to(dev),
                      has_initial_state=None if hi is None else hi.to(dev),
-                     cu_seqlens_host=cu, state_indices_host=sidx)
+                     cu_seqlens_host=cu, state_indices_host=sidx, algo=algo)
     B.gdn_read_device_status()
     torch.cuda.synchronize()
     ref_pool = pool.numpy().astype(np.float32).copy()
@@ -43,6 +47,7 @@ def run(seqs, Hk, Hv, Dk, Dv, dtype, dev, seed, sidx=None, has_init=None, slots=
     tol = H.TOL_F32 if dtype == torch.float32 else H.TOL_BF16
     H.check(out, ref, tol, "kda out")
     H.assert_close(H.f32(pool_d), ref_pool, tol, "kda state")
+    return out, pool_d
 
 
 @pytest.mark.parametrize("Dk", [16, 32, 64, 128, 256])
@@ -61,7 +66,7 @@ def test_kda_padding_and_fresh_states(cuda_device):
 
 
 def test_kda_long_sequence(cuda_device):
-    run([1000], 4, 8, 128, 128, torch.bfloat16, cuda_device, seed=5)
+    run([1000], 4, 8, 128, 128, torch.bfloat16, cuda_device, seed=5, algo=B.GDN_PREFILL_RECURRENT)
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
@@ -70,3 +75,43 @@ def test_kda_decode_form_padding_and_fresh_states(dtype, cuda_device):
     run([1] * 9, 2, 4, 128, 96, dtype, cuda_device, seed=6,
         sidx=torch.tensor([3, -1, 0, 8, 5, -1, 1, 2, 7], dtype=torch.int32),
         has_init=[1, 1, 0, 1, 0, 1, 1, 1, 0], slots=10)
+
+
+CHUNKED = B.GDN_PREFILL_CHUNKED
+
+
+def test_kda_chunked_chunk_boundaries(cuda_device):
+    run([1, 63, 64, 65, 127, 128, 129], 2, 4, 128, 128, torch.bfloat16, cuda_device, seed=11,
+        algo=CHUNKED)
+
+
+@pytest.mark.parametrize("g_scale", [6.0, 0.02])
+def test_kda_chunked_strong_and_weak_decay(g_scale, cuda_device):
+    """Per-token decays down to e^-6 per channel (products underflow within a
+    sub-chunk) and nearly none (the state keeps its whole history)."""
+    run([200, 77, 130], 2, 8, 128, 128, torch.bfloat16, cuda_device, seed=12, algo=CHUNKED,
+        g_scale=g_scale)
+
+
+def test_kda_chunked_padding_and_fresh_states(cuda_device):
+    run([70, 3, 129, 64], 1, 4, 128, 128, torch.bfloat16, cuda_device, seed=13, algo=CHUNKED,
+        sidx=torch.tensor([2, -1, 0, 5], dtype=torch.int32), has_init=[1, 1, 0, 1], slots=6)
+
+
+def test_kda_chunked_single_token_sequences(cuda_device):
+    """T == N on the chunked form: every chunk is one token long."""
+    run([1] * 9, 2, 4, 128, 128, torch.bfloat16, cuda_device, seed=14, algo=CHUNKED)
+
+
+def test_kda_chunked_matches_recurrent(cuda_device):
+    """Both GPU forms against the oracle, and against each other."""
+    o1, s1 = run([1000, 37], 4, 8, 128, 128, torch.bfloat16, cuda_device, seed=15, algo=CHUNKED)
+    o2, s2 = run([1000, 37], 4, 8, 128, 128, torch.bfloat16, cuda_device, seed=15,
+                 algo=B.GDN_PREFILL_RECURRENT)
+    e = H.rel_err_stored_bf16(H.f32(o1), H.f32(o2))
+    assert e <= H.TOL_BF16, f"chunked vs recurrent out {e:.3e}"
+
+
+def test_kda_chunked_full_size(cuda_device):
+    """The single-sequence prefill shape: 4096 tokens, Hk = 16, Hv = 32, D = 128."""
+    run([4096], 16, 32, 128, 128, torch.bfloat16, cuda_device, seed=16, algo=CHUNKED)

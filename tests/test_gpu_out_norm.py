@@ -11,7 +11,9 @@ rms(core) moves an output by at most that times |out / core| of the row:
 inv_rms * |weight * gate|), on top of the storage metric of tests/helpers.py.
 Also: the state a normed call leaves equals the state of the plain call bit
 for bit, and the normed output agrees with the standalone norm kernel run on
-the plain call's output (GPU against GPU) to one bf16 step.
+the plain call's output (GPU against GPU) to one bf16 step (bit for bit where
+the call runs that kernel itself).  The decode is checked on both routes: the
+norm kernel after the recurrence (the default) and inside the decode kernel.
 """
 import numpy as np
 import pytest
@@ -65,7 +67,7 @@ def compare(out_norm, out_plain, core_ref, zw, w, eps, sig, act_dtype, dev, what
     assert np.all(np.abs(a - b) <= step + 1e-30), f"{what}: fused and standalone norms differ"
 
 
-def run_decode_case(Bn, Hk, Hv, Dk, Dv, dtype, padded, sig, pad, dev, seed):
+def run_decode_case(Bn, Hk, Hv, Dk, Dv, dtype, padded, sig, pad, dev, seed, in_kernel=False):
     w = W.make_workload("d", seed, [1] * Bn, Hk, Hv, Dk, Dv, act_dtype=dtype, slots=Bn + 3,
                         padded=padded, n_decode=Bn, state_std=0.3)
     prep, _ = H.oracle_prepare(w)
@@ -81,7 +83,7 @@ def run_decode_case(Bn, Hk, Hv, Dk, Dv, dtype, padded, sig, pad, dev, seed):
         B.gdn_decode(acts["q"].to(dev), acts["k"].to(dev), acts["v"].to(dev), g.to(dev),
                      beta.to(dev), pool, out, state_indices=w.state_indices.to(dev),
                      norm_z=zd if normed else None, norm_weight=wt.to(dev) if normed else None,
-                     norm_eps=eps, norm_sigmoid=sig)
+                     norm_eps=eps, norm_sigmoid=sig, norm_in_kernel=in_kernel)
         B.gdn_read_device_status()
         outs.append(out)
         pools.append(pool)
@@ -91,26 +93,27 @@ def run_decode_case(Bn, Hk, Hv, Dk, Dv, dtype, padded, sig, pad, dev, seed):
                                  g.numpy(), beta.numpy(), ref_pool, 1.0 / np.sqrt(Dk),
                                  state_indices=w.state_indices.numpy(), dtype=np.float64)
     compare(outs[1], outs[0], core_ref, zw, wt, eps, sig, dtype, dev,
-            f"decode B{Bn} Dk{Dk} Dv{Dv}")
+            f"decode B{Bn} Dk{Dk} Dv{Dv}" + (" in kernel" if in_kernel else ""))
     if padded:  # padding rows stay zero
         assert torch.all(outs[1][padded].float() == 0)
 
 
 DECODE_CASES = [
     # B, Hk, Hv, Dk, Dv, dtype, padded rows, sigmoid gate, gate-row padding
-    (9, 2, 4, 128, 128, torch.bfloat16, [3], False, 0),    # two slices: a cluster of 2
-    (5, 1, 2, 128, 256, torch.bfloat16, None, True, 16),   # four slices
-    (4, 1, 2, 256, 256, torch.bfloat16, None, False, 0),   # eight slices: the largest cluster
+    (9, 2, 4, 128, 128, torch.bfloat16, [3], False, 0),    # two slices in one CTA
+    (5, 1, 2, 128, 256, torch.bfloat16, None, True, 16),   # four slices: the widest CTA
+    (4, 1, 2, 256, 256, torch.bfloat16, None, False, 0),   # eight slices: the norm kernel after
     (6, 2, 2, 64, 64, torch.float32, [0], False, 4),       # one slice
     (3, 1, 3, 16, 1024, torch.bfloat16, None, False, 8),   # eight slices of 128 rows
-    (3, 1, 2, 256, 512, torch.bfloat16, None, True, 0),    # 16 slices: the norm kernel after
+    (3, 1, 2, 32, 256, torch.bfloat16, None, True, 0),     # four slices of 64 rows
     (7, 2, 2, 128, 96, torch.float32, None, True, 0),      # a ragged second slice
 ]
 
 
+@pytest.mark.parametrize("in_kernel", [False, True])
 @pytest.mark.parametrize("case", range(len(DECODE_CASES)))
-def test_decode_out_norm(case, cuda_device):
-    run_decode_case(*DECODE_CASES[case], cuda_device, seed=900 + case)
+def test_decode_out_norm(case, in_kernel, cuda_device):
+    run_decode_case(*DECODE_CASES[case], cuda_device, seed=900 + case, in_kernel=in_kernel)
 
 
 def run_prefill_case(lens, Hk, Hv, dtype, algo, sig, pad, dev, seed, Dk=128, Dv=128):
