@@ -50,6 +50,10 @@ def parse_args():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the single-kernel decode / prefill workloads")
     ap.add_argument("--algo", type=int, default=0, help="prefill algorithm (0 auto)")
+    ap.add_argument("--extra-only", default=None,
+                    choices=["kda_prefill_4k", "kda_decode_b256", "spec_decode_r128x4",
+                             "spec_prepare_r128x4", "packed_decode_b256"],
+                    help="time one of the extra measurements alone (a small case for profiling)")
     return ap.parse_args()
 
 
@@ -230,22 +234,26 @@ def kernel_report(w, kernel_ms, peaks):
 # (dram__bytes_read.sum + dram__bytes_write.sum summed over the call's launches),
 # keyed by (call, workload), with the sha256 of the kernel sources they were
 # measured on (concatenated in the order listed): once a source changes the
-# figure no longer applies and the line reports null.  mixed_hv64's prefill call is too large to capture under
-# ncu's replay, so its figure is prefill_4k's scaled by the token-heads processed
-# (x4; the workspace and operand traffic grow in proportion to them).
+# figure no longer applies and the line reports null.  mixed_hv64 is too large
+# to capture under ncu's replay, so its figures are scaled from smaller cases
+# of the same kernels: the decode by the row-heads processed (x4; every byte
+# of that launch is per row-head), the fused prefill by the call's algorithmic
+# bytes (varlen_8's traffic was 0.962 of its algorithmic bytes; the per-token
+# share of key and value heads differs between the two workloads, so token-heads
+# would not scale it).
+_DECODE_SRC = (("gdn_recurrent.cu", "gdn_rowstep.cuh", "gdn_math.cuh"),
+               "27a316189865ac53a673efa7b8dd7d8cac0c7b20a4885acb1593f84a0d92486b")
+_FUSED_SRC = (("gdn_fused.cu", "gdn_chunk_common.cuh", "tcgen05.cuh"),
+              "78c0c2d216af283f0038d0c75fd77ab68cbd9a8f3e267ae418016685a9dce5a5")
+_CHUNKED_SRC = (("gdn_chunked.cu", "gdn_chunk_common.cuh", "tcgen05.cuh"),
+                "49ac86504ef894df2bde91e44e3e8f4896cafd82adc08a4d9d1930f7358beb07")
 MEASURED_TRAFFIC = {
-    ("prefill", "prefill_4k"): (334.6e6, ("gdn_chunked.cu",),
-                                "88d3a3e3bfad0885889fbce61c4d7fe02a9484fed34307f12f7a610d4853d718",
-                                "chunk_prep + chunk_scan of one call"),
-    ("prefill", "mixed_hv64"): (1338.4e6, ("gdn_chunked.cu",),
-                                "88d3a3e3bfad0885889fbce61c4d7fe02a9484fed34307f12f7a610d4853d718",
-                                "prefill_4k's call x 4 (token-heads)"),
-    ("decode", "decode_b256"): (1020.6e6, ("gdn_recurrent.cu", "gdn_rowstep.cuh", "gdn_math.cuh"),
-                                "3262d5358409cb7d1def5b51c482c5605b906b9de47fcf817c61b9bcc7218b0a",
-                                "one decode launch"),
-    ("decode", "mixed_hv64"): (4082.6e6, ("gdn_recurrent.cu", "gdn_rowstep.cuh", "gdn_math.cuh"),
-                               "3262d5358409cb7d1def5b51c482c5605b906b9de47fcf817c61b9bcc7218b0a",
-                               "decode_b256's launch x 4 (row-heads)"),
+    ("prefill", "prefill_4k"): (328.4e6,) + _CHUNKED_SRC + ("chunk_prep + chunk_scan of one call",),
+    ("prefill", "varlen_8"): (621.9e6,) + _FUSED_SRC + ("one fused_prefill launch",),
+    ("prefill", "mixed_hv64"): (343.0e6,) + _FUSED_SRC +
+                               ("varlen_8's fused launch scaled by algorithmic bytes (x0.552)",),
+    ("decode", "decode_b256"): (1017.8e6,) + _DECODE_SRC + ("one decode launch",),
+    ("decode", "mixed_hv64"): (4071.2e6,) + _DECODE_SRC + ("decode_b256's launch x 4 (row-heads)",),
 }
 
 
@@ -788,6 +796,12 @@ def main():
     from gated_delta_rule_44_gb300 import workloads as W
     B.lib()
     peaks = load_peaks()
+    if args.extra_only is not None:
+        fn = {"kda_prefill_4k": time_kda_prefill, "kda_decode_b256": time_kda_decode,
+              "spec_decode_r128x4": time_spec_decode, "spec_prepare_r128x4": time_spec_prepare,
+              "packed_decode_b256": time_packed_decode}[args.extra_only]
+        print(json.dumps({"extra": args.extra_only, "result": fn(dev, peaks)}), flush=True)
+        return 0
     w = W.named(args.workload)
     props = torch.cuda.get_device_properties(dev)
     bus = getattr(props, "pci_bus_id", None)

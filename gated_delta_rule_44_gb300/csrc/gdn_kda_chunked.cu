@@ -625,6 +625,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_scan_kernel(
         mbar_expect_tx(mb_el, 512);
         bulk_g2s(base + KScan::ELB + ((c + 1) & 1) * 512, blob(c + 1) + kBE, 512, mb_el);
         pend_el = c + 1;
+        // and the next chunk's images on their way into L2 (the stage is single-buffered)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                         reinterpret_cast<uint64_t>(blob(c + 1))),
+                     "r"(kBImg)
+                     : "memory");
       }
     }
     ok = __syncthreads_and(mbar_wait(mb_ld, c & 1, kWaitBudget));
