@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstdlib>
+#include <cstring>
 #include <cstdint>
 #include <string>
 #include <vector>
@@ -204,6 +206,33 @@ int check_spec_host(const int32_t* cu, const int32_t* sidx, const int32_t* nat, 
 
 bool fits_i32(int64_t v) { return v >= 0 && v <= INT32_MAX; }
 
+// GDN_DEBUG_CHECKS=1 in the environment (read once): metadata given only in
+// device memory is copied to the host and checked as its host mirror would be.
+bool debug_checks() {
+  static const bool on = [] {
+    const char* e = std::getenv("GDN_DEBUG_CHECKS");
+    return e != nullptr && std::strcmp(e, "1") == 0;
+  }();
+  return on;
+}
+
+// The host view of n int32 metadata values: the caller's host mirror, else
+// (under GDN_DEBUG_CHECKS) a copy of the device array made on the call's
+// stream, else nullptr (nothing to check on the host).
+int host_view(const int32_t* host, const int32_t* dev, int64_t n, cudaStream_t st,
+              std::vector<int32_t>& buf, const int32_t*& out) {
+  out = host;
+  if (host != nullptr || dev == nullptr || n <= 0 || !debug_checks()) return GDN_OK;
+  buf.resize(static_cast<size_t>(n));
+  cudaError_t e = cudaMemcpyAsync(buf.data(), dev, static_cast<size_t>(n) * sizeof(int32_t),
+                                  cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess)
+    return fail(GDN_ERR_CUDA, std::string("GDN_DEBUG_CHECKS metadata copy: ") + cudaGetErrorString(e));
+  out = buf.data();
+  return GDN_OK;
+}
+
 }  // namespace
 
 int gdn::report_error(int code, const char* msg) { return fail(code, msg); }
@@ -368,16 +397,21 @@ int gdn_prepare(const gdn_prepare_args* a, void* stream) {
   if (a == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "args is NULL");
   gdn::PrepareLaunch p;
   if (int rc = prepare_common(a, a->K - 1, &p)) return rc;
-  if (a->cu_seqlens_host != nullptr)
-    if (int rc = check_cu_host(a->cu_seqlens_host, a->N, a->T, "linear_attention_prepare_varlen"))
-      return rc;
-  if (a->state_indices_host != nullptr)
-    if (int rc = check_indices_host(a->state_indices_host, a->N, a->conv_state_slots)) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  std::vector<int32_t> cu_buf, idx_buf;
+  const int32_t *cuh = nullptr, *idxh = nullptr;
+  if (int rc = host_view(a->cu_seqlens_host, a->cu_seqlens, a->N + 1, st, cu_buf, cuh)) return rc;
+  if (int rc = host_view(a->state_indices_host, a->state_indices, a->N, st, idx_buf, idxh))
+    return rc;
+  if (cuh != nullptr)
+    if (int rc = check_cu_host(cuh, a->N, a->T, "linear_attention_prepare_varlen")) return rc;
+  if (idxh != nullptr)
+    if (int rc = check_indices_host(idxh, a->N, a->conv_state_slots)) return rc;
   if (a->state_indices == nullptr && a->N > a->conv_state_slots)
     return fail(GDN_ERR_SHAPE, "linear_attention_prepare conv_state has fewer slots than sequences");
   p.status = gdn::status_word();
   if (p.status == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
-  return launch_result(gdn::launch_prepare(p, static_cast<cudaStream_t>(stream)), "gdn_prepare");
+  return launch_result(gdn::launch_prepare(p, st), "gdn_prepare");
 }
 
 int gdn_spec_prepare(const gdn_spec_prepare_args* sa, void* stream) {
@@ -403,11 +437,16 @@ int gdn_spec_prepare(const gdn_spec_prepare_args* sa, void* stream) {
     return fail(GDN_ERR_UNSUPPORTED, "gdn_spec_prepare supports conv rows of at most 16 entries");
   // [qwen3_5.cpp] spec metadata rules on the host mirrors: requests of at
   // most max_q tokens, num_accepted in [1, max_q], one conv row per request
-  if (int rc = check_spec_host(a->cu_seqlens_host, nullptr, sa->num_accepted_host, a->N, max_q,
-                               a->T, a->conv_state_slots))
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  std::vector<int32_t> cu_buf, idx_buf, na_buf;
+  const int32_t *cuh = nullptr, *idxh = nullptr, *nah = nullptr;
+  if (int rc = host_view(a->cu_seqlens_host, a->cu_seqlens, a->N + 1, st, cu_buf, cuh)) return rc;
+  if (int rc = host_view(a->state_indices_host, a->state_indices, a->N, st, idx_buf, idxh))
     return rc;
-  if (int rc = check_spec_host(nullptr, a->state_indices_host, nullptr, a->N, 1, a->T,
-                               a->conv_state_slots))
+  if (int rc = host_view(sa->num_accepted_host, sa->num_accepted, a->N, st, na_buf, nah)) return rc;
+  if (int rc = check_spec_host(cuh, nullptr, nah, a->N, max_q, a->T, a->conv_state_slots))
+    return rc;
+  if (int rc = check_spec_host(nullptr, idxh, nullptr, a->N, 1, a->T, a->conv_state_slots))
     return rc;
   p.sidx = a->state_indices;
   p.has_init = nullptr;
@@ -415,8 +454,7 @@ int gdn_spec_prepare(const gdn_spec_prepare_args* sa, void* stream) {
   p.num_accepted = sa->num_accepted;
   p.status = gdn::status_word();
   if (p.status == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
-  return launch_result(gdn::launch_spec_prepare(p, static_cast<cudaStream_t>(stream)),
-                       "gdn_spec_prepare");
+  return launch_result(gdn::launch_spec_prepare(p, st), "gdn_spec_prepare");
 }
 
 namespace {
@@ -498,8 +536,15 @@ int gdn_packed_decode(const gdn_packed_decode_args* a, void* stream) {
                                      "conv_kernel in [2, 4]");
   if (!fits_i32(a->B * a->Hv * a->Dv) || !fits_i32(C))
     return fail(GDN_ERR_UNSUPPORTED, "packed GDN decode sizes exceed 32-bit indexing");
-  if (a->state_indices_host != nullptr)
-    if (int rc = check_indices_host(a->state_indices_host, a->B, a->state_slots)) return rc;
+  {
+    std::vector<int32_t> idx_buf;
+    const int32_t* idxh = nullptr;
+    if (int rc = host_view(a->state_indices_host, a->state_indices, a->B,
+                           static_cast<cudaStream_t>(stream), idx_buf, idxh))
+      return rc;
+    if (idxh != nullptr)
+      if (int rc = check_indices_host(idxh, a->B, a->state_slots)) return rc;
+  }
   gdn::PackedDecodeLaunch p{};
   p.B = (int)a->B;
   p.Hk = (int)a->Hk;
@@ -539,8 +584,15 @@ int gdn_decode(const gdn_decode_args* a, void* stream) {
     return rc;
   if (!gdn::recurrent_supported((int)a->Dk))
     return fail(GDN_ERR_UNSUPPORTED, "gdn_decode supports Dk in {16, 32, 64, 128, 256}");
-  if (a->state_indices_host != nullptr)
-    if (int rc = check_indices_host(a->state_indices_host, a->B, a->state_slots)) return rc;
+  {
+    std::vector<int32_t> idx_buf;
+    const int32_t* idxh = nullptr;
+    if (int rc = host_view(a->state_indices_host, a->state_indices, a->B,
+                           static_cast<cudaStream_t>(stream), idx_buf, idxh))
+      return rc;
+    if (idxh != nullptr)
+      if (int rc = check_indices_host(idxh, a->B, a->state_slots)) return rc;
+  }
   if (a->state_indices == nullptr && a->B > a->state_slots)
     return fail(GDN_ERR_SHAPE, "gated_delta_rule state has fewer slots than rows");
   gdn::RecurLaunch p{};
@@ -592,10 +644,19 @@ int gdn_kda_varlen(const gdn_kda_args* a, void* stream) {
     return fail(GDN_ERR_SHAPE, "kda_gated_delta_rule shape must be positive, got batch=" +
                                    S(a->N) + " total_tokens=" + S(a->T));
   if (require_ptr(a->cu_seqlens, "cu_seqlens")) return GDN_ERR_INVALID_ARGUMENT;
-  if (a->cu_seqlens_host != nullptr)
-    if (int rc = check_cu_host(a->cu_seqlens_host, a->N, a->T, "kda_gated_delta_rule")) return rc;
-  if (a->state_indices_host != nullptr)
-    if (int rc = check_indices_host(a->state_indices_host, a->N, a->state_slots)) return rc;
+  {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    std::vector<int32_t> cu_buf, idx_buf;
+    const int32_t *cuh = nullptr, *idxh = nullptr;
+    if (int rc = host_view(a->cu_seqlens_host, a->cu_seqlens, a->N + 1, st, cu_buf, cuh))
+      return rc;
+    if (int rc = host_view(a->state_indices_host, a->state_indices, a->N, st, idx_buf, idxh))
+      return rc;
+    if (cuh != nullptr)
+      if (int rc = check_cu_host(cuh, a->N, a->T, "kda_gated_delta_rule")) return rc;
+    if (idxh != nullptr)
+      if (int rc = check_indices_host(idxh, a->N, a->state_slots)) return rc;
+  }
   if (a->state_indices == nullptr && a->N > a->state_slots)
     return fail(GDN_ERR_SHAPE, "kda_gated_delta_rule state has fewer slots than sequences");
   if (!gdn::recurrent_supported((int)a->Dk))
@@ -680,9 +741,20 @@ int gdn_spec_decode(const gdn_spec_decode_args* a, void* stream) {
                   std::make_pair((const void*)a->state_indices, "state_indices"),
                   std::make_pair((const void*)a->num_accepted, "num_accepted")})
     if (int rc = require_ptr(pr.first, pr.second)) return rc;
-  if (int rc = check_spec_host(a->cu_seqlens_host, a->state_indices_host, a->num_accepted_host,
-                               a->n_reqs, a->num_cols, a->T, a->state_slots))
-    return rc;
+  {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    std::vector<int32_t> cu_buf, idx_buf, na_buf;
+    const int32_t *cuh = nullptr, *idxh = nullptr, *nah = nullptr;
+    if (int rc = host_view(a->cu_seqlens_host, a->cu_seqlens, a->n_reqs + 1, st, cu_buf, cuh))
+      return rc;
+    if (int rc = host_view(a->state_indices_host, a->state_indices, a->n_reqs * a->num_cols, st,
+                           idx_buf, idxh))
+      return rc;
+    if (int rc = host_view(a->num_accepted_host, a->num_accepted, a->n_reqs, st, na_buf, nah))
+      return rc;
+    if (int rc = check_spec_host(cuh, idxh, nah, a->n_reqs, a->num_cols, a->T, a->state_slots))
+      return rc;
+  }
   if (!gdn::recurrent_supported((int)a->Dk))
     return fail(GDN_ERR_UNSUPPORTED, "gdn_spec_decode supports Dk in {16, 32, 64, 128, 256}");
   if (!fits_i32(a->n_reqs * a->num_cols) || !fits_i32(a->T * a->Hv * a->Dv))
@@ -871,11 +943,19 @@ int gdn_prefill_varlen(const gdn_prefill_args* a, void* stream) {
   if (require_ptr(a->cu_seqlens, "cu_seqlens")) return GDN_ERR_INVALID_ARGUMENT;
   if (a->algo < GDN_PREFILL_AUTO || a->algo > GDN_PREFILL_FUSED)
     return fail(GDN_ERR_INVALID_ARGUMENT, "unknown prefill algo " + S(a->algo));
-  if (a->cu_seqlens_host != nullptr)
-    if (int rc = check_cu_host(a->cu_seqlens_host, a->N, a->T, "gated_delta_rule_varlen"))
+  {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    std::vector<int32_t> cu_buf, idx_buf;
+    const int32_t *cuh = nullptr, *idxh = nullptr;
+    if (int rc = host_view(a->cu_seqlens_host, a->cu_seqlens, a->N + 1, st, cu_buf, cuh))
       return rc;
-  if (a->state_indices_host != nullptr)
-    if (int rc = check_indices_host(a->state_indices_host, a->N, a->state_slots)) return rc;
+    if (int rc = host_view(a->state_indices_host, a->state_indices, a->N, st, idx_buf, idxh))
+      return rc;
+    if (cuh != nullptr)
+      if (int rc = check_cu_host(cuh, a->N, a->T, "gated_delta_rule_varlen")) return rc;
+    if (idxh != nullptr)
+      if (int rc = check_indices_host(idxh, a->N, a->state_slots)) return rc;
+  }
   if (a->state_indices == nullptr && a->N > a->state_slots)
     return fail(GDN_ERR_SHAPE, "gated_delta_rule state has fewer slots than sequences");
   const int32_t algo = gdn_prefill_resolve_algo(a->N, a->Hv, a->Dk, a->Dv, a->act_dtype, a->algo);

@@ -42,6 +42,12 @@
  *     malformed cu_seqlens when no host mirror was passed) are recorded in a
  *     per-device status word and the offending sequence is skipped;
  *     gdn_read_device_status() returns and clears it.
+ *   - GDN_DEBUG_CHECKS=1 in the environment (read once per process): a call
+ *     given cu_seqlens, state_indices or num_accepted in device memory only
+ *     copies them to the host on its stream, synchronises it, and applies the
+ *     host-mirror checks before launching ([qwen3_5.cpp] the fail-closed
+ *     validators' optional exhaustive re-check).  Not for use while the
+ *     stream is being captured into a graph.
  *   - Layouts (row-major, innermost last):
  *       mixed_qkv [T, >=C_conv], C_conv = 2*Hk*Dk + Hv*Dv, row stride in elements
  *       q, k      [T, Hk, Dk]          v, out [T, Hv, Dv]
