@@ -120,10 +120,13 @@ __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
   return raw + ((1024u - (umma::smem_u32(raw) & 1023u)) & 1023u);
 }
 
-// Sequence and chunk-in-sequence of global chunk `gc`, from cu_seqlens (warp 0).
-// Returns false when gc is past the last chunk or cu_seqlens is malformed.
+// Sequence and chunk-in-sequence of chunk `gc` in the enumeration of the
+// chunks whose index within their sequence lies in [j0, j1) (by sequence,
+// then chunk; [0, INT_MAX) enumerates every chunk, so gc is the global chunk
+// index), from cu_seqlens (warp 0).  Returns false when gc is past the last
+// such chunk or cu_seqlens is malformed.
 __device__ inline bool locate_chunk(const int32_t* __restrict__ cu, int N, int T, int gc, int& s_out,
-                             int& j_out, bool& bad) {
+                                    int& j_out, bool& bad, int j0 = 0, int j1 = 0x7fffffff) {
   const int lane = threadIdx.x & 31;
   int base = 0;
   bad = false;
@@ -133,7 +136,8 @@ __device__ inline bool locate_chunk(const int32_t* __restrict__ cu, int N, int T
     if (s < N) {
       const int lo = __ldg(cu + s), hi = __ldg(cu + s + 1);
       if (lo < 0 || hi <= lo || hi > T) bad = true;
-      nc = hi > lo ? (hi - lo + kC - 1) / kC : 0;
+      const int all = hi > lo ? (hi - lo + kC - 1) / kC : 0;
+      nc = max(0, min(all, j1) - j0);
     }
     int incl = nc;
 #pragma unroll
@@ -148,7 +152,7 @@ __device__ inline bool locate_chunk(const int32_t* __restrict__ cu, int N, int T
     if (hit) {
       const int src = __ffs(hit) - 1;
       s_out = s0 + src;
-      j_out = gc - base - __shfl_sync(0xffffffffu, excl, src);
+      j_out = j0 + gc - base - __shfl_sync(0xffffffffu, excl, src);
       return !bad;
     }
     base += __shfl_sync(0xffffffffu, incl, 31);

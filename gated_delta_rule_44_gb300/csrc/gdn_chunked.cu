@@ -51,6 +51,7 @@
 // Partial chunks: K, Q and V rows past the chunk end are zeroed in shared
 // memory and their g, beta taken as 0, so every derived row is exactly zero.
 #include <cuda.h>
+#include <algorithm>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -66,6 +67,16 @@ using namespace umma;
 using namespace chunk;
 
 constexpr long long kWaitBudget = 2000000000LL;  // ~1 s of SM clock per wait
+
+// Programmatic dependent launch: a grid launched with the programmatic
+// stream-serialisation attribute may start before the grid ahead of it on the
+// stream has finished; griddepcontrol.wait blocks until that grid has
+// completed and its memory is visible, and launch_dependents lets the next
+// such grid start.  Both are no-ops for grids launched the ordinary way.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 // Workspace blob of one (chunk, value head): everything of the chunk that does
 // not depend on the state.
@@ -113,30 +124,41 @@ constexpr int kBarP = 1;  // chunk_prep: warp 0 and the 4 P warps -- the P image
 
 __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-    const __grid_constant__ CUtensorMap tm_v, const RecurLaunch p, uint8_t* __restrict__ ws) {
+    const __grid_constant__ CUtensorMap tm_v, const RecurLaunch p, uint8_t* __restrict__ ws,
+    int j0, int j1) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = aligned_smem(smem_raw);
   __shared__ uint64_t mbar_tma, mbar_v, mbar_mma;
   __shared__ uint32_t tslot;
-  __shared__ int s_seq, s_chunk, s_ok;
+  __shared__ int s_seq, s_chunk, s_gc, s_ok;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3, hf = warp >> 2;
-  const int gc = blockIdx.x, hk = blockIdx.y;
+  const int hk = blockIdx.y;
   const int G = p.Hv / p.Hk;  // value heads of this key head: hk G .. hk G + G - 1
 
-  if (warp == 0) {
+  if (warp == 0) {  // this launch's piece: the chunks with index in [j0, j1) of every sequence
     int s = 0, j = 0;
     bool bad = false;
-    const bool ok = locate_chunk(p.cu, p.N, p.T, gc, s, j, bad);
+    const bool ok = locate_chunk(p.cu, p.N, p.T, blockIdx.x, s, j, bad, j0, j1);
+    bool bad2 = false;
+    const int sbase = ok ? chunk_base(p.cu, s, bad2) : 0;  // the sequence's first global chunk
     if (lane == 0) {
       s_seq = s;
       s_chunk = j;
+      s_gc = sbase + j;
       s_ok = ok ? 1 : 0;
-      if (bad && gc == 0 && hk == 0) atomicOr(p.status, kStatusBadSeqlens);
+      if (bad && blockIdx.x == 0 && hk == 0) atomicOr(p.status, kStatusBadSeqlens);
     }
   }
   __syncthreads();
-  if (!s_ok) return;  // uniform: past the last chunk (or malformed cu_seqlens)
+  // When the chunks are prepared in pieces, the piece's launch runs beside the
+  // scan of the piece before it (programmatic dependent launch) and must not
+  // complete before that scan has: CTA (0, 0) waits for it on every way out.
+  const bool waiter = blockIdx.x == 0 && blockIdx.y == 0;
+  if (!s_ok) {  // uniform: outside this piece, past the last chunk, or malformed cu_seqlens
+    if (waiter) griddep_wait();
+    return;
+  }
   const int s = s_seq;
   const int t0 = __ldg(p.cu + s) + kC * s_chunk;
   const int L = min(kC, __ldg(p.cu + s + 1) - t0);
@@ -205,6 +227,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
     }
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
+    if (waiter) griddep_wait();
     return;
   }
   if (L < kC) {  // zero K and Q rows past the chunk end
@@ -255,7 +278,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
 
   for (int jh = 0; jh < G; ++jh) {
     const int h = hk * G + jh;
-    uint8_t* blob = ws + ((int64_t)gc * p.Hv + h) * kBlobBytes;
+    uint8_t* blob = ws + ((int64_t)s_gc * p.Hv + h) * kBlobBytes;
     if (tid < 64) {
       sg[tid] = g_next;
       sb[tid] = b_next;
@@ -582,6 +605,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(
   fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 256);
+  if (waiter) griddep_wait();
 }
 
 // ---------------------------------------------------------------------------
@@ -641,7 +665,7 @@ constexpr int kBarW = 2;  // end-of-chunk barrier of the worker warps (not the i
 
 __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-    const RecurLaunch p, const uint8_t* __restrict__ ws, int n_chunks_max) {
+    const RecurLaunch p, const uint8_t* __restrict__ ws, int n_chunks_max, int j0, int j1) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = aligned_smem(smem_raw);
   __shared__ uint64_t mb_ld[2], mb_p[2], mb_ut, mb_utfree, mb_a, mb_c, mb_d[2], mb_s, mb_e;
@@ -657,11 +681,20 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
   const int h = sh % p.Hv, s = sh / p.Hv;
   const int hk = h / (p.Hv / p.Hk);
 
-  const int lo = __ldg(p.cu + s), hi = __ldg(p.cu + s + 1);
-  if (lo < 0 || hi <= lo || hi > p.T || __ldg(p.cu) != 0 || __ldg(p.cu + p.N) != p.T) {
+  const int slo = __ldg(p.cu + s), shi = __ldg(p.cu + s + 1);
+  if (slo < 0 || shi <= slo || shi > p.T || __ldg(p.cu) != 0 || __ldg(p.cu + p.N) != p.T) {
     if (tid == 0) atomicOr(p.status, kStatusBadSeqlens);
     return;
   }
+  // This launch's piece of the sequence: chunks [cb, ce) (all of them unless
+  // the chunks are processed in pieces); it starts from the state the
+  // previous piece left in the slot.
+  const int nch_seq = (shi - slo + kC - 1) / kC;
+  const int cb = min(j0, nch_seq), ce = min(j1, nch_seq);
+  if (cb >= ce) return;
+  const int lo = slo + cb * kC, hi = min(shi, slo + ce * kC);
+  griddep_wait();               // the piece's blobs (and the previous piece's state) are complete
+  griddep_launch_dependents();  // the next piece's preparation may start
   int slot = p.sidx != nullptr ? __ldg(p.sidx + s) : s;
   if (slot < -1 || slot >= p.slots) {
     if (tid == 0) atomicOr(p.status, kStatusBadIndex);
@@ -681,8 +714,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
     bool bad = false;
     const int b = chunk_base(p.cu, s, bad);
     if (lane == 0) {
-      s_base = b;
-      s_bad = (bad || b + nchunks > n_chunks_max) ? 1 : 0;
+      s_base = b + cb;
+      s_bad = (bad || b + nch_seq > n_chunks_max) ? 1 : 0;
     }
   }
   __syncthreads();
@@ -780,7 +813,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
   const int dk = quad * 32 + lane;
   float S[16];
   float* pool = p.pool + ((int64_t)slot * p.Hv + h) * kD * kD;
-  const bool init = p.has_init == nullptr || __ldg(p.has_init + s) != 0;
+  const bool init = cb > 0 || p.has_init == nullptr || __ldg(p.has_init + s) != 0;
   if (!issuer_warp) {
 #pragma unroll
     for (int e = 0; e < 16; ++e)
@@ -1043,6 +1076,37 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
 
 // ---- host ------------------------------------------------------------------------
 
+constexpr int kPieces = 4;  // pieces of chunk indices when the chains are few
+
+// Launches kern with the programmatic stream-serialisation attribute when pdl
+// is set (the grid may start while the one ahead of it on the stream runs).
+template <typename... Params, typename... Args>
+cudaError_t launch_maybe_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+  note_launch();
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 152;
+  }
+  return n;
+}
 
 }  // namespace
 
@@ -1053,6 +1117,12 @@ size_t chunked_workspace_bytes(int64_t T, int64_t N, int64_t Hv, int64_t Dk, int
   return static_cast<size_t>(max_chunks(T, N) * Hv) * kBlobBytes;
 }
 
+// Few chains (the scan would leave most SMs idle behind the preparation): the
+// chunks are taken in pieces of consecutive chunk indices.  Piece i's scan
+// runs beside piece i + 1's preparation on the other SMs; each launch after
+// the first is a programmatic dependent launch, the scan waits for its
+// piece's blobs (and, through the preparation's last CTA, for the previous
+// scan), and every launch keeps the stream's order for what follows.
 cudaError_t launch_chunked(const ChunkedLaunch& c, cudaStream_t s) {
   const RecurLaunch& p = c.r;
   CUtensorMap tq, tk, tv;
@@ -1073,17 +1143,26 @@ cudaError_t launch_chunked(const ChunkedLaunch& c, cudaStream_t s) {
   uint8_t* ws = static_cast<uint8_t*>(c.workspace);
   const int64_t nch = max_chunks(p.T, p.N);
   if (nch > 0x7fffffff || p.Hv > 65535) return cudaErrorInvalidConfiguration;
-  chunk_prep_kernel<<<dim3(static_cast<unsigned>(nch), p.Hk), kPrepThreads,
-                      PrepSmem::BYTES + 1024, s>>>(tq, tk, tv, p, ws);
-  note_launch();
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   const int64_t blocks = static_cast<int64_t>(p.N) * p.Hv * 2;
   if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  chunk_scan_kernel<<<static_cast<unsigned>(blocks), kScanThreads, ScanSmem::BYTES + 1024, s>>>(
-      tq, tk, p, ws, static_cast<int>(nch));
-  note_launch();
-  return cudaGetLastError();
+  const int64_t cmax = (p.T + kC - 1) / kC;  // chunks of the longest possible sequence
+  const bool pieces = 2 * blocks <= sm_count() && cmax >= 16;
+  const int step = pieces ? static_cast<int>((cmax + kPieces - 1) / kPieces) : 0x7fffffff;
+  const int n_pieces = pieces ? static_cast<int>((cmax + step - 1) / step) : 1;
+  for (int i = 0; i < n_pieces; ++i) {
+    const int j0 = pieces ? i * step : 0, j1 = pieces ? j0 + step : 0x7fffffff;
+    // chunks of the piece: at most `step` of each sequence, and no more than all
+    const int64_t n_piece = pieces ? std::min<int64_t>(nch, (int64_t)p.N * step) : nch;
+    cudaError_t e = launch_maybe_pdl(chunk_prep_kernel, dim3(static_cast<unsigned>(n_piece), p.Hk),
+                                     dim3(kPrepThreads), PrepSmem::BYTES + 1024, s, i > 0, tq, tk,
+                                     tv, p, ws, j0, j1);
+    if (e != cudaSuccess) return e;
+    e = launch_maybe_pdl(chunk_scan_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kScanThreads),
+                         ScanSmem::BYTES + 1024, s, pieces, tq, tk, p,
+                         static_cast<const uint8_t*>(ws), static_cast<int>(nch), j0, j1);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace gdn

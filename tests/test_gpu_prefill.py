@@ -3,7 +3,8 @@
 Every algorithm (the chunked tensor-core form in one fused launch and in two
 launches with a workspace, where supported, and the token-sequential recurrent
 form everywhere) is checked on: ragged varlen batches whose lengths
-straddle the chunk size (1, 63, 64, 65, 127, 128, 129, ...), padding slots,
+straddle the chunk size (1, 63, 64, 65, 127, 128, 129, ...), batches the
+two-launch form takes in pieces of chunk indices, padding slots,
 has_initial_state mixes, GQA ratios, f32 and bf16, in-kernel q/k norm, the
 weak-decay twins (slow decay, so a wrong carried state is not hidden), and the
 prefill workloads at full size (outputs of every head for the single 4096-token
@@ -92,6 +93,11 @@ SMALL = [
     ([40, 9, 17], 2, 6, 16, 24, torch.float32, [1], False, True),
     # eight value heads per key head: chunk_prep's loop over a key head's heads
     ([100, 37, 64, 1], 1, 8, 128, 128, torch.bfloat16, [1], False, True),
+    # few chains and more than 16 chunks: the two-launch form runs in pieces of
+    # chunk indices (each piece's scan resumes from the state the previous one
+    # stored, fresh sequences included), with a padded sequence
+    ([1030, 64, 1, 700], 2, 4, 128, 128, torch.bfloat16, [2], False, True),
+    ([1030, 64, 1, 700], 2, 4, 128, 128, torch.bfloat16, [1], True, False),
 ]
 
 
