@@ -10,6 +10,7 @@
 
 #include <mutex>
 
+#include "gdn_internal.h"
 #include "tcgen05.cuh"
 
 namespace gdn {
@@ -179,7 +180,49 @@ __device__ inline int chunk_base(const int32_t* __restrict__ cu, int s, bool& ba
 // Upper bound on the chunks of T tokens in N non-empty sequences.
 inline int64_t max_chunks(int64_t T, int64_t N) { return T / kC + N; }
 
+// Programmatic dependent launch: a grid launched with the programmatic
+// stream-serialisation attribute may start before the grid ahead of it on the
+// stream has finished; griddepcontrol.wait blocks until that grid has
+// completed and its memory is visible, and launch_dependents lets the next
+// such grid start.  Both are no-ops for grids launched the ordinary way.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- host: TMA tensor maps --------------------------------------------------------
+
+// Launches kern with the programmatic stream-serialisation attribute when pdl
+// is set (the grid may start while the one ahead of it on the stream runs).
+template <typename... Params, typename... Args>
+cudaError_t launch_maybe_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+  note_launch();
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+inline int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 152;
+  }
+  return n;
+}
+
+
 
 inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;

@@ -68,15 +68,6 @@ using namespace chunk;
 
 constexpr long long kWaitBudget = 2000000000LL;  // ~1 s of SM clock per wait
 
-// Programmatic dependent launch: a grid launched with the programmatic
-// stream-serialisation attribute may start before the grid ahead of it on the
-// stream has finished; griddepcontrol.wait blocks until that grid has
-// completed and its memory is visible, and launch_dependents lets the next
-// such grid start.  Both are no-ops for grids launched the ordinary way.
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void griddep_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
 
 // Workspace blob of one (chunk, value head): everything of the chunk that does
 // not depend on the state.
@@ -1077,36 +1068,6 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(
 // ---- host ------------------------------------------------------------------------
 
 constexpr int kPieces = 4;  // pieces of chunk indices when the chains are few
-
-// Launches kern with the programmatic stream-serialisation attribute when pdl
-// is set (the grid may start while the one ahead of it on the stream runs).
-template <typename... Params, typename... Args>
-cudaError_t launch_maybe_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
-                             cudaStream_t s, bool pdl, Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = pdl ? attr : nullptr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
-  note_launch();
-  return e != cudaSuccess ? e : cudaGetLastError();
-}
-
-int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-    cudaGetLastError();
-    return 152;
-  }
-  return n;
-}
 
 }  // namespace
 

@@ -55,6 +55,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "gdn_chunk_common.cuh"
@@ -78,6 +79,7 @@ constexpr uint32_t kBK = 81920;      // Kd hi, Kd lo: same layout (16 KB each)
 constexpr uint32_t kBImg = 114688;   // the images above: copied to the scan's stage as they are
 constexpr uint32_t kBE = 114688;     // prod_u E_u per channel, f32 [128]
 constexpr uint32_t kBlob = 115712;   // 113 KB
+constexpr int kKdaPieces = 4;        // pieces of chunk indices when the chains are few
 
 // bf16 element (t, d) of a [64 tok][128] tile stored as two SW128 boxes of 64 columns.
 __device__ __forceinline__ float tile_at(const uint8_t* tile, int t, int d) {
@@ -128,34 +130,43 @@ constexpr int kPrepThreads = 256;
 
 __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-    const RecurLaunch p, uint8_t* __restrict__ ws) {
+    const RecurLaunch p, uint8_t* __restrict__ ws, int j0, int j1) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = aligned_smem(smem_raw);
   __shared__ uint64_t mbar_tma, mbar_mma;
   __shared__ uint32_t tslot;
-  __shared__ int s_seq, s_chunk, s_ok;
+  __shared__ int s_seq, s_chunk, s_gc, s_ok;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int gc = blockIdx.x, h = blockIdx.y;
+  const int h = blockIdx.y;
   const int hk = h / (p.Hv / p.Hk);
 
-  if (warp == 0) {
+  if (warp == 0) {  // this launch's piece: the chunks with index in [j0, j1) of every sequence
     int s = 0, j = 0;
     bool bad = false;
-    const bool ok = locate_chunk(p.cu, p.N, p.T, gc, s, j, bad);
+    const bool ok = locate_chunk(p.cu, p.N, p.T, blockIdx.x, s, j, bad, j0, j1);
+    bool bad2 = false;
+    const int sbase = ok ? chunk_base(p.cu, s, bad2) : 0;  // the sequence's first global chunk
     if (lane == 0) {
       s_seq = s;
       s_chunk = j;
+      s_gc = sbase + j;
       s_ok = ok ? 1 : 0;
-      if (bad && gc == 0 && h == 0) atomicOr(p.status, kStatusBadSeqlens);
+      if (bad && blockIdx.x == 0 && h == 0) atomicOr(p.status, kStatusBadSeqlens);
     }
   }
   __syncthreads();
-  if (!s_ok) return;  // uniform: past the last chunk (or malformed cu_seqlens)
+  // In pieces, this launch runs beside the scan of the previous piece and
+  // must not complete before it: CTA (0, 0) waits for it on every way out.
+  const bool waiter = blockIdx.x == 0 && blockIdx.y == 0;
+  if (!s_ok) {  // uniform: outside this piece, past the last chunk, or malformed cu_seqlens
+    if (waiter) griddep_wait();
+    return;
+  }
   const int t0 = __ldg(p.cu + s_seq) + kC * s_chunk;
   const int L = min(kC, __ldg(p.cu + s_seq + 1) - t0);
   const uint32_t base = smem_u32(sm);
   const uint32_t mb_tma = smem_u32(&mbar_tma), mb_mma = smem_u32(&mbar_mma);
-  uint8_t* blob = ws + ((int64_t)gc * p.Hv + h) * kBlob;
+  uint8_t* blob = ws + ((int64_t)s_gc * p.Hv + h) * kBlob;
 
   if (tid == 0) {
     mbar_init(mb_tma, 1);
@@ -207,6 +218,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(
     }
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 64);
+    if (waiter) griddep_wait();
     return;
   }
 
@@ -478,6 +490,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(
   }
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 64);
+  if (waiter) griddep_wait();
 }
 
 // ---------------------------------------------------------------------------
@@ -500,7 +513,8 @@ constexpr uint32_t kSU = 256;   //       U^T hi | lo as packed bf16 pairs (32 + 
 constexpr int kScanThreads = 128;
 
 __global__ void __launch_bounds__(kScanThreads, 1) kda_scan_kernel(
-    const __grid_constant__ CUtensorMap tm_v, const RecurLaunch p, const uint8_t* __restrict__ ws) {
+    const __grid_constant__ CUtensorMap tm_v, const RecurLaunch p, const uint8_t* __restrict__ ws,
+    int j0, int j1) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = aligned_smem(smem_raw);
   __shared__ uint64_t mbar_ld, mbar_el, mbar_mma;
@@ -509,11 +523,19 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_scan_kernel(
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x % p.Hv, s = blockIdx.x / p.Hv;
 
-  const int lo = __ldg(p.cu + s), hi = __ldg(p.cu + s + 1);
-  if (lo < 0 || hi <= lo || hi > p.T || __ldg(p.cu) != 0 || __ldg(p.cu + p.N) != p.T) {
+  const int slo = __ldg(p.cu + s), shi = __ldg(p.cu + s + 1);
+  if (slo < 0 || shi <= slo || shi > p.T || __ldg(p.cu) != 0 || __ldg(p.cu + p.N) != p.T) {
     if (tid == 0) atomicOr(p.status, kStatusBadSeqlens);
     return;
   }
+  // This launch's piece of the sequence: chunks [cb, ce); it starts from the
+  // state the previous piece left in the slot.
+  const int nch_seq = (shi - slo + kC - 1) / kC;
+  const int cb = min(j0, nch_seq), ce = min(j1, nch_seq);
+  if (cb >= ce) return;
+  const int lo = slo + cb * kC, hi = min(shi, slo + ce * kC);
+  griddep_wait();               // the piece's blobs (and the previous piece's state) are complete
+  griddep_launch_dependents();  // the next piece's preparation may start
   int slot = p.sidx != nullptr ? __ldg(p.sidx + s) : s;
   if (slot < -1 || slot >= p.slots) {
     if (tid == 0) atomicOr(p.status, kStatusBadIndex);
@@ -532,7 +554,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_scan_kernel(
     bool bad = false;
     const int b = chunk_base(p.cu, s, bad);
     if (lane == 0) {
-      s_gc0 = b;
+      s_gc0 = b + cb;
       s_bad = bad ? 1 : 0;
     }
   }
@@ -562,7 +584,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_scan_kernel(
   const int dv = tid;
   const uint32_t la = static_cast<uint32_t>(warp * 32) << 16;
   float* prow = p.pool + (((int64_t)slot * p.Hv + h) * kD + dv) * kD;
-  const bool init = p.has_init == nullptr || __ldg(p.has_init + s) != 0;
+  const bool init = cb > 0 || p.has_init == nullptr || __ldg(p.has_init + s) != 0;
   // Copies and MMAs issued but not yet seen complete (thread 0's books, for a
   // clean exit after a wait that gave up).
   int pend_ld = -1, pend_el = -1, n_mma = 0;
@@ -810,6 +832,9 @@ size_t kda_chunked_workspace_bytes(int64_t T, int64_t N, int64_t Hv, int64_t Dk,
   return static_cast<size_t>(max_chunks(T, N) * Hv) * kBlob;
 }
 
+// In pieces of chunk indices when the chains are few, as the scalar-decay
+// two-launch form: each piece's preparation runs beside the previous piece's
+// scan (programmatic dependent launch).
 cudaError_t launch_kda_chunked(const ChunkedLaunch& c, cudaStream_t s) {
   const RecurLaunch& p = c.r;
   CUtensorMap tq, tk, tv;
@@ -829,17 +854,25 @@ cudaError_t launch_kda_chunked(const ChunkedLaunch& c, cudaStream_t s) {
   uint8_t* ws = static_cast<uint8_t*>(c.workspace);
   const int64_t nch = max_chunks(p.T, p.N);
   if (nch > 0x7fffffff || p.Hv > 65535) return cudaErrorInvalidConfiguration;
-  kda_prep_kernel<<<dim3(static_cast<unsigned>(nch), p.Hv), kPrepThreads, KPrep::BYTES + 1024,
-                    s>>>(tq, tk, p, ws);
-  note_launch();
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   const int64_t blocks = static_cast<int64_t>(p.N) * p.Hv;
   if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  kda_scan_kernel<<<static_cast<unsigned>(blocks), kScanThreads, KScan::BYTES + 1024, s>>>(tv, p,
-                                                                                           ws);
-  note_launch();
-  return cudaGetLastError();
+  const int64_t cmax = (p.T + kC - 1) / kC;
+  const bool pieces = 2 * blocks <= sm_count() && cmax >= 16;
+  const int step = pieces ? static_cast<int>((cmax + kKdaPieces - 1) / kKdaPieces) : 0x7fffffff;
+  const int n_pieces = pieces ? static_cast<int>((cmax + step - 1) / step) : 1;
+  for (int i = 0; i < n_pieces; ++i) {
+    const int j0 = pieces ? i * step : 0, j1 = pieces ? j0 + step : 0x7fffffff;
+    const int64_t n_piece = pieces ? std::min<int64_t>(nch, (int64_t)p.N * step) : nch;
+    cudaError_t e = launch_maybe_pdl(kda_prep_kernel, dim3(static_cast<unsigned>(n_piece), p.Hv),
+                                     dim3(kPrepThreads), KPrep::BYTES + 1024, s, i > 0, tq, tk, p,
+                                     ws, j0, j1);
+    if (e != cudaSuccess) return e;
+    e = launch_maybe_pdl(kda_scan_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kScanThreads),
+                         KScan::BYTES + 1024, s, pieces, tv, p, static_cast<const uint8_t*>(ws), j0,
+                         j1);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace gdn

@@ -115,3 +115,11 @@ def test_kda_chunked_matches_recurrent(cuda_device):
 def test_kda_chunked_full_size(cuda_device):
     """The single-sequence prefill shape: 4096 tokens, Hk = 16, Hv = 32, D = 128."""
     run([4096], 16, 32, 128, 128, torch.bfloat16, cuda_device, seed=16, algo=CHUNKED)
+
+
+def test_kda_chunked_pieces_padding_and_fresh_states(cuda_device):
+    """Few chains and more than 16 chunks: the chunked form runs in pieces of
+    chunk indices; later pieces resume from the state the previous piece
+    stored (a fresh sequence included), a padded sequence stays untouched."""
+    run([1100, 5, 300, 77], 1, 4, 128, 128, torch.bfloat16, cuda_device, seed=17, algo=CHUNKED,
+        sidx=torch.tensor([4, -1, 0, 2], dtype=torch.int32), has_init=[0, 1, 1, 0], slots=6)
