@@ -123,3 +123,41 @@ def test_kda_chunked_pieces_padding_and_fresh_states(cuda_device):
     stored (a fresh sequence included), a padded sequence stays untouched."""
     run([1100, 5, 300, 77], 1, 4, 128, 128, torch.bfloat16, cuda_device, seed=17, algo=CHUNKED,
         sidx=torch.tensor([4, -1, 0, 2], dtype=torch.int32), has_init=[0, 1, 1, 0], slots=6)
+
+
+def test_kda_chunked_pieces_cuda_graph_replay(cuda_device):
+    """The chunked KDA form in pieces (programmatic dependent launches)
+    captured in a CUDA graph: replays match eager calls bit for bit."""
+    dev = cuda_device
+    g0 = torch.Generator().manual_seed(18)
+    lens = [1100, 300]
+    T, N, Hk, Hv, D = sum(lens), len(lens), 1, 4, 128
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=dev)
+    q = (torch.randn(T, Hk, D, generator=g0) / np.sqrt(D)).to(torch.bfloat16).to(dev)
+    k = (torch.randn(T, Hk, D, generator=g0) / np.sqrt(D)).to(torch.bfloat16).to(dev)
+    v = torch.randn(T, Hv, D, generator=g0).to(torch.bfloat16).to(dev)
+    g = (-torch.rand(T, Hv, D, generator=g0) * 0.3).to(dev)
+    beta = (torch.rand(T, Hv, generator=g0) * 0.8 + 0.1).to(dev)
+    pool0 = torch.randn(N, Hv, D, D, generator=g0).to(dev) * 0.1
+    ws = torch.empty(B.gdn_kda_workspace_bytes(T, N, Hv, D, D, 1, CHUNKED), dtype=torch.uint8,
+                     device=dev)
+    pe, pg = pool0.clone(), pool0.clone()
+    oe = torch.empty(T, Hv, D, dtype=torch.bfloat16, device=dev)
+    og = torch.empty_like(oe)
+
+    def call(pool, out, stream=None):
+        B.gdn_kda_varlen(q, k, v, g, beta, pool, cu, out, algo=CHUNKED, workspace=ws,
+                         stream=stream)
+
+    call(pool0.clone(), torch.empty_like(oe))  # settles the host-side resources
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call(pg, og, stream=torch.cuda.current_stream())
+    for _ in range(3):
+        call(pe, oe)
+        graph.replay()
+        torch.cuda.synchronize()
+        B.gdn_read_device_status()
+        assert torch.equal(oe, og)
+        assert torch.equal(pe, pg)

@@ -16,6 +16,7 @@ import torch
 
 import helpers as H
 import oracle
+from gated_delta_rule_44_gb300 import binding as B
 from gated_delta_rule_44_gb300 import layer
 from gated_delta_rule_44_gb300 import workloads as W
 
@@ -151,6 +152,41 @@ def test_mixed_step_cuda_graph_replay(cuda_device):
         run(step_e, eager)
         graph.replay()
         torch.cuda.synchronize()
+        assert torch.equal(step_e.out, step_g.out)
+        assert torch.equal(eager["state_pool"], graphed["state_pool"])
+        assert torch.equal(eager["conv_pool"], graphed["conv_pool"])
+
+
+def test_pieces_cuda_graph_replay(cuda_device):
+    """A mixed step whose prefill takes the two-launch form in pieces chained
+    by programmatic dependent launch (2 prefill sequences x 4 heads, 21
+    chunks), captured in a CUDA graph: replays match eager steps bit for bit."""
+    dev = cuda_device
+    w = W.make_workload("graph", 404, [1, 1, 1100, 200], 2, 4, 128, 128, slots=7,
+                        n_decode=2, prefill_new=False, state_std=0.3)
+    assert B.gdn_prefill_resolve_algo(2, 4, 128, 128) == B.GDN_PREFILL_CHUNKED
+    eager, graphed = H.to_dev(w, dev), H.to_dev(w, dev)
+    step_e = layer.GdnStep(w.T, w.N, w.n_decode, w.Hk, w.Hv, w.Dk, w.Dv, w.K, w.act_dtype, dev)
+    step_g = layer.GdnStep(w.T, w.N, w.n_decode, w.Hk, w.Hv, w.Dk, w.Dv, w.K, w.act_dtype, dev)
+
+    def run(step, d, stream=None):
+        return step.run(d["mixed_qkv"], d["a_raw"], d["b_raw"], d["conv_weight"], d["A_log"],
+                        d["dt_bias"], d["cu_seqlens"], d["state_indices"],
+                        d["has_initial_state"], d["state_pool"], d["conv_pool"],
+                        d["cu_seqlens_prefill"], stream=stream)
+
+    warm = H.to_dev(w, dev)
+    run(step_g, warm)
+    torch.cuda.synchronize()
+    del warm
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run(step_g, graphed, stream=torch.cuda.current_stream())
+    for _ in range(3):
+        run(step_e, eager)
+        graph.replay()
+        torch.cuda.synchronize()
+        B.gdn_read_device_status()
         assert torch.equal(step_e.out, step_g.out)
         assert torch.equal(eager["state_pool"], graphed["state_pool"])
         assert torch.equal(eager["conv_pool"], graphed["conv_pool"])
