@@ -87,6 +87,15 @@ __device__ __forceinline__ float tile_at(const uint8_t* tile, int t, int d) {
       *reinterpret_cast<const __nv_bfloat16*>(tile + swz128_offset(t, d, 8192)));
 }
 
+// Four consecutive bf16 values (8 bytes, 8-byte aligned) as f32.
+__device__ __forceinline__ void ld_bf16x4(const uint8_t* p, float* v) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  v[0] = __uint_as_float(u.x << 16);
+  v[1] = __uint_as_float(u.x & 0xffff0000u);
+  v[2] = __uint_as_float(u.y << 16);
+  v[3] = __uint_as_float(u.y & 0xffff0000u);
+}
+
 __device__ __forceinline__ void st_bf16(uint8_t* p, float x) {
   *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(x);
 }
@@ -97,6 +106,13 @@ __device__ __forceinline__ void st_split1(uint8_t* hi, uint8_t* lo, float x) {
   *reinterpret_cast<uint16_t*>(hi) = static_cast<uint16_t>(__float_as_uint(h) >> 16);
   *reinterpret_cast<__nv_bfloat16*>(lo) = __float2bfloat16_rn(__fsub_rn(x, h));
 }
+
+// 2 x 4 tile of an off-diagonal A or P block: acc[i][e] = sum_d l_i[d] m[d] r_e[d]
+// over rows l_i = l0 + 8 i rows and r_e = r0 + 4 e rows (kLd floats apart), m
+// the Mid product of the block pair when MID.
+template <bool MID>
+__device__ __forceinline__ void offdiag_tile(const float* l0, const float* mrow, const float* r0,
+                                             float (&acc)[2][4]);
 
 // ---------------------------------------------------------------------------
 // Kernel 1: per (chunk, value head).  8 warps.
@@ -126,11 +142,55 @@ struct KPrep {
 static_assert(KPrep::KR + 48 * KPrep::kLd * 4 <= KPrep::TB, "operands fit before Tb");
 static_assert(KPrep::KD + 32768 <= KPrep::TB, "images fit before Tb");
 static_assert(KPrep::BYTES + 1024 <= 232448, "shared memory per CTA");
-constexpr int kPrepThreads = 256;
+
+template <bool MID>
+__device__ __forceinline__ void offdiag_tile(const float* l0, const float* mrow, const float* r0,
+                                             float (&acc)[2][4]) {
+  constexpr int LD = KPrep::kLd;
+  const float* l1 = l0 + 8 * LD;
+  // Paired f32 FMAs: lane x of acc2 sums the even channels, lane y the odd ones.
+  float2 acc2[2][4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc2[i][e] = make_float2(0.0f, 0.0f);
+#pragma unroll 4
+  for (int dd = 0; dd < kD; dd += 4) {
+    const float4 a0 = *reinterpret_cast<const float4*>(l0 + dd);
+    const float4 a1 = *reinterpret_cast<const float4*>(l1 + dd);
+    float2 x[2][2] = {{make_float2(a0.x, a0.y), make_float2(a0.z, a0.w)},
+                      {make_float2(a1.x, a1.y), make_float2(a1.z, a1.w)}};
+    if (MID) {
+      const float4 m = *reinterpret_cast<const float4*>(mrow + dd);
+      const float2 m0 = make_float2(m.x, m.y), m1 = make_float2(m.z, m.w);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        x[i][0] = __fmul2_rn(x[i][0], m0);
+        x[i][1] = __fmul2_rn(x[i][1], m1);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float4 kv = *reinterpret_cast<const float4*>(r0 + 4 * e * LD + dd);
+      const float2 k0 = make_float2(kv.x, kv.y), k1 = make_float2(kv.z, kv.w);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        acc2[i][e] = __ffma2_rn(x[i][0], k0, acc2[i][e]);
+        acc2[i][e] = __ffma2_rn(x[i][1], k1, acc2[i][e]);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[i][e] = acc2[i][e].x + acc2[i][e].y;
+}
+constexpr int kPrepThreads = 512;
 
 __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-    const RecurLaunch p, uint8_t* __restrict__ ws, int j0, int j1) {
+    const __grid_constant__ CUtensorMap tm_g, const RecurLaunch p, uint8_t* __restrict__ ws, int j0,
+    int j1) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = aligned_smem(smem_raw);
   __shared__ uint64_t mbar_tma, mbar_mma;
@@ -175,7 +235,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(
   }
   __syncthreads();
   if (tid == 0) {
-    mbar_expect_tx(mb_tma, 4 * 8192);
+    mbar_expect_tx(mb_tma, 4 * 8192 + 64 * kD * 4);
+    tma_load_3d(base + KPrep::E, &tm_g, mb_tma, 0, h, t0);
     tma_load_3d(base + KPrep::K, &tm_k, mb_tma, 0, hk, t0);
     tma_load_3d(base + KPrep::K + 8192, &tm_k, mb_tma, 64, hk, t0);
     tma_load_3d(base + KPrep::Q, &tm_q, mb_tma, 0, hk, t0);
@@ -197,21 +258,15 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(
   float* sBeta = reinterpret_cast<float*>(sm + KPrep::BETA);
   float* sEL = reinterpret_cast<float*>(sm + KPrep::EL);
   constexpr int LD = KPrep::kLd, AS = KPrep::kAs;
-  const int d = tid & 127, half = tid >> 7;
+  const int d = tid & 127, quarter = tid >> 7;
 
-  // E = e^{g} (g taken as 0 past the chunk end), beta (0 past the end).
-  for (int r = 0; r < 32; ++r) {
-    const int t = half * 32 + r;
-    const float gv = t < L ? __ldg(p.g + ((int64_t)(t0 + t) * p.Hv + h) * kD + d) : 0.0f;
-    sE[t * kD + d] = expf(gv);
-  }
   if (tid < 64) sBeta[tid] = tid < L ? __ldg(p.beta + (int64_t)(t0 + tid) * p.Hv + h) : 0.0f;
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = tslot;
   bool ok = __syncthreads_and(mbar_wait(mb_tma, 0, kWaitBudget));
-  if (!ok) {  // the K, Q tiles did not land: touch none of their bytes
+  if (!ok) {  // the g, K, Q tiles did not land: touch none of their bytes
     if (tid == 0) {
       atomicOr(p.status, kStatusTimeout);
       mbar_wait(mb_tma, 0, kWaitBudget);  // let the copies in flight finish
@@ -222,21 +277,26 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(
     return;
   }
 
-  // Scaled operands: thread (d, half) owns sub-chunks 2 half and 2 half + 1 of
-  // channel d.  Fwd runs from the sub-chunk start to t, Bwd from s + 1 to the
-  // sub-chunk end.
-  for (int bb = 0; bb < 2; ++bb) {
-    const int b = 2 * half + bb;
+  // Scaled operands: thread (d, b) owns sub-chunk b of channel d.  It first
+  // turns its g entries into E = e^{g} in place (g taken as 0 past the chunk
+  // end, where the rows are the next sequence's or the tensor's zero fill).
+  // Fwd runs from the sub-chunk start to t, Bwd from s + 1 to the sub-chunk end.
+  {
+    const int b = quarter;
     float f = 1.0f;
+#pragma unroll 4
     for (int r = 0; r < 16; ++r) {
       const int t = 16 * b + r;
-      f *= sE[t * kD + d];
+      const float e = t < L ? expf(sE[t * kD + d]) : 1.0f;
+      sE[t * kD + d] = e;
+      f *= e;
       sKL[t * LD + d] = tile_at(sK, t, d) * f;
       sQL[t * LD + d] = tile_at(sQ, t, d) * f;
     }
     sBlk[b * kD + d] = f;
     if (b < 3) {
       float w = 1.0f;
+#pragma unroll 4
       for (int r = 15; r >= 0; --r) {
         const int t = 16 * b + r;
         sKR[t * LD + d] = tile_at(sK, t, d) * w;
@@ -252,147 +312,221 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(
   }
   __syncthreads();
 
-  // Off-diagonal sub-blocks (t in I, s in J < I): warp w < 6 takes the pair
-  // (I, J) = (1,0), (2,0), (2,1), (3,0), (3,1), (3,2); lane r < 16 row 16 I + r
-  // of A, lane r >= 16 the same row of P; 16 columns each.
-  if (warp < 6) {
-    const int I = warp < 1 ? 1 : warp < 3 ? 2 : 3;
-    const int J = warp - I * (I - 1) / 2;
+  // Off-diagonal sub-blocks (t in I, s in J < I): 12 units, the six pairs
+  // (I, J) = (1,0), (2,0), (2,1), (3,0), (3,1), (3,2) times {A, P}, one per
+  // warp w < 12.  Lane (rg, cg) = (lane / 4, lane % 4) holds the 2 x 4 tile of
+  // rows 16 I + rg + 8 i and columns 16 J + cg + 4 e (rows 8 apart, columns 1
+  // apart: each 16-byte load of the warp hits distinct banks).
+  if (warp < 12) {
+    const int pair = warp >> 1, which = warp & 1;
+    const int I = pair < 1 ? 1 : pair < 3 ? 2 : 3;
+    const int J = pair - I * (I - 1) / 2;
     const int mi = I - J == 2 ? J : I - J == 3 ? 2 : -1;
-    const int t = 16 * I + (lane & 15);
-    const float* lrow = (lane < 16 ? sKL : sQL) + t * LD;
-    const float* mrow = sMid + (mi < 0 ? 0 : mi) * kD;
-    const float* kr = sKR + 16 * J * LD;
-    float acc[16];
+    const int rg = lane >> 2, cg = lane & 3;
+    const float* l0 = (which ? sQL : sKL) + (16 * I + rg) * LD;
+    const float* r0 = sKR + (16 * J + cg) * LD;
+    float acc[2][4];
+    if (mi >= 0)
+      offdiag_tile<true>(l0, sMid + mi * kD, r0, acc);
+    else
+      offdiag_tile<false>(l0, sMid, r0, acc);
 #pragma unroll
-    for (int c = 0; c < 16; ++c) acc[c] = 0.0f;
-#pragma unroll 2
-    for (int dd = 0; dd < kD; dd += 4) {
-      float4 a = *reinterpret_cast<const float4*>(lrow + dd);
-      if (mi >= 0) {
-        const float4 m = *reinterpret_cast<const float4*>(mrow + dd);
-        a.x *= m.x;
-        a.y *= m.y;
-        a.z *= m.z;
-        a.w *= m.w;
-      }
+    for (int i = 0; i < 2; ++i) {
+      const int t = 16 * I + rg + 8 * i;
+      const float f = which ? p.scale : sBeta[t];
+      float* dst = (which ? sP : sA) + t * AS + 16 * J + cg;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float4 kv = *reinterpret_cast<const float4*>(kr + c * LD + dd);
-        acc[c] = fmaf(a.x, kv.x, acc[c]);
-        acc[c] = fmaf(a.y, kv.y, acc[c]);
-        acc[c] = fmaf(a.z, kv.z, acc[c]);
-        acc[c] = fmaf(a.w, kv.w, acc[c]);
-      }
+      for (int e = 0; e < 4; ++e) dst[4 * e] = f * acc[i][e];
     }
-    const float f = lane < 16 ? sBeta[t] : p.scale;
-    float* dst = (lane < 16 ? sA : sP) + t * AS + 16 * J;
-#pragma unroll
-    for (int c = 0; c < 16; ++c) dst[c] = f * acc[c];
   }
 
-  // Diagonal sub-blocks: thread (b, s, dq) carries R = k_s . prod_{s<u<=t} E_u
-  // over 32 channels from t = s to the end of the sub-chunk; the four channel
-  // quarters are added by shuffles.
+  // Diagonal sub-blocks (s <= t inside one sub-chunk).  Warp w takes the
+  // columns s = w % 8 and s = 15 - w % 8 of sub-chunks 2 (w / 8) and
+  // 2 (w / 8) + 1: 17 rows per column pair, so the warps carry equal work and
+  // every trip count is warp-uniform.  Lane (b2, c) = (lane / 16, lane % 16)
+  // holds 8 channels of sub-chunk b = 2 (w / 8) + b2, the quads
+  // c + 16 ((j + b2) mod 2) for j < 2, and carries R = k_s . prod_{s<u<=t} E_u
+  // over them down the column.  The rows after the first go two at a time:
+  // the 16 lanes of a sub-chunk reduce the four partial dot products (A and P
+  // of both rows) by halving, so lane c ends with the full sum of value
+  // 2 (c / 8) + (c / 4) % 2.
   {
-    const int b = tid >> 6, s = (tid >> 2) & 15, dq = tid & 3;
-    float a[16], pp[16];
+    const int b2 = lane >> 4, c = lane & 15;
+    const int b = 2 * (warp >> 3) + b2;
+    int ch[2];
 #pragma unroll
-    for (int tt = 0; tt < 16; ++tt) a[tt] = pp[tt] = 0.0f;
+    for (int j = 0; j < 2; ++j) ch[j] = 4 * (c + 16 * ((j + b2) & 1));
+    const bool up8 = (c & 8) != 0, up4 = (c & 4) != 0;
 #pragma unroll 1
-    for (int dc = 0; dc < 4; ++dc) {
-      const int d0 = 32 * dq + 8 * dc;
+    for (int pass = 0; pass < 2; ++pass) {
+      const int s = pass == 0 ? (warp & 7) : 15 - (warp & 7);
       float R[8];
-      ld_bf16x8(sK + swz128_offset(16 * b + s, d0, 8192), R);
+      {  // row t = s: P only, R = k_s
+        const int t = 16 * b + s;
+        float qt[8];
 #pragma unroll
-      for (int tt = 0; tt < 16; ++tt) {
-        if (tt >= s) {
-          const int t = 16 * b + tt;
-          float kt[8], qt[8];
-          ld_bf16x8(sK + swz128_offset(t, d0, 8192), kt);
-          ld_bf16x8(sQ + swz128_offset(t, d0, 8192), qt);
-          if (tt > s) {
-            const float4 e0 = *reinterpret_cast<const float4*>(sE + t * kD + d0);
-            const float4 e1 = *reinterpret_cast<const float4*>(sE + t * kD + d0 + 4);
-            R[0] *= e0.x;
-            R[1] *= e0.y;
-            R[2] *= e0.z;
-            R[3] *= e0.w;
-            R[4] *= e1.x;
-            R[5] *= e1.y;
-            R[6] *= e1.z;
-            R[7] *= e1.w;
-          }
-          float sa = 0.0f, sp = 0.0f;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            sa = fmaf(kt[e], R[e], sa);
-            sp = fmaf(qt[e], R[e], sp);
-          }
-          a[tt] += sa;
-          pp[tt] += sp;
+        for (int j = 0; j < 2; ++j) {
+          ld_bf16x4(sK + swz128_offset(t, ch[j], 8192), R + 4 * j);
+          ld_bf16x4(sQ + swz128_offset(t, ch[j], 8192), qt + 4 * j);
         }
+        float2 p2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int e = 0; e < 8; e += 2)
+          p2 = __ffma2_rn(make_float2(qt[e], qt[e + 1]), make_float2(R[e], R[e + 1]), p2);
+        float pv = p2.x + p2.y;
+#pragma unroll
+        for (int m = 1; m < 16; m <<= 1) pv += __shfl_xor_sync(0xffffffffu, pv, m);
+        if (c == 0) sP[t * AS + 16 * b + s] = p.scale * pv;
       }
-    }
-#pragma unroll
-    for (int tt = 0; tt < 16; ++tt) {
-      a[tt] += __shfl_xor_sync(0xffffffffu, a[tt], 1);
-      a[tt] += __shfl_xor_sync(0xffffffffu, a[tt], 2);
-      pp[tt] += __shfl_xor_sync(0xffffffffu, pp[tt], 1);
-      pp[tt] += __shfl_xor_sync(0xffffffffu, pp[tt], 2);
-    }
-    if (dq == 0) {
-#pragma unroll
-      for (int tt = 0; tt < 16; ++tt) {
+#pragma unroll 1
+      for (int tt = s + 1; tt < 16; tt += 2) {
+        const bool two = tt + 1 < 16;  // warp-uniform
         const int t = 16 * b + tt;
-        if (tt > s) sA[t * AS + 16 * b + s] = sBeta[t] * a[tt];
-        if (tt >= s) sP[t * AS + 16 * b + s] = p.scale * pp[tt];
+        float v[4];
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          float2 a2 = make_float2(0.0f, 0.0f), p2 = make_float2(0.0f, 0.0f);
+          if (x == 0 || two) {
+            const int tx = t + x;
+            float kt[8], qt[8];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              ld_bf16x4(sK + swz128_offset(tx, ch[j], 8192), kt + 4 * j);
+              ld_bf16x4(sQ + swz128_offset(tx, ch[j], 8192), qt + 4 * j);
+              const float4 e = *reinterpret_cast<const float4*>(sE + tx * kD + ch[j]);
+              const float2 r0 = __fmul2_rn(make_float2(R[4 * j], R[4 * j + 1]), make_float2(e.x, e.y));
+              const float2 r1 =
+                  __fmul2_rn(make_float2(R[4 * j + 2], R[4 * j + 3]), make_float2(e.z, e.w));
+              R[4 * j] = r0.x;
+              R[4 * j + 1] = r0.y;
+              R[4 * j + 2] = r1.x;
+              R[4 * j + 3] = r1.y;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+              const float2 r = make_float2(R[e], R[e + 1]);
+              a2 = __ffma2_rn(make_float2(kt[e], kt[e + 1]), r, a2);
+              p2 = __ffma2_rn(make_float2(qt[e], qt[e + 1]), r, p2);
+            }
+          }
+          v[2 * x] = a2.x + a2.y;
+          v[2 * x + 1] = p2.x + p2.y;
+        }
+        // Halving: keep two of four (xor 8), one of two (xor 4), then add (xor 2, 1).
+        const float k0 = up8 ? v[2] : v[0], k1 = up8 ? v[3] : v[1];
+        const float s0 = up8 ? v[0] : v[2], s1 = up8 ? v[1] : v[3];
+        const float h0 = k0 + __shfl_xor_sync(0xffffffffu, s0, 8);
+        const float h1 = k1 + __shfl_xor_sync(0xffffffffu, s1, 8);
+        float w = (up4 ? h1 : h0) + __shfl_xor_sync(0xffffffffu, up4 ? h0 : h1, 4);
+        w += __shfl_xor_sync(0xffffffffu, w, 2);
+        w += __shfl_xor_sync(0xffffffffu, w, 1);
+        if ((c & 3) == 0 && (!up8 || two)) {
+          const int tw = t + (up8 ? 1 : 0);
+          if (up4)
+            sP[tw * AS + 16 * b + s] = p.scale * w;
+          else
+            sA[tw * AS + 16 * b + s] = sBeta[tw] * w;
+        }
       }
     }
   }
   __syncthreads();  // A and P complete; the f32 operands are dead
 
-  // Images over the operand space: thread (d, 0) runs prod_{u<=t} E_u forward
-  // (Ke, Qe and prod_u E_u), thread (d, 1) prod_{u>s} E_u backward (Kd).
-  if (half == 0) {
-    float pre = 1.0f;
-    for (int t = 0; t < kC; ++t) {
-      pre *= sE[t * kD + d];
-      const uint32_t off = swz128_offset(t, d, 8192);
-      st_bf16(sm + KPrep::KE + off, tile_at(sK, t, d) * pre);
-      st_split1(sm + KPrep::QE + off, sm + KPrep::QE + 16384 + off, tile_at(sQ, t, d) * pre);
+  // Warps 8-15 write the images over the operand space while warps 0-7
+  // solve for T (its barriers are named barrier 1 over those 256 threads).
+  if (warp >= 8) {
+    // Thread (dir, seg, quad) covers channels 4 quad .. 4 quad + 3 of the
+    // 16 rows of sub-chunk seg: forward (dir 0) with prod_{u<=t} E_u, started
+    // from the products of the sub-chunks before (Ke, Qe and, from the last
+    // sub-chunk, prod_u E_u), or backward (dir 1) with prod_{u>s} E_u started
+    // from the products of the sub-chunks after (Kd).
+    const int item = tid - 256, dir = item >> 7, seg = (item >> 5) & 3, c0 = 4 * (item & 31);
+    float run[4];
+    {
+      const float4 one = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+      float4 acc = one;
+      for (int b = dir ? seg + 1 : 0; b < (dir ? 4 : seg); ++b) {
+        const float4 bl = *reinterpret_cast<const float4*>(sBlk + b * kD + c0);
+        acc.x *= bl.x;
+        acc.y *= bl.y;
+        acc.z *= bl.z;
+        acc.w *= bl.w;
+      }
+      run[0] = acc.x;
+      run[1] = acc.y;
+      run[2] = acc.z;
+      run[3] = acc.w;
     }
-    sEL[d] = pre;
+    if (dir == 0) {
+#pragma unroll 4
+      for (int r = 0; r < 16; ++r) {
+        const int t = 16 * seg + r;
+        const float4 e = *reinterpret_cast<const float4*>(sE + t * kD + c0);
+        run[0] *= e.x;
+        run[1] *= e.y;
+        run[2] *= e.z;
+        run[3] *= e.w;
+        float kv[4], qv[4];
+        const uint32_t off = swz128_offset(t, c0, 8192);
+        ld_bf16x4(sK + off, kv);
+        ld_bf16x4(sQ + off, qv);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          kv[x] *= run[x];
+          qv[x] *= run[x];
+        }
+        *reinterpret_cast<uint2*>(sm + KPrep::KE + off) =
+            make_uint2(pack_bf16x2(kv[0], kv[1]), pack_bf16x2(kv[2], kv[3]));
+        uint32_t h0, l0, h1, l1;
+        split2(qv[0], qv[1], h0, l0);
+        split2(qv[2], qv[3], h1, l1);
+        *reinterpret_cast<uint2*>(sm + KPrep::QE + off) = make_uint2(h0, h1);
+        *reinterpret_cast<uint2*>(sm + KPrep::QE + 16384 + off) = make_uint2(l0, l1);
+      }
+      if (seg == 3)
+        *reinterpret_cast<float4*>(sEL + c0) = make_float4(run[0], run[1], run[2], run[3]);
+    } else {
+#pragma unroll 4
+      for (int r = 15; r >= 0; --r) {
+        const int t = 16 * seg + r;
+        float kv[4];
+        const uint32_t off = swz128_offset(t, c0, 8192);
+        ld_bf16x4(sK + off, kv);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) kv[x] *= run[x];
+        uint32_t h0, l0, h1, l1;
+        split2(kv[0], kv[1], h0, l0);
+        split2(kv[2], kv[3], h1, l1);
+        *reinterpret_cast<uint2*>(sm + KPrep::KD + off) = make_uint2(h0, h1);
+        *reinterpret_cast<uint2*>(sm + KPrep::KD + 16384 + off) = make_uint2(l0, l1);
+        const float4 e = *reinterpret_cast<const float4*>(sE + t * kD + c0);
+        run[0] *= e.x;
+        run[1] *= e.y;
+        run[2] *= e.z;
+        run[3] *= e.w;
+      }
+    }
   } else {
-    float suf = 1.0f;
-    for (int t = kC - 1; t >= 0; --t) {
-      const uint32_t off = swz128_offset(t, d, 8192);
-      st_split1(sm + KPrep::KD + off, sm + KPrep::KD + 16384 + off, tile_at(sK, t, d) * suf);
-      suf *= sE[t * kD + d];
+    // T = (I + A)^-1.  The four 16 x 16 diagonal blocks by forward
+    // substitution (lane = column; a block's 16 columns are one half-warp) ...
+    if (tid < 64) {
+      const int b0 = 16 * (tid >> 4), c = tid & 15;
+      float x[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        const float* arow = sA + (b0 + r) * AS + b0;
+        float acc = r == c ? 1.0f : 0.0f;
+#pragma unroll
+        for (int m = 0; m < r; ++m) acc = fmaf(-arow[m], x[m], acc);
+        x[r] = acc;
+      }
+      __syncwarp();
+#pragma unroll
+      for (int r = 0; r < 16; ++r) sA[(b0 + r) * AS + b0 + c] = x[r];
     }
-  }
-
-  // T = (I + A)^-1.  The four 16 x 16 diagonal blocks by forward substitution
-  // (lane = column; a block's 16 columns are one half-warp) ...
-  if (tid < 64) {
-    const int b0 = 16 * (tid >> 4), c = tid & 15;
-    float x[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      const float* arow = sA + (b0 + r) * AS + b0;
-      float acc = r == c ? 1.0f : 0.0f;
-#pragma unroll
-      for (int m = 0; m < r; ++m) acc = fmaf(-arow[m], x[m], acc);
-      x[r] = acc;
-    }
-    __syncwarp();
-#pragma unroll
-    for (int r = 0; r < 16; ++r) sA[(b0 + r) * AS + b0 + c] = x[r];
-  }
-  __syncthreads();
-  // ... then block row I from the rows above it:
-  //   Z_IJ = sum_{J <= K < I} A_IK T_KJ,  T_IJ = -T_II Z_IJ.
-  {
+    named_bar(1, 256);
+    // ... then block row I from the rows above it:
+    //   Z_IJ = sum_{J <= K < I} A_IK T_KJ,  T_IJ = -T_II Z_IJ.
     const int r = tid >> 4, c = tid & 15;
     for (int I = 1; I < 4; ++I) {
       for (int J = 0; J < I; ++J) {
@@ -404,7 +538,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(
         }
         sZ[J * 256 + r * 16 + c] = z;
       }
-      __syncthreads();
+      named_bar(1, 256);
       for (int J = 0; J < I; ++J) {
         const float* trow = sA + (16 * I + r) * AS + 16 * I;
         float y = 0.0f;
@@ -412,20 +546,27 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(
         for (int m = 0; m < 16; ++m) y = fmaf(trow[m], sZ[J * 256 + m * 16 + c], y);
         sA[(16 * I + r) * AS + 16 * J + c] = -y;
       }
-      __syncthreads();
+      named_bar(1, 256);
     }
   }
+  __syncthreads();
 
   // Tb = T diag(beta) and P as hi + lo images (zero above the diagonal); the P
   // images take the space of E, which is dead.
   for (int item = tid; item < 64 * 8; item += kPrepThreads) {
     const int i = item >> 3, q = item & 7;
-    float tv[8], pv[8];
+    float tv[8], pv[8], bv[8];
+    *reinterpret_cast<float4*>(tv) = *reinterpret_cast<const float4*>(sA + i * AS + 8 * q);
+    *reinterpret_cast<float4*>(tv + 4) = *reinterpret_cast<const float4*>(sA + i * AS + 8 * q + 4);
+    *reinterpret_cast<float4*>(pv) = *reinterpret_cast<const float4*>(sP + i * AS + 8 * q);
+    *reinterpret_cast<float4*>(pv + 4) = *reinterpret_cast<const float4*>(sP + i * AS + 8 * q + 4);
+    *reinterpret_cast<float4*>(bv) = *reinterpret_cast<const float4*>(sBeta + 8 * q);
+    *reinterpret_cast<float4*>(bv + 4) = *reinterpret_cast<const float4*>(sBeta + 8 * q + 4);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const int sc = 8 * q + e;
-      tv[e] = sc <= i ? sA[i * AS + sc] * sBeta[sc] : 0.0f;
-      pv[e] = sc <= i ? sP[i * AS + sc] : 0.0f;
+      const bool lower = 8 * q + e <= i;
+      tv[e] = lower ? tv[e] * bv[e] : 0.0f;
+      pv[e] = lower ? pv[e] : 0.0f;
     }
     const uint32_t off = swz128_offset(i, 8 * q, 8192);
     st_split8(sm + KPrep::TB + off, sm + KPrep::TB + 8192 + off, tv);
@@ -823,6 +964,22 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_scan_kernel(
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// g [rows, heads, 128] f32; box = 64 rows x 1 head x 128 channels, unswizzled
+// (row-major [64][128] in shared memory).  Rows past `rows` read as zeros.
+bool make_g_map(CUtensorMap* m, const float* g, int rows, int heads) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(heads),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 4,
+                           static_cast<cuuint64_t>(heads) * kD * 4};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kD), 1, static_cast<cuuint32_t>(kC)};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(g), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 bool kda_chunked_supported(int Dk, int Dv, bool bf16) { return bf16 && Dk == kD && Dv == kD; }
@@ -837,9 +994,9 @@ size_t kda_chunked_workspace_bytes(int64_t T, int64_t N, int64_t Hv, int64_t Dk,
 // scan (programmatic dependent launch).
 cudaError_t launch_kda_chunked(const ChunkedLaunch& c, cudaStream_t s) {
   const RecurLaunch& p = c.r;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, tg;
   if (!make_map(&tq, p.q, p.T, p.Hk) || !make_map(&tk, p.k, p.T, p.Hk) ||
-      !make_map(&tv, p.v, p.T, p.Hv))
+      !make_map(&tv, p.v, p.T, p.Hv) || !make_g_map(&tg, p.g, p.T, p.Hv))
     return cudaErrorInvalidValue;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
@@ -864,7 +1021,7 @@ cudaError_t launch_kda_chunked(const ChunkedLaunch& c, cudaStream_t s) {
     const int j0 = pieces ? i * step : 0, j1 = pieces ? j0 + step : 0x7fffffff;
     const int64_t n_piece = pieces ? std::min<int64_t>(nch, (int64_t)p.N * step) : nch;
     cudaError_t e = launch_maybe_pdl(kda_prep_kernel, dim3(static_cast<unsigned>(n_piece), p.Hv),
-                                     dim3(kPrepThreads), KPrep::BYTES + 1024, s, i > 0, tq, tk, p,
+                                     dim3(kPrepThreads), KPrep::BYTES + 1024, s, i > 0, tq, tk, tg, p,
                                      ws, j0, j1);
     if (e != cudaSuccess) return e;
     e = launch_maybe_pdl(kda_scan_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kScanThreads),
