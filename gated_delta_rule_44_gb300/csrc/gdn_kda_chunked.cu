@@ -107,84 +107,38 @@ __device__ __forceinline__ void st_split1(uint8_t* hi, uint8_t* lo, float x) {
   *reinterpret_cast<__nv_bfloat16*>(lo) = __float2bfloat16_rn(__fsub_rn(x, h));
 }
 
-// 2 x 4 tile of an off-diagonal A or P block: acc[i][e] = sum_d l_i[d] m[d] r_e[d]
-// over rows l_i = l0 + 8 i rows and r_e = r0 + 4 e rows (kLd floats apart), m
-// the Mid product of the block pair when MID.
-template <bool MID>
-__device__ __forceinline__ void offdiag_tile(const float* l0, const float* mrow, const float* r0,
-                                             float (&acc)[2][4]);
-
 // ---------------------------------------------------------------------------
 // Kernel 1: per (chunk, value head).  8 warps.
 struct KPrep {
   static constexpr uint32_t K = 0;           // K tile [64 tok][128 dk], 2 SW128 boxes (TMA)
   static constexpr uint32_t Q = 16384;       // Q tile
   static constexpr uint32_t E = 32768;       // e^{g}, f32 [64][128]; then the P hi, lo images
-  static constexpr uint32_t OP = 65536;      // f32 operands of A and P, rows kLd floats apart:
-  static constexpr uint32_t kLd = 132;
-  static constexpr uint32_t KL = OP;                    //   k_t Fwd_t  [64]
-  static constexpr uint32_t QL = OP + 64 * kLd * 4;     //   q_t Fwd_t  [64]
-  static constexpr uint32_t KR = OP + 128 * kLd * 4;    //   k_s Bwd_s  [48]
+  static constexpr uint32_t OP = 65536;      // bf16 operand images of the off-diagonal A, P:
+  static constexpr uint32_t kBox = 12288;    //   96 rows of 128 B per 64-channel box
+  static constexpr uint32_t RBH = OP;                   //   R hi: rows 0-15 R_1, 16-47 R_2, 48-95 R_3
+  static constexpr uint32_t RBL = OP + 2 * kBox;        //   R lo
+  static constexpr uint32_t LBH = OP + 4 * kBox;        //   L hi: rows 32 (I - 1) + [0, 16) k, + [16, 32) q
+  static constexpr uint32_t LBL = OP + 6 * kBox;        //   L lo
   static constexpr uint32_t KE = OP;                    // then: Ke image (16 KB), later -W^T
   static constexpr uint32_t QE = OP + 16384;            //       Qe hi, lo (16 KB each)
   static constexpr uint32_t KD = OP + 49152;            //       Kd hi, lo (16 KB each)
-  static constexpr uint32_t TB = OP + 93184;            // Tb hi, lo images (8 KB each)
+  static constexpr uint32_t TB = OP + 8 * kBox;         // Tb hi, lo images (8 KB each)
   static constexpr uint32_t AT = TB + 16384;            // A, then T in place, f32 [64][kAs]
   static constexpr uint32_t kAs = 68;
   static constexpr uint32_t PM = AT + 64 * kAs * 4;     // P, f32 [64][kAs]
-  static constexpr uint32_t Z = PM + 64 * kAs * 4;      // T solve scratch [3][16][16]
-  static constexpr uint32_t BLK = Z + 3 * 256 * 4;      // sub-chunk products [4][128]
-  static constexpr uint32_t MID = BLK + 4 * 128 * 4;    // Mid_20, Mid_31, Mid_30 [3][128]
-  static constexpr uint32_t BETA = MID + 3 * 128 * 4;   // [64]
+  static constexpr uint32_t Z = PM + 64 * kAs * 4;      // T solve scratch [32][kZs]
+  static constexpr uint32_t kZs = 36;
+  static constexpr uint32_t BLK = Z + 32 * kZs * 4;     // sub-chunk products [4][128]
+  static constexpr uint32_t BETA = BLK + 4 * 128 * 4;   // [64]
   static constexpr uint32_t EL = BETA + 64 * 4;         // prod_u E_u [128]
   static constexpr uint32_t BYTES = EL + 128 * 4;
 };
-static_assert(KPrep::KR + 48 * KPrep::kLd * 4 <= KPrep::TB, "operands fit before Tb");
 static_assert(KPrep::KD + 32768 <= KPrep::TB, "images fit before Tb");
+// The M = 128 product reads 32 rows past each 96-row R box; they exist in
+// shared memory (the next box or image) and only feed unread rows of D.
+static_assert(KPrep::RBL + 2 * KPrep::kBox + 32 * 128 <= KPrep::TB, "R reads stay in bounds");
 static_assert(KPrep::BYTES + 1024 <= 232448, "shared memory per CTA");
 
-template <bool MID>
-__device__ __forceinline__ void offdiag_tile(const float* l0, const float* mrow, const float* r0,
-                                             float (&acc)[2][4]) {
-  constexpr int LD = KPrep::kLd;
-  const float* l1 = l0 + 8 * LD;
-  // Paired f32 FMAs: lane x of acc2 sums the even channels, lane y the odd ones.
-  float2 acc2[2][4];
-#pragma unroll
-  for (int i = 0; i < 2; ++i)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc2[i][e] = make_float2(0.0f, 0.0f);
-#pragma unroll 4
-  for (int dd = 0; dd < kD; dd += 4) {
-    const float4 a0 = *reinterpret_cast<const float4*>(l0 + dd);
-    const float4 a1 = *reinterpret_cast<const float4*>(l1 + dd);
-    float2 x[2][2] = {{make_float2(a0.x, a0.y), make_float2(a0.z, a0.w)},
-                      {make_float2(a1.x, a1.y), make_float2(a1.z, a1.w)}};
-    if (MID) {
-      const float4 m = *reinterpret_cast<const float4*>(mrow + dd);
-      const float2 m0 = make_float2(m.x, m.y), m1 = make_float2(m.z, m.w);
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        x[i][0] = __fmul2_rn(x[i][0], m0);
-        x[i][1] = __fmul2_rn(x[i][1], m1);
-      }
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float4 kv = *reinterpret_cast<const float4*>(r0 + 4 * e * LD + dd);
-      const float2 k0 = make_float2(kv.x, kv.y), k1 = make_float2(kv.z, kv.w);
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        acc2[i][e] = __ffma2_rn(x[i][0], k0, acc2[i][e]);
-        acc2[i][e] = __ffma2_rn(x[i][1], k1, acc2[i][e]);
-      }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[i][e] = acc2[i][e].x + acc2[i][e].y;
-}
 constexpr int kPrepThreads = 512;
 
 __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(
@@ -242,22 +196,18 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(
     tma_load_3d(base + KPrep::Q, &tm_q, mb_tma, 0, hk, t0);
     tma_load_3d(base + KPrep::Q + 8192, &tm_q, mb_tma, 64, hk, t0);
   }
-  if (warp == 0) tmem_alloc(smem_u32(&tslot), 64);
+  if (warp == 0) tmem_alloc(smem_u32(&tslot), 128);
 
   const uint8_t* sK = sm + KPrep::K;
   const uint8_t* sQ = sm + KPrep::Q;
   float* sE = reinterpret_cast<float*>(sm + KPrep::E);
-  float* sKL = reinterpret_cast<float*>(sm + KPrep::KL);
-  float* sQL = reinterpret_cast<float*>(sm + KPrep::QL);
-  float* sKR = reinterpret_cast<float*>(sm + KPrep::KR);
   float* sA = reinterpret_cast<float*>(sm + KPrep::AT);
   float* sP = reinterpret_cast<float*>(sm + KPrep::PM);
   float* sZ = reinterpret_cast<float*>(sm + KPrep::Z);
   float* sBlk = reinterpret_cast<float*>(sm + KPrep::BLK);
-  float* sMid = reinterpret_cast<float*>(sm + KPrep::MID);
   float* sBeta = reinterpret_cast<float*>(sm + KPrep::BETA);
   float* sEL = reinterpret_cast<float*>(sm + KPrep::EL);
-  constexpr int LD = KPrep::kLd, AS = KPrep::kAs;
+  constexpr int AS = KPrep::kAs;
   const int d = tid & 127, quarter = tid >> 7;
 
   if (tid < 64) sBeta[tid] = tid < L ? __ldg(p.beta + (int64_t)(t0 + tid) * p.Hv + h) : 0.0f;
@@ -272,15 +222,24 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(
       mbar_wait(mb_tma, 0, kWaitBudget);  // let the copies in flight finish
     }
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 64);
+    if (warp == 0) tmem_dealloc(tmem, 128);
     if (waiter) griddep_wait();
     return;
   }
 
-  // Scaled operands: thread (d, b) owns sub-chunk b of channel d.  It first
-  // turns its g entries into E = e^{g} in place (g taken as 0 past the chunk
-  // end, where the rows are the next sequence's or the tensor's zero fill).
-  // Fwd runs from the sub-chunk start to t, Bwd from s + 1 to the sub-chunk end.
+  // Off-diagonal operands.  For t in sub-chunk I and s in an earlier one,
+  // prod_{s<u<=t} E_u = prod_{s<u<16I} E_u . prod_{16I<=u<=t} E_u, so
+  //   A_ts = beta_t R_I[s] . L_k[t],  P_ts = scale R_I[s] . L_q[t]
+  // with R_I[s] = k_s . prod_{s<u<16I} E_u and L_k[t], L_q[t] = k_t, q_t .
+  // prod_{16I<=u<=t} E_u (every factor a decay).  They go to the tensor core
+  // as hi + lo bf16 images (products hi.hi + hi.lo + lo.hi, about 16
+  // significant bits) in one product D = R L^T over all of them: M = 128
+  // (the R rows, 96 of them read), N = 96 (the L rows); the entries of
+  // sub-chunk I are D[r_I + s][32 (I - 1) + x] with r_I = 0, 16, 48.
+  // Pass 1: thread (d, b) turns its g entries of sub-chunk b into E = e^{g}
+  // in place (g taken as 0 past the chunk end, where the rows are the next
+  // sequence's or the tensor's zero fill), runs the product from the
+  // sub-chunk start to t and, for b >= 1, writes the L rows of sub-chunk b.
   {
     const int b = quarter;
     float f = 1.0f;
@@ -290,54 +249,78 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(
       const float e = t < L ? expf(sE[t * kD + d]) : 1.0f;
       sE[t * kD + d] = e;
       f *= e;
-      sKL[t * LD + d] = tile_at(sK, t, d) * f;
-      sQL[t * LD + d] = tile_at(sQ, t, d) * f;
-    }
-    sBlk[b * kD + d] = f;
-    if (b < 3) {
-      float w = 1.0f;
-#pragma unroll 4
-      for (int r = 15; r >= 0; --r) {
-        const int t = 16 * b + r;
-        sKR[t * LD + d] = tile_at(sK, t, d) * w;
-        w *= sE[t * kD + d];
+      if (b > 0) {
+        const uint32_t ok_k = swz128_offset(32 * (b - 1) + r, d, KPrep::kBox);
+        const uint32_t ok_q = swz128_offset(32 * (b - 1) + 16 + r, d, KPrep::kBox);
+        st_split1(sm + KPrep::LBH + ok_k, sm + KPrep::LBL + ok_k, tile_at(sK, t, d) * f);
+        st_split1(sm + KPrep::LBH + ok_q, sm + KPrep::LBL + ok_q, tile_at(sQ, t, d) * f);
       }
     }
+    sBlk[b * kD + d] = f;
   }
   __syncthreads();
-  if (tid < 128) {  // products of the whole sub-chunks between I and J
-    sMid[d] = sBlk[1 * kD + d];                          // (I, J) = (2, 0)
-    sMid[kD + d] = sBlk[2 * kD + d];                     // (3, 1)
-    sMid[2 * kD + d] = sBlk[1 * kD + d] * sBlk[2 * kD + d];  // (3, 0)
-  }
-  __syncthreads();
-
-  // Off-diagonal sub-blocks (t in I, s in J < I): 12 units, the six pairs
-  // (I, J) = (1,0), (2,0), (2,1), (3,0), (3,1), (3,2) times {A, P}, one per
-  // warp w < 12.  Lane (rg, cg) = (lane / 4, lane % 4) holds the 2 x 4 tile of
-  // rows 16 I + rg + 8 i and columns 16 J + cg + 4 e (rows 8 apart, columns 1
-  // apart: each 16-byte load of the warp hits distinct banks).
+  // Pass 2: the R rows.  Warp w < 12 takes the sub-chunk pair (J, I) =
+  // (0,1), (0,2), (0,3), (1,2), (1,3), (2,3) for w / 2 and rows
+  // 16 J + 8 (w % 2) .. + 7; lane = channel quad.  It runs prod_{s<u<16I} E_u
+  // backward from the end of its rows, started from the products of the rows
+  // after them in J and of the whole sub-chunks between J and I.
   if (warp < 12) {
-    const int pair = warp >> 1, which = warp & 1;
-    const int I = pair < 1 ? 1 : pair < 3 ? 2 : 3;
-    const int J = pair - I * (I - 1) / 2;
-    const int mi = I - J == 2 ? J : I - J == 3 ? 2 : -1;
-    const int rg = lane >> 2, cg = lane & 3;
-    const float* l0 = (which ? sQL : sKL) + (16 * I + rg) * LD;
-    const float* r0 = sKR + (16 * J + cg) * LD;
-    float acc[2][4];
-    if (mi >= 0)
-      offdiag_tile<true>(l0, sMid + mi * kD, r0, acc);
-    else
-      offdiag_tile<false>(l0, sMid, r0, acc);
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int t = 16 * I + rg + 8 * i;
-      const float f = which ? p.scale : sBeta[t];
-      float* dst = (which ? sP : sA) + t * AS + 16 * J + cg;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) dst[4 * e] = f * acc[i][e];
+    const int u = warp >> 1, hh = warp & 1, c0 = 4 * lane;
+    const int J = u < 3 ? 0 : u < 5 ? 1 : 2;
+    const int I = u < 3 ? u + 1 : u < 5 ? u - 1 : 3;
+    float w[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+    for (int bb = J + 1; bb < I; ++bb) {
+      const float4 bl = *reinterpret_cast<const float4*>(sBlk + bb * kD + c0);
+      w[0] *= bl.x;
+      w[1] *= bl.y;
+      w[2] *= bl.z;
+      w[3] *= bl.w;
     }
+    if (hh == 0) {
+#pragma unroll
+      for (int r = 8; r < 16; ++r) {
+        const float4 e = *reinterpret_cast<const float4*>(sE + (16 * J + r) * kD + c0);
+        w[0] *= e.x;
+        w[1] *= e.y;
+        w[2] *= e.z;
+        w[3] *= e.w;
+      }
+    }
+    const int rbase = I == 1 ? 0 : I == 2 ? 16 : 48;
+#pragma unroll
+    for (int r = 7; r >= 0; --r) {
+      const int t = 16 * J + 8 * hh + r;
+      float kv[4];
+      ld_bf16x4(sK + swz128_offset(t, c0, 8192), kv);
+      uint32_t h0, l0, h1, l1;
+      split2(kv[0] * w[0], kv[1] * w[1], h0, l0);
+      split2(kv[2] * w[2], kv[3] * w[3], h1, l1);
+      const uint32_t o = swz128_offset(rbase + t, c0, KPrep::kBox);
+      *reinterpret_cast<uint2*>(sm + KPrep::RBH + o) = make_uint2(h0, h1);
+      *reinterpret_cast<uint2*>(sm + KPrep::RBL + o) = make_uint2(l0, l1);
+      const float4 e = *reinterpret_cast<const float4*>(sE + t * kD + c0);
+      w[0] *= e.x;
+      w[1] *= e.y;
+      w[2] *= e.z;
+      w[3] *= e.w;
+    }
+  }
+  fence_proxy_async();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (tid == 0) {  // D into TMEM columns 0-95; the diagonal blocks run meanwhile
+    const uint32_t idesc = idesc_bf16_f32(128, 96, false, false);
+#pragma unroll
+    for (int part = 0; part < 3; ++part)  // hi.hi, hi.lo, lo.hi
+#pragma unroll
+      for (int kk = 0; kk < kD; kk += 16) {
+        const uint32_t ko = (kk >> 6) * KPrep::kBox + (kk & 63) * 2;
+        mma_bf16(tmem, desc_sw128(base + (part == 2 ? KPrep::RBL : KPrep::RBH) + ko, 16, 1024),
+                 desc_sw128(base + (part == 1 ? KPrep::LBL : KPrep::LBH) + ko, 16, 1024), idesc,
+                 part > 0 || kk > 0);
+      }
+    mma_commit(mb_mma);
   }
 
   // Diagonal sub-blocks (s <= t inside one sub-chunk).  Warp w takes the
@@ -430,7 +413,39 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(
       }
     }
   }
-  __syncthreads();  // A and P complete; the f32 operands are dead
+  // The off-diagonal blocks from D: warp w < 12 reads columns 32 (I - 1) ..
+  // 32 I - 1, I = w / 4 + 1, over its TMEM lane quarter (row m of D in lane
+  // m); the lanes whose row is a key row of R_I write theirs.
+  ok = __syncthreads_and(mbar_wait(mb_mma, 0, kWaitBudget));  // uniform: tcgen05.ld is warp-wide
+  fence_after_sync();
+  if (!ok) {  // the MMAs did not complete: drain them (bounded) and leave
+    if (tid == 0) {
+      atomicOr(p.status, kStatusTimeout);
+      mbar_wait(mb_mma, 0, kWaitBudget);
+    }
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 128);
+    if (waiter) griddep_wait();
+    return;
+  }
+  if (warp < 12) {
+    const int qd = warp & 3, I = (warp >> 2) + 1;
+    float v[32];
+    tmem_ld32(tmem + (static_cast<uint32_t>(qd * 32) << 16) + 32 * (I - 1), v);
+    tmem_ld_wait();
+    const int sc = 32 * qd + lane - (I == 1 ? 0 : I == 2 ? 16 : 48);
+    if (sc >= 0 && sc < 16 * I) {
+#pragma unroll
+      for (int x = 0; x < 16; ++x) {
+        const int t = 16 * I + x;
+        sA[t * AS + sc] = sBeta[t] * v[x];
+        sP[t * AS + sc] = p.scale * v[16 + x];
+      }
+    }
+  }
+  fence_before_sync();
+  __syncthreads();  // A and P complete; the operand images are dead
+  fence_after_sync();
 
   // Warps 8-15 write the images over the operand space while warps 0-7
   // solve for T (its barriers are named barrier 1 over those 256 threads).
@@ -507,46 +522,101 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(
       }
     }
   } else {
-    // T = (I + A)^-1.  The four 16 x 16 diagonal blocks by forward
-    // substitution (lane = column; a block's 16 columns are one half-warp) ...
-    if (tid < 64) {
-      const int b0 = 16 * (tid >> 4), c = tid & 15;
+    // T = (I + A)^-1 (A strictly lower triangular) by blocks, on warps 0-7:
+    // (1) the four 16 x 16 diagonal blocks by forward substitution, a
+    //     half-warp per block with lane = column c:
+    //     x_i = [i == c] - sum_{m < i} A[16b+i][16b+m] x_m;
+    // (2) each 32 x 32 diagonal block from its two: lower-left block
+    //     X = -D1 (A10 D0), D0 and D1 the inverted diagonal blocks;
+    // (3) the lower-left 32 x 32 block T21 = -T22 (A21 T11).
+    constexpr int ZS = KPrep::kZs;
+    if (warp < 2) {
+      const int b0 = 16 * (2 * warp + (lane >> 4)), c = lane & 15;
       float x[16];
 #pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        const float* arow = sA + (b0 + r) * AS + b0;
-        float acc = r == c ? 1.0f : 0.0f;
+      for (int i = 0; i < 16; ++i) {
+        const float* arow = sA + (b0 + i) * AS + b0;
+        float a0 = i == c ? 1.0f : 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
 #pragma unroll
-        for (int m = 0; m < r; ++m) acc = fmaf(-arow[m], x[m], acc);
-        x[r] = acc;
+        for (int m = 0; m < i; m += 4) {
+          const float4 av = *reinterpret_cast<const float4*>(arow + m);
+          a0 = fmaf(-av.x, x[m], a0);
+          if (m + 1 < i) a1 = fmaf(-av.y, x[m + 1], a1);
+          if (m + 2 < i) a2 = fmaf(-av.z, x[m + 2], a2);
+          if (m + 3 < i) a3 = fmaf(-av.w, x[m + 3], a3);
+        }
+        x[i] = (a0 + a1) + (a2 + a3);
       }
       __syncwarp();
 #pragma unroll
-      for (int r = 0; r < 16; ++r) sA[(b0 + r) * AS + b0 + c] = x[r];
+      for (int i = 0; i < 16; ++i) sA[(b0 + i) * AS + b0 + c] = x[i];
     }
     named_bar(1, 256);
-    // ... then block row I from the rows above it:
-    //   Z_IJ = sum_{J <= K < I} A_IK T_KJ,  T_IJ = -T_II Z_IJ.
-    const int r = tid >> 4, c = tid & 15;
-    for (int I = 1; I < 4; ++I) {
-      for (int J = 0; J < I; ++J) {
-        float z = 0.0f;
-        for (int K = J; K < I; ++K) {
-          const float* arow = sA + (16 * I + r) * AS + 16 * K;
+    {  // (2) Z = A10 D0 (thread: block B, row r, two columns), then X = -D1 Z
+      const int B = tid >> 7, r = (tid >> 3) & 15, c0 = (tid & 7) * 2;
+      const float* arow = sA + (32 * B + 16 + r) * AS + 32 * B;
+      float z0 = 0.0f, z1 = 0.0f;
 #pragma unroll
-          for (int m = 0; m < 16; ++m) z = fmaf(arow[m], sA[(16 * K + m) * AS + 16 * J + c], z);
+      for (int m = 0; m < 16; ++m) {
+        const float a = arow[m];
+        const float2 dv = *reinterpret_cast<const float2*>(sA + (32 * B + m) * AS + 32 * B + c0);
+        z0 = fmaf(a, dv.x, z0);
+        z1 = fmaf(a, dv.y, z1);
+      }
+      *reinterpret_cast<float2*>(sZ + (16 * B + r) * ZS + c0) = make_float2(z0, z1);
+      named_bar(1, 256);
+      const float* drow = sA + (32 * B + 16 + r) * AS + 32 * B + 16;
+      float x0 = 0.0f, x1 = 0.0f;
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        const float dv = drow[m];
+        const float2 z = *reinterpret_cast<const float2*>(sZ + (16 * B + m) * ZS + c0);
+        x0 = fmaf(dv, z.x, x0);
+        x1 = fmaf(dv, z.y, x1);
+      }
+      *reinterpret_cast<float2*>(sA + (32 * B + 16 + r) * AS + 32 * B + c0) =
+          make_float2(-x0, -x1);
+      // The upper-right 16 x 16 block of each 32 x 32 inverse is zero (nothing
+      // above the diagonal of A was written); step (3) reads whole rows.
+      *reinterpret_cast<float2*>(sA + (32 * B + r) * AS + 32 * B + 16 + c0) =
+          make_float2(0.0f, 0.0f);
+    }
+    named_bar(1, 256);
+    {  // (3) Y = A21 T11, then T21 = -T22 Y: thread -> row i, columns j0 .. j0 + 3
+      const int bi = tid >> 3, bj = (tid & 7) * 4;
+      float y[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      const float* arow = sA + (32 + bi) * AS;
+#pragma unroll
+      for (int k = 0; k < 32; k += 4) {
+        const float4 av4 = *reinterpret_cast<const float4*>(arow + k);
+        const float av[4] = {av4.x, av4.y, av4.z, av4.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 tv = *reinterpret_cast<const float4*>(sA + (k + q) * AS + bj);
+          y[0] = fmaf(av[q], tv.x, y[0]);
+          y[1] = fmaf(av[q], tv.y, y[1]);
+          y[2] = fmaf(av[q], tv.z, y[2]);
+          y[3] = fmaf(av[q], tv.w, y[3]);
         }
-        sZ[J * 256 + r * 16 + c] = z;
       }
+      *reinterpret_cast<float4*>(sZ + bi * ZS + bj) = make_float4(y[0], y[1], y[2], y[3]);
       named_bar(1, 256);
-      for (int J = 0; J < I; ++J) {
-        const float* trow = sA + (16 * I + r) * AS + 16 * I;
-        float y = 0.0f;
+      const float* trow = sA + (32 + bi) * AS + 32;
+      float w[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int m = 0; m < 16; ++m) y = fmaf(trow[m], sZ[J * 256 + m * 16 + c], y);
-        sA[(16 * I + r) * AS + 16 * J + c] = -y;
+      for (int k = 0; k < 32; k += 4) {
+        const float4 tv4 = *reinterpret_cast<const float4*>(trow + k);
+        const float tv[4] = {tv4.x, tv4.y, tv4.z, tv4.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 yv = *reinterpret_cast<const float4*>(sZ + (k + q) * ZS + bj);
+          w[0] = fmaf(tv[q], yv.x, w[0]);
+          w[1] = fmaf(tv[q], yv.y, w[1]);
+          w[2] = fmaf(tv[q], yv.z, w[2]);
+          w[3] = fmaf(tv[q], yv.w, w[3]);
+        }
       }
-      named_bar(1, 256);
+      *reinterpret_cast<float4*>(sA + (32 + bi) * AS + bj) = make_float4(-w[0], -w[1], -w[2], -w[3]);
     }
   }
   __syncthreads();
@@ -596,7 +666,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(
     bulk_s2g(blob + kBE, base + KPrep::EL, 512);
     bulk_commit();
   }
-  ok = __syncthreads_and(mbar_wait(mb_mma, 0, kWaitBudget));  // uniform: tcgen05.ld is warp-wide
+  ok = __syncthreads_and(mbar_wait(mb_mma, 1, kWaitBudget));  // uniform: tcgen05.ld is warp-wide
   fence_after_sync();
   if (ok && warp < 4) {  // -W^T image over Ke (the MMA has read Ke)
     const uint32_t la = static_cast<uint32_t>(warp * 32) << 16;
@@ -627,10 +697,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1) kda_prep_kernel(
   }
   if (!ok && tid == 0) {
     atomicOr(p.status, kStatusTimeout);
-    mbar_wait(mb_mma, 0, kWaitBudget);  // the MMA in flight
+    mbar_wait(mb_mma, 1, kWaitBudget);  // the MMA in flight
   }
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 64);
+  if (warp == 0) tmem_dealloc(tmem, 128);
   if (waiter) griddep_wait();
 }
 
