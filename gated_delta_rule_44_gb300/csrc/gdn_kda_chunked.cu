@@ -19,18 +19,16 @@
 //   S_L = S0 diag(prod_u E_u) + U^T Kd
 //
 // A and P.  The decay inside each dot product depends on the channel, so it
-// cannot be taken out as in the scalar-decay form.  They are computed on CUDA
-// cores in f32 from operands scaled about 16-token sub-chunk boundaries: for
-// t in sub-chunk I and s in an earlier sub-chunk J,
-//   prod_{s<u<=t} E_u = Fwd_t . Mid_IJ . Bwd_s
-// with Fwd_t the product from the start of I to t, Bwd_s the product from s + 1
-// to the end of J and Mid_IJ the products of the whole sub-chunks between them
-// (each factor a decay, <= 1).  Pairs inside one sub-chunk take running
-// products of E from s to t.
+// cannot be taken out as in the scalar-decay form.  They are split by 16-token
+// sub-chunks.  For t in sub-chunk I and s in an earlier one,
+//   prod_{s<u<=t} E_u = prod_{s<u<16I} E_u . prod_{16I<=u<=t} E_u
+// (both decays, <= 1), so those blocks are dot products of pre-scaled rows and
+// go to the tensor core as hi + lo bf16 images.  Pairs inside one sub-chunk
+// take running products of E from s to t on CUDA cores in f32.
 //
 // Two launches on the caller's stream:
 //  1. kda_prep (one CTA per (chunk, value head), all chunks in parallel): E, A
-//     and P (f32), T by 16 x 16 blocks, W^T = Ke^T Tb^T (tcgen05); writes the
+//     and P (f32), T by blocks, W^T = Ke^T Tb^T (tcgen05); writes the
 //     chunk's blob: the -W^T, P, Tb, Qe and Kd images (hi + lo bf16 pairs but
 //     W) in the shared-memory layouts the second kernel feeds to the tensor
 //     core, and prod_u E_u.
@@ -108,7 +106,7 @@ __device__ __forceinline__ void st_split1(uint8_t* hi, uint8_t* lo, float x) {
 }
 
 // ---------------------------------------------------------------------------
-// Kernel 1: per (chunk, value head).  8 warps.
+// Kernel 1: per (chunk, value head).  16 warps.
 struct KPrep {
   static constexpr uint32_t K = 0;           // K tile [64 tok][128 dk], 2 SW128 boxes (TMA)
   static constexpr uint32_t Q = 16384;       // Q tile
