@@ -98,16 +98,46 @@ struct Act<__nv_bfloat16> {
   }
 };
 
+// conv + SiLU of one token's V channels from its window (win[j] = the input
+// W - j tokens back, oldest first) and its own input xt, with channel pairs in
+// paired f32 arithmetic; returns the sum of the squares of y (even and odd
+// channels summed apart, then added).  The conv of each channel is the same
+// chain of fused multiply-adds, oldest tap first, as a scalar loop.
+template <int V, int KW, int WV>
+__device__ __forceinline__ float conv_silu_row(const float (&win)[WV][V], const float (&xt)[V],
+                                               const float (&wt)[V][KW], float (&y)[V]) {
+  constexpr int W = KW - 1;
+  float2 ss2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+  for (int i = 0; i < V; i += 2) {
+    float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int j = 0; j < W; ++j)
+      acc = __ffma2_rn(make_float2(win[j][i], win[j][i + 1]), make_float2(wt[i][j], wt[i + 1][j]), acc);
+    acc = __ffma2_rn(make_float2(xt[i], xt[i + 1]), make_float2(wt[i][W], wt[i + 1][W]), acc);
+    const float2 yy = math::silu2(acc);
+    y[i] = yy.x;
+    y[i + 1] = yy.y;
+    ss2 = __ffma2_rn(yy, yy, ss2);
+  }
+  return ss2.x + ss2.y;
+}
+
 // Largest s in [0, n) with cu[s] <= t (cu assumed non-decreasing; callers
 // re-check the bracket, so a malformed cu only yields a bounded wrong guess).
-__device__ __forceinline__ int find_seq(const int32_t* __restrict__ cu, int n, int t) {
-  int lo = 0, hi = n - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(cu + mid) <= t)
-      lo = mid;
-    else
-      hi = mid - 1;
+// A 32-way search by the whole warp: each round the lanes read 32 evenly
+// spaced entries of the remaining range and keep the span after the last one
+// <= t, so n = 1024 takes two dependent reads.  Called by every lane.
+__device__ __forceinline__ int find_seq(const int32_t* __restrict__ cu, int n, int t, int lane) {
+  int lo = 0, len = n;
+  while (len > 1) {
+    const int step = (len + 31) >> 5;
+    const int idx = lo + lane * step;
+    const bool le = lane * step < len && __ldg(cu + idx) <= t;
+    const unsigned m = __ballot_sync(0xffffffffu, le);
+    const int last = m != 0u ? 31 - __clz(static_cast<int>(m)) : 0;
+    lo += last * step;
+    len = min(step, len - last * step);
   }
   return lo;
 }
@@ -155,12 +185,42 @@ __global__ void __launch_bounds__(kThreads, 4) prepare_kernel(const PrepareLaunc
   const bool active = c0 < C;
   const bool is_qk = c0 < 2 * qk_total;
   const int group = p.Dk / V;  // lanes per key head (power of two <= 32)
+  constexpr int kG = 4;  // interior tiles: rows per group (their norms share shuffle rounds)
 
+  // Loads that need nothing but the tile go out before anything waits: the
+  // bounds of cu_seqlens, the W rows before the tile and its first kG rows (what
+  // an interior tile reads first; other tiles drop them) and the conv weights
+  // (V * KW consecutive floats, 16-byte aligned).
+  const int cu_first = __ldg(p.cu), cu_last = __ldg(p.cu + p.N);
+  const TA* xrow = x + (int64_t)t_begin * p.x_stride + c0;
+  const bool spec = active && t_begin >= W;
+  uint4 pre_w[WV], pre_x[kG];
+#pragma unroll
+  for (int j = 0; j < WV; ++j)
+    pre_w[j] = (spec && j < W) ? Act<TA>::load_raw(xrow - (int64_t)(W - j) * p.x_stride)
+                               : make_uint4(0, 0, 0, 0);
+#pragma unroll
+  for (int u = 0; u < kG; ++u)
+    pre_x[u] = (spec && t_begin + u < t_end) ? Act<TA>::load_raw(xrow + (int64_t)u * p.x_stride)
+                                             : make_uint4(0, 0, 0, 0);
   float wt[V][KW];
+  {
+    static_assert((V * KW) % 4 == 0, "weights as float4");
+    float wf[V * KW];
+    const float4* wsrc = reinterpret_cast<const float4*>(p.w + (int64_t)c0 * KW);
 #pragma unroll
-  for (int i = 0; i < V; ++i)
+    for (int q4 = 0; q4 < V * KW / 4; ++q4) {
+      const float4 f = active ? __ldg(wsrc + q4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      wf[4 * q4] = f.x;
+      wf[4 * q4 + 1] = f.y;
+      wf[4 * q4 + 2] = f.z;
+      wf[4 * q4 + 3] = f.w;
+    }
 #pragma unroll
-    for (int j = 0; j < KW; ++j) wt[i][j] = active ? __ldg(p.w + (int64_t)(c0 + i) * KW + j) : 0.0f;
+    for (int i = 0; i < V; ++i)
+#pragma unroll
+      for (int j = 0; j < KW; ++j) wt[i][j] = wf[i * KW + j];
+  }
 
   TA* __restrict__ out_ptr;  // row base of this thread's output vector
   int64_t out_stride;
@@ -179,16 +239,7 @@ __global__ void __launch_bounds__(kThreads, 4) prepare_kernel(const PrepareLaunc
   // and its own input.  Uniform across the warp: every lane joins the shuffles.
   auto emit = [&](int t, const float (&win)[WV][V], const float (&xt)[V]) {
     float y[V];
-    float ss = 0.0f;
-#pragma unroll
-    for (int i = 0; i < V; ++i) {
-      float acc = 0.0f;
-#pragma unroll
-      for (int j = 0; j < W; ++j) acc = fmaf(win[j][i], wt[i][j], acc);
-      acc = fmaf(xt[i], wt[i][W], acc);
-      y[i] = silu_f(acc);
-      ss = fmaf(y[i], y[i], ss);
-    }
+    float ss = conv_silu_row<V, KW, WV>(win, xt, wt, y);
     if (p.norm) {
       for (int m = 1; m < group; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
       if (is_qk) {
@@ -201,9 +252,9 @@ __global__ void __launch_bounds__(kThreads, 4) prepare_kernel(const PrepareLaunc
   };
 
   // Sequence bracket of the tile's first token.
-  int s = find_seq(p.cu, p.N, t_begin);
+  int s = find_seq(p.cu, p.N, t_begin, lane);
   int seq_lo = __ldg(p.cu + s), seq_hi = __ldg(p.cu + s + 1);
-  if (__ldg(p.cu) != 0 || __ldg(p.cu + p.N) != p.T || !(seq_lo <= t_begin && t_begin < seq_hi) ||
+  if (cu_first != 0 || cu_last != p.T || !(seq_lo <= t_begin && t_begin < seq_hi) ||
       seq_lo < 0 || seq_hi > p.T) {
     if (threadIdx.x == 0) atomicOr(p.status, kStatusBadSeqlens);
     return;
@@ -216,22 +267,15 @@ __global__ void __launch_bounds__(kThreads, 4) prepare_kernel(const PrepareLaunc
   // warp-uniform test: with 2*Hk*Dk below a multiple of the warp's channels a
   // warp holds k and v lanes), and the scaling on q and k lanes only; warps of
   // v channels alone skip both.
-  if (seq_lo + W <= t_begin && t_end <= seq_hi) {
-    constexpr int kG = 4;
+  if (seq_lo + W <= t_begin && t_end <= seq_hi) {  // here t_begin >= W: the early loads hold
     const int n = t_end - t_begin;
     const bool norm_warp = p.norm && (c0 - lane * V) < 2 * qk_total;  // lane 0's channel
-    const TA* xrow = x + (int64_t)t_begin * p.x_stride + c0;
     float win[WV][V];
 #pragma unroll
-    for (int j = 0; j < W; ++j) {
-      uint4 r = active ? Act<TA>::load_raw(xrow - (int64_t)(W - j) * p.x_stride) : make_uint4(0, 0, 0, 0);
-      Act<TA>::unpack(r, win[j]);
-    }
+    for (int j = 0; j < W; ++j) Act<TA>::unpack(pre_w[j], win[j]);
     uint4 nxt[kG];
 #pragma unroll
-    for (int u = 0; u < kG; ++u)
-      nxt[u] = (active && u < n) ? Act<TA>::load_raw(xrow + (int64_t)u * p.x_stride)
-                                 : make_uint4(0, 0, 0, 0);
+    for (int u = 0; u < kG; ++u) nxt[u] = pre_x[u];
 #pragma unroll 1
     for (int r0 = 0; r0 < n; r0 += kG) {
       float y[kG][V];
@@ -243,16 +287,7 @@ __global__ void __launch_bounds__(kThreads, 4) prepare_kernel(const PrepareLaunc
         const int r = r0 + kG + u;
         nxt[u] = (active && r < n) ? Act<TA>::load_raw(xrow + (int64_t)r * p.x_stride)
                                    : make_uint4(0, 0, 0, 0);
-        ss[u] = 0.0f;
-#pragma unroll
-        for (int i = 0; i < V; ++i) {
-          float acc = 0.0f;
-#pragma unroll
-          for (int j = 0; j < W; ++j) acc = fmaf(win[j][i], wt[i][j], acc);
-          acc = fmaf(xt[i], wt[i][W], acc);
-          y[u][i] = silu_f(acc);
-          ss[u] = fmaf(y[u][i], y[u][i], ss[u]);
-        }
+        ss[u] = conv_silu_row<V, KW, WV>(win, xt, wt, y[u]);
 #pragma unroll
         for (int j = 0; j + 1 < W; ++j)
 #pragma unroll
@@ -300,6 +335,17 @@ __global__ void __launch_bounds__(kThreads, 4) prepare_kernel(const PrepareLaunc
       one = s + lane < p.N && __ldg(p.cu + s + lane + 1) == t_begin + lane + 1;
     }
     if (__all_sync(0xffffffffu, one) && W > 0) {
+      // The slot and has_init of row i, read once by lane i of every warp (n <= 32).
+      int my_slot = -1;
+      bool my_init = false;
+      if (lane < n) {
+        my_slot = p.sidx != nullptr ? __ldg(p.sidx + s + lane) : s + lane;
+        if (my_slot < -1 || my_slot >= p.slots) {
+          atomicOr(p.status, kStatusBadIndex);
+          my_slot = -1;
+        }
+        my_init = my_slot >= 0 && (p.has_init == nullptr || __ldg(p.has_init + s + lane) != 0);
+      }
       constexpr int kBatch = 2;
       for (int b0 = 0; b0 < n; b0 += kBatch) {
         float tails[kBatch][WV][V];
@@ -314,9 +360,9 @@ __global__ void __launch_bounds__(kThreads, 4) prepare_kernel(const PrepareLaunc
           for (int j = 0; j < W; ++j)
 #pragma unroll
             for (int e = 0; e < V; ++e) tails[bi][j][e] = 0.0f;
+          const int slot = __shfl_sync(0xffffffffu, my_slot, i & 31);
+          const bool init = __shfl_sync(0xffffffffu, my_init ? 1 : 0, i & 31) != 0;
           if (i < n) {
-            const int slot = slot_of(s + i);
-            const bool init = slot >= 0 && (p.has_init == nullptr || __ldg(p.has_init + s + i) != 0);
             if (slot >= 0 && active) tp[bi] = p.conv_pool + ((int64_t)slot * C + c0) * W;
             if (active) xr[bi] = Act<TA>::load_raw(x + (int64_t)(t_begin + i) * p.x_stride + c0);
             if (init && active) {
@@ -599,16 +645,7 @@ __global__ void __launch_bounds__(kThreads) spec_prepare_kernel(const PrepareLau
   auto step = [&](int u, const float (&xt)[V]) {
     const int t = lo + u;
     float y[V];
-    float ss = 0.0f;
-#pragma unroll
-    for (int e = 0; e < V; ++e) {
-      float acc = 0.0f;
-#pragma unroll
-      for (int j = 0; j < W; ++j) acc = fmaf(win[j][e], wt[e][j], acc);
-      acc = fmaf(xt[e], wt[e][W], acc);
-      y[e] = silu_f(acc);
-      ss = fmaf(y[e], y[e], ss);
-    }
+    float ss = conv_silu_row<V, KW, W>(win, xt, wt, y);
     if (norm_warp) {
       for (int m = 1; m < group; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
       if (is_qk) {
