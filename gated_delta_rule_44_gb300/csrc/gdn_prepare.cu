@@ -11,8 +11,8 @@
 // 4 f32) and walks the tokens of a tile in order, keeping the last K-1 raw
 // inputs of its channels in registers (the conv window).  A warp therefore
 // reads 512 contiguous bytes of a token row per step; a CTA of 4 warps covers
-// 2 KB of the row.  grid.x = token tiles of `tile` tokens, grid.y = channel
-// blocks (+1 block row for the gates).  The L2 norm of a key head (Dk channels =
+// 2 KB of the row.  grid.x = channel blocks (+1 for the gates), grid.y = token
+// tiles of `tile` tokens.  The L2 norm of a key head (Dk channels =
 // Dk/8 lanes) is a shuffle reduction inside the warp.
 //
 // Conv-tail ownership.  The old tail of a sequence is read by the outputs of
@@ -144,17 +144,24 @@ __device__ __forceinline__ int find_seq(const int32_t* __restrict__ cu, int n, i
 
 template <typename TA, int KW>
 __global__ void __launch_bounds__(kThreads, 4) prepare_kernel(const PrepareLaunch p, int tile,
-                                                              int chan_blocks) {
+                                                              int chan_blocks, bool tiles_on_y) {
+  // blockIdx.x runs over the channel blocks (and the gate block), blockIdx.y
+  // over the tiles: the hardware hands out CTAs with x fastest, so every
+  // channel block of a tile goes out before the next tile (the one-token
+  // sequences, which take longest, come first in a mixed batch).  Above
+  // 65535 tiles the two swap.
+  const int tile_idx = tiles_on_y ? blockIdx.y : blockIdx.x;
+  const int cblk = tiles_on_y ? blockIdx.x : blockIdx.y;
   constexpr int V = Act<TA>::kVec;
   constexpr int W = KW - 1;  // conv tail length
   constexpr int WV = W > 0 ? W : 1;
   const int qk_total = p.Hk * p.Dk;
   const int C = 2 * qk_total + p.Hv * p.Dv;
-  const int t_begin = blockIdx.x * tile;
+  const int t_begin = tile_idx * tile;
   const int t_end = min(p.T, t_begin + tile);
   const TA* __restrict__ x = static_cast<const TA*>(p.x);
 
-  if (blockIdx.y == chan_blocks) {  // gates: g, beta per (token, value head)
+  if (cblk == chan_blocks) {  // gates: g, beta per (token, value head)
     const TA* __restrict__ a = static_cast<const TA*>(p.a);
     const TA* __restrict__ b = static_cast<const TA*>(p.b);
     const int n = (t_end - t_begin) * p.Hv;
@@ -173,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 4) prepare_kernel(const PrepareLaunc
   // block) into L2 up front, one bulk prefetch per row: the per-thread loads
   // below then wait on L2 rather than on HBM, without holding registers.
   {
-    const int cb = blockIdx.y * kThreads * V;
+    const int cb = cblk * kThreads * V;
     const int bytes = min(kThreads * V, C - cb) * static_cast<int>(sizeof(TA));
     const int r = t_begin - W + static_cast<int>(threadIdx.x);
     if (r >= 0 && r < t_end && bytes > 0)
@@ -181,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 4) prepare_kernel(const PrepareLaunc
                    "r"(bytes)
                    : "memory");
   }
-  const int c0 = ((blockIdx.y * kWarps + warp) * 32 + lane) * V;
+  const int c0 = ((cblk * kWarps + warp) * 32 + lane) * V;
   const bool active = c0 < C;
   const bool is_qk = c0 < 2 * qk_total;
   const int group = p.Dk / V;  // lanes per key head (power of two <= 32)
@@ -738,14 +745,18 @@ cudaError_t launch_k(const PrepareLaunch& p, cudaStream_t s) {
   constexpr int V = Act<TA>::kVec;
   const int C = 2 * p.Hk * p.Dk + p.Hv * p.Dv;
   const int chan_blocks = (C + kThreads * V - 1) / (kThreads * V);
-  // Tiles of at least K-1 tokens (tail ownership); shrink them while the grid
-  // is short of ~8 CTAs per SM.
+  // Tiles of at least K-1 tokens (tail ownership) and at most 32 (a decode
+  // tile reads its rows' slots one per lane); shrink them while the grid is
+  // short of ~8 CTAs per SM.
   int tile = 32;
   while (tile > 2 && (int64_t)((p.T + tile - 1) / tile) * chan_blocks < 8 * 152) tile >>= 1;
   if (tile < KW - 1) tile = KW - 1;  // >= K-1 for the tail ownership rule (K <= 8: <= 16)
-  dim3 grid((p.T + tile - 1) / tile, chan_blocks + 1);
-  if (grid.y > 65535) return cudaErrorInvalidConfiguration;
-  prepare_kernel<TA, KW><<<grid, kThreads, 0, s>>>(p, tile, chan_blocks);
+  const int64_t n_tiles = (p.T + tile - 1) / tile;
+  const bool tiles_on_y = n_tiles <= 65535;
+  if (chan_blocks + 1 > 65535) return cudaErrorInvalidConfiguration;
+  const dim3 grid = tiles_on_y ? dim3(chan_blocks + 1, static_cast<unsigned>(n_tiles))
+                               : dim3(static_cast<unsigned>(n_tiles), chan_blocks + 1);
+  prepare_kernel<TA, KW><<<grid, kThreads, 0, s>>>(p, tile, chan_blocks, tiles_on_y);
   note_launch();
   return cudaGetLastError();
 }
