@@ -56,26 +56,6 @@ __device__ __forceinline__ float silu_f(float x) {
   return x * recip_nr(1.0f + __expf(fminf(-x, 80.0f)));
 }
 
-// silu of two values with paired f32 arithmetic (the prepare's hot loop):
-// e^{-x} as 2^{-x log2(e)} on the hardware's approximate base-2 exponential,
-// capped at e^80 as in silu_f, then x / (1 + e^{-x}) on the refined reciprocal.
-__device__ __forceinline__ float2 silu2(float2 x) {
-  constexpr float kNegLog2e = -1.4426950408889634f;
-  constexpr float kCap = 80.0f * 1.4426950408889634f;
-  const float2 m = __fmul2_rn(x, make_float2(kNegLog2e, kNegLog2e));
-  float e0, e1;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(fminf(m.x, kCap)));
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(fminf(m.y, kCap)));
-  const float2 d = __fadd2_rn(make_float2(1.0f, 1.0f), make_float2(e0, e1));
-  float r0, r1;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(d.x));
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(d.y));
-  float2 r = make_float2(r0, r1);
-  const float2 t = __ffma2_rn(make_float2(-d.x, -d.y), r, make_float2(1.0f, 1.0f));
-  r = __ffma2_rn(r, t, r);
-  return __fmul2_rn(x, r);
-}
-
 // The gate of the gated RMSNorm ([cpu.rs] gated_rms_norm_f32: silu(z);
 // [cpu_ops.cpp] RmsNormGatedKernel's option: sigmoid(z)), with sigmoid(z) =
 // 1 / (1 + e^{-z}) on the refined reciprocal (e^{-z} capped at e^80).

@@ -98,6 +98,26 @@ struct Act<__nv_bfloat16> {
   }
 };
 
+// silu of two values with paired f32 arithmetic (the prepare's hot loop):
+// e^{-x} as 2^{-x log2(e)} on the hardware's approximate base-2 exponential,
+// capped at e^80 as in silu_f, then x / (1 + e^{-x}) on the refined reciprocal.
+__device__ __forceinline__ float2 silu2(float2 x) {
+  constexpr float kNegLog2e = -1.4426950408889634f;
+  constexpr float kCap = 80.0f * 1.4426950408889634f;
+  const float2 m = __fmul2_rn(x, make_float2(kNegLog2e, kNegLog2e));
+  float e0, e1;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(fminf(m.x, kCap)));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(fminf(m.y, kCap)));
+  const float2 d = __fadd2_rn(make_float2(1.0f, 1.0f), make_float2(e0, e1));
+  float r0, r1;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(d.x));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(d.y));
+  float2 r = make_float2(r0, r1);
+  const float2 t = __ffma2_rn(make_float2(-d.x, -d.y), r, make_float2(1.0f, 1.0f));
+  r = __ffma2_rn(r, t, r);
+  return __fmul2_rn(x, r);
+}
+
 // conv + SiLU of one token's V channels from its window (win[j] = the input
 // W - j tokens back, oldest first) and its own input xt, with channel pairs in
 // paired f32 arithmetic; returns the sum of the squares of y (even and odd
@@ -115,7 +135,7 @@ __device__ __forceinline__ float conv_silu_row(const float (&win)[WV][V], const 
     for (int j = 0; j < W; ++j)
       acc = __ffma2_rn(make_float2(win[j][i], win[j][i + 1]), make_float2(wt[i][j], wt[i + 1][j]), acc);
     acc = __ffma2_rn(make_float2(xt[i], xt[i + 1]), make_float2(wt[i][W], wt[i + 1][W]), acc);
-    const float2 yy = math::silu2(acc);
+    const float2 yy = silu2(acc);
     y[i] = yy.x;
     y[i + 1] = yy.y;
     ss2 = __ffma2_rn(yy, yy, ss2);
