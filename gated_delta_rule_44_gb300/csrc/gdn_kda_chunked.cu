@@ -77,7 +77,7 @@ constexpr uint32_t kBK = 81920;      // Kd hi, Kd lo: same layout (16 KB each)
 constexpr uint32_t kBImg = 114688;   // the images above: copied to the scan's stage as they are
 constexpr uint32_t kBE = 114688;     // prod_u E_u per channel, f32 [128]
 constexpr uint32_t kBlob = 115712;   // 113 KB
-constexpr int kKdaPieces = 4;        // pieces of chunk indices when the chains are few
+constexpr int kPrepWaves = 3;        // pieces: ~3 waves of preparation CTAs beside each scan piece
 
 // bf16 element (t, d) of a [64 tok][128] tile stored as two SW128 boxes of 64 columns.
 __device__ __forceinline__ float tile_at(const uint8_t* tile, int t, int d) {
@@ -92,10 +92,6 @@ __device__ __forceinline__ void ld_bf16x4(const uint8_t* p, float* v) {
   v[1] = __uint_as_float(u.x & 0xffff0000u);
   v[2] = __uint_as_float(u.y << 16);
   v[3] = __uint_as_float(u.y & 0xffff0000u);
-}
-
-__device__ __forceinline__ void st_bf16(uint8_t* p, float x) {
-  *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(x);
 }
 
 // hi + lo bf16 pair of x into two images at the same offset.
@@ -716,9 +712,12 @@ struct KScan {
 };
 static_assert(KScan::V % 1024 == 0, "swizzled tiles are 1024-byte aligned");
 static_assert(KScan::BYTES + 1024 <= 232448, "shared memory per CTA");
-constexpr uint32_t kSD1 = 0;    // TMEM: D1 = [U^T | O^T] (128 columns)
+constexpr uint32_t kSD1 = 0;    // TMEM: D1 = [U^T | O^T] (128 columns; O^T of odd chunks at kSO1)
 constexpr uint32_t kSS = 128;   //       the f32 state S[dv][dk] (128)
 constexpr uint32_t kSU = 256;   //       U^T hi | lo as packed bf16 pairs (32 + 32)
+constexpr uint32_t kSO1 = 320;  //       O^T of odd chunks (64): a chunk's output leaves while
+                                //       the next chunk's D1 runs
+__device__ __forceinline__ uint32_t o_col(int c) { return (c & 1) ? kSO1 : kSD1 + 64; }
 constexpr int kScanThreads = 128;
 
 __global__ void __launch_bounds__(kScanThreads, 1) kda_scan_kernel(
@@ -726,7 +725,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_scan_kernel(
     int j0, int j1) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = aligned_smem(smem_raw);
-  __shared__ uint64_t mbar_ld, mbar_el, mbar_mma;
+  __shared__ uint64_t mbar_ld, mbar_ldb, mbar_el, mbar_mma;
   __shared__ uint32_t tslot;
   __shared__ int s_gc0, s_bad;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -768,10 +767,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_scan_kernel(
     }
   }
   const uint32_t base = smem_u32(sm);
-  const uint32_t mb_ld = smem_u32(&mbar_ld), mb_el = smem_u32(&mbar_el),
-                 mb_mma = smem_u32(&mbar_mma);
+  const uint32_t mb_ld = smem_u32(&mbar_ld), mb_ldb = smem_u32(&mbar_ldb),
+                 mb_el = smem_u32(&mbar_el), mb_mma = smem_u32(&mbar_mma);
   if (tid == 0) {
     mbar_init(mb_ld, 1);
+    mbar_init(mb_ldb, 1);
     mbar_init(mb_el, 1);
     mbar_init(mb_mma, 1);
     fence_mbar_init();
@@ -796,13 +796,62 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_scan_kernel(
   const bool init = cb > 0 || p.has_init == nullptr || __ldg(p.has_init + s) != 0;
   // Copies and MMAs issued but not yet seen complete (thread 0's books, for a
   // clean exit after a wait that gave up).
-  int pend_ld = -1, pend_el = -1, n_mma = 0;
+  int pend_ld = -1, pend_ldb = -1, pend_el = -1, n_mma = 0;
   bool pend_mma = false;
+  // A chunk's stage in two parts: A (Tb, -W^T, Qe and V: read by D1 only) and
+  // B (P and Kd: read by D2 / D3), each on its own mbarrier, so the next
+  // chunk's part A lands while this chunk's state update runs, and part B
+  // after D2 / D3 have read this chunk's.
+  auto load_a = [&](int cc) {
+    const uint8_t* b = blob(cc);
+    mbar_expect_tx(mb_ld, 4 * 16384 + 2 * 8192);
+    bulk_g2s(base + KScan::ST + kBW, b + kBW, 16384, mb_ld);
+    bulk_g2s(base + KScan::ST + kBT, b + kBT, 16384, mb_ld);
+    bulk_g2s(base + KScan::ST + kBQ, b + kBQ, 16384, mb_ld);
+    bulk_g2s(base + KScan::ST + kBQ + 16384, b + kBQ + 16384, 16384, mb_ld);
+    tma_load_3d(base + KScan::V, &tm_v, mb_ld, 0, h, lo + cc * kC);
+    tma_load_3d(base + KScan::V + 8192, &tm_v, mb_ld, 64, h, lo + cc * kC);
+    pend_ld = cc;
+  };
+  auto load_b = [&](int cc) {
+    const uint8_t* b = blob(cc);
+    mbar_expect_tx(mb_ldb, 3 * 16384);
+    bulk_g2s(base + KScan::ST + kBP, b + kBP, 16384, mb_ldb);
+    bulk_g2s(base + KScan::ST + kBK, b + kBK, 16384, mb_ldb);
+    bulk_g2s(base + KScan::ST + kBK + 16384, b + kBK + 16384, 16384, mb_ldb);
+    pend_ldb = cc;
+  };
+  __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + KScan::OST);
+  // Output rows of chunk cc from its O^T columns: 32 tokens at a time through
+  // the staging rows (called by every thread).
+  auto emit_out = [&](int cc) {
+    const int t0c = lo + cc * kC, Lc = min(kC, hi - t0c);
+#pragma unroll 1
+    for (int j0 = 0; j0 < Lc; j0 += 32) {
+      float o[32];
+      tmem_ld32(tmem + o_col(cc) + la + j0, o);
+      tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) ost[e * kD + dv] = __float2bfloat16_rn(o[e]);
+      __syncthreads();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int idx = q * kScanThreads + tid;  // 16-byte vector: token idx / 16
+        const int r = idx >> 4, c16 = idx & 15;
+        if (j0 + r < Lc)
+          *reinterpret_cast<uint4*>(out + ((int64_t)(t0c + j0 + r) * p.Hv + h) * kD + c16 * 8) =
+              *reinterpret_cast<const uint4*>(ost + r * kD + c16 * 8);
+      }
+      __syncthreads();
+    }
+  };
 
   if (tid == 0) {
     mbar_expect_tx(mb_el, 512);
     bulk_g2s(base + KScan::ELB, blob(0) + kBE, 512, mb_el);
     pend_el = 0;
+    load_a(0);
+    load_b(0);
   }
   bool ok = mbar_wait(mb_el, 0, kWaitBudget);
   if (tid == 0 && ok) pend_el = -1;
@@ -837,36 +886,26 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_scan_kernel(
   const uint32_t id_q = idesc_bf16_f32(128, 64, false, false);
   const uint32_t id_d2 = idesc_bf16_f32(128, 128, false, true);
   const uint32_t id_d3 = idesc_bf16_f32(128, 64, false, false);
-  __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + KScan::OST);
 
   for (int c = 0; c < nch && ok; ++c) {
-    const int t0 = lo + c * kC;
-    const int L = min(kC, hi - t0);
     const bool last = c + 1 == nch;
-    if (tid == 0) {
-      fence_after_sync();
-      const uint8_t* b = blob(c);
-      mbar_expect_tx(mb_ld, kBImg + 2 * 8192);
-      for (uint32_t off = 0; off < kBImg; off += 16384)
-        bulk_g2s(base + KScan::ST + off, b + off, 16384, mb_ld);
-      tma_load_3d(base + KScan::V, &tm_v, mb_ld, 0, h, t0);
-      tma_load_3d(base + KScan::V + 8192, &tm_v, mb_ld, 64, h, t0);
-      pend_ld = c;
-      if (!last) {  // prod E of the next chunk, for the state update of this one
-        mbar_expect_tx(mb_el, 512);
-        bulk_g2s(base + KScan::ELB + ((c + 1) & 1) * 512, blob(c + 1) + kBE, 512, mb_el);
-        pend_el = c + 1;
-        // and the next chunk's images on their way into L2 (the stage is single-buffered)
+    if (tid == 0 && !last) {
+      // prod E of the next chunk, for the state update of this one
+      mbar_expect_tx(mb_el, 512);
+      bulk_g2s(base + KScan::ELB + ((c + 1) & 1) * 512, blob(c + 1) + kBE, 512, mb_el);
+      pend_el = c + 1;
+      if (c + 2 < nch)  // the images after the next on their way into L2
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
-                         reinterpret_cast<uint64_t>(blob(c + 1))),
+                         reinterpret_cast<uint64_t>(blob(c + 2))),
                      "r"(kBImg)
                      : "memory");
-      }
     }
-    ok = __syncthreads_and(mbar_wait(mb_ld, c & 1, kWaitBudget));
+    ok = __syncthreads_and(mbar_wait(mb_ld, c & 1, kWaitBudget) &&
+                           mbar_wait(mb_ldb, c & 1, kWaitBudget));
     if (!ok) break;
     if (tid == 0) {
       pend_ld = -1;
+      pend_ldb = -1;
       fence_after_sync();
       // Ut^T = V^T Tb^T into D1[:, 0:64]  (A = V MN-major, M = dv; B = Tb hi, lo)
 #pragma unroll
@@ -886,14 +925,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_scan_kernel(
                                   (kk % 64) * 2,
                               16, 1024),
                    desc_sw128(base + KScan::ST + kBW + (kk / 8) * 1024, 8192, 1024), id_w, true);
-      // D1[:, 64:128] = S Qe^T: S hi Qe hi, S lo Qe hi, S hi Qe lo
+      // O^T = S Qe^T (this chunk's O columns): S hi Qe hi, S lo Qe hi, S hi Qe lo
 #pragma unroll
       for (int pr = 0; pr < 3; ++pr) {
         const uint32_t sa = pr == 1 ? KScan::SL : KScan::SH;
         const uint32_t qo = pr == 2 ? 16384 : 0;
 #pragma unroll
         for (int kk = 0; kk < kD; kk += 16)
-          mma_bf16(tmem + kSD1 + 64,
+          mma_bf16(tmem + o_col(c),
                    desc_sw128(base + sa + (kk / 64) * 16384 + (kk % 64) * 2, 16, 1024),
                    desc_sw128(base + KScan::ST + kBQ + qo + (kk / 64) * 8192 + (kk % 64) * 2, 16,
                               1024),
@@ -902,20 +941,22 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_scan_kernel(
       mma_commit(mb_mma);
       pend_mma = true;
     }
+    if (c > 0) emit_out(c - 1);  // the previous chunk's output, beside D1
     ok = mbar_wait(mb_mma, n_mma & 1, kWaitBudget);
     ++n_mma;
     if (tid == 0 && ok) pend_mma = false;
     ok = __syncthreads_and(ok);  // uniform: tcgen05.ld / st are warp-wide
     if (!ok) break;
     fence_after_sync();
-    // U^T = D1[:, 0:64] as hi + lo pairs into TMEM; D1[:, 64:128] scaled in
+    if (tid == 0 && !last) load_a(c + 1);  // D1 has read Tb, -W^T, Qe and V
+    // U^T = D1[:, 0:64] as hi + lo pairs into TMEM; the O^T columns scaled in
     // place: O^T starts as scale (Qe S^T)^T, onto which P U accumulates.
     {
 #pragma unroll 1
       for (int j0 = 0; j0 < kC; j0 += 32) {
         float u[32], qs[32];
         tmem_ld32(tmem + kSD1 + la + j0, u);
-        tmem_ld32(tmem + kSD1 + 64 + la + j0, qs);
+        tmem_ld32(tmem + o_col(c) + la + j0, qs);
         tmem_ld_wait();
 #pragma unroll
         for (int j1 = 0; j1 < 32; j1 += 16) {
@@ -927,7 +968,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_scan_kernel(
         }
 #pragma unroll
         for (int e = 0; e < 32; ++e) qs[e] *= p.scale;
-        tmem_st32(tmem + kSD1 + 64 + la + j0, qs);
+        tmem_st32(tmem + o_col(c) + la + j0, qs);
       }
       tmem_st_wait();
     }
@@ -953,7 +994,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_scan_kernel(
         const uint32_t po = pr == 1 ? 8192 : 0;
 #pragma unroll
         for (int kk = 0; kk < kC; kk += 16)
-          mma_bf16_ta(tmem + kSD1 + 64, tmem + kSU + ua + kk / 2,
+          mma_bf16_ta(tmem + o_col(c), tmem + kSU + ua + kk / 2,
                       desc_sw128(base + KScan::ST + kBP + po + kk * 2, 16, 1024), id_d3, true);
       }
       mma_commit(mb_mma);
@@ -970,6 +1011,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_scan_kernel(
     ok = __syncthreads_and(ok);
     if (!ok) break;
     fence_after_sync();
+    if (tid == 0 && !last) load_b(c + 1);  // D2 / D3 have read P and Kd
     // S' = S0 diag(prod E) + U^T Kd: its images for the next D1 and S' diag(prod
     // E of the next chunk) back into TMEM; the last chunk's S' goes to the pool.
     const float* eln = elb + ((c + 1) & 1) * 128;
@@ -993,36 +1035,19 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_scan_kernel(
         tmem_st32(tmem + kSS + la + j0, v);
       }
     }
-    // Output rows: 32 tokens at a time through the staging rows.
-#pragma unroll 1
-    for (int j0 = 0; j0 < L; j0 += 32) {
-      float o[32];
-      tmem_ld32(tmem + kSD1 + 64 + la + j0, o);
-      tmem_ld_wait();
-#pragma unroll
-      for (int e = 0; e < 32; ++e) ost[e * kD + dv] = __float2bfloat16_rn(o[e]);
-      __syncthreads();
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int idx = q * kScanThreads + tid;  // 16-byte vector: token idx / 16
-        const int r = idx >> 4, c16 = idx & 15;
-        if (j0 + r < L)
-          *reinterpret_cast<uint4*>(out + ((int64_t)(t0 + j0 + r) * p.Hv + h) * kD + c16 * 8) =
-              *reinterpret_cast<const uint4*>(ost + r * kD + c16 * 8);
-      }
-      __syncthreads();
-    }
     if (!last) tmem_st_wait();
     fence_proxy_async();
     fence_before_sync();
     __syncthreads();
   }
 
+  if (ok) emit_out(nch - 1);
   // teardown: copies and MMAs still in flight (after a wait that gave up) land
   // first, then the TMEM is freed.
   if (!ok && tid == 0) {
     atomicOr(p.status, kStatusTimeout);
     if (pend_ld >= 0) mbar_wait(mb_ld, pend_ld & 1, kWaitBudget);
+    if (pend_ldb >= 0) mbar_wait(mb_ldb, pend_ldb & 1, kWaitBudget);
     if (pend_el >= 0) mbar_wait(mb_el, pend_el & 1, kWaitBudget);
     if (pend_mma) mbar_wait(mb_mma, (n_mma - 1) & 1, kWaitBudget);
   }
@@ -1083,7 +1108,14 @@ cudaError_t launch_kda_chunked(const ChunkedLaunch& c, cudaStream_t s) {
   if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
   const int64_t cmax = (p.T + kC - 1) / kC;
   const bool pieces = 2 * blocks <= sm_count() && cmax >= 16;
-  const int step = pieces ? static_cast<int>((cmax + kKdaPieces - 1) / kKdaPieces) : 0x7fffffff;
+  // A piece's preparation (one CTA per chunk of each sequence and value head,
+  // one per SM) fills about kPrepWaves waves of the SMs the scan leaves free,
+  // and holds at least 8 chunk indices (each piece restarts the scan).
+  const int64_t per_chunk = static_cast<int64_t>(p.N) * p.Hv;
+  const int64_t free_sms = std::max<int64_t>(1, sm_count() - blocks);
+  const int step = pieces ? static_cast<int>(std::min<int64_t>(
+                                cmax, std::max<int64_t>(8, kPrepWaves * free_sms / per_chunk)))
+                          : 0x7fffffff;
   const int n_pieces = pieces ? static_cast<int>((cmax + step - 1) / step) : 1;
   for (int i = 0; i < n_pieces; ++i) {
     const int j0 = pieces ? i * step : 0, j1 = pieces ? j0 + step : 0x7fffffff;
