@@ -547,16 +547,45 @@ __global__ void __launch_bounds__(kThreads) spec_prepare_kernel(const PrepareLau
   const int qk_total = p.Hk * p.Dk;
   const int C = 2 * qk_total + p.Hv * p.Dv;
   const int req = blockIdx.x;
+  const bool gate_block = blockIdx.y == chan_blocks;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cb = blockIdx.y * kThreads * V;
+  const int col = (warp * 32 + lane) * V;  // this thread's first column in the block
+  const int c0 = cb + col;
+  const bool active = !gate_block && c0 < C;
+  // Everything that needs only the request and the channel block is read
+  // before anything waits: cu_seqlens, the slot, the accepted count and the
+  // conv weights; the request's inputs and conv row follow in one more trip.
   const int lo = __ldg(p.cu + req), hi = __ldg(p.cu + req + 1);
-  if (__ldg(p.cu) != 0 || __ldg(p.cu + p.N) != p.T || lo < 0 || hi < lo || hi > p.T ||
-      hi - lo > max_q) {
+  const int cu_first = __ldg(p.cu), cu_last = __ldg(p.cu + p.N);
+  const int slot_in = gate_block ? -1 : __ldg(p.sidx + req);
+  const int accepted = gate_block ? 1 : __ldg(p.num_accepted + req);
+  float wt[V][KW];
+  {
+    static_assert((V * KW) % 4 == 0, "weights as float4");
+    float wf[V * KW];
+    const float4* wsrc = reinterpret_cast<const float4*>(p.w + (int64_t)c0 * KW);
+#pragma unroll
+    for (int q4 = 0; q4 < V * KW / 4; ++q4) {
+      const float4 f = active ? __ldg(wsrc + q4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      wf[4 * q4] = f.x;
+      wf[4 * q4 + 1] = f.y;
+      wf[4 * q4 + 2] = f.z;
+      wf[4 * q4 + 3] = f.w;
+    }
+#pragma unroll
+    for (int e = 0; e < V; ++e)
+#pragma unroll
+      for (int j = 0; j < KW; ++j) wt[e][j] = wf[e * KW + j];
+  }
+  if (cu_first != 0 || cu_last != p.T || lo < 0 || hi < lo || hi > p.T || hi - lo > max_q) {
     if (threadIdx.x == 0) atomicOr(p.status, kStatusBadSeqlens);
     return;
   }
   const int len = hi - lo;
   if (len == 0) return;  // an empty request reads and writes nothing
 
-  if (blockIdx.y == chan_blocks) {  // gates: g, beta per (token, value head)
+  if (gate_block) {  // gates: g, beta per (token, value head)
     const TA* __restrict__ a = static_cast<const TA*>(p.a);
     const TA* __restrict__ b = static_cast<const TA*>(p.b);
     for (int e = threadIdx.x; e < len * p.Hv; e += kThreads) {
@@ -569,23 +598,17 @@ __global__ void __launch_bounds__(kThreads) spec_prepare_kernel(const PrepareLau
     return;
   }
 
-  int slot = __ldg(p.sidx + req);
-  const int accepted = __ldg(p.num_accepted + req);
+  int slot = slot_in;
   if (slot >= p.slots || (slot >= 0 && (accepted < 1 || accepted > max_q))) {
     if (threadIdx.x == 0) atomicOr(p.status, kStatusBadIndex);
     slot = -1;
   }
   const bool live = slot >= 0;  // uniform across the CTA
   const int off = live ? accepted - 1 : 0;
-  const int cb = blockIdx.y * kThreads * V;
   const int nch = min(kThreads * V, C - cb);
   const int n4 = nch * SL / 4;  // nch is a multiple of V >= 4
   float* grow = live ? p.conv_pool + ((int64_t)slot * C + cb) * SL : nullptr;
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int col = (warp * 32 + lane) * V;  // this thread's first column in the block
-  const int c0 = cb + col;
-  const bool active = c0 < C;
   // The first kPre drafts' inputs are requested before the rows, so their
   // latency overlaps the staging.
   constexpr int kPre = 4;
@@ -626,11 +649,6 @@ __global__ void __launch_bounds__(kThreads) spec_prepare_kernel(const PrepareLau
   const int group = p.Dk / V;                        // lanes per key head
   const bool mine = live && active;
 
-  float wt[V][KW];
-#pragma unroll
-  for (int e = 0; e < V; ++e)
-#pragma unroll
-    for (int j = 0; j < KW; ++j) wt[e][j] = active ? __ldg(p.w + (int64_t)(c0 + e) * KW + j) : 0.0f;
   TA* __restrict__ out_ptr;
   int64_t out_stride;
   if (c0 < qk_total) {
