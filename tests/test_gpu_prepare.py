@@ -2,8 +2,8 @@
 
 Small cases span several token tiles and channel blocks, ragged sequence
 lengths (1, 2, 3, K-1, K, 63, 64, 65, ...), padding slots (-1), a mix of
-has_initial_state, conv widths 2..6, f32 and bf16; the five named workloads run
-at full size.  q, k, v, g, beta must match within the parity tolerance (q, k, v with the
+has_initial_state, conv widths 2..6, f32 and bf16, and more than 1024
+sequences; the five named workloads run at full size.  q, k, v, g, beta must match within the parity tolerance (q, k, v with the
 bf16-storage metric of tests/helpers.py when stored in bf16); the conv-tail
 pool holds raw inputs and must match bit for bit.
 """
@@ -39,6 +39,9 @@ CASES = [
     ([9, 300, 2], 4, 8, 128, 128, 4, torch.bfloat16, None, False),
     ([5, 33], 2, 2, 8, 8, 6, torch.float32, None, False),
     ([1] * 37, 2, 4, 256, 64, 4, torch.bfloat16, [0, 36], False),
+    # more than 1024 sequences: the tile's sequence search takes three rounds;
+    # one-token rows around longer sequences, with padding slots
+    ([1] * 1030 + [70, 3, 130] + [1] * 40, 1, 2, 16, 16, 4, torch.bfloat16, [5, 1031], False),
 ]
 
 
