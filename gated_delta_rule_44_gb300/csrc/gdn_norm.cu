@@ -63,6 +63,27 @@ struct Vec<float> {
   }
 };
 
+// math::norm_gate of two values with paired f32 arithmetic: e^{-z} as
+// 2^{-z log2(e)} on the hardware's base-2 exponential (capped at e^80), 1 / (1
+// + e^{-z}) on the approximate reciprocal refined by one Newton-Raphson step;
+// silu multiplies by z.  The same operations, two values an instruction.
+__device__ __forceinline__ float2 norm_gate2(float2 z, bool sigmoid_gate) {
+  constexpr float kNegLog2e = -1.4426950408889634f;
+  constexpr float kCap = 80.0f * 1.4426950408889634f;
+  const float2 m = __fmul2_rn(z, make_float2(kNegLog2e, kNegLog2e));
+  float e0, e1;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(fminf(m.x, kCap)));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(fminf(m.y, kCap)));
+  const float2 d = __fadd2_rn(make_float2(1.0f, 1.0f), make_float2(e0, e1));
+  float r0, r1;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(d.x));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(d.y));
+  float2 r = make_float2(r0, r1);
+  const float2 t = __ffma2_rn(make_float2(-d.x, -d.y), r, make_float2(1.0f, 1.0f));
+  r = __ffma2_rn(r, t, r);
+  return sigmoid_gate ? r : __fmul2_rn(z, r);
+}
+
 template <typename TA, int NV>
 __global__ void __launch_bounds__(kThreads) gated_rmsnorm_kernel(const NormLaunch p, int lpr) {
   constexpr int V = Vec<TA>::kN;
@@ -118,8 +139,13 @@ __global__ void __launch_bounds__(kThreads) gated_rmsnorm_kernel(const NormLaunc
       if (live && vi < nvec) {
         float o[V];
 #pragma unroll
-        for (int e = 0; e < V; ++e)
-          o[e] = x[j][e] * inv * w[j][e] * math::norm_gate(zz[j][e], p.sigmoid_gate);
+        for (int e = 0; e < V; e += 2) {
+          const float2 g = norm_gate2(make_float2(zz[j][e], zz[j][e + 1]), p.sigmoid_gate);
+          const float2 xs = __fmul2_rn(make_float2(x[j][e], x[j][e + 1]), make_float2(inv, inv));
+          const float2 oo = __fmul2_rn(__fmul2_rn(xs, make_float2(w[j][e], w[j][e + 1])), g);
+          o[e] = oo.x;
+          o[e + 1] = oo.y;
+        }
         Vec<TA>::store(out8 + (row * p.dim + static_cast<int64_t>(vi) * V) * es, o);
       }
     }
