@@ -97,7 +97,9 @@ typedef enum gdn_dtype {
 typedef enum gdn_prefill_algo {
   GDN_PREFILL_AUTO = 0,      /* a chunked form when supported (bf16, Dk = Dv = 128), else
                                 recurrent: see gdn_prefill_resolve_algo */
-  GDN_PREFILL_CHUNKED = 1,   /* chunk-64 WY/UT form on tcgen05 tensor cores, two launches that
+  GDN_PREFILL_CHUNKED = 1,   /* chunk-64 WY/UT form on tcgen05 tensor cores, two kernels (every
+                                chunk's preparation, then a scan; with few chains in pieces of
+                                chunk indices chained by programmatic dependent launch) that
                                 hand each chunk over through a caller workspace */
   GDN_PREFILL_RECURRENT = 2, /* token-sequential recurrence on CUDA cores */
   GDN_PREFILL_FUSED = 3      /* the chunk-64 form in one launch, one CTA per (sequence, value
@@ -385,9 +387,10 @@ int gdn_packed_decode(const gdn_packed_decode_args* args, void* stream);
  * aligned.
  * algo (gdn_prefill_algo; see gdn_kda_resolve_algo): RECURRENT runs on CUDA
  * cores, a CTA per (sequence, head, row slice); CHUNKED is the chunk-64 form
- * on tcgen05 tensor cores (bf16, Dk = Dv = 128), two launches that hand each
- * chunk over through a caller workspace of gdn_kda_workspace_bytes() bytes
- * (256-byte aligned); FUSED is not offered for KDA.
+ * on tcgen05 tensor cores (bf16, Dk = Dv = 128), two kernels (as
+ * GDN_PREFILL_CHUNKED, in pieces when the chains are few) that hand each chunk
+ * over through a caller workspace of gdn_kda_workspace_bytes() bytes (256-byte
+ * aligned); FUSED is not offered for KDA.
  * Supported: Dk in {16, 32, 64, 128, 256}; any Dv >= 1 (recurrent).
  * Errors as gdn_prefill_varlen (g: "kda_gated_delta_rule g length N <
  * expected T*Hv*Dk").
