@@ -119,19 +119,21 @@ def test_kda_chunked_full_size(cuda_device):
 
 def test_kda_chunked_pieces_padding_and_fresh_states(cuda_device):
     """Few chains and more than 16 chunks: the chunked form runs in pieces of
-    chunk indices; later pieces resume from the state the previous piece
-    stored (a fresh sequence included), a padded sequence stays untouched."""
-    run([1100, 5, 300, 77], 1, 4, 128, 128, torch.bfloat16, cuda_device, seed=17, algo=CHUNKED,
+    chunk indices (here 64 chains leave 88 SMs, so 8 chunk indices a piece and
+    3 pieces); later pieces resume from the state the previous piece stored (a
+    fresh sequence included), a padded sequence stays untouched."""
+    run([1100, 5, 300, 77], 4, 16, 128, 128, torch.bfloat16, cuda_device, seed=17, algo=CHUNKED,
         sidx=torch.tensor([4, -1, 0, 2], dtype=torch.int32), has_init=[0, 1, 1, 0], slots=6)
 
 
 def test_kda_chunked_pieces_cuda_graph_replay(cuda_device):
-    """The chunked KDA form in pieces (programmatic dependent launches)
-    captured in a CUDA graph: replays match eager calls bit for bit."""
+    """The chunked KDA form in pieces (programmatic dependent launches; 64
+    chains, 3 pieces of 8 chunk indices) captured in a CUDA graph: replays
+    match eager calls bit for bit."""
     dev = cuda_device
     g0 = torch.Generator().manual_seed(18)
     lens = [1100, 300]
-    T, N, Hk, Hv, D = sum(lens), len(lens), 1, 4, 128
+    T, N, Hk, Hv, D = sum(lens), len(lens), 8, 32, 128
     cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=dev)
     q = (torch.randn(T, Hk, D, generator=g0) / np.sqrt(D)).to(torch.bfloat16).to(dev)
     k = (torch.randn(T, Hk, D, generator=g0) / np.sqrt(D)).to(torch.bfloat16).to(dev)
