@@ -925,8 +925,10 @@ int32_t gdn_prefill_resolve_algo(int64_t N, int64_t Hv, int64_t Dk, int64_t Dv, 
 
 size_t gdn_prefill_workspace_bytes(int64_t T, int64_t N, int64_t Hv, int64_t Dk, int64_t Dv,
                                    int32_t act_dtype, int32_t algo) {
-  if (gdn_prefill_resolve_algo(N, Hv, Dk, Dv, act_dtype, algo) != GDN_PREFILL_CHUNKED) return 0;
   if (T <= 0 || N <= 0 || Hv <= 0) return 0;
+  const int32_t resolved = gdn_prefill_resolve_algo(N, Hv, Dk, Dv, act_dtype, algo);
+  if (resolved == GDN_PREFILL_FUSED) return gdn::fused_workspace_bytes(N, Hv);
+  if (resolved != GDN_PREFILL_CHUNKED) return 0;
   return gdn::chunked_workspace_bytes(T, N, Hv, Dk, Dv);
 }
 
@@ -1006,9 +1008,15 @@ int gdn_prefill_varlen(const gdn_prefill_args* a, void* stream) {
     if (!gdn::fused_supported((int)a->Dk, (int)a->Dv, p.bf16))
       return fail(GDN_ERR_UNSUPPORTED,
                   "the fused chunked prefill supports bf16 activations with Dk = Dv = 128");
+    // The workspace is optional here: with gdn_prefill_workspace_bytes() of it
+    // the chains are spread over the SMs when they outnumber them.
+    if (a->workspace != nullptr && (reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0)
+      return fail(GDN_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
     p.status = gdn::status_word();
     if (p.status == nullptr) return fail(GDN_ERR_CUDA, "device status word unavailable");
-    if (int rc = launch_result(gdn::launch_fused(p, st), "gdn_prefill_varlen(fused)")) return rc;
+    if (int rc = launch_result(gdn::launch_fused(p, a->workspace, a->workspace_bytes, st),
+                               "gdn_prefill_varlen(fused)"))
+      return rc;
     if (p.onorm_w == nullptr) return GDN_OK;
     return launch_result(launch_out_norm_pass(p, st), "gdn_prefill_varlen(output norm)");
   }

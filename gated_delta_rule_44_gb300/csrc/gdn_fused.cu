@@ -110,6 +110,126 @@ enum Mb : int {
   kMbPImg, kMbFac, kMbD1, kMbD1Free, kMbUReady, kMbSImg, kMbD2, kMbD3, kMbOFree, kMbEnd, kNumMb
 };
 
+// Chains spread over the SMs when they outnumber them (McNaughton's
+// wrap-around rule for preemptive jobs on identical machines).  The machines
+// are gangs of grp = Hv / Hk CTAs (of a grid of one CTA per SM) and the jobs
+// are the (sequence, key head) pairs: member m of a gang runs value head
+// hk * grp + m of every pair, so the heads that share K and Q run in step and
+// read each tile once from DRAM.  The pairs' chunks, in (sequence, key head)
+// order, are cut into consecutive ranges of C = max(ceil(total / gangs),
+// longest sequence) chunks, one per gang.  A pair cut between gangs g and
+// g + 1 runs its first chunks at the start of gang g + 1's range and the
+// rest at the end of gang g's (in that rule the two parts of a job never
+// overlap in time because C is at least the longest job), so gang g resumes
+// its chains from the states gang g + 1 stored long before and no CTA's start
+// waits for anything (one flag per chain, waited for with a bound; the launch
+// is cooperative, so every CTA is resident).  Two waves of 152 + 104 equal
+// chains become one range of ceil(4 * 16 * 32 / 38) = 54 chunks instead of 64.
+constexpr int kMaxSchedCtas = 1024;
+struct FusedSched {
+  int32_t* seq_chunks;  // [N] chunks of each live sequence (0: padded, invalid or empty)
+  int32_t* prefix;      // [N + 1] exclusive prefix of seq_chunks
+  int4* starts;         // [grid] per CTA: its first (sequence, value head), the chunks of that
+                        // chain the gang before holds, and the CTA's chunk count
+  unsigned* flags;      // [N * Hv] 1 once a chain's state was stored for the CTA that resumes it
+};
+
+// The TMA box at (c0, c1, c2) brought into L2 only (no smem, no mbarrier).
+__device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// One CTA: the chunks of every sequence (padded, invalid and empty ones get
+// none and their errors go to the status word), their prefix, C, each CTA's
+// start (CTAs past the last whole gang get none), and the flags cleared.
+__global__ void __launch_bounds__(1024, 1) fused_schedule_kernel(const RecurLaunch p,
+                                                                 const FusedSched sc, int grid) {
+  __shared__ int s_warp[32];
+  __shared__ int s_carry, s_max;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    s_carry = 0;
+    s_max = 0;
+    if (__ldg(p.cu) != 0 || __ldg(p.cu + p.N) != p.T) atomicOr(p.status, kStatusBadSeqlens);
+  }
+  __syncthreads();
+  for (int b0 = 0; b0 < p.N; b0 += 1024) {
+    const int sq = b0 + tid;
+    int n = 0;
+    if (sq < p.N) {
+      const int lo = __ldg(p.cu + sq), hi = __ldg(p.cu + sq + 1);
+      int slot = p.sidx != nullptr ? __ldg(p.sidx + sq) : sq;
+      const bool bad = lo < 0 || hi <= lo || hi > p.T;
+      if (bad) atomicOr(p.status, kStatusBadSeqlens);
+      if (slot < -1 || slot >= p.slots) {
+        atomicOr(p.status, kStatusBadIndex);
+        slot = -1;
+      }
+      n = (!bad && slot >= 0) ? (hi - lo + kC - 1) / kC : 0;
+      sc.seq_chunks[sq] = n;
+      atomicMax(&s_max, n);
+    }
+    int x = n;  // inclusive scan: the warp, then the warps
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = s_warp[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      s_warp[lane] = w;
+    }
+    __syncthreads();
+    const int incl = s_carry + x + (warp > 0 ? s_warp[warp - 1] : 0);
+    if (sq < p.N) sc.prefix[sq] = incl - n;
+    __syncthreads();
+    if (tid == 1023) s_carry = incl;
+    __syncthreads();
+  }
+  if (tid == 0) sc.prefix[p.N] = s_carry;
+  __syncthreads();
+  const int grp = p.Hv / p.Hk, gangs = grid / grp;
+  const int64_t total = static_cast<int64_t>(s_carry) * p.Hk;
+  const int64_t C = max((total + gangs - 1) / gangs, static_cast<int64_t>(s_max));
+  for (int j = tid; j < grid; j += 1024) {
+    int4 st = make_int4(0, 0, 0, 0);
+    const int g = j / grp, m = j % grp;
+    const int64_t g0 = static_cast<int64_t>(g) * C;
+    if (g < gangs && g0 < total) {  // the sequence holding chunk g0: the last with Hk * prefix <= g0
+      int lo = 0, hi = p.N - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (static_cast<int64_t>(sc.prefix[mid]) * p.Hk <= g0)
+          lo = mid;
+        else
+          hi = mid - 1;
+      }
+      const int n = sc.seq_chunks[lo];
+      const int64_t r = g0 - static_cast<int64_t>(sc.prefix[lo]) * p.Hk;
+      st = make_int4(lo, static_cast<int>(r / n) * grp + m, static_cast<int>(r % n),
+                     static_cast<int>(min(C, total - g0)));
+    }
+    sc.starts[j] = st;
+  }
+  for (int64_t q = tid; q < static_cast<int64_t>(p.N) * p.Hv; q += 1024) sc.flags[q] = 0u;
+}
+
 // Bounded wait that also gives up as soon as another role has given up.
 __device__ __forceinline__ bool wait_mb(uint32_t mb, uint32_t parity, volatile int* abort,
                                         unsigned* status) {
@@ -125,38 +245,107 @@ __device__ __forceinline__ bool wait_mb(uint32_t mb, uint32_t parity, volatile i
   }
 }
 
+// kSpread: the CTA runs the range the schedule gave it, else the one chain
+// (sequence, value head) = blockIdx.x (that instance keeps none of the
+// range's bookkeeping in registers).
+template <bool kSpread>
 __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-    const __grid_constant__ CUtensorMap tm_v, const RecurLaunch p) {
+    const __grid_constant__ CUtensorMap tm_v, const RecurLaunch p, const FusedSched sc) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = aligned_smem(smem_raw);
   __shared__ uint64_t mbs[kNumMb];
   __shared__ uint32_t tslot;
   __shared__ int s_abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.x % p.Hv, s = blockIdx.x / p.Hv;
-  const int hk = h / (p.Hv / p.Hk);
-
-  const int lo = __ldg(p.cu + s), hi = __ldg(p.cu + s + 1);
-  if (lo < 0 || hi <= lo || hi > p.T || __ldg(p.cu) != 0 || __ldg(p.cu + p.N) != p.T) {
-    if (tid == 0) atomicOr(p.status, kStatusBadSeqlens);
-    return;
-  }
-  int slot = p.sidx != nullptr ? __ldg(p.sidx + s) : s;
-  if (slot < -1 || slot >= p.slots) {
-    if (tid == 0) atomicOr(p.status, kStatusBadIndex);
-    slot = -1;
-  }
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-  if (slot < 0) {  // padded sequence: zero outputs, pool untouched
-    for (int idx = tid; idx < (hi - lo) * 16; idx += kThreads) {
-      const int t = lo + idx / 16, q16 = idx % 16;
-      *reinterpret_cast<uint4*>(out + ((int64_t)t * p.Hv + h) * kD + q16 * 8) =
-          make_uint4(0, 0, 0, 0);
+  // This CTA's chunks: cnt of them through the chains of its gang member's
+  // value heads, in (sequence, key head) order, from chain (s0, h0), of which
+  // the gang before holds the last k0 (this CTA runs the first n - k0); a
+  // last chain cut by the range's end runs its last chunks here.
+  int s0, h0, k0, cnt;
+  if constexpr (!kSpread) {
+    h0 = blockIdx.x % p.Hv;
+    s0 = blockIdx.x / p.Hv;
+    k0 = 0;
+    const int lo = __ldg(p.cu + s0), hi = __ldg(p.cu + s0 + 1);
+    if (lo < 0 || hi <= lo || hi > p.T || __ldg(p.cu) != 0 || __ldg(p.cu + p.N) != p.T) {
+      if (tid == 0) atomicOr(p.status, kStatusBadSeqlens);
+      return;
     }
-    return;
+    int slot = p.sidx != nullptr ? __ldg(p.sidx + s0) : s0;
+    if (slot < -1 || slot >= p.slots) {
+      if (tid == 0) atomicOr(p.status, kStatusBadIndex);
+      slot = -1;
+    }
+    if (slot < 0) {  // padded sequence: zero outputs, pool untouched
+      for (int idx = tid; idx < (hi - lo) * 16; idx += kThreads) {
+        const int t = lo + idx / 16, q16 = idx % 16;
+        *reinterpret_cast<uint4*>(out + ((int64_t)t * p.Hv + h0) * kD + q16 * 8) =
+            make_uint4(0, 0, 0, 0);
+      }
+      return;
+    }
+    cnt = (hi - lo + kC - 1) / kC;
+  } else {
+    const int4 st = sc.starts[blockIdx.x];
+    s0 = st.x;
+    h0 = st.y;
+    k0 = st.z;
+    cnt = st.w;
+    // The outputs of padded sequences (no chunks): chain q by CTA q % grid.
+    for (int64_t q = blockIdx.x; q < static_cast<int64_t>(p.N) * p.Hv; q += gridDim.x) {
+      const int sq = static_cast<int>(q / p.Hv), hq = static_cast<int>(q % p.Hv);
+      if (sc.seq_chunks[sq] != 0) continue;
+      const int lo = __ldg(p.cu + sq), hi = __ldg(p.cu + sq + 1);
+      if (lo < 0 || hi <= lo || hi > p.T) continue;  // malformed: reported, nothing written
+      for (int idx = tid; idx < (hi - lo) * 16; idx += kThreads) {
+        const int t = lo + idx / 16, q16 = idx % 16;
+        *reinterpret_cast<uint4*>(out + ((int64_t)t * p.Hv + hq) * kD + q16 * 8) =
+            make_uint4(0, 0, 0, 0);
+      }
+    }
+    if (cnt <= 0) return;
   }
-  const int nch = (hi - lo + kC - 1) / kC;
+  // A role's position in the CTA's chunks: chain (s, h), chunk k of its n
+  // (this CTA runs chunks up to e of it), the sequence's token range
+  // [lo, hi), and the chunks left.
+  struct ChunkIt {
+    int s, h, k, e, n, lo, hi, left;
+  };
+  auto it_start = [&]() {
+    ChunkIt x;
+    x.s = s0;
+    x.h = h0;
+    x.k = 0;
+    x.left = cnt;
+    x.lo = __ldg(p.cu + s0);
+    x.hi = __ldg(p.cu + s0 + 1);
+    x.n = kSpread ? sc.seq_chunks[s0] : cnt;
+    x.e = x.n - k0;
+    return x;
+  };
+  auto it_next = [&](ChunkIt& x) {
+    if constexpr (!kSpread) {
+      ++x.k;
+      return;
+    }
+    if (--x.left <= 0) return;
+    if (++x.k < x.e) return;
+    x.h += p.Hv / p.Hk;  // the gang member's head of the next key head
+    if (x.h >= p.Hv) {
+      x.h -= p.Hv;
+      do {
+        ++x.s;
+      } while (sc.seq_chunks[x.s] == 0);
+      x.lo = __ldg(p.cu + x.s);
+      x.hi = __ldg(p.cu + x.s + 1);
+      x.n = sc.seq_chunks[x.s];
+    }
+    x.e = x.n;
+    x.k = x.n - min(x.n, x.left);  // cut by the range's end: its last chunks
+  };
+  const int nch = cnt;
   const uint32_t base = smem_u32(sm);
   auto MB = [&](int i) { return smem_u32(&mbs[i]); };
   volatile int* abort = &s_abort;
@@ -177,36 +366,63 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
     // ---------------------------------------------------------------- loader
     if (lane == 0) {
       int last_kq[2] = {-1, -1}, n_v = 0;
-      auto load_kq = [&](int c) {
+      ChunkIt ikq = it_start(), iv = it_start();  // the chunks of the K/Q and of the V loads
+      const int grp = p.Hv / p.Hk;
+      auto load_kq = [&](int c) {  // chunks in order
         const uint32_t st = base + FusedSmem::KQ + (c & 1) * FusedSmem::kStage;
         const uint32_t mb = MB(kMbKq0 + (c & 1));
-        const int t0 = lo + c * kC;
+        const int t0 = ikq.lo + ikq.k * kC, hk = ikq.h / grp;
         mbar_expect_tx(mb, 4 * 8192);
         tma_load_3d(st + 0, &tm_k, mb, 0, hk, t0);
         tma_load_3d(st + 8192, &tm_q, mb, 0, hk, t0);
         tma_load_3d(st + 16384, &tm_k, mb, 64, hk, t0);
         tma_load_3d(st + 24576, &tm_q, mb, 64, hk, t0);
         last_kq[c & 1] = c;
+        it_next(ikq);
       };
-      auto load_v = [&](int c) {
+      auto load_v = [&](int c) {  // chunks in order
         const uint32_t mb = MB(kMbV);
-        const int t0 = lo + c * kC;
+        const int t0 = iv.lo + iv.k * kC;
         mbar_expect_tx(mb, 2 * 8192);
-        tma_load_3d(base + FusedSmem::WV, &tm_v, mb, 0, h, t0);
-        tma_load_3d(base + FusedSmem::WV + 8192, &tm_v, mb, 64, h, t0);
+        tma_load_3d(base + FusedSmem::WV, &tm_v, mb, 0, iv.h, t0);
+        tma_load_3d(base + FusedSmem::WV + 8192, &tm_v, mb, 64, iv.h, t0);
         n_v = c + 1;
+        it_next(iv);
+      };
+      // K / Q two chunks and V one chunk beyond the loads in flight go to L2
+      // early: heads that share K / Q do not run in step, and V is read once.
+      auto prefetch = [&](ChunkIt x, int ahead, bool kq) {
+        for (int i = 0; i < ahead; ++i) it_next(x);
+        if (x.k >= x.n) return;
+        const int t0 = x.lo + x.k * kC;
+        if (kq) {
+          const int hk = x.h / grp;
+          tma_prefetch_3d(&tm_k, 0, hk, t0);
+          tma_prefetch_3d(&tm_q, 0, hk, t0);
+          tma_prefetch_3d(&tm_k, 64, hk, t0);
+          tma_prefetch_3d(&tm_q, 64, hk, t0);
+        } else {
+          tma_prefetch_3d(&tm_v, 0, x.h, t0);
+          tma_prefetch_3d(&tm_v, 64, x.h, t0);
+        }
       };
       load_kq(0);
       if (nch > 1) load_kq(1);
       load_v(0);
+      prefetch(ikq, 0, true);
+      prefetch(ikq, 1, true);
+      prefetch(iv, 0, false);
+      prefetch(iv, 1, false);
       for (int c = 1; c < nch; ++c) {
         // V(c) replaces W^T(c - 1) once D1(c - 1) has read it.
         if (!wait_mb(MB(kMbD1), (c - 1) & 1, abort, p.status)) break;
         load_v(c);
+        if (c + 2 < nch) prefetch(iv, 1, false);
         if (c + 1 < nch) {  // stage (c + 1) % 2 is free once D2(c - 1) has read K(c - 1)
           if (!wait_mb(MB(kMbKqFree0 + ((c + 1) & 1)), ((c - 1) >> 1) & 1, abort, p.status))
             break;
           load_kq(c + 1);
+          if (c + 3 < nch) prefetch(ikq, 1, true);
         }
       }
       __syncwarp(1u);
@@ -350,16 +566,18 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
     constexpr int SY = FusedSmem::kYStride;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     float g_next = 0.0f, b_next = 0.0f;
-    auto load_gates = [&](int c) {  // ptid < 64
-      const int t0 = lo + c * kC, L = min(kC, hi - t0);
+    ChunkIt igt = it_start();
+    auto load_gates = [&]() {  // ptid < 64; chunks in order
+      const int t0 = igt.lo + igt.k * kC, L = min(kC, igt.hi - t0);
       if (ptid < L) {
-        g_next = __ldg(p.g + (int64_t)(t0 + ptid) * p.Hv + h);
-        b_next = __ldg(p.beta + (int64_t)(t0 + ptid) * p.Hv + h);
+        g_next = __ldg(p.g + (int64_t)(t0 + ptid) * p.Hv + igt.h);
+        b_next = __ldg(p.beta + (int64_t)(t0 + ptid) * p.Hv + igt.h);
       } else {
         g_next = b_next = 0.0f;
       }
+      it_next(igt);
     };
-    if (ptid < 64) load_gates(0);
+    if (ptid < 64) load_gates();
     float pv[32];  // this thread's P values (P-row warps) until the images go out
     const int i = (quad & 1) * 32 + lane;
     for (int c = 0; c < nch; ++c) {
@@ -417,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
       }
       named_bar(kBarPrep, kPrepThreads);
       if (ptid == 0) mbar_arrive(MB(kMbFac));
-      if (ptid < 64 && c + 1 < nch) load_gates(c + 1);  // consumed next chunk
+      if (ptid < 64 && c + 1 < nch) load_gates();  // chunk c + 1, consumed next chunk
       ok = wait_mb(MB(kMbG), c & 1, abort, p.status) && ok;
       fence_after_sync();
       // Lanes 0..63 of G hold K K^T -> A (f32, shared); lanes 64..127 hold
@@ -610,42 +828,91 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
     const int dv = quad * 32 + lane;
     const bool lead = warp == 10 && lane == 0;
     const uint32_t la = static_cast<uint32_t>(quad * 32) << 16;
-    float* prow = p.pool + (((int64_t)slot * p.Hv + h) * kD + dv) * kD;
-    const bool init = p.has_init == nullptr || __ldg(p.has_init + s) != 0;
-    bool ok = wait_mb(MB(kMbFac), 0, abort, p.status);
-    {
-      const float eL = fac[128];
-      for (int j = 0; j < kD; j += 16) {
-        float v[16];
+    ChunkIt it = it_start();  // the chain and chunk this role is on
+    // Row dv of the state of chain (sequence sq, value head hq) in the pool.
+    auto chain_row = [&](int sq, int hq) {
+      const int slot = p.sidx != nullptr ? __ldg(p.sidx + sq) : sq;
+      return p.pool + (((int64_t)slot * p.Hv + hq) * kD + dv) * kD;
+    };
+    // A chain's initial state into the S images and, times e^{gam_L} of its
+    // first chunk here, into TMEM.  A chain that starts mid-way here resumes
+    // from the state the CTA after stored (its flag waited for first).
+    auto init_chain = [&](const ChunkIt& x, float eL, bool okr) {
+      bool init = p.has_init == nullptr || __ldg(p.has_init + x.s) != 0;
+      if (kSpread && x.k > 0) {
+        if (lead) {
+          const unsigned* flag = sc.flags + (int64_t)x.s * p.Hv + x.h;
+          const long long t0 = clock64();
+          while (ld_acquire_u32(flag) == 0u) {
+            if (*abort) {
+              okr = false;
+              break;
+            }
+            if (clock64() - t0 > kWaitBudget) {
+              if (atomicExch(const_cast<int*>(abort), 1) == 0) atomicOr(p.status, kStatusTimeout);
+              okr = false;
+              break;
+            }
+          }
+          __threadfence();
+        }
+        okr = named_bar_and(kBarScan, kScanThreads, okr);
+        init = true;
+      }
+      const float* prow = chain_row(x.s, x.h);
+      constexpr int kB = kSpread ? 32 : 16;  // loads in flight per thread (mid-range switches)
+      for (int j = 0; j < kD; j += kB) {
+        float v[kB];
 #pragma unroll
-        for (int e = 0; e < 16; e += 4) {
+        for (int e = 0; e < kB; e += 4) {
           float4 f = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-          if (init) f = *reinterpret_cast<const float4*>(prow + j + e);
+          if (init && okr) f = __ldcg(reinterpret_cast<const float4*>(prow + j + e));
           v[e] = f.x;
           v[e + 1] = f.y;
           v[e + 2] = f.z;
           v[e + 3] = f.w;
         }
 #pragma unroll
-        for (int e = 0; e < 16; e += 8) {
+        for (int e = 0; e < kB; e += 8) {
           const uint32_t off = swz128_offset(dv, j + e, 16384);
           st_split8(sm + FusedSmem::SH + off, sm + FusedSmem::SL + off, v + e);
         }
 #pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] *= eL;
-        tmem_st16(tmem + kTS + la + j, v);
+        for (int e = 0; e < kB; ++e) v[e] *= eL;
+        if constexpr (kB == 32)
+          tmem_st32(tmem + kTS + la + j, v);
+        else
+          tmem_st16(tmem + kTS + la + j, v);
       }
-      tmem_st_wait();
-      fence_proxy_async();
-      fence_before_sync();
-    }
+      return okr;
+    };
+    float* const prow0 = chain_row(s0, h0);  // the one chain's row without a schedule
+    bool ok = wait_mb(MB(kMbFac), 0, abort, p.status);
+    ok = init_chain(it, fac[128], ok);
+    tmem_st_wait();
+    fence_proxy_async();
+    fence_before_sync();
     ok = named_bar_and(kBarScan, kScanThreads, ok);
     if (lead) mbar_arrive(MB(kMbSImg));
     // Per chunk: the W^T image (D1 waits), U (D2 and D3 wait), the state update
     // (the next D1 waits), the output rows (the next D1's Q half waits).
     for (int c = 0; c < nch && ok; ++c) {
-      const int t0 = lo + c * kC;
-      const int L = min(kC, hi - t0);
+      const int t0 = it.lo + it.k * kC;
+      const int L = min(kC, it.hi - t0);
+      if (kSpread && lead && it.k + 1 == it.e && c + 1 < nch) {
+        // The next chain's state into L2 a chunk before it is read (a resumed
+        // chain's may still be in flight: L2 keeps the line coherent).
+        ChunkIt nx = it;
+        it_next(nx);
+        if (nx.k > 0 || p.has_init == nullptr || __ldg(p.has_init + nx.s) != 0) {
+          const float* row0 = chain_row(nx.s, nx.h) - (int64_t)dv * kD;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(row0 + q * 4096),
+                         "r"(16384)
+                         : "memory");
+        }
+      }
       const float* F = fac + (c & 1) * FusedSmem::kFac;
       // W^T (TMEM lanes = dk, 64 token columns) -> the -W^T image, the MN-major
       // B operand of this chunk's D1 (V, which shared the space, is consumed).
@@ -708,22 +975,25 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
       }
       if (!ok) break;
       // S' = e^{gam_L} S + dS (in TMEM): its images for D1 of the next chunk,
-      // then S' e^{gam_L'} back (the next dS accumulates onto it); the last
-      // chunk's S' goes to the pool.
+      // then S' e^{gam_L'} back (the next dS accumulates onto it).  At the
+      // chain's last chunk here S' goes to the pool instead (with its flag when
+      // another CTA resumes the chain), and the next chain's state comes in.
       ok = wait_mb(MB(kMbD2), c & 1, abort, p.status) && ok;
       const bool last = c + 1 == nch;
+      const bool chain_end = last || (kSpread && it.k + 1 == it.e);
       float eLn = 0.0f;
       if (!last) {
         ok = wait_mb(MB(kMbFac), (c + 1) & 1, abort, p.status) && ok;
         eLn = fac[((c + 1) & 1) * FusedSmem::kFac + 128];
       }
       fence_after_sync();
+      float* prow = kSpread ? chain_row(it.s, it.h) : prow0;
 #pragma unroll 1
       for (int j0 = 0; j0 < kD; j0 += 32) {
         float v[32];
         tmem_ld32(tmem + kTS + la + j0, v);
         tmem_ld_wait();
-        if (last) {
+        if (chain_end) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             *reinterpret_cast<float4*>(prow + j0 + e) =
@@ -738,6 +1008,18 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
           for (int e = 0; e < 32; ++e) v[e] *= eLn;
           tmem_st32(tmem + kTS + la + j0, v);
         }
+      }
+      if (kSpread && chain_end && it.e < it.n) {  // another CTA resumes this chain: its flag
+        named_bar(kBarScan, kScanThreads);  // every row stored; the lead's fence covers them
+        if (lead) {
+          __threadfence();
+          atomicExch(sc.flags + (int64_t)it.s * p.Hv + it.h, 1u);
+        }
+      }
+      if (kSpread && chain_end && !last) {  // the next chain comes in (mid-way if cut by the range's end)
+        ChunkIt nx = it;
+        it_next(nx);
+        ok = init_chain(nx, eLn, ok);
       }
       if (!last) {
         tmem_st_wait();
@@ -768,7 +1050,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int r = (q * kScanThreads + stid) >> 4;  // the vector's token row
-            __nv_bfloat16* dst = out + ((int64_t)(t0 + j0 + r) * p.Hv + h) * kD + c16 * 8;
+            __nv_bfloat16* dst = out + ((int64_t)(t0 + j0 + r) * p.Hv + it.h) * kD + c16 * 8;
             if (j0 + r < L) {
               *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(ost + r * kD + c16 * 8);
             }
@@ -780,6 +1062,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
       ok = named_bar_and(kBarScan, kScanThreads, ok);
       if (lead) mbar_arrive(MB(kMbOFree));
       if (!ok) break;
+      it_next(it);
     }
   }
 
@@ -801,7 +1084,31 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
 
 bool fused_supported(int Dk, int Dv, bool bf16) { return bf16 && Dk == kD && Dv == kD; }
 
-cudaError_t launch_fused(const RecurLaunch& p, cudaStream_t s) {
+namespace {
+// Workspace of the schedule: seq_chunks [N], prefix [N + 1], starts
+// [kMaxSchedCtas], flags [N * Hv], each 256-byte aligned.
+constexpr size_t ws_align(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+struct SchedLayout {
+  size_t chunks, prefix, starts, flags, bytes;
+};
+SchedLayout sched_layout(int64_t N, int64_t Hv) {
+  SchedLayout l{};
+  l.chunks = 0;
+  l.prefix = ws_align(l.chunks + 4 * static_cast<size_t>(N));
+  l.starts = ws_align(l.prefix + 4 * static_cast<size_t>(N + 1));
+  l.flags = ws_align(l.starts + 16 * static_cast<size_t>(kMaxSchedCtas));
+  l.bytes = ws_align(l.flags + 4 * static_cast<size_t>(N * Hv));
+  return l;
+}
+}  // namespace
+
+size_t fused_workspace_bytes(int64_t N, int64_t Hv) {
+  if (N <= 0 || Hv <= 0) return 0;
+  return sched_layout(N, Hv).bytes;
+}
+
+cudaError_t launch_fused(const RecurLaunch& p, void* workspace, size_t workspace_bytes,
+                         cudaStream_t s) {
   CUtensorMap tq, tk, tv;
   if (!make_map(&tq, p.q, p.T, p.Hk) || !make_map(&tk, p.k, p.T, p.Hk) ||
       !make_map(&tv, p.v, p.T, p.Hv))
@@ -809,15 +1116,48 @@ cudaError_t launch_fused(const RecurLaunch& p, cudaStream_t s) {
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(fused_prefill_kernel,
+    attr_err = cudaFuncSetAttribute(fused_prefill_kernel<false>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     FusedSmem::BYTES + 1024);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(fused_prefill_kernel<true>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      FusedSmem::BYTES + 1024);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t blocks = static_cast<int64_t>(p.N) * p.Hv;
   if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  fused_prefill_kernel<<<static_cast<unsigned>(blocks), kThreads, FusedSmem::BYTES + 1024, s>>>(
-      tq, tk, tv, p);
+  const int sms = sm_count();
+  const SchedLayout l = sched_layout(p.N, p.Hv);
+  FusedSched sc{};
+  if (workspace != nullptr && workspace_bytes >= l.bytes && blocks > sms && sms <= kMaxSchedCtas &&
+      p.Hv / p.Hk <= sms) {
+    // More chains than SMs: one CTA per SM over the wrap-around schedule.
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    sc.seq_chunks = reinterpret_cast<int32_t*>(ws + l.chunks);
+    sc.prefix = reinterpret_cast<int32_t*>(ws + l.prefix);
+    sc.starts = reinterpret_cast<int4*>(ws + l.starts);
+    sc.flags = reinterpret_cast<unsigned*>(ws + l.flags);
+    fused_schedule_kernel<<<1, 1024, 0, s>>>(p, sc, sms);
+    note_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(sms));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = FusedSmem::BYTES + 1024;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // every CTA resident: the flag waits end
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, fused_prefill_kernel<true>, tq, tk, tv, p, sc);
+    note_launch();
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
+  fused_prefill_kernel<false><<<static_cast<unsigned>(blocks), kThreads, FusedSmem::BYTES + 1024, s>>>(
+      tq, tk, tv, p, sc);
   note_launch();
   return cudaGetLastError();
 }

@@ -143,9 +143,14 @@ bool kda_chunked_supported(int Dk, int Dv, bool bf16);
 size_t kda_chunked_workspace_bytes(int64_t T, int64_t N, int64_t Hv, int64_t Dk, int64_t Dv);
 cudaError_t launch_kda_chunked(const ChunkedLaunch& c, cudaStream_t s);
 
-// The same chunked form in one persistent launch (no workspace).
+// The same chunked form in one launch of one CTA per (sequence, value head);
+// with a workspace of fused_workspace_bytes() and more chains than SMs, one
+// CTA per SM over a wrap-around schedule of the chains' chunks (a small
+// schedule launch first).
 bool fused_supported(int Dk, int Dv, bool bf16);
-cudaError_t launch_fused(const RecurLaunch& p, cudaStream_t s);
+size_t fused_workspace_bytes(int64_t N, int64_t Hv);
+cudaError_t launch_fused(const RecurLaunch& p, void* workspace, size_t workspace_bytes,
+                         cudaStream_t s);
 
 // Gated RMSNorm of the recurrence output.
 struct NormLaunch {

@@ -102,9 +102,11 @@ typedef enum gdn_prefill_algo {
                                 chunk indices chained by programmatic dependent launch) that
                                 hand each chunk over through a caller workspace */
   GDN_PREFILL_RECURRENT = 2, /* token-sequential recurrence on CUDA cores */
-  GDN_PREFILL_FUSED = 3      /* the chunk-64 form in one launch, one CTA per (sequence, value
-                                head) preparing the next chunk while it carries the state;
-                                needs no workspace */
+  GDN_PREFILL_FUSED = 3      /* the chunk-64 form in one launch, a CTA preparing the next
+                                chunk while it carries the state: one CTA per (sequence,
+                                value head), or, given the optional workspace and more
+                                chains than SMs, one CTA per SM over even ranges of the
+                                chains' chunks (a short kernel computes the ranges first) */
 } gdn_prefill_algo;
 
 /* ---------------------------------------------------------------------------
@@ -248,7 +250,8 @@ int gdn_decode(const gdn_decode_args* args, void* stream);
  * The chunked algorithm splits each sequence into chunks of 64 tokens (the
  * last may be partial; chunks never cross sequences) and needs
  * gdn_prefill_workspace_bytes() bytes of 256-byte aligned device scratch in
- * `workspace`; the recurrent algorithm needs none.
+ * `workspace`; the fused algorithm takes the same (a few KB) optionally and
+ * runs one CTA per chain without it; the recurrent algorithm needs none.
  * ------------------------------------------------------------------------- */
 typedef struct gdn_prefill_args {
   int64_t T, N;
@@ -638,7 +641,8 @@ typedef struct gdn_mixed_meta {
 int gdn_validate_mixed(const gdn_mixed_meta* meta);
 
 /* Scratch bytes gdn_prefill_varlen needs for these sizes and algorithm (0 for
- * the recurrent and fused algorithms).  With GDN_PREFILL_AUTO it depends on
+ * the recurrent algorithm; for the fused one the bytes of its optional
+ * workspace).  With GDN_PREFILL_AUTO it depends on
  * the current device too (gdn_prefill_resolve_algo). */
 size_t gdn_prefill_workspace_bytes(int64_t T, int64_t N, int64_t Hv, int64_t Dk, int64_t Dv,
                                    int32_t act_dtype, int32_t algo);

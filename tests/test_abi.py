@@ -136,8 +136,15 @@ def test_prefill_workspace_rules():
     assert B.gdn_prefill_resolve_algo(1, 32, 128, 128, B.GDN_DTYPE_BF16,
                                       B.GDN_PREFILL_FUSED) == B.GDN_PREFILL_FUSED
     assert B.gdn_prefill_workspace_bytes(100, 2, 4, 32, 32, B.GDN_DTYPE_F32) == 0
-    # the fused form needs no workspace; an unknown algorithm is rejected
-    assert B.gdn_prefill_workspace_bytes(8192, 4, 64, 128, 128, B.GDN_DTYPE_BF16) == 0
+    # the fused form's optional workspace: per-sequence chunk counts and
+    # prefix, 1024 per-CTA starts, a flag per chain, each 256-byte aligned;
+    # a misaligned one is rejected; an unknown algorithm is rejected
+    a256 = lambda x: (x + 255) // 256 * 256
+    assert B.gdn_prefill_workspace_bytes(8192, 4, 64, 128, 128, B.GDN_DTYPE_BF16) == \
+        a256(4 * 4) + a256(4 * 5) + 16 * 1024 + a256(4 * 4 * 64)
+    rc, msg = call_prefill(prefill_args(algo=B.GDN_PREFILL_FUSED, workspace=FAKE + 16,
+                                        workspace_bytes=1 << 20))
+    assert rc == B.GDN_ERR_INVALID_ARGUMENT and "256-byte aligned" in msg
     assert B.gdn_prefill_workspace_bytes(4096, 1, 32, 128, 128, B.GDN_DTYPE_BF16) > 0
     assert call_prefill(prefill_args(algo=4))[0] == B.GDN_ERR_INVALID_ARGUMENT
     rc, msg = call_prefill(prefill_args(Dk=64, Dv=64, algo=B.GDN_PREFILL_FUSED))

@@ -142,3 +142,46 @@ def test_varlen_8_full_size(algo, weak, cuda_device):
         pytest.skip("algorithm not built for these dims")
     e = run_prefill(w, cuda_device, algo)
     print(f"varlen_8 algo={algo} weak={weak}: out err {e[0]:.2e}, state err {e[1]:.2e}")
+
+
+SPREAD = [
+    # more chains than SMs, so the fused form spreads the chains' chunks over
+    # one CTA per SM (chains cut between two CTAs resume from the state the
+    # other stored): decodes, ragged new prefills, padding
+    ([1] * 10 + [int(x) for x in np.random.default_rng(5).integers(2, 400, 35)], [3, 20]),
+    # one chain longer than the even share: every CTA's range is that chain's length
+    ([3000] + [int(x) for x in np.random.default_rng(6).integers(1, 200, 47)], [9]),
+]
+
+
+@pytest.mark.parametrize("case", range(len(SPREAD)))
+def test_fused_spread_over_sms(case, cuda_device):
+    """The fused form with its workspace (chunks spread over the SMs) against
+    the oracle, and bit for bit against the same call without the workspace
+    (one CTA per chain): a chain's state crosses CTAs through the pool in f32,
+    so the arithmetic does not change."""
+    seqlens, padded = SPREAD[case]
+    w = W.make_workload("p", 340 + case, seqlens, 2, 4, 128, 128, act_dtype=torch.bfloat16,
+                        slots=len(seqlens) + 2, padded=padded, prefill_new=True, n_decode=10,
+                        weak_decay=True, state_std=0.3)
+    assert w.N * w.Hv > torch.cuda.get_device_properties(cuda_device).multi_processor_count
+    run_prefill(w, cuda_device, B.GDN_PREFILL_FUSED)
+    ref_prep, _ = H.oracle_prepare(w, norm=True)
+    dev = cuda_device
+    args = [torch.from_numpy(ref_prep[k]).to(w.act_dtype).to(dev) for k in ("q", "k", "v")]
+    args += [torch.from_numpy(ref_prep[k]).to(dev) for k in ("g", "beta")]
+    ws_bytes = B.gdn_prefill_workspace_bytes(w.T, w.N, w.Hv, w.Dk, w.Dv, B.GDN_DTYPE_BF16,
+                                             B.GDN_PREFILL_FUSED)
+    assert ws_bytes > 0
+    results = []
+    for ws in (torch.empty(ws_bytes, dtype=torch.uint8, device=dev), None):
+        pool = w.state_pool.to(dev)
+        out = torch.full((w.T, w.Hv, w.Dv), float("nan"), dtype=w.act_dtype, device=dev)
+        B.gdn_prefill_varlen(*args, pool, w.cu_seqlens.to(dev), out,
+                             state_indices=w.state_indices.to(dev),
+                             has_initial_state=w.has_initial_state.to(dev),
+                             algo=B.GDN_PREFILL_FUSED, workspace=ws)
+        B.gdn_read_device_status()
+        results.append((out, pool))
+    assert torch.equal(results[0][0], results[1][0])
+    assert torch.equal(results[0][1], results[1][1])
