@@ -294,7 +294,8 @@ int gdn_prefill_varlen(const gdn_prefill_args* args, void* stream);
  * serving loop that must never call cudaMalloc (it can synchronise the device
  * and can fail under memory pressure).  This call takes the same arguments
  * except that workspace / workspace_bytes are ignored: it uses a fixed 64 MiB
- * scratch array that is part of the library's device image, and calls no
+ * scratch array that is part of the library's device image (as the chunked
+ * form's workspace, or as the fused form's optional one), and calls no
  * cudaMalloc, cudaFree or other allocating routine.
  *   - Limit: sizes whose gdn_prefill_workspace_bytes() exceeds 64 MiB
  *     (67108864 bytes) are rejected with GDN_ERR_INVALID_ARGUMENT before

@@ -146,11 +146,15 @@ def test_varlen_8_full_size(algo, weak, cuda_device):
 
 SPREAD = [
     # more chains than SMs, so the fused form spreads the chains' chunks over
-    # one CTA per SM (chains cut between two CTAs resume from the state the
-    # other stored): decodes, ragged new prefills, padding
-    ([1] * 10 + [int(x) for x in np.random.default_rng(5).integers(2, 400, 35)], [3, 20]),
-    # one chain longer than the even share: every CTA's range is that chain's length
-    ([3000] + [int(x) for x in np.random.default_rng(6).integers(1, 200, 47)], [9]),
+    # gangs of Hv / Hk CTAs, one CTA per SM (chains cut between two gangs
+    # resume from the state the other stored): decodes, ragged new prefills,
+    # padding
+    ([1] * 10 + [int(x) for x in np.random.default_rng(5).integers(2, 400, 35)], [3, 20], 2, 4),
+    # one sequence longer than the even share: every gang's range is its length
+    ([3000] + [int(x) for x in np.random.default_rng(6).integers(1, 200, 47)], [9], 2, 4),
+    # gangs of 3 (152 SMs leave 2 CTAs without a range) and of 8
+    ([1] * 10 + [int(x) for x in np.random.default_rng(7).integers(2, 700, 20)], [12], 2, 6),
+    ([1] * 10 + [int(x) for x in np.random.default_rng(8).integers(2, 900, 10)], [], 1, 8),
 ]
 
 
@@ -160,8 +164,8 @@ def test_fused_spread_over_sms(case, cuda_device):
     the oracle, and bit for bit against the same call without the workspace
     (one CTA per chain): a chain's state crosses CTAs through the pool in f32,
     so the arithmetic does not change."""
-    seqlens, padded = SPREAD[case]
-    w = W.make_workload("p", 340 + case, seqlens, 2, 4, 128, 128, act_dtype=torch.bfloat16,
+    seqlens, padded, Hk, Hv = SPREAD[case]
+    w = W.make_workload("p", 340 + case, seqlens, Hk, Hv, 128, 128, act_dtype=torch.bfloat16,
                         slots=len(seqlens) + 2, padded=padded, prefill_new=True, n_decode=10,
                         weak_decay=True, state_std=0.3)
     assert w.N * w.Hv > torch.cuda.get_device_properties(cuda_device).multi_processor_count
@@ -185,3 +189,40 @@ def test_fused_spread_over_sms(case, cuda_device):
         results.append((out, pool))
     assert torch.equal(results[0][0], results[1][0])
     assert torch.equal(results[0][1], results[1][1])
+
+
+def test_fused_spread_cuda_graph_replay(cuda_device):
+    """The spread fused form (its schedule kernel, then a cooperative launch)
+    captured in a CUDA graph: replays match eager calls bit for bit."""
+    dev = cuda_device
+    w = W.make_workload("p", 350, [int(x) for x in np.random.default_rng(9).integers(1, 300, 45)],
+                        2, 4, 128, 128, act_dtype=torch.bfloat16, weak_decay=True, state_std=0.3)
+    assert w.N * w.Hv > torch.cuda.get_device_properties(dev).multi_processor_count
+    ref_prep, _ = H.oracle_prepare(w, norm=True)
+    args = [torch.from_numpy(ref_prep[k]).to(w.act_dtype).to(dev) for k in ("q", "k", "v")]
+    args += [torch.from_numpy(ref_prep[k]).to(dev) for k in ("g", "beta")]
+    ws = torch.empty(B.gdn_prefill_workspace_bytes(w.T, w.N, w.Hv, w.Dk, w.Dv, B.GDN_DTYPE_BF16,
+                                                   B.GDN_PREFILL_FUSED),
+                     dtype=torch.uint8, device=dev)
+    cu, sidx, hi = (x.to(dev) for x in (w.cu_seqlens, w.state_indices, w.has_initial_state))
+    pool0 = w.state_pool.to(dev)
+    pe, pg = pool0.clone(), pool0.clone()
+    oe = torch.empty((w.T, w.Hv, w.Dv), dtype=w.act_dtype, device=dev)
+    og = torch.empty_like(oe)
+
+    def call(pool, out, stream=None):
+        B.gdn_prefill_varlen(*args, pool, cu, out, state_indices=sidx, has_initial_state=hi,
+                             algo=B.GDN_PREFILL_FUSED, workspace=ws, stream=stream)
+
+    call(pool0.clone(), torch.empty_like(oe))  # settles the host-side resources
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call(pg, og, stream=torch.cuda.current_stream())
+    for _ in range(3):
+        call(pe, oe)
+        graph.replay()
+        torch.cuda.synchronize()
+        B.gdn_read_device_status()
+        assert torch.equal(oe, og)
+        assert torch.equal(pe, pg)

@@ -34,12 +34,12 @@ def _noalloc():
     return fn
 
 
-def _args(q, k, v, g, beta, state, cu, sidx, hinit, out):
+def _args(q, k, v, g, beta, state, cu, sidx, hinit, out, algo=B.GDN_PREFILL_CHUNKED):
     T, Hk, Dk = q.shape
     _, Hv, Dv = v.shape
     return B.gdn_prefill_args(
         T=T, N=cu.numel() - 1, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, act_dtype=B.GDN_DTYPE_BF16,
-        use_qk_l2norm=0, scale=-1.0, algo=B.GDN_PREFILL_CHUNKED, q=q.data_ptr(), q_len=q.numel(),
+        use_qk_l2norm=0, scale=-1.0, algo=algo, q=q.data_ptr(), q_len=q.numel(),
         k=k.data_ptr(), k_len=k.numel(), v=v.data_ptr(), v_len=v.numel(), g=g.data_ptr(),
         g_len=g.numel(), beta=beta.data_ptr(), beta_len=beta.numel(), state=state.data_ptr(),
         state_slots=state.shape[0], state_len=state.numel(), cu_seqlens=cu.data_ptr(),
@@ -91,6 +91,41 @@ def test_noalloc_matches_allocating_entry_point(cuda_device):
         B.gdn_read_device_status()
         assert torch.equal(out, out_ref), f"out (call {call}) differs from the allocating call"
         assert torch.equal(state, state_ref), f"state (call {call}) differs"
+
+
+def test_noalloc_fused_spread(cuda_device):
+    """The fused form with more chains than SMs takes its schedule's workspace
+    from the scratch too: bit for bit the allocating call with a workspace,
+    and the one-CTA-per-chain call without one."""
+    dev = cuda_device
+    w = W.make_workload("noalloc", 901, [int(x) for x in np.random.default_rng(10).integers(1, 260, 44)],
+                        2, 4, 128, 128, weak_decay=True, state_std=0.3)
+    assert w.N * w.Hv > torch.cuda.get_device_properties(dev).multi_processor_count
+    need = B.gdn_prefill_workspace_bytes(w.T, w.N, w.Hv, w.Dk, w.Dv, B.GDN_DTYPE_BF16,
+                                         B.GDN_PREFILL_FUSED)
+    assert 0 < need <= 64 << 20
+    prep, _ = H.oracle_prepare(w)
+    q, k, v = (torch.from_numpy(prep[x]).to(torch.bfloat16).to(dev) for x in ("q", "k", "v"))
+    g = torch.from_numpy(prep["g"]).to(dev)
+    beta = torch.from_numpy(prep["beta"]).to(dev)
+    cu, sidx, hinit = (x.to(dev) for x in (w.cu_seqlens, w.state_indices, w.has_initial_state))
+    results = []
+    for ws in (torch.empty(need, dtype=torch.uint8, device=dev), None):
+        state = w.state_pool.to(dev)
+        out = torch.empty((w.T, w.Hv, w.Dv), dtype=torch.bfloat16, device=dev)
+        B.gdn_prefill_varlen(q, k, v, g, beta, state, cu, out, state_indices=sidx,
+                             has_initial_state=hinit, algo=B.GDN_PREFILL_FUSED, workspace=ws)
+        B.gdn_read_device_status()
+        results.append((out, state))
+    state = w.state_pool.to(dev)
+    out = torch.full((w.T, w.Hv, w.Dv), float("nan"), dtype=torch.bfloat16, device=dev)
+    a = _args(q, k, v, g, beta, state, cu, sidx, hinit, out, algo=B.GDN_PREFILL_FUSED)
+    rc = _noalloc()(ctypes.byref(a), torch.cuda.current_stream().cuda_stream)
+    assert rc == B.GDN_OK, B.lib().gdn_last_error_message().decode()
+    B.gdn_read_device_status()
+    for ref_out, ref_state in results:
+        assert torch.equal(out, ref_out)
+        assert torch.equal(state, ref_state)
 
 
 def test_noalloc_rejects_sizes_beyond_the_scratch(cuda_device):
