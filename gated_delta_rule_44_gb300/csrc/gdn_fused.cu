@@ -107,7 +107,8 @@ constexpr int kBarScan = 2;
 
 enum Mb : int {
   kMbKq0 = 0, kMbKq1, kMbKqFree0, kMbKqFree1, kMbV, kMbG, kMbGRead, kMbTwTu, kMbWu, kMbWImg,
-  kMbPImg, kMbFac, kMbD1, kMbD1Free, kMbUReady, kMbSImg, kMbD2, kMbD3, kMbOFree, kMbEnd, kNumMb
+  kMbPImg, kMbFac, kMbD1, kMbD1Free, kMbUReady, kMbSImg, kMbD2, kMbD3, kMbOFree, kMbEnd, kMbState,
+  kNumMb
 };
 
 // Chains spread over the SMs when they outnumber them (McNaughton's
@@ -140,6 +141,34 @@ __device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int c0, int c1
                    reinterpret_cast<uint64_t>(tmap)),
                "r"(c0), "r"(c1), "r"(c2)
                : "memory");
+}
+
+// A chain's f32 state moves between the pool and the SM by TMA, staged where
+// the S hi / lo images live (free whenever a chain starts or ends): four boxes
+// of [128 dv][32 dk] with the 128-byte swizzle, so that each thread's row is
+// read and written without bank conflicts.  Byte offset of column c (a
+// multiple of 4) of row r:
+__device__ __forceinline__ uint32_t stage_off(uint32_t r, uint32_t c) {
+  return (c >> 5) * 16384u + r * 128u + ((((c & 31u) >> 2) ^ (r & 7u)) << 4);
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst_smem, const void* tmap, uint32_t mbar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst_smem),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(mbar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src_smem, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];\n" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(c0), "r"(c1), "r"(src_smem)
+               : "memory");
+}
+// Orders this thread's global accesses of the generic proxy against those of
+// the async proxy (the TMA copies of a handed-over state and its flag).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;\n" ::: "memory");
 }
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
@@ -251,7 +280,8 @@ __device__ __forceinline__ bool wait_mb(uint32_t mb, uint32_t parity, volatile i
 template <bool kSpread>
 __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-    const __grid_constant__ CUtensorMap tm_v, const RecurLaunch p, const FusedSched sc) {
+    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_s,
+    const RecurLaunch p, const FusedSched sc) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = aligned_smem(smem_raw);
   __shared__ uint64_t mbs[kNumMb];
@@ -829,11 +859,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
     const bool lead = warp == 10 && lane == 0;
     const uint32_t la = static_cast<uint32_t>(quad * 32) << 16;
     ChunkIt it = it_start();  // the chain and chunk this role is on
-    // Row dv of the state of chain (sequence sq, value head hq) in the pool.
+    // The pool slot of sequence sq, and row dv of chain (sq, value head hq) there.
+    auto chain_slot = [&](int sq) { return p.sidx != nullptr ? __ldg(p.sidx + sq) : sq; };
     auto chain_row = [&](int sq, int hq) {
-      const int slot = p.sidx != nullptr ? __ldg(p.sidx + sq) : sq;
-      return p.pool + (((int64_t)slot * p.Hv + hq) * kD + dv) * kD;
+      return p.pool + (((int64_t)chain_slot(sq) * p.Hv + hq) * kD + dv) * kD;
     };
+    int n_state = 0, st_issued = 0, st_seen = 0;  // state loads (the counts on the lead)
     // A chain's initial state into the S images and, times e^{gam_L} of its
     // first chunk here, into TMEM.  A chain that starts mid-way here resumes
     // from the state the CTA after stored (its flag waited for first).
@@ -859,34 +890,67 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
         okr = named_bar_and(kBarScan, kScanThreads, okr);
         init = true;
       }
-      const float* prow = chain_row(x.s, x.h);
-      constexpr int kB = kSpread ? 32 : 16;  // loads in flight per thread (mid-range switches)
-      for (int j = 0; j < kD; j += kB) {
-        float v[kB];
+      if (init) {
+        // The state by TMA into the staging, each row into TMEM, and once
+        // every row is out of the staging, its images over it.
+        if (lead && okr) {
+          fence_proxy_async_global();
+          mbar_expect_tx(MB(kMbState), 4 * 16384);
+          const int row0 = (chain_slot(x.s) * p.Hv + x.h) * kD;
 #pragma unroll
-        for (int e = 0; e < kB; e += 4) {
-          float4 f = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-          if (init && okr) f = __ldcg(reinterpret_cast<const float4*>(prow + j + e));
-          v[e] = f.x;
-          v[e + 1] = f.y;
-          v[e + 2] = f.z;
-          v[e + 3] = f.w;
+          for (int b = 0; b < 4; ++b)
+            tma_load_2d(base + FusedSmem::SH + b * 16384, &tm_s, MB(kMbState), 32 * b, row0);
+          ++st_issued;
         }
+        const bool got = wait_mb(MB(kMbState), n_state & 1, abort, p.status);
+        if (lead && got) ++st_seen;
+        okr = got && okr;
+        ++n_state;
+#pragma unroll 1
+        for (int j0 = 0; j0 < kD; j0 += 32) {
+          float v[32];
 #pragma unroll
-        for (int e = 0; e < kB; e += 8) {
-          const uint32_t off = swz128_offset(dv, j + e, 16384);
-          st_split8(sm + FusedSmem::SH + off, sm + FusedSmem::SL + off, v + e);
+          for (int e = 0; e < 32; e += 4) {
+            const float4 f = *reinterpret_cast<const float4*>(sm + FusedSmem::SH + stage_off(dv, j0 + e));
+            v[e] = f.x;
+            v[e + 1] = f.y;
+            v[e + 2] = f.z;
+            v[e + 3] = f.w;
+          }
+          tmem_st32(tmem + kTS + la + j0, v);
         }
+        tmem_st_wait();
+        named_bar(kBarScan, kScanThreads);
+#pragma unroll 1
+        for (int j0 = 0; j0 < kD; j0 += 32) {
+          float v[32];
+          tmem_ld32(tmem + kTS + la + j0, v);
+          tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < kB; ++e) v[e] *= eL;
-        if constexpr (kB == 32)
-          tmem_st32(tmem + kTS + la + j, v);
-        else
-          tmem_st16(tmem + kTS + la + j, v);
+          for (int e = 0; e < 32; e += 8) {
+            const uint32_t off = swz128_offset(dv, j0 + e, 16384);
+            st_split8(sm + FusedSmem::SH + off, sm + FusedSmem::SL + off, v + e);
+          }
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] *= eL;
+          tmem_st32(tmem + kTS + la + j0, v);
+        }
+      } else {  // a fresh chain: zero images and state
+#pragma unroll 1
+        for (int j0 = 0; j0 < kD; j0 += 32) {
+          float v[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0.0f;
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            const uint32_t off = swz128_offset(dv, j0 + e, 16384);
+            st_split8(sm + FusedSmem::SH + off, sm + FusedSmem::SL + off, v + e);
+          }
+          tmem_st32(tmem + kTS + la + j0, v);
+        }
       }
       return okr;
     };
-    float* const prow0 = chain_row(s0, h0);  // the one chain's row without a schedule
     bool ok = wait_mb(MB(kMbFac), 0, abort, p.status);
     ok = init_chain(it, fac[128], ok);
     tmem_st_wait();
@@ -987,7 +1051,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
         eLn = fac[((c + 1) & 1) * FusedSmem::kFac + 128];
       }
       fence_after_sync();
-      float* prow = kSpread ? chain_row(it.s, it.h) : prow0;
 #pragma unroll 1
       for (int j0 = 0; j0 < kD; j0 += 32) {
         float v[32];
@@ -996,7 +1059,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
         if (chain_end) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(prow + j0 + e) =
+            *reinterpret_cast<float4*>(sm + FusedSmem::SH + stage_off(dv, j0 + e)) =
                 make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
         } else {
 #pragma unroll
@@ -1009,12 +1072,27 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
           tmem_st32(tmem + kTS + la + j0, v);
         }
       }
-      if (kSpread && chain_end && it.e < it.n) {  // another CTA resumes this chain: its flag
-        named_bar(kBarScan, kScanThreads);  // every row stored; the lead's fence covers them
+      if (chain_end) {  // the staged S' to the pool by TMA (and the flag when another CTA resumes it)
+        fence_proxy_async();
+        named_bar(kBarScan, kScanThreads);
         if (lead) {
-          __threadfence();
-          atomicExch(sc.flags + (int64_t)it.s * p.Hv + it.h, 1u);
+          const int row0 = (chain_slot(it.s) * p.Hv + it.h) * kD;
+#pragma unroll
+          for (int b = 0; b < 4; ++b)
+            tma_store_2d(&tm_s, base + FusedSmem::SH + b * 16384, 32 * b, row0);
+          bulk_commit();
+          if (kSpread && it.e < it.n) {
+            bulk_wait_all();
+            fence_proxy_async_global();
+            __threadfence();
+            atomicExch(sc.flags + (int64_t)it.s * p.Hv + it.h, 1u);
+          } else if (last) {
+            bulk_wait_all();
+          } else {
+            bulk_wait_read();
+          }
         }
+        named_bar(kBarScan, kScanThreads);  // the staging is free again
       }
       if (kSpread && chain_end && !last) {  // the next chain comes in (mid-way if cut by the range's end)
         ChunkIt nx = it;
@@ -1064,6 +1142,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
       if (!ok) break;
       it_next(it);
     }
+    if (lead && st_issued != st_seen)  // a state load still landing (after an abort)
+      mbar_wait(MB(kMbState), (n_state - 1) & 1, kWaitBudget);
   }
 
   // ---- teardown: every thread arrives here exactly once --------------------
@@ -1102,6 +1182,20 @@ SchedLayout sched_layout(int64_t N, int64_t Hv) {
 }
 }  // namespace
 
+// The state pool as rows of Dk f32 ([slots * Hv * Dv][Dk]) in boxes of
+// [128 rows][32 columns] with the 128-byte swizzle (one box per TMA copy).
+bool make_pool_map(CUtensorMap* m, float* pool, int64_t slots, int64_t Hv) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(slots * Hv * kD)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 4};
+  cuuint32_t box[2] = {32, 128};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, pool, dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t fused_workspace_bytes(int64_t N, int64_t Hv) {
   if (N <= 0 || Hv <= 0) return 0;
   return sched_layout(N, Hv).bytes;
@@ -1109,9 +1203,9 @@ size_t fused_workspace_bytes(int64_t N, int64_t Hv) {
 
 cudaError_t launch_fused(const RecurLaunch& p, void* workspace, size_t workspace_bytes,
                          cudaStream_t s) {
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, ts;
   if (!make_map(&tq, p.q, p.T, p.Hk) || !make_map(&tk, p.k, p.T, p.Hk) ||
-      !make_map(&tv, p.v, p.T, p.Hv))
+      !make_map(&tv, p.v, p.T, p.Hv) || !make_pool_map(&ts, p.pool, p.slots, p.Hv))
     return cudaErrorInvalidValue;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
@@ -1152,12 +1246,12 @@ cudaError_t launch_fused(const RecurLaunch& p, void* workspace, size_t workspace
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, fused_prefill_kernel<true>, tq, tk, tv, p, sc);
+    e = cudaLaunchKernelEx(&cfg, fused_prefill_kernel<true>, tq, tk, tv, ts, p, sc);
     note_launch();
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   fused_prefill_kernel<false><<<static_cast<unsigned>(blocks), kThreads, FusedSmem::BYTES + 1024, s>>>(
-      tq, tk, tv, p, sc);
+      tq, tk, tv, ts, p, sc);
   note_launch();
   return cudaGetLastError();
 }
