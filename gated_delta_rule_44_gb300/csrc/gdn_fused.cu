@@ -274,6 +274,15 @@ __device__ __forceinline__ bool wait_mb(uint32_t mb, uint32_t parity, volatile i
   }
 }
 
+// A role's position in the CTA's chunks: chain (s, h), chunk k of its n (the
+// CTA runs chunks up to e of it), the sequence's token range [lo, hi), and the
+// chunks left.  The prep and chain roles keep theirs in shared memory (one
+// thread advances it between two barriers), which keeps it out of the
+// registers of a kernel at its 128-register cap.
+struct ChunkIt {
+  int s, h, k, e, n, lo, hi, left;
+};
+
 // kSpread: the CTA runs the range the schedule gave it, else the one chain
 // (sequence, value head) = blockIdx.x (that instance keeps none of the
 // range's bookkeeping in registers).
@@ -286,6 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
   uint8_t* sm = aligned_smem(smem_raw);
   __shared__ uint64_t mbs[kNumMb];
   __shared__ uint32_t tslot;
+  __shared__ ChunkIt s_igt, s_it;  // the prep's gate chunk; the chain's chunk
   __shared__ int s_abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
@@ -337,12 +347,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
     }
     if (cnt <= 0) return;
   }
-  // A role's position in the CTA's chunks: chain (s, h), chunk k of its n
-  // (this CTA runs chunks up to e of it), the sequence's token range
-  // [lo, hi), and the chunks left.
-  struct ChunkIt {
-    int s, h, k, e, n, lo, hi, left;
-  };
   auto it_start = [&]() {
     ChunkIt x;
     x.s = s0;
@@ -596,16 +600,16 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
     constexpr int SY = FusedSmem::kYStride;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     float g_next = 0.0f, b_next = 0.0f;
-    ChunkIt igt = it_start();
-    auto load_gates = [&]() {  // ptid < 64; chunks in order
-      const int t0 = igt.lo + igt.k * kC, L = min(kC, igt.hi - t0);
+    if (ptid == 0) s_igt = it_start();
+    named_bar(kBarPrep, kPrepThreads);
+    auto load_gates = [&]() {  // ptid < 64; the chunk s_igt is on
+      const int t0 = s_igt.lo + s_igt.k * kC, L = min(kC, s_igt.hi - t0), hg = s_igt.h;
       if (ptid < L) {
-        g_next = __ldg(p.g + (int64_t)(t0 + ptid) * p.Hv + igt.h);
-        b_next = __ldg(p.beta + (int64_t)(t0 + ptid) * p.Hv + igt.h);
+        g_next = __ldg(p.g + (int64_t)(t0 + ptid) * p.Hv + hg);
+        b_next = __ldg(p.beta + (int64_t)(t0 + ptid) * p.Hv + hg);
       } else {
         g_next = b_next = 0.0f;
       }
-      it_next(igt);
     };
     if (ptid < 64) load_gates();
     float pv[32];  // this thread's P values (P-row warps) until the images go out
@@ -637,6 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
         (ptid < 64 ? skn : sqn)[r] = p.norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
       }
       named_bar(kBarPrep, kPrepThreads);
+      if (ptid == 0 && c + 1 < nch) it_next(s_igt);  // read for chunk c before this barrier
       if (pw == 0) {  // inclusive scan of g over the chunk (2 tokens per lane)
         const float a = sg[2 * lane], b = sg[2 * lane + 1];
         float x = a + b;
@@ -858,7 +863,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
     const int dv = quad * 32 + lane;
     const bool lead = warp == 10 && lane == 0;
     const uint32_t la = static_cast<uint32_t>(quad * 32) << 16;
-    ChunkIt it = it_start();  // the chain and chunk this role is on
+    if (lead) s_it = it_start();  // the chain and chunk this role is on
+    named_bar(kBarScan, kScanThreads);
     // The pool slot of sequence sq, and row dv of chain (sq, value head hq) there.
     auto chain_slot = [&](int sq) { return p.sidx != nullptr ? __ldg(p.sidx + sq) : sq; };
     auto chain_row = [&](int sq, int hq) {
@@ -952,7 +958,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
       return okr;
     };
     bool ok = wait_mb(MB(kMbFac), 0, abort, p.status);
-    ok = init_chain(it, fac[128], ok);
+    {
+      const ChunkIt x0 = s_it;
+      ok = init_chain(x0, fac[128], ok);
+    }
     tmem_st_wait();
     fence_proxy_async();
     fence_before_sync();
@@ -961,12 +970,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
     // Per chunk: the W^T image (D1 waits), U (D2 and D3 wait), the state update
     // (the next D1 waits), the output rows (the next D1's Q half waits).
     for (int c = 0; c < nch && ok; ++c) {
-      const int t0 = it.lo + it.k * kC;
-      const int L = min(kC, it.hi - t0);
-      if (kSpread && lead && it.k + 1 == it.e && c + 1 < nch) {
+      const int t0 = s_it.lo + s_it.k * kC;
+      const int L = min(kC, s_it.hi - t0);
+      const int hc = s_it.h;
+      if (kSpread && lead && s_it.k + 1 == s_it.e && c + 1 < nch) {
         // The next chain's state into L2 a chunk before it is read (a resumed
         // chain's may still be in flight: L2 keeps the line coherent).
-        ChunkIt nx = it;
+        ChunkIt nx = s_it;
         it_next(nx);
         if (nx.k > 0 || p.has_init == nullptr || __ldg(p.has_init + nx.s) != 0) {
           const float* row0 = chain_row(nx.s, nx.h) - (int64_t)dv * kD;
@@ -1044,7 +1054,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
       // another CTA resumes the chain), and the next chain's state comes in.
       ok = wait_mb(MB(kMbD2), c & 1, abort, p.status) && ok;
       const bool last = c + 1 == nch;
-      const bool chain_end = last || (kSpread && it.k + 1 == it.e);
+      const bool chain_end = last || (kSpread && s_it.k + 1 == s_it.e);
       float eLn = 0.0f;
       if (!last) {
         ok = wait_mb(MB(kMbFac), (c + 1) & 1, abort, p.status) && ok;
@@ -1076,16 +1086,16 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
         fence_proxy_async();
         named_bar(kBarScan, kScanThreads);
         if (lead) {
-          const int row0 = (chain_slot(it.s) * p.Hv + it.h) * kD;
+          const int row0 = (chain_slot(s_it.s) * p.Hv + s_it.h) * kD;
 #pragma unroll
           for (int b = 0; b < 4; ++b)
             tma_store_2d(&tm_s, base + FusedSmem::SH + b * 16384, 32 * b, row0);
           bulk_commit();
-          if (kSpread && it.e < it.n) {
+          if (kSpread && s_it.e < s_it.n) {
             bulk_wait_all();
             fence_proxy_async_global();
             __threadfence();
-            atomicExch(sc.flags + (int64_t)it.s * p.Hv + it.h, 1u);
+            atomicExch(sc.flags + (int64_t)s_it.s * p.Hv + s_it.h, 1u);
           } else if (last) {
             bulk_wait_all();
           } else {
@@ -1095,7 +1105,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
         named_bar(kBarScan, kScanThreads);  // the staging is free again
       }
       if (kSpread && chain_end && !last) {  // the next chain comes in (mid-way if cut by the range's end)
-        ChunkIt nx = it;
+        ChunkIt nx = s_it;
         it_next(nx);
         ok = init_chain(nx, eLn, ok);
       }
@@ -1128,7 +1138,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int r = (q * kScanThreads + stid) >> 4;  // the vector's token row
-            __nv_bfloat16* dst = out + ((int64_t)(t0 + j0 + r) * p.Hv + it.h) * kD + c16 * 8;
+            __nv_bfloat16* dst = out + ((int64_t)(t0 + j0 + r) * p.Hv + hc) * kD + c16 * 8;
             if (j0 + r < L) {
               *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(ost + r * kD + c16 * 8);
             }
@@ -1136,11 +1146,11 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
           named_bar(kBarScan, kScanThreads);
         }
       }
+      if (lead) it_next(s_it);  // every read of this chunk's s_it was before the S' barrier
       fence_before_sync();
       ok = named_bar_and(kBarScan, kScanThreads, ok);
       if (lead) mbar_arrive(MB(kMbOFree));
       if (!ok) break;
-      it_next(it);
     }
     if (lead && st_issued != st_seen)  // a state load still landing (after an abort)
       mbar_wait(MB(kMbState), (n_state - 1) & 1, kWaitBudget);
