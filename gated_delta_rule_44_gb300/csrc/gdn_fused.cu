@@ -1234,9 +1234,14 @@ cudaError_t launch_fused(const RecurLaunch& p, void* workspace, size_t workspace
   const int sms = sm_count();
   const SchedLayout l = sched_layout(p.N, p.Hv);
   FusedSched sc{};
-  if (workspace != nullptr && workspace_bytes >= l.bytes && blocks > sms && sms <= kMaxSchedCtas &&
+  // Ranges pay about 9 % a chunk in bookkeeping, so they are taken where one
+  // CTA per chain would leave a wave partly idle: on equal chains, waves
+  // ceil(w) against w = chains / SMs, more than 8 % apart.
+  const int64_t waves = (blocks + sms - 1) / sms;
+  const bool spread = blocks > sms && waves * sms * 100 > blocks * 108;
+  if (workspace != nullptr && workspace_bytes >= l.bytes && spread && sms <= kMaxSchedCtas &&
       p.Hv / p.Hk <= sms) {
-    // More chains than SMs: one CTA per SM over the wrap-around schedule.
+    // One CTA per SM over the wrap-around schedule.
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     sc.seq_chunks = reinterpret_cast<int32_t*>(ws + l.chunks);
     sc.prefix = reinterpret_cast<int32_t*>(ws + l.prefix);

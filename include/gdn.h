@@ -105,7 +105,8 @@ typedef enum gdn_prefill_algo {
   GDN_PREFILL_FUSED = 3      /* the chunk-64 form in one launch, a CTA preparing the next
                                 chunk while it carries the state: one CTA per (sequence,
                                 value head), or, given the optional workspace and more
-                                chains than SMs, one CTA per SM over even ranges of the
+                                chains than SMs (unless they nearly fill whole waves of
+                                one CTA per SM), one CTA per SM over even ranges of the
                                 chains' chunks (a short kernel computes the ranges first) */
 } gdn_prefill_algo;
 
