@@ -135,14 +135,6 @@ struct FusedSched {
   unsigned* flags;      // [N * Hv] 1 once a chain's state was stored for the CTA that resumes it
 };
 
-// The TMA box at (c0, c1, c2) brought into L2 only (no smem, no mbarrier).
-__device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n" ::"l"(
-                   reinterpret_cast<uint64_t>(tmap)),
-               "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
-
 // A chain's f32 state moves between the pool and the SM by TMA, staged where
 // the S hi / lo images live (free whenever a chain starts or ends): four boxes
 // of [128 dv][32 dk] with the 128-byte swizzle, so that each thread's row is
@@ -423,40 +415,17 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
         n_v = c + 1;
         it_next(iv);
       };
-      // K / Q two chunks and V one chunk beyond the loads in flight go to L2
-      // early: heads that share K / Q do not run in step, and V is read once.
-      auto prefetch = [&](ChunkIt x, int ahead, bool kq) {
-        for (int i = 0; i < ahead; ++i) it_next(x);
-        if (x.k >= x.n) return;
-        const int t0 = x.lo + x.k * kC;
-        if (kq) {
-          const int hk = x.h / grp;
-          tma_prefetch_3d(&tm_k, 0, hk, t0);
-          tma_prefetch_3d(&tm_q, 0, hk, t0);
-          tma_prefetch_3d(&tm_k, 64, hk, t0);
-          tma_prefetch_3d(&tm_q, 64, hk, t0);
-        } else {
-          tma_prefetch_3d(&tm_v, 0, x.h, t0);
-          tma_prefetch_3d(&tm_v, 64, x.h, t0);
-        }
-      };
       load_kq(0);
       if (nch > 1) load_kq(1);
       load_v(0);
-      prefetch(ikq, 0, true);
-      prefetch(ikq, 1, true);
-      prefetch(iv, 0, false);
-      prefetch(iv, 1, false);
       for (int c = 1; c < nch; ++c) {
         // V(c) replaces W^T(c - 1) once D1(c - 1) has read it.
         if (!wait_mb(MB(kMbD1), (c - 1) & 1, abort, p.status)) break;
         load_v(c);
-        if (c + 2 < nch) prefetch(iv, 1, false);
         if (c + 1 < nch) {  // stage (c + 1) % 2 is free once D2(c - 1) has read K(c - 1)
           if (!wait_mb(MB(kMbKqFree0 + ((c + 1) & 1)), ((c - 1) >> 1) & 1, abort, p.status))
             break;
           load_kq(c + 1);
-          if (c + 3 < nch) prefetch(ikq, 1, true);
         }
       }
       __syncwarp(1u);
@@ -865,11 +834,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
     const uint32_t la = static_cast<uint32_t>(quad * 32) << 16;
     if (lead) s_it = it_start();  // the chain and chunk this role is on
     named_bar(kBarScan, kScanThreads);
-    // The pool slot of sequence sq, and row dv of chain (sq, value head hq) there.
+    // The pool slot of sequence sq.
     auto chain_slot = [&](int sq) { return p.sidx != nullptr ? __ldg(p.sidx + sq) : sq; };
-    auto chain_row = [&](int sq, int hq) {
-      return p.pool + (((int64_t)chain_slot(sq) * p.Hv + hq) * kD + dv) * kD;
-    };
     int n_state = 0, st_issued = 0, st_seen = 0;  // state loads (the counts on the lead)
     // A chain's initial state into the S images and, times e^{gam_L} of its
     // first chunk here, into TMEM.  A chain that starts mid-way here resumes
@@ -973,20 +939,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
       const int t0 = s_it.lo + s_it.k * kC;
       const int L = min(kC, s_it.hi - t0);
       const int hc = s_it.h;
-      if (kSpread && lead && s_it.k + 1 == s_it.e && c + 1 < nch) {
-        // The next chain's state into L2 a chunk before it is read (a resumed
-        // chain's may still be in flight: L2 keeps the line coherent).
-        ChunkIt nx = s_it;
-        it_next(nx);
-        if (nx.k > 0 || p.has_init == nullptr || __ldg(p.has_init + nx.s) != 0) {
-          const float* row0 = chain_row(nx.s, nx.h) - (int64_t)dv * kD;
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(row0 + q * 4096),
-                         "r"(16384)
-                         : "memory");
-        }
-      }
       const float* F = fac + (c & 1) * FusedSmem::kFac;
       // W^T (TMEM lanes = dk, 64 token columns) -> the -W^T image, the MN-major
       // B operand of this chunk's D1 (V, which shared the space, is consumed).
