@@ -894,11 +894,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_scan_kernel(
       mbar_expect_tx(mb_el, 512);
       bulk_g2s(base + KScan::ELB + ((c + 1) & 1) * 512, blob(c + 1) + kBE, 512, mb_el);
       pend_el = c + 1;
-      if (c + 2 < nch)  // the images after the next on their way into L2
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
-                         reinterpret_cast<uint64_t>(blob(c + 2))),
-                     "r"(kBImg)
-                     : "memory");
+
     }
     ok = __syncthreads_and(mbar_wait(mb_ld, c & 1, kWaitBudget) &&
                            mbar_wait(mb_ldb, c & 1, kWaitBudget));
