@@ -1,7 +1,10 @@
 // gdn_fused.cu -- chunked (C = 64) WY/UT-form varlen prefill in ONE launch:
-// one CTA per (sequence, value head) carries the f32 state through the
+// a CTA carries a (sequence, value head) chain's f32 state through the
 // sequence's chunks while its own warps prepare the next chunk, so nothing of
-// a chunk but its output ever leaves the SM.
+// a chunk but its output (and, where a chain moves between CTAs, its state)
+// leaves the SM.  One CTA per chain, or, with more chains than SMs and the
+// optional workspace, one CTA per SM over even ranges of the chains' chunks
+// (the wrap-around schedule below).
 //
 // Defines the recurrence of [cpu.rs] (ferrum-kernels 0.8.0, src/ferrum_kernels/
 // backend/cpu.rs) recurrent_gated_delta_rule_varlen_f32 / [cpu_ops.cpp]
@@ -839,7 +842,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
     int n_state = 0, st_issued = 0, st_seen = 0;  // state loads (the counts on the lead)
     // A chain's initial state into the S images and, times e^{gam_L} of its
     // first chunk here, into TMEM.  A chain that starts mid-way here resumes
-    // from the state the CTA after stored (its flag waited for first).
+    // from the state its gang member in the next gang stored (its flag
+    // waited for first).
     auto init_chain = [&](const ChunkIt& x, float eL, bool okr) {
       bool init = p.has_init == nullptr || __ldg(p.has_init + x.s) != 0;
       if (kSpread && x.k > 0) {
