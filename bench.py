@@ -244,7 +244,7 @@ def kernel_report(w, kernel_ms, peaks):
 _DECODE_SRC = (("gdn_recurrent.cu", "gdn_rowstep.cuh", "gdn_math.cuh"),
                "27a316189865ac53a673efa7b8dd7d8cac0c7b20a4885acb1593f84a0d92486b")
 _FUSED_SRC = (("gdn_fused.cu", "gdn_chunk_common.cuh", "tcgen05.cuh"),
-              "541cb12bc06a7cbfd37a3d9c275fd4d270b2754b85c330f0a81c6cf0404b8fc0")
+              "9df2d58f12158d5b47fc8d1cc5095c7ca5787766269b6bfd8d67edd7f8847805")
 _CHUNKED_SRC = (("gdn_chunked.cu", "gdn_chunk_common.cuh", "tcgen05.cuh"),
                 "d52e0bff59df7a9a5c1e8b0a9d0701657d3c9cdd0d30d4ee728c9482d8f1080a")
 MEASURED_TRAFFIC = {

@@ -1190,7 +1190,7 @@ cudaError_t launch_fused(const RecurLaunch& p, void* workspace, size_t workspace
   const int sms = sm_count();
   const SchedLayout l = sched_layout(p.N, p.Hv);
   FusedSched sc{};
-  // Ranges pay about 9 % a chunk in bookkeeping, so they are taken where one
+  // Ranges pay about 6 % a chunk in bookkeeping, so they are taken where one
   // CTA per chain would leave a wave partly idle: on equal chains, waves
   // ceil(w) against w = chains / SMs, more than 8 % apart.
   const int64_t waves = (blocks + sms - 1) / sms;
