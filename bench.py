@@ -238,22 +238,22 @@ def kernel_report(w, kernel_ms, peaks):
 # to capture under ncu's replay, so its figures are scaled from smaller cases
 # of the same kernels: the decode by the row-heads processed (x4; every byte
 # of that launch is per row-head), the fused prefill by the call's algorithmic
-# bytes (varlen_8's traffic was 0.980 of its algorithmic bytes; the per-token
+# bytes (varlen_8's traffic was 0.981 of its algorithmic bytes; the per-token
 # share of key and value heads differs between the two workloads, so token-heads
 # would not scale it).
 _DECODE_SRC = (("gdn_recurrent.cu", "gdn_rowstep.cuh", "gdn_math.cuh"),
                "27a316189865ac53a673efa7b8dd7d8cac0c7b20a4885acb1593f84a0d92486b")
 _FUSED_SRC = (("gdn_fused.cu", "gdn_chunk_common.cuh", "tcgen05.cuh"),
-              "9df2d58f12158d5b47fc8d1cc5095c7ca5787766269b6bfd8d67edd7f8847805")
+              "c997708b7ffcf213efd037d64511a6ca2fbfc841a9ab640a6327f1cc2505a458")
 _CHUNKED_SRC = (("gdn_chunked.cu", "gdn_chunk_common.cuh", "tcgen05.cuh"),
                 "d52e0bff59df7a9a5c1e8b0a9d0701657d3c9cdd0d30d4ee728c9482d8f1080a")
 MEASURED_TRAFFIC = {
     ("prefill", "prefill_4k"): (244.0e6,) + _CHUNKED_SRC +
                                ("the call's 4 chunk_prep + 4 chunk_scan launches; ncu flushes L2 "
                                 "between them, so blob writes still in L2 are not counted",),
-    ("prefill", "varlen_8"): (633.6e6,) + _FUSED_SRC +
+    ("prefill", "varlen_8"): (633.9e6,) + _FUSED_SRC +
                              ("the fused_prefill launch (the schedule kernel's few KB not counted)",),
-    ("prefill", "mixed_hv64"): (349.5e6,) + _FUSED_SRC +
+    ("prefill", "mixed_hv64"): (349.7e6,) + _FUSED_SRC +
                                ("varlen_8's fused launch scaled by algorithmic bytes (x0.552)",),
     ("decode", "decode_b256"): (1017.8e6,) + _DECODE_SRC + ("one decode launch",),
     ("decode", "mixed_hv64"): (4071.2e6,) + _DECODE_SRC + ("decode_b256's launch x 4 (row-heads)",),

@@ -928,18 +928,33 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
       return okr;
     };
     bool ok = wait_mb(MB(kMbFac), 0, abort, p.status);
-    {
+    // With ranges a chain's state comes in at the top of its first chunk here
+    // (one place in the code for the first chain and every later one).
+    bool need_init = kSpread;
+    float eL_init = fac[128];  // e^{gam_L} of that chunk
+    if constexpr (!kSpread) {
       const ChunkIt x0 = s_it;
-      ok = init_chain(x0, fac[128], ok);
+      ok = init_chain(x0, eL_init, ok);
+      tmem_st_wait();
+      fence_proxy_async();
+      fence_before_sync();
+      ok = named_bar_and(kBarScan, kScanThreads, ok);
+      if (lead) mbar_arrive(MB(kMbSImg));
     }
-    tmem_st_wait();
-    fence_proxy_async();
-    fence_before_sync();
-    ok = named_bar_and(kBarScan, kScanThreads, ok);
-    if (lead) mbar_arrive(MB(kMbSImg));
     // Per chunk: the W^T image (D1 waits), U (D2 and D3 wait), the state update
     // (the next D1 waits), the output rows (the next D1's Q half waits).
     for (int c = 0; c < nch && ok; ++c) {
+      if (kSpread && need_init) {
+        const ChunkIt x0 = s_it;
+        ok = init_chain(x0, eL_init, ok);
+        tmem_st_wait();
+        fence_proxy_async();
+        fence_before_sync();
+        ok = named_bar_and(kBarScan, kScanThreads, ok);
+        if (lead) mbar_arrive(MB(kMbSImg));
+        need_init = false;
+        if (!ok) break;
+      }
       const int t0 = s_it.lo + s_it.k * kC;
       const int L = min(kC, s_it.hi - t0);
       const int hc = s_it.h;
@@ -1060,18 +1075,20 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
         }
         named_bar(kBarScan, kScanThreads);  // the staging is free again
       }
-      if (kSpread && chain_end && !last) {  // the next chain comes in (mid-way if cut by the range's end)
-        ChunkIt nx = s_it;
-        it_next(nx);
-        ok = init_chain(nx, eLn, ok);
+      // Past a chain's end here the next chain (mid-way if cut by the range's
+      // end) comes in at the top of the next chunk.
+      const bool next_init = kSpread && chain_end && !last;
+      if (next_init) {
+        need_init = true;
+        eL_init = eLn;
       }
-      if (!last) {
+      if (!last && !next_init) {
         tmem_st_wait();
         fence_proxy_async();
       }
       fence_before_sync();
       ok = named_bar_and(kBarScan, kScanThreads, ok);
-      if (lead && !last) mbar_arrive(MB(kMbSImg));
+      if (lead && !last && !next_init) mbar_arrive(MB(kMbSImg));
       if (!ok) break;
       // Output rows of the chunk: O^T[dv, i] = fo Q S^T + P U, then the
       // columns are free for the next chunk's D1.
