@@ -244,7 +244,7 @@ def kernel_report(w, kernel_ms, peaks):
 _DECODE_SRC = (("gdn_recurrent.cu", "gdn_rowstep.cuh", "gdn_math.cuh"),
                "27a316189865ac53a673efa7b8dd7d8cac0c7b20a4885acb1593f84a0d92486b")
 _FUSED_SRC = (("gdn_fused.cu", "gdn_chunk_common.cuh", "tcgen05.cuh"),
-              "c997708b7ffcf213efd037d64511a6ca2fbfc841a9ab640a6327f1cc2505a458")
+              "58e72a3ea6a4cc1ff4d8b4f047b10bcbf6fff1c2f1e9a49892082aeb670e871e")
 _CHUNKED_SRC = (("gdn_chunked.cu", "gdn_chunk_common.cuh", "tcgen05.cuh"),
                 "d52e0bff59df7a9a5c1e8b0a9d0701657d3c9cdd0d30d4ee728c9482d8f1080a")
 MEASURED_TRAFFIC = {

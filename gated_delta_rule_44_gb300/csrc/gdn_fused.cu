@@ -1022,7 +1022,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
       // S' = e^{gam_L} S + dS (in TMEM): its images for D1 of the next chunk,
       // then S' e^{gam_L'} back (the next dS accumulates onto it).  At the
       // chain's last chunk here S' goes to the pool instead (with its flag when
-      // another CTA resumes the chain), and the next chain's state comes in.
+      // the gang before resumes the chain); the next chain's state comes in
+      // at the top of the next chunk.
       ok = wait_mb(MB(kMbD2), c & 1, abort, p.status) && ok;
       const bool last = c + 1 == nch;
       const bool chain_end = last || (kSpread && s_it.k + 1 == s_it.e);
@@ -1053,7 +1054,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(
           tmem_st32(tmem + kTS + la + j0, v);
         }
       }
-      if (chain_end) {  // the staged S' to the pool by TMA (and the flag when another CTA resumes it)
+      if (chain_end) {  // the staged S' to the pool by TMA (and the flag when the gang before resumes it)
         fence_proxy_async();
         named_bar(kBarScan, kScanThreads);
         if (lead) {
