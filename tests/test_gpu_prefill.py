@@ -178,13 +178,17 @@ def test_fused_spread_over_sms(case, cuda_device):
                                              B.GDN_PREFILL_FUSED)
     assert ws_bytes > 0
     results = []
-    for ws in (torch.empty(ws_bytes, dtype=torch.uint8, device=dev), None):
+    for ws, launches in ((torch.empty(ws_bytes, dtype=torch.uint8, device=dev), 2), (None, 1)):
         pool = w.state_pool.to(dev)
         out = torch.full((w.T, w.Hv, w.Dv), float("nan"), dtype=w.act_dtype, device=dev)
+        n0 = B.gdn_launch_count()
         B.gdn_prefill_varlen(*args, pool, w.cu_seqlens.to(dev), out,
                              state_indices=w.state_indices.to(dev),
                              has_initial_state=w.has_initial_state.to(dev),
                              algo=B.GDN_PREFILL_FUSED, workspace=ws)
+        # the ranges run as the schedule kernel and the fused kernel; without
+        # the workspace the fused kernel alone runs one CTA per chain
+        assert B.gdn_launch_count() - n0 == launches
         B.gdn_read_device_status()
         results.append((out, pool))
     assert torch.equal(results[0][0], results[1][0])
