@@ -120,8 +120,10 @@ def test_noalloc_fused_spread(cuda_device):
     state = w.state_pool.to(dev)
     out = torch.full((w.T, w.Hv, w.Dv), float("nan"), dtype=torch.bfloat16, device=dev)
     a = _args(q, k, v, g, beta, state, cu, sidx, hinit, out, algo=B.GDN_PREFILL_FUSED)
+    n0 = B.gdn_launch_count()
     rc = _noalloc()(ctypes.byref(a), torch.cuda.current_stream().cuda_stream)
     assert rc == B.GDN_OK, B.lib().gdn_last_error_message().decode()
+    assert B.gdn_launch_count() - n0 == 2  # the schedule kernel, then the fused kernel
     B.gdn_read_device_status()
     for ref_out, ref_state in results:
         assert torch.equal(out, ref_out)
